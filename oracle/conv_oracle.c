@@ -1,0 +1,250 @@
+/*
+ * conv_oracle.c -- CPU oracle for the 2-D convolution forward pass (FPROP).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or calls
+ * this file; only the tests, the package's smoke check and the benchmark's
+ * CPU-baseline leg do.  It shares no code, header or table with the CUDA
+ * library.
+ *
+ * What it computes (the plain definition, written out):
+ *
+ *   y[n,k,p,q] = act( alpha * sum_{c<C} sum_{r<R} sum_{s<S}
+ *                        X(n, c, p*u + r*dh - pad_top, q*v + s*dw - pad_left) * w[k,c,r,s]
+ *                     + beta * y_in[n,k,p,q] + bias[k] )
+ *
+ * with X(...) = 0 outside [0,H) x [0,W) (zero padding) and act = identity or
+ * max(0, .).  Sources:
+ *   - "maxDNN: An Efficient Convolution Kernel for Deep Learning with Maxwell
+ *     GPUs", method section: every output coordinate is the product of the
+ *     input receptive field with the filter weights (a dot product over
+ *     c, r, s).
+ *   - "cuDNN: Efficient Primitives for Deep Learning", method section: tensors
+ *     and filters are addressed through descriptors with arbitrary strides;
+ *     non-square inputs and asymmetric padding are supported (method and
+ *     findings sections).
+ *   - "High Performance Zero-Memory Overhead Direct Convolutions", method
+ *     section: direct convolution, no packing.
+ * The filter is not flipped (cross-correlation).  Dilation enters as r*dh and
+ * s*dw, and the output extent uses the dilated filter extent dh*(R-1)+1 with
+ * a floor: a partial last window is dropped.  Bottom/right padding only
+ * changes the output extent.
+ *
+ * All arithmetic is FP64, in the loop order n, k, p, q, c, r, s, on the
+ * values given (the caller passes the same BF16/TF32-rounded inputs the GPU
+ * reads, widened exactly to double).  Alongside y it returns
+ * bound[n,k,p,q] = sum |x*w| (FP64), the scale of the parity tolerance.
+ *
+ * Element addresses go through caller-given strides (in elements), so a
+ * layout (NCHW, NHWC, a padded view) changes addressing only.
+ *
+ * Threads: plain pthreads split the (n,k) pairs; the thread count is the
+ * caller's.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+typedef long long i64;
+
+typedef struct {
+    const double *x;
+    i64 xs[4];            /* strides of x for n, c, h, w */
+    const double *w;
+    i64 ws[4];            /* strides of w for k, c, r, s */
+    double *y;            /* output, strides ys for n, k, p, q */
+    i64 ys[4];
+    double *bound;        /* sum |x*w|, same strides as y; may be NULL */
+    const double *y_in;   /* beta term input, same strides as y; may be NULL */
+    const double *bias;   /* K values; may be NULL */
+    int N, C, H, W, K, R, S;
+    int pt, pb, pl, pr;   /* pads: top, bottom, left, right */
+    int u, v, dh, dw;     /* strides and dilations */
+    double alpha, beta;
+    int relu;
+    i64 P, Q;
+} oracle_problem;
+
+/* Number of window positions along one axis: the count of o >= 0 with
+ * o*stride + dil*(filt-1) <= in - 1 + pad_lo + pad_hi, i.e. the dilated
+ * window fits inside the padded input. */
+i64 oracle_out_extent(i64 in, i64 pad_lo, i64 pad_hi, i64 filt, i64 dil, i64 stride)
+{
+    if (in <= 0 || filt <= 0 || dil <= 0 || stride <= 0 || pad_lo < 0 || pad_hi < 0)
+        return -1;
+    i64 eff = dil * (filt - 1) + 1;
+    i64 span = in + pad_lo + pad_hi - eff;
+    if (span < 0)
+        return 0;
+    return span / stride + 1;
+}
+
+/* One output element: the receptive-field dot product, then the epilogue. */
+static void oracle_one(const oracle_problem *pr, i64 n, i64 k, i64 p, i64 q,
+                       double *val_out, double *bnd_out)
+{
+    double acc = 0.0, bnd = 0.0;
+    for (i64 c = 0; c < pr->C; ++c) {
+        for (i64 r = 0; r < pr->R; ++r) {
+            i64 h = p * pr->u + r * pr->dh - pr->pt;
+            if (h < 0 || h >= pr->H)
+                continue;                       /* zero padding row */
+            for (i64 s = 0; s < pr->S; ++s) {
+                i64 wi = q * pr->v + s * pr->dw - pr->pl;
+                if (wi < 0 || wi >= pr->W)
+                    continue;                   /* zero padding column */
+                double xv = pr->x[n * pr->xs[0] + c * pr->xs[1] + h * pr->xs[2] + wi * pr->xs[3]];
+                double wv = pr->w[k * pr->ws[0] + c * pr->ws[1] + r * pr->ws[2] + s * pr->ws[3]];
+                acc += xv * wv;
+                bnd += fabs(xv * wv);
+            }
+        }
+    }
+    double val = pr->alpha * acc;
+    i64 yoff = n * pr->ys[0] + k * pr->ys[1] + p * pr->ys[2] + q * pr->ys[3];
+    if (pr->beta != 0.0 && pr->y_in)
+        val += pr->beta * pr->y_in[yoff];
+    if (pr->bias)
+        val += pr->bias[k];
+    if (pr->relu && val < 0.0)
+        val = 0.0;
+    *val_out = val;
+    *bnd_out = bnd;
+}
+
+typedef struct {
+    const oracle_problem *pr;
+    i64 first, last;      /* range of flattened (n,k) pairs */
+} oracle_slice;
+
+static void *oracle_worker(void *arg)
+{
+    const oracle_slice *sl = (const oracle_slice *)arg;
+    const oracle_problem *pr = sl->pr;
+    for (i64 nk = sl->first; nk < sl->last; ++nk) {
+        i64 n = nk / pr->K, k = nk % pr->K;
+        for (i64 p = 0; p < pr->P; ++p) {
+            for (i64 q = 0; q < pr->Q; ++q) {
+                double val, bnd;
+                oracle_one(pr, n, k, p, q, &val, &bnd);
+                i64 yoff = n * pr->ys[0] + k * pr->ys[1] + p * pr->ys[2] + q * pr->ys[3];
+                pr->y[yoff] = val;
+                if (pr->bound)
+                    pr->bound[yoff] = bnd;
+            }
+        }
+    }
+    return NULL;
+}
+
+static int oracle_fill(oracle_problem *pr,
+                       const double *x, const i64 *xs, const double *w, const i64 *ws,
+                       double *y, const i64 *ys, double *bound,
+                       int N, int C, int H, int W, int K, int R, int S,
+                       int pt, int pb, int pl, int prt, int u, int v, int dh, int dw,
+                       double alpha, double beta, const double *y_in, const double *bias, int relu)
+{
+    if (!x || !w || !xs || !ws || !ys)
+        return 1;
+    if (N < 0 || C <= 0 || H <= 0 || W <= 0 || K <= 0 || R <= 0 || S <= 0)
+        return 1;
+    pr->x = x; pr->w = w; pr->y = y; pr->bound = bound; pr->y_in = y_in; pr->bias = bias;
+    for (int i = 0; i < 4; ++i) {
+        pr->xs[i] = xs[i];
+        pr->ws[i] = ws[i];
+        pr->ys[i] = ys[i];
+    }
+    pr->N = N; pr->C = C; pr->H = H; pr->W = W; pr->K = K; pr->R = R; pr->S = S;
+    pr->pt = pt; pr->pb = pb; pr->pl = pl; pr->pr = prt;
+    pr->u = u; pr->v = v; pr->dh = dh; pr->dw = dw;
+    pr->alpha = alpha; pr->beta = beta; pr->relu = relu;
+    pr->P = oracle_out_extent(H, pt, pb, R, dh, u);
+    pr->Q = oracle_out_extent(W, pl, prt, S, dw, v);
+    if (pr->P <= 0 || pr->Q <= 0)
+        return 2;
+    return 0;
+}
+
+/*
+ * Full forward convolution.  Strides are in elements: xs = {n,c,h,w},
+ * ws = {k,c,r,s}, ys = {n,k,p,q} (y, bound and y_in share ys).
+ * Returns 0 on success, 1 on a bad argument, 2 when the output is empty.
+ */
+int oracle_conv2d_fprop(const double *x, const i64 *xs, const double *w, const i64 *ws,
+                        double *y, const i64 *ys, double *bound,
+                        int N, int C, int H, int W, int K, int R, int S,
+                        int pad_top, int pad_bottom, int pad_left, int pad_right,
+                        int u, int v, int dil_h, int dil_w,
+                        double alpha, double beta, const double *y_in, const double *bias,
+                        int relu, int nthreads)
+{
+    oracle_problem pr;
+    int rc = oracle_fill(&pr, x, xs, w, ws, y, ys, bound, N, C, H, W, K, R, S,
+                         pad_top, pad_bottom, pad_left, pad_right, u, v, dil_h, dil_w,
+                         alpha, beta, y_in, bias, relu);
+    if (rc)
+        return rc;
+    if (!y)
+        return 1;
+    i64 pairs = (i64)N * K;
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > 256)
+        nthreads = 256;
+    if ((i64)nthreads > pairs)
+        nthreads = (int)(pairs > 0 ? pairs : 1);
+    pthread_t tid[256];
+    oracle_slice sl[256];
+    int started[256];
+    for (int t = 0; t < nthreads; ++t) {
+        sl[t].pr = &pr;
+        sl[t].first = pairs * t / nthreads;
+        sl[t].last = pairs * (t + 1) / nthreads;
+        started[t] = 0;
+    }
+    for (int t = 1; t < nthreads; ++t)
+        started[t] = pthread_create(&tid[t], NULL, oracle_worker, &sl[t]) == 0;
+    oracle_worker(&sl[0]);
+    for (int t = 1; t < nthreads; ++t) {
+        if (started[t])
+            pthread_join(tid[t], NULL);
+        else
+            oracle_worker(&sl[t]);   /* thread could not start: do its share here */
+    }
+    return 0;
+}
+
+/*
+ * The same definition at a list of output coordinates pts[i] = (n,k,p,q),
+ * i < npts.  out[i] gets the epilogued value, bound_out[i] (if not NULL)
+ * gets sum |x*w|.  y_in (if beta != 0) is read with strides ys.
+ * Returns 0, 1 on a bad argument or coordinate, 2 when the output is empty.
+ */
+int oracle_conv2d_fprop_points(const double *x, const i64 *xs, const double *w, const i64 *ws,
+                               const i64 *ys, int N, int C, int H, int W, int K, int R, int S,
+                               int pad_top, int pad_bottom, int pad_left, int pad_right,
+                               int u, int v, int dil_h, int dil_w,
+                               double alpha, double beta, const double *y_in, const double *bias,
+                               int relu, const i64 *pts, i64 npts, double *out, double *bound_out)
+{
+    oracle_problem pr;
+    i64 zero_strides[4] = {0, 0, 0, 0};
+    int rc = oracle_fill(&pr, x, xs, w, ws, NULL, ys ? ys : zero_strides, NULL,
+                         N, C, H, W, K, R, S, pad_top, pad_bottom, pad_left, pad_right,
+                         u, v, dil_h, dil_w, alpha, beta, y_in, bias, relu);
+    if (rc)
+        return rc;
+    if (!pts || !out)
+        return 1;
+    for (i64 i = 0; i < npts; ++i) {
+        i64 n = pts[4 * i], k = pts[4 * i + 1], p = pts[4 * i + 2], q = pts[4 * i + 3];
+        if (n < 0 || n >= N || k < 0 || k >= K || p < 0 || p >= pr.P || q < 0 || q >= pr.Q)
+            return 1;
+        double val, bnd;
+        oracle_one(&pr, n, k, p, q, &val, &bnd);
+        out[i] = val;
+        if (bound_out)
+            bound_out[i] = bnd;
+    }
+    return 0;
+}

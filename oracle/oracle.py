@@ -1,0 +1,189 @@
+"""Python front end of the CPU oracle (``conv_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by the package's smoke
+check and by the benchmark's CPU-baseline leg, never by the product path.
+It shares no code with the CUDA library.
+
+``build()`` compiles ``conv_oracle.c`` with gcc into ``oracle/_build`` (no
+OpenMP runtime: plain pthreads).  ``conv2d_fprop`` takes numpy arrays in any
+layout (strides are read from the arrays) and returns FP64 y and
+bound = sum |x*w|.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import sys
+from typing import Optional, Tuple
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "conv_oracle.c")
+BUILD_DIR = os.path.join(HERE, "_build")
+LIB = os.path.join(BUILD_DIR, "libconv_oracle.so")
+
+_lib = None
+_i64p = ctypes.POINTER(ctypes.c_longlong)
+_dp = ctypes.POINTER(ctypes.c_double)
+
+
+def build(force: bool = False, src: str = SRC, out: str = LIB) -> str:
+    """Compile the oracle shared library (idempotent unless ``force``)."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fno-fast-math",
+           "-ffp-contract=off", "-o", tmp, src, "-lpthread", "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def load(path: Optional[str] = None):
+    """Load (building if needed) the oracle library; returns the ctypes handle."""
+    global _lib
+    if path is None and _lib is not None:
+        return _lib
+    p = path or build()
+    lib = ctypes.CDLL(p)
+    lib.oracle_out_extent.restype = ctypes.c_longlong
+    lib.oracle_out_extent.argtypes = [ctypes.c_longlong] * 6
+    common = [_dp, _i64p, _dp, _i64p]
+    ints = [ctypes.c_int] * 15
+    lib.oracle_conv2d_fprop.restype = ctypes.c_int
+    lib.oracle_conv2d_fprop.argtypes = (common + [_dp, _i64p, _dp] + ints
+                                        + [ctypes.c_double, ctypes.c_double, _dp, _dp,
+                                           ctypes.c_int, ctypes.c_int])
+    lib.oracle_conv2d_fprop_points.restype = ctypes.c_int
+    lib.oracle_conv2d_fprop_points.argtypes = (common + [_i64p] + ints
+                                               + [ctypes.c_double, ctypes.c_double, _dp, _dp,
+                                                  ctypes.c_int, _i64p, ctypes.c_longlong,
+                                                  _dp, _dp])
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def default_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def _strides(a: np.ndarray) -> np.ndarray:
+    return np.array([s // a.itemsize for s in a.strides], dtype=np.int64)
+
+
+def _ptr(a: Optional[np.ndarray]):
+    if a is None:
+        return None
+    return a.ctypes.data_as(_dp)
+
+
+def out_extent(inp, pad_lo, pad_hi, filt, dil, stride, lib=None) -> int:
+    lib = lib or load()
+    return int(lib.oracle_out_extent(inp, pad_lo, pad_hi, filt, dil, stride))
+
+
+def _as_f64_view(a: np.ndarray, name: str) -> np.ndarray:
+    if a.dtype != np.float64:
+        raise TypeError(f"{name} must be float64 (widen the rounded inputs exactly first)")
+    return a
+
+
+def conv2d_fprop(x: np.ndarray, w: np.ndarray, *, pads=(0, 0, 0, 0), stride=(1, 1),
+                 dilation=(1, 1), alpha: float = 1.0, beta: float = 0.0,
+                 y_in: Optional[np.ndarray] = None, bias: Optional[np.ndarray] = None,
+                 relu: bool = False, nthreads: Optional[int] = None,
+                 x_axes: str = "NCHW", w_axes: str = "KCRS", lib=None
+                 ) -> Tuple[np.ndarray, np.ndarray]:
+    """Forward convolution on FP64 arrays.
+
+    ``x`` is indexed with axes ``x_axes`` (a permutation of "NCHW"), ``w`` with
+    ``w_axes`` (a permutation of "KCRS"); any strides are allowed.  ``pads`` is
+    (top, bottom, left, right).  Returns (y, bound) as NCHW-shaped FP64 arrays
+    [N, K, P, Q].
+    """
+    lib = lib or load()
+    x = _as_f64_view(x, "x")
+    w = _as_f64_view(w, "w")
+    xs_ax = _strides(x)
+    ws_ax = _strides(w)
+    dims_x = dict(zip(x_axes, x.shape))
+    dims_w = dict(zip(w_axes, w.shape))
+    xs = np.array([xs_ax[x_axes.index(a)] for a in "NCHW"], dtype=np.int64)
+    ws = np.array([ws_ax[w_axes.index(a)] for a in "KCRS"], dtype=np.int64)
+    N, C, H, W = (dims_x[a] for a in "NCHW")
+    K, C2, R, S = (dims_w[a] for a in "KCRS")
+    if C2 != C:
+        raise ValueError("channel mismatch between x and w")
+    pt, pb, pl, pr = pads
+    u, v = stride
+    dh, dw = dilation
+    P = out_extent(H, pt, pb, R, dh, u, lib)
+    Q = out_extent(W, pl, pr, S, dw, v, lib)
+    if P <= 0 or Q <= 0:
+        raise ValueError(f"empty output (P={P}, Q={Q})")
+    y = np.zeros((N, K, P, Q), dtype=np.float64)
+    bound = np.zeros_like(y)
+    ys = _strides(y)
+    if y_in is not None:
+        y_in = np.ascontiguousarray(y_in, dtype=np.float64).reshape(N, K, P, Q)
+    if bias is not None:
+        bias = np.ascontiguousarray(bias, dtype=np.float64).reshape(K)
+    rc = lib.oracle_conv2d_fprop(
+        _ptr(x), xs.ctypes.data_as(_i64p), _ptr(w), ws.ctypes.data_as(_i64p),
+        _ptr(y), ys.ctypes.data_as(_i64p), _ptr(bound),
+        N, C, H, W, K, R, S, pt, pb, pl, pr, u, v, dh, dw,
+        float(alpha), float(beta), _ptr(y_in), _ptr(bias), int(bool(relu)),
+        int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError(f"oracle_conv2d_fprop returned {rc}")
+    return y, bound
+
+
+def conv2d_fprop_points(x: np.ndarray, w: np.ndarray, pts: np.ndarray, *, pads=(0, 0, 0, 0),
+                        stride=(1, 1), dilation=(1, 1), alpha: float = 1.0, beta: float = 0.0,
+                        y_in: Optional[np.ndarray] = None, bias: Optional[np.ndarray] = None,
+                        relu: bool = False, x_axes: str = "NCHW", w_axes: str = "KCRS",
+                        lib=None) -> Tuple[np.ndarray, np.ndarray]:
+    """The oracle at sampled output coordinates ``pts`` (int64 [n,4]: n,k,p,q).
+    ``y_in`` (if used) is an NCHW-shaped [N,K,P,Q] array.  Returns (values, bound)."""
+    lib = lib or load()
+    x = _as_f64_view(x, "x")
+    w = _as_f64_view(w, "w")
+    xs_ax = _strides(x)
+    ws_ax = _strides(w)
+    dims_x = dict(zip(x_axes, x.shape))
+    dims_w = dict(zip(w_axes, w.shape))
+    xs = np.array([xs_ax[x_axes.index(a)] for a in "NCHW"], dtype=np.int64)
+    ws = np.array([ws_ax[w_axes.index(a)] for a in "KCRS"], dtype=np.int64)
+    N, C, H, W = (dims_x[a] for a in "NCHW")
+    K, _, R, S = (dims_w[a] for a in "KCRS")
+    pts = np.ascontiguousarray(pts, dtype=np.int64).reshape(-1, 4)
+    out = np.zeros(len(pts), dtype=np.float64)
+    bnd = np.zeros(len(pts), dtype=np.float64)
+    ys = None
+    if y_in is not None:
+        y_in = np.ascontiguousarray(y_in, dtype=np.float64)
+        ys = _strides(y_in)
+    if bias is not None:
+        bias = np.ascontiguousarray(bias, dtype=np.float64).reshape(K)
+    pt, pb, pl, pr = pads
+    rc = lib.oracle_conv2d_fprop_points(
+        _ptr(x), xs.ctypes.data_as(_i64p), _ptr(w), ws.ctypes.data_as(_i64p),
+        ys.ctypes.data_as(_i64p) if ys is not None else None,
+        N, C, H, W, K, R, S, pt, pb, pl, pr, stride[0], stride[1], dilation[0], dilation[1],
+        float(alpha), float(beta), _ptr(y_in), _ptr(bias),
+        int(bool(relu)), pts.ctypes.data_as(_i64p), len(pts), _ptr(out), _ptr(bnd))
+    if rc != 0:
+        raise ValueError(f"oracle_conv2d_fprop_points returned {rc}")
+    return out, bnd
+
+
+if __name__ == "__main__":  # pragma: no cover
+    print(build(force="--force" in sys.argv))
