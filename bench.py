@@ -1,0 +1,436 @@
+"""Forward-convolution benchmark (conv fprop TFLOP/s, direct-convolution FLOPs).
+
+One step = the five convolution layers of the AlexNet-style stack (N=128,
+BF16, NHWC, FP32 output), each on its own seeded synthetic input, through the
+C ABI.  The metric counts only direct-convolution FLOPs 2*N*K*P*Q*C*R*S
+(maxDNN page, method and findings sections).  L2 is flushed (256 MiB write)
+between timed steps, outside the timed events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload alexnet|overfeat|resnet50|speech]
+
+--impl reference times the CPU oracle (FP64 direct convolution) on the host
+cores on a bounded sample of the same workload.  Under torchrun with N > 1
+every rank runs its own replica (the layer has no exchange step) and rank 0
+prints the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "conv fprop TFLOP/s (direct-conv FLOPs) and % of GB300 dense tensor-core peak"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def env_rank():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "deep_learning_convolution_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def layer_geometry(layer, P, Q):
+    """FLOPs and algorithmic bytes (x, w read once, y written once)."""
+    esz = 2 if layer.dtype == "bf16" else 4
+    flops = 2 * layer.N * layer.K * P * Q * layer.C * layer.R * layer.S
+    # activation bytes actually touched (a 1x1 strided layer reads only the sampled pixels)
+    if layer.R == 1 and layer.S == 1 and (layer.u > 1 or layer.v > 1):
+        x_bytes = layer.N * layer.C * P * Q * esz
+    else:
+        x_bytes = layer.N * layer.C * layer.H * layer.W * esz
+    w_bytes = layer.K * layer.C * layer.R * layer.S * esz
+    y_bytes = layer.N * layer.K * P * Q * 4
+    return flops, x_bytes + w_bytes + y_bytes
+
+
+# ---------------------------------------------------------------------------
+# clocks sampling
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int, interval_ms: int = 20):
+        self.proc = None
+        self.dev = device_index
+        self.interval = interval_ms
+
+    def query_once(self):
+        try:
+            out = subprocess.run(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                                  "-i", str(self.dev)], capture_output=True, text=True, timeout=20)
+            return [l for l in out.stdout.splitlines() if l.strip()]
+        except Exception:
+            return []
+
+    def start(self):
+        self.before = self.query_once()
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                 "-i", str(self.dev), "-lms", str(self.interval)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=10)
+                lines = [l for l in out.splitlines() if l.strip()]
+            except Exception:
+                self.proc.kill()
+        after = self.query_once()
+        return self.summarise(lines, self.before + after)
+
+    @staticmethod
+    def _parse(line):
+        f = [x.strip() for x in line.split(",")]
+        if len(f) < 9:
+            return None
+        try:
+            sm = float(f[1].split()[0])
+            smax = float(f[2].split()[0])
+        except ValueError:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = [n for n, v in zip(names, f[5:9]) if v.lower().startswith("active")]
+        return sm, smax, reasons
+
+    def summarise(self, during, around):
+        parsed = [p for p in map(self._parse, during) if p]
+        source = "during timed region"
+        if not parsed:
+            parsed = [p for p in map(self._parse, around) if p]
+            source = "around timed region (no sample landed inside)"
+        if not parsed:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "source": "nvidia-smi unavailable"}
+        reasons = sorted({r for p in parsed for r in p[2]})
+        return {"sm_mhz": statistics.median(p[0] for p in parsed),
+                "sm_max_mhz": max(p[1] for p in parsed), "reasons": reasons,
+                "samples": len(parsed), "source": source}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+    from deep_learning_convolution_gb300 import api, synth
+    from deep_learning_convolution_gb300 import build as dlc_build
+
+    dlc_build.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    stream = torch.cuda.current_stream()
+    handle = api.Handle(stream)
+    layers = synth.WORKLOADS[args.workload]
+
+    probs = []
+    for j, layer in enumerate(layers):
+        x, w, _ = synth.make_inputs(layer, synth.workload_seed(args.workload, j))
+        xt, wt = api.layer_tensors(layer, x, w, dev)
+        conv, y = api.layer_problem(handle, layer, xt, wt)
+        n, k, p, q = conv.output_dim()
+        flops, nbytes = layer_geometry(layer, p, q)
+        probs.append(dict(layer=layer, x=xt, w=wt, y=y, conv=conv, flops=flops, bytes=nbytes,
+                          kernel=conv.kernel(xt, wt, y), host_x=x, host_w=w))
+        del x, w
+    step_flops = sum(pr["flops"] for pr in probs)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        for pr in probs:
+            pr["conv"](pr["x"], pr["w"], pr["y"])
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    handle.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(probs) + 1)] for _ in range(K)]
+    sampler = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches0 = handle.launches()
+    sampler.start()
+    time.sleep(0.05)
+    for i in range(K):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        for j, pr in enumerate(probs):
+            pr["conv"](pr["x"], pr["w"], pr["y"])
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    launches = handle.launches() - launches0
+    handle.synchronize()  # raises if a kernel recorded a device error
+
+    per_layer_ms = [0.0] * len(probs)
+    total_ms = 0.0
+    for i in range(K):
+        total_ms += ev[i][0].elapsed_time(ev[i][-1])
+        for j in range(len(probs)):
+            per_layer_ms[j] += ev[i][j].elapsed_time(ev[i][j + 1])
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    value = step_flops * world * K / (total_ms * 1e-3) / 1e12
+
+    peaks = load_peaks()
+    peak_tf = peaks["bf16_tflops"] if args.workload != "speech" else peaks["bf16_tflops"] / 2
+    layer_rows = []
+    by_kernel = {}
+    for j, pr in enumerate(probs):
+        t_s = per_layer_ms[j] / K * 1e-3
+        tflops = pr["flops"] / t_s / 1e12
+        gbs = pr["bytes"] / t_s / 1e9
+        roof = min(peak_tf, pr["flops"] / pr["bytes"] * peaks["hbm_gbs"] / 1e3)
+        layer_rows.append({"layer": pr["layer"].name, "kernel": pr["kernel"],
+                           "us": round(t_s * 1e6, 2), "tflops": round(tflops, 1),
+                           "hbm_gbs": round(gbs, 1),
+                           "bound": "tensor" if roof >= peak_tf else "hbm",
+                           "roofline_tflops": round(roof, 1),
+                           "frac_of_roofline": round(tflops / roof, 4)})
+        k = by_kernel.setdefault(pr["kernel"], {"flops": 0, "bytes": 0, "ms": 0.0, "launches": 0})
+        k["flops"] += pr["flops"]
+        k["bytes"] += pr["bytes"]
+        k["ms"] += per_layer_ms[j]
+        k["launches"] += K
+    dom_name, dom = max(by_kernel.items(), key=lambda kv: kv[1]["ms"])
+    avg_launch_s = dom["ms"] / dom["launches"] * 1e-3
+    flops_per_launch = dom["flops"] / (dom["launches"] / K)
+    bytes_per_launch = dom["bytes"] / (dom["launches"] / K)
+    ai = flops_per_launch / bytes_per_launch
+    tensor_bound = ai * peaks["hbm_gbs"] / 1e3 >= peak_tf
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tfile):
+        with open(tfile) as f:
+            td = json.load(f)
+        ent = td.get(args.workload, {}).get(dom_name)
+        if ent and ent.get("kernel_sha") == kernel_source_hash():
+            traffic = ent.get("dram_bytes_per_launch")
+    if tensor_bound:
+        achieved = flops_per_launch / avg_launch_s / 1e12
+        roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak_tf,
+                    "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4), "traffic": traffic,
+                    "kernel": dom_name, "peak_source": f"{peaks['source']} bf16 burst" +
+                    (" x 1/2 (tf32)" if args.workload == "speech" else "")}
+    else:
+        achieved = bytes_per_launch / avg_launch_s / 1e9
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                    "traffic": traffic, "kernel": dom_name,
+                    "peak_source": f"{peaks['source']} copy bandwidth"}
+
+    # end to end: pinned host buffers -> device -> conv -> host, every step
+    e2e = run_e2e(args, probs, handle, stream, dev, step_flops, world)
+
+    result = None
+    if rank == 0:
+        dtype = "bf16" if layers[0].dtype == "bf16" else layers[0].dtype
+        result = {
+            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
+            "data": "synthetic",
+            "config": {"workload": f"{args.workload}_stack", "layers": [p["layer"].name for p in probs],
+                       "batch": layers[0].N, "layout": layers[0].layout,
+                       "output": "fp32", "l2": "flushed between steps (256 MiB write, untimed)",
+                       "parallelism": f"replicas{world}" if world > 1 else "single_gpu",
+                       "flops_per_step": step_flops},
+            "roofline": roofline,
+            "layers": layer_rows,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clocks,
+        }
+        if not args.no_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
+    for pr in probs:
+        pr["conv"].close()
+    handle.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return result
+
+
+def run_e2e(args, probs, handle, stream, dev, step_flops, world):
+    import numpy as np
+    import torch
+    steps = max(3, min(args.steps, args.e2e_steps))
+    host = []
+    h2d = d2h = 0
+    for pr in probs:
+        hx = torch.empty(pr["x"].shape, dtype=pr["x"].dtype, pin_memory=True)
+        hx.copy_(pr["x"].cpu())
+        hw = torch.empty(pr["w"].shape, dtype=pr["w"].dtype, pin_memory=True)
+        hw.copy_(pr["w"].cpu())
+        hy = torch.empty(pr["y"].shape, dtype=pr["y"].dtype, pin_memory=True)
+        host.append((hx, hw, hy))
+        h2d += hx.numel() * hx.element_size() + hw.numel() * hw.element_size()
+        d2h += hy.numel() * hy.element_size()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+
+    def one():
+        for pr, (hx, hw, hy) in zip(probs, host):
+            pr["x"].copy_(hx, non_blocking=True)
+            pr["w"].copy_(hw, non_blocking=True)
+            pr["conv"](pr["x"], pr["w"], pr["y"])
+            hy.copy_(pr["y"], non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        one()
+    end.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end)
+    value = step_flops * world * steps / (ms * 1e-3) / 1e12
+    return {"value": round(value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(ms / steps, 3)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_step(workload, images=1, threads=None):
+    """Runs the oracle over `images` images of every layer of the workload;
+    returns (direct-conv FLOPs, seconds, threads)."""
+    import numpy as np
+    from deep_learning_convolution_gb300 import synth
+    from oracle import oracle
+    threads = threads or oracle.default_threads()
+    flops = 0
+    secs = 0.0
+    for j, layer in enumerate(synth.WORKLOADS[workload]):
+        x, w, _ = synth.make_inputs(layer, synth.workload_seed(workload, j), batch=images)
+        x64, w64 = x.astype(np.float64), w.astype(np.float64)
+        t0 = time.perf_counter()
+        y, _ = oracle.conv2d_fprop(x64, w64, pads=(layer.pad_top, layer.pad_bottom,
+                                                   layer.pad_left, layer.pad_right),
+                                   stride=(layer.u, layer.v), dilation=(layer.dil_h, layer.dil_w),
+                                   nthreads=threads)
+        secs += time.perf_counter() - t0
+        flops += 2 * images * layer.K * y.shape[2] * y.shape[3] * layer.C * layer.R * layer.S
+    return flops, secs, threads
+
+
+def cpu_baseline(workload, budget_s=15.0):
+    from oracle import oracle
+    oracle.build()
+    flops, secs, threads = oracle_sample_step(workload, images=1)
+    total_f, total_s, runs = flops, secs, 1
+    while total_s < budget_s and runs < 64:
+        f, s, _ = oracle_sample_step(workload, images=1)
+        total_f += f
+        total_s += s
+        runs += 1
+    return {"value": round(total_f / total_s / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{runs} x (1 image through every {workload} layer, all K, full P x Q), "
+                      f"FP64 direct convolution, {total_s:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    from oracle import oracle
+    oracle.build()
+    for _ in range(args.warmup):
+        oracle_sample_step(args.workload, images=1)
+    flops = 0
+    secs = 0.0
+    threads = oracle.default_threads()
+    for _ in range(args.steps):
+        f, s, threads = oracle_sample_step(args.workload, images=1)
+        flops += f
+        secs += s
+    value = flops / secs / 1e12
+    sample = (f"each step: 1 image of the {args.workload} stack through every layer "
+              f"(all K, full P x Q), FP64 direct convolution on {threads} host threads")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": f"{args.workload}_stack", "sample": "1 image per step"},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="alexnet",
+                    choices=["alexnet", "overfeat", "resnet50", "speech"])
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local_rank = env_rank()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_ours(args, rank, world, local_rank)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

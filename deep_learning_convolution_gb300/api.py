@@ -1,0 +1,211 @@
+"""Descriptor marshalling for torch tensors on top of the C ABI.
+
+Only argument marshalling: descriptor values and device pointers are read
+from torch tensors and passed to the C functions in :mod:`binding`; the
+convolution itself runs in ``libdlc.so``.
+
+Axis strings name the logical meaning of a tensor's dimensions: activations
+use a permutation of ``"NCHW"`` (``"NHWC"`` for channels-last storage),
+filters ``"KCRS"`` or ``"KRSC"``.  Any torch strides are passed through, so
+views (sub-tensors, padded rows) work where the kernel supports them.
+"""
+from __future__ import annotations
+
+from typing import Optional, Sequence
+
+from . import binding as B
+
+MATH = {"fp32": B.DLC_MATH_FP32, "tf32": B.DLC_MATH_TF32, "bf16": B.DLC_MATH_BF16}
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return B.DLC_DATA_FLOAT
+    if t.dtype == torch.bfloat16:
+        return B.DLC_DATA_BFLOAT16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _logical(t, axes: str, order: str):
+    """(sizes, strides) of tensor t in the logical axis order `order`."""
+    if sorted(axes) != sorted(order) or t.dim() != 4:
+        raise ValueError(f"axes {axes!r} do not describe a 4-D {order} tensor")
+    sizes = [t.shape[axes.index(a)] for a in order]
+    strides = [t.stride(axes.index(a)) for a in order]
+    return sizes, strides
+
+
+class Handle:
+    """Owns a dlcHandle_t bound to the current device; follows torch's
+    current stream unless a stream is given."""
+
+    def __init__(self, stream=None):
+        import torch
+        self.h = B.dlcCreate()
+        self.set_stream(stream if stream is not None else torch.cuda.current_stream())
+
+    def set_stream(self, stream):
+        B.dlcSetStream(self.h, int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream))
+
+    def synchronize(self):
+        B.dlcSynchronize(self.h)
+
+    def launches(self) -> int:
+        return B.dlcGetLaunchCount(self.h)
+
+    def last_device_error(self):
+        return B.dlcGetLastDeviceError(self.h)
+
+    def close(self):
+        if self.h is not None:
+            B.dlcDestroy(self.h)
+            self.h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+
+class Conv2dForward:
+    """Descriptors of one forward-convolution problem built from example
+    tensors; calling it launches dlcConvolution(BiasActivation)Forward."""
+
+    def __init__(self, handle: Handle, x, w, y, *, x_axes: str = "NCHW", w_axes: str = "KCRS",
+                 y_axes: str = "NCHW", pads: Sequence[int] = (0, 0, 0, 0),
+                 stride: Sequence[int] = (1, 1), dilation: Sequence[int] = (1, 1),
+                 math: str = "bf16"):
+        self.handle = handle
+        self.x_desc = B.dlcCreateTensorDescriptor()
+        self.w_desc = B.dlcCreateFilterDescriptor()
+        self.y_desc = B.dlcCreateTensorDescriptor()
+        self.conv = B.dlcCreateConvolutionDescriptor()
+        xs, xst = _logical(x, x_axes, "NCHW")
+        B.dlcSetTensor4dDescriptorEx(self.x_desc, _dtype_code(x), *xs, *xst)
+        if w_axes == "KCRS":
+            fmt = B.DLC_TENSOR_NCHW
+        elif w_axes == "KRSC":
+            fmt = B.DLC_TENSOR_NHWC
+        else:
+            raise ValueError("filters must be KCRS or KRSC")
+        if not w.is_contiguous():
+            raise ValueError("filter tensors must be dense (contiguous)")
+        ws, _ = _logical(w, w_axes, "KCRS")
+        B.dlcSetFilter4dDescriptor(self.w_desc, _dtype_code(w), fmt, *ws)
+        ys, yst = _logical(y, y_axes, "NCHW")
+        B.dlcSetTensor4dDescriptorEx(self.y_desc, _dtype_code(y), *ys, *yst)
+        B.dlcSetConvolution2dDescriptor(self.conv, 0, 0, int(stride[0]), int(stride[1]),
+                                        int(dilation[0]), int(dilation[1]), MATH[math])
+        B.dlcSetConvolution2dPadding(self.conv, *[int(p) for p in pads])
+
+    def output_dim(self):
+        return B.dlcGetConvolution2dForwardOutputDim(self.conv, self.x_desc, self.w_desc)
+
+    def workspace_size(self) -> int:
+        return B.dlcGetConvolutionForwardWorkspaceSize(self.handle.h, self.x_desc, self.w_desc,
+                                                       self.conv, self.y_desc)
+
+    def kernel(self, x=None, w=None, y=None) -> str:
+        k = B.dlcGetConvolutionForwardKernel(
+            self.handle.h, self.x_desc, x.data_ptr() if x is not None else 0, self.w_desc,
+            w.data_ptr() if w is not None else 0, self.conv, self.y_desc,
+            y.data_ptr() if y is not None else 0)
+        return B.KERNEL_NAMES[k]
+
+    def __call__(self, x, w, y, alpha: float = 1.0, beta: float = 0.0, bias=None,
+                 relu: bool = False):
+        if bias is None and not relu:
+            B.dlcConvolutionForward(self.handle.h, alpha, self.x_desc, x.data_ptr(), self.w_desc,
+                                    w.data_ptr(), self.conv, beta, self.y_desc, y.data_ptr())
+        else:
+            B.dlcConvolutionBiasActivationForward(
+                self.handle.h, alpha, self.x_desc, x.data_ptr(), self.w_desc, w.data_ptr(),
+                self.conv, beta, bias.data_ptr() if bias is not None else 0,
+                B.DLC_ACTIVATION_RELU if relu else B.DLC_ACTIVATION_IDENTITY, self.y_desc,
+                y.data_ptr())
+        return y
+
+    def close(self):
+        for d, f in ((self.x_desc, B.dlcDestroyTensorDescriptor),
+                     (self.y_desc, B.dlcDestroyTensorDescriptor),
+                     (self.w_desc, B.dlcDestroyFilterDescriptor),
+                     (self.conv, B.dlcDestroyConvolutionDescriptor)):
+            if d is not None:
+                f(d)
+        self.x_desc = self.y_desc = self.w_desc = self.conv = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def output_dim(x, w, *, x_axes="NCHW", w_axes="KCRS", pads=(0, 0, 0, 0), stride=(1, 1),
+               dilation=(1, 1)):
+    """(N, K, P, Q) from the library's descriptor call (no GPU work)."""
+    xd = B.dlcCreateTensorDescriptor()
+    wd = B.dlcCreateFilterDescriptor()
+    cd = B.dlcCreateConvolutionDescriptor()
+    try:
+        xs, xst = _logical(x, x_axes, "NCHW")
+        B.dlcSetTensor4dDescriptorEx(xd, _dtype_code(x), *xs, *xst)
+        ws, _ = _logical(w, w_axes, "KCRS")
+        B.dlcSetFilter4dDescriptor(wd, _dtype_code(w),
+                                   B.DLC_TENSOR_NCHW if w_axes == "KCRS" else B.DLC_TENSOR_NHWC, *ws)
+        B.dlcSetConvolution2dDescriptor(cd, 0, 0, int(stride[0]), int(stride[1]),
+                                        int(dilation[0]), int(dilation[1]), B.DLC_MATH_FP32)
+        B.dlcSetConvolution2dPadding(cd, *[int(p) for p in pads])
+        return B.dlcGetConvolution2dForwardOutputDim(cd, xd, wd)
+    finally:
+        B.dlcDestroyTensorDescriptor(xd)
+        B.dlcDestroyFilterDescriptor(wd)
+        B.dlcDestroyConvolutionDescriptor(cd)
+
+
+def layer_axes(layer):
+    """(x_axes, w_axes) of a synth.Layer's storage layout."""
+    return ("NHWC", "KRSC") if layer.layout == "NHWC" else ("NCHW", "KCRS")
+
+
+def layer_tensors(layer, x_nchw, w_kcrs, device):
+    """Device tensors x and w for a synth.Layer from logical-NCHW / KCRS numpy
+    arrays (already rounded), stored in the layer's layout (dense)."""
+    import numpy as np
+    import torch
+    from . import synth
+    if layer.dtype == "bf16":
+        xb = synth.round_to_bf16_bits(x_nchw).view(np.int16).reshape(x_nchw.shape)
+        wb = synth.round_to_bf16_bits(w_kcrs).view(np.int16).reshape(w_kcrs.shape)
+        xt = torch.from_numpy(xb).view(torch.bfloat16)
+        wt = torch.from_numpy(wb).view(torch.bfloat16)
+    else:
+        xt = torch.from_numpy(np.ascontiguousarray(x_nchw, dtype=np.float32))
+        wt = torch.from_numpy(np.ascontiguousarray(w_kcrs, dtype=np.float32))
+    if layer.layout == "NHWC":
+        xt = xt.permute(0, 2, 3, 1)
+        wt = wt.permute(0, 2, 3, 1)
+    return xt.contiguous().to(device), wt.contiguous().to(device)
+
+
+def layer_problem(handle, layer, xt, wt, y_dtype=None, y_axes=None):
+    """A Conv2dForward for a synth.Layer plus its freshly allocated y
+    (FP32 by default, in the layer's layout unless y_axes is given)."""
+    import torch
+    x_axes, w_axes = layer_axes(layer)
+    pads = (layer.pad_top, layer.pad_bottom, layer.pad_left, layer.pad_right)
+    stride, dil = (layer.u, layer.v), (layer.dil_h, layer.dil_w)
+    n, k, p, q = output_dim(xt, wt, x_axes=x_axes, w_axes=w_axes, pads=pads, stride=stride,
+                            dilation=dil)
+    y_axes = y_axes or x_axes
+    shape = [dict(N=n, C=k, H=p, W=q)[a] for a in y_axes]
+    y = torch.empty(shape, dtype=y_dtype or torch.float32, device=xt.device)
+    conv = Conv2dForward(handle, xt, wt, y, x_axes=x_axes, w_axes=w_axes, y_axes=y_axes,
+                         pads=pads, stride=stride, dilation=dil, math=math_of(layer))
+    return conv, y
+
+
+def math_of(layer) -> str:
+    return {"bf16": "bf16", "tf32": "tf32", "f32": "fp32"}[layer.dtype]

@@ -1,0 +1,494 @@
+// api.cu -- the C ABI: handles, descriptors, validation and kernel dispatch.
+//
+// Descriptor-based C interface with arbitrary strides and caller-owned device
+// buffers, following the cuDNN page's method section; zero workspace
+// following the zero-memory-overhead direct convolution page.
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "internal.h"
+
+namespace {
+
+int64_t out_extent(int64_t in, int64_t lo, int64_t hi, int64_t filt, int64_t dil, int64_t stride) {
+    int64_t eff = dil * (filt - 1) + 1;
+    int64_t span = in + lo + hi - eff;
+    if (span < 0) return 0;
+    return span / stride + 1;
+}
+
+size_t elt_size(dlcDataType_t t) { return t == DLC_DATA_BFLOAT16 ? 2 : 4; }
+
+bool valid_dtype(int t) { return t == DLC_DATA_FLOAT || t == DLC_DATA_BFLOAT16; }
+bool valid_format(int f) { return f == DLC_TENSOR_NCHW || f == DLC_TENSOR_NHWC; }
+
+// Largest element offset reachable through (extent, stride) pairs.
+int64_t max_offset(const int64_t *ext, const int64_t *str, int nd) {
+    int64_t m = 0;
+    for (int i = 0; i < nd; ++i) m += (ext[i] - 1) * str[i];
+    return m;
+}
+
+// True if distinct index tuples map to distinct offsets (no self-overlap):
+// sorted by stride, each stride must reach past the span of the smaller ones.
+bool strides_injective(const int64_t *ext, const int64_t *str, int nd) {
+    int idx[4] = {0, 1, 2, 3};
+    std::sort(idx, idx + nd, [&](int a, int b) { return str[a] < str[b]; });
+    int64_t span = 0;  // max offset of the dims seen so far
+    for (int i = 0; i < nd; ++i) {
+        int d = idx[i];
+        if (ext[d] == 1) continue;
+        if (str[d] <= span) return false;
+        span += (ext[d] - 1) * str[d];
+    }
+    return true;
+}
+
+bool ranges_overlap(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) {
+    return a0 < b1 && b0 < a1;
+}
+
+void filter_strides(const dlcFilterStruct *f, int64_t *ws) {
+    if (f->format == DLC_TENSOR_NCHW) {  // KCRS
+        ws[3] = 1;
+        ws[2] = f->s;
+        ws[1] = (int64_t)f->r * f->s;
+        ws[0] = (int64_t)f->c * f->r * f->s;
+    } else {  // KRSC
+        ws[1] = 1;
+        ws[3] = f->c;
+        ws[2] = (int64_t)f->s * f->c;
+        ws[0] = (int64_t)f->r * f->s * f->c;
+    }
+}
+
+// Validates descriptors (and pointers when check_ptrs) and fills `pb`.
+dlcStatus_t resolve(dlcTensorDescriptor_t xd, const void *x, dlcFilterDescriptor_t wd,
+                    const void *w, dlcConvolutionDescriptor_t cd, dlcTensorDescriptor_t yd,
+                    void *y, bool check_ptrs, ConvProblem &pb) {
+    if (!xd || !wd || !cd || !yd) return DLC_STATUS_BAD_PARAM;
+    if (!xd->set || !wd->set || !cd->set || !yd->set) return DLC_STATUS_NOT_INITIALIZED;
+    if (xd->c != wd->c) return DLC_STATUS_BAD_PARAM;
+    if (xd->dtype != wd->dtype) return DLC_STATUS_BAD_PARAM;
+    int64_t P = out_extent(xd->h, cd->pad_top, cd->pad_bottom, wd->r, cd->dil_h, cd->u);
+    int64_t Q = out_extent(xd->w, cd->pad_left, cd->pad_right, wd->s, cd->dil_w, cd->v);
+    if (P < 1 || Q < 1 || P > INT32_MAX || Q > INT32_MAX) return DLC_STATUS_BAD_PARAM;
+    if (yd->n != xd->n || yd->c != wd->k || yd->h != P || yd->w != Q) return DLC_STATUS_BAD_PARAM;
+
+    switch (cd->math) {
+        case DLC_MATH_FP32: break;
+        case DLC_MATH_TF32:
+            if (xd->dtype != DLC_DATA_FLOAT) return DLC_STATUS_NOT_SUPPORTED;
+            break;
+        case DLC_MATH_BF16:
+            if (xd->dtype != DLC_DATA_BFLOAT16) return DLC_STATUS_NOT_SUPPORTED;
+            break;
+        default: return DLC_STATUS_BAD_PARAM;
+    }
+
+    pb.N = xd->n; pb.C = xd->c; pb.H = xd->h; pb.W = xd->w;
+    pb.K = wd->k; pb.R = wd->r; pb.S = wd->s; pb.P = (int)P; pb.Q = (int)Q;
+    pb.pt = cd->pad_top; pb.pb = cd->pad_bottom; pb.pl = cd->pad_left; pb.pr = cd->pad_right;
+    pb.u = cd->u; pb.v = cd->v; pb.dh = cd->dil_h; pb.dw = cd->dil_w;
+    pb.math = cd->math;
+    pb.xdt = xd->dtype;
+    pb.ydt = yd->dtype;
+    pb.wfmt = wd->format;
+    for (int i = 0; i < 4; ++i) {
+        pb.xs[i] = xd->stride[i];
+        pb.ys[i] = yd->stride[i];
+    }
+    filter_strides(wd, pb.ws);
+    pb.x = x; pb.w = w; pb.y = y;
+    pb.bias = nullptr; pb.alpha = 1.f; pb.beta = 0.f; pb.relu = 0;
+
+    const int64_t yext[4] = {pb.N, pb.K, pb.P, pb.Q};
+    if (!strides_injective(yext, pb.ys, 4)) return DLC_STATUS_BAD_PARAM;
+    const int64_t xext[4] = {pb.N, pb.C, pb.H, pb.W};
+    const int64_t wext[4] = {pb.K, pb.C, pb.R, pb.S};
+    const int64_t xmax = max_offset(xext, pb.xs, 4);
+    const int64_t wmax = max_offset(wext, pb.ws, 4);
+    const int64_t ymax = max_offset(yext, pb.ys, 4);
+    const int64_t lim = (int64_t)1 << 60;
+    if (xmax >= lim || wmax >= lim || ymax >= lim) return DLC_STATUS_BAD_PARAM;
+
+    if (check_ptrs) {
+        if (!x || !w || !y) return DLC_STATUS_BAD_PARAM;
+        const size_t ex = elt_size(pb.xdt), ey = elt_size(pb.ydt);
+        if ((uintptr_t)x % ex || (uintptr_t)w % ex || (uintptr_t)y % ey) return DLC_STATUS_BAD_PARAM;
+        uintptr_t x0 = (uintptr_t)x, x1 = x0 + (uintptr_t)(xmax + 1) * ex;
+        uintptr_t w0 = (uintptr_t)w, w1 = w0 + (uintptr_t)(wmax + 1) * ex;
+        uintptr_t y0 = (uintptr_t)y, y1 = y0 + (uintptr_t)(ymax + 1) * ey;
+        if (ranges_overlap(x0, x1, y0, y1) || ranges_overlap(w0, w1, y0, y1))
+            return DLC_STATUS_BAD_PARAM;
+    }
+    return DLC_STATUS_SUCCESS;
+}
+
+dlcKernel_t pick_kernel(const dlcContext *ctx, const ConvProblem &pb) {
+    if (pb.math == DLC_MATH_FP32) return DLC_KERNEL_FFMA;
+    return dlc_tc_variant(ctx, pb);
+}
+
+dlcStatus_t pending_device_error(dlcContext *h) {
+    volatile int *e = h->h_err;
+    return (e && e[0] != 0) ? DLC_STATUS_EXECUTION_FAILED : DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t forward(dlcHandle_t h, const float *alpha, dlcTensorDescriptor_t xd, const void *x,
+                    dlcFilterDescriptor_t wd, const void *w, dlcConvolutionDescriptor_t cd,
+                    const float *beta, const float *bias, int relu, dlcTensorDescriptor_t yd,
+                    void *y) {
+    if (!h) return DLC_STATUS_NOT_INITIALIZED;
+    if (!alpha || !beta) return DLC_STATUS_BAD_PARAM;
+    ConvProblem pb;
+    dlcStatus_t st = resolve(xd, x, wd, w, cd, yd, y, true, pb);
+    if (st != DLC_STATUS_SUCCESS) return st;
+    if ((uintptr_t)bias % 4) return DLC_STATUS_BAD_PARAM;
+    pb.alpha = *alpha;
+    pb.beta = *beta;
+    pb.bias = bias;
+    pb.relu = relu;
+    st = pending_device_error(h);
+    if (st != DLC_STATUS_SUCCESS) return st;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return DLC_STATUS_BAD_PARAM;
+    dlcKernel_t k = pick_kernel(h, pb);
+    if (k == DLC_KERNEL_FFMA) return dlc_launch_ffma(h, pb);
+    if (k == DLC_KERNEL_NONE) return DLC_STATUS_NOT_SUPPORTED;
+    return dlc_launch_tc(h, pb, k);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *dlcGetErrorString(dlcStatus_t s) {
+    switch (s) {
+        case DLC_STATUS_SUCCESS: return "DLC_STATUS_SUCCESS";
+        case DLC_STATUS_NOT_INITIALIZED: return "DLC_STATUS_NOT_INITIALIZED";
+        case DLC_STATUS_BAD_PARAM: return "DLC_STATUS_BAD_PARAM";
+        case DLC_STATUS_NOT_SUPPORTED: return "DLC_STATUS_NOT_SUPPORTED";
+        case DLC_STATUS_EXECUTION_FAILED: return "DLC_STATUS_EXECUTION_FAILED";
+        case DLC_STATUS_INTERNAL_ERROR: return "DLC_STATUS_INTERNAL_ERROR";
+        case DLC_STATUS_ALLOC_FAILED: return "DLC_STATUS_ALLOC_FAILED";
+    }
+    return "DLC_STATUS_UNKNOWN";
+}
+
+dlcStatus_t dlcGetVersion(int *version) {
+    if (!version) return DLC_STATUS_BAD_PARAM;
+    *version = DLC_VERSION;
+    return DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlcCreate(dlcHandle_t *handle) {
+    if (!handle) return DLC_STATUS_BAD_PARAM;
+    *handle = nullptr;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DLC_STATUS_EXECUTION_FAILED;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return DLC_STATUS_EXECUTION_FAILED;
+    if (prop.major != 10 || prop.minor != 3) return DLC_STATUS_NOT_SUPPORTED;
+    dlcContext *h = new (std::nothrow) dlcContext();
+    if (!h) return DLC_STATUS_ALLOC_FAILED;
+    h->device = dev;
+    h->sm_count = prop.multiProcessorCount;
+    if (cudaHostAlloc((void **)&h->h_err, 4 * sizeof(int), cudaHostAllocMapped) != cudaSuccess) {
+        delete h;
+        return DLC_STATUS_EXECUTION_FAILED;
+    }
+    std::memset(h->h_err, 0, 4 * sizeof(int));
+    if (cudaHostGetDevicePointer((void **)&h->d_err, h->h_err, 0) != cudaSuccess) {
+        cudaFreeHost(h->h_err);
+        delete h;
+        return DLC_STATUS_EXECUTION_FAILED;
+    }
+    cudaDriverEntryPointQueryResult q1, q2;
+    void *f1 = nullptr, *f2 = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f1, 12000, cudaEnableDefault,
+                                         &q1) != cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess ||
+        cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &f2, 12000, cudaEnableDefault,
+                                         &q2) != cudaSuccess ||
+        q2 != cudaDriverEntryPointSuccess) {
+        cudaFreeHost(h->h_err);
+        delete h;
+        return DLC_STATUS_EXECUTION_FAILED;
+    }
+    h->encode_tiled = reinterpret_cast<EncodeTiledFn>(f1);
+    h->encode_im2col = reinterpret_cast<EncodeIm2colFn>(f2);
+    const char *tmo = std::getenv("DLC_WAIT_TIMEOUT_US");
+    if (tmo) {
+        long long us = std::atoll(tmo);
+        if (us >= 1 && us <= 60000000LL) h->timeout_ns = (unsigned long long)us * 1000ull;
+    }
+    *handle = h;
+    return DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlcDestroy(dlcHandle_t h) {
+    if (!h) return DLC_STATUS_NOT_INITIALIZED;
+    if (h->h_err) cudaFreeHost(h->h_err);
+    delete h;
+    return DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlcSetStream(dlcHandle_t h, void *stream) {
+    if (!h) return DLC_STATUS_NOT_INITIALIZED;
+    h->stream = static_cast<cudaStream_t>(stream);
+    return DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlcGetStream(dlcHandle_t h, void **stream) {
+    if (!h) return DLC_STATUS_NOT_INITIALIZED;
+    if (!stream) return DLC_STATUS_BAD_PARAM;
+    *stream = h->stream;
+    return DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlcGetLastDeviceError(dlcHandle_t h, int *code, int *detail) {
+    if (!h) return DLC_STATUS_NOT_INITIALIZED;
+    if (!code || !detail) return DLC_STATUS_BAD_PARAM;
+    if (cudaStreamSynchronize(h->stream) != cudaSuccess) return DLC_STATUS_EXECUTION_FAILED;
+    volatile int *e = h->h_err;
+    *code = e[0];
+    *detail = e[1];
+    e[0] = 0;
+    e[1] = 0;
+    return DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlcSynchronize(dlcHandle_t h) {
+    int code = 0, detail = 0;
+    dlcStatus_t st = dlcGetLastDeviceError(h, &code, &detail);
+    if (st != DLC_STATUS_SUCCESS) return st;
+    return code ? DLC_STATUS_EXECUTION_FAILED : DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlcGetLaunchCount(dlcHandle_t h, uint64_t *count) {
+    if (!h) return DLC_STATUS_NOT_INITIALIZED;
+    if (!count) return DLC_STATUS_BAD_PARAM;
+    *count = h->launches;
+    return DLC_STATUS_SUCCESS;
+}
+
+// ---- tensor descriptors ----------------------------------------------------
+dlcStatus_t dlcCreateTensorDescriptor(dlcTensorDescriptor_t *d) {
+    if (!d) return DLC_STATUS_BAD_PARAM;
+    *d = new (std::nothrow) dlcTensorStruct();
+    return *d ? DLC_STATUS_SUCCESS : DLC_STATUS_ALLOC_FAILED;
+}
+
+dlcStatus_t dlcDestroyTensorDescriptor(dlcTensorDescriptor_t d) {
+    delete d;
+    return DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlcSetTensor4dDescriptorEx(dlcTensorDescriptor_t d, dlcDataType_t dtype, int n, int c,
+                                       int h, int w, int64_t ns, int64_t cs, int64_t hs,
+                                       int64_t ws) {
+    if (!d) return DLC_STATUS_BAD_PARAM;
+    if (!valid_dtype(dtype) || n < 1 || c < 1 || h < 1 || w < 1) return DLC_STATUS_BAD_PARAM;
+    if (ns < 0 || cs < 0 || hs < 0 || ws < 0) return DLC_STATUS_BAD_PARAM;
+    const int64_t lim = (int64_t)1 << 40;
+    if (ns > lim || cs > lim || hs > lim || ws > lim) return DLC_STATUS_BAD_PARAM;
+    d->dtype = dtype;
+    d->n = n; d->c = c; d->h = h; d->w = w;
+    d->stride[0] = ns; d->stride[1] = cs; d->stride[2] = hs; d->stride[3] = ws;
+    d->set = 1;
+    return DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlcSetTensor4dDescriptor(dlcTensorDescriptor_t d, dlcTensorFormat_t f,
+                                     dlcDataType_t dtype, int n, int c, int h, int w) {
+    if (!d) return DLC_STATUS_BAD_PARAM;
+    if (!valid_format(f) || n < 1 || c < 1 || h < 1 || w < 1) return DLC_STATUS_BAD_PARAM;
+    const int64_t C = c, H = h, W = w;
+    if (f == DLC_TENSOR_NCHW)
+        return dlcSetTensor4dDescriptorEx(d, dtype, n, c, h, w, C * H * W, H * W, W, 1);
+    return dlcSetTensor4dDescriptorEx(d, dtype, n, c, h, w, H * W * C, 1, W * C, C);
+}
+
+dlcStatus_t dlcGetTensor4dDescriptor(dlcTensorDescriptor_t d, dlcDataType_t *dtype, int *n,
+                                     int *c, int *h, int *w, int64_t *ns, int64_t *cs,
+                                     int64_t *hs, int64_t *ws) {
+    if (!d) return DLC_STATUS_BAD_PARAM;
+    if (!d->set) return DLC_STATUS_NOT_INITIALIZED;
+    if (dtype) *dtype = d->dtype;
+    if (n) *n = d->n;
+    if (c) *c = d->c;
+    if (h) *h = d->h;
+    if (w) *w = d->w;
+    if (ns) *ns = d->stride[0];
+    if (cs) *cs = d->stride[1];
+    if (hs) *hs = d->stride[2];
+    if (ws) *ws = d->stride[3];
+    return DLC_STATUS_SUCCESS;
+}
+
+// ---- filter descriptors ------------------------------------------------------
+dlcStatus_t dlcCreateFilterDescriptor(dlcFilterDescriptor_t *d) {
+    if (!d) return DLC_STATUS_BAD_PARAM;
+    *d = new (std::nothrow) dlcFilterStruct();
+    return *d ? DLC_STATUS_SUCCESS : DLC_STATUS_ALLOC_FAILED;
+}
+
+dlcStatus_t dlcDestroyFilterDescriptor(dlcFilterDescriptor_t d) {
+    delete d;
+    return DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlcSetFilter4dDescriptor(dlcFilterDescriptor_t d, dlcDataType_t dtype,
+                                     dlcTensorFormat_t f, int k, int c, int r, int s) {
+    if (!d) return DLC_STATUS_BAD_PARAM;
+    if (!valid_dtype(dtype) || !valid_format(f) || k < 1 || c < 1 || r < 1 || s < 1)
+        return DLC_STATUS_BAD_PARAM;
+    if ((int64_t)k * c * r * s >= ((int64_t)1 << 40)) return DLC_STATUS_BAD_PARAM;
+    d->dtype = dtype;
+    d->format = f;
+    d->k = k; d->c = c; d->r = r; d->s = s;
+    d->set = 1;
+    return DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlcGetFilter4dDescriptor(dlcFilterDescriptor_t d, dlcDataType_t *dtype,
+                                     dlcTensorFormat_t *f, int *k, int *c, int *r, int *s) {
+    if (!d) return DLC_STATUS_BAD_PARAM;
+    if (!d->set) return DLC_STATUS_NOT_INITIALIZED;
+    if (dtype) *dtype = d->dtype;
+    if (f) *f = d->format;
+    if (k) *k = d->k;
+    if (c) *c = d->c;
+    if (r) *r = d->r;
+    if (s) *s = d->s;
+    return DLC_STATUS_SUCCESS;
+}
+
+// ---- convolution descriptors ---------------------------------------------------
+dlcStatus_t dlcCreateConvolutionDescriptor(dlcConvolutionDescriptor_t *d) {
+    if (!d) return DLC_STATUS_BAD_PARAM;
+    *d = new (std::nothrow) dlcConvolutionStruct();
+    return *d ? DLC_STATUS_SUCCESS : DLC_STATUS_ALLOC_FAILED;
+}
+
+dlcStatus_t dlcDestroyConvolutionDescriptor(dlcConvolutionDescriptor_t d) {
+    delete d;
+    return DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlcSetConvolution2dDescriptor(dlcConvolutionDescriptor_t d, int pad_h, int pad_w,
+                                          int u, int v, int dil_h, int dil_w, dlcMathType_t math) {
+    if (!d) return DLC_STATUS_BAD_PARAM;
+    if (pad_h < 0 || pad_w < 0 || u < 1 || v < 1 || dil_h < 1 || dil_w < 1)
+        return DLC_STATUS_BAD_PARAM;
+    if (math != DLC_MATH_FP32 && math != DLC_MATH_TF32 && math != DLC_MATH_BF16)
+        return DLC_STATUS_BAD_PARAM;
+    const int big = 1 << 20;
+    if (pad_h > big || pad_w > big || u > big || v > big || dil_h > big || dil_w > big)
+        return DLC_STATUS_BAD_PARAM;
+    d->pad_top = d->pad_bottom = pad_h;
+    d->pad_left = d->pad_right = pad_w;
+    d->u = u; d->v = v; d->dil_h = dil_h; d->dil_w = dil_w;
+    d->math = math;
+    d->set = 1;
+    return DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlcSetConvolution2dPadding(dlcConvolutionDescriptor_t d, int pt, int pb, int pl,
+                                       int pr) {
+    if (!d) return DLC_STATUS_BAD_PARAM;
+    if (!d->set) return DLC_STATUS_NOT_INITIALIZED;
+    const int big = 1 << 20;
+    if (pt < 0 || pb < 0 || pl < 0 || pr < 0 || pt > big || pb > big || pl > big || pr > big)
+        return DLC_STATUS_BAD_PARAM;
+    d->pad_top = pt; d->pad_bottom = pb; d->pad_left = pl; d->pad_right = pr;
+    return DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlcGetConvolution2dDescriptor(dlcConvolutionDescriptor_t d, int *pt, int *pb, int *pl,
+                                          int *pr, int *u, int *v, int *dh, int *dw,
+                                          dlcMathType_t *math) {
+    if (!d) return DLC_STATUS_BAD_PARAM;
+    if (!d->set) return DLC_STATUS_NOT_INITIALIZED;
+    if (pt) *pt = d->pad_top;
+    if (pb) *pb = d->pad_bottom;
+    if (pl) *pl = d->pad_left;
+    if (pr) *pr = d->pad_right;
+    if (u) *u = d->u;
+    if (v) *v = d->v;
+    if (dh) *dh = d->dil_h;
+    if (dw) *dw = d->dil_w;
+    if (math) *math = d->math;
+    return DLC_STATUS_SUCCESS;
+}
+
+// ---- forward ------------------------------------------------------------------
+dlcStatus_t dlcGetConvolution2dForwardOutputDim(dlcConvolutionDescriptor_t cd,
+                                                dlcTensorDescriptor_t xd, dlcFilterDescriptor_t wd,
+                                                int *n, int *k, int *p, int *q) {
+    if (!cd || !xd || !wd || !n || !k || !p || !q) return DLC_STATUS_BAD_PARAM;
+    if (!cd->set || !xd->set || !wd->set) return DLC_STATUS_NOT_INITIALIZED;
+    if (xd->c != wd->c) return DLC_STATUS_BAD_PARAM;
+    int64_t P = out_extent(xd->h, cd->pad_top, cd->pad_bottom, wd->r, cd->dil_h, cd->u);
+    int64_t Q = out_extent(xd->w, cd->pad_left, cd->pad_right, wd->s, cd->dil_w, cd->v);
+    if (P < 1 || Q < 1 || P > INT32_MAX || Q > INT32_MAX) return DLC_STATUS_BAD_PARAM;
+    *n = xd->n;
+    *k = wd->k;
+    *p = (int)P;
+    *q = (int)Q;
+    return DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlcGetConvolutionForwardWorkspaceSize(dlcHandle_t h, dlcTensorDescriptor_t xd,
+                                                  dlcFilterDescriptor_t wd,
+                                                  dlcConvolutionDescriptor_t cd,
+                                                  dlcTensorDescriptor_t yd, size_t *bytes) {
+    if (!h) return DLC_STATUS_NOT_INITIALIZED;
+    if (!bytes) return DLC_STATUS_BAD_PARAM;
+    ConvProblem pb;
+    dlcStatus_t st = resolve(xd, nullptr, wd, nullptr, cd, yd, nullptr, false, pb);
+    if (st != DLC_STATUS_SUCCESS) return st;
+    *bytes = 0;
+    return DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlcGetConvolutionForwardKernel(dlcHandle_t h, dlcTensorDescriptor_t xd, const void *x,
+                                           dlcFilterDescriptor_t wd, const void *w,
+                                           dlcConvolutionDescriptor_t cd, dlcTensorDescriptor_t yd,
+                                           const void *y, dlcKernel_t *kernel) {
+    if (!h) return DLC_STATUS_NOT_INITIALIZED;
+    if (!kernel) return DLC_STATUS_BAD_PARAM;
+    ConvProblem pb;
+    dlcStatus_t st = resolve(xd, x, wd, w, cd, yd, const_cast<void *>(y), false, pb);
+    if (st != DLC_STATUS_SUCCESS) return st;
+    *kernel = pick_kernel(h, pb);
+    return *kernel == DLC_KERNEL_NONE ? DLC_STATUS_NOT_SUPPORTED : DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlcConvolutionForward(dlcHandle_t h, const float *alpha, dlcTensorDescriptor_t xd,
+                                  const void *x, dlcFilterDescriptor_t wd, const void *w,
+                                  dlcConvolutionDescriptor_t cd, const float *beta,
+                                  dlcTensorDescriptor_t yd, void *y) {
+    return forward(h, alpha, xd, x, wd, w, cd, beta, nullptr, 0, yd, y);
+}
+
+dlcStatus_t dlcConvolutionBiasActivationForward(dlcHandle_t h, const float *alpha,
+                                                dlcTensorDescriptor_t xd, const void *x,
+                                                dlcFilterDescriptor_t wd, const void *w,
+                                                dlcConvolutionDescriptor_t cd, const float *beta,
+                                                const float *bias, dlcActivationMode_t act,
+                                                dlcTensorDescriptor_t yd, void *y) {
+    if (act != DLC_ACTIVATION_IDENTITY && act != DLC_ACTIVATION_RELU) return DLC_STATUS_BAD_PARAM;
+    return forward(h, alpha, xd, x, wd, w, cd, beta, bias, act == DLC_ACTIVATION_RELU, yd, y);
+}
+
+dlcStatus_t dlcDebugWaitTimeoutSelfTest(dlcHandle_t h, int timeout_us) {
+    if (!h) return DLC_STATUS_NOT_INITIALIZED;
+    if (timeout_us < 1 || timeout_us > 1000000) return DLC_STATUS_BAD_PARAM;
+    return dlc_launch_wait_selftest(h, (unsigned long long)timeout_us * 1000ull);
+}
+
+}  // extern "C"

@@ -1,0 +1,77 @@
+// internal.h -- host-side structures shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dlc.h"
+
+struct dlcTensorStruct {
+    int set = 0;
+    dlcDataType_t dtype = DLC_DATA_FLOAT;
+    int n = 0, c = 0, h = 0, w = 0;
+    int64_t stride[4] = {0, 0, 0, 0};  // n, c, h, w (elements)
+};
+
+struct dlcFilterStruct {
+    int set = 0;
+    dlcDataType_t dtype = DLC_DATA_FLOAT;
+    dlcTensorFormat_t format = DLC_TENSOR_NCHW;
+    int k = 0, c = 0, r = 0, s = 0;
+};
+
+struct dlcConvolutionStruct {
+    int set = 0;
+    int pad_top = 0, pad_bottom = 0, pad_left = 0, pad_right = 0;
+    int u = 1, v = 1, dil_h = 1, dil_w = 1;
+    dlcMathType_t math = DLC_MATH_FP32;
+};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+typedef CUresult (*EncodeIm2colFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const int *,
+                                   const int *, cuuint32_t, cuuint32_t, const cuuint32_t *,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct dlcContext {
+    int device = 0;
+    int sm_count = 0;
+    cudaStream_t stream = nullptr;
+    int *h_err = nullptr;   // mapped host words: [0] code, [1] detail
+    int *d_err = nullptr;   // device alias of h_err
+    uint64_t launches = 0;
+    unsigned long long timeout_ns = 2000000000ull;  // pipeline wait limit
+    EncodeTiledFn encode_tiled = nullptr;
+    EncodeIm2colFn encode_im2col = nullptr;
+};
+
+// A fully resolved forward problem (validated by the API layer).
+struct ConvProblem {
+    int N, C, H, W, K, R, S, P, Q;
+    int pt, pb, pl, pr, u, v, dh, dw;
+    dlcMathType_t math;
+    dlcDataType_t xdt;   // storage of x and w
+    dlcDataType_t ydt;   // storage of y
+    dlcTensorFormat_t wfmt;
+    const void *x;
+    int64_t xs[4];       // n, c, h, w
+    const void *w;
+    int64_t ws[4];       // k, c, r, s
+    void *y;
+    int64_t ys[4];       // n, k, p, q
+    const float *bias;
+    float alpha, beta;
+    int relu;
+};
+
+// Kernel launchers (conv_ffma.cu, conv_tc.cu).  They return SUCCESS or an
+// error status and count launches in ctx->launches.
+dlcStatus_t dlc_launch_ffma(dlcContext *ctx, const ConvProblem &pb);
+dlcKernel_t dlc_tc_variant(const dlcContext *ctx, const ConvProblem &pb);
+dlcStatus_t dlc_launch_tc(dlcContext *ctx, const ConvProblem &pb, dlcKernel_t variant);
+dlcStatus_t dlc_launch_wait_selftest(dlcContext *ctx, unsigned long long timeout_ns);

@@ -1,0 +1,267 @@
+/*
+ * dlc.h -- C ABI of the GB300 (sm_103a) 2-D convolution forward library.
+ *
+ * The library computes the forward (FPROP) convolution layer
+ *
+ *   y[n,k,p,q] = act( alpha * sum_{c,r,s} x[n, c, p*u + r*dh - pad_top, q*v + s*dw - pad_left]
+ *                                         * w[k,c,r,s]
+ *                     + beta * y[n,k,p,q] + bias[k] )
+ *
+ * (cross-correlation; x reads as zero outside the image; act is identity or
+ * ReLU), with P = floor((H + pad_top + pad_bottom - dh*(R-1) - 1) / u) + 1 and
+ * Q likewise along W.
+ *
+ * Sources on the pages:
+ *  - "cuDNN: Efficient Primitives for Deep Learning", method section: a C
+ *    language API whose tensors and filters are opaque descriptors with
+ *    arbitrary strides and layouts; the caller owns every device buffer and no
+ *    auxiliary buffer is used; non-square inputs and asymmetric padding are
+ *    supported (findings section).
+ *  - "maxDNN: An Efficient Convolution Kernel for Deep Learning with Maxwell
+ *    GPUs", method section: each output coordinate is the product of the input
+ *    receptive field with the filter weights; efficiency counts only the
+ *    direct-convolution FLOPs 2*N*K*P*Q*C*R*S.
+ *  - "High-Performance Deep Learning via a Single Building Block", method
+ *    section: the kernel is a batch-reduce GEMM, C += sum_i A_i * B_i, here
+ *    with i running over the filter taps (r,s) and channel blocks.
+ *  - "High Performance Zero-Memory Overhead Direct Convolutions", abstract and
+ *    method section: no packing and no extra memory -- the workspace size is
+ *    always 0.
+ *
+ * Conventions (all functions):
+ *  - Every function returns a dlcStatus_t.  Pointers to descriptors and
+ *    handles are host pointers; x, w, y and bias are device pointers owned by
+ *    the caller; alpha and beta are host pointers to float.
+ *  - Sizes and strides are in elements, not bytes.
+ *  - Calls that launch work are asynchronous on the handle's stream.  Launch
+ *    errors are reported by the call itself.  Errors that kernels detect on
+ *    the device (a pipeline wait that ran out of time) are recorded in the
+ *    handle and reported as DLC_STATUS_EXECUTION_FAILED by the next launching
+ *    call on that handle and by dlcSynchronize(), which clears them.
+ *  - The library allocates no device memory on the forward path.  dlcCreate
+ *    allocates one small mapped host word for device error reports.
+ *  - A handle is not thread-safe; use one handle per host thread.
+ */
+#ifndef DLC_H_
+#define DLC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DLC_VERSION 100
+
+typedef enum {
+    DLC_STATUS_SUCCESS = 0,
+    DLC_STATUS_NOT_INITIALIZED = 1,   /* handle or descriptor not created/set */
+    DLC_STATUS_BAD_PARAM = 2,         /* shape, stride, pointer or size error */
+    DLC_STATUS_NOT_SUPPORTED = 3,     /* valid request this library does not offer */
+    DLC_STATUS_EXECUTION_FAILED = 4,  /* launch failed or a kernel reported an error */
+    DLC_STATUS_INTERNAL_ERROR = 5,
+    DLC_STATUS_ALLOC_FAILED = 6       /* host allocation failed */
+} dlcStatus_t;
+
+/* Storage type of x, w and y.  x and w must share it; y may be FLOAT or
+ * BFLOAT16 independently.  Bias is always FLOAT. */
+typedef enum {
+    DLC_DATA_FLOAT = 0,
+    DLC_DATA_BFLOAT16 = 1
+} dlcDataType_t;
+
+/* Layouts.  For activations NCHW / NHWC; for filters NCHW means KCRS and NHWC
+ * means KRSC. */
+typedef enum {
+    DLC_TENSOR_NCHW = 0,
+    DLC_TENSOR_NHWC = 1
+} dlcTensorFormat_t;
+
+/* Arithmetic.  FP32: FP32 products and sums on CUDA cores (FFMA), any storage
+ * type.  TF32: tensor cores, FLOAT storage read as TF32, FP32 accumulation.
+ * BF16: tensor cores, BFLOAT16 storage, FP32 accumulation. */
+typedef enum {
+    DLC_MATH_FP32 = 0,
+    DLC_MATH_TF32 = 1,
+    DLC_MATH_BF16 = 2
+} dlcMathType_t;
+
+typedef enum {
+    DLC_ACTIVATION_IDENTITY = 0,
+    DLC_ACTIVATION_RELU = 1
+} dlcActivationMode_t;
+
+/* Which kernel a forward call launches (diagnostic). */
+typedef enum {
+    DLC_KERNEL_NONE = 0,
+    DLC_KERNEL_FFMA = 1,          /* strict FP32 direct convolution, CUDA cores */
+    DLC_KERNEL_TC_IM2COL = 2,     /* tcgen05 implicit GEMM, TMA im2col activations */
+    DLC_KERNEL_TC_GATHER = 3      /* tcgen05 implicit GEMM, gathered activations */
+} dlcKernel_t;
+
+/* Device error codes recorded by kernels (dlcGetLastDeviceError). */
+typedef enum {
+    DLC_DEVERR_NONE = 0,
+    DLC_DEVERR_WAIT_TIMEOUT = 1   /* a pipeline barrier wait ran out of time */
+} dlcDeviceError_t;
+
+typedef struct dlcContext *dlcHandle_t;
+typedef struct dlcTensorStruct *dlcTensorDescriptor_t;
+typedef struct dlcFilterStruct *dlcFilterDescriptor_t;
+typedef struct dlcConvolutionStruct *dlcConvolutionDescriptor_t;
+
+/* ---- library ------------------------------------------------------------ */
+
+/* Human-readable name of a status code; never NULL. */
+const char *dlcGetErrorString(dlcStatus_t status);
+
+/* DLC_VERSION of the loaded library, written to *version. */
+dlcStatus_t dlcGetVersion(int *version);
+
+/* ---- handle ------------------------------------------------------------- */
+
+/* Creates a handle bound to the current CUDA device and the legacy default
+ * stream.  Allocates the host-side context and one mapped host word for
+ * device error reports.  BAD_PARAM if handle is NULL, NOT_SUPPORTED if the
+ * device is not compute capability 10.3, EXECUTION_FAILED on a CUDA error. */
+dlcStatus_t dlcCreate(dlcHandle_t *handle);
+
+/* Frees the handle (does not synchronize; the caller must ensure no launched
+ * work is still pending). */
+dlcStatus_t dlcDestroy(dlcHandle_t handle);
+
+/* Sets the stream (a cudaStream_t passed as void*; NULL = legacy default
+ * stream) on which later calls launch. */
+dlcStatus_t dlcSetStream(dlcHandle_t handle, void *stream);
+dlcStatus_t dlcGetStream(dlcHandle_t handle, void **stream);
+
+/* Synchronizes the handle's stream.  Returns EXECUTION_FAILED if a kernel
+ * recorded a device error since the last call (the error is then cleared). */
+dlcStatus_t dlcSynchronize(dlcHandle_t handle);
+
+/* Synchronizes, then writes the last recorded device error code
+ * (dlcDeviceError_t) and its detail word (which wait gave up) and clears
+ * them. */
+dlcStatus_t dlcGetLastDeviceError(dlcHandle_t handle, int *code, int *detail);
+
+/* Number of kernels this handle has launched since creation. */
+dlcStatus_t dlcGetLaunchCount(dlcHandle_t handle, uint64_t *count);
+
+/* ---- tensor descriptors (x and y) ---------------------------------------- */
+
+dlcStatus_t dlcCreateTensorDescriptor(dlcTensorDescriptor_t *desc);
+dlcStatus_t dlcDestroyTensorDescriptor(dlcTensorDescriptor_t desc);
+
+/* Dense 4-D tensor in NCHW or NHWC order.  All sizes must be >= 1 and the
+ * element count must fit in 63 bits. */
+dlcStatus_t dlcSetTensor4dDescriptor(dlcTensorDescriptor_t desc, dlcTensorFormat_t format,
+                                     dlcDataType_t dtype, int n, int c, int h, int w);
+
+/* 4-D tensor with arbitrary non-negative strides (elements) for the logical
+ * axes n, c, h, w: any layout, including sub-tensor views. */
+dlcStatus_t dlcSetTensor4dDescriptorEx(dlcTensorDescriptor_t desc, dlcDataType_t dtype,
+                                       int n, int c, int h, int w,
+                                       int64_t nStride, int64_t cStride,
+                                       int64_t hStride, int64_t wStride);
+
+dlcStatus_t dlcGetTensor4dDescriptor(dlcTensorDescriptor_t desc, dlcDataType_t *dtype,
+                                     int *n, int *c, int *h, int *w,
+                                     int64_t *nStride, int64_t *cStride,
+                                     int64_t *hStride, int64_t *wStride);
+
+/* ---- filter descriptors (w) ---------------------------------------------- */
+
+dlcStatus_t dlcCreateFilterDescriptor(dlcFilterDescriptor_t *desc);
+dlcStatus_t dlcDestroyFilterDescriptor(dlcFilterDescriptor_t desc);
+
+/* Dense K x C x R x S filter bank; format NCHW = KCRS, NHWC = KRSC. */
+dlcStatus_t dlcSetFilter4dDescriptor(dlcFilterDescriptor_t desc, dlcDataType_t dtype,
+                                     dlcTensorFormat_t format, int k, int c, int r, int s);
+
+dlcStatus_t dlcGetFilter4dDescriptor(dlcFilterDescriptor_t desc, dlcDataType_t *dtype,
+                                     dlcTensorFormat_t *format, int *k, int *c, int *r, int *s);
+
+/* ---- convolution descriptors --------------------------------------------- */
+
+dlcStatus_t dlcCreateConvolutionDescriptor(dlcConvolutionDescriptor_t *desc);
+dlcStatus_t dlcDestroyConvolutionDescriptor(dlcConvolutionDescriptor_t desc);
+
+/* Symmetric padding pad_h (top and bottom) and pad_w (left and right),
+ * strides u (vertical) and v (horizontal), dilations, arithmetic.  Pads >= 0,
+ * strides and dilations >= 1. */
+dlcStatus_t dlcSetConvolution2dDescriptor(dlcConvolutionDescriptor_t desc, int pad_h, int pad_w,
+                                          int u, int v, int dilation_h, int dilation_w,
+                                          dlcMathType_t math);
+
+/* Asymmetric padding (replaces the symmetric pads). */
+dlcStatus_t dlcSetConvolution2dPadding(dlcConvolutionDescriptor_t desc, int pad_top,
+                                       int pad_bottom, int pad_left, int pad_right);
+
+dlcStatus_t dlcGetConvolution2dDescriptor(dlcConvolutionDescriptor_t desc, int *pad_top,
+                                          int *pad_bottom, int *pad_left, int *pad_right,
+                                          int *u, int *v, int *dilation_h, int *dilation_w,
+                                          dlcMathType_t *math);
+
+/* ---- forward convolution ------------------------------------------------- */
+
+/* Output dimensions N, K, P, Q.  BAD_PARAM if C differs between x and w or
+ * if the dilated filter does not fit the padded input (P or Q < 1). */
+dlcStatus_t dlcGetConvolution2dForwardOutputDim(dlcConvolutionDescriptor_t conv,
+                                                dlcTensorDescriptor_t xDesc,
+                                                dlcFilterDescriptor_t wDesc,
+                                                int *n, int *k, int *p, int *q);
+
+/* Workspace needed by dlcConvolutionForward: always 0 bytes (zero memory
+ * overhead).  Validates the problem like the forward call. */
+dlcStatus_t dlcGetConvolutionForwardWorkspaceSize(dlcHandle_t handle,
+                                                  dlcTensorDescriptor_t xDesc,
+                                                  dlcFilterDescriptor_t wDesc,
+                                                  dlcConvolutionDescriptor_t conv,
+                                                  dlcTensorDescriptor_t yDesc, size_t *bytes);
+
+/* Kernel a forward call with these descriptors and pointers would launch;
+ * x, w and y may be NULL (alignment is then taken as satisfied). */
+dlcStatus_t dlcGetConvolutionForwardKernel(dlcHandle_t handle,
+                                           dlcTensorDescriptor_t xDesc, const void *x,
+                                           dlcFilterDescriptor_t wDesc, const void *w,
+                                           dlcConvolutionDescriptor_t conv,
+                                           dlcTensorDescriptor_t yDesc, const void *y,
+                                           dlcKernel_t *kernel);
+
+/* y = alpha * conv(x, w) + beta * y.
+ * x: device, xDesc layout; w: device, wDesc layout; y: device, yDesc layout
+ * with dims (N, K, P, Q) and strides that map distinct elements to distinct
+ * addresses.  beta == 0 means y is not read (NaN in y is overwritten).
+ * y must not overlap x or w (BAD_PARAM).  x and w must share a storage type
+ * that matches the math mode: FP32 math takes FLOAT or BFLOAT16, TF32 math
+ * takes FLOAT, BF16 math takes BFLOAT16 (else NOT_SUPPORTED). */
+dlcStatus_t dlcConvolutionForward(dlcHandle_t handle, const float *alpha,
+                                  dlcTensorDescriptor_t xDesc, const void *x,
+                                  dlcFilterDescriptor_t wDesc, const void *w,
+                                  dlcConvolutionDescriptor_t conv, const float *beta,
+                                  dlcTensorDescriptor_t yDesc, void *y);
+
+/* y = act(alpha * conv(x, w) + beta * y + bias[k]); bias is a device array of
+ * K floats or NULL (no bias).  Otherwise as dlcConvolutionForward. */
+dlcStatus_t dlcConvolutionBiasActivationForward(dlcHandle_t handle, const float *alpha,
+                                                dlcTensorDescriptor_t xDesc, const void *x,
+                                                dlcFilterDescriptor_t wDesc, const void *w,
+                                                dlcConvolutionDescriptor_t conv,
+                                                const float *beta, const float *bias,
+                                                dlcActivationMode_t activation,
+                                                dlcTensorDescriptor_t yDesc, void *y);
+
+/* ---- self test of the device error path ---------------------------------- */
+
+/* Launches one block whose pipeline wait is on a barrier nothing completes,
+ * with a limit of timeout_us microseconds (1..1000000).  The kernel records
+ * DLC_DEVERR_WAIT_TIMEOUT and returns; no GPU fault is involved.  Used by the
+ * tests of the error path. */
+dlcStatus_t dlcDebugWaitTimeoutSelfTest(dlcHandle_t handle, int timeout_us);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DLC_H_ */

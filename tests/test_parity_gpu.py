@@ -1,0 +1,255 @@
+"""GPU parity of the C-ABI forward convolution against the CPU oracle.
+
+Small problems are checked element by element (several 128-row tiles, ragged
+M and K tails); the full workloads are checked on sampled outputs (65536
+random plus all border rows and columns of two images x eight filters) in the
+launch configuration the benchmark times.  Guard bands around y catch writes
+outside the output; y starts as NaN when beta == 0 so unwritten outputs fail.
+"""
+import numpy as np
+import pytest
+
+from deep_learning_convolution_gb300 import synth
+from gpu_util import run_and_check
+
+pytestmark = pytest.mark.gpu
+
+L = synth.Layer
+
+
+def P(*a):
+    return dict(pad_top=a[0], pad_bottom=a[1], pad_left=a[2], pad_right=a[3])
+
+
+@pytest.fixture(scope="module")
+def handle():
+    import torch
+    from deep_learning_convolution_gb300 import api
+    from deep_learning_convolution_gb300 import build as dlc_build
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need CUDA")
+    dlc_build.build()
+    h = api.Handle()
+    yield h
+    h.close()
+
+
+# ---------------------------------------------------------------------------
+# strict FP32 (FFMA)
+# ---------------------------------------------------------------------------
+
+def test_tiny_fp32_config_full(handle):
+    layer = synth.WORKLOADS["tiny"][0]
+    assert run_and_check(handle, layer, synth.workload_seed("tiny", 0), full=True,
+                         expect_kernel="ffma") == "ffma"
+
+
+def test_fp32_math_on_bf16_storage_nhwc(handle):
+    layer = L("ffma_bf16", 2, 6, 9, 11, 5, 3, 2, **P(1, 0, 2, 1), u=2, dil_w=2, dtype="bf16",
+              layout="NHWC")
+    # FP32 math requested explicitly through a BF16 layer: use the API directly
+    import torch
+    from deep_learning_convolution_gb300 import api
+    x, w, _ = synth.make_inputs(layer, 5)
+    xt, wt = api.layer_tensors(layer, x, w, "cuda")
+    n, k, p, q = api.output_dim(xt, wt, x_axes="NHWC", w_axes="KRSC", pads=(1, 0, 2, 1),
+                                stride=(2, 1), dilation=(1, 2))
+    y = torch.full((n, k, p, q), float("nan"), device="cuda")
+    conv = api.Conv2dForward(handle, xt, wt, y, x_axes="NHWC", w_axes="KRSC", y_axes="NCHW",
+                             pads=(1, 0, 2, 1), stride=(2, 1), dilation=(1, 2), math="fp32")
+    assert conv.kernel(xt, wt, y) == "ffma"
+    conv(xt, wt, y)
+    torch.cuda.synchronize()
+    from oracle import oracle
+    ref, bound = oracle.conv2d_fprop(x.astype(np.float64), w.astype(np.float64),
+                                     pads=(1, 0, 2, 1), stride=(2, 1), dilation=(1, 2))
+    assert (np.abs(y.double().cpu().numpy() - ref) <= 1e-5 * bound + 1e-6).all()
+
+
+# ---------------------------------------------------------------------------
+# tensor cores, TMA im2col producer
+# ---------------------------------------------------------------------------
+
+IM2COL_CASES = [
+    L("bf16_c64_k96_3x3", 2, 64, 17, 17, 96, 3, 3, **P(1, 1, 1, 1)),
+    L("bf16_c96_k256_5x5", 2, 96, 14, 14, 256, 5, 5),
+    L("bf16_c64_k40_asym_dil_stride", 3, 64, 19, 23, 40, 3, 2, **P(2, 0, 1, 3), u=2, v=1,
+      dil_h=2, dil_w=2),
+    L("bf16_c128_k384_1x1", 2, 128, 9, 13, 384, 1, 1),
+    L("bf16_c64_k64_1x1_s2", 3, 64, 15, 15, 64, 1, 1, u=2, v=2),
+    L("bf16_c192_k130_3x3_s3", 2, 192, 16, 21, 130, 3, 3, **P(1, 1, 1, 1), u=3, v=3),
+    L("bf16_c64_k16_7x7_s2_p3", 2, 64, 23, 23, 16, 7, 7, **P(3, 3, 3, 3), u=2, v=2),
+    L("tf32_c32_k48_3x3_nhwc", 2, 32, 15, 15, 48, 3, 3, **P(1, 1, 1, 1), dtype="tf32"),
+    L("tf32_c64_k96_5x3_nhwc", 2, 64, 12, 10, 96, 5, 3, **P(2, 1, 0, 2), u=1, v=2, dtype="tf32"),
+]
+
+
+@pytest.mark.parametrize("layer", IM2COL_CASES, ids=lambda l: l.name)
+def test_tc_im2col_parity_full(handle, layer):
+    run_and_check(handle, layer, 1000 + IM2COL_CASES.index(layer), full=True,
+                  expect_kernel="tc_im2col")
+
+
+# ---------------------------------------------------------------------------
+# tensor cores, gather producer (NCHW, small C, KCRS filters with NHWC)
+# ---------------------------------------------------------------------------
+
+GATHER_CASES = [
+    L("bf16_c3_k64_11x11_s4_nhwc", 2, 3, 35, 35, 64, 11, 11, **P(2, 2, 2, 2), u=4, v=4),
+    L("bf16_c3_k96_11x11_s4_nopad", 2, 3, 39, 43, 96, 11, 11, u=4, v=4),
+    L("bf16_c16_k48_3x3_nchw", 2, 16, 14, 18, 48, 3, 3, **P(1, 1, 1, 1), layout="NCHW"),
+    L("tf32_c1_k32_21x11_speechlike", 2, 1, 50, 70, 32, 21, 11, **P(10, 10, 5, 5), u=2, v=2,
+      dtype="tf32", layout="NCHW"),
+    L("tf32_c8_k32_7x5_s2x1_nchw", 2, 8, 27, 40, 32, 7, 5, **P(3, 3, 2, 2), u=2, v=1,
+      dtype="tf32", layout="NCHW"),
+    L("bf16_c5_k100_3x3_dil", 2, 5, 13, 12, 100, 3, 3, **P(2, 2, 2, 2), dil_h=2, dil_w=2),
+]
+
+
+@pytest.mark.parametrize("layer", GATHER_CASES, ids=lambda l: l.name)
+def test_tc_gather_parity_full(handle, layer):
+    run_and_check(handle, layer, 2000 + GATHER_CASES.index(layer), full=True,
+                  expect_kernel="tc_gather")
+
+
+def test_kcrs_filters_with_nhwc_activations_use_gather(handle):
+    import torch
+    from deep_learning_convolution_gb300 import api
+    from oracle import oracle
+    layer = L("bf16_nhwc_kcrs", 2, 64, 11, 11, 48, 3, 3, **P(1, 1, 1, 1))
+    x, w, _ = synth.make_inputs(layer, 77)
+    xt, _ = api.layer_tensors(layer, x, w, "cuda")
+    wt = torch.from_numpy(synth.round_to_bf16_bits(w).view(np.int16).reshape(w.shape)).view(
+        torch.bfloat16).cuda()
+    y = torch.full((2, 11, 11, 48), float("nan"), device="cuda")
+    conv = api.Conv2dForward(handle, xt, wt, y, x_axes="NHWC", w_axes="KCRS", y_axes="NHWC",
+                             pads=(1, 1, 1, 1), math="bf16")
+    assert conv.kernel(xt, wt, y) == "tc_gather"
+    conv(xt, wt, y)
+    torch.cuda.synchronize()
+    ref, bound = oracle.conv2d_fprop(x.astype(np.float64), w.astype(np.float64), pads=(1, 1, 1, 1))
+    got = y.permute(0, 3, 1, 2).double().cpu().numpy()
+    assert (np.abs(got - ref) <= 1e-5 * bound + 1e-6).all()
+
+
+# ---------------------------------------------------------------------------
+# seeded sweep of small ragged shapes over both precisions and layouts
+# ---------------------------------------------------------------------------
+
+SWEEP = synth.random_small_layers(31, 24, dtypes=("bf16", "tf32"), layouts=("NHWC", "NCHW"))
+
+
+@pytest.mark.parametrize("layer", SWEEP, ids=lambda l: l.name)
+def test_random_sweep_parity(handle, layer):
+    run_and_check(handle, layer, 3000 + SWEEP.index(layer), full=True)
+
+
+# ---------------------------------------------------------------------------
+# epilogue: alpha, beta * y, bias, ReLU, BF16 output, other y layouts
+# ---------------------------------------------------------------------------
+
+EPI_LAYERS = [IM2COL_CASES[0], GATHER_CASES[2], GATHER_CASES[3]]
+
+
+@pytest.mark.parametrize("layer", EPI_LAYERS, ids=lambda l: l.name)
+@pytest.mark.parametrize("alpha,beta,bias,relu", [
+    (0.5, 0.0, True, True), (1.0, -0.75, False, False), (-2.0, 1.5, True, True)])
+def test_epilogue_parity(handle, layer, alpha, beta, bias, relu):
+    run_and_check(handle, layer, 4000, full=True, alpha=alpha, beta=beta, with_bias=bias,
+                  relu=relu)
+
+
+@pytest.mark.parametrize("y_axes", ["NCHW", "NHWC", "CNHW"])
+def test_output_layouts(handle, y_axes):
+    run_and_check(handle, IM2COL_CASES[2], 4100, full=True, y_axes=y_axes)
+
+
+def test_bf16_output(handle):
+    import torch
+    run_and_check(handle, IM2COL_CASES[0], 4200, full=True, y_dtype=torch.bfloat16, beta=0.5,
+                  with_bias=True)
+
+
+# ---------------------------------------------------------------------------
+# the benchmark workloads at full size, sampled
+# ---------------------------------------------------------------------------
+
+FULL = [(wl, j) for wl in ("alexnet", "overfeat", "resnet50", "speech")
+        for j in range(len(synth.WORKLOADS[wl]))]
+
+
+@pytest.mark.parametrize("wl,j", FULL, ids=lambda v: str(v))
+def test_full_workload_layer_sampled(handle, wl, j):
+    layer = synth.WORKLOADS[wl][j]
+    run_and_check(handle, layer, synth.workload_seed(wl, j), full=False)
+
+
+# ---------------------------------------------------------------------------
+# API behaviour on the device
+# ---------------------------------------------------------------------------
+
+def test_workspace_is_zero_and_kernel_choice(handle):
+    import torch
+    from deep_learning_convolution_gb300 import api
+    expect = {"alexnet": ["tc_gather"] + ["tc_im2col"] * 4,
+              "overfeat": ["tc_gather"] + ["tc_im2col"] * 4,
+              "speech": ["tc_gather", "tc_gather"], "tiny": ["ffma"]}
+    for wl, kinds in expect.items():
+        for layer, kind in zip(synth.WORKLOADS[wl], kinds):
+            x, w, _ = synth.make_inputs(layer, 1, batch=1)
+            xt, wt = api.layer_tensors(layer, x, w, "cuda")
+            conv, y = api.layer_problem(handle, layer, xt, wt)
+            assert conv.workspace_size() == 0
+            assert conv.kernel(xt, wt, y) == kind, layer.name
+            conv.close()
+
+
+def test_launch_count_and_in_place_rejected(handle):
+    import torch
+    from deep_learning_convolution_gb300 import api, binding as B
+    layer = IM2COL_CASES[0]
+    x, w, _ = synth.make_inputs(layer, 9)
+    xt, wt = api.layer_tensors(layer, x, w, "cuda")
+    conv, y = api.layer_problem(handle, layer, xt, wt)
+    before = handle.launches()
+    conv(xt, wt, y)
+    conv(xt, wt, y)
+    assert handle.launches() == before + 2
+    # y aliasing x is rejected
+    big = torch.zeros(max(xt.numel(), y.numel()) * 2, dtype=torch.float32, device="cuda")
+    with pytest.raises(B.DlcError) as e:
+        B.dlcConvolutionForward(handle.h, 1.0, conv.x_desc, big.data_ptr(), conv.w_desc,
+                                wt.data_ptr(), conv.conv, 0.0, conv.y_desc, big.data_ptr())
+    assert e.value.status == B.DLC_STATUS_BAD_PARAM
+    torch.cuda.synchronize()
+
+
+def test_math_dtype_mismatch_not_supported(handle):
+    import torch
+    from deep_learning_convolution_gb300 import api, binding as B
+    x = torch.zeros(1, 8, 8, 64, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(16, 3, 3, 64, dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros(1, 8, 8, 16, device="cuda")
+    conv = api.Conv2dForward(handle, x, w, y, x_axes="NHWC", w_axes="KRSC", y_axes="NHWC",
+                             pads=(1, 1, 1, 1), math="tf32")
+    with pytest.raises(B.DlcError) as e:
+        conv(x, w, y)
+    assert e.value.status == B.DLC_STATUS_NOT_SUPPORTED
+
+
+def test_device_wait_timeout_reports_error_and_recovers(handle):
+    """A pipeline wait on a barrier nothing completes runs out after 2 ms;
+    the kernel records the error (no fault) and the context stays usable."""
+    import torch
+    from deep_learning_convolution_gb300 import binding as B
+    B.dlcDebugWaitTimeoutSelfTest(handle.h, 2000)
+    code, detail = handle.last_device_error()
+    assert code == B.DLC_DEVERR_WAIT_TIMEOUT and detail == 99
+    # cleared; a pending error blocks launches until read
+    B.dlcDebugWaitTimeoutSelfTest(handle.h, 1000)
+    torch.cuda.synchronize()
+    with pytest.raises(B.DlcError) as e:
+        handle.synchronize()
+    assert e.value.status == B.DLC_STATUS_EXECUTION_FAILED
+    handle.synchronize()  # cleared now
+    run_and_check(handle, IM2COL_CASES[0], 5000, full=True)
