@@ -409,6 +409,36 @@ def run_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_profile_layer(args):
+    """Launches one layer of the workload `reps` times (for ncu captures); prints
+    the CUDA-event time per launch of a second batch of `reps` launches."""
+    import torch
+    from deep_learning_convolution_gb300 import api, synth
+    from deep_learning_convolution_gb300 import build as dlc_build
+    dlc_build.build()
+    j = args.profile_layer
+    layer = synth.WORKLOADS[args.workload][j]
+    x, w, _ = synth.make_inputs(layer, synth.workload_seed(args.workload, j), batch=args.batch)
+    handle = api.Handle()
+    xt, wt = api.layer_tensors(layer, x, w, "cuda")
+    conv, y = api.layer_problem(handle, layer, xt, wt)
+    for _ in range(args.reps):
+        conv(xt, wt, y)
+    torch.cuda.synchronize()
+    handle.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(args.reps):
+        conv(xt, wt, y)
+    end.record()
+    torch.cuda.synchronize()
+    handle.synchronize()
+    print(json.dumps({"layer": layer.name, "kernel": conv.kernel(xt, wt, y),
+                      "us_per_launch": round(start.elapsed_time(end) * 1e3 / args.reps, 2)}))
+    conv.close()
+    handle.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -420,7 +450,14 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-layer", type=int, default=None,
+                    help="launch only this layer of the workload 2*reps times (ncu captures)")
+    ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--batch", type=int, default=None, help="override N (profile mode)")
     args = ap.parse_args()
+    if args.profile_layer is not None:
+        run_profile_layer(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     rank, world, local_rank = env_rank()

@@ -206,6 +206,13 @@ dlcStatus_t dlcCreate(dlcHandle_t *handle) {
         delete h;
         return DLC_STATUS_EXECUTION_FAILED;
     }
+    if (cudaMalloc((void **)&h->sk_flags, DLC_SK_FLAGS * sizeof(int)) != cudaSuccess ||
+        cudaMemset(h->sk_flags, 0, DLC_SK_FLAGS * sizeof(int)) != cudaSuccess) {
+        if (h->sk_flags) cudaFree(h->sk_flags);
+        cudaFreeHost(h->h_err);
+        delete h;
+        return DLC_STATUS_EXECUTION_FAILED;
+    }
     cudaDriverEntryPointQueryResult q1, q2;
     void *f1 = nullptr, *f2 = nullptr;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f1, 12000, cudaEnableDefault,
@@ -214,6 +221,7 @@ dlcStatus_t dlcCreate(dlcHandle_t *handle) {
         cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &f2, 12000, cudaEnableDefault,
                                          &q2) != cudaSuccess ||
         q2 != cudaDriverEntryPointSuccess) {
+        cudaFree(h->sk_flags);
         cudaFreeHost(h->h_err);
         delete h;
         return DLC_STATUS_EXECUTION_FAILED;
@@ -232,6 +240,7 @@ dlcStatus_t dlcCreate(dlcHandle_t *handle) {
 dlcStatus_t dlcDestroy(dlcHandle_t h) {
     if (!h) return DLC_STATUS_NOT_INITIALIZED;
     if (h->h_err) cudaFreeHost(h->h_err);
+    if (h->sk_flags) cudaFree(h->sk_flags);
     delete h;
     return DLC_STATUS_SUCCESS;
 }
@@ -258,6 +267,9 @@ dlcStatus_t dlcGetLastDeviceError(dlcHandle_t h, int *code, int *detail) {
     *detail = e[1];
     e[0] = 0;
     e[1] = 0;
+    // a kernel that gave up may have left split-tile flags raised
+    if (*code != 0 && cudaMemset(h->sk_flags, 0, DLC_SK_FLAGS * sizeof(int)) != cudaSuccess)
+        return DLC_STATUS_EXECUTION_FAILED;
     return DLC_STATUS_SUCCESS;
 }
 

@@ -31,6 +31,7 @@
 // committed and waited for, tensor memory is released.
 #include <cuda_bf16.h>
 
+#include <cstdlib>
 #include <cstring>
 #include <type_traits>
 
@@ -46,6 +47,11 @@ constexpr int ROW_BYTES = 128;                 // one 128-byte swizzle row of th
 constexpr int A_STAGE_BYTES = BM * ROW_BYTES;  // 16 KiB
 constexpr int MAX_DYN_SMEM = 232448;           // 227 KiB per block (opt-in)
 constexpr int BAR_AREA = 256;
+constexpr int EPI_BUF_BYTES = 32 * 16 * 4;          // one warp's 32 rows x 16 FP32 columns
+constexpr int EPI_SMEM = 4 * 2 * EPI_BUF_BYTES;     // 4 epilogue warps, double-buffered
+
+enum { MODE_IM2COL = 0, MODE_GATHER = 1, MODE_RUNS = 2 };
+constexpr int GATHER_GROUPS = 2;
 
 struct TcParams {
     int N, C, H, W, K, R, S, P, Q;
@@ -59,10 +65,18 @@ struct TcParams {
     const float *bias;
     float alpha, beta;
     int relu, y_bf16;
+    int y_tma;                      // epilogue stores y through the 2-D tensor map tmY
     int BN, stages, num_kb, c_blocks;
     int n_tiles;
+    int b_res;                      // gather modes: all num_kb filter blocks resident in smem
+    int run_len, num_runs;          // run gather: elements per run, number of runs
+    int slot, rpb;                  // run gather: slot elements per run, runs per k-block
+    int nchw_runs;                  // runs over s of one (c, r) (else over (s, c) of one r)
     long long num_tiles;
     uint32_t idesc, tmem_cols, acc_stride;  // acc_stride: TMEM column offset of accumulator 1
+    int sk;                         // stream-K schedule over (tile, k-block) units
+    long long sk_units;             // units per CTA (>= num_kb, so a tile has <= 2 parts)
+    int *sk_flags;                  // per-tile partial-ready flags (zero between launches)
     int *err;
     unsigned long long timeout_ns;
 };
@@ -86,6 +100,46 @@ __device__ __forceinline__ TileCoord tile_coord(const TcParams &p, long long til
     return tc;
 }
 
+// One piece of work: k-blocks [kb0, kb1) of one output tile.
+struct Seg {
+    long long tile;
+    int kb0, kb1;
+};
+
+// The CTA's sequence of segments.  Data-parallel: whole tiles blockIdx.x,
+// blockIdx.x + gridDim.x, ...  Stream-K: the contiguous range of sk_units
+// (tile, k-block) units starting at blockIdx.x * sk_units; it may begin with
+// the last k-blocks of one tile and end with the first k-blocks of another.
+struct WorkIter {
+    long long u, u_end;
+    __device__ __forceinline__ explicit WorkIter(const TcParams &p) {
+        if (p.sk) {
+            const long long total = p.num_tiles * p.num_kb;
+            u = (long long)blockIdx.x * p.sk_units;
+            u_end = u + p.sk_units < total ? u + p.sk_units : total;
+        } else {
+            u = blockIdx.x;
+            u_end = p.num_tiles;
+        }
+    }
+    __device__ __forceinline__ bool next(const TcParams &p, Seg &sg) {
+        if (u >= u_end) return false;
+        if (p.sk) {
+            sg.tile = u / p.num_kb;
+            sg.kb0 = (int)(u - sg.tile * p.num_kb);
+            const long long left = u_end - u;
+            sg.kb1 = (long long)(p.num_kb - sg.kb0) <= left ? p.num_kb : sg.kb0 + (int)left;
+            u += sg.kb1 - sg.kb0;
+        } else {
+            sg.tile = u;
+            sg.kb0 = 0;
+            sg.kb1 = p.num_kb;
+            u += gridDim.x;
+        }
+        return true;
+    }
+};
+
 // ---------------------------------------------------------------------------
 // producer, TMA variant (one thread)
 // ---------------------------------------------------------------------------
@@ -98,29 +152,36 @@ __device__ void produce_tma(const TcParams &p, const CUtensorMap *tmA, const CUt
     const uint32_t tx = A_STAGE_BYTES + b_stage;
     int it = 0;
     bool ok = true;
-    for (long long tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-        const TileCoord tc = tile_coord(p, tile);
+    WorkIter wi(p);
+    Seg sg;
+    while (ok && wi.next(p, sg)) {
+        const TileCoord tc = tile_coord(p, sg.tile);
         const int n0 = (int)(tc.m0 / p.PQ);
         const int rem = (int)(tc.m0 - (long long)n0 * p.PQ);
         const int p0 = rem / p.Q, q0 = rem - (rem / p.Q) * p.Q;
         const int wc = q0 * p.v - p.pl;  // first window origin of the tile
         const int hc = p0 * p.u - p.pt;
-        for (int r = 0; ok && r < p.R; ++r) {
-            for (int s = 0; ok && s < p.S; ++s) {
-                for (int cb = 0; cb < p.c_blocks; ++cb) {
-                    const int stage = it % ST;
-                    const uint32_t ph = (uint32_t)(it / ST) & 1u;
-                    if (!mbar_wait(&empty[stage], ph ^ 1u, ctl, 1)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&full[stage], tx);
-                    tma_load_im2col_4d(smA + (size_t)stage * A_STAGE_BYTES, tmA, &full[stage],
-                                       cb * BK, wc, hc, n0, (uint16_t)(s * p.dw),
-                                       (uint16_t)(r * p.dh));
-                    tma_load_4d(smB + (size_t)stage * b_stage, tmB, &full[stage], cb * BK, s, r,
-                                tc.k0);
-                    ++it;
+        // k-block kb = (r*S + s)*c_blocks + cb
+        int cb = sg.kb0 % p.c_blocks;
+        const int rs = sg.kb0 / p.c_blocks;
+        int s = rs % p.S, r = rs / p.S;
+        for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+            const int stage = it % ST;
+            const uint32_t ph = (uint32_t)(it / ST) & 1u;
+            if (!mbar_wait(&empty[stage], ph ^ 1u, ctl, 1)) {
+                ok = false;
+                break;
+            }
+            mbar_arrive_expect_tx(&full[stage], tx);
+            tma_load_im2col_4d(smA + (size_t)stage * A_STAGE_BYTES, tmA, &full[stage], cb * BK, wc,
+                               hc, n0, (uint16_t)(s * p.dw), (uint16_t)(r * p.dh));
+            tma_load_4d(smB + (size_t)stage * b_stage, tmB, &full[stage], cb * BK, s, r, tc.k0);
+            ++it;
+            if (++cb == p.c_blocks) {
+                cb = 0;
+                if (++s == p.S) {
+                    s = 0;
+                    ++r;
                 }
             }
         }
@@ -131,7 +192,9 @@ __device__ void produce_tma(const TcParams &p, const CUtensorMap *tmA, const CUt
 }
 
 // ---------------------------------------------------------------------------
-// producer, gather variant (128 threads, thread t writes A row t)
+// producers, gather variants (GROUPS x 128 threads; thread t of a group
+// writes A row t of the stages its group owns: stage iteration it belongs to
+// group it % GROUPS, so GROUPS stages are filled concurrently)
 // ---------------------------------------------------------------------------
 template <typename T>
 __device__ __forceinline__ uint32_t pack2(T lo, T hi);
@@ -140,7 +203,15 @@ __device__ __forceinline__ uint32_t pack2<uint16_t>(uint16_t lo, uint16_t hi) {
     return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
-// Walks the flattened reduction index kk = (r*S + s)*C + c of one operand row.
+__device__ __forceinline__ void store_chunk(uint8_t *row, int row_idx, int chunk, uint32_t a0,
+                                            uint32_t a1, uint32_t a2, uint32_t a3) {
+    uint8_t *dst = row + ((chunk ^ (row_idx & 7)) << 4);  // 128-byte swizzle
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(dst)), "r"(a0),
+                 "r"(a1), "r"(a2), "r"(a3)
+                 : "memory");
+}
+
+// Element-gather reduction order: kk = (r*S + s)*C + c, any strides.
 struct RscWalker {
     int r, s, c;
     __device__ __forceinline__ void start(int kk0, int C, int S) {
@@ -160,29 +231,203 @@ struct RscWalker {
     }
 };
 
-template <typename T>
-__device__ __forceinline__ void store_row_chunk(uint8_t *row, int row_idx, int chunk,
-                                                const uint32_t (&w4)[4]) {
-    uint8_t *dst = row + ((chunk ^ (row_idx & 7)) << 4);
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(dst)), "r"(w4[0]),
-                 "r"(w4[1]), "r"(w4[2]), "r"(w4[3])
-                 : "memory");
+// One 16-byte chunk (BK/8 elements) of an element-gather operand row.
+template <typename T, bool IS_A>
+__device__ __forceinline__ void gather_elem_chunk(const TcParams &p, const T *base, bool ok, int h0,
+                                                  int w0, int kk0, uint32_t (&o)[4]) {
+    constexpr int PER_WORD = 4 / (int)sizeof(T);
+    RscWalker wk;
+    wk.start(kk0, p.C, p.S);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        T e[PER_WORD];
+#pragma unroll
+        for (int j = 0; j < PER_WORD; ++j) {
+            T val = 0;
+            if (ok && wk.r < p.R) {
+                if constexpr (IS_A) {
+                    const int h = h0 + wk.r * p.dh, wi = w0 + wk.s * p.dw;
+                    if (h >= 0 && h < p.H && wi >= 0 && wi < p.W)
+                        val = base[wk.c * p.xs[1] + h * p.xs[2] + wi * p.xs[3]];
+                } else {
+                    val = base[wk.c * p.ws[1] + wk.r * p.ws[2] + wk.s * p.ws[3]];
+                }
+            }
+            e[j] = val;
+            wk.step(p.C, p.S);
+        }
+        if constexpr (PER_WORD == 2) o[q] = pack2<T>(e[0], e[1]);
+        else o[q] = (uint32_t)e[0];
+    }
 }
 
+// Run-gather reduction layout.  A run is a sequence of elements that are
+// contiguous in memory -- the (s, c) elements of one filter row r for
+// channels-innermost activations with KRSC filters, the s elements of one
+// (c, r) pair for width-innermost activations with KCRS filters.  Each
+// 128-byte reduction row of a k-block holds `rpb` runs, each in its own slot
+// of `slot` elements (a whole number of 16-byte chunks); the rest of the row
+// is zero.  Run index j = c*R + r (width-innermost) or r (channels-innermost).
+
+// Streams one run into its slot: elements [e_lo, e_hi) of the run (the rest
+// are zero) are read from `src` (element 0 of the run) with aligned 128-bit
+// loads that each hold at least one requested byte, realigned with selects and
+// funnel shifts, and stored as the slot's `nchunks` swizzled 16-byte chunks
+// starting at chunk `c0` of the row.
 template <typename T>
+__device__ __forceinline__ void stream_run(uint8_t *row, int row_idx, int c0, int nchunks,
+                                           const T *src, int e_lo, int e_hi) {
+    constexpr int EPC = 16 / (int)sizeof(T);
+    const uintptr_t a = reinterpret_cast<uintptr_t>(src);
+    const uintptr_t lo = a + (uintptr_t)e_lo * sizeof(T);   // first requested byte
+    const uintptr_t hi = a + (uintptr_t)e_hi * sizeof(T);   // one past the last
+    const uintptr_t base = a & ~(uintptr_t)15;
+    const int q = (int)((a >> 2) & 3u);                     // word offset inside a vector
+    const int sh = (int)(a & 3u) * 8;                       // byte shift inside a word
+    auto vec = [&](int k, uint32_t (&v)[4]) {
+        const uintptr_t va = base + (uintptr_t)k * 16;
+        if (va < hi && va + 16 > lo) {
+            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(va));
+            v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+        } else {
+            v[0] = v[1] = v[2] = v[3] = 0u;
+        }
+    };
+    uint32_t cur[4], nxt[4];
+    vec(0, cur);
+#pragma unroll 1
+    for (int j = 0; j < nchunks; ++j) {
+        vec(j + 1, nxt);
+        uint32_t w[5];
+#pragma unroll
+        for (int i = 0; i < 5; ++i) {  // w[i] = word q+i of cur:nxt
+            const uint32_t c0v = i < 4 ? cur[i] : nxt[i - 4];
+            const uint32_t c1v = i + 1 < 4 ? cur[i + 1] : nxt[i + 1 - 4];
+            const uint32_t c2v = i + 2 < 4 ? cur[i + 2] : nxt[i + 2 - 4];
+            const uint32_t c3v = i + 3 < 4 ? cur[i + 3] : nxt[i + 3 - 4];
+            w[i] = q == 0 ? c0v : (q == 1 ? c1v : (q == 2 ? c2v : c3v));
+        }
+        uint32_t o[4];
+        const int e0 = j * EPC;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t v = __funnelshift_r(w[i], w[i + 1], sh);
+            if constexpr (sizeof(T) == 2) {
+                const int el = e0 + 2 * i;
+                const bool lo_ok = el >= e_lo && el < e_hi;
+                const bool hi_ok = el + 1 >= e_lo && el + 1 < e_hi;
+                v &= (lo_ok ? 0x0000FFFFu : 0u) | (hi_ok ? 0xFFFF0000u : 0u);
+            } else {
+                const int el = e0 + i;
+                if (el < e_lo || el >= e_hi) v = 0u;
+            }
+            o[i] = v;
+        }
+        store_chunk(row, row_idx, c0 + j, o[0], o[1], o[2], o[3]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
+    }
+}
+
+// Fills A row `t` (output pixel m) of reduction block kb in the slot layout.
+// Run elements [e_lo, e_hi) of the row's window lie inside the image along W;
+// filter rows outside [0, H) and rows past the tile are zero.
+template <typename T>
+__device__ __forceinline__ void fill_a_row_runs(const TcParams &p, uint8_t *row, int t, int kb,
+                                                bool valid, const T *xn, int h0, int w0, int e_lo,
+                                                int e_hi) {
+    constexpr int EPC = 16 / (int)sizeof(T);
+    const int cps = p.slot / EPC;  // chunks per slot
+    int c0 = 0;
+    for (int ri = 0; ri < p.rpb; ++ri, c0 += cps) {
+        const int run = kb * p.rpb + ri;
+        int c = 0, r = run;
+        if (p.nchw_runs) {
+            c = run / p.R;
+            r = run - c * p.R;
+        }
+        const int h = h0 + r * p.dh;
+        if (valid && run < p.num_runs && h >= 0 && h < p.H && e_lo < e_hi) {
+            const T *src = xn + (long long)h * p.xs[2] +
+                           (p.nchw_runs ? (long long)c * p.xs[1] + w0 : (long long)w0 * p.C);
+            stream_run<T>(row, t, c0, cps, src, e_lo, e_hi);
+        } else {
+            for (int j = 0; j < cps; ++j) store_chunk(row, t, c0 + j, 0u, 0u, 0u, 0u);
+        }
+    }
+    for (; c0 < 8; ++c0) store_chunk(row, t, c0, 0u, 0u, 0u, 0u);
+}
+
+// Fills the BN filter rows of reduction block kb into `dst`, the tasks spread
+// over `nthr` threads (run gather: one task per (row, run); element gather:
+// one task per (row, 16-byte chunk)).
+template <typename T, int MODE>
+__device__ void fill_b_block(const TcParams &p, uint8_t *dst, int kb, int k0, int tid, int nthr) {
+    constexpr int EPC = 16 / (int)sizeof(T);
+    const T *w = static_cast<const T *>(p.w);
+    if constexpr (MODE == MODE_RUNS) {
+        const int cps = p.slot / EPC;
+        const int tasks = p.BN * 8;  // (row, slot) pairs; slots past rpb fill the row's zeros
+        for (int task = tid; task < tasks; task += nthr) {
+            const int br = task >> 3, ri = task & 7;
+            uint8_t *rowp = dst + br * ROW_BYTES;
+            if (ri >= p.rpb) {
+                for (int cc = ri == p.rpb ? p.rpb * cps : 8; cc < 8; ++cc)
+                    store_chunk(rowp, br, cc, 0u, 0u, 0u, 0u);
+                continue;
+            }
+            const int k = k0 + br;
+            const int run = kb * p.rpb + ri;
+            if (k < p.K && run < p.num_runs) {
+                int c = 0, r = run;
+                if (p.nchw_runs) {
+                    c = run / p.R;
+                    r = run - c * p.R;
+                }
+                const T *src = w + (long long)k * p.ws[0] + (long long)r * p.ws[2] +
+                               (p.nchw_runs ? (long long)c * p.ws[1] : 0);
+                stream_run<T>(rowp, br, ri * cps, cps, src, 0, p.run_len);
+            } else {
+                for (int j = 0; j < cps; ++j) store_chunk(rowp, br, ri * cps + j, 0u, 0u, 0u, 0u);
+            }
+        }
+    } else {
+        const int tasks = p.BN * 8;
+        for (int task = tid; task < tasks; task += nthr) {
+            const int br = task >> 3, j = task & 7;
+            const int k = k0 + br;
+            uint32_t o[4] = {0u, 0u, 0u, 0u};
+            if (k < p.K)
+                gather_elem_chunk<T, false>(p, w + (long long)k * p.ws[0], true, 0, 0,
+                                            (kb * 8 + j) * EPC, o);
+            store_chunk(dst + br * ROW_BYTES, br, j, o[0], o[1], o[2], o[3]);
+        }
+    }
+}
+
+template <typename T, int MODE, int GROUPS>
 __device__ void produce_gather(const TcParams &p, uint8_t *smA, uint8_t *smB, uint64_t *full,
-                               uint64_t *empty, const WaitCtl &ctl) {
+                               uint64_t *empty, uint64_t *bres, const WaitCtl &ctl) {
+    constexpr int EPC = 16 / (int)sizeof(T);
     constexpr int BK = ROW_BYTES / (int)sizeof(T);
-    constexpr int PER_WORD = 4 / (int)sizeof(T);
-    const int t = threadIdx.x;  // 0..127
+    const int group = threadIdx.x >> 7;  // producer warps are 0 .. 4*GROUPS-1
+    const int t = threadIdx.x & 127;
     const int ST = p.stages;
     const uint32_t b_stage = (uint32_t)p.BN * ROW_BYTES;
     const T *x = static_cast<const T *>(p.x);
-    const T *w = static_cast<const T *>(p.w);
+
+    if (p.b_res) {  // the whole filter tile stays in shared memory
+        for (int kb = 0; kb < p.num_kb; ++kb)
+            fill_b_block<T, MODE>(p, smB + (size_t)kb * b_stage, kb, 0, threadIdx.x, 128 * GROUPS);
+        fence_proxy_async_smem();
+        mbar_arrive(bres);
+    }
     int it = 0;
     bool ok = true;
-    for (long long tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-        const TileCoord tc = tile_coord(p, tile);
+    WorkIter wi(p);
+    Seg sg;
+    while (ok && wi.next(p, sg)) {
+        const TileCoord tc = tile_coord(p, sg.tile);
         const long long m = tc.m0 + t;
         const bool valid = m < p.M;
         int n = 0, op = 0, oq = 0;
@@ -194,73 +439,32 @@ __device__ void produce_gather(const TcParams &p, uint8_t *smA, uint8_t *smB, ui
         }
         const int h0 = op * p.u - p.pt, w0 = oq * p.v - p.pl;
         const T *xn = x + (long long)n * p.xs[0];
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        // run elements whose pixel lies inside the image along W (dw == 1 in run mode)
+        const int run_c = p.nchw_runs ? 1 : p.C;
+        const int e_lo = max(0, -w0) * run_c;
+        const int e_hi = max(0, min(p.S, p.W - w0)) * run_c;  // <= run_len
+        for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
+            if (GROUPS > 1 && (it % GROUPS) != group) continue;
             const int stage = it % ST;
             const uint32_t ph = (uint32_t)(it / ST) & 1u;
             if (!mbar_wait(&empty[stage], ph ^ 1u, ctl, 6)) {
                 ok = false;
                 break;
             }
-            const int kk0 = kb * BK;
-            // A row t
-            {
-                uint8_t *row = smA + (size_t)stage * A_STAGE_BYTES + t * ROW_BYTES;
-                RscWalker wk;
-                wk.start(kk0, p.C, p.S);
+            uint8_t *arow = smA + (size_t)stage * A_STAGE_BYTES + t * ROW_BYTES;
+            if constexpr (MODE == MODE_RUNS) {
+                fill_a_row_runs<T>(p, arow, t, kb, valid, xn, h0, w0, e_lo, e_hi);
+            } else {
 #pragma unroll 1
-                for (int ch = 0; ch < 8; ++ch) {
-                    uint32_t w4[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        T e[PER_WORD];
-#pragma unroll
-                        for (int j = 0; j < PER_WORD; ++j) {
-                            T val = 0;
-                            if (valid && wk.r < p.R) {
-                                const int h = h0 + wk.r * p.dh, wi = w0 + wk.s * p.dw;
-                                if (h >= 0 && h < p.H && wi >= 0 && wi < p.W)
-                                    val = xn[wk.c * p.xs[1] + h * p.xs[2] + wi * p.xs[3]];
-                            }
-                            e[j] = val;
-                            wk.step(p.C, p.S);
-                        }
-                        if constexpr (PER_WORD == 2) w4[q] = pack2<T>(e[0], e[1]);
-                        else w4[q] = (uint32_t)e[0];
-                    }
-                    store_row_chunk<T>(row, t, ch, w4);
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t o[4];
+                    gather_elem_chunk<T, true>(p, xn, valid, h0, w0, kb * BK + j * EPC, o);
+                    store_chunk(arow, t, j, o[0], o[1], o[2], o[3]);
                 }
             }
-            // B rows t, t+128 (filters k0 + row)
-            for (int br = t; br < p.BN; br += BM) {
-                uint8_t *row = smB + (size_t)stage * b_stage + br * ROW_BYTES;
-                const int k = tc.k0 + br;
-                const bool kval = k < p.K;
-                const T *wk_ptr = w + (long long)(kval ? k : 0) * p.ws[0];
-                RscWalker wk;
-                wk.start(kk0, p.C, p.S);
-#pragma unroll 1
-                for (int ch = 0; ch < 8; ++ch) {
-                    uint32_t w4[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        T e[PER_WORD];
-#pragma unroll
-                        for (int j = 0; j < PER_WORD; ++j) {
-                            T val = 0;
-                            if (kval && wk.r < p.R)
-                                val = wk_ptr[wk.c * p.ws[1] + wk.r * p.ws[2] + wk.s * p.ws[3]];
-                            e[j] = val;
-                            wk.step(p.C, p.S);
-                        }
-                        if constexpr (PER_WORD == 2) w4[q] = pack2<T>(e[0], e[1]);
-                        else w4[q] = (uint32_t)e[0];
-                    }
-                    store_row_chunk<T>(row, br, ch, w4);
-                }
-            }
+            if (!p.b_res) fill_b_block<T, MODE>(p, smB + (size_t)stage * b_stage, kb, tc.k0, t, 128);
             fence_proxy_async_smem();
             mbar_arrive(&full[stage]);
-            ++it;
         }
     }
 }
@@ -271,19 +475,22 @@ __device__ void produce_gather(const TcParams &p, uint8_t *smA, uint8_t *smB, ui
 template <bool TF32>
 __device__ void issue_mma(const TcParams &p, uint32_t tmem_base, uint8_t *smA, uint8_t *smB,
                           uint64_t *full, uint64_t *empty, uint64_t *tfull, uint64_t *tempty,
-                          uint64_t *mma_done, const WaitCtl &ctl) {
+                          uint64_t *mma_done, uint64_t *bres, const WaitCtl &ctl) {
     const int ST = p.stages;
     const uint32_t b_stage = (uint32_t)p.BN * ROW_BYTES;
     const uint32_t a0 = smem_u32(smA), b0 = smem_u32(smB);
     int it = 0, t = 0;
     bool ok = true;
-    for (long long tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+    if (p.b_res && !mbar_wait(bres, 0u, ctl, 7)) ok = false;
+    WorkIter wi(p);
+    Seg sg;
+    while (ok && wi.next(p, sg)) {
         const int buf = t & 1;
         const uint32_t aph = (uint32_t)(t >> 1) & 1u;
         if (!mbar_wait(&tempty[buf], aph ^ 1u, ctl, 3)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + (uint32_t)buf * p.acc_stride;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
             const int stage = it % ST;
             const uint32_t ph = (uint32_t)(it / ST) & 1u;
             if (!mbar_wait(&full[stage], ph, ctl, 4)) {
@@ -292,12 +499,12 @@ __device__ void issue_mma(const TcParams &p, uint32_t tmem_base, uint8_t *smA, u
             }
             tc_fence_after_sync();
             const uint32_t a_addr = a0 + (uint32_t)stage * A_STAGE_BYTES;
-            const uint32_t b_addr = b0 + (uint32_t)stage * b_stage;
+            const uint32_t b_addr = b0 + (uint32_t)(p.b_res ? kb : stage) * b_stage;
 #pragma unroll
             for (int k = 0; k < ROW_BYTES / 32; ++k) {
                 const uint64_t ad = sw128_kmajor_desc(a_addr + k * 32);
                 const uint64_t bd = sw128_kmajor_desc(b_addr + k * 32);
-                const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
+                const uint32_t acc = (kb > sg.kb0 || k > 0) ? 1u : 0u;
                 if constexpr (TF32) umma_tf32(d_tmem, ad, bd, p.idesc, acc);
                 else umma_bf16(d_tmem, ad, bd, p.idesc, acc);
             }
@@ -325,15 +532,73 @@ __device__ __forceinline__ unsigned short f32_to_bf16_bits(float f) {
     return *reinterpret_cast<unsigned short *>(&b);
 }
 
+// Writes one thread's 16 finished values into its row of the warp's staging
+// buffer (32 rows x 64 bytes for FP32, x 32 bytes for BF16) in the tensor
+// map's swizzle: 64-byte rows swizzle 16-byte chunks by (row / 2) % 4, 32-byte
+// rows by (row / 4) % 2.
+__device__ __forceinline__ void stage_row(uint8_t *buf, int lane, const float (&val)[16], bool bf16) {
+    if (!bf16) {
+        uint8_t *rowp = buf + lane * 64;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint8_t *dst = rowp + ((j ^ ((lane >> 1) & 3)) << 4);
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(dst)),
+                         "f"(val[4 * j]), "f"(val[4 * j + 1]), "f"(val[4 * j + 2]),
+                         "f"(val[4 * j + 3])
+                         : "memory");
+        }
+    } else {
+        uint8_t *rowp = buf + lane * 32;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                __nv_bfloat162 h = __floats2bfloat162_rn(val[8 * j + 2 * i], val[8 * j + 2 * i + 1]);
+                w[i] = *reinterpret_cast<uint32_t *>(&h);
+            }
+            uint8_t *dst = rowp + ((j ^ ((lane >> 2) & 1)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(dst)), "r"(w[0]),
+                         "r"(w[1]), "r"(w[2]), "r"(w[3])
+                         : "memory");
+        }
+    }
+}
+
+// Named barrier of the four epilogue warps (id 1; the block-wide barrier is 0).
+__device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Waits (bounded) until another CTA has published the partial sum of a tile.
+__device__ bool wait_partial_flag(int *flag, const WaitCtl &ctl) {
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        if (v != 0) return true;
+        if (*ctl.abort_flag) return false;
+        if (globaltimer_ns() - t0 > ctl.timeout_ns) {
+            *ctl.abort_flag = 1;
+            record_error(ctl.err, 1 /* DLC_DEVERR_WAIT_TIMEOUT */, 8);
+            return false;
+        }
+        __nanosleep(128);
+    }
+}
+
 __device__ void epilogue(const TcParams &p, uint32_t tmem_base, uint64_t *tfull, uint64_t *tempty,
-                         const WaitCtl &ctl) {
+                         uint8_t *epi_smem, const CUtensorMap *tmY, const WaitCtl &ctl) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int quad = warp & 3;  // TMEM lanes this warp may read: 32*quad .. 32*quad+31
     const int row = quad * 32 + lane;
+    const bool leader = threadIdx.x == blockDim.x - 128;  // first epilogue thread
     float *yf = static_cast<float *>(p.y);
     unsigned short *yb = static_cast<unsigned short *>(p.y);
+    uint8_t *my_bufs = epi_smem + quad * 2 * EPI_BUF_BYTES;
+    int nbuf = 0;  // staging buffers used so far by this warp
     int t = 0;
-    for (long long tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+    WorkIter wi(p);
+    Seg sg;
+    while (wi.next(p, sg)) {
         const int buf = t & 1;
         const uint32_t aph = (uint32_t)(t >> 1) & 1u;
         int okw = 0;
@@ -342,7 +607,22 @@ __device__ void epilogue(const TcParams &p, uint32_t tmem_base, uint64_t *tfull,
         if (!okw) break;
         __syncwarp();
         tc_fence_after_sync();
-        const TileCoord tc = tile_coord(p, tile);
+        const TileCoord tc = tile_coord(p, sg.tile);
+        // Stream-K: a tile split between two CTAs.  The CTA holding its last
+        // k-blocks runs them first and parks the raw FP32 partial sum in y
+        // (tail); the CTA holding its first k-blocks runs them last, adds the
+        // parked partial and applies the epilogue (head).
+        const bool tail = p.sk && sg.kb0 > 0;
+        const bool head = p.sk && sg.kb0 == 0 && sg.kb1 < p.num_kb;
+        bool have_partial = false;
+        if (head) {
+            if (leader) {
+                int *flag = p.sk_flags + sg.tile;
+                if (wait_partial_flag(flag, ctl)) *flag = 0;  // consumed; zero for the next launch
+            }
+            epilogue_bar();
+            have_partial = !*ctl.abort_flag;
+        }
         const long long m = tc.m0 + row;
         const bool valid = m < p.M;
         long long ybase = 0;
@@ -357,8 +637,76 @@ __device__ void epilogue(const TcParams &p, uint32_t tmem_base, uint64_t *tfull,
             uint32_t v[16];
             tmem_ld_32x32b_x16(taddr + (uint32_t)c0, v);
             tmem_ld_wait();
-            if (!valid) continue;
             const int kbase = tc.k0 + c0;
+            // 16 consecutive filters of one pixel contiguous and 16-byte aligned in y
+            const bool vec16 = valid && p.ys[1] == 1 && kbase + 16 <= p.K &&
+                               ((reinterpret_cast<uintptr_t>(yf + ybase + kbase) & 15u) == 0);
+            if (tail) {  // park the raw partial sum (FP32 y, any strides)
+                if (vec16) {
+                    float4 *dst = reinterpret_cast<float4 *>(yf + ybase + kbase);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        __stcg(dst + j, make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                                    __uint_as_float(v[4 * j + 2]),
+                                                    __uint_as_float(v[4 * j + 3])));
+                } else if (valid) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (kbase + j < p.K)
+                            __stcg(yf + ybase + (long long)(kbase + j) * p.ys[1], __uint_as_float(v[j]));
+                }
+                continue;
+            }
+            if (have_partial && vec16) {
+                const float4 *src = reinterpret_cast<const float4 *>(yf + ybase + kbase);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float4 f = __ldcg(src + j);
+                    v[4 * j] = __float_as_uint(__uint_as_float(v[4 * j]) + f.x);
+                    v[4 * j + 1] = __float_as_uint(__uint_as_float(v[4 * j + 1]) + f.y);
+                    v[4 * j + 2] = __float_as_uint(__uint_as_float(v[4 * j + 2]) + f.z);
+                    v[4 * j + 3] = __float_as_uint(__uint_as_float(v[4 * j + 3]) + f.w);
+                }
+            } else if (have_partial && valid) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (kbase + j < p.K)
+                        v[j] = __float_as_uint(__uint_as_float(v[j]) +
+                                               __ldcg(yf + ybase + (long long)(kbase + j) * p.ys[1]));
+            }
+            if (p.y_tma) {
+                if (kbase >= p.K) break;  // warp-uniform
+                float val[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    float f = p.alpha * __uint_as_float(v[j]);
+                    const int k = kbase + j;
+                    if (valid && k < p.K) {
+                        if (p.beta != 0.f) {
+                            const long long yo = ybase + k;
+                            f = __fmaf_rn(p.beta, p.y_bf16 ? bf16_bits_to_f32(yb[yo]) : yf[yo], f);
+                        }
+                        if (p.bias) f += __ldg(p.bias + k);
+                    }
+                    if (p.relu) f = fmaxf(f, 0.f);
+                    val[j] = f;
+                }
+                uint8_t *sb = my_bufs + (nbuf & 1) * EPI_BUF_BYTES;
+                if (nbuf >= 2) {  // the store issued from this buffer two chunks ago
+                    if (lane == 0) bulk_wait_group_read<1>();
+                    __syncwarp();
+                }
+                stage_row(sb, lane, val, p.y_bf16 != 0);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(tmY, sb, kbase, (int)(tc.m0 + quad * 32));
+                    bulk_commit_group();
+                }
+                ++nbuf;
+                continue;
+            }
+            if (!valid) continue;
             const bool full16 = kbase + 16 <= p.K;
             const long long yo0 = ybase + (long long)kbase * p.ys[1];
             float val[16];
@@ -393,44 +741,64 @@ __device__ void epilogue(const TcParams &p, uint32_t tmem_base, uint64_t *tfull,
                 }
             }
         }
+        if (tail) {  // publish the partial once every epilogue thread has stored its part
+            __threadfence();
+            epilogue_bar();
+            if (leader)
+                asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.sk_flags + sg.tile), "r"(1)
+                             : "memory");
+        }
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);
         ++t;
     }
+    // staged stores must finish reading shared memory (and land) before exit
+    if (p.y_tma && lane == 0) bulk_wait_group_all();
+    __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <bool TF32, bool GATHER>
-__global__ void __launch_bounds__(GATHER ? 288 : 192, 1)
+template <int MODE>
+struct KernelShape {
+    static constexpr int PROD_WARPS = MODE == MODE_IM2COL ? 1 : 4 * GATHER_GROUPS;
+    static constexpr int THREADS = (PROD_WARPS + 5) * 32;  // + MMA warp + 4 epilogue warps
+};
+
+template <bool TF32, int MODE>
+__global__ void __launch_bounds__(KernelShape<MODE>::THREADS, 1)
     conv_fprop_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tmA,
-                         const __grid_constant__ CUtensorMap tmB) {
+                         const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmY) {
     using T = typename std::conditional<TF32, uint32_t, uint16_t>::type;
     constexpr int BK = ROW_BYTES / (int)sizeof(T);
-    constexpr int PROD_WARPS = GATHER ? 4 : 1;
+    constexpr int PROD_WARPS = KernelShape<MODE>::PROD_WARPS;
     constexpr int MMA_WARP = PROD_WARPS;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     const int ST = p.stages;
+    const int b_blocks = p.b_res ? p.num_kb : ST;
     uint8_t *smA = smem;
     uint8_t *smB = smem + (size_t)ST * A_STAGE_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smB + (size_t)ST * p.BN * ROW_BYTES);
+    uint8_t *epi_smem = smB + (size_t)b_blocks * p.BN * ROW_BYTES;  // 1024-aligned
+    uint64_t *bars = reinterpret_cast<uint64_t *>(epi_smem + (p.y_tma ? EPI_SMEM : 0));
     uint64_t *full = bars;
     uint64_t *empty = bars + ST;
     uint64_t *tfull = bars + 2 * ST;
     uint64_t *tempty = tfull + 2;
     uint64_t *mma_done = tempty + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    uint64_t *bres = mma_done + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bres + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int i = 0; i < ST; ++i) {
-            mbar_init(&full[i], GATHER ? 128u : 1u);
+            mbar_init(&full[i], MODE == MODE_IM2COL ? 1u : 128u);
             mbar_init(&empty[i], 1u);
         }
         for (int i = 0; i < 2; ++i) {
@@ -438,10 +806,11 @@ __global__ void __launch_bounds__(GATHER ? 288 : 192, 1)
             mbar_init(&tempty[i], 4u);  // one arrival per epilogue warp
         }
         mbar_init(mma_done, 1u);
+        mbar_init(bres, 128u * GATHER_GROUPS);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (!GATHER && warp == 0 && lane == 0) {
+    if (MODE == MODE_IM2COL && warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
     }
@@ -456,12 +825,17 @@ __global__ void __launch_bounds__(GATHER ? 288 : 192, 1)
     const WaitCtl ctl{abort_flag, p.err, p.timeout_ns};
 
     if (warp < PROD_WARPS) {
-        if constexpr (GATHER) produce_gather<T>(p, smA, smB, full, empty, ctl);
-        else if (lane == 0) produce_tma<BK>(p, &tmA, &tmB, smA, smB, full, empty, ctl);
+        if constexpr (MODE == MODE_IM2COL) {
+            if (lane == 0) produce_tma<BK>(p, &tmA, &tmB, smA, smB, full, empty, ctl);
+        } else {
+            produce_gather<T, MODE, GATHER_GROUPS>(p, smA, smB, full, empty, bres, ctl);
+        }
     } else if (warp == MMA_WARP) {
-        if (lane == 0) issue_mma<TF32>(p, tmem_base, smA, smB, full, empty, tfull, tempty, mma_done, ctl);
+        if (lane == 0)
+            issue_mma<TF32>(p, tmem_base, smA, smB, full, empty, tfull, tempty, mma_done, bres, ctl);
     } else {
-        epilogue(p, tmem_base, tfull, tempty, ctl);
+        if (p.y_tma && lane == 0) prefetch_tmap(&tmY);
+        epilogue(p, tmem_base, tfull, tempty, epi_smem, &tmY, ctl);
     }
     __syncwarp();
     tc_fence_before_sync();
@@ -522,6 +896,32 @@ bool im2col_ok(const ConvProblem &pb) {
     return true;
 }
 
+// Run gather: channels-innermost activations with densely packed pixels and
+// KRSC filters (runs over (s, c) of one filter row), or width-innermost
+// activations with KCRS filters (runs over s of one (c, r)); no dilation
+// along W so that a run is contiguous.
+bool runs_ok(const ConvProblem &pb, int *run_len, int *num_runs, int *nchw) {
+    if (pb.dw != 1) return false;
+    long long len, runs;
+    if (pb.xs[1] == 1 && pb.xs[3] == pb.C && pb.wfmt == DLC_TENSOR_NHWC) {
+        len = (long long)pb.S * pb.C;
+        runs = pb.R;
+        *nchw = 0;
+    } else if (pb.xs[3] == 1 && pb.wfmt == DLC_TENSOR_NCHW) {
+        len = pb.S;
+        runs = (long long)pb.C * pb.R;
+        *nchw = 1;
+    } else {
+        return false;
+    }
+    const long long epc = 16 / (pb.xdt == DLC_DATA_BFLOAT16 ? 2 : 4);
+    if (((len + epc - 1) / epc) * epc > ROW_BYTES / (16 / epc)) return false;  // one run per row at most
+    if (runs > 0x3fffffffLL) return false;
+    *run_len = (int)len;
+    *num_runs = (int)runs;
+    return true;
+}
+
 int choose_bn(int K) {
     if (K <= 256) return ((K + 15) / 16) * 16;
     int best = 256;
@@ -536,14 +936,35 @@ int choose_bn(int K) {
     return best;
 }
 
-template <bool TF32, bool GATHER>
-cudaError_t launch_kernel(const TcParams &tp, const CUtensorMap &a, const CUtensorMap &b, int grid,
-                          size_t smem, cudaStream_t st) {
-    auto kern = conv_fprop_tc_kernel<TF32, GATHER>;
+template <bool TF32, int MODE>
+cudaError_t launch_kernel(const TcParams &tp, const CUtensorMap &a, const CUtensorMap &b,
+                          const CUtensorMap &y, int grid, size_t smem, cudaStream_t st) {
+    auto kern = conv_fprop_tc_kernel<TF32, MODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, GATHER ? 288 : 192, smem, st>>>(tp, a, b);
+    kern<<<grid, KernelShape<MODE>::THREADS, smem, st>>>(tp, a, b, y);
     return cudaGetLastError();
+}
+
+template <bool TF32>
+cudaError_t launch_mode(int mode, const TcParams &tp, const CUtensorMap &a, const CUtensorMap &b,
+                        const CUtensorMap &y, int grid, size_t smem, cudaStream_t st) {
+    if (mode == MODE_IM2COL) return launch_kernel<TF32, MODE_IM2COL>(tp, a, b, y, grid, smem, st);
+    if (mode == MODE_RUNS) return launch_kernel<TF32, MODE_RUNS>(tp, a, b, y, grid, smem, st);
+    return launch_kernel<TF32, MODE_GATHER>(tp, a, b, y, grid, smem, st);
+}
+
+// y as a 2-D [M rows, K columns] tensor for bulk tensor stores: K contiguous,
+// every output pixel row at one uniform pitch, 16-byte aligned base and pitch.
+bool y_tma_ok(const ConvProblem &pb) {
+    const long long e = pb.ydt == DLC_DATA_BFLOAT16 ? 2 : 4;
+    if (pb.ys[1] != 1) return false;
+    const long long pitch = pb.ys[3];
+    if (pitch < pb.K || (pitch * e) % 16 || pitch * e >= (1LL << 40)) return false;
+    if (pb.P > 1 && pb.ys[2] != (long long)pb.Q * pitch) return false;
+    if (pb.N > 1 && pb.ys[0] != (long long)pb.P * pb.Q * pitch) return false;
+    if (pb.y && ((uintptr_t)pb.y % 16)) return false;
+    return (long long)pb.N * pb.P * pb.Q <= 0xffffffffLL;
 }
 
 }  // namespace
@@ -551,18 +972,25 @@ cudaError_t launch_kernel(const TcParams &tp, const CUtensorMap &a, const CUtens
 dlcKernel_t dlc_tc_variant(const dlcContext *, const ConvProblem &pb) {
     if (!tc_math_ok(pb)) return DLC_KERNEL_NONE;
     if (!fits_i32((long long)pb.P * pb.Q)) return DLC_KERNEL_NONE;
-    return im2col_ok(pb) ? DLC_KERNEL_TC_IM2COL : DLC_KERNEL_TC_GATHER;
+    if (im2col_ok(pb)) return DLC_KERNEL_TC_IM2COL;
+    int a, b, c;
+    if (runs_ok(pb, &a, &b, &c)) return DLC_KERNEL_TC_GATHER_RUNS;
+    return DLC_KERNEL_TC_GATHER;
 }
 
 dlcStatus_t dlc_launch_tc(dlcContext *ctx, const ConvProblem &pb, dlcKernel_t variant) {
-    if (variant != DLC_KERNEL_TC_IM2COL && variant != DLC_KERNEL_TC_GATHER)
-        return DLC_STATUS_INTERNAL_ERROR;
+    int mode;
+    if (variant == DLC_KERNEL_TC_IM2COL) mode = MODE_IM2COL;
+    else if (variant == DLC_KERNEL_TC_GATHER_RUNS) mode = MODE_RUNS;
+    else if (variant == DLC_KERNEL_TC_GATHER) mode = MODE_GATHER;
+    else return DLC_STATUS_INTERNAL_ERROR;
     const bool tf32 = pb.math == DLC_MATH_TF32;
-    const bool gather = variant == DLC_KERNEL_TC_GATHER;
     const int e = elt_bytes(pb);
     const int BK = ROW_BYTES / e;
+    const int EPC = 16 / e;
 
     TcParams tp;
+    std::memset(&tp, 0, sizeof(tp));
     tp.N = pb.N; tp.C = pb.C; tp.H = pb.H; tp.W = pb.W; tp.K = pb.K; tp.R = pb.R; tp.S = pb.S;
     tp.P = pb.P; tp.Q = pb.Q;
     tp.pt = pb.pt; tp.pl = pb.pl; tp.u = pb.u; tp.v = pb.v; tp.dh = pb.dh; tp.dw = pb.dw;
@@ -577,20 +1005,72 @@ dlcStatus_t dlc_launch_tc(dlcContext *ctx, const ConvProblem &pb, dlcKernel_t va
     tp.alpha = pb.alpha; tp.beta = pb.beta; tp.relu = pb.relu;
     tp.y_bf16 = pb.ydt == DLC_DATA_BFLOAT16;
     tp.BN = choose_bn(pb.K);
-    const int b_stage = tp.BN * ROW_BYTES;
-    int stages = (MAX_DYN_SMEM - 1024 - BAR_AREA) / (A_STAGE_BYTES + b_stage);
-    tp.stages = stages > 8 ? 8 : stages;
+    // tuning knobs for tile sweeps: DLC_TC_BN (multiple of 16, 16..256), DLC_TC_STAGES (2..8)
+    if (const char *ev = std::getenv("DLC_TC_BN")) {
+        const int bn = std::atoi(ev);
+        if (bn >= 16 && bn <= 256 && bn % 16 == 0) tp.BN = bn;
+    }
     tp.c_blocks = (pb.C + BK - 1) / BK;
-    if (gather) {
-        const long long kg = (long long)pb.R * pb.S * pb.C;
-        if (kg > 0x7fffffffLL - BK) return DLC_STATUS_NOT_SUPPORTED;
-        tp.num_kb = (int)((kg + BK - 1) / BK);
-    } else {
+    if (mode == MODE_IM2COL) {
         tp.num_kb = pb.R * pb.S * tp.c_blocks;
+    } else if (mode == MODE_RUNS) {
+        if (!runs_ok(pb, &tp.run_len, &tp.num_runs, &tp.nchw_runs)) return DLC_STATUS_INTERNAL_ERROR;
+        tp.slot = ((tp.run_len + EPC - 1) / EPC) * EPC;
+        tp.rpb = BK / tp.slot;
+        tp.num_kb = (tp.num_runs + tp.rpb - 1) / tp.rpb;
+    } else {
+        const long long kg = (long long)pb.R * pb.S * pb.C;
+        if (kg > 0x3fffffffLL) return DLC_STATUS_NOT_SUPPORTED;
+        tp.num_kb = (int)((kg + BK - 1) / BK);
     }
     tp.n_tiles = (pb.K + tp.BN - 1) / tp.BN;
     const long long m_tiles = (tp.M + BM - 1) / BM;
     tp.num_tiles = m_tiles * tp.n_tiles;
+
+    // shared memory: A stages plus either B stages or the resident filter
+    // tile, plus the epilogue's staging buffers when y is stored by TMA
+    // Bulk-tensor stores of y measured slower than direct stores from the
+    // epilogue registers (small per-warp boxes), so they are opt-in.
+    tp.y_tma = 0;
+    if (const char *ev = std::getenv("DLC_TC_YTMA")) tp.y_tma = y_tma_ok(pb) && std::atoi(ev) != 0;
+    const int b_stage = tp.BN * ROW_BYTES;
+    const int budget = MAX_DYN_SMEM - 1024 - BAR_AREA - (tp.y_tma ? EPI_SMEM : 0);
+    const long long b_all = (long long)tp.num_kb * b_stage;
+    tp.b_res = (mode != MODE_IM2COL && tp.n_tiles == 1 && b_all <= 120 * 1024 &&
+                budget - b_all >= 4 * A_STAGE_BYTES) ? 1 : 0;
+    int stages = tp.b_res ? (int)((budget - b_all) / A_STAGE_BYTES)
+                          : budget / (A_STAGE_BYTES + b_stage);
+    tp.stages = stages > 8 ? 8 : stages;
+    if (const char *ev = std::getenv("DLC_TC_STAGES")) {
+        const int st = std::atoi(ev);
+        if (st >= 2 && st < tp.stages) tp.stages = st;
+    }
+    if (tp.stages < 2) return DLC_STATUS_INTERNAL_ERROR;
+    const long long b_bytes = tp.b_res ? b_all : (long long)tp.stages * b_stage;
+
+    // Stream-K when whole tiles would leave the last round badly filled: equal
+    // (tile, k-block) ranges per CTA, at most two parts per tile (units per CTA
+    // >= k-blocks per tile because tiles >= CTAs).  The partial is parked in y,
+    // so it needs FP32 y and beta == 0.
+    long long grid = tp.num_tiles < ctx->sm_count ? tp.num_tiles : ctx->sm_count;
+    tp.sk = 0;
+    tp.sk_units = 0;
+    tp.sk_flags = ctx->sk_flags;
+    const bool sk_legal = ctx->sk_flags && pb.beta == 0.f && !tp.y_bf16 &&
+                          tp.num_tiles >= ctx->sm_count && tp.num_tiles <= DLC_SK_FLAGS &&
+                          tp.num_kb >= 4;
+    if (sk_legal) {
+        const long long rounds = (tp.num_tiles + ctx->sm_count - 1) / ctx->sm_count;
+        const double fill = (double)tp.num_tiles / (double)(rounds * ctx->sm_count);
+        tp.sk = (rounds <= 3 && fill < 0.8 && tp.num_kb >= 16) ? 1 : 0;
+        if (const char *ev = std::getenv("DLC_TC_STREAMK")) tp.sk = std::atoi(ev) != 0;
+    }
+    if (tp.sk) {
+        const long long total = tp.num_tiles * tp.num_kb;
+        tp.sk_units = (total + ctx->sm_count - 1) / ctx->sm_count;
+        grid = (total + tp.sk_units - 1) / tp.sk_units;
+    }
+
     const uint32_t fmt = tf32 ? 2u : 1u;  // operand format: BF16 = 1, TF32 = 2
     tp.idesc = (1u << 4)                  // FP32 accumulator
                | (fmt << 7) | (fmt << 10)  // A and B formats
@@ -602,10 +1082,25 @@ dlcStatus_t dlc_launch_tc(dlcContext *ctx, const ConvProblem &pb, dlcKernel_t va
     tp.err = ctx->d_err;
     tp.timeout_ns = ctx->timeout_ns;
 
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, ty;
     std::memset(&ta, 0, sizeof(ta));
     std::memset(&tb, 0, sizeof(tb));
-    if (!gather) {
+    std::memset(&ty, 0, sizeof(ty));
+    if (tp.y_tma) {
+        const bool yb16 = pb.ydt == DLC_DATA_BFLOAT16;
+        const long long ye = yb16 ? 2 : 4;
+        const cuuint64_t ydim[2] = {(cuuint64_t)pb.K, (cuuint64_t)tp.M};
+        const cuuint64_t ystr[1] = {(cuuint64_t)(pb.ys[3] * ye)};
+        const cuuint32_t ybox[2] = {16, 32};
+        const cuuint32_t ones[2] = {1, 1};
+        CUresult r = ctx->encode_tiled(
+            &ty, yb16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, pb.y,
+            ydim, ystr, ybox, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            yb16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return DLC_STATUS_EXECUTION_FAILED;
+    }
+    if (mode == MODE_IM2COL) {
         const CUtensorMapDataType dt =
             tf32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
         const cuuint64_t gdim[4] = {(cuuint64_t)pb.C, (cuuint64_t)pb.W, (cuuint64_t)pb.H,
@@ -633,17 +1128,11 @@ dlcStatus_t dlc_launch_tc(dlcContext *ctx, const ConvProblem &pb, dlcKernel_t va
         if (r != CUDA_SUCCESS) return DLC_STATUS_EXECUTION_FAILED;
     }
 
-    const size_t smem = 1024 + (size_t)tp.stages * (A_STAGE_BYTES + b_stage) + BAR_AREA;
-    long long grid = tp.num_tiles < ctx->sm_count ? tp.num_tiles : ctx->sm_count;
+    const size_t smem = 1024 + (size_t)tp.stages * A_STAGE_BYTES + (size_t)b_bytes +
+                        (tp.y_tma ? EPI_SMEM : 0) + BAR_AREA;
     if (grid < 1) grid = 1;
-    cudaError_t err;
-    if (tf32) {
-        err = gather ? launch_kernel<true, true>(tp, ta, tb, (int)grid, smem, ctx->stream)
-                     : launch_kernel<true, false>(tp, ta, tb, (int)grid, smem, ctx->stream);
-    } else {
-        err = gather ? launch_kernel<false, true>(tp, ta, tb, (int)grid, smem, ctx->stream)
-                     : launch_kernel<false, false>(tp, ta, tb, (int)grid, smem, ctx->stream);
-    }
+    cudaError_t err = tf32 ? launch_mode<true>(mode, tp, ta, tb, ty, (int)grid, smem, ctx->stream)
+                           : launch_mode<false>(mode, tp, ta, tb, ty, (int)grid, smem, ctx->stream);
     if (err != cudaSuccess) return DLC_STATUS_EXECUTION_FAILED;
     ctx->launches += 1;
     return DLC_STATUS_SUCCESS;

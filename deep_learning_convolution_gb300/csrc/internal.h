@@ -46,9 +46,13 @@ struct dlcContext {
     int *d_err = nullptr;   // device alias of h_err
     uint64_t launches = 0;
     unsigned long long timeout_ns = 2000000000ull;  // pipeline wait limit
+    int *sk_flags = nullptr;  // DLC_SK_FLAGS per-tile flags of split tiles (zero between launches)
     EncodeTiledFn encode_tiled = nullptr;
     EncodeIm2colFn encode_im2col = nullptr;
 };
+
+// Split-tile flags owned by a handle: at most this many tiles per launch use them.
+#define DLC_SK_FLAGS 4096
 
 // A fully resolved forward problem (validated by the API layer).
 struct ConvProblem {

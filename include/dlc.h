@@ -97,7 +97,10 @@ typedef enum {
     DLC_KERNEL_NONE = 0,
     DLC_KERNEL_FFMA = 1,          /* strict FP32 direct convolution, CUDA cores */
     DLC_KERNEL_TC_IM2COL = 2,     /* tcgen05 implicit GEMM, TMA im2col activations */
-    DLC_KERNEL_TC_GATHER = 3      /* tcgen05 implicit GEMM, gathered activations */
+    DLC_KERNEL_TC_GATHER = 3,     /* tcgen05 implicit GEMM, element-gathered operands */
+    DLC_KERNEL_TC_GATHER_RUNS = 4 /* tcgen05 implicit GEMM, operands gathered as contiguous
+                                     runs: (s,c) of a filter row for NHWC + KRSC, s of a
+                                     (c,r) pair for NCHW + KCRS */
 } dlcKernel_t;
 
 /* Device error codes recorded by kernels (dlcGetLastDeviceError). */

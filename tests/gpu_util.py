@@ -71,15 +71,42 @@ def oracle_points_parallel(x64, w64, pts, kw, threads=None, **epi):
     return np.concatenate([r[0] for r in res]), np.concatenate([r[1] for r in res])
 
 
+def strided_view(xt, axes: str, kind: str):
+    """The same logical tensor stored inside a larger buffer: "chan_pad" pads
+    the channel axis, "width_pad" the W axis, "image_pad" each image."""
+    import torch
+    pad = {"chan_pad": ("C", 8), "width_pad": ("W", 5), "image_pad": ("N", 0)}[kind]
+    shape = list(xt.shape)
+    if kind == "image_pad":
+        big = torch.zeros([shape[0], shape[1] * shape[2] * shape[3] + 40], dtype=xt.dtype,
+                          device=xt.device)
+        view = big[:, 8:8 + shape[1] * shape[2] * shape[3]].view(shape)
+    else:
+        ax = axes.index(pad[0])
+        shape[ax] += pad[1]
+        big = torch.zeros(shape, dtype=xt.dtype, device=xt.device)
+        sl = [slice(None)] * 4
+        sl[ax] = slice(3 if kind == "width_pad" else 0, (3 if kind == "width_pad" else 0) + xt.shape[ax])
+        view = big[tuple(sl)]
+    view.copy_(xt)
+    return view
+
+
 def run_and_check(handle, layer, seed, *, batch=None, full=None, alpha=1.0, beta=0.0,
                   with_bias=False, relu=False, y_dtype=None, y_axes=None, expect_kernel=None,
-                  guard=True, points=65536):
+                  guard=True, points=65536, view=None, w_axes=None):
     """Runs one layer on the GPU and checks it against the oracle.
-    Returns the kernel name the library chose."""
+    `view` stores x as a strided view (see strided_view); `w_axes` overrides
+    the filter layout.  Returns the kernel name the library chose."""
     import torch
     x, w, bias = synth.make_inputs(layer, seed, batch=batch, with_bias=with_bias)
     xt, wt = api.layer_tensors(layer, x, w, "cuda")
-    x_axes, w_axes = api.layer_axes(layer)
+    x_axes, w_axes0 = api.layer_axes(layer)
+    if w_axes is not None and w_axes != w_axes0:
+        wt = wt.permute(*[w_axes0.index(a) for a in w_axes]).contiguous()
+    w_axes = w_axes or w_axes0
+    if view is not None:
+        xt = strided_view(xt, x_axes, view)
     kw = layer_kwargs(layer)
     n, k, p, q = api.output_dim(xt, wt, x_axes=x_axes, w_axes=w_axes, **kw)
     y_axes = y_axes or x_axes

@@ -91,10 +91,11 @@ def test_tc_im2col_parity_full(handle, layer):
 
 
 # ---------------------------------------------------------------------------
-# tensor cores, gather producer (NCHW, small C, KCRS filters with NHWC)
+# tensor cores, run-gather producer (NHWC + KRSC runs over (s,c); NCHW + KCRS
+# runs over s): the C=3 / C=1 first layers and the NCHW speech layers
 # ---------------------------------------------------------------------------
 
-GATHER_CASES = [
+RUN_CASES = [
     L("bf16_c3_k64_11x11_s4_nhwc", 2, 3, 35, 35, 64, 11, 11, **P(2, 2, 2, 2), u=4, v=4),
     L("bf16_c3_k96_11x11_s4_nopad", 2, 3, 39, 43, 96, 11, 11, u=4, v=4),
     L("bf16_c16_k48_3x3_nchw", 2, 16, 14, 18, 48, 3, 3, **P(1, 1, 1, 1), layout="NCHW"),
@@ -102,34 +103,97 @@ GATHER_CASES = [
       dtype="tf32", layout="NCHW"),
     L("tf32_c8_k32_7x5_s2x1_nchw", 2, 8, 27, 40, 32, 7, 5, **P(3, 3, 2, 2), u=2, v=1,
       dtype="tf32", layout="NCHW"),
+    L("bf16_c5_k40_4x3_dilh2_nhwc", 3, 5, 17, 16, 40, 4, 3, **P(0, 2, 1, 0), dil_h=2, u=1, v=3),
+    L("tf32_c3_k300_3x3_nhwc", 2, 3, 20, 21, 300, 3, 3, **P(1, 1, 1, 1), dtype="tf32"),
+    L("bf16_c24_k64_5x5_nhwc", 2, 24, 13, 13, 64, 5, 5, **P(2, 2, 2, 2)),
+]
+
+
+@pytest.mark.parametrize("layer", RUN_CASES, ids=lambda l: l.name)
+def test_tc_runs_parity_full(handle, layer):
+    run_and_check(handle, layer, 2000 + RUN_CASES.index(layer), full=True,
+                  expect_kernel="tc_runs")
+
+
+# ---------------------------------------------------------------------------
+# tensor cores, element-gather producer (any strides: dilation along W, KCRS
+# filters with NHWC activations, channel-padded views)
+# ---------------------------------------------------------------------------
+
+GATHER_CASES = [
     L("bf16_c5_k100_3x3_dil", 2, 5, 13, 12, 100, 3, 3, **P(2, 2, 2, 2), dil_h=2, dil_w=2),
+    L("tf32_c16_k32_3x3_dilw3_nchw", 2, 16, 15, 19, 32, 3, 3, **P(1, 1, 3, 3), dil_w=3,
+      dtype="tf32", layout="NCHW"),
 ]
 
 
 @pytest.mark.parametrize("layer", GATHER_CASES, ids=lambda l: l.name)
 def test_tc_gather_parity_full(handle, layer):
-    run_and_check(handle, layer, 2000 + GATHER_CASES.index(layer), full=True,
+    run_and_check(handle, layer, 2500 + GATHER_CASES.index(layer), full=True,
                   expect_kernel="tc_gather")
 
 
 def test_kcrs_filters_with_nhwc_activations_use_gather(handle):
+    layer = L("bf16_nhwc_kcrs", 2, 64, 11, 11, 48, 3, 3, **P(1, 1, 1, 1))
+    run_and_check(handle, layer, 77, full=True, w_axes="KCRS", expect_kernel="tc_gather")
+
+
+@pytest.mark.parametrize("layer,view,kernel", [
+    (L("bf16_c64_view", 2, 64, 12, 13, 80, 3, 3, **P(1, 1, 1, 1)), "chan_pad", "tc_im2col"),
+    (L("bf16_c64_imgpad", 2, 64, 12, 13, 80, 3, 3, **P(1, 1, 1, 1)), "image_pad", "tc_im2col"),
+    (L("bf16_c24_view", 2, 24, 12, 13, 48, 3, 3, **P(1, 1, 1, 1)), "chan_pad", "tc_gather"),
+    (L("tf32_nchw_wview", 2, 4, 12, 13, 32, 3, 5, **P(1, 1, 2, 2), dtype="tf32",
+       layout="NCHW"), "width_pad", "tc_runs"),
+], ids=lambda v: v.name if hasattr(v, "name") else str(v))
+def test_strided_views(handle, layer, view, kernel):
+    run_and_check(handle, layer, 2600, full=True, view=view, expect_kernel=kernel)
+
+
+# ---------------------------------------------------------------------------
+# stream-K schedule (tiles split between two CTAs, partial parked in y)
+# ---------------------------------------------------------------------------
+
+SK_CASES = [
+    (L("sk_bf16_c64_k64_70", 4, 64, 70, 70, 64, 3, 3, **P(1, 1, 1, 1)), {}),
+    (L("sk_bf16_c64_k300_70", 2, 64, 70, 70, 300, 3, 3, **P(1, 1, 1, 1)), {}),
+    (L("sk_tf32_nchw_c16_k32_99", 2, 16, 99, 99, 32, 3, 3, **P(1, 1, 1, 1), dtype="tf32",
+       layout="NCHW"), {}),
+    (L("sk_bf16_c64_k64_70_epi", 4, 64, 70, 70, 64, 3, 3, **P(1, 1, 1, 1)),
+     dict(alpha=0.5, with_bias=True, relu=True)),
+    (L("sk_bf16_c64_k64_70_ynchw", 4, 64, 70, 70, 64, 3, 3, **P(1, 1, 1, 1)),
+     dict(y_axes="NCHW", with_bias=True)),
+]
+
+
+@pytest.mark.parametrize("layer,kw", SK_CASES, ids=lambda v: v.name if hasattr(v, "name") else "")
+def test_stream_k_parity_full(handle, layer, kw, monkeypatch):
+    monkeypatch.setenv("DLC_TC_STREAMK", "1")
+    run_and_check(handle, layer, 2700 + [c[0] for c in SK_CASES].index(layer), full=True, **kw)
+
+
+def test_stream_k_is_deterministic_and_flags_reset(handle, monkeypatch):
+    """Two launches in a row give bit-identical y (fixed summation order; the
+    split-tile flags are consumed and zeroed by each launch)."""
     import torch
     from deep_learning_convolution_gb300 import api
-    from oracle import oracle
-    layer = L("bf16_nhwc_kcrs", 2, 64, 11, 11, 48, 3, 3, **P(1, 1, 1, 1))
-    x, w, _ = synth.make_inputs(layer, 77)
-    xt, _ = api.layer_tensors(layer, x, w, "cuda")
-    wt = torch.from_numpy(synth.round_to_bf16_bits(w).view(np.int16).reshape(w.shape)).view(
-        torch.bfloat16).cuda()
-    y = torch.full((2, 11, 11, 48), float("nan"), device="cuda")
-    conv = api.Conv2dForward(handle, xt, wt, y, x_axes="NHWC", w_axes="KCRS", y_axes="NHWC",
-                             pads=(1, 1, 1, 1), math="bf16")
-    assert conv.kernel(xt, wt, y) == "tc_gather"
+    monkeypatch.setenv("DLC_TC_STREAMK", "1")
+    layer = SK_CASES[0][0]
+    x, w, _ = synth.make_inputs(layer, 11)
+    xt, wt = api.layer_tensors(layer, x, w, "cuda")
+    conv, y = api.layer_problem(handle, layer, xt, wt)
+    conv(xt, wt, y)
+    y1 = y.clone()
+    y.fill_(float("nan"))
     conv(xt, wt, y)
     torch.cuda.synchronize()
-    ref, bound = oracle.conv2d_fprop(x.astype(np.float64), w.astype(np.float64), pads=(1, 1, 1, 1))
-    got = y.permute(0, 3, 1, 2).double().cpu().numpy()
-    assert (np.abs(got - ref) <= 1e-5 * bound + 1e-6).all()
+    handle.synchronize()
+    assert torch.equal(y1, y)
+    monkeypatch.setenv("DLC_TC_STREAMK", "0")
+    conv(xt, wt, y)
+    torch.cuda.synchronize()
+    # data-parallel schedule sums in another order: equal within the bound only
+    assert torch.allclose(y1, y, rtol=1e-5, atol=1e-4)
+    conv.close()
 
 
 # ---------------------------------------------------------------------------
@@ -148,7 +212,7 @@ def test_random_sweep_parity(handle, layer):
 # epilogue: alpha, beta * y, bias, ReLU, BF16 output, other y layouts
 # ---------------------------------------------------------------------------
 
-EPI_LAYERS = [IM2COL_CASES[0], GATHER_CASES[2], GATHER_CASES[3]]
+EPI_LAYERS = [IM2COL_CASES[0], RUN_CASES[2], RUN_CASES[3], GATHER_CASES[0]]
 
 
 @pytest.mark.parametrize("layer", EPI_LAYERS, ids=lambda l: l.name)
@@ -191,9 +255,10 @@ def test_full_workload_layer_sampled(handle, wl, j):
 def test_workspace_is_zero_and_kernel_choice(handle):
     import torch
     from deep_learning_convolution_gb300 import api
-    expect = {"alexnet": ["tc_gather"] + ["tc_im2col"] * 4,
-              "overfeat": ["tc_gather"] + ["tc_im2col"] * 4,
-              "speech": ["tc_gather", "tc_gather"], "tiny": ["ffma"]}
+    expect = {"alexnet": ["tc_runs"] + ["tc_im2col"] * 4,
+              "overfeat": ["tc_runs"] + ["tc_im2col"] * 4,
+              "resnet50": ["tc_im2col"] * len(synth.WORKLOADS["resnet50"]),
+              "speech": ["tc_runs", "tc_runs"], "tiny": ["ffma"]}
     for wl, kinds in expect.items():
         for layer, kind in zip(synth.WORKLOADS[wl], kinds):
             x, w, _ = synth.make_inputs(layer, 1, batch=1)
