@@ -31,6 +31,7 @@
 // committed and waited for, tensor memory is released.
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cstdlib>
 #include <cstring>
 #include <type_traits>
@@ -69,8 +70,10 @@ struct TcParams {
     int BN, stages, num_kb, c_blocks;
     int n_tiles;
     int b_res;                      // gather modes: all num_kb filter blocks resident in smem
-    int run_len, num_runs;          // run gather: elements per run, number of runs
-    int slot, rpb;                  // run gather: slot elements per run, runs per k-block
+    int run_len, num_runs, cpr;     // run gather: elements per run, runs, 16-byte chunks per run
+    int img_tiles;                  // > 0: image-aligned M tiles, this many per image
+    int halo;                       // run gather stages each tile's input rows in shared memory
+    int halo_bytes;                 // bytes of one halo buffer (two are used)
     int nchw_runs;                  // runs over s of one (c, r) (else over (s, c) of one r)
     long long num_tiles;
     uint32_t idesc, tmem_cols, acc_stride;  // acc_stride: TMEM column offset of accumulator 1
@@ -89,14 +92,28 @@ __device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity, const
 }
 
 struct TileCoord {
-    long long m0;
-    int k0;
+    long long m0;  // first output pixel (flattened n, p, q)
+    int k0;        // first filter
+    int rows;      // valid rows of the tile (<= BM)
 };
 
+// M tiles run over the flattened (n, p, q) pixels, or -- when img_tiles > 0 --
+// image by image (img_tiles tiles per image, the last one ragged), so that a
+// tile never spans two images.
 __device__ __forceinline__ TileCoord tile_coord(const TcParams &p, long long tile) {
     TileCoord tc;
-    tc.m0 = (tile / p.n_tiles) * BM;
+    const long long mt = tile / p.n_tiles;
     tc.k0 = (int)(tile % p.n_tiles) * p.BN;
+    if (p.img_tiles > 0) {
+        const long long n = mt / p.img_tiles;
+        const int t = (int)(mt - n * p.img_tiles);
+        tc.m0 = n * p.PQ + (long long)t * BM;
+        tc.rows = min(BM, p.PQ - t * BM);
+    } else {
+        tc.m0 = mt * BM;
+        const long long left = p.M - tc.m0;
+        tc.rows = left < BM ? (int)left : BM;
+    }
     return tc;
 }
 
@@ -264,150 +281,330 @@ __device__ __forceinline__ void gather_elem_chunk(const TcParams &p, const T *ba
 // Run-gather reduction layout.  A run is a sequence of elements that are
 // contiguous in memory -- the (s, c) elements of one filter row r for
 // channels-innermost activations with KRSC filters, the s elements of one
-// (c, r) pair for width-innermost activations with KCRS filters.  Each
-// 128-byte reduction row of a k-block holds `rpb` runs, each in its own slot
-// of `slot` elements (a whole number of 16-byte chunks); the rest of the row
-// is zero.  Run index j = c*R + r (width-innermost) or r (channels-innermost).
-
-// Streams one run into its slot: elements [e_lo, e_hi) of the run (the rest
-// are zero) are read from `src` (element 0 of the run) with aligned 128-bit
-// loads that each hold at least one requested byte, realigned with selects and
-// funnel shifts, and stored as the slot's `nchunks` swizzled 16-byte chunks
-// starting at chunk `c0` of the row.
-template <typename T>
-__device__ __forceinline__ void stream_run(uint8_t *row, int row_idx, int c0, int nchunks,
-                                           const T *src, int e_lo, int e_hi) {
-    constexpr int EPC = 16 / (int)sizeof(T);
-    const uintptr_t a = reinterpret_cast<uintptr_t>(src);
-    const uintptr_t lo = a + (uintptr_t)e_lo * sizeof(T);   // first requested byte
-    const uintptr_t hi = a + (uintptr_t)e_hi * sizeof(T);   // one past the last
-    const uintptr_t base = a & ~(uintptr_t)15;
-    const int q = (int)((a >> 2) & 3u);                     // word offset inside a vector
-    const int sh = (int)(a & 3u) * 8;                       // byte shift inside a word
-    auto vec = [&](int k, uint32_t (&v)[4]) {
-        const uintptr_t va = base + (uintptr_t)k * 16;
-        if (va < hi && va + 16 > lo) {
-            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(va));
-            v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+// (c, r) pair for width-innermost activations with KCRS filters.  Runs are
+// padded to whole 16-byte chunks (cpr chunks each) and packed one after the
+// other along the reduction; run index = r, or c*R + r.
+struct RunPos {
+    int run, cr, c, r;  // run index, chunk within run, and the run's (c, r)
+    __device__ __forceinline__ void start(const TcParams &p, int g) {
+        run = g / p.cpr;
+        cr = g - run * p.cpr;
+        if (p.nchw_runs) {
+            c = run / p.R;
+            r = run - c * p.R;
         } else {
-            v[0] = v[1] = v[2] = v[3] = 0u;
+            c = 0;
+            r = run;
         }
-    };
-    uint32_t cur[4], nxt[4];
-    vec(0, cur);
-#pragma unroll 1
-    for (int j = 0; j < nchunks; ++j) {
-        vec(j + 1, nxt);
-        uint32_t w[5];
-#pragma unroll
-        for (int i = 0; i < 5; ++i) {  // w[i] = word q+i of cur:nxt
-            const uint32_t c0v = i < 4 ? cur[i] : nxt[i - 4];
-            const uint32_t c1v = i + 1 < 4 ? cur[i + 1] : nxt[i + 1 - 4];
-            const uint32_t c2v = i + 2 < 4 ? cur[i + 2] : nxt[i + 2 - 4];
-            const uint32_t c3v = i + 3 < 4 ? cur[i + 3] : nxt[i + 3 - 4];
-            w[i] = q == 0 ? c0v : (q == 1 ? c1v : (q == 2 ? c2v : c3v));
-        }
-        uint32_t o[4];
-        const int e0 = j * EPC;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            uint32_t v = __funnelshift_r(w[i], w[i + 1], sh);
-            if constexpr (sizeof(T) == 2) {
-                const int el = e0 + 2 * i;
-                const bool lo_ok = el >= e_lo && el < e_hi;
-                const bool hi_ok = el + 1 >= e_lo && el + 1 < e_hi;
-                v &= (lo_ok ? 0x0000FFFFu : 0u) | (hi_ok ? 0xFFFF0000u : 0u);
-            } else {
-                const int el = e0 + i;
-                if (el < e_lo || el >= e_hi) v = 0u;
+    }
+    __device__ __forceinline__ void step(const TcParams &p) {
+        if (++cr == p.cpr) {
+            cr = 0;
+            ++run;
+            if (++r == p.R && p.nchw_runs) {
+                r = 0;
+                ++c;
             }
-            o[i] = v;
         }
-        store_chunk(row, row_idx, c0 + j, o[0], o[1], o[2], o[3]);
+    }
+};
+
+// Loads the chunk of EPC elements that starts at `src`, of which only chunk
+// elements [ja, jb) are requested (0 <= ja < jb <= EPC), as aligned 32-bit
+// words into raw[0..4] (one 128-bit load when the whole chunk is requested and
+// aligned).  A word is loaded only if it holds a requested element, so nothing
+// outside the requested elements' words is touched; *mis is the element
+// misalignment of `src` (BF16 only).  `src` itself may lie outside the tensor
+// when ja > 0.
+template <typename T>
+__device__ __forceinline__ void load_chunk_raw(const T *src, int ja, int jb, uint32_t (&raw)[5],
+                                               int &mis) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(src);
+    constexpr int EPC = 16 / (int)sizeof(T);
+    if (ja == 0 && jb == EPC && (a & 15u) == 0) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a));
+        raw[0] = v.x; raw[1] = v.y; raw[2] = v.z; raw[3] = v.w; raw[4] = 0;
+        mis = 0;
+        return;
+    }
+    if constexpr (sizeof(T) == 2) {
+        mis = (int)((a >> 1) & 1u);
+        const uint32_t *wp = reinterpret_cast<const uint32_t *>(a & ~(uintptr_t)3);
+        // word i holds chunk elements 2i - mis and 2i + 1 - mis
 #pragma unroll
-        for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
+        for (int i = 0; i < 5; ++i) {
+            const bool need = (2 * i - mis < jb) && (2 * i + 1 - mis >= ja);
+            raw[i] = need ? __ldg(wp + i) : 0u;
+        }
+    } else {
+        mis = 0;
+        const uint32_t *wp = reinterpret_cast<const uint32_t *>(a);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) raw[i] = (i >= ja && i < jb) ? __ldg(wp + i) : 0u;
+        raw[4] = 0;
     }
 }
 
-// Fills A row `t` (output pixel m) of reduction block kb in the slot layout.
+// Zeroes chunk elements outside [ja, jb).
+template <typename T>
+__device__ __forceinline__ void mask_chunk(uint32_t (&o)[4], int ja, int jb) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (sizeof(T) == 2) {
+            const bool lo_ok = (2 * i >= ja) && (2 * i < jb);
+            const bool hi_ok = (2 * i + 1 >= ja) && (2 * i + 1 < jb);
+            o[i] &= (lo_ok ? 0x0000FFFFu : 0u) | (hi_ok ? 0xFFFF0000u : 0u);
+        } else {
+            if (i < ja || i >= jb) o[i] = 0u;
+        }
+    }
+}
+
+// Aligns the raw words of load_chunk_raw and zeroes elements outside [ja, jb).
+template <typename T>
+__device__ __forceinline__ void combine_chunk(const uint32_t (&raw)[5], int mis, int ja, int jb,
+                                              uint32_t (&o)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i] = mis ? __funnelshift_r(raw[i], raw[i + 1], 16) : raw[i];
+    mask_chunk<T>(o, ja, jb);
+}
+
+// The 16 bytes starting at byte `off` (0..15) of the 32-byte window v0:v1.
+__device__ __forceinline__ void realign16(const uint4 &v0, const uint4 &v1, int off,
+                                          uint32_t (&o)[4]) {
+    const uint32_t win[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    const int q = off >> 2, sh = (off & 3) * 8;
+    uint32_t w[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i)
+        w[i] = q == 0 ? win[i] : (q == 1 ? win[i + 1] : (q == 2 ? win[i + 2] : win[i + 3]));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i] = __funnelshift_r(w[i], w[i + 1], sh);
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t saddr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(saddr));
+    return v;
+}
+
+// Fills A row `t` (output pixel m) of reduction block kb from global memory.
 // Run elements [e_lo, e_hi) of the row's window lie inside the image along W;
-// filter rows outside [0, H) and rows past the tile are zero.
+// filter rows outside [0, H) are zero.  Every load of the row is issued
+// before the first store.
 template <typename T>
 __device__ __forceinline__ void fill_a_row_runs(const TcParams &p, uint8_t *row, int t, int kb,
                                                 bool valid, const T *xn, int h0, int w0, int e_lo,
                                                 int e_hi) {
     constexpr int EPC = 16 / (int)sizeof(T);
-    const int cps = p.slot / EPC;  // chunks per slot
-    int c0 = 0;
-    for (int ri = 0; ri < p.rpb; ++ri, c0 += cps) {
-        const int run = kb * p.rpb + ri;
-        int c = 0, r = run;
-        if (p.nchw_runs) {
-            c = run / p.R;
-            r = run - c * p.R;
+    RunPos rp;
+    rp.start(p, kb * 8);
+    uint32_t raw[8][5];
+    int mis[8], jas[8], jbs[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        int ja = 0, jb = 0;
+        const T *src = xn;
+        if (valid && rp.run < p.num_runs) {
+            const int h = h0 + rp.r * p.dh;
+            if (h >= 0 && h < p.H) {
+                const int e0 = rp.cr * EPC;
+                const int lo = max(e0, e_lo), hi = min(e0 + EPC, e_hi);
+                if (lo < hi) {
+                    ja = lo - e0;
+                    jb = hi - e0;
+                    src = xn + (long long)h * p.xs[2] +
+                          (p.nchw_runs ? (long long)rp.c * p.xs[1] + w0 : (long long)w0 * p.C) + e0;
+                }
+            }
         }
-        const int h = h0 + r * p.dh;
-        if (valid && run < p.num_runs && h >= 0 && h < p.H && e_lo < e_hi) {
-            const T *src = xn + (long long)h * p.xs[2] +
-                           (p.nchw_runs ? (long long)c * p.xs[1] + w0 : (long long)w0 * p.C);
-            stream_run<T>(row, t, c0, cps, src, e_lo, e_hi);
+        jas[j] = ja;
+        jbs[j] = jb;
+        mis[j] = 0;
+        if (ja < jb) {
+            load_chunk_raw<T>(src, ja, jb, raw[j], mis[j]);
         } else {
-            for (int j = 0; j < cps; ++j) store_chunk(row, t, c0 + j, 0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int i = 0; i < 5; ++i) raw[j][i] = 0u;
         }
+        rp.step(p);
     }
-    for (; c0 < 8; ++c0) store_chunk(row, t, c0, 0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint32_t o[4];
+        combine_chunk<T>(raw[j], mis[j], jas[j], jbs[j], o);
+        store_chunk(row, t, j, o[0], o[1], o[2], o[3]);
+    }
 }
 
-// Fills the BN filter rows of reduction block kb into `dst`, the tasks spread
-// over `nthr` threads (run gather: one task per (row, run); element gather:
-// one task per (row, 16-byte chunk)).
+__device__ __forceinline__ uint32_t lds32(uint32_t saddr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(saddr));
+    return v;
+}
+
+// Fills A row `t` of reduction block kb from the tile's halo: input rows
+// [hr0, hr0 + hrows) of the tile's image, full width, staged at shared byte
+// address `hs` (element (hr0, 0, 0)).  Channels-innermost runs only.  A chunk
+// is read as the 32-bit words that cover it (a BF16 chunk starts 0 or 2 bytes
+// into a word) and shifted into place; only chunks cut by the image border
+// or by the run's end are masked.  The halo buffers are padded so that the
+// words around a chunk stay inside this CTA's shared memory.
+template <typename T>
+__device__ __forceinline__ void fill_a_row_halo(const TcParams &p, uint8_t *row, int t, int kb,
+                                                bool valid, uint32_t hs, int hr0, int hrows,
+                                                int h0, int w0, int e_lo, int e_hi) {
+    constexpr int EPC = 16 / (int)sizeof(T);
+    RunPos rp;
+    rp.start(p, kb * 8);
+    const int rowel = (w0 - 0) * p.C;  // element offset of the window start in a halo row
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint32_t o[4] = {0u, 0u, 0u, 0u};
+        if (valid && rp.run < p.num_runs) {
+            const int hr = h0 + rp.r * p.dh - hr0;
+            if (hr >= 0 && hr < hrows) {  // rows outside the halo are outside the image
+                const int e0 = rp.cr * EPC;
+                const int ja = max(e_lo - e0, 0), jb = min(e_hi - e0, EPC);
+                if (ja < jb) {
+                    const int el = hr * p.W * p.C + rowel + e0;  // may be < 0 when ja > 0
+                    const uint32_t sa = hs + (uint32_t)(el * (int)sizeof(T));
+                    const uint32_t wa = sa & ~3u;
+                    if constexpr (sizeof(T) == 2) {
+                        uint32_t w[5];
+#pragma unroll
+                        for (int i = 0; i < 5; ++i) w[i] = lds32(wa + 4 * i);
+                        const uint32_t sh = (sa & 2u) * 8u;  // 0 or 16
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) o[i] = __funnelshift_r(w[i], w[i + 1], sh);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) o[i] = lds32(wa + 4 * i);
+                    }
+                    if (ja != 0 || jb != EPC) mask_chunk<T>(o, ja, jb);
+                }
+            }
+        }
+        store_chunk(row, t, j, o[0], o[1], o[2], o[3]);
+        rp.step(p);
+    }
+}
+
+// Copies input rows [hr0, hr0 + hrows) of image n (contiguous bytes) into the
+// halo buffer at shared address `dst` with 16-byte cp.async copies of the
+// aligned envelope (each copied 16-byte block holds at least one byte of the
+// rows); returns the shared address of element (hr0, 0, 0).
+template <typename T>
+__device__ __forceinline__ uint32_t halo_copy(const TcParams &p, uint32_t dst, int n, int hr0,
+                                              int hrows, int tid, int nthr) {
+    const uintptr_t src = reinterpret_cast<uintptr_t>(static_cast<const T *>(p.x) +
+                                                      (long long)n * p.xs[0] +
+                                                      (long long)hr0 * p.xs[2]);
+    const uintptr_t a0 = src & ~(uintptr_t)15;
+    if (hrows > 0) {
+        const uintptr_t a1 = (src + (uintptr_t)hrows * p.xs[2] * sizeof(T) + 15) & ~(uintptr_t)15;
+        for (uintptr_t a = a0 + (uintptr_t)tid * 16; a < a1; a += (uintptr_t)nthr * 16)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + (uint32_t)(a - a0)),
+                         "l"(a)
+                         : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    return dst + (uint32_t)(src - a0);
+}
+
+// Input rows of the tile's image that a tile reads: [hr0, hr0 + hrows).
+__device__ __forceinline__ void tile_halo_rows(const TcParams &p, const TileCoord &tc, int &n,
+                                               int &hr0, int &hrows) {
+    n = (int)(tc.m0 / p.PQ);
+    const int ml = (int)(tc.m0 - (long long)n * p.PQ);
+    const int pa = ml / p.Q, pb = (ml + tc.rows - 1) / p.Q;
+    const int lo = max(0, pa * p.u - p.pt);
+    const int hi = min(p.H - 1, pb * p.u - p.pt + p.dh * (p.R - 1));
+    hr0 = lo;
+    hrows = hi >= lo ? hi - lo + 1 : 0;
+}
+
+// Fills the BN filter rows of reduction block kb into `dst`; one task per
+// (row, 16-byte chunk), spread over `nthr` threads, four tasks per thread at a
+// time with all their loads issued first.
 template <typename T, int MODE>
 __device__ void fill_b_block(const TcParams &p, uint8_t *dst, int kb, int k0, int tid, int nthr) {
     constexpr int EPC = 16 / (int)sizeof(T);
+    constexpr int BATCH = 4;
     const T *w = static_cast<const T *>(p.w);
-    if constexpr (MODE == MODE_RUNS) {
-        const int cps = p.slot / EPC;
-        const int tasks = p.BN * 8;  // (row, slot) pairs; slots past rpb fill the row's zeros
-        for (int task = tid; task < tasks; task += nthr) {
-            const int br = task >> 3, ri = task & 7;
-            uint8_t *rowp = dst + br * ROW_BYTES;
-            if (ri >= p.rpb) {
-                for (int cc = ri == p.rpb ? p.rpb * cps : 8; cc < 8; ++cc)
-                    store_chunk(rowp, br, cc, 0u, 0u, 0u, 0u);
-                continue;
-            }
-            const int k = k0 + br;
-            const int run = kb * p.rpb + ri;
-            if (k < p.K && run < p.num_runs) {
-                int c = 0, r = run;
-                if (p.nchw_runs) {
-                    c = run / p.R;
-                    r = run - c * p.R;
+    const int tasks = p.BN * 8;
+    for (int base = tid; base < tasks; base += BATCH * nthr) {
+        uint32_t o[BATCH][4];
+        if constexpr (MODE == MODE_RUNS) {
+            uint32_t raw[BATCH][5];
+            int mis[BATCH], jbs[BATCH];
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) {
+                const int task = base + b * nthr;
+                const int br = task >> 3, j = task & 7;
+                const int k = k0 + br;
+                jbs[b] = 0;
+                mis[b] = 0;
+#pragma unroll
+                for (int i = 0; i < 5; ++i) raw[b][i] = 0u;
+                if (task < tasks && k < p.K) {
+                    RunPos rp;
+                    rp.start(p, kb * 8 + j);
+                    if (rp.run < p.num_runs) {
+                        const int e0 = rp.cr * EPC;
+                        jbs[b] = min(EPC, p.run_len - e0);
+                        const T *src = w + (long long)k * p.ws[0] + (long long)rp.r * p.ws[2] +
+                                       (p.nchw_runs ? (long long)rp.c * p.ws[1] : 0) + e0;
+                        load_chunk_raw<T>(src, 0, jbs[b], raw[b], mis[b]);
+                    }
                 }
-                const T *src = w + (long long)k * p.ws[0] + (long long)r * p.ws[2] +
-                               (p.nchw_runs ? (long long)c * p.ws[1] : 0);
-                stream_run<T>(rowp, br, ri * cps, cps, src, 0, p.run_len);
-            } else {
-                for (int j = 0; j < cps; ++j) store_chunk(rowp, br, ri * cps + j, 0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) combine_chunk<T>(raw[b], mis[b], 0, jbs[b], o[b]);
+        } else {
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) {
+                const int task = base + b * nthr;
+                const int br = task >> 3, j = task & 7;
+                const int k = k0 + br;
+                o[b][0] = o[b][1] = o[b][2] = o[b][3] = 0u;
+                if (task < tasks && k < p.K)
+                    gather_elem_chunk<T, false>(p, w + (long long)k * p.ws[0], true, 0, 0,
+                                                (kb * 8 + j) * EPC, o[b]);
             }
         }
-    } else {
-        const int tasks = p.BN * 8;
-        for (int task = tid; task < tasks; task += nthr) {
-            const int br = task >> 3, j = task & 7;
-            const int k = k0 + br;
-            uint32_t o[4] = {0u, 0u, 0u, 0u};
-            if (k < p.K)
-                gather_elem_chunk<T, false>(p, w + (long long)k * p.ws[0], true, 0, 0,
-                                            (kb * 8 + j) * EPC, o);
-            store_chunk(dst + br * ROW_BYTES, br, j, o[0], o[1], o[2], o[3]);
+#pragma unroll
+        for (int b = 0; b < BATCH; ++b) {
+            const int task = base + b * nthr;
+            if (task < tasks) {
+                const int br = task >> 3, j = task & 7;
+                store_chunk(dst + br * ROW_BYTES, br, j, o[b][0], o[b][1], o[b][2], o[b][3]);
+            }
         }
     }
 }
 
+// Shared byte offset of element (hr0, 0, 0) inside its halo buffer: the copy
+// starts at the 16-byte boundary at or below it.
+template <typename T>
+__device__ __forceinline__ uint32_t halo_align(const TcParams &p, int n, int hr0) {
+    const uintptr_t src = reinterpret_cast<uintptr_t>(static_cast<const T *>(p.x) +
+                                                      (long long)n * p.xs[0] +
+                                                      (long long)hr0 * p.xs[2]);
+    return (uint32_t)(src & 15u);
+}
+
+// Named barrier of all producer threads (id 2).
+template <int GROUPS>
+__device__ __forceinline__ void producer_bar() {
+    asm volatile("bar.sync 2, %0;" ::"n"(128 * GROUPS) : "memory");
+}
+
 template <typename T, int MODE, int GROUPS>
-__device__ void produce_gather(const TcParams &p, uint8_t *smA, uint8_t *smB, uint64_t *full,
-                               uint64_t *empty, uint64_t *bres, const WaitCtl &ctl) {
+__device__ void produce_gather(const TcParams &p, uint8_t *smA, uint8_t *smB, uint8_t *smH,
+                               uint64_t *full, uint64_t *empty, uint64_t *bres, const WaitCtl &ctl) {
     constexpr int EPC = 16 / (int)sizeof(T);
     constexpr int BK = ROW_BYTES / (int)sizeof(T);
     const int group = threadIdx.x >> 7;  // producer warps are 0 .. 4*GROUPS-1
@@ -415,6 +612,8 @@ __device__ void produce_gather(const TcParams &p, uint8_t *smA, uint8_t *smB, ui
     const int ST = p.stages;
     const uint32_t b_stage = (uint32_t)p.BN * ROW_BYTES;
     const T *x = static_cast<const T *>(p.x);
+    const bool halo = MODE == MODE_RUNS && p.halo;
+    const uint32_t hbase = smem_u32(smH);
 
     if (p.b_res) {  // the whole filter tile stays in shared memory
         for (int kb = 0; kb < p.num_kb; ++kb)
@@ -422,14 +621,42 @@ __device__ void produce_gather(const TcParams &p, uint8_t *smA, uint8_t *smB, ui
         fence_proxy_async_smem();
         mbar_arrive(bres);
     }
-    int it = 0;
-    bool ok = true;
     WorkIter wi(p);
     Seg sg;
-    while (ok && wi.next(p, sg)) {
+    if (halo) {  // prefetch the first tile's input rows
+        WorkIter w2 = wi;
+        Seg s2;
+        if (w2.next(p, s2)) {
+            int n, r0, rows;
+            tile_halo_rows(p, tile_coord(p, s2.tile), n, r0, rows);
+            halo_copy<T>(p, hbase, n, r0, rows, threadIdx.x, 128 * GROUPS);
+        }
+    }
+    int it = 0, seq = 0;
+    bool ok = true;
+    // Every producer thread walks every segment (even after an abort) so that
+    // the named barriers below are always reached by all of them.
+    while (wi.next(p, sg)) {
         const TileCoord tc = tile_coord(p, sg.tile);
+        int hn = 0, hr0 = 0, hrows = 0;
+        uint32_t hs = 0;
+        if (halo) {
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            producer_bar<GROUPS>();  // this tile's rows landed; the previous tile is done
+            tile_halo_rows(p, tc, hn, hr0, hrows);
+            hs = hbase + (uint32_t)(seq & 1) * p.halo_bytes + halo_align<T>(p, hn, hr0);
+            WorkIter w2 = wi;  // prefetch the next tile into the other buffer
+            Seg s2;
+            if (w2.next(p, s2)) {
+                int n2, r2, rows2;
+                tile_halo_rows(p, tile_coord(p, s2.tile), n2, r2, rows2);
+                halo_copy<T>(p, hbase + (uint32_t)((seq + 1) & 1) * p.halo_bytes, n2, r2, rows2,
+                             threadIdx.x, 128 * GROUPS);
+            }
+            ++seq;
+        }
         const long long m = tc.m0 + t;
-        const bool valid = m < p.M;
+        const bool valid = t < tc.rows;
         int n = 0, op = 0, oq = 0;
         if (valid) {
             n = (int)(m / p.PQ);
@@ -445,15 +672,19 @@ __device__ void produce_gather(const TcParams &p, uint8_t *smA, uint8_t *smB, ui
         const int e_hi = max(0, min(p.S, p.W - w0)) * run_c;  // <= run_len
         for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
             if (GROUPS > 1 && (it % GROUPS) != group) continue;
+            if (!ok) continue;
             const int stage = it % ST;
             const uint32_t ph = (uint32_t)(it / ST) & 1u;
             if (!mbar_wait(&empty[stage], ph ^ 1u, ctl, 6)) {
                 ok = false;
-                break;
+                continue;
             }
             uint8_t *arow = smA + (size_t)stage * A_STAGE_BYTES + t * ROW_BYTES;
             if constexpr (MODE == MODE_RUNS) {
-                fill_a_row_runs<T>(p, arow, t, kb, valid, xn, h0, w0, e_lo, e_hi);
+                if (halo)
+                    fill_a_row_halo<T>(p, arow, t, kb, valid, hs, hr0, hrows, h0, w0, e_lo, e_hi);
+                else
+                    fill_a_row_runs<T>(p, arow, t, kb, valid, xn, h0, w0, e_lo, e_hi);
             } else {
 #pragma unroll 1
                 for (int j = 0; j < 8; ++j) {
@@ -467,6 +698,7 @@ __device__ void produce_gather(const TcParams &p, uint8_t *smA, uint8_t *smB, ui
             mbar_arrive(&full[stage]);
         }
     }
+    if (halo) asm volatile("cp.async.wait_all;" ::: "memory");  // no copy may outlive the CTA
 }
 
 // ---------------------------------------------------------------------------
@@ -624,7 +856,7 @@ __device__ void epilogue(const TcParams &p, uint32_t tmem_base, uint64_t *tfull,
             have_partial = !*ctl.abort_flag;
         }
         const long long m = tc.m0 + row;
-        const bool valid = m < p.M;
+        const bool valid = row < tc.rows;
         long long ybase = 0;
         if (valid) {
             const int n = (int)(m / p.PQ);
@@ -784,7 +1016,8 @@ __global__ void __launch_bounds__(KernelShape<MODE>::THREADS, 1)
     const int b_blocks = p.b_res ? p.num_kb : ST;
     uint8_t *smA = smem;
     uint8_t *smB = smem + (size_t)ST * A_STAGE_BYTES;
-    uint8_t *epi_smem = smB + (size_t)b_blocks * p.BN * ROW_BYTES;  // 1024-aligned
+    uint8_t *smH = smB + (size_t)b_blocks * p.BN * ROW_BYTES;  // halo buffers (run gather)
+    uint8_t *epi_smem = smH + (p.halo ? 2 * (size_t)p.halo_bytes : 0);
     uint64_t *bars = reinterpret_cast<uint64_t *>(epi_smem + (p.y_tma ? EPI_SMEM : 0));
     uint64_t *full = bars;
     uint64_t *empty = bars + ST;
@@ -828,7 +1061,7 @@ __global__ void __launch_bounds__(KernelShape<MODE>::THREADS, 1)
         if constexpr (MODE == MODE_IM2COL) {
             if (lane == 0) produce_tma<BK>(p, &tmA, &tmB, smA, smB, full, empty, ctl);
         } else {
-            produce_gather<T, MODE, GATHER_GROUPS>(p, smA, smB, full, empty, bres, ctl);
+            produce_gather<T, MODE, GATHER_GROUPS>(p, smA, smB, smH, full, empty, bres, ctl);
         }
     } else if (warp == MMA_WARP) {
         if (lane == 0)
@@ -914,9 +1147,7 @@ bool runs_ok(const ConvProblem &pb, int *run_len, int *num_runs, int *nchw) {
     } else {
         return false;
     }
-    const long long epc = 16 / (pb.xdt == DLC_DATA_BFLOAT16 ? 2 : 4);
-    if (((len + epc - 1) / epc) * epc > ROW_BYTES / (16 / epc)) return false;  // one run per row at most
-    if (runs > 0x3fffffffLL) return false;
+    if (len > 4096 || runs * (len + 8) > 0x3fffffffLL) return false;
     *run_len = (int)len;
     *num_runs = (int)runs;
     return true;
@@ -1015,16 +1246,38 @@ dlcStatus_t dlc_launch_tc(dlcContext *ctx, const ConvProblem &pb, dlcKernel_t va
         tp.num_kb = pb.R * pb.S * tp.c_blocks;
     } else if (mode == MODE_RUNS) {
         if (!runs_ok(pb, &tp.run_len, &tp.num_runs, &tp.nchw_runs)) return DLC_STATUS_INTERNAL_ERROR;
-        tp.slot = ((tp.run_len + EPC - 1) / EPC) * EPC;
-        tp.rpb = BK / tp.slot;
-        tp.num_kb = (tp.num_runs + tp.rpb - 1) / tp.rpb;
+        tp.cpr = (tp.run_len + EPC - 1) / EPC;
+        const long long chunks = (long long)tp.num_runs * tp.cpr;
+        tp.num_kb = (int)((chunks + 7) / 8);
     } else {
         const long long kg = (long long)pb.R * pb.S * pb.C;
         if (kg > 0x3fffffffLL) return DLC_STATUS_NOT_SUPPORTED;
         tp.num_kb = (int)((kg + BK - 1) / BK);
     }
     tp.n_tiles = (pb.K + tp.BN - 1) / tp.BN;
-    const long long m_tiles = (tp.M + BM - 1) / BM;
+    // Halo staging (run gather, channels-innermost, dense rows): M tiles are
+    // image-aligned and each tile's input rows are staged in shared memory.
+    long long halo_rows = 0;
+    if (mode == MODE_RUNS && !tp.nchw_runs && pb.xs[2] == (long long)pb.W * pb.C) {
+        const int it_img = (tp.PQ + BM - 1) / BM;
+        for (int t = 0; t < it_img; ++t) {
+            const int ml = t * BM, rows = std::min(BM, tp.PQ - ml);
+            const int pa = ml / pb.Q, pbb = (ml + rows - 1) / pb.Q;
+            const int lo = std::max(0, pa * pb.u - pb.pt);
+            const int hi = std::min(pb.H - 1, pbb * pb.u - pb.pt + pb.dh * (pb.R - 1));
+            halo_rows = std::max<long long>(halo_rows, hi >= lo ? hi - lo + 1 : 0);
+        }
+        const long long hb = ((halo_rows * pb.xs[2] * e + 16 + 127) / 128) * 128 + 128;
+        if (hb <= 48 * 1024) {
+            tp.halo = 1;
+            tp.halo_bytes = (int)hb;
+            tp.img_tiles = it_img;
+        }
+        if (const char *ev = std::getenv("DLC_TC_HALO"))
+            if (std::atoi(ev) == 0) tp.halo = 0, tp.halo_bytes = 0, tp.img_tiles = 0;
+    }
+    const long long m_tiles =
+        tp.img_tiles > 0 ? (long long)pb.N * tp.img_tiles : (tp.M + BM - 1) / BM;
     tp.num_tiles = m_tiles * tp.n_tiles;
 
     // shared memory: A stages plus either B stages or the resident filter
@@ -1032,9 +1285,11 @@ dlcStatus_t dlc_launch_tc(dlcContext *ctx, const ConvProblem &pb, dlcKernel_t va
     // Bulk-tensor stores of y measured slower than direct stores from the
     // epilogue registers (small per-warp boxes), so they are opt-in.
     tp.y_tma = 0;
-    if (const char *ev = std::getenv("DLC_TC_YTMA")) tp.y_tma = y_tma_ok(pb) && std::atoi(ev) != 0;
+    if (const char *ev = std::getenv("DLC_TC_YTMA"))
+        tp.y_tma = y_tma_ok(pb) && tp.img_tiles == 0 && std::atoi(ev) != 0;
     const int b_stage = tp.BN * ROW_BYTES;
-    const int budget = MAX_DYN_SMEM - 1024 - BAR_AREA - (tp.y_tma ? EPI_SMEM : 0);
+    const int budget = MAX_DYN_SMEM - 1024 - BAR_AREA - (tp.y_tma ? EPI_SMEM : 0) -
+                       (tp.halo ? 2 * tp.halo_bytes : 0);
     const long long b_all = (long long)tp.num_kb * b_stage;
     tp.b_res = (mode != MODE_IM2COL && tp.n_tiles == 1 && b_all <= 120 * 1024 &&
                 budget - b_all >= 4 * A_STAGE_BYTES) ? 1 : 0;
@@ -1048,10 +1303,9 @@ dlcStatus_t dlc_launch_tc(dlcContext *ctx, const ConvProblem &pb, dlcKernel_t va
     if (tp.stages < 2) return DLC_STATUS_INTERNAL_ERROR;
     const long long b_bytes = tp.b_res ? b_all : (long long)tp.stages * b_stage;
 
-    // Stream-K when whole tiles would leave the last round badly filled: equal
-    // (tile, k-block) ranges per CTA, at most two parts per tile (units per CTA
-    // >= k-blocks per tile because tiles >= CTAs).  The partial is parked in y,
-    // so it needs FP32 y and beta == 0.
+    // Stream-K: equal (tile, k-block) ranges per CTA, at most two parts per
+    // tile (units per CTA >= k-blocks per tile because tiles >= CTAs).  The
+    // partial is parked in y, so it needs FP32 y and beta == 0.
     long long grid = tp.num_tiles < ctx->sm_count ? tp.num_tiles : ctx->sm_count;
     tp.sk = 0;
     tp.sk_units = 0;
@@ -1060,9 +1314,9 @@ dlcStatus_t dlc_launch_tc(dlcContext *ctx, const ConvProblem &pb, dlcKernel_t va
                           tp.num_tiles >= ctx->sm_count && tp.num_tiles <= DLC_SK_FLAGS &&
                           tp.num_kb >= 4;
     if (sk_legal) {
-        const long long rounds = (tp.num_tiles + ctx->sm_count - 1) / ctx->sm_count;
-        const double fill = (double)tp.num_tiles / (double)(rounds * ctx->sm_count);
-        tp.sk = (rounds <= 3 && fill < 0.8 && tp.num_kb >= 16) ? 1 : 0;
+        // Measured no faster than whole tiles on the small-image layers (the
+        // parked partial costs an extra pass over the split tiles), so the
+        // stream-K schedule is opt-in: DLC_TC_STREAMK=1.
         if (const char *ev = std::getenv("DLC_TC_STREAMK")) tp.sk = std::atoi(ev) != 0;
     }
     if (tp.sk) {
@@ -1129,7 +1383,8 @@ dlcStatus_t dlc_launch_tc(dlcContext *ctx, const ConvProblem &pb, dlcKernel_t va
     }
 
     const size_t smem = 1024 + (size_t)tp.stages * A_STAGE_BYTES + (size_t)b_bytes +
-                        (tp.y_tma ? EPI_SMEM : 0) + BAR_AREA;
+                        (tp.halo ? 2 * (size_t)tp.halo_bytes : 0) + (tp.y_tma ? EPI_SMEM : 0) +
+                        BAR_AREA;
     if (grid < 1) grid = 1;
     cudaError_t err = tf32 ? launch_mode<true>(mode, tp, ta, tb, ty, (int)grid, smem, ctx->stream)
                            : launch_mode<false>(mode, tp, ta, tb, ty, (int)grid, smem, ctx->stream);
