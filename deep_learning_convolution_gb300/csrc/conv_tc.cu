@@ -74,6 +74,8 @@ struct TcParams {
     int img_tiles;                  // > 0: image-aligned M tiles, this many per image
     int halo;                       // run gather stages each tile's input rows in shared memory
     int halo_bytes;                 // bytes of one halo buffer (two are used)
+    int ctab;                       // run gather: per-(k-block, chunk) table in shared memory
+    int epc;                        // elements per 16-byte chunk
     int nchw_runs;                  // runs over s of one (c, r) (else over (s, c) of one r)
     long long num_tiles;
     uint32_t idesc, tmem_cols, acc_stride;  // acc_stride: TMEM column offset of accumulator 1
@@ -455,40 +457,57 @@ __device__ __forceinline__ uint32_t lds32(uint32_t saddr) {
 template <typename T>
 __device__ __forceinline__ void fill_a_row_halo(const TcParams &p, uint8_t *row, int t, int kb,
                                                 bool valid, uint32_t hs, int hr0, int hrows,
-                                                int h0, int w0, int e_lo, int e_hi) {
+                                                int h0, int w0, int e_lo, int e_hi,
+                                                const int4 *ctab) {
     constexpr int EPC = 16 / (int)sizeof(T);
-    RunPos rp;
-    rp.start(p, kb * 8);
-    const int rowel = (w0 - 0) * p.C;  // element offset of the window start in a halo row
+    const int WC = p.W * p.C;
+    const int hb = h0 - hr0;                  // halo row of filter row 0
+    const int base = hb * WC + w0 * p.C;      // halo element of (filter row 0, s = 0, c = 0)
+    const int4 *tb = ctab + kb * 8;
+    uint32_t o[8][4];
+    // all shared loads of the row first (the stores below are compiler
+    // barriers), then the stores
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        uint32_t o[4] = {0u, 0u, 0u, 0u};
-        if (valid && rp.run < p.num_runs) {
-            const int hr = h0 + rp.r * p.dh - hr0;
-            if (hr >= 0 && hr < hrows) {  // rows outside the halo are outside the image
-                const int e0 = rp.cr * EPC;
-                const int ja = max(e_lo - e0, 0), jb = min(e_hi - e0, EPC);
-                if (ja < jb) {
-                    const int el = hr * p.W * p.C + rowel + e0;  // may be < 0 when ja > 0
-                    const uint32_t sa = hs + (uint32_t)(el * (int)sizeof(T));
-                    const uint32_t wa = sa & ~3u;
-                    if constexpr (sizeof(T) == 2) {
-                        uint32_t w[5];
+        o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0u;
+        const int4 e = tb[j];  // (filter row r, channel c, element offset e0, in range)
+        const int hr = hb + e.x * p.dh;
+        if (valid && e.w && (unsigned)hr < (unsigned)hrows) {  // rows off the halo are padding
+            const int ja = max(e_lo - e.z, 0), jb = min(e_hi - e.z, EPC);
+            if (ja < jb) {
+                const int el = base + e.x * p.dh * WC + e.z;  // may be < 0 when ja > 0
+                const uint32_t sa = hs + (uint32_t)(el * (int)sizeof(T));
+                const uint32_t wa = sa & ~3u;
+                if constexpr (sizeof(T) == 2) {
+                    uint32_t w[5];
 #pragma unroll
-                        for (int i = 0; i < 5; ++i) w[i] = lds32(wa + 4 * i);
-                        const uint32_t sh = (sa & 2u) * 8u;  // 0 or 16
+                    for (int i = 0; i < 5; ++i) w[i] = lds32(wa + 4 * i);
+                    const uint32_t sh = (sa & 2u) * 8u;  // 0 or 16
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) o[i] = __funnelshift_r(w[i], w[i + 1], sh);
-                    } else {
+                    for (int i = 0; i < 4; ++i) o[j][i] = __funnelshift_r(w[i], w[i + 1], sh);
+                } else {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) o[i] = lds32(wa + 4 * i);
-                    }
-                    if (ja != 0 || jb != EPC) mask_chunk<T>(o, ja, jb);
+                    for (int i = 0; i < 4; ++i) o[j][i] = lds32(wa + 4 * i);
                 }
+                if ((ja | (jb - EPC)) != 0) mask_chunk<T>(o[j], ja, jb);
             }
         }
-        store_chunk(row, t, j, o[0], o[1], o[2], o[3]);
-        rp.step(p);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) store_chunk(row, t, j, o[j][0], o[j][1], o[j][2], o[j][3]);
+}
+
+// The per-(k-block, chunk) table of the run layout: filter row, channel,
+// element offset inside the run, and whether the chunk holds a run at all.
+template <int GROUPS>
+__device__ void build_chunk_table(const TcParams &p, int4 *tab) {
+    constexpr int EPC_BF16 = 8;
+    (void)EPC_BF16;
+    const int epc = p.epc;
+    for (int i = threadIdx.x; i < p.num_kb * 8; i += 128 * GROUPS) {
+        RunPos rp;
+        rp.start(p, i);
+        tab[i] = make_int4(rp.r, rp.c, rp.cr * epc, rp.run < p.num_runs ? 1 : 0);
     }
 }
 
@@ -604,7 +623,8 @@ __device__ __forceinline__ void producer_bar() {
 
 template <typename T, int MODE, int GROUPS>
 __device__ void produce_gather(const TcParams &p, uint8_t *smA, uint8_t *smB, uint8_t *smH,
-                               uint64_t *full, uint64_t *empty, uint64_t *bres, const WaitCtl &ctl) {
+                               int4 *ctab, uint64_t *full, uint64_t *empty, uint64_t *bres,
+                               const WaitCtl &ctl) {
     constexpr int EPC = 16 / (int)sizeof(T);
     constexpr int BK = ROW_BYTES / (int)sizeof(T);
     const int group = threadIdx.x >> 7;  // producer warps are 0 .. 4*GROUPS-1
@@ -620,6 +640,10 @@ __device__ void produce_gather(const TcParams &p, uint8_t *smA, uint8_t *smB, ui
             fill_b_block<T, MODE>(p, smB + (size_t)kb * b_stage, kb, 0, threadIdx.x, 128 * GROUPS);
         fence_proxy_async_smem();
         mbar_arrive(bres);
+    }
+    if (MODE == MODE_RUNS && p.ctab) {
+        build_chunk_table<GROUPS>(p, ctab);
+        producer_bar<GROUPS>();
     }
     WorkIter wi(p);
     Seg sg;
@@ -682,7 +706,8 @@ __device__ void produce_gather(const TcParams &p, uint8_t *smA, uint8_t *smB, ui
             uint8_t *arow = smA + (size_t)stage * A_STAGE_BYTES + t * ROW_BYTES;
             if constexpr (MODE == MODE_RUNS) {
                 if (halo)
-                    fill_a_row_halo<T>(p, arow, t, kb, valid, hs, hr0, hrows, h0, w0, e_lo, e_hi);
+                    fill_a_row_halo<T>(p, arow, t, kb, valid, hs, hr0, hrows, h0, w0, e_lo, e_hi,
+                                       ctab);
                 else
                     fill_a_row_runs<T>(p, arow, t, kb, valid, xn, h0, w0, e_lo, e_hi);
             } else {
@@ -1017,7 +1042,8 @@ __global__ void __launch_bounds__(KernelShape<MODE>::THREADS, 1)
     uint8_t *smA = smem;
     uint8_t *smB = smem + (size_t)ST * A_STAGE_BYTES;
     uint8_t *smH = smB + (size_t)b_blocks * p.BN * ROW_BYTES;  // halo buffers (run gather)
-    uint8_t *epi_smem = smH + (p.halo ? 2 * (size_t)p.halo_bytes : 0);
+    int4 *ctab = reinterpret_cast<int4 *>(smH + (p.halo ? 2 * (size_t)p.halo_bytes : 0));
+    uint8_t *epi_smem = reinterpret_cast<uint8_t *>(ctab) + (p.ctab ? (size_t)p.num_kb * 8 * 16 : 0);
     uint64_t *bars = reinterpret_cast<uint64_t *>(epi_smem + (p.y_tma ? EPI_SMEM : 0));
     uint64_t *full = bars;
     uint64_t *empty = bars + ST;
@@ -1061,7 +1087,7 @@ __global__ void __launch_bounds__(KernelShape<MODE>::THREADS, 1)
         if constexpr (MODE == MODE_IM2COL) {
             if (lane == 0) produce_tma<BK>(p, &tmA, &tmB, smA, smB, full, empty, ctl);
         } else {
-            produce_gather<T, MODE, GATHER_GROUPS>(p, smA, smB, smH, full, empty, bres, ctl);
+            produce_gather<T, MODE, GATHER_GROUPS>(p, smA, smB, smH, ctab, full, empty, bres, ctl);
         }
     } else if (warp == MMA_WARP) {
         if (lane == 0)
@@ -1276,6 +1302,9 @@ dlcStatus_t dlc_launch_tc(dlcContext *ctx, const ConvProblem &pb, dlcKernel_t va
         if (const char *ev = std::getenv("DLC_TC_HALO"))
             if (std::atoi(ev) == 0) tp.halo = 0, tp.halo_bytes = 0, tp.img_tiles = 0;
     }
+    tp.epc = EPC;
+    tp.ctab = (tp.halo && tp.num_kb * 8 * 16 <= 16 * 1024) ? 1 : 0;
+    if (tp.halo && !tp.ctab) tp.halo = 0, tp.halo_bytes = 0, tp.img_tiles = 0;
     const long long m_tiles =
         tp.img_tiles > 0 ? (long long)pb.N * tp.img_tiles : (tp.M + BM - 1) / BM;
     tp.num_tiles = m_tiles * tp.n_tiles;
@@ -1288,8 +1317,9 @@ dlcStatus_t dlc_launch_tc(dlcContext *ctx, const ConvProblem &pb, dlcKernel_t va
     if (const char *ev = std::getenv("DLC_TC_YTMA"))
         tp.y_tma = y_tma_ok(pb) && tp.img_tiles == 0 && std::atoi(ev) != 0;
     const int b_stage = tp.BN * ROW_BYTES;
+    const int ctab_bytes = tp.ctab ? tp.num_kb * 8 * 16 : 0;
     const int budget = MAX_DYN_SMEM - 1024 - BAR_AREA - (tp.y_tma ? EPI_SMEM : 0) -
-                       (tp.halo ? 2 * tp.halo_bytes : 0);
+                       (tp.halo ? 2 * tp.halo_bytes : 0) - ctab_bytes;
     const long long b_all = (long long)tp.num_kb * b_stage;
     tp.b_res = (mode != MODE_IM2COL && tp.n_tiles == 1 && b_all <= 120 * 1024 &&
                 budget - b_all >= 4 * A_STAGE_BYTES) ? 1 : 0;
@@ -1383,8 +1413,8 @@ dlcStatus_t dlc_launch_tc(dlcContext *ctx, const ConvProblem &pb, dlcKernel_t va
     }
 
     const size_t smem = 1024 + (size_t)tp.stages * A_STAGE_BYTES + (size_t)b_bytes +
-                        (tp.halo ? 2 * (size_t)tp.halo_bytes : 0) + (tp.y_tma ? EPI_SMEM : 0) +
-                        BAR_AREA;
+                        (tp.halo ? 2 * (size_t)tp.halo_bytes : 0) + ctab_bytes +
+                        (tp.y_tma ? EPI_SMEM : 0) + BAR_AREA;
     if (grid < 1) grid = 1;
     cudaError_t err = tf32 ? launch_mode<true>(mode, tp, ta, tb, ty, (int)grid, smem, ctx->stream)
                            : launch_mode<false>(mode, tp, ta, tb, ty, (int)grid, smem, ctx->stream);
