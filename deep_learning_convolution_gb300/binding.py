@@ -86,6 +86,8 @@ SIGNATURES = {
     "dlcConvolutionBiasActivationForward": [_h, _pf, _h, c_void_p, _h, c_void_p, _h, _pf,
                                             c_void_p, c_int, _h, c_void_p],
     "dlcDebugWaitTimeoutSelfTest": [_h, c_int],
+    "dlcConvolutionForwardNoAlloc": [c_void_p, _pf, _h, c_void_p, _h, c_void_p, _h, _pf, _h,
+                                     c_void_p, c_void_p],
 }
 _RESTYPES = {"dlcGetErrorString": c_char_p}
 
@@ -292,3 +294,11 @@ def dlcConvolutionBiasActivationForward(handle, alpha, x_desc, x_ptr, w_desc, w_
 
 def dlcDebugWaitTimeoutSelfTest(handle, timeout_us: int):
     _call("dlcDebugWaitTimeoutSelfTest", handle, timeout_us)
+
+
+def dlcConvolutionForwardNoAlloc(stream_ptr, alpha, x_desc, x_ptr, w_desc, w_ptr, conv, beta,
+                                 y_desc, y_ptr, status_ptr=0):
+    a, b = c_float(alpha), c_float(beta)
+    _call("dlcConvolutionForwardNoAlloc", c_void_p(stream_ptr or None), byref(a), x_desc,
+          c_void_p(x_ptr), w_desc, c_void_p(w_ptr), conv, byref(b), y_desc, c_void_p(y_ptr),
+          c_void_p(status_ptr or None))

@@ -6,9 +6,16 @@
 #include <algorithm>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "internal.h"
+
+// Scratch of dlcConvolutionForwardNoAlloc: DLC_NOALLOC_MAX_TILES split-tile
+// flags followed by two error words.  Device code never names it; host code
+// passes its device address, looked up once per device.
+static __device__ __align__(256) int dlc_noalloc_scratch[DLC_NOALLOC_MAX_TILES + 64];
+static_assert(DLC_NOALLOC_MAX_TILES == DLC_SK_FLAGS, "one flag per split-capable tile");
 
 namespace {
 
@@ -495,6 +502,95 @@ dlcStatus_t dlcConvolutionBiasActivationForward(dlcHandle_t h, const float *alph
                                                 dlcTensorDescriptor_t yd, void *y) {
     if (act != DLC_ACTIVATION_IDENTITY && act != DLC_ACTIVATION_RELU) return DLC_STATUS_BAD_PARAM;
     return forward(h, alpha, xd, x, wd, w, cd, beta, bias, act == DLC_ACTIVATION_RELU, yd, y);
+}
+
+// Per-device set-up of the allocation-free entry point: the scratch array's
+// device address (cudaGetSymbolAddress with the device current), the SM count
+// and the tensor-map encoders.  Done by the first call on each device.
+namespace {
+struct NoAllocDevice {
+    int ready = 0;
+    int *scratch = nullptr;
+    int sm_count = 0;
+    EncodeTiledFn encode_tiled = nullptr;
+    EncodeIm2colFn encode_im2col = nullptr;
+};
+constexpr int kNoAllocMaxDevices = 64;
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+std::mutex g_noalloc_mu;
+
+dlcStatus_t noalloc_setup(int dev, NoAllocDevice **out) {
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return DLC_STATUS_NOT_SUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    NoAllocDevice &d = g_noalloc_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return DLC_STATUS_EXECUTION_FAILED;
+        if (major != 10 || minor != 3) return DLC_STATUS_NOT_SUPPORTED;
+        int *ptr = nullptr;
+        if (cudaGetSymbolAddress((void **)&ptr, dlc_noalloc_scratch) != cudaSuccess || !ptr)
+            return DLC_STATUS_EXECUTION_FAILED;
+        cudaDriverEntryPointQueryResult q1, q2;
+        void *f1 = nullptr, *f2 = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f1, 12000, cudaEnableDefault,
+                                             &q1) != cudaSuccess ||
+            q1 != cudaDriverEntryPointSuccess ||
+            cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &f2, 12000,
+                                             cudaEnableDefault, &q2) != cudaSuccess ||
+            q2 != cudaDriverEntryPointSuccess)
+            return DLC_STATUS_EXECUTION_FAILED;
+        d.scratch = ptr;
+        d.sm_count = sms;
+        d.encode_tiled = reinterpret_cast<EncodeTiledFn>(f1);
+        d.encode_im2col = reinterpret_cast<EncodeIm2colFn>(f2);
+        d.ready = 1;
+    }
+    *out = &d;
+    return DLC_STATUS_SUCCESS;
+}
+}  // namespace
+
+dlcStatus_t dlcConvolutionForwardNoAlloc(void *stream, const float *alpha,
+                                         dlcTensorDescriptor_t xd, const void *x,
+                                         dlcFilterDescriptor_t wd, const void *w,
+                                         dlcConvolutionDescriptor_t cd, const float *beta,
+                                         dlcTensorDescriptor_t yd, void *y, int *status) {
+    if (!alpha || !beta) return DLC_STATUS_BAD_PARAM;
+    if ((uintptr_t)status % sizeof(int)) return DLC_STATUS_BAD_PARAM;
+    ConvProblem pb;
+    dlcStatus_t st = resolve(xd, x, wd, w, cd, yd, y, true, pb);
+    if (st != DLC_STATUS_SUCCESS) return st;
+    pb.alpha = *alpha;
+    pb.beta = *beta;
+    if (pb.math == DLC_MATH_FP32) return DLC_STATUS_NOT_SUPPORTED;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DLC_STATUS_EXECUTION_FAILED;
+    NoAllocDevice *nd = nullptr;
+    st = noalloc_setup(dev, &nd);
+    if (st != DLC_STATUS_SUCCESS) return st;
+
+    // A context on the stack: no handle, no allocation.
+    dlcContext ctx;
+    ctx.device = dev;
+    ctx.sm_count = nd->sm_count;
+    ctx.stream = static_cast<cudaStream_t>(stream);
+    ctx.h_err = nullptr;
+    ctx.d_err = status ? status : nd->scratch + DLC_NOALLOC_MAX_TILES;
+    ctx.sk_flags = nd->scratch;
+    ctx.force_sk = 1;
+    ctx.encode_tiled = nd->encode_tiled;
+    ctx.encode_im2col = nd->encode_im2col;
+    const dlcKernel_t k = dlc_tc_variant(&ctx, pb);
+    if (k == DLC_KERNEL_NONE || k == DLC_KERNEL_FFMA) return DLC_STATUS_NOT_SUPPORTED;
+    // the flags and the error words start at zero on every call
+    if (cudaMemsetAsync(nd->scratch, 0, (DLC_NOALLOC_MAX_TILES + 2) * sizeof(int), ctx.stream) !=
+            cudaSuccess ||
+        (status && cudaMemsetAsync(status, 0, 2 * sizeof(int), ctx.stream) != cudaSuccess))
+        return DLC_STATUS_EXECUTION_FAILED;
+    return dlc_launch_tc(&ctx, pb, k);
 }
 
 dlcStatus_t dlcDebugWaitTimeoutSelfTest(dlcHandle_t h, int timeout_us) {

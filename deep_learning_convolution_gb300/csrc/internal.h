@@ -47,6 +47,7 @@ struct dlcContext {
     uint64_t launches = 0;
     unsigned long long timeout_ns = 2000000000ull;  // pipeline wait limit
     int *sk_flags = nullptr;  // DLC_SK_FLAGS per-tile flags of split tiles (zero between launches)
+    int force_sk = 0;         // use the stream-K schedule whenever it is legal
     EncodeTiledFn encode_tiled = nullptr;
     EncodeIm2colFn encode_im2col = nullptr;
 };
@@ -79,3 +80,4 @@ dlcStatus_t dlc_launch_ffma(dlcContext *ctx, const ConvProblem &pb);
 dlcKernel_t dlc_tc_variant(const dlcContext *ctx, const ConvProblem &pb);
 dlcStatus_t dlc_launch_tc(dlcContext *ctx, const ConvProblem &pb, dlcKernel_t variant);
 dlcStatus_t dlc_launch_wait_selftest(dlcContext *ctx, unsigned long long timeout_ns);
+

@@ -263,6 +263,51 @@ dlcStatus_t dlcConvolutionBiasActivationForward(dlcHandle_t handle, const float 
  * tests of the error path. */
 dlcStatus_t dlcDebugWaitTimeoutSelfTest(dlcHandle_t handle, int timeout_us);
 
+/* ---- forward convolution that allocates nothing ---------------------------
+ *
+ * No counterpart on the pages: this is a service for callers that may not
+ * allocate memory after start-up -- for example a serving process whose
+ * memory is reserved once at start-up, or a plug-in inside a framework that
+ * owns all device memory through its own allocator.  Such callers cannot
+ * create a handle (dlcCreate allocates its error word and split-tile flags).
+ *
+ * dlcConvolutionForwardNoAlloc computes y = alpha * conv(x, w) + beta * y like
+ * dlcConvolutionForward, with tensor-core math only (TF32 or BF16; FP32 math
+ * returns NOT_SUPPORTED), launched on `stream` (a cudaStream_t as void*,
+ * NULL = legacy default stream) of the current device.  It allocates no host
+ * or device memory and calls no allocating routine.  Besides x, w, y and
+ * `status` it uses only a fixed scratch array compiled into the library
+ * (DLC_NOALLOC_MAX_TILES split-tile flags and two error words); every GPU that
+ * loads the library holds that array until the process exits.
+ *
+ * The tile schedule is stream-K whenever it is legal (beta == 0, FLOAT y, at
+ * least one tile per SM): the CTAs of a launch meet through the scratch
+ * flags.  Problems with more than DLC_NOALLOC_MAX_TILES output tiles (128
+ * pixels x up to 256 filters each) are rejected with NOT_SUPPORTED, and so is
+ * any problem the library cannot run on its tensor-core kernel.
+ *
+ * The first call on a device sets that device up (it looks up the scratch
+ * array's device address and the tensor-map encoders); make that first call
+ * before any stream capture.  Every call reuses the same scratch array and
+ * clears its flags on `stream` before launching, so calls whose work overlaps
+ * on the GPU (other streams, other host threads) race with each other: issue
+ * them one at a time.
+ *
+ * status: NULL, or a device-accessible array of two ints owned by the caller;
+ *   the call zeroes it on `stream`, and a kernel that gives up on a pipeline
+ *   wait writes dlcDeviceError_t code and detail there.  With NULL such an
+ *   error goes to the scratch array and is not reported.
+ * Errors: BAD_PARAM / NOT_SUPPORTED as for dlcConvolutionForward, plus the
+ * above; EXECUTION_FAILED if the set-up or the launch fails.
+ */
+#define DLC_NOALLOC_MAX_TILES 4096
+
+dlcStatus_t dlcConvolutionForwardNoAlloc(void *stream, const float *alpha,
+                                         dlcTensorDescriptor_t xDesc, const void *x,
+                                         dlcFilterDescriptor_t wDesc, const void *w,
+                                         dlcConvolutionDescriptor_t conv, const float *beta,
+                                         dlcTensorDescriptor_t yDesc, void *y, int *status);
+
 #ifdef __cplusplus
 }
 #endif
