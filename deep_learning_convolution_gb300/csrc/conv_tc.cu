@@ -169,7 +169,8 @@ __device__ void produce_tma(const TcParams &p, const CUtensorMap *tmA, const CUt
     const int ST = p.stages;
     const uint32_t b_stage = (uint32_t)p.BN * ROW_BYTES;
     const uint32_t tx = A_STAGE_BYTES + b_stage;
-    int it = 0;
+    int it = 0, stage = 0;
+    uint32_t ph = 0;
     bool ok = true;
     WorkIter wi(p);
     Seg sg;
@@ -185,8 +186,6 @@ __device__ void produce_tma(const TcParams &p, const CUtensorMap *tmA, const CUt
         const int rs = sg.kb0 / p.c_blocks;
         int s = rs % p.S, r = rs / p.S;
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-            const int stage = it % ST;
-            const uint32_t ph = (uint32_t)(it / ST) & 1u;
             if (!mbar_wait(&empty[stage], ph ^ 1u, ctl, 1)) {
                 ok = false;
                 break;
@@ -196,6 +195,10 @@ __device__ void produce_tma(const TcParams &p, const CUtensorMap *tmA, const CUt
                                hc, n0, (uint16_t)(s * p.dw), (uint16_t)(r * p.dh));
             tma_load_4d(smB + (size_t)stage * b_stage, tmB, &full[stage], cb * BK, s, r, tc.k0);
             ++it;
+            if (++stage == ST) {
+                stage = 0;
+                ph ^= 1u;
+            }
             if (++cb == p.c_blocks) {
                 cb = 0;
                 if (++s == p.S) {
@@ -656,7 +659,8 @@ __device__ void produce_gather(const TcParams &p, uint8_t *smA, uint8_t *smB, ui
             halo_copy<T>(p, hbase, n, r0, rows, threadIdx.x, 128 * GROUPS);
         }
     }
-    int it = 0, seq = 0;
+    int it = 0, seq = 0, stage = 0;
+    uint32_t ph = 0;
     bool ok = true;
     // Every producer thread walks every segment (even after an abort) so that
     // the named barriers below are always reached by all of them.
@@ -694,16 +698,23 @@ __device__ void produce_gather(const TcParams &p, uint8_t *smA, uint8_t *smB, ui
         const int run_c = p.nchw_runs ? 1 : p.C;
         const int e_lo = max(0, -w0) * run_c;
         const int e_hi = max(0, min(p.S, p.W - w0)) * run_c;  // <= run_len
-        for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
-            if (GROUPS > 1 && (it % GROUPS) != group) continue;
-            if (!ok) continue;
-            const int stage = it % ST;
-            const uint32_t ph = (uint32_t)(it / ST) & 1u;
-            if (!mbar_wait(&empty[stage], ph ^ 1u, ctl, 6)) {
+        for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+            // iteration `it` uses ring slot `stage` in pass parity `ph`; the
+            // groups take iterations in turn
+            const int my_stage = stage;
+            const uint32_t my_ph = ph;
+            const bool mine = (GROUPS == 1) || ((it % GROUPS) == group);
+            ++it;
+            if (++stage == ST) {
+                stage = 0;
+                ph ^= 1u;
+            }
+            if (!mine || !ok) continue;
+            if (!mbar_wait(&empty[my_stage], my_ph ^ 1u, ctl, 6)) {
                 ok = false;
                 continue;
             }
-            uint8_t *arow = smA + (size_t)stage * A_STAGE_BYTES + t * ROW_BYTES;
+            uint8_t *arow = smA + (size_t)my_stage * A_STAGE_BYTES + t * ROW_BYTES;
             if constexpr (MODE == MODE_RUNS) {
                 if (halo)
                     fill_a_row_halo<T>(p, arow, t, kb, valid, hs, hr0, hrows, h0, w0, e_lo, e_hi,
@@ -718,9 +729,10 @@ __device__ void produce_gather(const TcParams &p, uint8_t *smA, uint8_t *smB, ui
                     store_chunk(arow, t, j, o[0], o[1], o[2], o[3]);
                 }
             }
-            if (!p.b_res) fill_b_block<T, MODE>(p, smB + (size_t)stage * b_stage, kb, tc.k0, t, 128);
+            if (!p.b_res)
+                fill_b_block<T, MODE>(p, smB + (size_t)my_stage * b_stage, kb, tc.k0, t, 128);
             fence_proxy_async_smem();
-            mbar_arrive(&full[stage]);
+            mbar_arrive(&full[my_stage]);
         }
     }
     if (halo) asm volatile("cp.async.wait_all;" ::: "memory");  // no copy may outlive the CTA
@@ -729,16 +741,25 @@ __device__ void produce_gather(const TcParams &p, uint8_t *smA, uint8_t *smB, ui
 // ---------------------------------------------------------------------------
 // MMA issuer (one thread)
 // ---------------------------------------------------------------------------
+// The loop body is kept short: the issuing thread shares its scheduler with
+// an epilogue warp, and every instruction it spends between MMAs is tensor
+// time lost.  Stage/phase advance by increments, shared-memory descriptors by
+// adds to their 14-bit address field (16-byte units; 227 KB stays below 2^14).
 template <bool TF32>
 __device__ void issue_mma(const TcParams &p, uint32_t tmem_base, uint8_t *smA, uint8_t *smB,
                           uint64_t *full, uint64_t *empty, uint64_t *tfull, uint64_t *tempty,
                           uint64_t *mma_done, uint64_t *bres, const WaitCtl &ctl) {
     const int ST = p.stages;
-    const uint32_t b_stage = (uint32_t)p.BN * ROW_BYTES;
-    const uint32_t a0 = smem_u32(smA), b0 = smem_u32(smB);
-    int it = 0, t = 0;
+    const uint64_t a_desc0 = sw128_kmajor_desc(smem_u32(smA));
+    const uint64_t b_desc0 = sw128_kmajor_desc(smem_u32(smB));
+    const uint32_t a_step = A_STAGE_BYTES >> 4;               // per stage
+    const uint32_t b_step = ((uint32_t)p.BN * ROW_BYTES) >> 4;  // per stage or resident block
+    const uint32_t idesc = p.idesc;
+    const bool b_res = p.b_res != 0;
+    int stage = 0, t = 0;
+    uint32_t phase = 0;
     bool ok = true;
-    if (p.b_res && !mbar_wait(bres, 0u, ctl, 7)) ok = false;
+    if (b_res && !mbar_wait(bres, 0u, ctl, 7)) ok = false;
     WorkIter wi(p);
     Seg sg;
     while (ok && wi.next(p, sg)) {
@@ -747,26 +768,33 @@ __device__ void issue_mma(const TcParams &p, uint32_t tmem_base, uint8_t *smA, u
         if (!mbar_wait(&tempty[buf], aph ^ 1u, ctl, 3)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + (uint32_t)buf * p.acc_stride;
+        uint32_t acc = 0u;
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-            const int stage = it % ST;
-            const uint32_t ph = (uint32_t)(it / ST) & 1u;
-            if (!mbar_wait(&full[stage], ph, ctl, 4)) {
+            if (!mbar_wait(&full[stage], phase, ctl, 4)) {
                 ok = false;
                 break;
             }
             tc_fence_after_sync();
-            const uint32_t a_addr = a0 + (uint32_t)stage * A_STAGE_BYTES;
-            const uint32_t b_addr = b0 + (uint32_t)(p.b_res ? kb : stage) * b_stage;
-#pragma unroll
-            for (int k = 0; k < ROW_BYTES / 32; ++k) {
-                const uint64_t ad = sw128_kmajor_desc(a_addr + k * 32);
-                const uint64_t bd = sw128_kmajor_desc(b_addr + k * 32);
-                const uint32_t acc = (kb > sg.kb0 || k > 0) ? 1u : 0u;
-                if constexpr (TF32) umma_tf32(d_tmem, ad, bd, p.idesc, acc);
-                else umma_bf16(d_tmem, ad, bd, p.idesc, acc);
+            const uint64_t ad = a_desc0 + (uint64_t)((uint32_t)stage * a_step);
+            const uint64_t bd = b_desc0 + (uint64_t)((uint32_t)(b_res ? kb : stage) * b_step);
+            // four K slices of 32 bytes: +2 in the descriptor's 16-byte address units
+            if constexpr (TF32) {
+                umma_tf32(d_tmem, ad, bd, idesc, acc);
+                umma_tf32(d_tmem, ad + 2, bd + 2, idesc, 1u);
+                umma_tf32(d_tmem, ad + 4, bd + 4, idesc, 1u);
+                umma_tf32(d_tmem, ad + 6, bd + 6, idesc, 1u);
+            } else {
+                umma_bf16(d_tmem, ad, bd, idesc, acc);
+                umma_bf16(d_tmem, ad + 2, bd + 2, idesc, 1u);
+                umma_bf16(d_tmem, ad + 4, bd + 4, idesc, 1u);
+                umma_bf16(d_tmem, ad + 6, bd + 6, idesc, 1u);
             }
             umma_commit(&empty[stage]);  // stage free once these MMAs are done
-            ++it;
+            acc = 1u;
+            if (++stage == ST) {
+                stage = 0;
+                phase ^= 1u;
+            }
         }
         if (!ok) break;
         umma_commit(&tfull[buf]);        // accumulator ready for the epilogue
