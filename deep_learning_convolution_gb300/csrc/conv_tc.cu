@@ -48,7 +48,7 @@ constexpr int ROW_BYTES = 128;                 // one 128-byte swizzle row of th
 constexpr int A_STAGE_BYTES = BM * ROW_BYTES;  // 16 KiB
 constexpr int MAX_DYN_SMEM = 232448;           // 227 KiB per block (opt-in)
 constexpr int BAR_AREA = 256;
-constexpr int EPI_BUF_BYTES = 32 * 16 * 4;          // one warp's 32 rows x 16 FP32 columns
+constexpr int EPI_BUF_BYTES = 32 * 128;            // one warp's 32 rows x 32 FP32 columns
 constexpr int EPI_SMEM = 4 * 2 * EPI_BUF_BYTES;     // 4 epilogue warps, double-buffered
 
 enum { MODE_IM2COL = 0, MODE_GATHER = 1, MODE_RUNS = 2 };
@@ -372,27 +372,6 @@ __device__ __forceinline__ void combine_chunk(const uint32_t (&raw)[5], int mis,
 #pragma unroll
     for (int i = 0; i < 4; ++i) o[i] = mis ? __funnelshift_r(raw[i], raw[i + 1], 16) : raw[i];
     mask_chunk<T>(o, ja, jb);
-}
-
-// The 16 bytes starting at byte `off` (0..15) of the 32-byte window v0:v1.
-__device__ __forceinline__ void realign16(const uint4 &v0, const uint4 &v1, int off,
-                                          uint32_t (&o)[4]) {
-    const uint32_t win[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    const int q = off >> 2, sh = (off & 3) * 8;
-    uint32_t w[5];
-#pragma unroll
-    for (int i = 0; i < 5; ++i)
-        w[i] = q == 0 ? win[i] : (q == 1 ? win[i + 1] : (q == 2 ? win[i + 2] : win[i + 3]));
-#pragma unroll
-    for (int i = 0; i < 4; ++i) o[i] = __funnelshift_r(w[i], w[i + 1], sh);
-}
-
-__device__ __forceinline__ uint4 lds128(uint32_t saddr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(saddr));
-    return v;
 }
 
 // Fills A row `t` (output pixel m) of reduction block kb from global memory.
@@ -817,36 +796,18 @@ __device__ __forceinline__ unsigned short f32_to_bf16_bits(float f) {
     return *reinterpret_cast<unsigned short *>(&b);
 }
 
-// Writes one thread's 16 finished values into its row of the warp's staging
-// buffer (32 rows x 64 bytes for FP32, x 32 bytes for BF16) in the tensor
-// map's swizzle: 64-byte rows swizzle 16-byte chunks by (row / 2) % 4, 32-byte
-// rows by (row / 4) % 2.
-__device__ __forceinline__ void stage_row(uint8_t *buf, int lane, const float (&val)[16], bool bf16) {
-    if (!bf16) {
-        uint8_t *rowp = buf + lane * 64;
+// Writes 16 finished FP32 values (columns 16*half .. 16*half+15 of a 32-column
+// group) into row `lane` of a warp's 32 x 128-byte staging buffer, in the
+// 128-byte swizzle of the y tensor map (16-byte chunk j of row r at j ^ (r % 8)).
+__device__ __forceinline__ void stage_half_row(uint8_t *buf, int lane, int half,
+                                               const float (&val)[16]) {
+    uint8_t *rowp = buf + lane * 128;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint8_t *dst = rowp + ((j ^ ((lane >> 1) & 3)) << 4);
-            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(dst)),
-                         "f"(val[4 * j]), "f"(val[4 * j + 1]), "f"(val[4 * j + 2]),
-                         "f"(val[4 * j + 3])
-                         : "memory");
-        }
-    } else {
-        uint8_t *rowp = buf + lane * 32;
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            uint32_t w[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                __nv_bfloat162 h = __floats2bfloat162_rn(val[8 * j + 2 * i], val[8 * j + 2 * i + 1]);
-                w[i] = *reinterpret_cast<uint32_t *>(&h);
-            }
-            uint8_t *dst = rowp + ((j ^ ((lane >> 2) & 1)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(dst)), "r"(w[0]),
-                         "r"(w[1]), "r"(w[2]), "r"(w[3])
-                         : "memory");
-        }
+    for (int j = 0; j < 4; ++j) {
+        uint8_t *dst = rowp + (((half * 4 + j) ^ (lane & 7)) << 4);
+        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(dst)),
+                     "f"(val[4 * j]), "f"(val[4 * j + 1]), "f"(val[4 * j + 2]), "f"(val[4 * j + 3])
+                     : "memory");
     }
 }
 
@@ -870,6 +831,8 @@ __device__ bool wait_partial_flag(int *flag, const WaitCtl &ctl) {
     }
 }
 
+// DEPTH 16-column TMEM loads are in flight before each wait.
+template <int DEPTH>
 __device__ void epilogue(const TcParams &p, uint32_t tmem_base, uint64_t *tfull, uint64_t *tempty,
                          uint8_t *epi_smem, const CUtensorMap *tmY, const WaitCtl &ctl) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -918,10 +881,23 @@ __device__ void epilogue(const TcParams &p, uint32_t tmem_base, uint64_t *tfull,
             ybase = (long long)n * p.ys[0] + (long long)op * p.ys[2] + (long long)oq * p.ys[3];
         }
         const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)buf * p.acc_stride;
-        for (int c0 = 0; c0 < p.BN; c0 += 16) {
-            uint32_t v[16];
-            tmem_ld_32x32b_x16(taddr + (uint32_t)c0, v);
-            tmem_ld_wait();
+        // bulk stores need this warp's 32 rows to be rows of this tile (an
+        // image-aligned tile may end early; rows past M are clipped by the map)
+        const bool tma_warp = p.y_tma && !tail && (p.img_tiles == 0 || quad * 32 + 32 <= tc.rows);
+        int half = 0;  // which 16-column half of the current 32-column group
+        bool stop = false;
+        for (int c00 = 0; c00 < p.BN && !stop; c00 += 16 * DEPTH) {
+        const int nsub = min(DEPTH, (p.BN - c00) >> 4);
+        uint32_t vv[DEPTH][16];
+#pragma unroll
+        for (int q = 0; q < DEPTH; ++q)
+            if (q < nsub) tmem_ld_32x32b_x16(taddr + (uint32_t)(c00 + 16 * q), vv[q]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < DEPTH; ++q) {
+            if (q >= nsub || stop) break;
+            uint32_t (&v)[16] = vv[q];
+            const int c0 = c00 + 16 * q;
             const int kbase = tc.k0 + c0;
             // 16 consecutive filters of one pixel contiguous and 16-byte aligned in y
             const bool vec16 = valid && p.ys[1] == 1 && kbase + 16 <= p.K &&
@@ -959,36 +935,41 @@ __device__ void epilogue(const TcParams &p, uint32_t tmem_base, uint64_t *tfull,
                         v[j] = __float_as_uint(__uint_as_float(v[j]) +
                                                __ldcg(yf + ybase + (long long)(kbase + j) * p.ys[1]));
             }
-            if (p.y_tma) {
-                if (kbase >= p.K) break;  // warp-uniform
+            if (tma_warp) {
+                if (kbase >= p.K) {  // warp-uniform; nothing is pending here
+                    stop = true;
+                    break;
+                }
                 float val[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     float f = p.alpha * __uint_as_float(v[j]);
                     const int k = kbase + j;
                     if (valid && k < p.K) {
-                        if (p.beta != 0.f) {
-                            const long long yo = ybase + k;
-                            f = __fmaf_rn(p.beta, p.y_bf16 ? bf16_bits_to_f32(yb[yo]) : yf[yo], f);
-                        }
+                        if (p.beta != 0.f) f = __fmaf_rn(p.beta, yf[ybase + k], f);
                         if (p.bias) f += __ldg(p.bias + k);
                     }
                     if (p.relu) f = fmaxf(f, 0.f);
                     val[j] = f;
                 }
                 uint8_t *sb = my_bufs + (nbuf & 1) * EPI_BUF_BYTES;
-                if (nbuf >= 2) {  // the store issued from this buffer two chunks ago
+                if (half == 0 && nbuf >= 2) {  // the store issued from this buffer two groups ago
                     if (lane == 0) bulk_wait_group_read<1>();
                     __syncwarp();
                 }
-                stage_row(sb, lane, val, p.y_bf16 != 0);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_2d(tmY, sb, kbase, (int)(tc.m0 + quad * 32));
-                    bulk_commit_group();
+                stage_half_row(sb, lane, half, val);
+                if (half == 1 || c0 + 16 >= p.BN || kbase + 16 >= p.K) {  // group complete
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(tmY, sb, kbase - 16 * half, (int)(tc.m0 + quad * 32));
+                        bulk_commit_group();
+                    }
+                    ++nbuf;
+                    half = 0;
+                } else {
+                    half = 1;
                 }
-                ++nbuf;
                 continue;
             }
             if (!valid) continue;
@@ -1025,6 +1006,7 @@ __device__ void epilogue(const TcParams &p, uint32_t tmem_base, uint64_t *tfull,
                     }
                 }
             }
+        }
         }
         if (tail) {  // publish the partial once every epilogue thread has stored its part
             __threadfence();
@@ -1068,11 +1050,12 @@ __global__ void __launch_bounds__(KernelShape<MODE>::THREADS, 1)
     const int ST = p.stages;
     const int b_blocks = p.b_res ? p.num_kb : ST;
     uint8_t *smA = smem;
-    uint8_t *smB = smem + (size_t)ST * A_STAGE_BYTES;
+    uint8_t *epi_smem = smem + (size_t)ST * A_STAGE_BYTES;  // 1024-aligned staging of y
+    uint8_t *smB = epi_smem + (p.y_tma ? EPI_SMEM : 0);
     uint8_t *smH = smB + (size_t)b_blocks * p.BN * ROW_BYTES;  // halo buffers (run gather)
     int4 *ctab = reinterpret_cast<int4 *>(smH + (p.halo ? 2 * (size_t)p.halo_bytes : 0));
-    uint8_t *epi_smem = reinterpret_cast<uint8_t *>(ctab) + (p.ctab ? (size_t)p.num_kb * 8 * 16 : 0);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(epi_smem + (p.y_tma ? EPI_SMEM : 0));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(ctab) +
+                                                  (p.ctab ? (size_t)p.num_kb * 8 * 16 : 0));
     uint64_t *full = bars;
     uint64_t *empty = bars + ST;
     uint64_t *tfull = bars + 2 * ST;
@@ -1122,7 +1105,8 @@ __global__ void __launch_bounds__(KernelShape<MODE>::THREADS, 1)
             issue_mma<TF32>(p, tmem_base, smA, smB, full, empty, tfull, tempty, mma_done, bres, ctl);
     } else {
         if (p.y_tma && lane == 0) prefetch_tmap(&tmY);
-        epilogue(p, tmem_base, tfull, tempty, epi_smem, &tmY, ctl);
+        // the gather kernels run 13 warps and have fewer registers per thread
+        epilogue<MODE == MODE_IM2COL ? 4 : 1>(p, tmem_base, tfull, tempty, epi_smem, &tmY, ctl);
     }
     __syncwarp();
     tc_fence_before_sync();
@@ -1343,12 +1327,19 @@ dlcStatus_t dlc_launch_tc(dlcContext *ctx, const ConvProblem &pb, dlcKernel_t va
     // tile, plus the epilogue's staging buffers when y is stored by TMA
     // Bulk-tensor stores of y measured slower than direct stores from the
     // epilogue registers (small per-warp boxes), so they are opt-in.
-    tp.y_tma = 0;
-    if (const char *ev = std::getenv("DLC_TC_YTMA"))
-        tp.y_tma = y_tma_ok(pb) && tp.img_tiles == 0 && std::atoi(ev) != 0;
+    // FP32 y written through a 2-D [M, K] tensor map: bulk stores of 32-row x
+    // 32-column groups from a staging buffer per epilogue warp (DLC_TC_YTMA=0
+    // falls back to per-thread vector stores).
+    // The im2col kernel's TMA unit is busy with operand loads (bulk stores
+    // there measured up to 2.4x slower), so there y goes out through direct
+    // vector stores from the epilogue registers.
+    const bool y_rows = y_tma_ok(pb) && !tp.y_bf16 && (tp.n_tiles == 1 || tp.BN % 32 == 0);
+    tp.y_tma = (y_rows && mode != MODE_IM2COL) ? 1 : 0;
+    if (const char *ev = std::getenv("DLC_TC_YTMA")) tp.y_tma = y_rows && std::atoi(ev) != 0;
     const int b_stage = tp.BN * ROW_BYTES;
     const int ctab_bytes = tp.ctab ? tp.num_kb * 8 * 16 : 0;
-    const int budget = MAX_DYN_SMEM - 1024 - BAR_AREA - (tp.y_tma ? EPI_SMEM : 0) -
+    const int epi_bytes = tp.y_tma ? EPI_SMEM : 0;
+    const int budget = MAX_DYN_SMEM - 1024 - BAR_AREA - epi_bytes -
                        (tp.halo ? 2 * tp.halo_bytes : 0) - ctab_bytes;
     const long long b_all = (long long)tp.num_kb * b_stage;
     tp.b_res = (mode != MODE_IM2COL && tp.n_tiles == 1 && b_all <= 120 * 1024 &&
@@ -1406,12 +1397,12 @@ dlcStatus_t dlc_launch_tc(dlcContext *ctx, const ConvProblem &pb, dlcKernel_t va
         const long long ye = yb16 ? 2 : 4;
         const cuuint64_t ydim[2] = {(cuuint64_t)pb.K, (cuuint64_t)tp.M};
         const cuuint64_t ystr[1] = {(cuuint64_t)(pb.ys[3] * ye)};
-        const cuuint32_t ybox[2] = {16, 32};
+        const cuuint32_t ybox[2] = {32, 32};
         const cuuint32_t ones[2] = {1, 1};
         CUresult r = ctx->encode_tiled(
             &ty, yb16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, pb.y,
             ydim, ystr, ybox, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            yb16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return DLC_STATUS_EXECUTION_FAILED;
     }
@@ -1444,8 +1435,8 @@ dlcStatus_t dlc_launch_tc(dlcContext *ctx, const ConvProblem &pb, dlcKernel_t va
     }
 
     const size_t smem = 1024 + (size_t)tp.stages * A_STAGE_BYTES + (size_t)b_bytes +
-                        (tp.halo ? 2 * (size_t)tp.halo_bytes : 0) + ctab_bytes +
-                        (tp.y_tma ? EPI_SMEM : 0) + BAR_AREA;
+                        (tp.halo ? 2 * (size_t)tp.halo_bytes : 0) + ctab_bytes + epi_bytes +
+                        BAR_AREA;
     if (grid < 1) grid = 1;
     cudaError_t err = tf32 ? launch_mode<true>(mode, tp, ta, tb, ty, (int)grid, smem, ctx->stream)
                            : launch_mode<false>(mode, tp, ta, tb, ty, (int)grid, smem, ctx->stream);
