@@ -80,4 +80,7 @@ dlcStatus_t dlc_launch_ffma(dlcContext *ctx, const ConvProblem &pb);
 dlcKernel_t dlc_tc_variant(const dlcContext *ctx, const ConvProblem &pb);
 dlcStatus_t dlc_launch_tc(dlcContext *ctx, const ConvProblem &pb, dlcKernel_t variant);
 dlcStatus_t dlc_launch_wait_selftest(dlcContext *ctx, unsigned long long timeout_ns);
+// conv_window.cu: layers with few channels per horizontal stride step.
+bool dlc_window_ok(const ConvProblem &pb);
+dlcStatus_t dlc_launch_window(dlcContext *ctx, const ConvProblem &pb);
 

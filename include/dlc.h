@@ -98,9 +98,13 @@ typedef enum {
     DLC_KERNEL_FFMA = 1,          /* strict FP32 direct convolution, CUDA cores */
     DLC_KERNEL_TC_IM2COL = 2,     /* tcgen05 implicit GEMM, TMA im2col activations */
     DLC_KERNEL_TC_GATHER = 3,     /* tcgen05 implicit GEMM, element-gathered operands */
-    DLC_KERNEL_TC_GATHER_RUNS = 4 /* tcgen05 implicit GEMM, operands gathered as contiguous
+    DLC_KERNEL_TC_GATHER_RUNS = 4, /* tcgen05 implicit GEMM, operands gathered as contiguous
                                      runs: (s,c) of a filter row for NHWC + KRSC, s of a
                                      (c,r) pair for NCHW + KCRS */
+    DLC_KERNEL_TC_WINDOW = 5      /* tcgen05 implicit GEMM for few channels per stride step
+                                     (v*C*element size <= 64 bytes, no horizontal dilation,
+                                     K <= 256): lowered rows read in place from packed input
+                                     rows in shared memory */
 } dlcKernel_t;
 
 /* Device error codes recorded by kernels (dlcGetLastDeviceError). */

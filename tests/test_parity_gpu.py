@@ -110,9 +110,73 @@ RUN_CASES = [
 
 
 @pytest.mark.parametrize("layer", RUN_CASES, ids=lambda l: l.name)
-def test_tc_runs_parity_full(handle, layer):
+def test_tc_runs_parity_full(handle, layer, monkeypatch):
+    # most of these layers take the window kernel by default
+    monkeypatch.setenv("DLC_TC_WINDOW", "0")
     run_and_check(handle, layer, 2000 + RUN_CASES.index(layer), full=True,
                   expect_kernel="tc_runs")
+
+
+# ---------------------------------------------------------------------------
+# tensor cores, window kernel: few channels per horizontal stride step; the
+# lowered rows are read in place from packed input-row strips
+# ---------------------------------------------------------------------------
+
+WINDOW_CASES = [
+    # 24-byte phase pixels (32-byte swizzled strips), 4-byte copies (pl*C*2 = 12),
+    # four output rows per tile
+    L("win_bf16_c3_k64_11x11_s4_pad2", 2, 3, 67, 67, 64, 11, 11, **P(2, 2, 2, 2), u=4, v=4),
+    # no padding: 8-byte copies; K = 96
+    L("win_bf16_c3_k96_11x11_s4_nopad", 2, 3, 99, 99, 96, 11, 11, u=4, v=4),
+    # 16-byte phase pixels (no swizzle), wide rows: 150 pixels -> two 128-pixel
+    # segments per output row; left pad 2 -> 4-byte copies
+    L("win_bf16_c3_k64_7x7_s2_wide", 1, 3, 9, 300, 64, 7, 7, **P(3, 3, 2, 4), u=2, v=2),
+    # left pad 3: no aligned copy size, element loads throughout
+    L("win_bf16_c3_k64_7x7_s2_pad3", 2, 3, 20, 41, 64, 7, 7, **P(3, 3, 3, 3), u=2, v=2),
+    # two output rows per tile (Q + A - 1 = 54), odd P: a half-empty last tile
+    L("win_bf16_c8_k32_5x5_two_rows", 2, 8, 25, 50, 32, 5, 5, **P(2, 2, 2, 2)),
+    # 64-byte phase pixels (64-byte swizzle), TF32 and BF16
+    L("win_tf32_c16_k32_3x3", 2, 16, 19, 23, 32, 3, 3, **P(1, 1, 1, 1), dtype="tf32"),
+    L("win_bf16_c24_k64_5x5", 2, 24, 13, 13, 64, 5, 5, **P(2, 2, 2, 2)),
+    # K not a multiple of 16 or 32; BN = 208; K = 1
+    L("win_bf16_c3_k200_5x5_s2", 2, 3, 31, 29, 200, 5, 5, **P(2, 1, 2, 1), u=2, v=2),
+    L("win_bf16_c3_k40_3x3", 2, 3, 17, 17, 40, 3, 3, **P(1, 1, 1, 1)),
+    L("win_bf16_c1_k1_3x3", 2, 1, 17, 17, 1, 3, 3, **P(1, 1, 1, 1)),
+    # vertical stride and dilation, asymmetric pads
+    L("win_bf16_c8_k48_3x3_s2x1", 2, 8, 21, 22, 48, 3, 3, **P(0, 2, 1, 0), u=2),
+    L("win_bf16_c5_k40_4x3_dilh2_s3", 3, 5, 17, 16, 40, 4, 3, **P(0, 2, 1, 0), dil_h=2, v=3),
+    # NCHW activations: C = 1 (contiguous phase pixels), C = 8 (element loads)
+    L("win_tf32_c1_k32_21x11_s2_nchw", 2, 1, 50, 70, 32, 21, 11, **P(10, 10, 5, 5), u=2, v=2,
+      dtype="tf32", layout="NCHW"),
+    L("win_tf32_c8_k32_7x5_s2x1_nchw", 2, 8, 27, 40, 32, 7, 5, **P(3, 3, 2, 2), u=2, v=1,
+      dtype="tf32", layout="NCHW"),
+    # 1x1 filters, more tiles than SMs
+    L("win_bf16_c4_k16_1x1_many", 40, 4, 30, 30, 16, 1, 1),
+]
+
+
+@pytest.mark.parametrize("layer", WINDOW_CASES, ids=lambda l: l.name)
+def test_tc_window_parity_full(handle, layer):
+    run_and_check(handle, layer, 2300 + WINDOW_CASES.index(layer), full=True,
+                  expect_kernel="tc_window")
+
+
+@pytest.mark.parametrize("layer", [WINDOW_CASES[i] for i in (0, 1, 4, 5, 12)],
+                         ids=lambda l: l.name)
+def test_tc_window_staged_rows(handle, layer, monkeypatch):
+    """Input rows bulk-copied to shared memory and repacked there (opt-in)."""
+    monkeypatch.setenv("DLC_TC_WINRAW", "1")
+    run_and_check(handle, layer, 2350 + WINDOW_CASES.index(layer), full=True,
+                  expect_kernel="tc_window")
+
+
+@pytest.mark.parametrize("y_axes", ["NCHW", "NHWC"])
+def test_tc_window_epilogue(handle, y_axes):
+    import torch
+    run_and_check(handle, WINDOW_CASES[0], 2390, full=True, y_axes=y_axes, alpha=-0.5,
+                  beta=0.75, with_bias=True, relu=True, expect_kernel="tc_window")
+    run_and_check(handle, WINDOW_CASES[4], 2391, full=True, y_axes=y_axes,
+                  y_dtype=torch.bfloat16, beta=0.5, with_bias=True, expect_kernel="tc_window")
 
 
 # ---------------------------------------------------------------------------
@@ -144,8 +208,15 @@ def test_kcrs_filters_with_nhwc_activations_use_gather(handle):
     (L("bf16_c24_view", 2, 24, 12, 13, 48, 3, 3, **P(1, 1, 1, 1)), "chan_pad", "tc_gather"),
     (L("tf32_nchw_wview", 2, 4, 12, 13, 32, 3, 5, **P(1, 1, 2, 2), dtype="tf32",
        layout="NCHW"), "width_pad", "tc_runs"),
+    (L("bf16_c24_view_w", 2, 24, 12, 13, 48, 3, 3, **P(1, 1, 1, 1)), "chan_pad", "tc_window"),
+    (L("bf16_c3_imgpad_w", 2, 3, 30, 31, 64, 5, 5, **P(2, 2, 2, 2), u=2, v=2), "image_pad",
+     "tc_window"),
+    (L("tf32_nchw_wview_w", 2, 4, 12, 13, 32, 3, 5, **P(1, 1, 2, 2), dtype="tf32",
+       layout="NCHW"), "width_pad", "tc_window"),
 ], ids=lambda v: v.name if hasattr(v, "name") else str(v))
-def test_strided_views(handle, layer, view, kernel):
+def test_strided_views(handle, layer, view, kernel, monkeypatch):
+    if kernel != "tc_window":
+        monkeypatch.setenv("DLC_TC_WINDOW", "0")
     run_and_check(handle, layer, 2600, full=True, view=view, expect_kernel=kernel)
 
 
@@ -168,6 +239,7 @@ SK_CASES = [
 @pytest.mark.parametrize("layer,kw", SK_CASES, ids=lambda v: v.name if hasattr(v, "name") else "")
 def test_stream_k_parity_full(handle, layer, kw, monkeypatch):
     monkeypatch.setenv("DLC_TC_STREAMK", "1")
+    monkeypatch.setenv("DLC_TC_WINDOW", "0")
     run_and_check(handle, layer, 2700 + [c[0] for c in SK_CASES].index(layer), full=True, **kw)
 
 
@@ -212,13 +284,16 @@ def test_random_sweep_parity(handle, layer):
 # epilogue: alpha, beta * y, bias, ReLU, BF16 output, other y layouts
 # ---------------------------------------------------------------------------
 
-EPI_LAYERS = [IM2COL_CASES[0], RUN_CASES[2], RUN_CASES[3], GATHER_CASES[0]]
+EPI_LAYERS = [IM2COL_CASES[0], RUN_CASES[2], RUN_CASES[3], GATHER_CASES[0], WINDOW_CASES[2]]
 
 
 @pytest.mark.parametrize("layer", EPI_LAYERS, ids=lambda l: l.name)
 @pytest.mark.parametrize("alpha,beta,bias,relu", [
     (0.5, 0.0, True, True), (1.0, -0.75, False, False), (-2.0, 1.5, True, True)])
-def test_epilogue_parity(handle, layer, alpha, beta, bias, relu):
+@pytest.mark.parametrize("window", [True, False], ids=["default", "no_window"])
+def test_epilogue_parity(handle, layer, alpha, beta, bias, relu, window, monkeypatch):
+    if not window:
+        monkeypatch.setenv("DLC_TC_WINDOW", "0")
     run_and_check(handle, layer, 4000, full=True, alpha=alpha, beta=beta, with_bias=bias,
                   relu=relu)
 
@@ -255,8 +330,8 @@ def test_full_workload_layer_sampled(handle, wl, j):
 def test_workspace_is_zero_and_kernel_choice(handle):
     import torch
     from deep_learning_convolution_gb300 import api
-    expect = {"alexnet": ["tc_runs"] + ["tc_im2col"] * 4,
-              "overfeat": ["tc_runs"] + ["tc_im2col"] * 4,
+    expect = {"alexnet": ["tc_window"] + ["tc_im2col"] * 4,
+              "overfeat": ["tc_window"] + ["tc_im2col"] * 4,
               "resnet50": ["tc_im2col"] * len(synth.WORKLOADS["resnet50"]),
               "speech": ["tc_runs", "tc_runs"], "tiny": ["ffma"]}
     for wl, kinds in expect.items():

@@ -24,7 +24,8 @@ L = synth.Layer
     # library's scratch flags are in use
     L("noalloc_bf16_c64_k64_70", 4, 64, 70, 70, 64, 3, 3, pad_top=1, pad_bottom=1, pad_left=1,
       pad_right=1),
-    L("noalloc_tf32_nchw_c16_k32_99", 2, 16, 99, 99, 32, 3, 3, pad_top=1, pad_bottom=1,
+    # 32 channels: more than the window kernel takes, so the stream-K schedule runs
+    L("noalloc_tf32_nchw_c32_k32_99", 2, 32, 99, 99, 32, 3, 3, pad_top=1, pad_bottom=1,
       pad_left=1, pad_right=1, dtype="tf32", layout="NCHW"),
 ], ids=lambda l: l.name)
 def test_no_alloc_matches_handle_path_twice(layer):
