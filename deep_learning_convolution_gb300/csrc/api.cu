@@ -15,6 +15,8 @@
 // flags followed by two error words.  Device code never names it; host code
 // passes its device address, looked up once per device.
 static __device__ __align__(256) int dlc_noalloc_scratch[DLC_NOALLOC_MAX_TILES + 64];
+// Its repacked filter image for the window kernel.
+static __device__ __align__(256) unsigned char dlc_noalloc_wpack[DLC_WPACK_BYTES];
 static_assert(DLC_NOALLOC_MAX_TILES == DLC_SK_FLAGS, "one flag per split-capable tile");
 
 namespace {
@@ -214,8 +216,10 @@ dlcStatus_t dlcCreate(dlcHandle_t *handle) {
         return DLC_STATUS_EXECUTION_FAILED;
     }
     if (cudaMalloc((void **)&h->sk_flags, DLC_SK_FLAGS * sizeof(int)) != cudaSuccess ||
-        cudaMemset(h->sk_flags, 0, DLC_SK_FLAGS * sizeof(int)) != cudaSuccess) {
+        cudaMemset(h->sk_flags, 0, DLC_SK_FLAGS * sizeof(int)) != cudaSuccess ||
+        cudaMalloc(&h->wpack, DLC_WPACK_BYTES) != cudaSuccess) {
         if (h->sk_flags) cudaFree(h->sk_flags);
+        if (h->wpack) cudaFree(h->wpack);
         cudaFreeHost(h->h_err);
         delete h;
         return DLC_STATUS_EXECUTION_FAILED;
@@ -229,6 +233,7 @@ dlcStatus_t dlcCreate(dlcHandle_t *handle) {
                                          &q2) != cudaSuccess ||
         q2 != cudaDriverEntryPointSuccess) {
         cudaFree(h->sk_flags);
+        cudaFree(h->wpack);
         cudaFreeHost(h->h_err);
         delete h;
         return DLC_STATUS_EXECUTION_FAILED;
@@ -248,6 +253,7 @@ dlcStatus_t dlcDestroy(dlcHandle_t h) {
     if (!h) return DLC_STATUS_NOT_INITIALIZED;
     if (h->h_err) cudaFreeHost(h->h_err);
     if (h->sk_flags) cudaFree(h->sk_flags);
+    if (h->wpack) cudaFree(h->wpack);
     delete h;
     return DLC_STATUS_SUCCESS;
 }
@@ -511,6 +517,7 @@ namespace {
 struct NoAllocDevice {
     int ready = 0;
     int *scratch = nullptr;
+    void *wpack = nullptr;
     int sm_count = 0;
     EncodeTiledFn encode_tiled = nullptr;
     EncodeIm2colFn encode_im2col = nullptr;
@@ -531,7 +538,9 @@ dlcStatus_t noalloc_setup(int dev, NoAllocDevice **out) {
             return DLC_STATUS_EXECUTION_FAILED;
         if (major != 10 || minor != 3) return DLC_STATUS_NOT_SUPPORTED;
         int *ptr = nullptr;
-        if (cudaGetSymbolAddress((void **)&ptr, dlc_noalloc_scratch) != cudaSuccess || !ptr)
+        void *wptr = nullptr;
+        if (cudaGetSymbolAddress((void **)&ptr, dlc_noalloc_scratch) != cudaSuccess || !ptr ||
+            cudaGetSymbolAddress(&wptr, dlc_noalloc_wpack) != cudaSuccess || !wptr)
             return DLC_STATUS_EXECUTION_FAILED;
         cudaDriverEntryPointQueryResult q1, q2;
         void *f1 = nullptr, *f2 = nullptr;
@@ -543,6 +552,7 @@ dlcStatus_t noalloc_setup(int dev, NoAllocDevice **out) {
             q2 != cudaDriverEntryPointSuccess)
             return DLC_STATUS_EXECUTION_FAILED;
         d.scratch = ptr;
+        d.wpack = wptr;
         d.sm_count = sms;
         d.encode_tiled = reinterpret_cast<EncodeTiledFn>(f1);
         d.encode_im2col = reinterpret_cast<EncodeIm2colFn>(f2);
@@ -580,6 +590,7 @@ dlcStatus_t dlcConvolutionForwardNoAlloc(void *stream, const float *alpha,
     ctx.h_err = nullptr;
     ctx.d_err = status ? status : nd->scratch + DLC_NOALLOC_MAX_TILES;
     ctx.sk_flags = nd->scratch;
+    ctx.wpack = nd->wpack;
     ctx.force_sk = 1;
     ctx.encode_tiled = nd->encode_tiled;
     ctx.encode_im2col = nd->encode_im2col;

@@ -67,8 +67,8 @@ struct WinParams {
     int row_bytes;    // bytes of one input row (x_word)
     int x_raw;        // input rows are bulk-copied to shared memory, then repacked
     int raw_rows;     // input rows one tile spans: (J-1)*u + (R-1)*dh + 1
-    int w_raw;        // the filter tensor is bulk-copied to shared memory, then packed
-    int w_bytes;      // its bytes (w_raw)
+    const void *wpack;  // the filter slabs, packed by window_pack_filters
+    int b_img_bytes;    // their bytes: R*steps*BN rows of 32
     int num_tiles;
     long long xs[4], ws[4], ys[4];
     const void *x;
@@ -132,19 +132,6 @@ __device__ __forceinline__ uint32_t pack_word(const T (&e)[4 / sizeof(T)]) {
 // element by element -- phase pixel a, phase phi, channel c, tap s = v*a+phi --
 // and writes it a word at a time, sixteen words' loads in flight before their
 // stores.
-template <typename T>
-__device__ __forceinline__ T lds_elem(uint32_t addr) {
-    if constexpr (sizeof(T) == 2) {
-        unsigned short v;
-        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
-        return v;
-    } else {
-        uint32_t v;
-        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-        return v;
-    }
-}
-
 // Barrier of the eight producer warps (id 2) that also ANDs a predicate.
 __device__ __forceinline__ bool producers_and(bool v) {
     uint32_t r;
@@ -163,72 +150,39 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
     return v;
 }
 
-// Packs the filter slabs.  A table in shared memory at `stab` first maps
-// window element e (phase pixel e / (D/e_size), element phi*C + c inside it)
-// to the element offset c*ws[1] + s*ws[3] of tap s = v*a + phi, or -1 for
-// padding.  Lane l then fills word l % 8 of slab rows (tid/8) + 32*i, walking
-// (filter k, slab (r, st)) incrementally; eight words' loads are in flight
-// before their stores.  wsrc: the filter tensor's bytes in shared memory (a
-// bulk copy of w), or 0 to read w from global memory.
+// The filter taps as MMA B operands, packed by a small kernel launched ahead
+// of the convolution into device memory, in the exact shared-memory image the
+// convolution then bulk-copies: slab (r, st) holds BN rows (filters) of the
+// 32 window bytes [32*st, 32*st + 32) of filter row r, 32-byte swizzled K-major
+// (row k at 32*k; its two 16-byte halves exchanged where address bit 7 is set,
+// which the image reproduces because the slabs start 256-byte aligned).  One
+// thread per 4-byte word.
 template <typename T>
-__device__ void pack_filters(const WinParams &p, uint32_t sB, int tid, uint32_t wsrc,
-                             uint32_t stab) {
-    constexpr int ESZ = (int)sizeof(T), EPW = 4 / ESZ, BATCH = 8;
-    constexpr uint32_t NONE = 0xffffffffu;
+__global__ void window_pack_filters(const __grid_constant__ WinParams p, uint32_t *img) {
+    constexpr int ESZ = (int)sizeof(T), EPW = 4 / ESZ;
+    const int words = p.R * p.steps * p.BN * 8;
+    const int wi = blockIdx.x * blockDim.x + threadIdx.x;
+    if (wi >= words) return;
     const T *w = static_cast<const T *>(p.w);
-    const int epp = p.D / ESZ;                  // elements per phase pixel
-    const int E = p.steps * (32 / ESZ);         // window elements
-    for (int e = tid; e < E; e += PROD_THREADS) {
-        const int a = e / epp, eb = e - a * epp;
-        int off = -1;
-        if (eb < p.v * p.C) {
-            const int phi = eb / p.C, c = eb - phi * p.C;
-            const int s = p.v * a + phi;
-            if (s < p.S) off = (int)((long long)c * p.ws[1] + (long long)s * p.ws[3]);
-        }
-        sts32(stab + 4u * e, (uint32_t)off);
+    const int row = wi >> 3, wd = wi & 7;
+    const int sl = row / p.BN, k = row - sl * p.BN;
+    const int r = sl / p.steps, st = sl - r * p.steps;
+    T e[EPW];
+#pragma unroll
+    for (int i = 0; i < EPW; ++i) {
+        const int b = 32 * st + 4 * wd + i * ESZ;  // byte of the window
+        const int a = b / p.D;
+        const int eps = (b - a * p.D) / ESZ;        // element of phase pixel a
+        const int phi = eps / p.C, c = eps - phi * p.C;
+        const int s = p.v * a + phi;
+        const bool in = k < p.K && eps < p.v * p.C && s < p.S;
+        e[i] = in ? w[(long long)k * p.ws[0] + (long long)c * p.ws[1] + (long long)r * p.ws[2] +
+                      (long long)s * p.ws[3]]
+                  : (T)0;
     }
-    producers_and(true);
-    const int wd = tid & 7;
-    const int rows = p.R * p.steps * p.BN;
-    int row = tid >> 3, k = row, r = 0, st = 0;
-    while (k >= p.BN) {
-        k -= p.BN;
-        if (++st == p.steps) st = 0, ++r;
-    }
-#pragma unroll 1
-    while (row < rows) {
-        T val[BATCH][EPW];
-        uint32_t dst[BATCH];
-#pragma unroll
-        for (int bi = 0; bi < BATCH; ++bi) {
-            dst[bi] = NONE;
-#pragma unroll
-            for (int i = 0; i < EPW; ++i) val[bi][i] = (T)0;
-            if (row < rows) {
-                const int e0 = st * (32 / ESZ) + wd * EPW;
-                const long long kr = (long long)k * p.ws[0] + (long long)r * p.ws[2];
-#pragma unroll
-                for (int i = 0; i < EPW; ++i) {
-                    const int off = (int)lds32(stab + 4u * (e0 + i));
-                    if (k < p.K && off >= 0)
-                        val[bi][i] = wsrc ? lds_elem<T>(wsrc + (uint32_t)(kr + off) * ESZ) : w[kr + off];
-                }
-                const uint32_t raddr = sB + (uint32_t)row * 32u;
-                dst[bi] = raddr + ((((uint32_t)(wd >> 2)) ^ ((raddr >> 7) & 1u)) << 4) +
-                          ((uint32_t)(wd & 3) << 2);
-            }
-            row += PROD_THREADS / 8;
-            k += PROD_THREADS / 8;
-            while (k >= p.BN) {
-                k -= p.BN;
-                if (++st == p.steps) st = 0, ++r;
-            }
-        }
-#pragma unroll
-        for (int bi = 0; bi < BATCH; ++bi)
-            if (dst[bi] != NONE) sts32(dst[bi], pack_word<T>(val[bi]));
-    }
+    const uint32_t off = (uint32_t)row * 32u + ((((uint32_t)(wd >> 2)) ^ ((uint32_t)(row >> 2) & 1u)) << 4) +
+                         ((uint32_t)(wd & 3) << 2);
+    img[off >> 2] = pack_word<T>(e);
 }
 
 // Packs the R strips of one tile.  Lane l of a warp owns word l % wpp of strip
@@ -406,37 +360,20 @@ __device__ void issue_raw_rows(const WinParams &p, uint32_t sR, const WinTile &w
 template <typename T>
 __device__ void win_produce(const WinParams &p, uint32_t sB, uint32_t sS, uint32_t sR,
                             uint64_t *full, uint64_t *empty, uint64_t *bres, uint64_t *rawbar,
-                            uint64_t *wbar, const WaitCtl &ctl) {
+                            const WaitCtl &ctl) {
     constexpr int ESZ = (int)sizeof(T);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t sS1 = sS + (uint32_t)p.R * p.strip_bytes;  // strip buffer 1
     const uint32_t raw_bytes = (uint32_t)p.raw_rows * (uint32_t)p.row_bytes;
     volatile int no_abort = 0;
     const WaitCtl drain{&no_abort, p.err, p.timeout_ns};  // waits for copies in flight
-    // Filters: bulk copy into strip buffer 1 (free until the second tile), or
-    // element loads from global memory.  Input rows of the first tile: bulk
-    // copy into staging buffer 0.
+    // The packed filter image: one bulk copy, completing on bres (the MMA
+    // issuer waits there).  Input rows of the first tile: staging buffer 0.
     int raw_issued = (p.x_raw && (int)blockIdx.x < p.num_tiles) ? 1 : 0, raw_done = 0;
     if (tid == 0) {
-        if (p.w_raw) {
-            mbar_arrive_expect_tx(wbar, (uint32_t)p.w_bytes);
-            bulk_load_1d(sS1, p.w, (uint32_t)p.w_bytes, wbar);
-        }
+        mbar_arrive_expect_tx(bres, (uint32_t)p.b_img_bytes);
+        bulk_load_1d(sB, p.wpack, (uint32_t)p.b_img_bytes, bres);
         if (raw_issued) issue_raw_rows(p, sR, win_tile(p, blockIdx.x), &rawbar[0], ESZ);
     }
-    bool ok = true;
-    if (p.w_raw) ok = producers_and(mbar_wait(wbar, 0u, ctl, 10));
-    if (!ok) {
-        if (tid == 0) {
-            mbar_wait(wbar, 0u, drain, 91);
-            if (raw_issued) mbar_wait(&rawbar[0], 0u, drain, 92);
-        }
-        return;
-    }
-    pack_filters<T>(p, sB, tid, p.w_raw ? sS1 : 0u, sS);  // table in strip buffer 0
-    fence_proxy_async_smem();
-    mbar_arrive(bres);
-    producers_and(true);  // every producer is done with strip buffers 0 and 1
     int it = 0;
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
         const int buf = it & 1;
@@ -471,9 +408,12 @@ __device__ void win_produce(const WinParams &p, uint32_t sB, uint32_t sS, uint32
         }
     }
     cp_async_commit_wait_all();  // nothing may land after the CTA exits
-    // after an early exit a bulk copy of input rows may still be in flight
-    if (tid == 0 && raw_issued > raw_done)
-        mbar_wait(&rawbar[raw_done & 1], (uint32_t)(raw_done >> 1) & 1u, drain, 93);
+    // after an early exit a bulk copy may still be in flight
+    if (tid == 0) {
+        if (raw_issued > raw_done)
+            mbar_wait(&rawbar[raw_done & 1], (uint32_t)(raw_done >> 1) & 1u, drain, 93);
+        mbar_wait(bres, 0u, drain, 94);
+    }
 }
 
 __device__ __forceinline__ bool win_drain(uint64_t *bar, uint32_t parity, const WinParams &p) {
@@ -699,8 +639,7 @@ __global__ void __launch_bounds__(WIN_THREADS, 1)
     uint64_t *mma_done = bars + 8;
     uint64_t *bres = bars + 9;
     uint64_t *rawbar = bars + 10;  // two: one per staging buffer
-    uint64_t *wbar = bars + 12;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 12);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -712,10 +651,9 @@ __global__ void __launch_bounds__(WIN_THREADS, 1)
             mbar_init(&tempty[i], 4u);
         }
         mbar_init(mma_done, 1u);
-        mbar_init(bres, PROD_THREADS);
+        mbar_init(bres, 1u);
         mbar_init(&rawbar[0], 1u);
         mbar_init(&rawbar[1], 1u);
-        mbar_init(wbar, 1u);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -731,9 +669,10 @@ __global__ void __launch_bounds__(WIN_THREADS, 1)
     const uint32_t sB = smem_u32(bptr), sS = smem_u32(sptr), sR = smem_u32(rptr);
 
     if (warp < MMA_WARP) {
-        win_produce<T>(p, sB, sS, sR, full, empty, bres, rawbar, wbar, ctl);
+        win_produce<T>(p, sB, sS, sR, full, empty, bres, rawbar, ctl);
     } else if (warp == MMA_WARP) {
-        if (lane == 0) win_mma<TF32>(p, tmem_base, sB, sS, full, empty, tfull, tempty, mma_done, bres, ctl);
+        if (lane == 0)
+            win_mma<TF32>(p, tmem_base, sB, sS, full, empty, tfull, tempty, mma_done, bres, ctl);
     } else {
         if (p.y_tma && lane == 0) prefetch_tmap(&tmY);
         win_epilogue(p, tmem_base, tfull, tempty, epi, &tmY, ctl);
@@ -814,8 +753,8 @@ bool window_plan(const ConvProblem &pb, WinParams *wp, size_t *smem_out) {
         p.x_raw = 1;
         base += 2 * p.raw_rows * rowb;
     }
-    // the filter pack's offset table lives in strip buffer 0 for a moment
-    if ((long long)p.steps * (32 / e) * 4 > (long long)pb.R * p.strip_bytes) return false;
+    // the packed filter image goes through the handle's repacking buffer
+    if ((long long)pb.R * p.steps * p.BN * 32 > DLC_WPACK_BYTES) return false;
     if (wp) *wp = p;
     if (smem_out) *smem_out = (size_t)base;
     return true;
@@ -877,24 +816,9 @@ dlcStatus_t dlc_launch_window(dlcContext *ctx, const ConvProblem &pb) {
         const char *ev = std::getenv("DLC_TC_WINRAW");
         if (!(ev && std::atoi(ev) != 0)) p.x_raw = 0;
     }
-    // the filter tensor as one dense block (some order of K, C, R, S)
-    {
-        long long st[4] = {pb.ws[0], pb.ws[1], pb.ws[2], pb.ws[3]};
-        long long ext[4] = {pb.K, pb.C, pb.R, pb.S};
-        int ord[4] = {0, 1, 2, 3};
-        std::sort(ord, ord + 4, [&](int a, int b) { return st[a] < st[b]; });
-        long long expect = 1;
-        bool dense = true;
-        for (int i = 0; i < 4; ++i) {
-            if (ext[ord[i]] > 1 && st[ord[i]] != expect) dense = false;
-            expect *= ext[ord[i]];
-        }
-        const long long wb = expect * e;
-        p.w_bytes = (int)wb;
-        p.w_raw = (dense && wb % 16 == 0 && ((uintptr_t)pb.w % 16) == 0 &&
-                   wb <= (long long)pb.R * p.strip_bytes && wb < (1LL << 30))
-                      ? 1 : 0;
-    }
+    if (!ctx->wpack) return DLC_STATUS_INTERNAL_ERROR;
+    p.wpack = ctx->wpack;
+    p.b_img_bytes = p.R * p.steps * p.BN * 32;
     p.y_tma = (win_y_tma_ok(pb) && smem + WIN_EPI_SMEM <= (size_t)WIN_MAX_SMEM) ? 1 : 0;
     if (const char *ev = std::getenv("DLC_TC_YTMA")) p.y_tma = p.y_tma && std::atoi(ev) != 0;
     if (p.y_tma) smem += WIN_EPI_SMEM;
@@ -930,6 +854,16 @@ dlcStatus_t dlc_launch_window(dlcContext *ctx, const ConvProblem &pb) {
                                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return DLC_STATUS_EXECUTION_FAILED;
+    }
+    {
+        const int words = p.R * p.steps * p.BN * 8;
+        const int blocks = (words + 255) / 256;
+        if (tf32)
+            window_pack_filters<uint32_t><<<blocks, 256, 0, ctx->stream>>>(p, static_cast<uint32_t *>(ctx->wpack));
+        else
+            window_pack_filters<uint16_t><<<blocks, 256, 0, ctx->stream>>>(p, static_cast<uint32_t *>(ctx->wpack));
+        if (cudaGetLastError() != cudaSuccess) return DLC_STATUS_EXECUTION_FAILED;
+        ctx->launches += 1;
     }
     int grid = p.num_tiles < ctx->sm_count ? p.num_tiles : ctx->sm_count;
     if (grid < 1) grid = 1;

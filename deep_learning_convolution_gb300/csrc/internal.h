@@ -47,6 +47,7 @@ struct dlcContext {
     uint64_t launches = 0;
     unsigned long long timeout_ns = 2000000000ull;  // pipeline wait limit
     int *sk_flags = nullptr;  // DLC_SK_FLAGS per-tile flags of split tiles (zero between launches)
+    void *wpack = nullptr;    // DLC_WPACK_BYTES: filters repacked for the window kernel
     int force_sk = 0;         // use the stream-K schedule whenever it is legal
     EncodeTiledFn encode_tiled = nullptr;
     EncodeIm2colFn encode_im2col = nullptr;
@@ -54,6 +55,9 @@ struct dlcContext {
 
 // Split-tile flags owned by a handle: at most this many tiles per launch use them.
 #define DLC_SK_FLAGS 4096
+// Device bytes a handle keeps for the window kernel's repacked filter image
+// (at most the shared memory of one CTA).
+#define DLC_WPACK_BYTES (256 * 1024)
 
 // A fully resolved forward problem (validated by the API layer).
 struct ConvProblem {

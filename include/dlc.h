@@ -39,7 +39,11 @@
  *    handle and reported as DLC_STATUS_EXECUTION_FAILED by the next launching
  *    call on that handle and by dlcSynchronize(), which clears them.
  *  - The library allocates no device memory on the forward path.  dlcCreate
- *    allocates one small mapped host word for device error reports.
+ *    allocates one small mapped host word for device error reports, the
+ *    split-tile flags and a 256 KiB device buffer where forward calls of the
+ *    few-channel kernel repack the filters before the convolution reads
+ *    them (so two calls on one handle must not overlap on the GPU: use one
+ *    handle per stream).
  *  - A handle is not thread-safe; use one handle per host thread.
  */
 #ifndef DLC_H_
@@ -129,8 +133,9 @@ dlcStatus_t dlcGetVersion(int *version);
 /* ---- handle ------------------------------------------------------------- */
 
 /* Creates a handle bound to the current CUDA device and the legacy default
- * stream.  Allocates the host-side context and one mapped host word for
- * device error reports.  BAD_PARAM if handle is NULL, NOT_SUPPORTED if the
+ * stream.  Allocates the host-side context, one mapped host word for
+ * device error reports, the split-tile flags and the 256 KiB filter-repacking
+ * buffer.  BAD_PARAM if handle is NULL, NOT_SUPPORTED if the
  * device is not compute capability 10.3, EXECUTION_FAILED on a CUDA error. */
 dlcStatus_t dlcCreate(dlcHandle_t *handle);
 
@@ -273,16 +278,18 @@ dlcStatus_t dlcDebugWaitTimeoutSelfTest(dlcHandle_t handle, int timeout_us);
  * allocate memory after start-up -- for example a serving process whose
  * memory is reserved once at start-up, or a plug-in inside a framework that
  * owns all device memory through its own allocator.  Such callers cannot
- * create a handle (dlcCreate allocates its error word and split-tile flags).
+ * create a handle (dlcCreate allocates its error word, split-tile flags and
+ * filter-repacking buffer).
  *
  * dlcConvolutionForwardNoAlloc computes y = alpha * conv(x, w) + beta * y like
  * dlcConvolutionForward, with tensor-core math only (TF32 or BF16; FP32 math
  * returns NOT_SUPPORTED), launched on `stream` (a cudaStream_t as void*,
  * NULL = legacy default stream) of the current device.  It allocates no host
  * or device memory and calls no allocating routine.  Besides x, w, y and
- * `status` it uses only a fixed scratch array compiled into the library
- * (DLC_NOALLOC_MAX_TILES split-tile flags and two error words); every GPU that
- * loads the library holds that array until the process exits.
+ * `status` it uses only fixed scratch arrays compiled into the library
+ * (DLC_NOALLOC_MAX_TILES split-tile flags and two error words, and 256 KiB
+ * where the few-channel kernel repacks the filters); every GPU that loads the
+ * library holds those arrays until the process exits.
  *
  * The tile schedule is stream-K whenever it is legal (beta == 0, FLOAT y, at
  * least one tile per SM): the CTAs of a launch meet through the scratch
@@ -292,7 +299,7 @@ dlcStatus_t dlcDebugWaitTimeoutSelfTest(dlcHandle_t handle, int timeout_us);
  *
  * The first call on a device sets that device up (it looks up the scratch
  * array's device address and the tensor-map encoders); make that first call
- * before any stream capture.  Every call reuses the same scratch array and
+ * before any stream capture.  Every call reuses the same scratch arrays and
  * clears its flags on `stream` before launching, so calls whose work overlaps
  * on the GPU (other streams, other host threads) race with each other: issue
  * them one at a time.
