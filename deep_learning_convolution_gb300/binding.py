@@ -41,12 +41,14 @@ DLC_KERNEL_TC_IM2COL = 2
 DLC_KERNEL_TC_GATHER = 3
 DLC_KERNEL_TC_GATHER_RUNS = 4
 DLC_KERNEL_TC_WINDOW = 5
+DLC_KERNEL_TC_IM2COL_PAIR = 6
 DLC_DEVERR_NONE = 0
 DLC_DEVERR_WAIT_TIMEOUT = 1
 
 KERNEL_NAMES = {DLC_KERNEL_NONE: "none", DLC_KERNEL_FFMA: "ffma",
                 DLC_KERNEL_TC_IM2COL: "tc_im2col", DLC_KERNEL_TC_GATHER: "tc_gather",
-                DLC_KERNEL_TC_GATHER_RUNS: "tc_runs", DLC_KERNEL_TC_WINDOW: "tc_window"}
+                DLC_KERNEL_TC_GATHER_RUNS: "tc_runs", DLC_KERNEL_TC_WINDOW: "tc_window",
+                DLC_KERNEL_TC_IM2COL_PAIR: "tc_im2col_pair"}
 
 _h = c_void_p          # opaque handle / descriptor
 _ph = POINTER(c_void_p)

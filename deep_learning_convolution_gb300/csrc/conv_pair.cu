@@ -1,0 +1,534 @@
+// conv_pair.cu -- the im2col implicit GEMM of conv_tc.cu on pairs of SMs:
+// tcgen05.mma with cta_group::2 (M = 256, 128 output pixels per SM).
+//
+// Same lowering as the single-SM im2col kernel (maxDNN page, method section:
+// an output coordinate is its receptive field times the filters; batch-reduce
+// GEMM page, method section: acc += sum_i A_i B_i^T over filter taps and
+// channel blocks; cuDNN page, method section: the lowered matrix exists only
+// as on-chip tiles).  What the pair changes is where the operands come from:
+// a cluster of two CTAs shares one MMA of M = 256 rows and N = BN filters.
+// Each CTA loads its own 128 rows of A (im2col TMA) and HALF of the BN filter
+// rows of B into its own shared memory, so per SM the operand traffic per
+// MMA falls from A + B to A + B/2 -- the single-SM kernel's stages are bound by
+// that traffic at BN = 192..256.
+//
+// Roles (per CTA, 6 warps): warp 0 lane 0 issues the TMA loads of both CTAs'
+// halves of a stage, which complete on the LEADER's (rank 0) full barrier;
+// warp 1 lane 0 of the leader alone issues the MMAs and commits each stage
+// back to the empty barriers of both CTAs (multicast); warps 2-5 of each CTA
+// read their CTA's 128 accumulator rows from tensor memory, apply the epilogue
+// and store y, then release the accumulator on the leader's barrier.  Every
+// wait is bounded; both CTAs meet at a cluster barrier before tensor memory is
+// released.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <type_traits>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace {
+
+using namespace dlc;
+
+constexpr int PBM = 128;                    // output pixels per CTA
+constexpr int PROW = 128;                   // bytes of one swizzled reduction row
+constexpr int PA_BYTES = PBM * PROW;        // A stage: 16 KiB
+constexpr int PAIR_THREADS = 192;
+constexpr int PAIR_MAX_SMEM = 232448;
+constexpr int PAIR_BAR_AREA = 256;
+constexpr int PAIR_EPI_BUF = 32 * 128;             // one warp's 32 rows x 32 FP32 columns
+constexpr int PAIR_EPI_SMEM = 4 * 2 * PAIR_EPI_BUF;  // 4 epilogue warps, double-buffered
+
+struct PairParams {
+    int N, C, H, W, K, R, S, P, Q;
+    int pt, pl, u, v, dh, dw;
+    long long M;  // N*P*Q
+    int PQ;
+    long long ys[4];
+    void *y;
+    const float *bias;
+    float alpha, beta;
+    int relu, y_bf16;
+    int y_tma;         // y through 2-D bulk tensor stores of 32 x 32 blocks
+    int BN;            // filters per pair tile (BN/2 per CTA)
+    int stages, num_kb, c_blocks, n_tiles;
+    int num_tiles;     // pair tiles: ceil(M / 256) * n_tiles
+    uint32_t idesc, tmem_cols, acc_stride;
+    int *err;
+    unsigned long long timeout_ns;
+};
+
+__device__ __forceinline__ bool pair_drain(uint64_t *bar, uint32_t parity, const PairParams &p) {
+    volatile int dummy = 0;
+    WaitCtl c{&dummy, p.err, p.timeout_ns};
+    return mbar_wait(bar, parity, c, 95);
+}
+
+template <int BK>
+__device__ void pair_produce(const PairParams &p, uint32_t rank, const CUtensorMap *tmA,
+                             const CUtensorMap *tmB, uint32_t sA, uint32_t sB, uint64_t *full,
+                             uint64_t *empty, const WaitCtl &ctl) {
+    const int ST = p.stages;
+    const uint32_t b_half = (uint32_t)(p.BN / 2) * PROW;
+    const uint32_t tx = 2u * (PA_BYTES + b_half);  // both CTAs' bytes land on the leader's barrier
+    const uint32_t full0 = mapa_shared(smem_u32(full), 0);  // the leader's full barriers
+    int stage = 0;
+    uint32_t ph = 0;
+    for (int t = (int)cluster_id_x(); t < p.num_tiles; t += (int)num_clusters_x()) {
+        const long long m0 = (long long)(t / p.n_tiles) * (2 * PBM) + (long long)rank * PBM;
+        const int k0 = (t % p.n_tiles) * p.BN + (int)rank * (p.BN / 2);
+        const int n0 = (int)(m0 / p.PQ);
+        const int rem = (int)(m0 - (long long)n0 * p.PQ);
+        const int p0 = rem / p.Q, q0 = rem - (rem / p.Q) * p.Q;
+        const int wc = q0 * p.v - p.pl;  // first window origin of this CTA's rows
+        const int hc = p0 * p.u - p.pt;
+        int cb = 0, s = 0, r = 0;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+            if (!mbar_wait(&empty[stage], ph ^ 1u, ctl, 1)) return;
+            if (rank == 0) mbar_arrive_expect_tx(&full[stage], tx);
+            tma_load_im2col_4d_pair(sA + (uint32_t)stage * PA_BYTES, tmA, full0 + 8u * stage, cb * BK,
+                                    wc, hc, n0, (uint16_t)(s * p.dw), (uint16_t)(r * p.dh));
+            tma_load_4d_pair(sB + (uint32_t)stage * b_half, tmB, full0 + 8u * stage, cb * BK, s, r, k0);
+            if (++stage == ST) stage = 0, ph ^= 1u;
+            if (++cb == p.c_blocks) {
+                cb = 0;
+                if (++s == p.S) s = 0, ++r;
+            }
+        }
+    }
+}
+
+template <bool TF32>
+__device__ void pair_mma(const PairParams &p, uint32_t tmem_base, uint32_t sA, uint32_t sB,
+                         uint64_t *full, uint64_t *empty, uint64_t *tfull, uint64_t *tempty,
+                         uint64_t *mma_done, const WaitCtl &ctl) {
+    const int ST = p.stages;
+    const uint32_t b_half = (uint32_t)(p.BN / 2) * PROW;
+    const uint64_t a0 = sw128_kmajor_desc(sA), b0 = sw128_kmajor_desc(sB);
+    const uint64_t a_step = PA_BYTES >> 4, b_step = b_half >> 4;
+    int stage = 0, it = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int t = (int)cluster_id_x(); ok && t < p.num_tiles; t += (int)num_clusters_x(), ++it) {
+        const int buf = it & 1;
+        const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+        if (!mbar_wait(&tempty[buf], aph ^ 1u, ctl, 3)) {
+            ok = false;
+            break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d = tmem_base + (uint32_t)buf * p.acc_stride;
+        uint64_t ad = a0 + a_step * stage, bd = b0 + b_step * stage;
+        uint32_t acc = 0;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+            if (!mbar_wait(&full[stage], ph, ctl, 4)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {  // 32 bytes of the 128-byte row each
+                if constexpr (TF32)
+                    umma_tf32_pair(d, ad + 2u * j, bd + 2u * j, p.idesc, acc);
+                else
+                    umma_bf16_pair(d, ad + 2u * j, bd + 2u * j, p.idesc, acc);
+                acc = 1;
+            }
+            umma_commit_pair(&empty[stage], 3);  // both CTAs' slots free once these are done
+            if (++stage == ST) {
+                stage = 0;
+                ph ^= 1u;
+                ad = a0;
+                bd = b0;
+            } else {
+                ad += a_step;
+                bd += b_step;
+            }
+        }
+        if (!ok) break;
+        umma_commit_pair(&tfull[buf], 3);  // both CTAs' accumulator rows are ready
+    }
+    if (!ok) {
+        // gave up: loads of either CTA issued for stages not consumed land on
+        // these barriers; wait for them briefly so no copy outlives the CTAs
+        volatile int dummy = 0;
+        const WaitCtl brief{&dummy, p.err, 50000000ull};
+        for (int j = 0; j < ST; ++j) {
+            if (!mbar_wait(&full[stage], ph, brief, 96)) break;
+            if (++stage == ST) stage = 0, ph ^= 1u;
+        }
+    }
+    // every MMA issued must complete before the pair releases tensor memory
+    umma_commit_pair(mma_done, 3);
+}
+
+__device__ __forceinline__ float pair_bf16_to_f32(unsigned short b) {
+    return __uint_as_float((uint32_t)b << 16);
+}
+
+__device__ __forceinline__ unsigned short pair_f32_to_bf16(float f) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// beta*y + bias and ReLU on alpha*acc, in place: columns k0 .. k0+31 of one pixel.
+__device__ __noinline__ void pair_epi_math(const PairParams &p, bool valid, long long ybase, int k0,
+                                           float (&val)[32]) {
+    const float *yf = static_cast<const float *>(p.y);
+    const unsigned short *yb = static_cast<const unsigned short *>(p.y);
+    for (int i = 0; i < 32; ++i) {
+        const int k = k0 + i;
+        float f = val[i];
+        if (valid && k < p.K) {
+            const long long yo = ybase + (long long)k * p.ys[1];
+            if (p.beta != 0.f) f = __fmaf_rn(p.beta, p.y_bf16 ? pair_bf16_to_f32(yb[yo]) : yf[yo], f);
+            if (p.bias) f += __ldg(p.bias + k);
+        }
+        if (p.relu) f = fmaxf(f, 0.f);
+        val[i] = f;
+    }
+}
+
+// alpha*acc + beta*y + bias, ReLU, store: columns k0 .. k0+31 of one output pixel.
+__device__ __noinline__ void pair_store_general(const PairParams &p, bool valid, long long ybase,
+                                                int k0, float (&val)[32]) {
+    float *yf = static_cast<float *>(p.y);
+    unsigned short *yb = static_cast<unsigned short *>(p.y);
+    if (!valid) return;
+    for (int i = 0; i < 32; ++i) {
+        const int k = k0 + i;
+        if (k >= p.K) break;
+        const long long yo = ybase + (long long)k * p.ys[1];
+        float f = val[i];
+        if (p.beta != 0.f) f = __fmaf_rn(p.beta, p.y_bf16 ? pair_bf16_to_f32(yb[yo]) : yf[yo], f);
+        if (p.bias) f += __ldg(p.bias + k);
+        if (p.relu) f = fmaxf(f, 0.f);
+        if (p.y_bf16)
+            yb[yo] = pair_f32_to_bf16(f);
+        else
+            yf[yo] = f;
+    }
+}
+
+// Row `lane` of a warp's 32 x 32 FP32 staging block, 128-byte swizzled like
+// the y tensor map (16-byte chunk j of row l at chunk j ^ (l % 8)).
+__device__ __forceinline__ void pair_stage_row(uint32_t buf, int lane, const float (&val)[32]) {
+    const uint32_t rowp = buf + (uint32_t)lane * 128u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(rowp + (((uint32_t)j ^ (lane & 7)) << 4)),
+                     "f"(val[4 * j]), "f"(val[4 * j + 1]), "f"(val[4 * j + 2]), "f"(val[4 * j + 3])
+                     : "memory");
+}
+
+__device__ void pair_epilogue(const PairParams &p, uint32_t rank, uint32_t tmem_base,
+                              uint64_t *tfull, uint64_t *tempty, uint32_t epi_smem,
+                              const CUtensorMap *tmY, const WaitCtl &ctl) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
+    const int row = quad * 32 + lane;
+    const bool plain = p.beta == 0.f && p.bias == nullptr && !p.relu && !p.y_bf16 && p.ys[1] == 1;
+    const uint32_t tempty0 = mapa_shared(smem_u32(tempty), 0);  // the leader's barriers
+    float *yf = static_cast<float *>(p.y);
+    const uint32_t my_bufs = epi_smem + (uint32_t)(quad * 2 * PAIR_EPI_BUF);
+    int nbuf = 0;
+    int it = 0;
+    for (int t = (int)cluster_id_x(); t < p.num_tiles; t += (int)num_clusters_x(), ++it) {
+        const int buf = it & 1;
+        const uint32_t ph = (uint32_t)(it >> 1) & 1u;
+        int okw = 0;
+        if (lane == 0) okw = mbar_wait(&tfull[buf], ph, ctl, 5) ? 1 : 0;
+        okw = __shfl_sync(0xffffffffu, okw, 0);
+        if (!okw) break;
+        __syncwarp();
+        tc_fence_after_sync();
+        const long long m = (long long)(t / p.n_tiles) * (2 * PBM) + (long long)rank * PBM + row;
+        const int kt = (t % p.n_tiles) * p.BN;
+        const bool valid = m < p.M;
+        long long ybase = 0;
+        if (valid) {
+            const int n = (int)(m / p.PQ);
+            const int rem = (int)(m - (long long)n * p.PQ);
+            const int op = rem / p.Q, oq = rem - op * p.Q;
+            ybase = (long long)n * p.ys[0] + (long long)op * p.ys[2] + (long long)oq * p.ys[3];
+        }
+        const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)buf * p.acc_stride;
+        for (int c0 = 0; c0 < p.BN && kt + c0 < p.K; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(taddr + (uint32_t)c0, v);
+            tmem_ld_wait();
+            float val[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) val[i] = p.alpha * __uint_as_float(v[i]);
+            const int k0 = kt + c0;
+            if (p.y_tma) {
+                if (m - lane >= p.M) continue;  // the warp's rows are all past M
+                if (!plain) {
+                    float lv[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) lv[i] = val[i];
+                    pair_epi_math(p, valid, ybase, k0, lv);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) val[i] = lv[i];
+                }
+                const uint32_t sb = my_bufs + (uint32_t)(nbuf & 1) * PAIR_EPI_BUF;
+                if (nbuf >= 2) {  // the store issued from this buffer two groups ago
+                    if (lane == 0) bulk_wait_group_read<1>();
+                    __syncwarp();
+                }
+                pair_stage_row(sb, lane, val);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {  // rows past M and columns past K are not written
+                    tma_store_2d_s(tmY, sb, k0, (int)(m - lane));
+                    bulk_commit_group();
+                }
+                ++nbuf;
+                continue;
+            }
+            if (plain && valid && k0 + 32 <= p.K &&
+                ((reinterpret_cast<uintptr_t>(yf + ybase + k0) & 15u) == 0)) {
+                float4 *dst = reinterpret_cast<float4 *>(yf + ybase + k0);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    dst[i] = make_float4(val[4 * i], val[4 * i + 1], val[4 * i + 2], val[4 * i + 3]);
+            } else {
+                float lv[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) lv[i] = val[i];
+                pair_store_general(p, valid, ybase, k0, lv);
+            }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty0 + 8u * buf);  // release on the leader
+    }
+    // staged stores must finish reading shared memory before the CTA exits
+    if (p.y_tma && lane == 0) bulk_wait_group_all();
+    __syncwarp();
+}
+
+template <bool TF32>
+__global__ void __launch_bounds__(PAIR_THREADS, 1)
+    conv_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmY) {
+    constexpr int BK = PROW / (TF32 ? 4 : 2);
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);  // same offset in both CTAs
+    const int ST = p.stages;
+    const uint32_t b_half = (uint32_t)(p.BN / 2) * PROW;
+    uint8_t *smA = smem;
+    uint8_t *smB = smA + (size_t)ST * PA_BYTES;
+    uint8_t *epi = smB + (size_t)ST * b_half;  // y staging (y_tma), 1024-aligned
+    uint64_t *bars = reinterpret_cast<uint64_t *>(epi + (p.y_tma ? PAIR_EPI_SMEM : 0));
+    uint64_t *full = bars;
+    uint64_t *empty = bars + ST;
+    uint64_t *tfull = bars + 2 * ST;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *mma_done = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < ST; ++i) {
+            mbar_init(&full[i], 1u);   // the leader's expect-tx arrival (+ both CTAs' bytes)
+            mbar_init(&empty[i], 1u);  // the leader's multicast commit
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tfull[i], 1u);
+            mbar_init(&tempty[i], 8u);  // four epilogue warps of each CTA (leader's copy)
+        }
+        mbar_init(mma_done, 1u);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, p.tmem_cols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers exist before any remote arrival
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    const WaitCtl ctl{abort_flag, p.err, p.timeout_ns};
+    const uint32_t sA = smem_u32(smA), sB = smem_u32(smB);
+
+    if (warp == 0) {
+        if (lane == 0) pair_produce<BK>(p, rank, &tmA, &tmB, sA, sB, full, empty, ctl);
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) pair_mma<TF32>(p, tmem_base, sA, sB, full, empty, tfull, tempty, mma_done, ctl);
+        // the leader's final commit reaches both CTAs; it also covers every
+        // stage the MMAs consumed, i.e. every load of either CTA
+        if (lane == 0) pair_drain(mma_done, 0u, p);
+    } else {
+        if (p.y_tma && lane == 0) prefetch_tmap(&tmY);
+        pair_epilogue(p, rank, tmem_base, tfull, tempty, smem_u32(epi), &tmY, ctl);
+    }
+    __syncwarp();
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync();  // neither CTA leaves while the pair's MMAs or loads may touch it
+    tc_fence_after_sync();
+    if (warp == 1) tmem_dealloc_pair(tmem_base, p.tmem_cols);
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+// The pair kernel serves every im2col-eligible problem unless DLC_TC_PAIR=0
+// or the context asks for the stream-K schedule (the single-SM kernel's).
+bool dlc_pair_enabled(const dlcContext *ctx) {
+    if (ctx && ctx->force_sk) return false;
+    const char *ev = std::getenv("DLC_TC_PAIR");
+    return !(ev && std::atoi(ev) == 0);
+}
+
+dlcStatus_t dlc_launch_pair(dlcContext *ctx, const ConvProblem &pb) {
+    const bool tf32 = pb.math == DLC_MATH_TF32;
+    const int e = tf32 ? 4 : 2;
+    const int BK = PROW / e;
+    PairParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.N = pb.N; p.C = pb.C; p.H = pb.H; p.W = pb.W; p.K = pb.K; p.R = pb.R; p.S = pb.S;
+    p.P = pb.P; p.Q = pb.Q;
+    p.pt = pb.pt; p.pl = pb.pl; p.u = pb.u; p.v = pb.v; p.dh = pb.dh; p.dw = pb.dw;
+    p.M = (long long)pb.N * pb.P * pb.Q;
+    p.PQ = pb.P * pb.Q;
+    for (int i = 0; i < 4; ++i) p.ys[i] = pb.ys[i];
+    p.y = pb.y; p.bias = pb.bias;
+    p.alpha = pb.alpha; p.beta = pb.beta; p.relu = pb.relu;
+    p.y_bf16 = pb.ydt == DLC_DATA_BFLOAT16;
+    // BN: a multiple of 32 (each CTA holds BN/2 filter rows, whole 16-row groups)
+    if (pb.K <= 256) {
+        p.BN = ((pb.K + 31) / 32) * 32;
+    } else {
+        p.BN = 256;
+        long long best = -1;
+        for (int bn : {256, 192, 128}) {
+            const long long pad = (long long)((pb.K + bn - 1) / bn) * bn;
+            if (best < 0 || pad < best) best = pad, p.BN = bn;
+        }
+    }
+    if (const char *ev = std::getenv("DLC_TC_PAIR_BN")) {
+        const int bn = std::atoi(ev);
+        if (bn >= 32 && bn <= 256 && bn % 32 == 0) p.BN = bn;
+    }
+    p.c_blocks = (pb.C + BK - 1) / BK;
+    p.num_kb = pb.R * pb.S * p.c_blocks;
+    p.n_tiles = (pb.K + p.BN - 1) / p.BN;
+    const long long m_pairs = (p.M + 2 * PBM - 1) / (2 * PBM);
+    if (m_pairs * p.n_tiles > 0x7fffffffLL) return DLC_STATUS_NOT_SUPPORTED;
+    p.num_tiles = (int)(m_pairs * p.n_tiles);
+    // y through bulk tensor stores: FP32, K contiguous, uniform pixel pitch
+    {
+        const bool dense = pb.ydt == DLC_DATA_FLOAT && pb.ys[1] == 1 && pb.ys[3] >= pb.K &&
+                           (pb.ys[3] * 4) % 16 == 0 && (pb.P <= 1 || pb.ys[2] == (long long)pb.Q * pb.ys[3]) &&
+                           (pb.N <= 1 || pb.ys[0] == (long long)pb.P * pb.Q * pb.ys[3]) &&
+                           ((uintptr_t)pb.y % 16) == 0 && p.M <= 0x7fffffffLL;
+        const char *ev = std::getenv("DLC_TC_PAIR_YTMA");  // =0 for direct stores
+        p.y_tma = (dense && !(ev && std::atoi(ev) == 0)) ? 1 : 0;
+    }
+    const int epi_bytes = p.y_tma ? PAIR_EPI_SMEM : 0;
+    const int stage_bytes = PA_BYTES + (p.BN / 2) * PROW;
+    // slack after the barriers: one more half filter tile, so that no operand
+    // read of the last stage can leave the CTA's shared memory
+    const int slack = (p.BN / 2) * PROW;
+    int st = (PAIR_MAX_SMEM - 1024 - PAIR_BAR_AREA - slack - epi_bytes) / stage_bytes;
+    p.stages = st > 8 ? 8 : st;
+    if (const char *ev = std::getenv("DLC_TC_STAGES")) {
+        const int s2 = std::atoi(ev);
+        if (s2 >= 2 && s2 < p.stages) p.stages = s2;
+    }
+    if (p.stages < 2) return DLC_STATUS_INTERNAL_ERROR;
+    const uint32_t fmt = tf32 ? 2u : 1u;
+    p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(p.BN >> 3) << 17) |
+              ((uint32_t)((2 * PBM) >> 4) << 24);
+    uint32_t cols = 32;
+    while (cols < (uint32_t)(2 * p.BN)) cols <<= 1;
+    p.tmem_cols = cols;
+    p.acc_stride = cols / 2;
+    p.err = ctx->d_err;
+    p.timeout_ns = ctx->timeout_ns;
+
+    // tensor maps: x through im2col (128 pixels x BK channels), w tiled with a
+    // box of BN/2 filters (one CTA's half)
+    CUtensorMap ta, tb;
+    std::memset(&ta, 0, sizeof(ta));
+    std::memset(&tb, 0, sizeof(tb));
+    const CUtensorMapDataType dt =
+        tf32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const cuuint64_t gdim[4] = {(cuuint64_t)pb.C, (cuuint64_t)pb.W, (cuuint64_t)pb.H, (cuuint64_t)pb.N};
+    const cuuint64_t gstr[3] = {(cuuint64_t)(pb.xs[3] * e), (cuuint64_t)(pb.xs[2] * e),
+                                (cuuint64_t)(pb.xs[0] * e)};
+    const int lower[2] = {-pb.pl, -pb.pt};
+    const int upper[2] = {pb.pr - pb.dw * (pb.S - 1), pb.pb - pb.dh * (pb.R - 1)};
+    const cuuint32_t estr[4] = {1, (cuuint32_t)pb.v, (cuuint32_t)pb.u, 1};
+    CUresult r = ctx->encode_im2col(&ta, dt, 4, const_cast<void *>(pb.x), gdim, gstr, lower, upper,
+                                    (cuuint32_t)BK, (cuuint32_t)PBM, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return DLC_STATUS_EXECUTION_FAILED;
+    const cuuint64_t wdim[4] = {(cuuint64_t)pb.C, (cuuint64_t)pb.S, (cuuint64_t)pb.R, (cuuint64_t)pb.K};
+    const cuuint64_t wstr[3] = {(cuuint64_t)(pb.ws[3] * e), (cuuint64_t)(pb.ws[2] * e),
+                                (cuuint64_t)(pb.ws[0] * e)};
+    const cuuint32_t box[4] = {(cuuint32_t)BK, 1, 1, (cuuint32_t)(p.BN / 2)};
+    const cuuint32_t ones[4] = {1, 1, 1, 1};
+    r = ctx->encode_tiled(&tb, dt, 4, const_cast<void *>(pb.w), wdim, wstr, box, ones,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return DLC_STATUS_EXECUTION_FAILED;
+
+    const size_t smem = 1024 + (size_t)p.stages * stage_bytes + epi_bytes + PAIR_BAR_AREA + slack;
+    CUtensorMap ty;
+    std::memset(&ty, 0, sizeof(ty));
+    if (p.y_tma) {
+        const cuuint64_t ydim[2] = {(cuuint64_t)pb.K, (cuuint64_t)p.M};
+        const cuuint64_t ystr[1] = {(cuuint64_t)(pb.ys[3] * 4)};
+        const cuuint32_t ybox[2] = {32, 32};
+        const cuuint32_t yones[2] = {1, 1};
+        if (ctx->encode_tiled(&ty, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, pb.y, ydim, ystr, ybox, yones,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return DLC_STATUS_EXECUTION_FAILED;
+    }
+    auto kern = tf32 ? conv_pair_kernel<true> : conv_pair_kernel<false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return DLC_STATUS_EXECUTION_FAILED;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(PAIR_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = ctx->stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // one pair per two SMs that can hold a cluster at once (persistent pairs)
+    int max_clusters = 0;
+    cfg.gridDim = dim3(2 * (ctx->sm_count / 2), 1, 1);
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, (const void *)kern, &cfg) != cudaSuccess ||
+        max_clusters < 1)
+        return DLC_STATUS_EXECUTION_FAILED;
+    const int clusters = std::min(max_clusters, std::max(1, p.num_tiles));
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    if (cudaLaunchKernelEx(&cfg, kern, p, ta, tb, ty) != cudaSuccess) return DLC_STATUS_EXECUTION_FAILED;
+    ctx->launches += 1;
+    return DLC_STATUS_SUCCESS;
+}

@@ -1238,10 +1238,10 @@ bool y_tma_ok(const ConvProblem &pb) {
 
 }  // namespace
 
-dlcKernel_t dlc_tc_variant(const dlcContext *, const ConvProblem &pb) {
+dlcKernel_t dlc_tc_variant(const dlcContext *ctx, const ConvProblem &pb) {
     if (!tc_math_ok(pb)) return DLC_KERNEL_NONE;
     if (!fits_i32((long long)pb.P * pb.Q)) return DLC_KERNEL_NONE;
-    if (im2col_ok(pb)) return DLC_KERNEL_TC_IM2COL;
+    if (im2col_ok(pb)) return dlc_pair_enabled(ctx) ? DLC_KERNEL_TC_IM2COL_PAIR : DLC_KERNEL_TC_IM2COL;
     if (dlc_window_ok(pb)) return DLC_KERNEL_TC_WINDOW;
     int a, b, c;
     if (runs_ok(pb, &a, &b, &c)) return DLC_KERNEL_TC_GATHER_RUNS;
@@ -1250,6 +1250,7 @@ dlcKernel_t dlc_tc_variant(const dlcContext *, const ConvProblem &pb) {
 
 dlcStatus_t dlc_launch_tc(dlcContext *ctx, const ConvProblem &pb, dlcKernel_t variant) {
     if (variant == DLC_KERNEL_TC_WINDOW) return dlc_launch_window(ctx, pb);
+    if (variant == DLC_KERNEL_TC_IM2COL_PAIR) return dlc_launch_pair(ctx, pb);
     int mode;
     if (variant == DLC_KERNEL_TC_IM2COL) mode = MODE_IM2COL;
     else if (variant == DLC_KERNEL_TC_GATHER_RUNS) mode = MODE_RUNS;

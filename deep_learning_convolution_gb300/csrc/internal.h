@@ -87,4 +87,7 @@ dlcStatus_t dlc_launch_wait_selftest(dlcContext *ctx, unsigned long long timeout
 // conv_window.cu: layers with few channels per horizontal stride step.
 bool dlc_window_ok(const ConvProblem &pb);
 dlcStatus_t dlc_launch_window(dlcContext *ctx, const ConvProblem &pb);
+// conv_pair.cu: the im2col lowering on pairs of SMs (DLC_TC_PAIR=0 turns it off).
+bool dlc_pair_enabled(const dlcContext *ctx);
+dlcStatus_t dlc_launch_pair(dlcContext *ctx, const ConvProblem &pb);
 

@@ -105,10 +105,13 @@ typedef enum {
     DLC_KERNEL_TC_GATHER_RUNS = 4, /* tcgen05 implicit GEMM, operands gathered as contiguous
                                      runs: (s,c) of a filter row for NHWC + KRSC, s of a
                                      (c,r) pair for NCHW + KCRS */
-    DLC_KERNEL_TC_WINDOW = 5      /* tcgen05 implicit GEMM for few channels per stride step
+    DLC_KERNEL_TC_WINDOW = 5,     /* tcgen05 implicit GEMM for few channels per stride step
                                      (v*C*element size <= 64 bytes, no horizontal dilation,
                                      K <= 256): lowered rows read in place from packed input
                                      rows in shared memory */
+    DLC_KERNEL_TC_IM2COL_PAIR = 6 /* the TC_IM2COL lowering on pairs of SMs (a cluster of two
+                                     CTAs shares each MMA of 256 output pixels; each CTA
+                                     loads half of the filter tile) */
 } dlcKernel_t;
 
 /* Device error codes recorded by kernels (dlcGetLastDeviceError). */

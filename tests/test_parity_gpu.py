@@ -85,9 +85,47 @@ IM2COL_CASES = [
 
 
 @pytest.mark.parametrize("layer", IM2COL_CASES, ids=lambda l: l.name)
-def test_tc_im2col_parity_full(handle, layer):
+def test_tc_im2col_parity_full(handle, layer, monkeypatch):
+    monkeypatch.setenv("DLC_TC_PAIR", "0")  # the single-SM kernel
     run_and_check(handle, layer, 1000 + IM2COL_CASES.index(layer), full=True,
                   expect_kernel="tc_im2col")
+
+
+# the same lowering on pairs of SMs (cta_group::2, M = 256 per MMA)
+PAIR_CASES = IM2COL_CASES + [
+    # more pair tiles than SM pairs (every cluster runs several), two filter tiles
+    L("pair_bf16_c64_k512_3x3_many", 24, 64, 28, 28, 512, 3, 3, **P(1, 1, 1, 1)),
+    # ragged: the last pair tile's second CTA has no rows at all
+    L("pair_bf16_c64_k64_3x3_ragged", 1, 64, 11, 11, 64, 3, 3, **P(1, 1, 1, 1)),
+]
+
+
+@pytest.mark.parametrize("bn", [None, 64], ids=["bn_auto", "bn64"])
+@pytest.mark.parametrize("layer", PAIR_CASES, ids=lambda l: l.name)
+def test_tc_im2col_pair_parity_full(handle, layer, bn, monkeypatch):
+    """Direct stores of y from the epilogue registers."""
+    monkeypatch.setenv("DLC_TC_PAIR_YTMA", "0")
+    if bn:
+        monkeypatch.setenv("DLC_TC_PAIR_BN", str(bn))
+    run_and_check(handle, layer, 1100 + PAIR_CASES.index(layer), full=True,
+                  expect_kernel="tc_im2col_pair")
+
+
+@pytest.mark.parametrize("layer", [PAIR_CASES[i] for i in (0, 1, 2, 5, 8, 9, 10)],
+                         ids=lambda l: l.name)
+def test_tc_im2col_pair_bulk_stores(handle, layer):
+    """y written through 2-D bulk tensor stores of 32 x 32 blocks (the default)."""
+    run_and_check(handle, layer, 1150 + PAIR_CASES.index(layer), full=True, with_bias=True,
+                  relu=True, expect_kernel="tc_im2col_pair")
+
+
+def test_tc_im2col_pair_epilogue(handle):
+    import torch
+    layer = IM2COL_CASES[1]
+    run_and_check(handle, layer, 1190, full=True, alpha=-0.5, beta=0.75, with_bias=True,
+                  relu=True, expect_kernel="tc_im2col_pair")
+    run_and_check(handle, layer, 1191, full=True, y_dtype=torch.bfloat16, beta=0.5,
+                  with_bias=True, y_axes="NCHW", expect_kernel="tc_im2col_pair")
 
 
 # ---------------------------------------------------------------------------
@@ -205,6 +243,10 @@ def test_kcrs_filters_with_nhwc_activations_use_gather(handle):
 @pytest.mark.parametrize("layer,view,kernel", [
     (L("bf16_c64_view", 2, 64, 12, 13, 80, 3, 3, **P(1, 1, 1, 1)), "chan_pad", "tc_im2col"),
     (L("bf16_c64_imgpad", 2, 64, 12, 13, 80, 3, 3, **P(1, 1, 1, 1)), "image_pad", "tc_im2col"),
+    (L("bf16_c64_view_pair", 2, 64, 12, 13, 80, 3, 3, **P(1, 1, 1, 1)), "chan_pad",
+     "tc_im2col_pair"),
+    (L("bf16_c64_imgpad_pair", 2, 64, 12, 13, 80, 3, 3, **P(1, 1, 1, 1)), "image_pad",
+     "tc_im2col_pair"),
     (L("bf16_c24_view", 2, 24, 12, 13, 48, 3, 3, **P(1, 1, 1, 1)), "chan_pad", "tc_gather"),
     (L("tf32_nchw_wview", 2, 4, 12, 13, 32, 3, 5, **P(1, 1, 2, 2), dtype="tf32",
        layout="NCHW"), "width_pad", "tc_runs"),
@@ -217,6 +259,8 @@ def test_kcrs_filters_with_nhwc_activations_use_gather(handle):
 def test_strided_views(handle, layer, view, kernel, monkeypatch):
     if kernel != "tc_window":
         monkeypatch.setenv("DLC_TC_WINDOW", "0")
+    if kernel == "tc_im2col":
+        monkeypatch.setenv("DLC_TC_PAIR", "0")
     run_and_check(handle, layer, 2600, full=True, view=view, expect_kernel=kernel)
 
 
@@ -240,6 +284,7 @@ SK_CASES = [
 def test_stream_k_parity_full(handle, layer, kw, monkeypatch):
     monkeypatch.setenv("DLC_TC_STREAMK", "1")
     monkeypatch.setenv("DLC_TC_WINDOW", "0")
+    monkeypatch.setenv("DLC_TC_PAIR", "0")
     run_and_check(handle, layer, 2700 + [c[0] for c in SK_CASES].index(layer), full=True, **kw)
 
 
@@ -249,6 +294,7 @@ def test_stream_k_is_deterministic_and_flags_reset(handle, monkeypatch):
     import torch
     from deep_learning_convolution_gb300 import api
     monkeypatch.setenv("DLC_TC_STREAMK", "1")
+    monkeypatch.setenv("DLC_TC_PAIR", "0")
     layer = SK_CASES[0][0]
     x, w, _ = synth.make_inputs(layer, 11)
     xt, wt = api.layer_tensors(layer, x, w, "cuda")
@@ -330,9 +376,9 @@ def test_full_workload_layer_sampled(handle, wl, j):
 def test_workspace_is_zero_and_kernel_choice(handle):
     import torch
     from deep_learning_convolution_gb300 import api
-    expect = {"alexnet": ["tc_window"] + ["tc_im2col"] * 4,
-              "overfeat": ["tc_window"] + ["tc_im2col"] * 4,
-              "resnet50": ["tc_im2col"] * len(synth.WORKLOADS["resnet50"]),
+    expect = {"alexnet": ["tc_window"] + ["tc_im2col_pair"] * 4,
+              "overfeat": ["tc_window"] + ["tc_im2col_pair"] * 4,
+              "resnet50": ["tc_im2col_pair"] * len(synth.WORKLOADS["resnet50"]),
               "speech": ["tc_runs", "tc_runs"], "tiny": ["ffma"]}
     for wl, kinds in expect.items():
         for layer, kind in zip(synth.WORKLOADS[wl], kinds):
