@@ -116,7 +116,7 @@ __device__ void pair_mma(const PairParams &p, uint32_t tmem_base, uint32_t sA, u
     for (int t = (int)cluster_id_x(); ok && t < p.num_tiles; t += (int)num_clusters_x(), ++it) {
         const int buf = it & 1;
         const uint32_t aph = (uint32_t)(it >> 1) & 1u;
-        if (!mbar_wait(&tempty[buf], aph ^ 1u, ctl, 3)) {
+        if (!mbar_wait_cluster(&tempty[buf], aph ^ 1u, ctl, 3)) {  // both CTAs' epilogues
             ok = false;
             break;
         }

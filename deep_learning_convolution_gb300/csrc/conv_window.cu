@@ -23,6 +23,10 @@
 // phase pixels of input row (p0+j)*u + r*dh - pt at pixel offset j*Qs; tile
 // rows past Q read pixels whose value does not matter and are not stored.
 //
+// CTA pairs (opt-in, DLC_TC_WINPAIR=1): a cluster of two CTAs shares
+// each MMA over M = 256 rows (one tile per CTA, tcgen05 cta_group::2); each CTA
+// packs its own strips and holds half of the filters.
+//
 // Roles (one persistent CTA per SM): eight producer warps pack the strips of
 // the next tile into one of two buffers (batched 4-/8-byte loads; padding and
 // the packing tail are zero-filled); one thread issues R*steps MMAs (32 bytes
@@ -68,8 +72,10 @@ struct WinParams {
     int x_raw;        // input rows are bulk-copied to shared memory, then repacked
     int raw_rows;     // input rows one tile spans: (J-1)*u + (R-1)*dh + 1
     const void *wpack;  // the filter slabs, packed by window_pack_filters
-    int b_img_bytes;    // their bytes: R*steps*BN rows of 32
-    int num_tiles;
+    int b_img_bytes;    // bytes of one CTA's part: R*steps*(BN/ctas) rows of 32
+    int pair;           // launched as CTA pairs (cta_group::2, M = 256 per MMA)
+    int num_tiles;      // 128-row tiles
+    int num_units;      // per-CTA work units: tiles, or pairs of tiles (pair)
     long long xs[4], ws[4], ys[4];
     const void *x;
     const void *w;
@@ -132,18 +138,6 @@ __device__ __forceinline__ uint32_t pack_word(const T (&e)[4 / sizeof(T)]) {
 // element by element -- phase pixel a, phase phi, channel c, tap s = v*a+phi --
 // and writes it a word at a time, sixteen words' loads in flight before their
 // stores.
-// Barrier of the eight producer warps (id 2) that also ANDs a predicate.
-__device__ __forceinline__ bool producers_and(bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 2, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}\n"
-        : "=r"(r)
-        : "r"((uint32_t)v)
-        : "memory");
-    return r != 0;
-}
-
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
     uint32_t v;
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
@@ -152,7 +146,8 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
 
 // The filter taps as MMA B operands, packed by a small kernel launched ahead
 // of the convolution into device memory, in the exact shared-memory image the
-// convolution then bulk-copies: slab (r, st) holds BN rows (filters) of the
+// convolution then bulk-copies (for CTA pairs: two images, each with its half
+// of the filters, one per CTA): slab (r, st) holds BN rows (filters) of the
 // 32 window bytes [32*st, 32*st + 32) of filter row r, 32-byte swizzled K-major
 // (row k at 32*k; its two 16-byte halves exchanged where address bit 7 is set,
 // which the image reproduces because the slabs start 256-byte aligned).  One
@@ -167,6 +162,9 @@ __global__ void window_pack_filters(const __grid_constant__ WinParams p, uint32_
     const int row = wi >> 3, wd = wi & 7;
     const int sl = row / p.BN, k = row - sl * p.BN;
     const int r = sl / p.steps, st = sl - r * p.steps;
+    // a pair's CTA `rank` holds filters [rank*BN/2, (rank+1)*BN/2) of every slab
+    const int bnc = p.pair ? p.BN / 2 : p.BN;
+    const int rank = k / bnc, row_cta = sl * bnc + (k - rank * bnc);
     T e[EPW];
 #pragma unroll
     for (int i = 0; i < EPW; ++i) {
@@ -180,7 +178,8 @@ __global__ void window_pack_filters(const __grid_constant__ WinParams p, uint32_
                       (long long)s * p.ws[3]]
                   : (T)0;
     }
-    const uint32_t off = (uint32_t)row * 32u + ((((uint32_t)(wd >> 2)) ^ ((uint32_t)(row >> 2) & 1u)) << 4) +
+    const uint32_t off = (uint32_t)rank * (uint32_t)p.b_img_bytes + (uint32_t)row_cta * 32u +
+                         ((((uint32_t)(wd >> 2)) ^ ((uint32_t)(row_cta >> 2) & 1u)) << 4) +
                          ((uint32_t)(wd & 3) << 2);
     img[off >> 2] = pack_word<T>(e);
 }
@@ -291,127 +290,187 @@ __device__ void pack_strips(const WinParams &p, uint32_t sbuf, const WinTile &wt
     }
 }
 
+__device__ __forceinline__ void sts128v(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
 // Repacks the R strips of one tile from its input rows staged in shared
-// memory at sR (row i = input row p0*u - pt + i, row_bytes each): the same
-// lane-to-word mapping as the word copy, four steps' loads before their
+// memory at sR (row i = input row p0*u - pt + i, row_bytes each).  Lane l of a
+// warp builds 16-byte chunk l % (D/16) of strip pixel l / (D/16) of each group
+// of 512/D pixels: up to four 4-byte loads from the staged row (zero outside
+// the row and past the data) and one 16-byte store, the chunk index XORed with
+// address bits 7.. of its pixel.  Two steps' loads are in flight before their
 // stores.
 __device__ void repack_strips(const WinParams &p, uint32_t sbuf, uint32_t sR, const WinTile &wt,
                               int warp, int lane) {
-    const int wpp = p.D >> 2;
-    const int dp = lane >> (p.d_log2 - 2), wp = lane & (wpp - 1);
-    const int G = 32 / wpp;
-    const uint32_t chmask = (uint32_t)(p.D >> 4) - 1u;
+    const int chl = p.d_log2 - 4;  // log2 of 16-byte chunks per phase pixel
+    const int kap = lane & ((1 << chl) - 1);
+    const int dp = lane >> chl;
+    const int G = 32 >> chl;       // strip pixels per warp step
+    const uint32_t chmask = (1u << chl) - 1u;
     const int q_need = p.Q + p.A - 1;
     const int nseg = p.R * p.J;
     const int lb = p.pl * p.C * (p.nb / (p.v * p.C));  // bytes of pl input pixels
-    const uint32_t inner = (uint32_t)(wp * 4);
+    const int b0 = kap * 16;                            // first byte of the chunk in its pixel
+    const int nwords = max(0, min(4, (p.nb - b0) >> 2)); // data words of the chunk
     const int gnb = G * p.nb;
+    const uint32_t rowb = (uint32_t)p.row_bytes;
+    // the tile's warp steps (segment by segment) split into eight equal ranges
+    const int nst0 = p.Qs / G;                                   // steps of a segment
+    const int nst_last = (p.strip_px - (p.J > 1 ? (p.J - 1) * p.Qs : 0)) / G;  // last of a strip
+    const int per_strip = (p.J - 1) * nst0 + nst_last;
+    const int total = p.R * per_strip;
+    const int lo = (int)(((long long)total * warp) / (PROD_THREADS / 32));
+    const int hi = (int)(((long long)total * (warp + 1)) / (PROD_THREADS / 32));
+    int seg_start = 0;
 #pragma unroll 1
-    for (int sg = warp; sg < nseg; sg += PROD_THREADS / 32) {
+    for (int sg = 0; sg < nseg && seg_start < hi; ++sg) {
         const int r = sg / p.J, j = sg - r * p.J;
+        const int nst_all = (j == p.J - 1) ? nst_last : nst0;
+        const int s_lo = max(0, lo - seg_start), nst = min(nst_all, hi - seg_start);
+        seg_start += nst_all;
+        if (s_lo >= nst) continue;
         const int pix0 = p.J > 1 ? j * p.Qs : 0;
-        const int nst = ((j == p.J - 1) ? p.strip_px - pix0 : p.Qs) / G;
         const int pr = wt.p0 + j;
         const int h = pr * p.u + r * p.dh - p.pt;
         const int P0 = (p.J > 1 ? 0 : wt.q0) + dp;
         int st_end = 0;
-        if (pr < p.P && h >= 0 && h < p.H && wp < p.nbw)
-            st_end = p.J > 1 ? max(0, (q_need - P0 + G - 1) / G) : nst;
-        const uint32_t rb = sR + (uint32_t)(j * p.u + r * p.dh) * (uint32_t)p.row_bytes;
-        int bt = P0 * p.nb - lb + (int)inner;
-        uint32_t paddr = sbuf + (uint32_t)r * p.strip_bytes + (uint32_t)(pix0 + dp) * p.D;
-        for (int st0 = 0; st0 < nst; st0 += 4) {
-            uint32_t v[4];
+        if (pr < p.P && h >= 0 && h < p.H && nwords > 0)
+            st_end = p.J > 1 ? max(0, (q_need - P0 + G - 1) / G) : nst_all;
+        const uint32_t rb = sR + (uint32_t)(j * p.u + r * p.dh) * rowb;
+        int bt = P0 * p.nb - lb + b0 + s_lo * gnb;
+        uint32_t paddr = sbuf + (uint32_t)r * p.strip_bytes + (uint32_t)(pix0 + dp) * p.D + 512u * s_lo;
+        for (int st0 = s_lo; st0 < nst; st0 += 2) {
+            uint32_t v[2][4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
+            for (int k = 0; k < 2; ++k) {
                 const int st = st0 + k, b = bt + k * gnb;
-                v[k] = (st < st_end && (unsigned)b < (unsigned)p.row_bytes) ? lds32(rb + b) : 0u;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    v[k][i] = (st < st_end && i < nwords && (unsigned)(b + 4 * i) < rowb) ? lds32(rb + b + 4 * i) : 0u;
             }
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint32_t pa = paddr + 128u * k;  // G pixels of D bytes per step
+            for (int k = 0; k < 2; ++k) {
+                const uint32_t pa = paddr + 512u * k;  // G pixels of D bytes per step
                 if (st0 + k < nst)
-                    sts32(pa + ((((inner >> 4) ^ ((pa >> 7) & chmask)) << 4) | (inner & 15u)), v[k]);
+                    sts128v(pa + (((uint32_t)kap ^ ((pa >> 7) & chmask)) << 4), v[k][0], v[k][1], v[k][2], v[k][3]);
             }
-            bt += 4 * gnb;
-            paddr += 512u;
+            bt += 2 * gnb;
+            paddr += 1024u;
         }
     }
 }
 
-// Bulk-copies the input rows of tile wt to sR; completes on rawbar.
-__device__ void issue_raw_rows(const WinParams &p, uint32_t sR, const WinTile &wt, uint64_t *rawbar,
-                               int esz) {
+// Bulk-copies the input rows of a tile to sR (row i = input row p0*u - pt + i)
+// as one copy of the rows inside the image -- they are consecutive in x --
+// completing on rawbar.  A tile past the last one (the second half of an odd
+// pair) loads nothing but still completes the barrier's phase.
+__device__ void issue_raw_rows(const WinParams &p, uint32_t sR, int tile, uint64_t *rawbar, int esz) {
+    int lo = 0, n = 0;
+    const WinTile wt = win_tile(p, tile < p.num_tiles ? tile : 0);
     const int h0 = wt.p0 * p.u - p.pt;
-    int valid = 0;
-    for (int i = 0; i < p.raw_rows; ++i)
-        valid += (h0 + i >= 0 && h0 + i < p.H) ? 1 : 0;
-    mbar_arrive_expect_tx(rawbar, (uint32_t)(valid * p.row_bytes));
-    const char *xb = static_cast<const char *>(p.x);
-    for (int i = 0; i < p.raw_rows; ++i) {
-        const int h = h0 + i;
-        if (h < 0 || h >= p.H) continue;
-        bulk_load_1d(sR + (uint32_t)i * (uint32_t)p.row_bytes,
-                     xb + ((long long)wt.n * p.xs[0] + (long long)h * p.xs[2]) * esz,
-                     (uint32_t)p.row_bytes, rawbar);
+    if (tile < p.num_tiles) {
+        lo = max(0, -h0);
+        n = min(p.raw_rows, p.H - h0) - lo;
+        if (n < 0) n = 0;
     }
+    const uint32_t bytes = (uint32_t)n * (uint32_t)p.row_bytes;
+    mbar_arrive_expect_tx(rawbar, bytes);
+    if (n > 0)
+        bulk_load_1d(sR + (uint32_t)lo * (uint32_t)p.row_bytes,
+                     static_cast<const char *>(p.x) +
+                         ((long long)wt.n * p.xs[0] + (long long)(h0 + lo) * p.xs[2]) * esz,
+                     bytes, rawbar);
 }
 
-template <typename T>
-__device__ void win_produce(const WinParams &p, uint32_t sB, uint32_t sS, uint32_t sR,
-                            uint64_t *full, uint64_t *empty, uint64_t *bres, uint64_t *rawbar,
+// Work units: a CTA takes units u = unit0, unit0 + stride, ...; unit u is tile
+// u, or for a pair tiles 2u (leader) and 2u + 1 (peer).
+template <bool PAIR>
+__device__ __forceinline__ int unit0() {
+    return PAIR ? (int)cluster_id_x() : (int)blockIdx.x;
+}
+template <bool PAIR>
+__device__ __forceinline__ int unit_stride() {
+    return PAIR ? (int)num_clusters_x() : (int)gridDim.x;
+}
+
+template <typename T, bool PAIR>
+__device__ void win_produce(const WinParams &p, uint32_t rank, uint32_t sB, uint32_t sS,
+                            uint32_t sR, uint64_t *full, uint64_t *empty, uint64_t *bres,
+                            uint64_t *bpeer, uint64_t *rawbar, uint64_t *rawfree,
                             const WaitCtl &ctl) {
     constexpr int ESZ = (int)sizeof(T);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t raw_bytes = (uint32_t)p.raw_rows * (uint32_t)p.row_bytes;
+    const uint32_t full_l = PAIR ? mapa_shared(smem_u32(full), 0) : smem_u32(full);  // leader's
     volatile int no_abort = 0;
     const WaitCtl drain{&no_abort, p.err, p.timeout_ns};  // waits for copies in flight
-    // The packed filter image: one bulk copy, completing on bres (the MMA
-    // issuer waits there).  Input rows of the first tile: staging buffer 0.
-    int raw_issued = (p.x_raw && (int)blockIdx.x < p.num_tiles) ? 1 : 0, raw_done = 0;
+    const int u0 = unit0<PAIR>(), us = unit_stride<PAIR>();
+    auto tile_of = [&](int u) { return PAIR ? 2 * u + (int)rank : u; };
+    // This CTA's part of the packed filter image: one bulk copy on bres.  Input
+    // rows of the first two units: staging buffers 0 and 1 (three in all).
+    int raw_issued = 0, raw_done = 0;
     if (tid == 0) {
         mbar_arrive_expect_tx(bres, (uint32_t)p.b_img_bytes);
-        bulk_load_1d(sB, p.wpack, (uint32_t)p.b_img_bytes, bres);
-        if (raw_issued) issue_raw_rows(p, sR, win_tile(p, blockIdx.x), &rawbar[0], ESZ);
+        bulk_load_1d(sB, static_cast<const char *>(p.wpack) + (size_t)rank * p.b_img_bytes,
+                     (uint32_t)p.b_img_bytes, bres);
+    }
+    if (p.x_raw) {
+        for (int k = 0; k < 2 && u0 + k * us < p.num_units; ++k) {
+            if (tid == 0) issue_raw_rows(p, sR + (uint32_t)k * raw_bytes, tile_of(u0 + k * us), &rawbar[k], ESZ);
+            ++raw_issued;
+        }
+    }
+    if (PAIR && rank == 1 && tid == 0) {  // the leader's MMAs read this CTA's filters too
+        if (mbar_wait(bres, 0u, ctl, 12)) mbar_arrive_cluster(mapa_shared(smem_u32(bpeer), 0));
     }
     int it = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+    for (int u = u0; u < p.num_units; u += us, ++it) {
         const int buf = it & 1;
         const uint32_t ph = (uint32_t)(it >> 1) & 1u;
         const uint32_t sbuf = sS + (uint32_t)(buf * p.R) * p.strip_bytes;
-        const WinTile wt = win_tile(p, t);
-        bool w_ok = mbar_wait(&empty[buf], ph ^ 1u, ctl, 1);
+        const int tile = tile_of(u);
+        bool ok = mbar_wait(&empty[buf], ph ^ 1u, ctl, 1);
+        if (p.x_raw) ok = ok && mbar_wait(&rawbar[it % 3], (uint32_t)(it / 3) & 1u, ctl, 11);
+        if (!ok) break;
+        if (p.x_raw) ++raw_done;
+        if (tile < p.num_tiles) {
+            const WinTile wt = win_tile(p, tile);
+            if (p.x_raw)
+                repack_strips(p, sbuf, sR + (uint32_t)(it % 3) * raw_bytes, wt, warp, lane);
+            else
+                pack_strips<T>(p, sbuf, wt, warp, lane);
+        }
+        cp_async_commit_wait_all();
+        fence_proxy_async_smem();
+        if (PAIR)
+            mbar_arrive_cluster(full_l + 8u * buf);  // every producer thread of both CTAs
+        else
+            mbar_arrive(&full[buf]);
         if (p.x_raw) {
-            // staging buffer `buf` holds this tile's rows (copy number it)
-            w_ok = w_ok && mbar_wait(&rawbar[buf], ph, ctl, 11);
-            if (!producers_and(w_ok)) break;  // every producer leaves together
-            ++raw_done;
-            // all producers are past the previous tile, so the other staging
-            // buffer is free: fetch the next tile's rows while this one is packed
-            if (t + (int)gridDim.x < p.num_tiles) {
+            mbar_arrive(&rawfree[it % 3]);  // this thread is done with the staged rows
+            // the rows of the unit after next go into the buffer of the previous
+            // unit once every producer has released it
+            if (u + 2 * us < p.num_units) {
                 ++raw_issued;
                 if (tid == 0) {
-                    fence_proxy_async_smem();
-                    issue_raw_rows(p, sR + (uint32_t)(buf ^ 1) * raw_bytes,
-                                   win_tile(p, t + gridDim.x), &rawbar[buf ^ 1], ESZ);
+                    const int prev = it - 1;
+                    if (prev < 0 || mbar_wait(&rawfree[prev % 3], (uint32_t)(prev / 3) & 1u, ctl, 14)) {
+                        fence_proxy_async_smem();
+                        issue_raw_rows(p, sR + (uint32_t)((it + 2) % 3) * raw_bytes, tile_of(u + 2 * us),
+                                       &rawbar[(it + 2) % 3], ESZ);
+                    } else {
+                        --raw_issued;
+                    }
                 }
             }
-            repack_strips(p, sbuf, sR + (uint32_t)buf * raw_bytes, wt, warp, lane);
-            fence_proxy_async_smem();
-            mbar_arrive(&full[buf]);
-        } else {
-            if (!w_ok) break;
-            pack_strips<T>(p, sbuf, wt, warp, lane);
-            cp_async_commit_wait_all();
-            fence_proxy_async_smem();
-            mbar_arrive(&full[buf]);
         }
     }
     cp_async_commit_wait_all();  // nothing may land after the CTA exits
-    // after an early exit a bulk copy may still be in flight
+    // after an early exit, bulk copies may still be in flight
     if (tid == 0) {
-        if (raw_issued > raw_done)
-            mbar_wait(&rawbar[raw_done & 1], (uint32_t)(raw_done >> 1) & 1u, drain, 93);
+        for (int j = raw_done; j < raw_issued; ++j) mbar_wait(&rawbar[j % 3], (uint32_t)(j / 3) & 1u, drain, 93);
         mbar_wait(bres, 0u, drain, 94);
     }
 }
@@ -422,27 +481,29 @@ __device__ __forceinline__ bool win_drain(uint64_t *bar, uint32_t parity, const 
     return mbar_wait(bar, parity, c, 90);
 }
 
-template <bool TF32>
+template <bool TF32, bool PAIR>
 __device__ void win_mma(const WinParams &p, uint32_t tmem_base, uint32_t sB, uint32_t sS,
                         uint64_t *full, uint64_t *empty, uint64_t *tfull, uint64_t *tempty,
-                        uint64_t *mma_done, uint64_t *bres, const WaitCtl &ctl) {
+                        uint64_t *mma_done, uint64_t *bres, uint64_t *bpeer, const WaitCtl &ctl) {
     // 64-bit descriptors advanced in place: the start address (16-byte units)
     // sits in the low bits and stays below 256 KiB, so the additions never
     // carry into other fields.  B slabs: 32-byte swizzle, 8-row groups 256
-    // bytes apart.
+    // bytes apart, BN/2 rows per CTA for a pair.
     const uint64_t b0 = (uint64_t)((sB >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)(256 >> 4) << 32) |
                         (1ull << 46) | (6ull << 29 << 32);
-    const uint64_t slab16 = (uint64_t)p.BN * 2u;  // slab bytes / 16
+    const uint64_t slab16 = (uint64_t)(PAIR ? p.BN / 2 : p.BN) * 2u;  // slab bytes / 16
     const uint64_t strip16 = (uint64_t)(p.strip_bytes >> 4);
     const int R = p.R, steps = p.steps;
     const uint32_t idesc = p.idesc;
     bool ok = mbar_wait(bres, 0u, ctl, 7);
+    if (PAIR) ok = ok && mbar_wait_cluster(bpeer, 0u, ctl, 13);
     int it = 0;
-    for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++it) {
+    for (int u = unit0<PAIR>(); ok && u < p.num_units; u += unit_stride<PAIR>(), ++it) {
         const int buf = it & 1;
         const uint32_t ph = (uint32_t)(it >> 1) & 1u;
-        if (!mbar_wait(&tempty[buf], ph ^ 1u, ctl, 3)) break;
-        if (!mbar_wait(&full[buf], ph, ctl, 4)) break;
+        // (pairs: the other CTA's epilogue and producers arrive remotely)
+        if (!(PAIR ? mbar_wait_cluster(&tempty[buf], ph ^ 1u, ctl, 3) : mbar_wait(&tempty[buf], ph ^ 1u, ctl, 3))) break;
+        if (!(PAIR ? mbar_wait_cluster(&full[buf], ph, ctl, 4) : mbar_wait(&full[buf], ph, ctl, 4))) break;
         tc_fence_after_sync();
         const uint32_t d = tmem_base + (uint32_t)buf * p.acc_stride;
         uint64_t a_row = p.a_hi | (uint64_t)(((sS + (uint32_t)(buf * R) * (uint32_t)p.strip_bytes) >> 4) & 0x3FFFu);
@@ -452,21 +513,35 @@ __device__ void win_mma(const WinParams &p, uint32_t tmem_base, uint32_t sB, uin
             uint64_t ad = a_row;
 #pragma unroll 4
             for (int st = 0; st < steps; ++st) {  // 32 bytes of window per MMA
-                if constexpr (TF32)
-                    umma_tf32_nc(d, ad, bd, idesc, acc);
-                else
-                    umma_bf16_nc(d, ad, bd, idesc, acc);
+                if constexpr (PAIR) {
+                    if constexpr (TF32)
+                        umma_tf32_pair(d, ad, bd, idesc, acc);
+                    else
+                        umma_bf16_pair(d, ad, bd, idesc, acc);
+                } else {
+                    if constexpr (TF32)
+                        umma_tf32_nc(d, ad, bd, idesc, acc);
+                    else
+                        umma_bf16_nc(d, ad, bd, idesc, acc);
+                }
                 acc = 1;
                 ad += 2;
                 bd += slab16;
             }
         }
-        umma_commit(&empty[buf]);  // strip buffer free once these MMAs are done
-        umma_commit(&tfull[buf]);  // accumulator ready for the epilogue
+        if (PAIR) {
+            umma_commit_pair(&empty[buf], 3);  // both CTAs' strip buffers free
+            umma_commit_pair(&tfull[buf], 3);  // both CTAs' accumulator rows ready
+        } else {
+            umma_commit(&empty[buf]);
+            umma_commit(&tfull[buf]);
+        }
     }
     // Every MMA issued must complete before tensor memory is released.
-    umma_commit(mma_done);
-    win_drain(mma_done, 0u, p);
+    if (PAIR)
+        umma_commit_pair(mma_done, 3);
+    else
+        umma_commit(mma_done);
 }
 
 // Row `lane` of a warp's 32 x 32 FP32 staging block, in the 128-byte swizzle
@@ -531,7 +606,8 @@ __device__ __noinline__ void win_store_direct(const WinParams &p, long long ybas
     }
 }
 
-__device__ void win_epilogue(const WinParams &p, uint32_t tmem_base, uint64_t *tfull,
+template <bool PAIR>
+__device__ void win_epilogue(const WinParams &p, uint32_t rank, uint32_t tmem_base, uint64_t *tfull,
                              uint64_t *tempty, uint8_t *epi_smem, const CUtensorMap *tmY,
                              const WaitCtl &ctl) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -540,18 +616,21 @@ __device__ void win_epilogue(const WinParams &p, uint32_t tmem_base, uint64_t *t
     const bool plain = p.beta == 0.f && p.bias == nullptr && !p.relu;
     uint8_t *my_buf = epi_smem + quad * WIN_EPI_BUF;
     const int kend = min(p.BN, ((p.K + 31) / 32) * 32);
+    const uint32_t tempty_l = PAIR ? mapa_shared(smem_u32(tempty), 0) : smem_u32(tempty);
     int nbuf = 0;
     int it = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+    for (int u = unit0<PAIR>(); u < p.num_units; u += unit_stride<PAIR>(), ++it) {
         const int buf = it & 1;
         const uint32_t ph = (uint32_t)(it >> 1) & 1u;
+        const int t = PAIR ? 2 * u + (int)rank : u;
         int okw = 0;
         if (lane == 0) okw = mbar_wait(&tfull[buf], ph, ctl, 5) ? 1 : 0;
         okw = __shfl_sync(0xffffffffu, okw, 0);
         if (!okw) break;
         __syncwarp();
         tc_fence_after_sync();
-        const WinTile wt = win_tile(p, t);
+        const bool have = t < p.num_tiles;  // a pair's second tile may not exist
+        const WinTile wt = win_tile(p, have ? t : 0);
         int j, q, qw;
         if (p.J > 1) {
             j = row >> p.qs_log2;
@@ -565,7 +644,7 @@ __device__ void win_epilogue(const WinParams &p, uint32_t tmem_base, uint64_t *t
         const int pr = wt.p0 + j;
         // the same for the whole warp (Qs >= 32): its output row exists and
         // holds at least one of the warp's pixels
-        const bool row_in = pr < p.P && qw < p.Q;
+        const bool row_in = have && pr < p.P && qw < p.Q;
         const bool valid = row_in && q < p.Q;
         const long long ybase =
             (long long)wt.n * p.ys[0] + (long long)pr * p.ys[2] + (long long)q * p.ys[3];
@@ -611,77 +690,101 @@ __device__ void win_epilogue(const WinParams &p, uint32_t tmem_base, uint64_t *t
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[buf]);
+        if (lane == 0) {
+            if (PAIR)
+                mbar_arrive_cluster(tempty_l + 8u * buf);  // released on the leader
+            else
+                mbar_arrive(&tempty[buf]);
+        }
     }
     // staged stores must finish reading shared memory before the CTA exits
     if (p.y_tma && lane == 0) bulk_wait_group_all();
     __syncwarp();
 }
 
-template <bool TF32>
+template <bool TF32, bool PAIR>
 __global__ void __launch_bounds__(WIN_THREADS, 1)
     conv_window_kernel(const __grid_constant__ WinParams p, const __grid_constant__ CUtensorMap tmY) {
     using T = typename std::conditional<TF32, uint32_t, uint16_t>::type;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
-    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);  // same offset in both CTAs
     uint8_t *epi = smem;  // y staging (1024-aligned)
     uint8_t *bptr = epi + (p.y_tma ? WIN_EPI_SMEM : 0);
-    const size_t b_bytes = (((size_t)p.R * p.steps * p.BN * 32) + 1023) & ~(size_t)1023;
+    const size_t b_bytes = ((size_t)p.b_img_bytes + 1023) & ~(size_t)1023;
     uint8_t *sptr = bptr + b_bytes;
-    uint8_t *rptr = sptr + (size_t)2 * p.R * p.strip_bytes;  // staged input rows, 2 buffers
+    uint8_t *rptr = sptr + (size_t)2 * p.R * p.strip_bytes;  // staged input rows, 3 buffers
     uint64_t *bars = reinterpret_cast<uint64_t *>(
-        rptr + (p.x_raw ? (size_t)2 * p.raw_rows * p.row_bytes : 0));
+        rptr + (p.x_raw ? (size_t)3 * p.raw_rows * p.row_bytes : 0));
     uint64_t *full = bars;
     uint64_t *empty = bars + 2;
     uint64_t *tfull = bars + 4;
     uint64_t *tempty = bars + 6;
     uint64_t *mma_done = bars + 8;
     uint64_t *bres = bars + 9;
-    uint64_t *rawbar = bars + 10;  // two: one per staging buffer
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 12);
+    uint64_t *bpeer = bars + 10;
+    uint64_t *rawbar = bars + 11;   // three: one per staging buffer (rows landed)
+    uint64_t *rawfree = bars + 14;  // three: every producer done with the buffer
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 17);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&full[i], PROD_THREADS);
+            mbar_init(&full[i], PAIR ? 2u * PROD_THREADS : PROD_THREADS);  // every producer
             mbar_init(&empty[i], 1u);
             mbar_init(&tfull[i], 1u);
-            mbar_init(&tempty[i], 4u);
+            mbar_init(&tempty[i], PAIR ? 8u : 4u);  // the epilogue warps (of both CTAs)
         }
         mbar_init(mma_done, 1u);
         mbar_init(bres, 1u);
-        mbar_init(&rawbar[0], 1u);
-        mbar_init(&rawbar[1], 1u);
+        mbar_init(bpeer, 1u);
+        for (int i = 0; i < 3; ++i) {
+            mbar_init(&rawbar[i], 1u);
+            mbar_init(&rawfree[i], PROD_THREADS);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == MMA_WARP) {
-        tmem_alloc(tmem_slot, p.tmem_cols);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(tmem_slot, p.tmem_cols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, p.tmem_cols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before_sync();
     __syncthreads();
+    if (PAIR) cluster_sync();  // both CTAs' barriers exist before any remote arrival
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
     const WaitCtl ctl{abort_flag, p.err, p.timeout_ns};
     const uint32_t sB = smem_u32(bptr), sS = smem_u32(sptr), sR = smem_u32(rptr);
 
     if (warp < MMA_WARP) {
-        win_produce<T>(p, sB, sS, sR, full, empty, bres, rawbar, ctl);
+        win_produce<T, PAIR>(p, rank, sB, sS, sR, full, empty, bres, bpeer, rawbar, rawfree, ctl);
     } else if (warp == MMA_WARP) {
-        if (lane == 0)
-            win_mma<TF32>(p, tmem_base, sB, sS, full, empty, tfull, tempty, mma_done, bres, ctl);
+        if (lane == 0 && rank == 0)
+            win_mma<TF32, PAIR>(p, tmem_base, sB, sS, full, empty, tfull, tempty, mma_done, bres, bpeer, ctl);
+        if (lane == 0) win_drain(mma_done, 0u, p);  // the (leader's) final commit reaches this CTA
     } else {
         if (p.y_tma && lane == 0) prefetch_tmap(&tmY);
-        win_epilogue(p, tmem_base, tfull, tempty, epi, &tmY, ctl);
+        win_epilogue<PAIR>(p, rank, tmem_base, tfull, tempty, epi, &tmY, ctl);
     }
     __syncwarp();
     tc_fence_before_sync();
     __syncthreads();
+    if (PAIR) cluster_sync();  // neither CTA leaves while the pair's MMAs may read it
     tc_fence_after_sync();
-    if (warp == MMA_WARP) tmem_dealloc(tmem_base, p.tmem_cols);
+    if (warp == MMA_WARP) {
+        if (PAIR)
+            tmem_dealloc_pair(tmem_base, p.tmem_cols);
+        else
+            tmem_dealloc(tmem_base, p.tmem_cols);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -729,7 +832,12 @@ bool window_plan(const ConvProblem &pb, WinParams *wp, size_t *smem_out) {
     // the last MMA step of a row may read past pixel A-1 (16-byte pixels come
     // in pairs); those pixels carry zero weights but must hold finite data
     p.strip_px = WBM - 1 + (p.steps * 32 + D - 1) / D;
-    p.strip_px = ((p.strip_px + 128 / D - 1) / (128 / D)) * (128 / D);  // whole warp steps
+    // whole warp steps: 4-byte words per lane (128/D pixels per step), or
+    // 16-byte chunks per lane when input rows are staged (512/D pixels)
+    const char *raw_ev = std::getenv("DLC_TC_WINRAW");
+    const bool raw_on = raw_ev && std::atoi(raw_ev) != 0;
+    const int step_px = raw_on ? 512 / D : 128 / D;
+    p.strip_px = ((p.strip_px + step_px - 1) / step_px) * step_px;
     const int span = D == 64 ? 512 : 256;
     p.strip_bytes = ((p.strip_px * D + span - 1) / span) * span;
     const int G = 128 / D;
@@ -737,24 +845,37 @@ bool window_plan(const ConvProblem &pb, WinParams *wp, size_t *smem_out) {
     if ((long long)pb.N * p.PB * p.segs > 0x7fffffffLL) return false;
     p.num_tiles = pb.N * p.PB * p.segs;
     p.BN = ((pb.K + 15) / 16) * 16;
-    const long long b_bytes = (((long long)pb.R * p.steps * p.BN * 32) + 1023) & ~1023LL;
+    // CTA pairs share each MMA (M = 256) and split the filters.  The kernel is
+    // producer-bound at N = 64 (packing, not MMA, sets the tile period), and
+    // pairing two SMs' producers measured slower, so pairs are opt-in:
+    // DLC_TC_WINPAIR=1.
+    {
+        const char *ev = std::getenv("DLC_TC_WINPAIR");
+        p.pair = (p.num_tiles >= 2 && ev && std::atoi(ev) != 0) ? 1 : 0;
+    }
+    p.num_units = p.pair ? (p.num_tiles + 1) / 2 : p.num_tiles;
+    p.b_img_bytes = pb.R * p.steps * (p.pair ? p.BN / 2 : p.BN) * 32;
+    const long long b_bytes = ((long long)p.b_img_bytes + 1023) & ~1023LL;
     const long long strips = 2LL * pb.R * p.strip_bytes;
     if ((long long)pb.R * p.strip_px * 4 > 0x7fffffffLL) return false;
     long long base = 1024 + b_bytes + strips + WIN_BAR_AREA;
     if (base > WIN_MAX_SMEM) return false;
     // Input rows staged whole by bulk copies: channels-innermost (or C == 1)
-    // dense rows whose starts and lengths are 16-byte multiples.
+    // dense rows whose starts and lengths are 16-byte multiples.  Measured
+    // slower than the 4-byte copies, so opt-in (DLC_TC_WINRAW=1); its shared
+    // memory is reserved only then.
     p.raw_rows = (p.J - 1) * pb.u + (pb.R - 1) * pb.dh + 1;
     const long long rowb = (long long)pb.W * pb.C * e;
     const bool rows_dense = (pb.C == 1 && pb.xs[3] == 1) || (pb.xs[1] == 1 && pb.xs[3] == pb.C);
-    if (rows_dense && rowb % 16 == 0 && (pb.xs[0] * e) % 16 == 0 && (pb.xs[2] * e) % 16 == 0 &&
-        p.raw_rows * rowb < (1LL << 20) && base + 2 * p.raw_rows * rowb <= WIN_MAX_SMEM &&
+    if (raw_on && rows_dense && pb.xs[2] == (long long)pb.W * pb.xs[3] && rowb % 16 == 0 &&
+        (pb.xs[0] * e) % 16 == 0 && (pb.xs[2] * e) % 16 == 0 &&
+        p.raw_rows * rowb < (1LL << 20) && base + 3 * p.raw_rows * rowb <= WIN_MAX_SMEM &&
         ((long long)pb.pl * pb.C * e) % 4 == 0 && nb % 4 == 0) {
         p.x_raw = 1;
-        base += 2 * p.raw_rows * rowb;
+        base += 3 * p.raw_rows * rowb;
     }
     // the packed filter image goes through the handle's repacking buffer
-    if ((long long)pb.R * p.steps * p.BN * 32 > DLC_WPACK_BYTES) return false;
+    if ((long long)pb.R * p.steps * p.BN * 32 > DLC_WPACK_BYTES) return false;  // both parts
     if (wp) *wp = p;
     if (smem_out) *smem_out = (size_t)base;
     return true;
@@ -773,13 +894,38 @@ bool win_y_tma_ok(const ConvProblem &pb) {
 }
 
 template <bool TF32>
-cudaError_t win_launch(const WinParams &p, const CUtensorMap &ty, int grid, size_t smem,
+cudaError_t win_launch(const WinParams &p, const CUtensorMap &ty, int sm_count, size_t smem,
                        cudaStream_t st) {
-    auto kern = conv_window_kernel<TF32>;
+    if (!p.pair) {
+        auto kern = conv_window_kernel<TF32, false>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        const int grid = std::max(1, std::min(p.num_units, sm_count));
+        kern<<<grid, WIN_THREADS, smem, st>>>(p, ty);
+        return cudaGetLastError();
+    }
+    auto kern = conv_window_kernel<TF32, true>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, WIN_THREADS, smem, st>>>(p, ty);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(WIN_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(2 * (sm_count / 2), 1, 1);
+    int max_clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&max_clusters, (const void *)kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (max_clusters < 1) return cudaErrorLaunchOutOfResources;
+    cfg.gridDim = dim3(2 * std::min(max_clusters, p.num_units), 1, 1);
+    return cudaLaunchKernelEx(&cfg, kern, p, ty);
 }
 
 }  // namespace
@@ -810,22 +956,15 @@ dlcStatus_t dlc_launch_window(dlcContext *ctx, const ConvProblem &pb) {
                    ? 1 : 0;
     p.row_bytes = (int)((long long)pb.W * pb.C * e);
     if (p.x_raw && ((uintptr_t)pb.x % 16) != 0) p.x_raw = 0;  // smem stays reserved
-    // Staging whole rows measured slower than the 4-byte copies (the staging
-    // needs a producer-wide barrier per tile), so it is opt-in: DLC_TC_WINRAW=1.
-    {
-        const char *ev = std::getenv("DLC_TC_WINRAW");
-        if (!(ev && std::atoi(ev) != 0)) p.x_raw = 0;
-    }
     if (!ctx->wpack) return DLC_STATUS_INTERNAL_ERROR;
     p.wpack = ctx->wpack;
-    p.b_img_bytes = p.R * p.steps * p.BN * 32;
     p.y_tma = (win_y_tma_ok(pb) && smem + WIN_EPI_SMEM <= (size_t)WIN_MAX_SMEM) ? 1 : 0;
     if (const char *ev = std::getenv("DLC_TC_YTMA")) p.y_tma = p.y_tma && std::atoi(ev) != 0;
     if (p.y_tma) smem += WIN_EPI_SMEM;
 
     const uint32_t fmt = tf32 ? 2u : 1u;
     p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(p.BN >> 3) << 17) |
-              ((uint32_t)(WBM >> 4) << 24);
+              ((uint32_t)((p.pair ? 2 * WBM : WBM) >> 4) << 24);
     uint32_t cols = 32;
     while (cols < (uint32_t)(2 * p.BN)) cols <<= 1;
     p.tmem_cols = cols;
@@ -865,10 +1004,8 @@ dlcStatus_t dlc_launch_window(dlcContext *ctx, const ConvProblem &pb) {
         if (cudaGetLastError() != cudaSuccess) return DLC_STATUS_EXECUTION_FAILED;
         ctx->launches += 1;
     }
-    int grid = p.num_tiles < ctx->sm_count ? p.num_tiles : ctx->sm_count;
-    if (grid < 1) grid = 1;
-    cudaError_t err = tf32 ? win_launch<true>(p, ty, grid, smem, ctx->stream)
-                           : win_launch<false>(p, ty, grid, smem, ctx->stream);
+    cudaError_t err = tf32 ? win_launch<true>(p, ty, ctx->sm_count, smem, ctx->stream)
+                           : win_launch<false>(p, ty, ctx->sm_count, smem, ctx->stream);
     if (err != cudaSuccess) return DLC_STATUS_EXECUTION_FAILED;
     ctx->launches += 1;
     return DLC_STATUS_SUCCESS;

@@ -94,6 +94,39 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
     }
 }
 
+// The same wait with cluster-scope acquire: for a barrier that receives
+// arrivals released by threads of the other CTA of a pair, whose shared-memory
+// writes the waiting side then reads (directly or through the tensor core).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, const WaitCtl &ctl,
+                                                  int where) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    uint32_t n = 0;
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((++n & 31u) == 0) {
+            if (*ctl.abort_flag) return false;
+            if (globaltimer_ns() - t0 > ctl.timeout_ns) {
+                *ctl.abort_flag = 1;
+                record_error(ctl.err, 1 /* DLC_DEVERR_WAIT_TIMEOUT */, where);
+                return false;
+            }
+        }
+    }
+}
+
 // ---- proxy fences -----------------------------------------------------------
 // Makes this thread's generic-proxy shared-memory writes visible to the async
 // proxy (TMA, tcgen05.mma operand reads).

@@ -190,6 +190,10 @@ WINDOW_CASES = [
       dtype="tf32", layout="NCHW"),
     # 1x1 filters, more tiles than SMs
     L("win_bf16_c4_k16_1x1_many", 40, 4, 30, 30, 16, 1, 1),
+    # an odd number of tiles (5): the last CTA pair has one tile
+    L("win_bf16_c3_k64_11x11_s4_odd_tiles", 1, 3, 75, 67, 64, 11, 11, **P(2, 2, 2, 2), u=4, v=4),
+    # a single tile: one CTA, no pair
+    L("win_bf16_c3_k32_5x5_one_tile", 1, 3, 9, 9, 32, 5, 5, **P(2, 2, 2, 2)),
 ]
 
 
@@ -199,12 +203,23 @@ def test_tc_window_parity_full(handle, layer):
                   expect_kernel="tc_window")
 
 
-@pytest.mark.parametrize("layer", [WINDOW_CASES[i] for i in (0, 1, 4, 5, 12)],
+@pytest.mark.parametrize("pair", ["1", "0"], ids=["pairs", "single"])
+@pytest.mark.parametrize("layer", [WINDOW_CASES[i] for i in (0, 1, 4, 5, 12, 15)],
                          ids=lambda l: l.name)
-def test_tc_window_staged_rows(handle, layer, monkeypatch):
+def test_tc_window_staged_rows(handle, layer, pair, monkeypatch):
     """Input rows bulk-copied to shared memory and repacked there (opt-in)."""
     monkeypatch.setenv("DLC_TC_WINRAW", "1")
+    monkeypatch.setenv("DLC_TC_WINPAIR", pair)
     run_and_check(handle, layer, 2350 + WINDOW_CASES.index(layer), full=True,
+                  expect_kernel="tc_window")
+
+
+@pytest.mark.parametrize("layer", [WINDOW_CASES[i] for i in (0, 2, 5, 7, 12, 13, 15, 16)],
+                         ids=lambda l: l.name)
+def test_tc_window_cta_pairs(handle, layer, monkeypatch):
+    """CTA pairs sharing each MMA over 256 rows (opt-in)."""
+    monkeypatch.setenv("DLC_TC_WINPAIR", "1")
+    run_and_check(handle, layer, 2370 + WINDOW_CASES.index(layer), full=True,
                   expect_kernel="tc_window")
 
 
