@@ -71,6 +71,7 @@ struct WinParams {
     int row_bytes;    // bytes of one input row (x_word)
     int x_raw;        // input rows are bulk-copied to shared memory, then repacked
     int raw_rows;     // input rows one tile spans: (J-1)*u + (R-1)*dh + 1
+    int raw_bufs;     // staging buffers (2 or 3): rows are fetched raw_bufs-1 units ahead
     const void *wpack;  // the filter slabs, packed by window_pack_filters
     int b_img_bytes;    // bytes of one CTA's part: R*steps*(BN/ctas) rows of 32
     int pair;           // launched as CTA pairs (cta_group::2, M = 256 per MMA)
@@ -409,7 +410,8 @@ __device__ void win_produce(const WinParams &p, uint32_t rank, uint32_t sB, uint
     const int u0 = unit0<PAIR>(), us = unit_stride<PAIR>();
     auto tile_of = [&](int u) { return PAIR ? 2 * u + (int)rank : u; };
     // This CTA's part of the packed filter image: one bulk copy on bres.  Input
-    // rows of the first two units: staging buffers 0 and 1 (three in all).
+    // rows of the first NB-1 units go to staging buffers 0 .. NB-2.
+    const int NB = p.raw_bufs;
     int raw_issued = 0, raw_done = 0;
     if (tid == 0) {
         mbar_arrive_expect_tx(bres, (uint32_t)p.b_img_bytes);
@@ -417,7 +419,7 @@ __device__ void win_produce(const WinParams &p, uint32_t rank, uint32_t sB, uint
                      (uint32_t)p.b_img_bytes, bres);
     }
     if (p.x_raw) {
-        for (int k = 0; k < 2 && u0 + k * us < p.num_units; ++k) {
+        for (int k = 0; k < NB - 1 && u0 + k * us < p.num_units; ++k) {
             if (tid == 0) issue_raw_rows(p, sR + (uint32_t)k * raw_bytes, tile_of(u0 + k * us), &rawbar[k], ESZ);
             ++raw_issued;
         }
@@ -432,13 +434,30 @@ __device__ void win_produce(const WinParams &p, uint32_t rank, uint32_t sB, uint
         const uint32_t sbuf = sS + (uint32_t)(buf * p.R) * p.strip_bytes;
         const int tile = tile_of(u);
         bool ok = mbar_wait(&empty[buf], ph ^ 1u, ctl, 1);
-        if (p.x_raw) ok = ok && mbar_wait(&rawbar[it % 3], (uint32_t)(it / 3) & 1u, ctl, 11);
+        if (p.x_raw) ok = ok && mbar_wait(&rawbar[it % NB], (uint32_t)(it / NB) & 1u, ctl, 11);
         if (!ok) break;
-        if (p.x_raw) ++raw_done;
+        if (p.x_raw) {
+            ++raw_done;
+            // the rows of unit it+NB-1 go into the buffer of unit it-1 once every
+            // producer has released it
+            if (u + (NB - 1) * us < p.num_units) {
+                ++raw_issued;
+                if (tid == 0) {
+                    const int prev = it - 1;
+                    if (prev < 0 || mbar_wait(&rawfree[prev % NB], (uint32_t)(prev / NB) & 1u, ctl, 14)) {
+                        fence_proxy_async_smem();
+                        issue_raw_rows(p, sR + (uint32_t)((it + NB - 1) % NB) * raw_bytes,
+                                       tile_of(u + (NB - 1) * us), &rawbar[(it + NB - 1) % NB], ESZ);
+                    } else {
+                        --raw_issued;
+                    }
+                }
+            }
+        }
         if (tile < p.num_tiles) {
             const WinTile wt = win_tile(p, tile);
             if (p.x_raw)
-                repack_strips(p, sbuf, sR + (uint32_t)(it % 3) * raw_bytes, wt, warp, lane);
+                repack_strips(p, sbuf, sR + (uint32_t)(it % NB) * raw_bytes, wt, warp, lane);
             else
                 pack_strips<T>(p, sbuf, wt, warp, lane);
         }
@@ -448,29 +467,12 @@ __device__ void win_produce(const WinParams &p, uint32_t rank, uint32_t sB, uint
             mbar_arrive_cluster(full_l + 8u * buf);  // every producer thread of both CTAs
         else
             mbar_arrive(&full[buf]);
-        if (p.x_raw) {
-            mbar_arrive(&rawfree[it % 3]);  // this thread is done with the staged rows
-            // the rows of the unit after next go into the buffer of the previous
-            // unit once every producer has released it
-            if (u + 2 * us < p.num_units) {
-                ++raw_issued;
-                if (tid == 0) {
-                    const int prev = it - 1;
-                    if (prev < 0 || mbar_wait(&rawfree[prev % 3], (uint32_t)(prev / 3) & 1u, ctl, 14)) {
-                        fence_proxy_async_smem();
-                        issue_raw_rows(p, sR + (uint32_t)((it + 2) % 3) * raw_bytes, tile_of(u + 2 * us),
-                                       &rawbar[(it + 2) % 3], ESZ);
-                    } else {
-                        --raw_issued;
-                    }
-                }
-            }
-        }
+        if (p.x_raw) mbar_arrive(&rawfree[it % NB]);  // this thread is done with the staged rows
     }
     cp_async_commit_wait_all();  // nothing may land after the CTA exits
     // after an early exit, bulk copies may still be in flight
     if (tid == 0) {
-        for (int j = raw_done; j < raw_issued; ++j) mbar_wait(&rawbar[j % 3], (uint32_t)(j / 3) & 1u, drain, 93);
+        for (int j = raw_done; j < raw_issued; ++j) mbar_wait(&rawbar[j % NB], (uint32_t)(j / NB) & 1u, drain, 93);
         mbar_wait(bres, 0u, drain, 94);
     }
 }
@@ -713,9 +715,9 @@ __global__ void __launch_bounds__(WIN_THREADS, 1)
     uint8_t *bptr = epi + (p.y_tma ? WIN_EPI_SMEM : 0);
     const size_t b_bytes = ((size_t)p.b_img_bytes + 1023) & ~(size_t)1023;
     uint8_t *sptr = bptr + b_bytes;
-    uint8_t *rptr = sptr + (size_t)2 * p.R * p.strip_bytes;  // staged input rows, 3 buffers
+    uint8_t *rptr = sptr + (size_t)2 * p.R * p.strip_bytes;  // staged input rows
     uint64_t *bars = reinterpret_cast<uint64_t *>(
-        rptr + (p.x_raw ? (size_t)3 * p.raw_rows * p.row_bytes : 0));
+        rptr + (p.x_raw ? (size_t)p.raw_bufs * p.raw_rows * p.row_bytes : 0));
     uint64_t *full = bars;
     uint64_t *empty = bars + 2;
     uint64_t *tfull = bars + 4;
@@ -867,12 +869,15 @@ bool window_plan(const ConvProblem &pb, WinParams *wp, size_t *smem_out) {
     p.raw_rows = (p.J - 1) * pb.u + (pb.R - 1) * pb.dh + 1;
     const long long rowb = (long long)pb.W * pb.C * e;
     const bool rows_dense = (pb.C == 1 && pb.xs[3] == 1) || (pb.xs[1] == 1 && pb.xs[3] == pb.C);
+    // three buffers if they fit beside the y staging, else two, else none
+    p.raw_bufs = base + 3 * p.raw_rows * rowb + WIN_EPI_SMEM <= WIN_MAX_SMEM ? 3 : 2;
     if (raw_on && rows_dense && pb.xs[2] == (long long)pb.W * pb.xs[3] && rowb % 16 == 0 &&
         (pb.xs[0] * e) % 16 == 0 && (pb.xs[2] * e) % 16 == 0 &&
-        p.raw_rows * rowb < (1LL << 20) && base + 3 * p.raw_rows * rowb <= WIN_MAX_SMEM &&
+        p.raw_rows * rowb < (1LL << 20) &&
+        base + p.raw_bufs * p.raw_rows * rowb + WIN_EPI_SMEM <= WIN_MAX_SMEM &&
         ((long long)pb.pl * pb.C * e) % 4 == 0 && nb % 4 == 0) {
         p.x_raw = 1;
-        base += 3 * p.raw_rows * rowb;
+        base += p.raw_bufs * p.raw_rows * rowb;
     }
     // the packed filter image goes through the handle's repacking buffer
     if ((long long)pb.R * p.steps * p.BN * 32 > DLC_WPACK_BYTES) return false;  // both parts
