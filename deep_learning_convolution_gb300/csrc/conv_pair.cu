@@ -57,10 +57,37 @@ struct PairParams {
     int BN;            // filters per pair tile (BN/2 per CTA)
     int stages, num_kb, c_blocks, n_tiles;
     int num_tiles;     // pair tiles: ceil(M / 256) * n_tiles
+    // Split tail: tiles [full_tiles, num_tiles) -- the part of the last wave
+    // that would leave most pairs idle -- are each split into tail_splits
+    // ranges of k-blocks whose partial sums are added into y (zeroed first).
+    int full_tiles, tail_splits, num_units;
     uint32_t idesc, tmem_cols, acc_stride;
     int *err;
     unsigned long long timeout_ns;
 };
+
+// Work unit u: a whole tile, or one k-block range of a tail tile.
+struct PairUnit {
+    int tile, kb0, kb1, split;
+};
+
+__device__ __forceinline__ PairUnit pair_unit(const PairParams &p, int u) {
+    PairUnit w;
+    if (u < p.full_tiles) {
+        w.tile = u;
+        w.kb0 = 0;
+        w.kb1 = p.num_kb;
+        w.split = 0;
+    } else {
+        const int v = u - p.full_tiles;
+        const int t = v / p.tail_splits, sp = v - t * p.tail_splits;
+        w.tile = p.full_tiles + t;
+        w.kb0 = (int)((long long)p.num_kb * sp / p.tail_splits);
+        w.kb1 = (int)((long long)p.num_kb * (sp + 1) / p.tail_splits);
+        w.split = 1;
+    }
+    return w;
+}
 
 __device__ __forceinline__ bool pair_drain(uint64_t *bar, uint32_t parity, const PairParams &p) {
     volatile int dummy = 0;
@@ -78,7 +105,9 @@ __device__ void pair_produce(const PairParams &p, uint32_t rank, const CUtensorM
     const uint32_t full0 = mapa_shared(smem_u32(full), 0);  // the leader's full barriers
     int stage = 0;
     uint32_t ph = 0;
-    for (int t = (int)cluster_id_x(); t < p.num_tiles; t += (int)num_clusters_x()) {
+    for (int u = (int)cluster_id_x(); u < p.num_units; u += (int)num_clusters_x()) {
+        const PairUnit w = pair_unit(p, u);
+        const int t = w.tile;
         const long long m0 = (long long)(t / p.n_tiles) * (2 * PBM) + (long long)rank * PBM;
         const int k0 = (t % p.n_tiles) * p.BN + (int)rank * (p.BN / 2);
         const int n0 = (int)(m0 / p.PQ);
@@ -86,8 +115,10 @@ __device__ void pair_produce(const PairParams &p, uint32_t rank, const CUtensorM
         const int p0 = rem / p.Q, q0 = rem - (rem / p.Q) * p.Q;
         const int wc = q0 * p.v - p.pl;  // first window origin of this CTA's rows
         const int hc = p0 * p.u - p.pt;
-        int cb = 0, s = 0, r = 0;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        int cb = w.kb0 % p.c_blocks;
+        const int rs0 = w.kb0 / p.c_blocks;
+        int s = rs0 % p.S, r = rs0 / p.S;
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
             if (!mbar_wait(&empty[stage], ph ^ 1u, ctl, 1)) return;
             if (rank == 0) mbar_arrive_expect_tx(&full[stage], tx);
             tma_load_im2col_4d_pair(sA + (uint32_t)stage * PA_BYTES, tmA, full0 + 8u * stage, cb * BK,
@@ -113,7 +144,8 @@ __device__ void pair_mma(const PairParams &p, uint32_t tmem_base, uint32_t sA, u
     int stage = 0, it = 0;
     uint32_t ph = 0;
     bool ok = true;
-    for (int t = (int)cluster_id_x(); ok && t < p.num_tiles; t += (int)num_clusters_x(), ++it) {
+    for (int u = (int)cluster_id_x(); ok && u < p.num_units; u += (int)num_clusters_x(), ++it) {
+        const PairUnit w = pair_unit(p, u);
         const int buf = it & 1;
         const uint32_t aph = (uint32_t)(it >> 1) & 1u;
         if (!mbar_wait_cluster(&tempty[buf], aph ^ 1u, ctl, 3)) {  // both CTAs' epilogues
@@ -124,7 +156,7 @@ __device__ void pair_mma(const PairParams &p, uint32_t tmem_base, uint32_t sA, u
         const uint32_t d = tmem_base + (uint32_t)buf * p.acc_stride;
         uint64_t ad = a0 + a_step * stage, bd = b0 + b_step * stage;
         uint32_t acc = 0;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
             if (!mbar_wait(&full[stage], ph, ctl, 4)) {
                 ok = false;
                 break;
@@ -236,7 +268,9 @@ __device__ void pair_epilogue(const PairParams &p, uint32_t rank, uint32_t tmem_
     const uint32_t my_bufs = epi_smem + (uint32_t)(quad * 2 * PAIR_EPI_BUF);
     int nbuf = 0;
     int it = 0;
-    for (int t = (int)cluster_id_x(); t < p.num_tiles; t += (int)num_clusters_x(), ++it) {
+    for (int u = (int)cluster_id_x(); u < p.num_units; u += (int)num_clusters_x(), ++it) {
+        const PairUnit w = pair_unit(p, u);
+        const int t = w.tile;
         const int buf = it & 1;
         const uint32_t ph = (uint32_t)(it >> 1) & 1u;
         int okw = 0;
@@ -283,7 +317,10 @@ __device__ void pair_epilogue(const PairParams &p, uint32_t rank, uint32_t tmem_
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {  // rows past M and columns past K are not written
-                    tma_store_2d_s(tmY, sb, k0, (int)(m - lane));
+                    if (w.split)  // a partial sum: added into y (zeroed before the launch)
+                        tma_reduce_add_2d_s(tmY, sb, k0, (int)(m - lane));
+                    else
+                        tma_store_2d_s(tmY, sb, k0, (int)(m - lane));
                     bulk_commit_group();
                 }
                 ++nbuf;
@@ -526,7 +563,32 @@ dlcStatus_t dlc_launch_pair(dlcContext *ctx, const ConvProblem &pb) {
     if (cudaOccupancyMaxActiveClusters(&max_clusters, (const void *)kern, &cfg) != cudaSuccess ||
         max_clusters < 1)
         return DLC_STATUS_EXECUTION_FAILED;
-    const int clusters = std::min(max_clusters, std::max(1, p.num_tiles));
+    // Split tail: when the last wave would leave at least half the pairs
+    // idle, its tiles are split along the reduction over the idle pairs (plain
+    // epilogue only: the partial sums are added by bulk reduce-adds into y,
+    // zeroed here first).  DLC_TC_PAIR_SPLIT=0 turns it off.
+    int clusters = std::min(max_clusters, std::max(1, p.num_tiles));
+    p.full_tiles = p.num_tiles;
+    p.tail_splits = 1;
+    p.num_units = p.num_tiles;
+    {
+        const char *ev = std::getenv("DLC_TC_PAIR_SPLIT");
+        const bool plain = p.y_tma && pb.beta == 0.f && pb.bias == nullptr && !pb.relu;
+        const int C = max_clusters;
+        const int rem = p.num_tiles % C;
+        const int splits = rem > 0 ? std::min(std::min(C / rem, p.num_kb), 16) : 1;
+        if (plain && splits >= 2 && !(ev && std::atoi(ev) == 0)) {
+            p.full_tiles = p.num_tiles - rem;
+            p.tail_splits = splits;
+            p.num_units = p.full_tiles + rem * splits;
+            clusters = C;
+            const long long row0 = (long long)(p.full_tiles / p.n_tiles) * (2 * PBM);
+            if (row0 < p.M &&
+                cudaMemset2DAsync(static_cast<float *>(pb.y) + row0 * pb.ys[3], (size_t)pb.ys[3] * 4, 0,
+                                  (size_t)pb.K * 4, (size_t)(p.M - row0), ctx->stream) != cudaSuccess)
+                return DLC_STATUS_EXECUTION_FAILED;
+        }
+    }
     cfg.gridDim = dim3(2 * clusters, 1, 1);
     if (cudaLaunchKernelEx(&cfg, kern, p, ta, tb, ty) != cudaSuccess) return DLC_STATUS_EXECUTION_FAILED;
     ctx->launches += 1;

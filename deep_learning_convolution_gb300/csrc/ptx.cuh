@@ -214,6 +214,16 @@ __device__ __forceinline__ void tma_store_2d_s(const CUtensorMap *m, uint32_t sr
         : "memory");
 }
 
+// Bulk tensor reduce-add of a 2-D FP32 box from shared memory into global
+// memory (element-wise atomic add at the L2; out-of-tensor parts are skipped).
+__device__ __forceinline__ void tma_reduce_add_2d_s(const CUtensorMap *m, uint32_t src, int c0, int c1) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(m)),
+        "r"(src), "r"(c0), "r"(c1)
+        : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

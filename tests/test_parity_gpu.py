@@ -119,6 +119,17 @@ def test_tc_im2col_pair_bulk_stores(handle, layer):
                   relu=True, expect_kernel="tc_im2col_pair")
 
 
+@pytest.mark.parametrize("split", ["1", "0"], ids=["split_tail", "whole_tiles"])
+@pytest.mark.parametrize("layer", [PAIR_CASES[i] for i in (0, 1, 3, 7, 9, 10)],
+                         ids=lambda l: l.name)
+def test_tc_im2col_pair_split_tail(handle, layer, split, monkeypatch):
+    """Plain epilogue: tiles of the last, mostly idle wave are split along the
+    reduction and their partial sums added into y by bulk reduce-adds."""
+    monkeypatch.setenv("DLC_TC_PAIR_SPLIT", split)
+    run_and_check(handle, layer, 1170 + PAIR_CASES.index(layer), full=True, alpha=0.75,
+                  expect_kernel="tc_im2col_pair")
+
+
 def test_tc_im2col_pair_epilogue(handle):
     import torch
     layer = IM2COL_CASES[1]
