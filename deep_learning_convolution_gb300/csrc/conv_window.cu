@@ -18,22 +18,33 @@
 // and stay resident in shared memory.
 //
 // Tiles: the 128 MMA rows are J output rows of one image (Qs rows each, Qs a
-// power of two >= Q+A-1, J = 128/Qs) or, for wide rows (J = 1), 128 consecutive
-// pixels of one output row.  Strip r of a tile holds, for output row j, the
-// phase pixels of input row (p0+j)*u + r*dh - pt at pixel offset j*Qs; tile
-// rows past Q read pixels whose value does not matter and are not stored.
+// power of two covering every pixel a stored output reads, J = 128/Qs) or, for
+// wide rows (J = 1), 128 consecutive pixels of one output row; tile rows past
+// Q read pixels whose value does not matter and are not stored.
+//
+// Row ring: the phase-pixel rows live in shared memory once per input row, not
+// once per filter row.  Input row h = p0*u - pt + i of a tile (i < rows =
+// (J-1)*u + (R-1)*dh + 1) goes to ring slot (h mod u, floor(h/u)): the u phases
+// of the vertical stride each hold a ring of RS slots, so input rows h and
+// h + u -- what output rows j and j+1 of a tile read for one filter row -- sit
+// in adjacent slots, and filter row r reads J consecutive slots as one operand
+// (J-1 mirror slots after each ring keep a wrapped run contiguous).  A CTA
+// walks consecutive tiles of one image, so each tile adds only the J*u input
+// rows its predecessor did not hold.
 //
 // CTA pairs (opt-in, DLC_TC_WINPAIR=1): a cluster of two CTAs shares
 // each MMA over M = 256 rows (one tile per CTA, tcgen05 cta_group::2); each CTA
-// packs its own strips and holds half of the filters.
+// fills its own ring, at the same offsets as its peer, and holds half of the
+// filters.
 //
-// Roles (one persistent CTA per SM): eight producer warps pack the strips of
-// the next tile into one of two buffers (batched 4-/8-byte loads; padding and
-// the packing tail are zero-filled); one thread issues R*steps MMAs (32 bytes
-// of reduction each) per tile into one of two TMEM accumulators; four epilogue
-// warps read the accumulator, apply alpha, beta*y, bias and ReLU and store y
-// (bulk tensor stores of 32x32 blocks when y is dense FP32).  Every wait is
-// bounded and records an error word when it runs out.
+// Roles (one persistent CTA per SM): eight producer warps write the new rows of
+// the next tile into the ring (4-byte asynchronous copies, or element loads;
+// padding words, pixels outside the image and rows outside it are zeros); one
+// thread issues R*steps MMAs (32 bytes of reduction each) per tile into one of
+// two TMEM accumulators; four epilogue warps read the accumulator, apply
+// alpha, beta*y, bias and ReLU and store y (bulk tensor stores of 32x32 blocks
+// when y is dense FP32).  Every wait is bounded and records an error word when
+// it runs out.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -55,7 +66,8 @@ constexpr int WIN_THREADS = PROD_THREADS + 32 + 128;
 constexpr int WIN_MAX_SMEM = 232448;
 constexpr int WIN_EPI_BUF = 32 * 128;                // one warp's 32 rows x 32 FP32 columns
 constexpr int WIN_EPI_SMEM = 4 * WIN_EPI_BUF;        // 4 epilogue warps, one buffer each
-constexpr int WIN_BAR_AREA = 256;
+constexpr int WIN_MAX_ROWS = 224;                  // input rows per tile (ring table)
+constexpr int WIN_BAR_AREA = 128 + 4 * WIN_MAX_ROWS;  // barriers, then the ring table
 
 struct WinParams {
     int N, C, H, W, K, R, S, P, Q;
@@ -65,13 +77,17 @@ struct WinParams {
     int D, d_log2;    // bytes per phase pixel and its log2
     int nb, nbw;      // data bytes (v*C elements) and data words of a phase pixel
     int steps;        // MMAs per filter row (32 bytes of window each)
+    int px_read;      // phase pixels one output's MMAs read: steps*32/D
     int Qs, qs_log2, J, segs, PB;
-    int strip_px, strip_bytes;
-    int groups;       // warp steps per strip: strip_px / (32 / (D/4)), rounded up
+    int rows;         // input rows one tile spans: (J-1)*u + (R-1)*dh + 1
+    int kb_off;       // floor(-pt/u): ring index of a tile's first row, less p0
+    int kspan;        // ring indices floor(h/u) one tile's rows span
+    int RS, RSJ;      // ring slots per phase, and with the J-1 mirror slots
+    int slot_px, slot_bytes;  // phase pixels and bytes of one ring slot
+    int disc_wait;    // RS < 2*kspan: a tile that starts a new run of rows waits
+                      // for the MMAs of the tile before it
+    int ring_bytes;
     int row_bytes;    // bytes of one input row (x_word)
-    int x_raw;        // input rows are bulk-copied to shared memory, then repacked
-    int raw_rows;     // input rows one tile spans: (J-1)*u + (R-1)*dh + 1
-    int raw_bufs;     // staging buffers (2 or 3): rows are fetched raw_bufs-1 units ahead
     const void *wpack;  // the filter slabs, packed by window_pack_filters
     int b_img_bytes;    // bytes of one CTA's part: R*steps*(BN/ctas) rows of 32
     int pair;           // launched as CTA pairs (cta_group::2, M = 256 per MMA)
@@ -88,7 +104,7 @@ struct WinParams {
                       // start on 4-byte boundaries
     int BN;
     uint32_t idesc, tmem_cols, acc_stride;
-    uint64_t a_hi;    // strip descriptor bits other than the start address
+    uint64_t a_hi;    // ring descriptor bits other than the start address
     int *err;
     unsigned long long timeout_ns;
 };
@@ -97,15 +113,35 @@ struct WinTile {
     int n, p0, q0;
 };
 
+// Tile t: the row blocks of one (image, segment) are consecutive, so a CTA
+// that walks consecutive tiles moves down one image J output rows at a time.
 __device__ __forceinline__ WinTile win_tile(const WinParams &p, int t) {
     WinTile wt;
-    const int rest = t / p.segs;
-    const int seg = t - rest * p.segs;
-    const int n = rest / p.PB;
-    wt.p0 = (rest - n * p.PB) * p.J;
+    const int rest = t / p.PB;
+    const int n = rest / p.segs;
     wt.n = n;
-    wt.q0 = seg * WBM;
+    wt.q0 = (rest - n * p.segs) * WBM;
+    wt.p0 = (t - rest * p.PB) * p.J;
     return wt;
+}
+
+__device__ __forceinline__ int floor_div(int a, int b) { return a >= 0 ? a / b : -((b - 1 - a) / b); }
+
+// Ring table entry of tile row i (input row p0*u - pt + i): the first slot of
+// its phase, (i - pt) mod u times RSJ, in the high half and its ring index
+// floor((i - pt)/u) - kb_off in the low half.  Both are independent of p0, so
+// both CTAs of a pair place their rows alike.
+__device__ __forceinline__ uint32_t ring_entry(const WinParams &p, int i) {
+    const int a = i - p.pt;
+    const int k = floor_div(a, p.u);
+    return ((uint32_t)((a - k * p.u) * p.RSJ) << 16) | (uint32_t)(k - p.kb_off);
+}
+// Ring slot of a row with table entry e for ring base `base`; pos is its
+// position in the phase's ring (below RS).
+__device__ __forceinline__ int ring_slot(const WinParams &p, uint32_t e, int base, int &pos) {
+    pos = base + (int)(e & 0xffffu);
+    if (pos >= p.RS) pos -= p.RS;
+    return (int)(e >> 16) + pos;
 }
 
 // Element eps of a phase pixel (input pixel w0 + eps/C, channel eps%C) of
@@ -130,19 +166,6 @@ __device__ __forceinline__ uint32_t pack_word(const T (&e)[4 / sizeof(T)]) {
         return (uint32_t)e[0] | ((uint32_t)e[1] << 16);
     else
         return (uint32_t)e[0];
-}
-
-// The filter taps as MMA B operands: slab (r, st) holds BN rows (filters) of
-// the 32 window bytes [32*st, 32*st + 32) of filter row r, in the 32-byte
-// swizzled K-major layout (row k at 32*k; its two 16-byte halves exchanged
-// where address bit 7 is set).  A thread walks the window of one (k, r) pair
-// element by element -- phase pixel a, phase phi, channel c, tap s = v*a+phi --
-// and writes it a word at a time, sixteen words' loads in flight before their
-// stores.
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-    return v;
 }
 
 // The filter taps as MMA B operands, packed by a small kernel launched ahead
@@ -185,296 +208,177 @@ __global__ void window_pack_filters(const __grid_constant__ WinParams p, uint32_
     img[off >> 2] = pack_word<T>(e);
 }
 
-// Packs the R strips of one tile.  Lane l of a warp owns word l % wpp of strip
-// pixel l / wpp of each group of 32/wpp consecutive strip pixels (wpp = D/4
-// words per phase pixel), so a warp writes 128 contiguous bytes per step; the
-// 16-byte chunk of a word is XORed with address bits 7.. of its pixel (the
-// swizzle of D-byte rows; none for D = 16).  When the input row is one
-// contiguous, 4-byte-aligned byte run (x_word), a phase pixel's data are
-// bytes [(v*P - pl)*C, +v*C) of that run and every word is one 4-byte
-// cp.async (zero-filled outside the row and in the padding words; the last
-// word of a row may be partial).  Otherwise elements are loaded one by one,
-// four steps' loads in flight before their stores.
+// Writes input rows i in [i0, rows) of one tile into their ring slots (and
+// mirror slots), phase pixels [P0, P0 + need) where need covers every pixel a
+// stored output reads (P0 = q0 for wide rows, else 0).  The tile's (row, warp
+// step) pairs are split into eight equal ranges, one per producer warp.  Lane
+// l owns word l % wpp of pixel l / wpp of each step's 32/wpp consecutive
+// pixels (wpp = D/4 words per phase pixel), so a warp writes 128 contiguous
+// bytes per step; the 16-byte chunk of a word is XORed with address bits 7..
+// of its pixel (the swizzle of D-byte rows; none for D = 16).  When the input
+// row is one contiguous, 4-byte-aligned byte run (x_word), a phase pixel's
+// data are bytes [(v*P - pl)*C, +v*C) of that run and every word is one
+// 4-byte cp.async (zero-filled outside the row, in the padding words and for
+// rows outside the image; the last word of a row may be partial).  Otherwise
+// elements are loaded one by one, four steps' loads in flight before their
+// stores.
 template <typename T>
-__device__ void pack_strips(const WinParams &p, uint32_t sbuf, const WinTile &wt, int warp,
-                            int lane) {
+__device__ void pack_rows(const WinParams &p, uint32_t ring, const uint32_t *rtab, const WinTile &wt,
+                          int base, int i0, int warp, int lane) {
     constexpr int ESZ = (int)sizeof(T), EPW = 4 / ESZ;
-    constexpr uint32_t NONE = 0xffffffffu;
+    constexpr int NW = PROD_THREADS / 32;
     const int wpp = p.D >> 2;
     const int dp = lane >> (p.d_log2 - 2), wp = lane & (wpp - 1);
-    const int G = 32 / wpp;  // strip pixels per warp step
-    const int chmask = (p.D >> 4) - 1;
-    const int q_need = p.Q + p.A - 1;
-    const int total = p.R * p.groups;
+    const int G = 32 / wpp;  // pixels per warp step
+    const uint32_t chmask = (uint32_t)(p.D >> 4) - 1u;
+    const int P0 = p.J > 1 ? 0 : wt.q0;
+    const int need = min(p.slot_px, (p.J > 1 ? p.Q : p.Q - wt.q0) - 1 + p.px_read);
+    const int spr = (need + G - 1) / G;  // warp steps per row
+    const int total = (p.rows - i0) * spr;
+    const int lo = (int)(((long long)total * warp) / NW);
+    const int hi = (int)(((long long)total * (warp + 1)) / NW);
+    const uint32_t inner = (uint32_t)(wp * 4);
+    const uint32_t mdelta = (uint32_t)p.RS * (uint32_t)p.slot_bytes;  // slot -> its mirror
     const char *xb = static_cast<const char *>(p.x);
-    // strip pixel -> destination word address, input row and phase pixel
-    auto decode = [&](int it, uint32_t &dst, long long &rowoff, int &P) -> bool {
-        const int r = it / p.groups;
-        const int sig = (it - r * p.groups) * G + dp;
-        dst = NONE;
-        if (sig >= p.strip_px) return false;
-        int j;
-        bool ok;
-        if (p.J > 1) {
-            j = sig >> p.qs_log2;
-            P = sig & (p.Qs - 1);
-            ok = j < p.J && P < q_need;
-        } else {
-            j = 0;
-            P = wt.q0 + sig;
-            ok = true;
-        }
-        const int pr = wt.p0 + j;
-        const int h = pr * p.u + r * p.dh - p.pt;
-        ok = ok && pr < p.P && h >= 0 && h < p.H && wp < p.nbw;
-        const uint32_t paddr = sbuf + (uint32_t)r * p.strip_bytes + (uint32_t)sig * p.D;
-        const int byte = wp * 4;
-        dst = paddr + ((((uint32_t)(byte >> 4) ^ ((paddr >> 7) & chmask)) << 4) | (uint32_t)(byte & 15));
-        rowoff = (long long)wt.n * p.xs[0] + (long long)h * p.xs[2];
-        return ok;
-    };
-    if (p.x_word) {
-        // segments (r, j): J per strip, each Qs strip pixels; the last one of a
-        // strip also takes the strip's tail pixels (strip_px is a multiple of G)
-        const int nseg = p.R * p.J;
-        const int lb = p.pl * p.C * ESZ;  // phase pixel P's data start at byte P*nb - lb
-        const uint32_t inner = (uint32_t)(wp * 4);
-        const int gnb = G * p.nb;          // row bytes advanced per warp step
+    const int lb = p.pl * p.C * ESZ;  // phase pixel P's data start at byte P*nb - lb
 #pragma unroll 1
-        for (int sg = warp; sg < nseg; sg += PROD_THREADS / 32) {
-            const int r = sg / p.J, j = sg - r * p.J;
-            const int pix0 = p.J > 1 ? j * p.Qs : 0;
-            const int nst = ((j == p.J - 1) ? p.strip_px - pix0 : p.Qs) / G;  // warp steps
-            const int pr = wt.p0 + j;
-            const int h = pr * p.u + r * p.dh - p.pt;
-            const int P0 = (p.J > 1 ? 0 : wt.q0) + dp;
-            // steps whose word may hold data: the row exists, the word is a data
-            // word, and (J > 1) the pixel is one a valid output row reads
-            int st_end = 0;
-            if (pr < p.P && h >= 0 && h < p.H && wp < p.nbw)
-                st_end = p.J > 1 ? max(0, (q_need - P0 + G - 1) / G) : nst;
-            const char *rowp = xb + ((long long)wt.n * p.xs[0] + (long long)(h < 0 ? 0 : h) * p.xs[2]) * ESZ;
-            int bt = P0 * p.nb - lb + (int)inner;  // byte of the row this lane copies
-            uint32_t paddr = sbuf + (uint32_t)r * p.strip_bytes + (uint32_t)(pix0 + dp) * p.D;
+    for (int item = lo; item < hi;) {
+        const int ri = item / spr;
+        const int st0 = item - ri * spr;
+        const int st1 = min(spr, st0 + (hi - item));
+        item += st1 - st0;
+        const int i = i0 + ri;
+        const int h = wt.p0 * p.u - p.pt + i;
+        const bool row_ok = h >= 0 && h < p.H;  // rows outside the image are zeros
+        int pos;
+        const int slot = ring_slot(p, rtab[i], base, pos);
+        const bool mirror = pos < p.J - 1;
+        uint32_t paddr = ring + (uint32_t)slot * (uint32_t)p.slot_bytes + (uint32_t)(st0 * G + dp) * p.D;
+        if (p.x_word) {
+            const char *rowp = xb + ((long long)wt.n * p.xs[0] + (long long)(row_ok ? h : 0) * p.xs[2]) * ESZ;
+            int bt = (P0 + st0 * G + dp) * p.nb - lb + (int)inner;  // byte of the row this lane copies
+            const bool lane_ok = row_ok && wp < p.nbw;
+            const int gnb = G * p.nb;
 #pragma unroll 4
-            for (int st = 0; st < nst; ++st) {
-                const bool in = st < st_end && (unsigned)bt < (unsigned)p.row_bytes;
+            for (int st = st0; st < st1; ++st) {
+                const bool in = lane_ok && (unsigned)bt < (unsigned)p.row_bytes;
                 const uint32_t n = in ? (uint32_t)min(p.row_bytes - bt, 4) : 0u;
-                const uint32_t dst = paddr + ((((inner >> 4) ^ ((paddr >> 7) & chmask)) << 4) |
-                                              (inner & 15u));
-                cp_async_4(dst, in ? rowp + bt : xb, n);
+                const uint32_t dst = paddr + ((((inner >> 4) ^ ((paddr >> 7) & chmask)) << 4) | (inner & 15u));
+                const char *src = in ? rowp + bt : xb;
+                cp_async_4(dst, src, n);
+                if (mirror) cp_async_4(dst + mdelta, src, n);
                 bt += gnb;
-                paddr += 128u;  // G pixels of D bytes
+                paddr += 128u;
             }
+            continue;
         }
-        return;
-    }
-    constexpr int STEPS = 4;
+        const long long rowoff = (long long)wt.n * p.xs[0] + (long long)(row_ok ? h : 0) * p.xs[2];
+        int w0 = (P0 + st0 * G + dp) * p.v - p.pl;  // first input pixel of this lane's phase pixel
+        const int eps0 = wp * EPW;
 #pragma unroll 1
-    for (int it0 = warp; it0 < total; it0 += STEPS * (PROD_THREADS / 32)) {
-        uint32_t dst[STEPS];
-        T val[STEPS][EPW];
+        for (int st = st0; st < st1; st += 4) {
+            T val[4][EPW];
 #pragma unroll
-        for (int sidx = 0; sidx < STEPS; ++sidx) {
-            const int it = it0 + sidx * (PROD_THREADS / 32);
-            long long rowoff = 0;
-            int P = 0;
-            const bool ok = it < total && decode(it, dst[sidx], rowoff, P);
-            if (it >= total) dst[sidx] = NONE;
+            for (int k = 0; k < 4; ++k)
 #pragma unroll
-            for (int i = 0; i < EPW; ++i)
-                val[sidx][i] = ok ? phase_elem<T>(p, rowoff, P * p.v - p.pl, wp * EPW + i) : (T)0;
-        }
+                for (int e = 0; e < EPW; ++e)
+                    val[k][e] = (row_ok && st + k < st1) ? phase_elem<T>(p, rowoff, w0 + k * G * p.v, eps0 + e) : (T)0;
 #pragma unroll
-        for (int sidx = 0; sidx < STEPS; ++sidx)
-            if (dst[sidx] != NONE) sts32(dst[sidx], pack_word<T>(val[sidx]));
-    }
-}
-
-__device__ __forceinline__ void sts128v(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-                 : "memory");
-}
-
-// Repacks the R strips of one tile from its input rows staged in shared
-// memory at sR (row i = input row p0*u - pt + i, row_bytes each).  Lane l of a
-// warp builds 16-byte chunk l % (D/16) of strip pixel l / (D/16) of each group
-// of 512/D pixels: up to four 4-byte loads from the staged row (zero outside
-// the row and past the data) and one 16-byte store, the chunk index XORed with
-// address bits 7.. of its pixel.  Two steps' loads are in flight before their
-// stores.
-__device__ void repack_strips(const WinParams &p, uint32_t sbuf, uint32_t sR, const WinTile &wt,
-                              int warp, int lane) {
-    const int chl = p.d_log2 - 4;  // log2 of 16-byte chunks per phase pixel
-    const int kap = lane & ((1 << chl) - 1);
-    const int dp = lane >> chl;
-    const int G = 32 >> chl;       // strip pixels per warp step
-    const uint32_t chmask = (1u << chl) - 1u;
-    const int q_need = p.Q + p.A - 1;
-    const int nseg = p.R * p.J;
-    const int lb = p.pl * p.C * (p.nb / (p.v * p.C));  // bytes of pl input pixels
-    const int b0 = kap * 16;                            // first byte of the chunk in its pixel
-    const int nwords = max(0, min(4, (p.nb - b0) >> 2)); // data words of the chunk
-    const int gnb = G * p.nb;
-    const uint32_t rowb = (uint32_t)p.row_bytes;
-    // the tile's warp steps (segment by segment) split into eight equal ranges
-    const int nst0 = p.Qs / G;                                   // steps of a segment
-    const int nst_last = (p.strip_px - (p.J > 1 ? (p.J - 1) * p.Qs : 0)) / G;  // last of a strip
-    const int per_strip = (p.J - 1) * nst0 + nst_last;
-    const int total = p.R * per_strip;
-    const int lo = (int)(((long long)total * warp) / (PROD_THREADS / 32));
-    const int hi = (int)(((long long)total * (warp + 1)) / (PROD_THREADS / 32));
-    int seg_start = 0;
-#pragma unroll 1
-    for (int sg = 0; sg < nseg && seg_start < hi; ++sg) {
-        const int r = sg / p.J, j = sg - r * p.J;
-        const int nst_all = (j == p.J - 1) ? nst_last : nst0;
-        const int s_lo = max(0, lo - seg_start), nst = min(nst_all, hi - seg_start);
-        seg_start += nst_all;
-        if (s_lo >= nst) continue;
-        const int pix0 = p.J > 1 ? j * p.Qs : 0;
-        const int pr = wt.p0 + j;
-        const int h = pr * p.u + r * p.dh - p.pt;
-        const int P0 = (p.J > 1 ? 0 : wt.q0) + dp;
-        int st_end = 0;
-        if (pr < p.P && h >= 0 && h < p.H && nwords > 0)
-            st_end = p.J > 1 ? max(0, (q_need - P0 + G - 1) / G) : nst_all;
-        const uint32_t rb = sR + (uint32_t)(j * p.u + r * p.dh) * rowb;
-        int bt = P0 * p.nb - lb + b0 + s_lo * gnb;
-        uint32_t paddr = sbuf + (uint32_t)r * p.strip_bytes + (uint32_t)(pix0 + dp) * p.D + 512u * s_lo;
-        for (int st0 = s_lo; st0 < nst; st0 += 2) {
-            uint32_t v[2][4];
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const int st = st0 + k, b = bt + k * gnb;
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    v[k][i] = (st < st_end && i < nwords && (unsigned)(b + 4 * i) < rowb) ? lds32(rb + b + 4 * i) : 0u;
+            for (int k = 0; k < 4; ++k) {
+                if (st + k >= st1) break;
+                const uint32_t pa = paddr + 128u * k;
+                const uint32_t dst = pa + ((((inner >> 4) ^ ((pa >> 7) & chmask)) << 4) | (inner & 15u));
+                const uint32_t word = pack_word<T>(val[k]);
+                sts32(dst, word);
+                if (mirror) sts32(dst + mdelta, word);
             }
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const uint32_t pa = paddr + 512u * k;  // G pixels of D bytes per step
-                if (st0 + k < nst)
-                    sts128v(pa + (((uint32_t)kap ^ ((pa >> 7) & chmask)) << 4), v[k][0], v[k][1], v[k][2], v[k][3]);
-            }
-            bt += 2 * gnb;
-            paddr += 1024u;
+            w0 += 4 * G * p.v;
+            paddr += 512u;
         }
     }
 }
 
-// Bulk-copies the input rows of a tile to sR (row i = input row p0*u - pt + i)
-// as one copy of the rows inside the image -- they are consecutive in x --
-// completing on rawbar.  A tile past the last one (the second half of an odd
-// pair) loads nothing but still completes the barrier's phase.
-__device__ void issue_raw_rows(const WinParams &p, uint32_t sR, int tile, uint64_t *rawbar, int esz) {
-    int lo = 0, n = 0;
-    const WinTile wt = win_tile(p, tile < p.num_tiles ? tile : 0);
-    const int h0 = wt.p0 * p.u - p.pt;
-    if (tile < p.num_tiles) {
-        lo = max(0, -h0);
-        n = min(p.raw_rows, p.H - h0) - lo;
-        if (n < 0) n = 0;
-    }
-    const uint32_t bytes = (uint32_t)n * (uint32_t)p.row_bytes;
-    mbar_arrive_expect_tx(rawbar, bytes);
-    if (n > 0)
-        bulk_load_1d(sR + (uint32_t)lo * (uint32_t)p.row_bytes,
-                     static_cast<const char *>(p.x) +
-                         ((long long)wt.n * p.xs[0] + (long long)(h0 + lo) * p.xs[2]) * esz,
-                     bytes, rawbar);
-}
-
-// Work units: a CTA takes units u = unit0, unit0 + stride, ...; unit u is tile
-// u, or for a pair tiles 2u (leader) and 2u + 1 (peer).
+// A CTA (or CTA pair) takes the contiguous units [ub, ue); unit u is tile u,
+// or for a pair tile u (leader) and tile u + num_units (peer).
 template <bool PAIR>
-__device__ __forceinline__ int unit0() {
-    return PAIR ? (int)cluster_id_x() : (int)blockIdx.x;
+__device__ __forceinline__ void unit_range(const WinParams &p, int &ub, int &ue) {
+    const long long c = PAIR ? (long long)cluster_id_x() : (long long)blockIdx.x;
+    const long long g = PAIR ? (long long)num_clusters_x() : (long long)gridDim.x;
+    ub = (int)((p.num_units * c) / g);
+    ue = (int)((p.num_units * (c + 1)) / g);
 }
 template <bool PAIR>
-__device__ __forceinline__ int unit_stride() {
-    return PAIR ? (int)num_clusters_x() : (int)gridDim.x;
+__device__ __forceinline__ int tile_of(const WinParams &p, int u, uint32_t rank) {
+    return (PAIR && rank) ? u + p.num_units : u;
 }
+// Walks a CTA's units [ub, ue).  Unit u continues unit u-1 when, for every
+// CTA of the pair, it holds the next J output rows of the same image and
+// segment; its ring base then moves J slots (only the last J*u rows of the
+// tile are new), else kspan slots (every row is new).
+template <bool PAIR>
+struct UnitWalk {
+    int pbL, pbP, base;
+    __device__ UnitWalk(const WinParams &p, int ub)
+        : pbL(ub % p.PB), pbP((ub + p.num_units) % p.PB), base(0) {}
+    // to unit u = (previous unit) + 1; whether u continues the previous unit
+    __device__ __forceinline__ bool next(const WinParams &p, int u) {
+        if (++pbL == p.PB) pbL = 0;
+        if (++pbP == p.PB) pbP = 0;
+        const bool cont = pbL != 0 && (!PAIR || u + p.num_units >= p.num_tiles || pbP != 0);
+        base += cont ? p.J : p.kspan;
+        if (base >= p.RS) base -= p.RS;
+        return cont;
+    }
+};
 
 template <typename T, bool PAIR>
-__device__ void win_produce(const WinParams &p, uint32_t rank, uint32_t sB, uint32_t sS,
-                            uint32_t sR, uint64_t *full, uint64_t *empty, uint64_t *bres,
-                            uint64_t *bpeer, uint64_t *rawbar, uint64_t *rawfree,
-                            const WaitCtl &ctl) {
-    constexpr int ESZ = (int)sizeof(T);
+__device__ void win_produce(const WinParams &p, uint32_t rank, uint32_t sB, uint32_t sRing,
+                            const uint32_t *rtab, uint64_t *full, uint64_t *empty, uint64_t *bres,
+                            uint64_t *bpeer, const WaitCtl &ctl) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t raw_bytes = (uint32_t)p.raw_rows * (uint32_t)p.row_bytes;
     const uint32_t full_l = PAIR ? mapa_shared(smem_u32(full), 0) : smem_u32(full);  // leader's
     volatile int no_abort = 0;
     const WaitCtl drain{&no_abort, p.err, p.timeout_ns};  // waits for copies in flight
-    const int u0 = unit0<PAIR>(), us = unit_stride<PAIR>();
-    auto tile_of = [&](int u) { return PAIR ? 2 * u + (int)rank : u; };
-    // This CTA's part of the packed filter image: one bulk copy on bres.  Input
-    // rows of the first NB-1 units go to staging buffers 0 .. NB-2.
-    const int NB = p.raw_bufs;
-    int raw_issued = 0, raw_done = 0;
+    int ub, ue;
+    unit_range<PAIR>(p, ub, ue);
+    // this CTA's part of the packed filter image: one bulk copy on bres
     if (tid == 0) {
         mbar_arrive_expect_tx(bres, (uint32_t)p.b_img_bytes);
         bulk_load_1d(sB, static_cast<const char *>(p.wpack) + (size_t)rank * p.b_img_bytes,
                      (uint32_t)p.b_img_bytes, bres);
     }
-    if (p.x_raw) {
-        for (int k = 0; k < NB - 1 && u0 + k * us < p.num_units; ++k) {
-            if (tid == 0) issue_raw_rows(p, sR + (uint32_t)k * raw_bytes, tile_of(u0 + k * us), &rawbar[k], ESZ);
-            ++raw_issued;
-        }
-    }
     if (PAIR && rank == 1 && tid == 0) {  // the leader's MMAs read this CTA's filters too
         if (mbar_wait(bres, 0u, ctl, 12)) mbar_arrive_cluster(mapa_shared(smem_u32(bpeer), 0));
     }
+    // Pixels past `need` and the tail after the last slot are read only by
+    // tile rows that are not stored: zero them once so they hold finite data.
+    for (uint32_t i = (uint32_t)tid; i < (uint32_t)p.ring_bytes / 16u; i += PROD_THREADS)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(sRing + 16u * i), "r"(0u) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(PROD_THREADS) : "memory");  // producer warps only
+    UnitWalk<PAIR> walk(p, ub);
     int it = 0;
-    for (int u = u0; u < p.num_units; u += us, ++it) {
+    for (int u = ub; u < ue; ++u, ++it) {
+        const bool cont = u > ub && walk.next(p, u);
         const int buf = it & 1;
         const uint32_t ph = (uint32_t)(it >> 1) & 1u;
-        const uint32_t sbuf = sS + (uint32_t)(buf * p.R) * p.strip_bytes;
-        const int tile = tile_of(u);
         bool ok = mbar_wait(&empty[buf], ph ^ 1u, ctl, 1);
-        if (p.x_raw) ok = ok && mbar_wait(&rawbar[it % NB], (uint32_t)(it / NB) & 1u, ctl, 11);
+        // a short ring: the previous tile's rows must be free before a new run overwrites them
+        if (ok && !cont && p.disc_wait && it >= 1)
+            ok = mbar_wait(&empty[(it - 1) & 1], (uint32_t)((it - 1) >> 1) & 1u, ctl, 15);
         if (!ok) break;
-        if (p.x_raw) {
-            ++raw_done;
-            // the rows of unit it+NB-1 go into the buffer of unit it-1 once every
-            // producer has released it
-            if (u + (NB - 1) * us < p.num_units) {
-                ++raw_issued;
-                if (tid == 0) {
-                    const int prev = it - 1;
-                    if (prev < 0 || mbar_wait(&rawfree[prev % NB], (uint32_t)(prev / NB) & 1u, ctl, 14)) {
-                        fence_proxy_async_smem();
-                        issue_raw_rows(p, sR + (uint32_t)((it + NB - 1) % NB) * raw_bytes,
-                                       tile_of(u + (NB - 1) * us), &rawbar[(it + NB - 1) % NB], ESZ);
-                    } else {
-                        --raw_issued;
-                    }
-                }
-            }
-        }
-        if (tile < p.num_tiles) {
-            const WinTile wt = win_tile(p, tile);
-            if (p.x_raw)
-                repack_strips(p, sbuf, sR + (uint32_t)(it % NB) * raw_bytes, wt, warp, lane);
-            else
-                pack_strips<T>(p, sbuf, wt, warp, lane);
-        }
+        const int tile = tile_of<PAIR>(p, u, rank);
+        if (tile < p.num_tiles)
+            pack_rows<T>(p, sRing, rtab, win_tile(p, tile), walk.base, cont ? max(0, p.rows - p.J * p.u) : 0,
+                         warp, lane);
         cp_async_commit_wait_all();
         fence_proxy_async_smem();
         if (PAIR)
             mbar_arrive_cluster(full_l + 8u * buf);  // every producer thread of both CTAs
         else
             mbar_arrive(&full[buf]);
-        if (p.x_raw) mbar_arrive(&rawfree[it % NB]);  // this thread is done with the staged rows
     }
     cp_async_commit_wait_all();  // nothing may land after the CTA exits
-    // after an early exit, bulk copies may still be in flight
-    if (tid == 0) {
-        for (int j = raw_done; j < raw_issued; ++j) mbar_wait(&rawbar[j % NB], (uint32_t)(j / NB) & 1u, drain, 93);
-        mbar_wait(bres, 0u, drain, 94);
-    }
+    if (tid == 0) mbar_wait(bres, 0u, drain, 94);  // after an early exit the filter copy may be in flight
 }
 
 __device__ __forceinline__ bool win_drain(uint64_t *bar, uint32_t parity, const WinParams &p) {
@@ -484,8 +388,8 @@ __device__ __forceinline__ bool win_drain(uint64_t *bar, uint32_t parity, const 
 }
 
 template <bool TF32, bool PAIR>
-__device__ void win_mma(const WinParams &p, uint32_t tmem_base, uint32_t sB, uint32_t sS,
-                        uint64_t *full, uint64_t *empty, uint64_t *tfull, uint64_t *tempty,
+__device__ void win_mma(const WinParams &p, uint32_t tmem_base, uint32_t sB, uint32_t sRing,
+                        const uint32_t *rtab, uint64_t *full, uint64_t *empty, uint64_t *tfull, uint64_t *tempty,
                         uint64_t *mma_done, uint64_t *bres, uint64_t *bpeer, const WaitCtl &ctl) {
     // 64-bit descriptors advanced in place: the start address (16-byte units)
     // sits in the low bits and stays below 256 KiB, so the additions never
@@ -494,13 +398,18 @@ __device__ void win_mma(const WinParams &p, uint32_t tmem_base, uint32_t sB, uin
     const uint64_t b0 = (uint64_t)((sB >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)(256 >> 4) << 32) |
                         (1ull << 46) | (6ull << 29 << 32);
     const uint64_t slab16 = (uint64_t)(PAIR ? p.BN / 2 : p.BN) * 2u;  // slab bytes / 16
-    const uint64_t strip16 = (uint64_t)(p.strip_bytes >> 4);
     const int R = p.R, steps = p.steps;
     const uint32_t idesc = p.idesc;
     bool ok = mbar_wait(bres, 0u, ctl, 7);
     if (PAIR) ok = ok && mbar_wait_cluster(bpeer, 0u, ctl, 13);
+    int ub, ue;
+    unit_range<PAIR>(p, ub, ue);
+    UnitWalk<PAIR> walk(p, ub);
+    const uint32_t slot16 = (uint32_t)p.slot_bytes >> 4;
+    const uint64_t ring_desc = p.a_hi | (uint64_t)((sRing >> 4) & 0x3FFFu);
     int it = 0;
-    for (int u = unit0<PAIR>(); ok && u < p.num_units; u += unit_stride<PAIR>(), ++it) {
+    for (int u = ub; ok && u < ue; ++u, ++it) {
+        if (u > ub) walk.next(p, u);
         const int buf = it & 1;
         const uint32_t ph = (uint32_t)(it >> 1) & 1u;
         // (pairs: the other CTA's epilogue and producers arrive remotely)
@@ -508,11 +417,13 @@ __device__ void win_mma(const WinParams &p, uint32_t tmem_base, uint32_t sB, uin
         if (!(PAIR ? mbar_wait_cluster(&full[buf], ph, ctl, 4) : mbar_wait(&full[buf], ph, ctl, 4))) break;
         tc_fence_after_sync();
         const uint32_t d = tmem_base + (uint32_t)buf * p.acc_stride;
-        uint64_t a_row = p.a_hi | (uint64_t)(((sS + (uint32_t)(buf * R) * (uint32_t)p.strip_bytes) >> 4) & 0x3FFFu);
         uint64_t bd = b0;
         uint32_t acc = 0;
-        for (int r = 0; r < R; ++r, a_row += strip16) {
-            uint64_t ad = a_row;
+        for (int r = 0; r < R; ++r) {
+            // filter row r reads slots (r*dh, j = 0 .. J-1) as one operand
+            int pos;
+            const int slot = ring_slot(p, rtab[r * p.dh], walk.base, pos);
+            uint64_t ad = ring_desc + (uint64_t)((uint32_t)slot * slot16);  // stays below 256 KiB
 #pragma unroll 4
             for (int st = 0; st < steps; ++st) {  // 32 bytes of window per MMA
                 if constexpr (PAIR) {
@@ -532,7 +443,7 @@ __device__ void win_mma(const WinParams &p, uint32_t tmem_base, uint32_t sB, uin
             }
         }
         if (PAIR) {
-            umma_commit_pair(&empty[buf], 3);  // both CTAs' strip buffers free
+            umma_commit_pair(&empty[buf], 3);  // both CTAs' rings may take new rows
             umma_commit_pair(&tfull[buf], 3);  // both CTAs' accumulator rows ready
         } else {
             umma_commit(&empty[buf]);
@@ -621,10 +532,12 @@ __device__ void win_epilogue(const WinParams &p, uint32_t rank, uint32_t tmem_ba
     const uint32_t tempty_l = PAIR ? mapa_shared(smem_u32(tempty), 0) : smem_u32(tempty);
     int nbuf = 0;
     int it = 0;
-    for (int u = unit0<PAIR>(); u < p.num_units; u += unit_stride<PAIR>(), ++it) {
+    int ub, ue;
+    unit_range<PAIR>(p, ub, ue);
+    for (int u = ub; u < ue; ++u, ++it) {
         const int buf = it & 1;
         const uint32_t ph = (uint32_t)(it >> 1) & 1u;
-        const int t = PAIR ? 2 * u + (int)rank : u;
+        const int t = tile_of<PAIR>(p, u, rank);
         int okw = 0;
         if (lane == 0) okw = mbar_wait(&tfull[buf], ph, ctl, 5) ? 1 : 0;
         okw = __shfl_sync(0xffffffffu, okw, 0);
@@ -714,10 +627,8 @@ __global__ void __launch_bounds__(WIN_THREADS, 1)
     uint8_t *epi = smem;  // y staging (1024-aligned)
     uint8_t *bptr = epi + (p.y_tma ? WIN_EPI_SMEM : 0);
     const size_t b_bytes = ((size_t)p.b_img_bytes + 1023) & ~(size_t)1023;
-    uint8_t *sptr = bptr + b_bytes;
-    uint8_t *rptr = sptr + (size_t)2 * p.R * p.strip_bytes;  // staged input rows
-    uint64_t *bars = reinterpret_cast<uint64_t *>(
-        rptr + (p.x_raw ? (size_t)p.raw_bufs * p.raw_rows * p.row_bytes : 0));
+    uint8_t *ring = bptr + b_bytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + p.ring_bytes);
     uint64_t *full = bars;
     uint64_t *empty = bars + 2;
     uint64_t *tfull = bars + 4;
@@ -725,10 +636,9 @@ __global__ void __launch_bounds__(WIN_THREADS, 1)
     uint64_t *mma_done = bars + 8;
     uint64_t *bres = bars + 9;
     uint64_t *bpeer = bars + 10;
-    uint64_t *rawbar = bars + 11;   // three: one per staging buffer (rows landed)
-    uint64_t *rawfree = bars + 14;  // three: every producer done with the buffer
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 17);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 11);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    uint32_t *rtab = reinterpret_cast<uint32_t *>(bars + 16);  // ring table, one entry per tile row
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
@@ -742,13 +652,10 @@ __global__ void __launch_bounds__(WIN_THREADS, 1)
         mbar_init(mma_done, 1u);
         mbar_init(bres, 1u);
         mbar_init(bpeer, 1u);
-        for (int i = 0; i < 3; ++i) {
-            mbar_init(&rawbar[i], 1u);
-            mbar_init(&rawfree[i], PROD_THREADS);
-        }
         *abort_flag = 0;
         fence_mbar_init();
     }
+    for (int i = threadIdx.x; i < p.rows; i += WIN_THREADS) rtab[i] = ring_entry(p, i);
     if (warp == MMA_WARP) {
         if (PAIR) {
             tmem_alloc_pair(tmem_slot, p.tmem_cols);
@@ -764,13 +671,13 @@ __global__ void __launch_bounds__(WIN_THREADS, 1)
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
     const WaitCtl ctl{abort_flag, p.err, p.timeout_ns};
-    const uint32_t sB = smem_u32(bptr), sS = smem_u32(sptr), sR = smem_u32(rptr);
+    const uint32_t sB = smem_u32(bptr), sRing = smem_u32(ring);
 
     if (warp < MMA_WARP) {
-        win_produce<T, PAIR>(p, rank, sB, sS, sR, full, empty, bres, bpeer, rawbar, rawfree, ctl);
+        win_produce<T, PAIR>(p, rank, sB, sRing, rtab, full, empty, bres, bpeer, ctl);
     } else if (warp == MMA_WARP) {
         if (lane == 0 && rank == 0)
-            win_mma<TF32, PAIR>(p, tmem_base, sB, sS, full, empty, tfull, tempty, mma_done, bres, bpeer, ctl);
+            win_mma<TF32, PAIR>(p, tmem_base, sB, sRing, rtab, full, empty, tfull, tempty, mma_done, bres, bpeer, ctl);
         if (lane == 0) win_drain(mma_done, 0u, p);  // the (leader's) final commit reaches this CTA
     } else {
         if (p.y_tma && lane == 0) prefetch_tmap(&tmY);
@@ -823,7 +730,9 @@ bool window_plan(const ConvProblem &pb, WinParams *wp, size_t *smem_out) {
     p.nb = (int)nb;
     p.nbw = (int)((nb + 3) / 4);
     p.steps = (p.A * D + 31) / 32;
-    const int need = pb.Q + p.A - 1;
+    p.px_read = p.steps * 32 / D;
+    // pixels the stored outputs of a row read: Q - 1 + px_read
+    const int need = pb.Q - 1 + p.px_read;
     if (need <= 32) p.Qs = 32;
     else if (need <= 64) p.Qs = 64;
     else p.Qs = 128;
@@ -831,25 +740,29 @@ bool window_plan(const ConvProblem &pb, WinParams *wp, size_t *smem_out) {
     p.J = WBM / p.Qs;
     p.segs = p.J > 1 ? 1 : (pb.Q + WBM - 1) / WBM;
     p.PB = (pb.P + p.J - 1) / p.J;
-    // the last MMA step of a row may read past pixel A-1 (16-byte pixels come
-    // in pairs); those pixels carry zero weights but must hold finite data
-    p.strip_px = WBM - 1 + (p.steps * 32 + D - 1) / D;
-    // whole warp steps: 4-byte words per lane (128/D pixels per step), or
-    // 16-byte chunks per lane when input rows are staged (512/D pixels)
-    const char *raw_ev = std::getenv("DLC_TC_WINRAW");
-    const bool raw_on = raw_ev && std::atoi(raw_ev) != 0;
-    const int step_px = raw_on ? 512 / D : 128 / D;
-    p.strip_px = ((p.strip_px + step_px - 1) / step_px) * step_px;
+    // A slot holds the phase pixels of one input row: Qs of them (J > 1; the
+    // operand of a filter row runs on into the next slot), or for wide rows
+    // the 128 + px_read - 1 a segment reads, in whole warp steps (128/D
+    // pixels), padded to the swizzle span.
     const int span = D == 64 ? 512 : 256;
-    p.strip_bytes = ((p.strip_px * D + span - 1) / span) * span;
-    const int G = 128 / D;
-    p.groups = (p.strip_px + G - 1) / G;
+    const int step_px = 128 / D;
+    if (p.J > 1) {
+        p.slot_px = p.Qs;
+        p.slot_bytes = p.Qs * D;
+    } else {
+        p.slot_px = ((WBM - 1 + p.px_read + step_px - 1) / step_px) * step_px;
+        p.slot_bytes = ((p.slot_px * D + span - 1) / span) * span;
+    }
+    p.rows = (p.J - 1) * pb.u + (pb.R - 1) * pb.dh + 1;
+    if (p.rows > WIN_MAX_ROWS) return false;
+    auto fdiv = [](long long a, long long b) { return a >= 0 ? a / b : -((b - 1 - a) / b); };
+    p.kb_off = (int)fdiv(-pb.pt, pb.u);
+    p.kspan = (int)(fdiv((long long)p.rows - 1 - pb.pt, pb.u) - p.kb_off + 1);
     if ((long long)pb.N * p.PB * p.segs > 0x7fffffffLL) return false;
     p.num_tiles = pb.N * p.PB * p.segs;
     p.BN = ((pb.K + 15) / 16) * 16;
-    // CTA pairs share each MMA (M = 256) and split the filters.  The kernel is
-    // producer-bound at N = 64 (packing, not MMA, sets the tile period), and
-    // pairing two SMs' producers measured slower, so pairs are opt-in:
+    // CTA pairs share each MMA (M = 256) and split the filters.  Pairing two
+    // SMs' producers measured slower at N = 64, so pairs are opt-in:
     // DLC_TC_WINPAIR=1.
     {
         const char *ev = std::getenv("DLC_TC_WINPAIR");
@@ -858,27 +771,25 @@ bool window_plan(const ConvProblem &pb, WinParams *wp, size_t *smem_out) {
     p.num_units = p.pair ? (p.num_tiles + 1) / 2 : p.num_tiles;
     p.b_img_bytes = pb.R * p.steps * (p.pair ? p.BN / 2 : p.BN) * 32;
     const long long b_bytes = ((long long)p.b_img_bytes + 1023) & ~1023LL;
-    const long long strips = 2LL * pb.R * p.strip_bytes;
-    if ((long long)pb.R * p.strip_px * 4 > 0x7fffffffLL) return false;
-    long long base = 1024 + b_bytes + strips + WIN_BAR_AREA;
-    if (base > WIN_MAX_SMEM) return false;
-    // Input rows staged whole by bulk copies: channels-innermost (or C == 1)
-    // dense rows whose starts and lengths are 16-byte multiples.  Measured
-    // slower than the 4-byte copies, so opt-in (DLC_TC_WINRAW=1); its shared
-    // memory is reserved only then.
-    p.raw_rows = (p.J - 1) * pb.u + (pb.R - 1) * pb.dh + 1;
-    const long long rowb = (long long)pb.W * pb.C * e;
-    const bool rows_dense = (pb.C == 1 && pb.xs[3] == 1) || (pb.xs[1] == 1 && pb.xs[3] == pb.C);
-    // three buffers if they fit beside the y staging, else two, else none
-    p.raw_bufs = base + 3 * p.raw_rows * rowb + WIN_EPI_SMEM <= WIN_MAX_SMEM ? 3 : 2;
-    if (raw_on && rows_dense && pb.xs[2] == (long long)pb.W * pb.xs[3] && rowb % 16 == 0 &&
-        (pb.xs[0] * e) % 16 == 0 && (pb.xs[2] * e) % 16 == 0 &&
-        p.raw_rows * rowb < (1LL << 20) &&
-        base + p.raw_bufs * p.raw_rows * rowb + WIN_EPI_SMEM <= WIN_MAX_SMEM &&
-        ((long long)pb.pl * pb.C * e) % 4 == 0 && nb % 4 == 0) {
-        p.x_raw = 1;
-        base += p.raw_bufs * p.raw_rows * rowb;
+    // Ring: 2*kspan slots per phase let a tile that starts a new run fill
+    // slots its predecessor does not read; if that does not fit, kspan + J
+    // slots and such a tile first waits for its predecessor's MMAs.  After the
+    // last slot: the pixels the operand of a J > 1 tile reads past it.
+    const long long tail = ((long long)p.px_read * D + 1023) & ~1023LL;
+    auto ring_of = [&](int rs) { return (long long)pb.u * (rs + p.J - 1) * p.slot_bytes + tail; };
+    const long long fixed = 1024 + b_bytes + WIN_BAR_AREA;
+    p.RS = 2 * p.kspan;
+    p.disc_wait = 0;
+    if (fixed + ring_of(p.RS) > WIN_MAX_SMEM) {
+        p.RS = p.kspan + p.J;
+        p.disc_wait = 1;
     }
+    p.RSJ = p.RS + p.J - 1;
+    if ((long long)pb.u * p.RSJ >= 65536) return false;  // ring table fields
+    const long long ring = ring_of(p.RS);
+    if (fixed + ring > WIN_MAX_SMEM) return false;
+    p.ring_bytes = (int)ring;
+    const long long base = fixed + ring;
     // the packed filter image goes through the handle's repacking buffer
     if ((long long)pb.R * p.steps * p.BN * 32 > DLC_WPACK_BYTES) return false;  // both parts
     if (wp) *wp = p;
@@ -960,7 +871,6 @@ dlcStatus_t dlc_launch_window(dlcContext *ctx, const ConvProblem &pb) {
                 ((long long)pb.pl * pb.C * e) % 4 == 0 && (long long)pb.W * pb.C * e < (1LL << 30))
                    ? 1 : 0;
     p.row_bytes = (int)((long long)pb.W * pb.C * e);
-    if (p.x_raw && ((uintptr_t)pb.x % 16) != 0) p.x_raw = 0;  // smem stays reserved
     if (!ctx->wpack) return DLC_STATUS_INTERNAL_ERROR;
     p.wpack = ctx->wpack;
     p.y_tma = (win_y_tma_ok(pb) && smem + WIN_EPI_SMEM <= (size_t)WIN_MAX_SMEM) ? 1 : 0;
@@ -974,7 +884,7 @@ dlcStatus_t dlc_launch_window(dlcContext *ctx, const ConvProblem &pb) {
     while (cols < (uint32_t)(2 * p.BN)) cols <<= 1;
     p.tmem_cols = cols;
     p.acc_stride = cols / 2;
-    // strips: rows D bytes apart, 8-row groups 8*D apart; 16-byte rows use no
+    // ring slots: rows D bytes apart, 8-row groups 8*D apart; 16-byte rows use no
     // swizzle and a 16-byte step between the two K halves of an MMA
     if (p.D == 16)
         p.a_hi = ((uint64_t)(16 >> 4) << 16) | ((uint64_t)(128 >> 4) << 32) | (1ull << 46);

@@ -168,7 +168,7 @@ def test_tc_runs_parity_full(handle, layer, monkeypatch):
 
 # ---------------------------------------------------------------------------
 # tensor cores, window kernel: few channels per horizontal stride step; the
-# lowered rows are read in place from packed input-row strips
+# lowered rows are read in place from a ring of packed input rows
 # ---------------------------------------------------------------------------
 
 WINDOW_CASES = [
@@ -205,6 +205,11 @@ WINDOW_CASES = [
     L("win_bf16_c3_k64_11x11_s4_odd_tiles", 1, 3, 75, 67, 64, 11, 11, **P(2, 2, 2, 2), u=4, v=4),
     # a single tile: one CTA, no pair
     L("win_bf16_c3_k32_5x5_one_tile", 1, 3, 9, 9, 32, 5, 5, **P(2, 2, 2, 2)),
+    # wide rows of 64-byte phase pixels and 9 filter rows: the ring of 2*kspan
+    # slots does not fit beside the filters, so the short ring (kspan + 1
+    # slots) runs, where a tile that starts a new image waits for the MMAs of
+    # the tile before it
+    L("win_bf16_c24_k64_9x3_wide_short_ring", 19, 24, 12, 150, 64, 9, 3, **P(4, 4, 1, 1)),
 ]
 
 
@@ -214,18 +219,7 @@ def test_tc_window_parity_full(handle, layer):
                   expect_kernel="tc_window")
 
 
-@pytest.mark.parametrize("pair", ["1", "0"], ids=["pairs", "single"])
-@pytest.mark.parametrize("layer", [WINDOW_CASES[i] for i in (0, 1, 4, 5, 12, 15)],
-                         ids=lambda l: l.name)
-def test_tc_window_staged_rows(handle, layer, pair, monkeypatch):
-    """Input rows bulk-copied to shared memory and repacked there (opt-in)."""
-    monkeypatch.setenv("DLC_TC_WINRAW", "1")
-    monkeypatch.setenv("DLC_TC_WINPAIR", pair)
-    run_and_check(handle, layer, 2350 + WINDOW_CASES.index(layer), full=True,
-                  expect_kernel="tc_window")
-
-
-@pytest.mark.parametrize("layer", [WINDOW_CASES[i] for i in (0, 2, 5, 7, 12, 13, 15, 16)],
+@pytest.mark.parametrize("layer", [WINDOW_CASES[i] for i in (0, 2, 5, 7, 12, 13, 15, 16, 17)],
                          ids=lambda l: l.name)
 def test_tc_window_cta_pairs(handle, layer, monkeypatch):
     """CTA pairs sharing each MMA over 256 rows (opt-in)."""
