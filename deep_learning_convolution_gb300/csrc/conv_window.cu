@@ -65,9 +65,11 @@ constexpr int MMA_WARP = PROD_THREADS / 32;          // warp 8
 constexpr int WIN_THREADS = PROD_THREADS + 32 + 128;
 constexpr int WIN_MAX_SMEM = 232448;
 constexpr int WIN_EPI_BUF = 32 * 128;                // one warp's 32 rows x 32 FP32 columns
-constexpr int WIN_EPI_SMEM = 4 * WIN_EPI_BUF;        // 4 epilogue warps, one buffer each
+constexpr int WIN_EPI_SMEM = 4 * WIN_EPI_BUF;        // 4 epilogue warps, one buffer each (x2 when
+                                                     // two fit: a store overlaps the next staging)
 constexpr int WIN_MAX_ROWS = 224;                  // input rows per tile (ring table)
-constexpr int WIN_BAR_AREA = 128 + 4 * WIN_MAX_ROWS;  // barriers, then the ring table
+constexpr int WIN_MAX_MMAS = 256;                  // MMAs per tile (descriptor table)
+constexpr int WIN_BAR_AREA = 128 + 4 * WIN_MAX_ROWS + 4 * WIN_MAX_MMAS;  // barriers, tables
 
 struct WinParams {
     int N, C, H, W, K, R, S, P, Q;
@@ -88,6 +90,8 @@ struct WinParams {
                       // for the MMAs of the tile before it
     int ring_bytes;
     int row_bytes;    // bytes of one input row (x_word)
+    int x_stage;      // new input rows arrive by one bulk copy per tile into a stage buffer
+    int stage_bytes;  // bytes of one of the two stage buffers: rows * row_bytes
     const void *wpack;  // the filter slabs, packed by window_pack_filters
     int b_img_bytes;    // bytes of one CTA's part: R*steps*(BN/ctas) rows of 32
     int pair;           // launched as CTA pairs (cta_group::2, M = 256 per MMA)
@@ -100,6 +104,7 @@ struct WinParams {
     const float *bias;
     float alpha, beta;
     int relu, y_bf16, y_tma;
+    int epi_bufs;     // staging buffers per epilogue warp (1 or 2)
     int x_word;       // input rows are contiguous 4-byte-aligned runs, phase pixels
                       // start on 4-byte boundaries
     int BN;
@@ -112,18 +117,6 @@ struct WinParams {
 struct WinTile {
     int n, p0, q0;
 };
-
-// Tile t: the row blocks of one (image, segment) are consecutive, so a CTA
-// that walks consecutive tiles moves down one image J output rows at a time.
-__device__ __forceinline__ WinTile win_tile(const WinParams &p, int t) {
-    WinTile wt;
-    const int rest = t / p.PB;
-    const int n = rest / p.segs;
-    wt.n = n;
-    wt.q0 = (rest - n * p.segs) * WBM;
-    wt.p0 = (t - rest * p.PB) * p.J;
-    return wt;
-}
 
 __device__ __forceinline__ int floor_div(int a, int b) { return a >= 0 ? a / b : -((b - 1 - a) / b); }
 
@@ -241,10 +234,9 @@ __device__ void pack_rows(const WinParams &p, uint32_t ring, const uint32_t *rta
     const uint32_t mdelta = (uint32_t)p.RS * (uint32_t)p.slot_bytes;  // slot -> its mirror
     const char *xb = static_cast<const char *>(p.x);
     const int lb = p.pl * p.C * ESZ;  // phase pixel P's data start at byte P*nb - lb
+    int ri = lo / spr, st0 = lo - (lo / spr) * spr;  // the warp's first (row, step)
 #pragma unroll 1
-    for (int item = lo; item < hi;) {
-        const int ri = item / spr;
-        const int st0 = item - ri * spr;
+    for (int item = lo; item < hi; ++ri, st0 = 0) {
         const int st1 = min(spr, st0 + (hi - item));
         item += st1 - st0;
         const int i = i0 + ri;
@@ -257,13 +249,16 @@ __device__ void pack_rows(const WinParams &p, uint32_t ring, const uint32_t *rta
         if (p.x_word) {
             const char *rowp = xb + ((long long)wt.n * p.xs[0] + (long long)(row_ok ? h : 0) * p.xs[2]) * ESZ;
             int bt = (P0 + st0 * G + dp) * p.nb - lb + (int)inner;  // byte of the row this lane copies
-            const bool lane_ok = row_ok && wp < p.nbw;
+            // padding words and rows outside the image copy nothing (zero fill)
+            const int lim = (row_ok && wp < p.nbw) ? p.row_bytes : 0;
             const int gnb = G * p.nb;
+            // slots start on a swizzle period, so step st's chunk XOR is st & chmask
 #pragma unroll 4
             for (int st = st0; st < st1; ++st) {
-                const bool in = lane_ok && (unsigned)bt < (unsigned)p.row_bytes;
-                const uint32_t n = in ? (uint32_t)min(p.row_bytes - bt, 4) : 0u;
-                const uint32_t dst = paddr + ((((inner >> 4) ^ ((paddr >> 7) & chmask)) << 4) | (inner & 15u));
+                const int rem = lim - bt;
+                const bool in = bt >= 0 && rem > 0;
+                const uint32_t n = in ? (uint32_t)min(rem, 4) : 0u;
+                const uint32_t dst = paddr + (inner ^ (((uint32_t)st & chmask) << 4));
                 const char *src = in ? rowp + bt : xb;
                 cp_async_4(dst, src, n);
                 if (mirror) cp_async_4(dst + mdelta, src, n);
@@ -286,14 +281,110 @@ __device__ void pack_rows(const WinParams &p, uint32_t ring, const uint32_t *rta
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 if (st + k >= st1) break;
-                const uint32_t pa = paddr + 128u * k;
-                const uint32_t dst = pa + ((((inner >> 4) ^ ((pa >> 7) & chmask)) << 4) | (inner & 15u));
+                const uint32_t dst = paddr + 128u * k + (inner ^ (((uint32_t)(st + k) & chmask) << 4));
                 const uint32_t word = pack_word<T>(val[k]);
                 sts32(dst, word);
                 if (mirror) sts32(dst + mdelta, word);
             }
             w0 += 4 * G * p.v;
             paddr += 512u;
+        }
+    }
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ void sts128v(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+// Bulk-copies the new rows of a tile -- tile rows i in [i0, rows), input rows
+// p0*u - pt + i -- that lie inside the image into stage buffer `sbuf` (stage
+// row i - i0; dense rows are consecutive in x, so one copy), completing on
+// `bar`.  A tile past the last one (a pair's missing second tile) copies
+// nothing but still completes the barrier's phase.
+__device__ void stage_rows(const WinParams &p, uint32_t sbuf, const WinTile &wt, bool valid, int i0,
+                           uint64_t *bar, int esz) {
+    int lo = 0, n = 0;
+    long long src = 0;
+    if (valid) {
+        const int h0 = wt.p0 * p.u - p.pt + i0;
+        lo = max(0, -h0);
+        n = max(0, min(p.rows - i0, p.H - h0) - lo);
+        src = ((long long)wt.n * p.xs[0] + (long long)(h0 + lo) * p.xs[2]) * esz;
+    }
+    const uint32_t bytes = (uint32_t)n * (uint32_t)p.row_bytes;
+    mbar_arrive_expect_tx(bar, bytes);
+    if (n > 0)
+        bulk_load_1d(sbuf + (uint32_t)lo * (uint32_t)p.row_bytes, static_cast<const char *>(p.x) + src, bytes, bar);
+}
+
+// Packs a tile's new rows from the stage buffer into their ring slots (and
+// mirror slots), the pixels pack_rows covers.  Lane l builds 16-byte chunk
+// l % (D/16) of pixel l / (D/16) of each step's 512/D pixels: up to four
+// 4-byte loads from the staged row (zeros outside the row, past the data and
+// for rows outside the image) and one 16-byte store, its chunk XORed with
+// address bits 7.. (a step spans whole swizzle periods, so the XOR depends on
+// the lane only).  Two steps' loads are in flight before their stores.
+__device__ void repack_rows(const WinParams &p, uint32_t ring, uint32_t sbuf, const uint32_t *rtab,
+                            const WinTile &wt, int base, int i0, int warp, int lane) {
+    constexpr int NW = PROD_THREADS / 32;
+    const int chl = p.d_log2 - 4;  // log2 of 16-byte chunks per phase pixel
+    const int kap = lane & ((1 << chl) - 1);
+    const int dp = lane >> chl;
+    const int G = 32 >> chl;       // pixels per warp step
+    const uint32_t chmask = (uint32_t)(p.D >> 4) - 1u;
+    const uint32_t cho = (((uint32_t)kap ^ (((uint32_t)(dp * p.D) >> 7) & chmask)) << 4);
+    const int P0 = p.J > 1 ? 0 : wt.q0;
+    const int need = min(p.slot_px, (p.J > 1 ? p.Q : p.Q - wt.q0) - 1 + p.px_read);
+    const int spr = (need + G - 1) / G;
+    const int total = (p.rows - i0) * spr;
+    const int lo = (int)(((long long)total * warp) / NW);
+    const int hi = (int)(((long long)total * (warp + 1)) / NW);
+    const int esz = p.nb / (p.v * p.C);
+    const int lb = p.pl * p.C * esz;
+    const int b0 = kap * 16;                              // first byte of the chunk in its pixel
+    const int nwords = max(0, min(4, (p.nb - b0) >> 2));  // data words of the chunk
+    const uint32_t rowb = (uint32_t)p.row_bytes;
+    const uint32_t mdelta = (uint32_t)p.RS * (uint32_t)p.slot_bytes;
+    const int gnb = G * p.nb;
+    int ri = lo / spr, st0 = lo - (lo / spr) * spr;  // the warp's first (row, step)
+#pragma unroll 1
+    for (int item = lo; item < hi; ++ri, st0 = 0) {
+        const int st1 = min(spr, st0 + (hi - item));
+        item += st1 - st0;
+        const int i = i0 + ri;
+        const int h = wt.p0 * p.u - p.pt + i;
+        const int nw = (h >= 0 && h < p.H) ? nwords : 0;  // rows outside the image are zeros
+        int pos;
+        const int slot = ring_slot(p, rtab[i], base, pos);
+        const bool mirror = pos < p.J - 1;
+        const uint32_t rb = sbuf + (uint32_t)ri * rowb;
+        int bt = (P0 + st0 * G + dp) * p.nb - lb + b0;
+        uint32_t paddr = ring + (uint32_t)slot * (uint32_t)p.slot_bytes + (uint32_t)(st0 * G + dp) * p.D + cho;
+        for (int st = st0; st < st1; st += 2) {
+            uint32_t v[2][4];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int b = bt + k * gnb;
+#pragma unroll
+                for (int w = 0; w < 4; ++w)
+                    v[k][w] = (st + k < st1 && w < nw && (unsigned)(b + 4 * w) < rowb) ? lds32(rb + b + 4 * w) : 0u;
+            }
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                // a step may run past the slot's last pixel (wide rows): skip those
+                if (st + k >= st1 || (st + k) * G + dp >= p.slot_px) break;
+                const uint32_t dst = paddr + 512u * k;
+                sts128v(dst, v[k][0], v[k][1], v[k][2], v[k][3]);
+                if (mirror) sts128v(dst + mdelta, v[k][0], v[k][1], v[k][2], v[k][3]);
+            }
+            bt += 2 * gnb;
+            paddr += 1024u;
         }
     }
 }
@@ -314,27 +405,53 @@ __device__ __forceinline__ int tile_of(const WinParams &p, int u, uint32_t rank)
 // Walks a CTA's units [ub, ue).  Unit u continues unit u-1 when, for every
 // CTA of the pair, it holds the next J output rows of the same image and
 // segment; its ring base then moves J slots (only the last J*u rows of the
-// tile are new), else kspan slots (every row is new).
+// tile are new), else kspan slots (every row is new).  The walk also keeps
+// the coordinates of this CTA's tile (rank 1 of a pair: tile u + num_units),
+// so no role divides per tile.  Tile t is image t / (segs*PB), segment
+// (t / PB) % segs, output rows (t % PB)*J ..: the row blocks of one (image,
+// segment) are consecutive, so a CTA moves down one image J rows at a time.
 template <bool PAIR>
 struct UnitWalk {
     int pbL, pbP, base;
-    __device__ UnitWalk(const WinParams &p, int ub)
-        : pbL(ub % p.PB), pbP((ub + p.num_units) % p.PB), base(0) {}
+    int n, seg, valid;  // this CTA's tile: image, segment, exists
+    __device__ UnitWalk(const WinParams &p, int ub, uint32_t rank)
+        : pbL(ub % p.PB), pbP((ub + p.num_units) % p.PB), base(0) {
+        const int t = tile_of<PAIR>(p, ub, rank);
+        const int rest = t / p.PB;
+        n = rest / p.segs;
+        seg = rest - n * p.segs;
+        valid = t < p.num_tiles;
+        own_rank = (int)rank;
+    }
+    int own_rank;
     // to unit u = (previous unit) + 1; whether u continues the previous unit
     __device__ __forceinline__ bool next(const WinParams &p, int u) {
         if (++pbL == p.PB) pbL = 0;
         if (++pbP == p.PB) pbP = 0;
+        if ((PAIR && own_rank ? pbP : pbL) == 0 && ++seg == p.segs) {
+            seg = 0;
+            ++n;
+        }
+        if (PAIR && own_rank) valid = u + p.num_units < p.num_tiles;
         const bool cont = pbL != 0 && (!PAIR || u + p.num_units >= p.num_tiles || pbP != 0);
         base += cont ? p.J : p.kspan;
         if (base >= p.RS) base -= p.RS;
         return cont;
     }
+    __device__ __forceinline__ WinTile tile(const WinParams &p) const {
+        WinTile wt;
+        wt.n = n;
+        wt.q0 = seg * WBM;
+        wt.p0 = (PAIR && own_rank ? pbP : pbL) * p.J;
+        return wt;
+    }
 };
 
 template <typename T, bool PAIR>
 __device__ void win_produce(const WinParams &p, uint32_t rank, uint32_t sB, uint32_t sRing,
-                            const uint32_t *rtab, uint64_t *full, uint64_t *empty, uint64_t *bres,
-                            uint64_t *bpeer, const WaitCtl &ctl) {
+                            uint32_t sStage, const uint32_t *rtab, uint64_t *full, uint64_t *empty,
+                            uint64_t *bres, uint64_t *bpeer, uint64_t *sfull, const WaitCtl &ctl) {
+    constexpr int ESZ = (int)sizeof(T);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t full_l = PAIR ? mapa_shared(smem_u32(full), 0) : smem_u32(full);  // leader's
     volatile int no_abort = 0;
@@ -355,21 +472,47 @@ __device__ void win_produce(const WinParams &p, uint32_t rank, uint32_t sB, uint
     for (uint32_t i = (uint32_t)tid; i < (uint32_t)p.ring_bytes / 16u; i += PROD_THREADS)
         asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(sRing + 16u * i), "r"(0u) : "memory");
     asm volatile("bar.sync 1, %0;" ::"n"(PROD_THREADS) : "memory");  // producer warps only
-    UnitWalk<PAIR> walk(p, ub);
+    // Staged rows: the rows of unit u + 1 are copied while unit u is packed.
+    int staged = 0;  // stage copies issued (thread 0)
+    UnitWalk<PAIR> walk(p, ub, rank);
+    if (p.x_stage && tid == 0 && ub < ue) {
+        stage_rows(p, sStage, walk.tile(p), walk.valid, 0, &sfull[0], ESZ);
+        staged = 1;
+    }
     int it = 0;
     for (int u = ub; u < ue; ++u, ++it) {
         const bool cont = u > ub && walk.next(p, u);
+        const int i0 = cont ? max(0, p.rows - p.J * p.u) : 0;
         const int buf = it & 1;
         const uint32_t ph = (uint32_t)(it >> 1) & 1u;
         bool ok = mbar_wait(&empty[buf], ph ^ 1u, ctl, 1);
         // a short ring: the previous tile's rows must be free before a new run overwrites them
         if (ok && !cont && p.disc_wait && it >= 1)
             ok = mbar_wait(&empty[(it - 1) & 1], (uint32_t)((it - 1) >> 1) & 1u, ctl, 15);
-        if (!ok) break;
-        const int tile = tile_of<PAIR>(p, u, rank);
-        if (tile < p.num_tiles)
-            pack_rows<T>(p, sRing, rtab, win_tile(p, tile), walk.base, cont ? max(0, p.rows - p.J * p.u) : 0,
-                         warp, lane);
+        if (p.x_stage) {
+            ok = ok && mbar_wait(&sfull[buf], ph, ctl, 16);
+            // every producer is past unit u - 1, whose stage buffer the next
+            // copy overwrites; the decision to go on is the same for all
+            int stop = (!ok || *ctl.abort_flag) ? 1 : 0;
+            asm volatile("{\n\t.reg .pred q, r;\n\tsetp.ne.b32 q, %1, 0;\n\t"
+                         "bar.red.or.pred r, 1, %2, q;\n\tselp.b32 %0, 1, 0, r;\n\t}\n"
+                         : "=r"(stop) : "r"(stop), "n"(PROD_THREADS) : "memory");
+            if (stop) break;
+            if (tid == 0 && u + 1 < ue) {
+                fence_proxy_async_smem();  // the reads of unit u - 1 before the copy's writes
+                UnitWalk<PAIR> nx = walk;
+                const bool c1 = nx.next(p, u + 1);
+                stage_rows(p, sStage + (uint32_t)((it + 1) & 1) * (uint32_t)p.stage_bytes, nx.tile(p),
+                           nx.valid, c1 ? max(0, p.rows - p.J * p.u) : 0, &sfull[(it + 1) & 1], ESZ);
+                ++staged;
+            }
+            if (walk.valid)
+                repack_rows(p, sRing, sStage + (uint32_t)buf * (uint32_t)p.stage_bytes, rtab,
+                            walk.tile(p), walk.base, i0, warp, lane);
+        } else {
+            if (!ok) break;
+            if (walk.valid) pack_rows<T>(p, sRing, rtab, walk.tile(p), walk.base, i0, warp, lane);
+        }
         cp_async_commit_wait_all();
         fence_proxy_async_smem();
         if (PAIR)
@@ -378,7 +521,11 @@ __device__ void win_produce(const WinParams &p, uint32_t rank, uint32_t sB, uint
             mbar_arrive(&full[buf]);
     }
     cp_async_commit_wait_all();  // nothing may land after the CTA exits
-    if (tid == 0) mbar_wait(bres, 0u, drain, 94);  // after an early exit the filter copy may be in flight
+    if (tid == 0) {
+        // after an early exit the filter copy and a stage copy may be in flight
+        mbar_wait(bres, 0u, drain, 94);
+        for (int j = it; j < staged; ++j) mbar_wait(&sfull[j & 1], (uint32_t)(j >> 1) & 1u, drain, 95);
+    }
 }
 
 __device__ __forceinline__ bool win_drain(uint64_t *bar, uint32_t parity, const WinParams &p) {
@@ -387,45 +534,65 @@ __device__ __forceinline__ bool win_drain(uint64_t *bar, uint32_t parity, const 
     return mbar_wait(bar, parity, c, 90);
 }
 
+// A wait by lane 0 whose outcome the whole warp takes.
+template <bool CLUSTER>
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const WaitCtl &ctl, int code) {
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0)
+        ok = (CLUSTER ? mbar_wait_cluster(bar, parity, ctl, code) : mbar_wait(bar, parity, ctl, code)) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
+
 template <bool TF32, bool PAIR>
 __device__ void win_mma(const WinParams &p, uint32_t tmem_base, uint32_t sB, uint32_t sRing,
-                        const uint32_t *rtab, uint64_t *full, uint64_t *empty, uint64_t *tfull, uint64_t *tempty,
-                        uint64_t *mma_done, uint64_t *bres, uint64_t *bpeer, const WaitCtl &ctl) {
-    // 64-bit descriptors advanced in place: the start address (16-byte units)
-    // sits in the low bits and stays below 256 KiB, so the additions never
-    // carry into other fields.  B slabs: 32-byte swizzle, 8-row groups 256
-    // bytes apart, BN/2 rows per CTA for a pair.
+                        const uint32_t *rtab, uint32_t *atab, uint64_t *full, uint64_t *empty,
+                        uint64_t *tfull, uint64_t *tempty, uint64_t *mma_done, uint64_t *bres,
+                        uint64_t *bpeer, const WaitCtl &ctl) {
+    // B slabs: 32-byte swizzle, 8-row groups 256 bytes apart, BN/2 rows per
+    // CTA for a pair; the descriptor advances in place (its start address, in
+    // 16-byte units, stays below 256 KiB and never carries into other fields).
+    const int lane = threadIdx.x & 31;
     const uint64_t b0 = (uint64_t)((sB >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)(256 >> 4) << 32) |
                         (1ull << 46) | (6ull << 29 << 32);
     const uint64_t slab16 = (uint64_t)(PAIR ? p.BN / 2 : p.BN) * 2u;  // slab bytes / 16
-    const int R = p.R, steps = p.steps;
+    const int steps = p.steps, nm = p.R * p.steps;
     const uint32_t idesc = p.idesc;
-    bool ok = mbar_wait(bres, 0u, ctl, 7);
-    if (PAIR) ok = ok && mbar_wait_cluster(bpeer, 0u, ctl, 13);
+    const uint32_t slot16 = (uint32_t)p.slot_bytes >> 4;
+    const uint32_t a_lo0 = (uint32_t)p.a_hi + ((sRing >> 4) & 0x3FFFu);
+    const uint64_t a_hi = p.a_hi & 0xFFFFFFFF00000000ull;
+    bool ok = warp_wait<false>(bres, 0u, ctl, 7);
+    if (PAIR) ok = ok && warp_wait<true>(bpeer, 0u, ctl, 13);
     int ub, ue;
     unit_range<PAIR>(p, ub, ue);
-    UnitWalk<PAIR> walk(p, ub);
-    const uint32_t slot16 = (uint32_t)p.slot_bytes >> 4;
-    const uint64_t ring_desc = p.a_hi | (uint64_t)((sRing >> 4) & 0x3FFFu);
+    UnitWalk<PAIR> walk(p, ub, 0u);
     int it = 0;
     for (int u = ub; ok && u < ue; ++u, ++it) {
         if (u > ub) walk.next(p, u);
+        // this unit's A descriptors, one per MMA, built by the warp while the
+        // previous unit's MMAs run: MMA (r, st) reads the J slots from tile
+        // row r*dh's slot on, 32*st bytes into each pixel window
+        for (int m = lane; m < nm; m += 32) {
+            const int r = m / steps, st = m - r * steps;
+            int pos;
+            const int slot = ring_slot(p, rtab[r * p.dh], walk.base, pos);
+            atab[m] = a_lo0 + (uint32_t)slot * slot16 + 2u * (uint32_t)st;  // below 256 KiB
+        }
+        __syncwarp();
         const int buf = it & 1;
         const uint32_t ph = (uint32_t)(it >> 1) & 1u;
         // (pairs: the other CTA's epilogue and producers arrive remotely)
-        if (!(PAIR ? mbar_wait_cluster(&tempty[buf], ph ^ 1u, ctl, 3) : mbar_wait(&tempty[buf], ph ^ 1u, ctl, 3))) break;
-        if (!(PAIR ? mbar_wait_cluster(&full[buf], ph, ctl, 4) : mbar_wait(&full[buf], ph, ctl, 4))) break;
+        if (!warp_wait<PAIR>(&tempty[buf], ph ^ 1u, ctl, 3)) break;
+        if (!warp_wait<PAIR>(&full[buf], ph, ctl, 4)) break;
         tc_fence_after_sync();
-        const uint32_t d = tmem_base + (uint32_t)buf * p.acc_stride;
-        uint64_t bd = b0;
-        uint32_t acc = 0;
-        for (int r = 0; r < R; ++r) {
-            // filter row r reads slots (r*dh, j = 0 .. J-1) as one operand
-            int pos;
-            const int slot = ring_slot(p, rtab[r * p.dh], walk.base, pos);
-            uint64_t ad = ring_desc + (uint64_t)((uint32_t)slot * slot16);  // stays below 256 KiB
+        if (lane == 0) {
+            const uint32_t d = tmem_base + (uint32_t)buf * p.acc_stride;
+            uint64_t bd = b0;
 #pragma unroll 4
-            for (int st = 0; st < steps; ++st) {  // 32 bytes of window per MMA
+            for (int m = 0; m < nm; ++m) {  // 32 bytes of window per MMA
+                const uint64_t ad = a_hi | atab[m];
+                const uint32_t acc = m > 0 ? 1u : 0u;
                 if constexpr (PAIR) {
                     if constexpr (TF32)
                         umma_tf32_pair(d, ad, bd, idesc, acc);
@@ -437,24 +604,26 @@ __device__ void win_mma(const WinParams &p, uint32_t tmem_base, uint32_t sB, uin
                     else
                         umma_bf16_nc(d, ad, bd, idesc, acc);
                 }
-                acc = 1;
-                ad += 2;
                 bd += slab16;
             }
+            if (PAIR) {
+                umma_commit_pair(&empty[buf], 3);  // both CTAs' rings may take new rows
+                umma_commit_pair(&tfull[buf], 3);  // both CTAs' accumulator rows ready
+            } else {
+                umma_commit(&empty[buf]);
+                umma_commit(&tfull[buf]);
+            }
         }
-        if (PAIR) {
-            umma_commit_pair(&empty[buf], 3);  // both CTAs' rings may take new rows
-            umma_commit_pair(&tfull[buf], 3);  // both CTAs' accumulator rows ready
-        } else {
-            umma_commit(&empty[buf]);
-            umma_commit(&tfull[buf]);
-        }
+        __syncwarp();
     }
     // Every MMA issued must complete before tensor memory is released.
-    if (PAIR)
-        umma_commit_pair(mma_done, 3);
-    else
-        umma_commit(mma_done);
+    if (lane == 0) {
+        if (PAIR)
+            umma_commit_pair(mma_done, 3);
+        else
+            umma_commit(mma_done);
+    }
+    __syncwarp();
 }
 
 // Row `lane` of a warp's 32 x 32 FP32 staging block, in the 128-byte swizzle
@@ -527,25 +696,26 @@ __device__ void win_epilogue(const WinParams &p, uint32_t rank, uint32_t tmem_ba
     const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
     const int row = quad * 32 + lane;
     const bool plain = p.beta == 0.f && p.bias == nullptr && !p.relu;
-    uint8_t *my_buf = epi_smem + quad * WIN_EPI_BUF;
+    uint8_t *my_buf = epi_smem + quad * p.epi_bufs * WIN_EPI_BUF;
     const int kend = min(p.BN, ((p.K + 31) / 32) * 32);
     const uint32_t tempty_l = PAIR ? mapa_shared(smem_u32(tempty), 0) : smem_u32(tempty);
     int nbuf = 0;
     int it = 0;
     int ub, ue;
     unit_range<PAIR>(p, ub, ue);
+    UnitWalk<PAIR> walk(p, ub, rank);
     for (int u = ub; u < ue; ++u, ++it) {
+        if (u > ub) walk.next(p, u);
         const int buf = it & 1;
         const uint32_t ph = (uint32_t)(it >> 1) & 1u;
-        const int t = tile_of<PAIR>(p, u, rank);
         int okw = 0;
         if (lane == 0) okw = mbar_wait(&tfull[buf], ph, ctl, 5) ? 1 : 0;
         okw = __shfl_sync(0xffffffffu, okw, 0);
         if (!okw) break;
         __syncwarp();
         tc_fence_after_sync();
-        const bool have = t < p.num_tiles;  // a pair's second tile may not exist
-        const WinTile wt = win_tile(p, have ? t : 0);
+        const bool have = walk.valid;  // a pair's second tile may not exist
+        const WinTile wt = walk.tile(p);
         int j, q, qw;
         if (p.J > 1) {
             j = row >> p.qs_log2;
@@ -582,9 +752,15 @@ __device__ void win_epilogue(const WinParams &p, uint32_t rank, uint32_t tmem_ba
                     for (int i = 0; i < 32; ++i) val[i] = lv[i];
                 }
                 if (p.y_tma) {
-                    uint8_t *sb = my_buf;
-                    if (nbuf >= 1) {  // the previous store has read the buffer
-                        if (lane == 0) bulk_wait_group_read<0>();
+                    uint8_t *sb = my_buf + (p.epi_bufs == 2 ? (nbuf & 1) * WIN_EPI_BUF : 0);
+                    // the store that last used this buffer has read it
+                    if (nbuf >= p.epi_bufs) {
+                        if (lane == 0) {
+                            if (p.epi_bufs == 2)
+                                bulk_wait_group_read<1>();
+                            else
+                                bulk_wait_group_read<0>();
+                        }
                         __syncwarp();
                     }
                     win_stage_row(sb, lane, val);
@@ -625,10 +801,11 @@ __global__ void __launch_bounds__(WIN_THREADS, 1)
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);  // same offset in both CTAs
     uint8_t *epi = smem;  // y staging (1024-aligned)
-    uint8_t *bptr = epi + (p.y_tma ? WIN_EPI_SMEM : 0);
+    uint8_t *bptr = epi + (p.y_tma ? p.epi_bufs * WIN_EPI_SMEM : 0);
     const size_t b_bytes = ((size_t)p.b_img_bytes + 1023) & ~(size_t)1023;
     uint8_t *ring = bptr + b_bytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + p.ring_bytes);
+    uint8_t *stage = ring + p.ring_bytes;  // two stage buffers (x_stage)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(stage + (p.x_stage ? 2 * (size_t)p.stage_bytes : 0));
     uint64_t *full = bars;
     uint64_t *empty = bars + 2;
     uint64_t *tfull = bars + 4;
@@ -636,9 +813,11 @@ __global__ void __launch_bounds__(WIN_THREADS, 1)
     uint64_t *mma_done = bars + 8;
     uint64_t *bres = bars + 9;
     uint64_t *bpeer = bars + 10;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 11);
+    uint64_t *sfull = bars + 11;  // two: a stage buffer's rows landed
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     uint32_t *rtab = reinterpret_cast<uint32_t *>(bars + 16);  // ring table, one entry per tile row
+    uint32_t *atab = rtab + WIN_MAX_ROWS;                        // A descriptors of a unit, one per MMA
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
@@ -652,6 +831,8 @@ __global__ void __launch_bounds__(WIN_THREADS, 1)
         mbar_init(mma_done, 1u);
         mbar_init(bres, 1u);
         mbar_init(bpeer, 1u);
+        mbar_init(&sfull[0], 1u);
+        mbar_init(&sfull[1], 1u);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -671,13 +852,13 @@ __global__ void __launch_bounds__(WIN_THREADS, 1)
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
     const WaitCtl ctl{abort_flag, p.err, p.timeout_ns};
-    const uint32_t sB = smem_u32(bptr), sRing = smem_u32(ring);
+    const uint32_t sB = smem_u32(bptr), sRing = smem_u32(ring), sStage = smem_u32(stage);
 
     if (warp < MMA_WARP) {
-        win_produce<T, PAIR>(p, rank, sB, sRing, rtab, full, empty, bres, bpeer, ctl);
+        win_produce<T, PAIR>(p, rank, sB, sRing, sStage, rtab, full, empty, bres, bpeer, sfull, ctl);
     } else if (warp == MMA_WARP) {
-        if (lane == 0 && rank == 0)
-            win_mma<TF32, PAIR>(p, tmem_base, sB, sRing, rtab, full, empty, tfull, tempty, mma_done, bres, bpeer, ctl);
+        if (rank == 0)  // the whole warp runs the issuing loop; one lane issues
+            win_mma<TF32, PAIR>(p, tmem_base, sB, sRing, rtab, atab, full, empty, tfull, tempty, mma_done, bres, bpeer, ctl);
         if (lane == 0) win_drain(mma_done, 0u, p);  // the (leader's) final commit reaches this CTA
     } else {
         if (p.y_tma && lane == 0) prefetch_tmap(&tmY);
@@ -742,8 +923,8 @@ bool window_plan(const ConvProblem &pb, WinParams *wp, size_t *smem_out) {
     p.PB = (pb.P + p.J - 1) / p.J;
     // A slot holds the phase pixels of one input row: Qs of them (J > 1; the
     // operand of a filter row runs on into the next slot), or for wide rows
-    // the 128 + px_read - 1 a segment reads, in whole warp steps (128/D
-    // pixels), padded to the swizzle span.
+    // the 128 + px_read - 1 a segment reads, in whole warp steps of the
+    // 4-byte copies (128/D pixels), padded to the swizzle span.
     const int span = D == 64 ? 512 : 256;
     const int step_px = 128 / D;
     if (p.J > 1) {
@@ -754,7 +935,7 @@ bool window_plan(const ConvProblem &pb, WinParams *wp, size_t *smem_out) {
         p.slot_bytes = ((p.slot_px * D + span - 1) / span) * span;
     }
     p.rows = (p.J - 1) * pb.u + (pb.R - 1) * pb.dh + 1;
-    if (p.rows > WIN_MAX_ROWS) return false;
+    if (p.rows > WIN_MAX_ROWS || pb.R * p.steps > WIN_MAX_MMAS) return false;
     auto fdiv = [](long long a, long long b) { return a >= 0 ? a / b : -((b - 1 - a) / b); };
     p.kb_off = (int)fdiv(-pb.pt, pb.u);
     p.kspan = (int)(fdiv((long long)p.rows - 1 - pb.pt, pb.u) - p.kb_off + 1);
@@ -875,7 +1056,22 @@ dlcStatus_t dlc_launch_window(dlcContext *ctx, const ConvProblem &pb) {
     p.wpack = ctx->wpack;
     p.y_tma = (win_y_tma_ok(pb) && smem + WIN_EPI_SMEM <= (size_t)WIN_MAX_SMEM) ? 1 : 0;
     if (const char *ev = std::getenv("DLC_TC_YTMA")) p.y_tma = p.y_tma && std::atoi(ev) != 0;
-    if (p.y_tma) smem += WIN_EPI_SMEM;
+    const size_t epi1 = p.y_tma ? (size_t)WIN_EPI_SMEM : 0;
+    // Staged rows: dense rows whose starts and lengths are 16-byte multiples
+    // arrive by one bulk copy per tile (DLC_TC_WINSTAGE=0 keeps the 4-byte copies).
+    {
+        const long long stage = (long long)p.rows * p.row_bytes;
+        const bool dense = pb.xs[2] == (long long)pb.W * pb.xs[3];
+        bool on = p.x_word && dense && p.row_bytes % 16 == 0 && ((uintptr_t)pb.x % 16) == 0 &&
+                  (pb.xs[0] * e) % 16 == 0 && (pb.xs[2] * e) % 16 == 0 && stage < (1LL << 20) &&
+                  smem + 2 * (size_t)stage + epi1 <= (size_t)WIN_MAX_SMEM;
+        if (const char *ev = std::getenv("DLC_TC_WINSTAGE")) on = on && std::atoi(ev) != 0;
+        p.x_stage = on ? 1 : 0;
+        p.stage_bytes = on ? (int)stage : 0;
+        if (on) smem += 2 * (size_t)stage;
+    }
+    p.epi_bufs = (p.y_tma && smem + 2 * WIN_EPI_SMEM <= (size_t)WIN_MAX_SMEM) ? 2 : 1;
+    if (p.y_tma) smem += (size_t)p.epi_bufs * WIN_EPI_SMEM;
 
     const uint32_t fmt = tf32 ? 2u : 1u;
     p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(p.BN >> 3) << 17) |

@@ -219,6 +219,14 @@ def test_tc_window_parity_full(handle, layer):
                   expect_kernel="tc_window")
 
 
+@pytest.mark.parametrize("layer", [WINDOW_CASES[i] for i in (4, 5, 6, 10, 14)], ids=lambda l: l.name)
+def test_tc_window_word_copies(handle, layer, monkeypatch):
+    """Rows that could be bulk-staged, copied word by word instead."""
+    monkeypatch.setenv("DLC_TC_WINSTAGE", "0")
+    run_and_check(handle, layer, 2360 + WINDOW_CASES.index(layer), full=True,
+                  expect_kernel="tc_window")
+
+
 @pytest.mark.parametrize("layer", [WINDOW_CASES[i] for i in (0, 2, 5, 7, 12, 13, 15, 16, 17)],
                          ids=lambda l: l.name)
 def test_tc_window_cta_pairs(handle, layer, monkeypatch):
