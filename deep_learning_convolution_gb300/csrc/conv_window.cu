@@ -69,7 +69,7 @@ constexpr int WIN_EPI_SMEM = 4 * WIN_EPI_BUF;        // 4 epilogue warps, one bu
                                                      // two fit: a store overlaps the next staging)
 constexpr int WIN_MAX_ROWS = 224;                  // input rows per tile (ring table)
 constexpr int WIN_MAX_MMAS = 256;                  // MMAs per tile (descriptor table)
-constexpr int WIN_BAR_AREA = 128 + 4 * WIN_MAX_ROWS + 4 * WIN_MAX_MMAS;  // barriers, tables
+constexpr int WIN_BAR_AREA = 192 + 4 * WIN_MAX_ROWS + 8 * WIN_MAX_MMAS;  // barriers, tables
 
 struct WinParams {
     int N, C, H, W, K, R, S, P, Q;
@@ -109,6 +109,7 @@ struct WinParams {
                       // start on 4-byte boundaries
     int BN;
     uint32_t idesc, tmem_cols, acc_stride;
+    int nacc_log2;    // TMEM accumulators: 2 or 4
     uint64_t a_hi;    // ring descriptor bits other than the start address
     int *err;
     unsigned long long timeout_ns;
@@ -449,13 +450,15 @@ struct UnitWalk {
 
 template <typename T, bool PAIR>
 __device__ void win_produce(const WinParams &p, uint32_t rank, uint32_t sB, uint32_t sRing,
-                            uint32_t sStage, const uint32_t *rtab, uint64_t *full, uint64_t *empty,
+                            uint32_t sStage, const uint32_t *rtab, uint32_t *atab, uint64_t *full, uint64_t *empty,
                             uint64_t *bres, uint64_t *bpeer, uint64_t *sfull, const WaitCtl &ctl) {
     constexpr int ESZ = (int)sizeof(T);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t full_l = PAIR ? mapa_shared(smem_u32(full), 0) : smem_u32(full);  // leader's
     volatile int no_abort = 0;
     const WaitCtl drain{&no_abort, p.err, p.timeout_ns};  // waits for copies in flight
+    const uint32_t slot16 = (uint32_t)p.slot_bytes >> 4;
+    const uint32_t a_lo0 = (uint32_t)p.a_hi + ((sRing >> 4) & 0x3FFFu);  // descriptor low word of slot 0
     int ub, ue;
     unit_range<PAIR>(p, ub, ue);
     // this CTA's part of the packed filter image: one bulk copy on bres
@@ -513,6 +516,17 @@ __device__ void win_produce(const WinParams &p, uint32_t rank, uint32_t sB, uint
             if (!ok) break;
             if (walk.valid) pack_rows<T>(p, sRing, rtab, walk.tile(p), walk.base, i0, warp, lane);
         }
+        if (warp == 0) {
+            // the unit's MMA operands for the MMA warp: MMA (r, st) reads the J
+            // slots from tile row r*dh's slot on, 32*st bytes into each window
+            uint32_t *tab = atab + buf * WIN_MAX_MMAS;
+            for (int r = lane; r < p.R; r += 32) {
+                int pos;
+                const int slot = ring_slot(p, rtab[r * p.dh], walk.base, pos);
+                const uint32_t a = a_lo0 + (uint32_t)slot * slot16;  // below 256 KiB
+                for (int st = 0; st < p.steps; ++st) tab[r * p.steps + st] = a + 2u * (uint32_t)st;
+            }
+        }
         cp_async_commit_wait_all();
         fence_proxy_async_smem();
         if (PAIR)
@@ -546,8 +560,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const 
 }
 
 template <bool TF32, bool PAIR>
-__device__ void win_mma(const WinParams &p, uint32_t tmem_base, uint32_t sB, uint32_t sRing,
-                        const uint32_t *rtab, uint32_t *atab, uint64_t *full, uint64_t *empty,
+__device__ void win_mma(const WinParams &p, uint32_t tmem_base, uint32_t sB, const uint32_t *atab,
+                        uint64_t *full, uint64_t *empty,
                         uint64_t *tfull, uint64_t *tempty, uint64_t *mma_done, uint64_t *bres,
                         uint64_t *bpeer, const WaitCtl &ctl) {
     // B slabs: 32-byte swizzle, 8-row groups 256 bytes apart, BN/2 rows per
@@ -557,41 +571,30 @@ __device__ void win_mma(const WinParams &p, uint32_t tmem_base, uint32_t sB, uin
     const uint64_t b0 = (uint64_t)((sB >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)(256 >> 4) << 32) |
                         (1ull << 46) | (6ull << 29 << 32);
     const uint64_t slab16 = (uint64_t)(PAIR ? p.BN / 2 : p.BN) * 2u;  // slab bytes / 16
-    const int steps = p.steps, nm = p.R * p.steps;
+    const int nm = p.R * p.steps;
     const uint32_t idesc = p.idesc;
-    const uint32_t slot16 = (uint32_t)p.slot_bytes >> 4;
-    const uint32_t a_lo0 = (uint32_t)p.a_hi + ((sRing >> 4) & 0x3FFFu);
     const uint64_t a_hi = p.a_hi & 0xFFFFFFFF00000000ull;
     bool ok = warp_wait<false>(bres, 0u, ctl, 7);
     if (PAIR) ok = ok && warp_wait<true>(bpeer, 0u, ctl, 13);
     int ub, ue;
     unit_range<PAIR>(p, ub, ue);
-    UnitWalk<PAIR> walk(p, ub, 0u);
     int it = 0;
     for (int u = ub; ok && u < ue; ++u, ++it) {
-        if (u > ub) walk.next(p, u);
-        // this unit's A descriptors, one per MMA, built by the warp while the
-        // previous unit's MMAs run: MMA (r, st) reads the J slots from tile
-        // row r*dh's slot on, 32*st bytes into each pixel window
-        for (int m = lane; m < nm; m += 32) {
-            const int r = m / steps, st = m - r * steps;
-            int pos;
-            const int slot = ring_slot(p, rtab[r * p.dh], walk.base, pos);
-            atab[m] = a_lo0 + (uint32_t)slot * slot16 + 2u * (uint32_t)st;  // below 256 KiB
-        }
-        __syncwarp();
         const int buf = it & 1;
         const uint32_t ph = (uint32_t)(it >> 1) & 1u;
+        const int abuf = it & ((1 << p.nacc_log2) - 1);  // accumulator
+        const uint32_t aph = (uint32_t)(it >> p.nacc_log2) & 1u;
         // (pairs: the other CTA's epilogue and producers arrive remotely)
-        if (!warp_wait<PAIR>(&tempty[buf], ph ^ 1u, ctl, 3)) break;
+        if (!warp_wait<PAIR>(&tempty[abuf], aph ^ 1u, ctl, 3)) break;
         if (!warp_wait<PAIR>(&full[buf], ph, ctl, 4)) break;
         tc_fence_after_sync();
         if (lane == 0) {
-            const uint32_t d = tmem_base + (uint32_t)buf * p.acc_stride;
+            const uint32_t d = tmem_base + (uint32_t)abuf * p.acc_stride;
+            const uint32_t *tab = atab + buf * WIN_MAX_MMAS;  // written by the producers
             uint64_t bd = b0;
 #pragma unroll 4
             for (int m = 0; m < nm; ++m) {  // 32 bytes of window per MMA
-                const uint64_t ad = a_hi | atab[m];
+                const uint64_t ad = a_hi | tab[m];
                 const uint32_t acc = m > 0 ? 1u : 0u;
                 if constexpr (PAIR) {
                     if constexpr (TF32)
@@ -608,10 +611,10 @@ __device__ void win_mma(const WinParams &p, uint32_t tmem_base, uint32_t sB, uin
             }
             if (PAIR) {
                 umma_commit_pair(&empty[buf], 3);  // both CTAs' rings may take new rows
-                umma_commit_pair(&tfull[buf], 3);  // both CTAs' accumulator rows ready
+                umma_commit_pair(&tfull[abuf], 3);  // both CTAs' accumulator rows ready
             } else {
                 umma_commit(&empty[buf]);
-                umma_commit(&tfull[buf]);
+                umma_commit(&tfull[abuf]);
             }
         }
         __syncwarp();
@@ -706,8 +709,8 @@ __device__ void win_epilogue(const WinParams &p, uint32_t rank, uint32_t tmem_ba
     UnitWalk<PAIR> walk(p, ub, rank);
     for (int u = ub; u < ue; ++u, ++it) {
         if (u > ub) walk.next(p, u);
-        const int buf = it & 1;
-        const uint32_t ph = (uint32_t)(it >> 1) & 1u;
+        const int buf = it & ((1 << p.nacc_log2) - 1);  // accumulator
+        const uint32_t ph = (uint32_t)(it >> p.nacc_log2) & 1u;
         int okw = 0;
         if (lane == 0) okw = mbar_wait(&tfull[buf], ph, ctl, 5) ? 1 : 0;
         okw = __shfl_sync(0xffffffffu, okw, 0);
@@ -808,16 +811,16 @@ __global__ void __launch_bounds__(WIN_THREADS, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(stage + (p.x_stage ? 2 * (size_t)p.stage_bytes : 0));
     uint64_t *full = bars;
     uint64_t *empty = bars + 2;
-    uint64_t *tfull = bars + 4;
-    uint64_t *tempty = bars + 6;
-    uint64_t *mma_done = bars + 8;
-    uint64_t *bres = bars + 9;
-    uint64_t *bpeer = bars + 10;
-    uint64_t *sfull = bars + 11;  // two: a stage buffer's rows landed
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
+    uint64_t *tfull = bars + 4;   // four: an accumulator is ready
+    uint64_t *tempty = bars + 8;  // four: an accumulator is free
+    uint64_t *mma_done = bars + 12;
+    uint64_t *bres = bars + 13;
+    uint64_t *bpeer = bars + 14;
+    uint64_t *sfull = bars + 15;  // two: a stage buffer's rows landed
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 17);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    uint32_t *rtab = reinterpret_cast<uint32_t *>(bars + 16);  // ring table, one entry per tile row
-    uint32_t *atab = rtab + WIN_MAX_ROWS;                        // A descriptors of a unit, one per MMA
+    uint32_t *rtab = reinterpret_cast<uint32_t *>(bars + 24);  // ring table, one entry per tile row
+    uint32_t *atab = rtab + WIN_MAX_ROWS;  // two tables of a unit's A descriptors, one entry per MMA
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
@@ -825,6 +828,8 @@ __global__ void __launch_bounds__(WIN_THREADS, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&full[i], PAIR ? 2u * PROD_THREADS : PROD_THREADS);  // every producer
             mbar_init(&empty[i], 1u);
+        }
+        for (int i = 0; i < 4; ++i) {
             mbar_init(&tfull[i], 1u);
             mbar_init(&tempty[i], PAIR ? 8u : 4u);  // the epilogue warps (of both CTAs)
         }
@@ -855,10 +860,10 @@ __global__ void __launch_bounds__(WIN_THREADS, 1)
     const uint32_t sB = smem_u32(bptr), sRing = smem_u32(ring), sStage = smem_u32(stage);
 
     if (warp < MMA_WARP) {
-        win_produce<T, PAIR>(p, rank, sB, sRing, sStage, rtab, full, empty, bres, bpeer, sfull, ctl);
+        win_produce<T, PAIR>(p, rank, sB, sRing, sStage, rtab, atab, full, empty, bres, bpeer, sfull, ctl);
     } else if (warp == MMA_WARP) {
         if (rank == 0)  // the whole warp runs the issuing loop; one lane issues
-            win_mma<TF32, PAIR>(p, tmem_base, sB, sRing, rtab, atab, full, empty, tfull, tempty, mma_done, bres, bpeer, ctl);
+            win_mma<TF32, PAIR>(p, tmem_base, sB, atab, full, empty, tfull, tempty, mma_done, bres, bpeer, ctl);
         if (lane == 0) win_drain(mma_done, 0u, p);  // the (leader's) final commit reaches this CTA
     } else {
         if (p.y_tma && lane == 0) prefetch_tmap(&tmY);
@@ -1076,10 +1081,13 @@ dlcStatus_t dlc_launch_window(dlcContext *ctx, const ConvProblem &pb) {
     const uint32_t fmt = tf32 ? 2u : 1u;
     p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(p.BN >> 3) << 17) |
               ((uint32_t)((p.pair ? 2 * WBM : WBM) >> 4) << 24);
-    uint32_t cols = 32;
-    while (cols < (uint32_t)(2 * p.BN)) cols <<= 1;
-    p.tmem_cols = cols;
-    p.acc_stride = cols / 2;
+    // TMEM: four accumulators when they fit in 512 columns, else two, so the
+    // MMAs of the next tiles need not wait for the epilogue
+    uint32_t acc = 32;
+    while (acc < (uint32_t)p.BN) acc <<= 1;
+    p.nacc_log2 = 4 * acc <= 512 ? 2 : 1;
+    p.acc_stride = acc;
+    p.tmem_cols = acc << p.nacc_log2;
     // ring slots: rows D bytes apart, 8-row groups 8*D apart; 16-byte rows use no
     // swizzle and a 16-byte step between the two K halves of an MMA
     if (p.D == 16)
