@@ -353,6 +353,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
     conv_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmY) {
     constexpr int BK = PROW / (TF32 ? 4 : 2);
+    griddep_launch_dependents();  // the next grid may claim SMs this one leaves
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);  // same offset in both CTAs
@@ -400,6 +401,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
     const uint32_t tmem_base = *tmem_slot;
     const WaitCtl ctl{abort_flag, p.err, p.timeout_ns};
     const uint32_t sA = smem_u32(smA), sB = smem_u32(smB);
+    griddep_wait();  // no global memory before the grid ahead of this one is done
 
     if (warp == 0) {
         if (lane == 0) pair_produce<BK>(p, rank, &tmA, &tmB, sA, sB, full, empty, ctl);
@@ -427,6 +429,14 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
 // ---------------------------------------------------------------------------
 // The pair kernel serves every im2col-eligible problem unless DLC_TC_PAIR=0
 // or the context asks for the stream-K schedule (the single-SM kernel's).
+bool dlc_pdl_enabled() {
+    static const bool on = [] {
+        const char *ev = std::getenv("DLC_PDL");
+        return !(ev && std::atoi(ev) == 0);
+    }();
+    return on;
+}
+
 bool dlc_pair_enabled(const dlcContext *ctx) {
     if (ctx && ctx->force_sk) return false;
     const char *ev = std::getenv("DLC_TC_PAIR");
@@ -547,16 +557,18 @@ dlcStatus_t dlc_launch_pair(dlcContext *ctx, const ConvProblem &pb) {
         return DLC_STATUS_EXECUTION_FAILED;
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = dlc_pdl_enabled() ? 1 : 0;
     cfg.blockDim = dim3(PAIR_THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = ctx->stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 1;  // the occupancy query takes the cluster shape only
     // one pair per two SMs that can hold a cluster at once (persistent pairs)
     int max_clusters = 0;
     cfg.gridDim = dim3(2 * (ctx->sm_count / 2), 1, 1);
@@ -590,6 +602,7 @@ dlcStatus_t dlc_launch_pair(dlcContext *ctx, const ConvProblem &pb) {
         }
     }
     cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, kern, p, ta, tb, ty) != cudaSuccess) return DLC_STATUS_EXECUTION_FAILED;
     ctx->launches += 1;
     return DLC_STATUS_SUCCESS;

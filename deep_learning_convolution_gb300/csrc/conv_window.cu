@@ -173,6 +173,8 @@ __device__ __forceinline__ uint32_t pack_word(const T (&e)[4 / sizeof(T)]) {
 template <typename T>
 __global__ void window_pack_filters(const __grid_constant__ WinParams p, uint32_t *img) {
     constexpr int ESZ = (int)sizeof(T), EPW = 4 / ESZ;
+    griddep_wait();  // the previous convolution may still read the image
+    griddep_launch_dependents();
     const int words = p.R * p.steps * p.BN * 8;
     const int wi = blockIdx.x * blockDim.x + threadIdx.x;
     if (wi >= words) return;
@@ -800,6 +802,7 @@ template <bool TF32, bool PAIR>
 __global__ void __launch_bounds__(WIN_THREADS, 1)
     conv_window_kernel(const __grid_constant__ WinParams p, const __grid_constant__ CUtensorMap tmY) {
     using T = typename std::conditional<TF32, uint32_t, uint16_t>::type;
+    griddep_launch_dependents();  // the next grid may claim SMs this one leaves
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);  // same offset in both CTAs
@@ -858,6 +861,7 @@ __global__ void __launch_bounds__(WIN_THREADS, 1)
     const uint32_t tmem_base = *tmem_slot;
     const WaitCtl ctl{abort_flag, p.err, p.timeout_ns};
     const uint32_t sB = smem_u32(bptr), sRing = smem_u32(ring), sStage = smem_u32(stage);
+    griddep_wait();  // no global memory before the grid ahead of this one is done
 
     if (warp < MMA_WARP) {
         win_produce<T, PAIR>(p, rank, sB, sRing, sStage, rtab, atab, full, empty, bres, bpeer, sfull, ctl);
@@ -998,34 +1002,38 @@ bool win_y_tma_ok(const ConvProblem &pb) {
 template <bool TF32>
 cudaError_t win_launch(const WinParams &p, const CUtensorMap &ty, int sm_count, size_t smem,
                        cudaStream_t st) {
-    if (!p.pair) {
-        auto kern = conv_window_kernel<TF32, false>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        const int grid = std::max(1, std::min(p.num_units, sm_count));
-        kern<<<grid, WIN_THREADS, smem, st>>>(p, ty);
-        return cudaGetLastError();
-    }
-    auto kern = conv_window_kernel<TF32, true>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = dlc_pdl_enabled() ? 1 : 0;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.blockDim = dim3(WIN_THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (!p.pair) {
+        auto kern = conv_window_kernel<TF32, false>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        cfg.gridDim = dim3(std::max(1, std::min(p.num_units, sm_count)), 1, 1);
+        return cudaLaunchKernelEx(&cfg, kern, p, ty);
+    }
+    auto kern = conv_window_kernel<TF32, true>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cfg.attrs = attr + 1;  // the occupancy query takes the cluster shape only
     cfg.gridDim = dim3(2 * (sm_count / 2), 1, 1);
     int max_clusters = 0;
     e = cudaOccupancyMaxActiveClusters(&max_clusters, (const void *)kern, &cfg);
     if (e != cudaSuccess) return e;
     if (max_clusters < 1) return cudaErrorLaunchOutOfResources;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
     cfg.gridDim = dim3(2 * std::min(max_clusters, p.num_units), 1, 1);
     return cudaLaunchKernelEx(&cfg, kern, p, ty);
 }
@@ -1115,12 +1123,20 @@ dlcStatus_t dlc_launch_window(dlcContext *ctx, const ConvProblem &pb) {
     }
     {
         const int words = p.R * p.steps * p.BN * 8;
-        const int blocks = (words + 255) / 256;
-        if (tf32)
-            window_pack_filters<uint32_t><<<blocks, 256, 0, ctx->stream>>>(p, static_cast<uint32_t *>(ctx->wpack));
-        else
-            window_pack_filters<uint16_t><<<blocks, 256, 0, ctx->stream>>>(p, static_cast<uint32_t *>(ctx->wpack));
-        if (cudaGetLastError() != cudaSuccess) return DLC_STATUS_EXECUTION_FAILED;
+        cudaLaunchConfig_t cfg;
+        std::memset(&cfg, 0, sizeof(cfg));
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = dlc_pdl_enabled() ? 1 : 0;
+        cfg.gridDim = dim3((words + 255) / 256, 1, 1);
+        cfg.blockDim = dim3(256, 1, 1);
+        cfg.stream = ctx->stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        uint32_t *img = static_cast<uint32_t *>(ctx->wpack);
+        const cudaError_t e = tf32 ? cudaLaunchKernelEx(&cfg, window_pack_filters<uint32_t>, p, img)
+                                   : cudaLaunchKernelEx(&cfg, window_pack_filters<uint16_t>, p, img);
+        if (e != cudaSuccess) return DLC_STATUS_EXECUTION_FAILED;
         ctx->launches += 1;
     }
     cudaError_t err = tf32 ? win_launch<true>(p, ty, ctx->sm_count, smem, ctx->stream)

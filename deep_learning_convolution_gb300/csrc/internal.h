@@ -89,5 +89,8 @@ bool dlc_window_ok(const ConvProblem &pb);
 dlcStatus_t dlc_launch_window(dlcContext *ctx, const ConvProblem &pb);
 // conv_pair.cu: the im2col lowering on pairs of SMs (DLC_TC_PAIR=0 turns it off).
 bool dlc_pair_enabled(const dlcContext *ctx);
+// Launches of the window and pair kernels overlap the tail of the grid before
+// them (programmatic dependent launch) unless DLC_PDL=0.
+bool dlc_pdl_enabled();
 dlcStatus_t dlc_launch_pair(dlcContext *ctx, const ConvProblem &pb);
 

@@ -127,6 +127,18 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity
     }
 }
 
+// ---- programmatic dependent launch ------------------------------------------
+// A grid launched with programmatic stream serialization may start while the
+// grid before it in the stream is still running.  The earlier grid lets it be
+// scheduled (launch_dependents; it then takes SMs the earlier grid leaves), and
+// the later grid waits, before its first global-memory access, until the
+// earlier grid has completed and its writes are visible (wait).  Both are
+// no-ops without such a launch.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- proxy fences -----------------------------------------------------------
 // Makes this thread's generic-proxy shared-memory writes visible to the async
 // proxy (TMA, tcgen05.mma operand reads).
