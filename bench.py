@@ -317,19 +317,63 @@ def run_e2e(args, probs, handle, stream, dev, step_flops, world):
         d2h += hy.numel() * hy.element_size()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
+    # The layers of a step are independent problems, so their copies overlap
+    # other layers' convolutions: inputs go in on one copy stream, results
+    # come out on another, and events keep each layer's buffers ordered (its
+    # inputs land before its convolution; the previous step's convolution is
+    # done reading them before they are overwritten; the previous read-back of
+    # y is done before the convolution writes y again).  Every step still
+    # moves all inputs in and all results out.
+    s_in = torch.cuda.Stream(device=dev)
+    s_outs = [torch.cuda.Stream(device=dev) for _ in range(args.e2e_out_streams)]
+    nl = len(probs)
+    ev_in = [torch.cuda.Event() for _ in range(nl)]
+    ev_conv = [None] * nl
+    ev_out = [[None] * len(s_outs) for _ in range(nl)]
+    # each y comes back in equal contiguous parts, one per read-back stream
+    # (copy engines work in parallel)
+    parts = []
+    for pr, (hx, hw, hy) in zip(probs, host):
+        dv, hv = pr["y"].view(-1), hy.view(-1)
+        n = dv.numel()
+        cuts = [n * i // len(s_outs) for i in range(len(s_outs) + 1)]
+        parts.append([(dv[a:b], hv[a:b]) for a, b in zip(cuts[:-1], cuts[1:])])
 
     def one():
-        for pr, (hx, hw, hy) in zip(probs, host):
-            pr["x"].copy_(hx, non_blocking=True)
-            pr["w"].copy_(hw, non_blocking=True)
+        for j, (pr, (hx, hw, hy)) in enumerate(zip(probs, host)):
+            with torch.cuda.stream(s_in):
+                if ev_conv[j] is not None:
+                    s_in.wait_event(ev_conv[j])
+                pr["x"].copy_(hx, non_blocking=True)
+                pr["w"].copy_(hw, non_blocking=True)
+                ev_in[j].record(s_in)
+            stream.wait_event(ev_in[j])
+            for ev in ev_out[j]:
+                if ev is not None:
+                    stream.wait_event(ev)
             pr["conv"](pr["x"], pr["w"], pr["y"])
-            hy.copy_(pr["y"], non_blocking=True)
+            ev_conv[j] = torch.cuda.Event()
+            ev_conv[j].record(stream)
+            for i, (so, (dpart, hpart)) in enumerate(zip(s_outs, parts[j])):
+                with torch.cuda.stream(so):
+                    so.wait_event(ev_conv[j])
+                    hpart.copy_(dpart, non_blocking=True)
+                    ev_out[j][i] = torch.cuda.Event()
+                    ev_out[j][i].record(so)
+
+    def join():  # the compute stream waits for every copy of the step
+        for j in range(nl):
+            for ev in ev_out[j]:
+                stream.wait_event(ev)
 
     one()
+    join()
     torch.cuda.synchronize()
     start.record(stream)
+    s_in.wait_event(start)  # no copy of the timed steps starts before the clock
     for _ in range(steps):
         one()
+    join()
     end.record(stream)
     torch.cuda.synchronize()
     ms = start.elapsed_time(end)
@@ -448,6 +492,8 @@ def main():
     ap.add_argument("--workload", default="alexnet",
                     choices=["alexnet", "overfeat", "resnet50", "speech"])
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-out-streams", type=int, default=1,
+                    help="streams the end-to-end run reads results back on")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-layer", type=int, default=None,
