@@ -71,6 +71,24 @@ def layer_geometry(layer, P, Q):
     return flops, x_bytes + w_bytes + y_bytes
 
 
+def layer_output_dims(layer):
+    P = (layer.H + layer.pad_top + layer.pad_bottom - (layer.dil_h * (layer.R - 1) + 1)) // layer.u + 1
+    Q = (layer.W + layer.pad_left + layer.pad_right - (layer.dil_w * (layer.S - 1) + 1)) // layer.v + 1
+    return P, Q
+
+
+def workload_config(workload, world):
+    """The `config` both arms print: the workload and how a step is timed."""
+    from deep_learning_convolution_gb300 import synth
+    layers = synth.WORKLOADS[workload]
+    step_flops = sum(layer_geometry(l, *layer_output_dims(l))[0] for l in layers)
+    return {"workload": f"{workload}_stack", "layers": [l.name for l in layers],
+            "batch": layers[0].N, "layout": layers[0].layout,
+            "output": "fp32", "l2": "flushed between steps (256 MiB write, untimed)",
+            "parallelism": f"replicas{world}" if world > 1 else "single_gpu",
+            "flops_per_step": step_flops}
+
+
 # ---------------------------------------------------------------------------
 # clocks sampling
 # ---------------------------------------------------------------------------
@@ -279,11 +297,7 @@ def run_ours(args, rank, world, local_rank):
             "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
             "data": "synthetic",
-            "config": {"workload": f"{args.workload}_stack", "layers": [p["layer"].name for p in probs],
-                       "batch": layers[0].N, "layout": layers[0].layout,
-                       "output": "fp32", "l2": "flushed between steps (256 MiB write, untimed)",
-                       "parallelism": f"replicas{world}" if world > 1 else "single_gpu",
-                       "flops_per_step": step_flops},
+            "config": workload_config(args.workload, world),
             "roofline": roofline,
             "layers": layer_rows,
             "e2e": e2e,
@@ -446,7 +460,7 @@ def run_reference(args, rank, world):
             "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": f"{args.workload}_stack", "sample": "1 image per step"},
+            "config": workload_config(args.workload, world),
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
