@@ -13,9 +13,9 @@
 // D bytes apart -- no swizzle with 16-byte rows and a 16-byte K step between
 // core matrices, or the 32-/64-byte swizzle, which the tensor core applies on
 // absolute shared-memory address bits -- therefore reads the lowered rows of
-// up to 128 consecutive output pixels straight out of one strip of phase
-// pixels.  Filter taps are reordered to the same (a, phi, c) order once per CTA
-// and stay resident in shared memory.
+// up to 128 consecutive output pixels straight out of the packed input row.
+// Filter taps are reordered to the same (a, phi, c) order once per call and
+// stay resident in every CTA's shared memory.
 //
 // Tiles: the 128 MMA rows are J output rows of one image (Qs rows each, Qs a
 // power of two covering every pixel a stored output reads, J = 128/Qs) or, for

@@ -460,48 +460,6 @@ __device__ __forceinline__ void umma_commit_pair(uint64_t *bar, uint16_t mask) {
         : "memory");
 }
 
-// The same MMAs and commits issued by one elected lane of a converged warp.
-// Every lane of the warp runs the issuing loop, so descriptors and addresses
-// stay warp-uniform values and the MMAs go out back to back.
-#define DLC_ELECT_MMA(KIND, GROUP)                                                         \
-    asm volatile("{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\t"                               \
-                 "elect.sync r|e, 0xffffffff;\n\t"                                         \
-                 "setp.ne.b32 p, %4, 0;\n\t"                                               \
-                 "@e tcgen05.mma.cta_group::" GROUP ".kind::" KIND " [%0], %1, %2, %3, p;\n\t}\n" \
-                 ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate))
-__device__ __forceinline__ void umma_bf16_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-    DLC_ELECT_MMA("f16", "1");
-}
-__device__ __forceinline__ void umma_tf32_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-    DLC_ELECT_MMA("tf32", "1");
-}
-__device__ __forceinline__ void umma_bf16_pair_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                                 uint32_t idesc, uint32_t accumulate) {
-    DLC_ELECT_MMA("f16", "2");
-}
-__device__ __forceinline__ void umma_tf32_pair_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                                 uint32_t idesc, uint32_t accumulate) {
-    DLC_ELECT_MMA("tf32", "2");
-}
-#undef DLC_ELECT_MMA
-__device__ __forceinline__ void umma_commit_w(uint64_t *bar) {
-    asm volatile(
-        "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\telect.sync r|e, 0xffffffff;\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-__device__ __forceinline__ void umma_commit_pair_w(uint64_t *bar, uint16_t mask) {
-    asm volatile(
-        "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\telect.sync r|e, 0xffffffff;\n\t"
-        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;\n\t}\n" ::"r"(smem_u32(bar)),
-        "h"(mask)
-        : "memory");
-}
-
 // Shared-memory matrix descriptor for a K-major operand tile stored with the
 // 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart, tile
 // base 1024-byte aligned.  `saddr` may be advanced by multiples of 16 bytes
