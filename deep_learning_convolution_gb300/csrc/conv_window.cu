@@ -69,7 +69,13 @@ constexpr int WIN_EPI_SMEM = 4 * WIN_EPI_BUF;        // 4 epilogue warps, one bu
                                                      // two fit: a store overlaps the next staging)
 constexpr int WIN_MAX_ROWS = 224;                  // input rows per tile (ring table)
 constexpr int WIN_MAX_MMAS = 256;                  // MMAs per tile (descriptor table)
-constexpr int WIN_BAR_AREA = 192 + 4 * WIN_MAX_ROWS + 8 * WIN_MAX_MMAS;  // barriers, tables
+constexpr int WIN_BARS = 192;                      // barriers, TMEM slot, abort flag
+// barriers, then the ring table (one word per tile row) and two descriptor
+// tables (one word per MMA): sized per problem, as the largest layers need
+// every byte of shared memory
+__host__ __device__ constexpr int win_bar_area(int rows, int mmas) {
+    return (WIN_BARS + 4 * rows + 8 * mmas + 15) / 16 * 16;
+}
 
 struct WinParams {
     int N, C, H, W, K, R, S, P, Q;
@@ -521,7 +527,7 @@ __device__ void win_produce(const WinParams &p, uint32_t rank, uint32_t sB, uint
         if (warp == 0) {
             // the unit's MMA operands for the MMA warp: MMA (r, st) reads the J
             // slots from tile row r*dh's slot on, 32*st bytes into each window
-            uint32_t *tab = atab + buf * WIN_MAX_MMAS;
+            uint32_t *tab = atab + buf * p.R * p.steps;
             for (int r = lane; r < p.R; r += 32) {
                 int pos;
                 const int slot = ring_slot(p, rtab[r * p.dh], walk.base, pos);
@@ -592,7 +598,7 @@ __device__ void win_mma(const WinParams &p, uint32_t tmem_base, uint32_t sB, con
         tc_fence_after_sync();
         if (lane == 0) {
             const uint32_t d = tmem_base + (uint32_t)abuf * p.acc_stride;
-            const uint32_t *tab = atab + buf * WIN_MAX_MMAS;  // written by the producers
+            const uint32_t *tab = atab + buf * nm;  // written by the producers
             uint64_t bd = b0;
 #pragma unroll 4
             for (int m = 0; m < nm; ++m) {  // 32 bytes of window per MMA
@@ -823,7 +829,7 @@ __global__ void __launch_bounds__(WIN_THREADS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 17);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     uint32_t *rtab = reinterpret_cast<uint32_t *>(bars + 24);  // ring table, one entry per tile row
-    uint32_t *atab = rtab + WIN_MAX_ROWS;  // two tables of a unit's A descriptors, one entry per MMA
+    uint32_t *atab = rtab + p.rows;  // two tables of a unit's A descriptors, one entry per MMA
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
@@ -967,7 +973,7 @@ bool window_plan(const ConvProblem &pb, WinParams *wp, size_t *smem_out) {
     // last slot: the pixels the operand of a J > 1 tile reads past it.
     const long long tail = ((long long)p.px_read * D + 1023) & ~1023LL;
     auto ring_of = [&](int rs) { return (long long)pb.u * (rs + p.J - 1) * p.slot_bytes + tail; };
-    const long long fixed = 1024 + b_bytes + WIN_BAR_AREA;
+    const long long fixed = 1024 + b_bytes + win_bar_area(p.rows, pb.R * p.steps);
     p.RS = 2 * p.kspan;
     p.disc_wait = 0;
     if (fixed + ring_of(p.RS) > WIN_MAX_SMEM) {

@@ -368,7 +368,7 @@ def test_workspace_is_zero_and_kernel_choice(handle):
     expect = {"alexnet": ["tc_window"] + ["tc_im2col_pair"] * 4,
               "overfeat": ["tc_window"] + ["tc_im2col_pair"] * 4,
               "resnet50": ["tc_im2col_pair"] * len(synth.WORKLOADS["resnet50"]),
-              "speech": ["tc_runs", "tc_runs"], "tiny": ["ffma"]}
+              "speech": ["tc_window", "tc_runs"], "tiny": ["ffma"]}
     for wl, kinds in expect.items():
         for layer, kind in zip(synth.WORKLOADS[wl], kinds):
             x, w, _ = synth.make_inputs(layer, 1, batch=1)

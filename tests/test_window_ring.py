@@ -55,7 +55,7 @@ def plan(layer, esz, pair):
     BN = -(-K // 16) * 16
     b_img = R * steps * (BN // 2 if pair else BN) * 32
     tail = -(-(px_read * D) // 1024) * 1024
-    fixed = 1024 + -(-b_img // 1024) * 1024 + 192 + 4 * 224 + 8 * 256
+    fixed = 1024 + -(-b_img // 1024) * 1024 + -(-(192 + 4 * rows + 8 * R * steps) // 16) * 16
 
     def ring_of(rs):
         return u * (rs + J - 1) * slot_bytes + tail
@@ -137,7 +137,8 @@ def walk_cta(p, pair, ub, ue, rank, new_run_step=None):
 
 @pytest.mark.parametrize("pair", [False, True], ids=["single", "pairs"])
 @pytest.mark.parametrize("layer", WINDOW_CASES + [synth.WORKLOADS["alexnet"][0],
-                                                  synth.WORKLOADS["overfeat"][0]],
+                                                  synth.WORKLOADS["overfeat"][0],
+                                                  synth.WORKLOADS["speech"][0]],
                          ids=lambda l: l.name)
 def test_ring_rows_reach_their_mmas(layer, pair):
     esz = 4 if layer.dtype == "tf32" else 2
