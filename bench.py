@@ -37,6 +37,18 @@ def env_rank():
         int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def aggregate_over_ranks(total_ms, step_flops, steps, world, device="cpu"):
+    """The slowest rank's timed total (one MAX all-reduce across the ranks of
+    the default process group) and the whole-job throughput in TFLOP/s: every
+    rank runs the full workload (replicas), so the job does world x the FLOPs."""
+    if world > 1:
+        import torch
+        t = torch.tensor([total_ms], device=device, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return total_ms, step_flops * world * steps / (total_ms * 1e-3) / 1e12
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -232,12 +244,8 @@ def run_ours(args, rank, world, local_rank):
         total_ms += ev[i][0].elapsed_time(ev[i][-1])
         for j in range(len(probs)):
             per_layer_ms[j] += ev[i][j].elapsed_time(ev[i][j + 1])
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms, value = aggregate_over_ranks(total_ms, step_flops, K, world, dev)
     ms_per_step = total_ms / K
-    value = step_flops * world * K / (total_ms * 1e-3) / 1e12
 
     peaks = load_peaks()
     peak_tf = peaks["bf16_tflops"] if args.workload != "speech" else peaks["bf16_tflops"] / 2
@@ -390,8 +398,7 @@ def run_e2e(args, probs, handle, stream, dev, step_flops, world):
     join()
     end.record(stream)
     torch.cuda.synchronize()
-    ms = start.elapsed_time(end)
-    value = step_flops * world * steps / (ms * 1e-3) / 1e12
+    ms, value = aggregate_over_ranks(start.elapsed_time(end), step_flops, steps, world, dev)
     return {"value": round(value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(ms / steps, 3)}
 

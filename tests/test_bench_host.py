@@ -1,0 +1,93 @@
+"""bench.py's host logic on the CPU: the max-over-ranks aggregation with two
+gloo ranks, and the reference arm's JSON line (rank 0 prints it, other ranks
+exit without work)."""
+import importlib.util
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _bench():
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_worker(rank, world, port, totals, q):
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms, value = _bench().aggregate_over_ranks(totals[rank], 2.0e12, 4, world, "cpu")
+        q.put((rank, ms, value))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_slowest_rank_sets_the_job_time():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    totals = [10.0, 12.5]
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_worker, args=(r, 2, port, totals, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+    for p in procs:
+        if p.is_alive():
+            p.kill()
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=5) for _ in range(2))
+    for rank, ms, value in got:
+        assert ms == 12.5, f"rank {rank} kept its own time"
+        # every rank runs the whole workload: 2 ranks x 4 steps x 2 TFLOP in 12.5 ms
+        assert value == pytest.approx(2 * 4 * 2.0 / 12.5e-3)
+
+
+def test_one_rank_keeps_its_own_time():
+    ms, value = _bench().aggregate_over_ranks(8.0, 1.0e12, 2, 1)
+    assert ms == 8.0 and value == pytest.approx(2 * 1.0 / 8.0e-3)
+
+
+def _run_reference(rank, world):
+    env = dict(os.environ, RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    return subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1",
+                           "--warmup", "3"], cwd=ROOT, env=env, capture_output=True, text=True,
+                          timeout=600)
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    r = _run_reference(1, 2)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
+
+
+def test_reference_arm_prints_the_contract_line():
+    r = _run_reference(0, 1)
+    assert r.returncode == 0, r.stderr
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    bench = _bench()
+    assert d["impl"] == "reference"
+    assert d["metric"] == bench.METRIC and d["unit"] == "TFLOP/s" and d["higher_is_better"]
+    assert d["config"] == bench.workload_config("alexnet", 1)
+    assert d["value"] > 0 and d["steps"] == 1 and d["warmup"] == 3
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
