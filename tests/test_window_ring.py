@@ -162,3 +162,35 @@ def test_ring_model_catches_a_wrong_base_step():
         for c in range(3):
             ub, ue = p["units"] * c // 3, p["units"] * (c + 1) // 3
             walk_cta(p, False, ub, ue, 0, new_run_step=p["J"])
+
+
+def test_ring_random_layers():
+    """Random few-channel layers (strides, dilation, pads, widths, batch): the
+    plan, when it accepts the layer, keeps every operand on the right rows."""
+    import numpy as np
+    rng = np.random.default_rng(20260602)
+    checked = 0
+    for _ in range(300):
+        u, v = int(rng.integers(1, 5)), int(rng.integers(1, 5))
+        R, S = int(rng.integers(1, 12)), int(rng.integers(1, 12))
+        dh = int(rng.integers(1, 3))
+        C = int(rng.integers(1, 9))
+        pads = [int(rng.integers(0, 4)) for _ in range(4)]
+        H = int(rng.integers(dh * (R - 1) + 1, 80))
+        W = int(rng.integers(S, 300))
+        n = int(rng.integers(1, 6))
+        K = int(rng.choice([16, 32, 64, 96, 128]))
+        layer = synth.Layer("rand", n, C, H, W, K, R, S, pad_top=pads[0], pad_bottom=pads[1],
+                            pad_left=pads[2], pad_right=pads[3], u=u, v=v, dil_h=dh)
+        for pair in (False, True):
+            p = plan(layer, 2, pair)
+            if p is None or p["P"] < 1:
+                continue
+            checked += 1
+            for grid in (152, 5):
+                G = min(grid, p["units"])
+                for c in range(G):
+                    ub, ue = p["units"] * c // G, p["units"] * (c + 1) // G
+                    for rank in ((0, 1) if pair else (0,)):
+                        walk_cta(p, pair, ub, ue, rank)
+    assert checked > 100
