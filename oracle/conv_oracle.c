@@ -248,3 +248,210 @@ int oracle_conv2d_fprop_points(const double *x, const i64 *xs, const double *w, 
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------
+ * Backward passes (the next rows of the path; no kernel yet).
+ *
+ * "cuDNN: Efficient Primitives for Deep Learning", method section: the
+ * library offers, beside the forward convolution, routines for the gradients
+ * with respect to the data and to the filters.  Both are the plain
+ * derivatives of the forward sum above (alpha = 1, no epilogue):
+ *
+ *   dx[n,c,h,w]  = sum over k, r, s and over the outputs (p, q) that read
+ *                  input pixel (h, w) through tap (r, s), i.e.
+ *                  p*u + r*dh - pad_top = h and q*v + s*dw - pad_left = w,
+ *                  0 <= p < P, 0 <= q < Q, of dy[n,k,p,q] * w[k,c,r,s];
+ *   dw[k,c,r,s]  = sum_{n, p<P, q<Q} dy[n,k,p,q]
+ *                      * X(n, c, p*u + r*dh - pad_top, q*v + s*dw - pad_left),
+ *                  with X = 0 outside the image.
+ *
+ * Each returns alongside the sum of |products| (the same tolerance scale as
+ * the forward bound).  FP64, loop orders (n,c,h,w,k,r,s) and (k,c,r,s,n,p,q),
+ * pthreads over (n,c) and (k,c) pairs.
+ * ------------------------------------------------------------------------ */
+
+typedef struct {
+    const double *dy;  i64 dys[4];   /* n, k, p, q */
+    const double *w;   i64 ws[4];    /* k, c, r, s */
+    const double *x;   i64 xs[4];    /* n, c, h, w (wgrad input) */
+    double *out;       i64 os[4];    /* dx: n, c, h, w  -- dw: k, c, r, s */
+    double *bound;                   /* same strides as out; may be NULL */
+    int N, C, H, W, K, R, S;
+    int pt, pl, u, v, dh, dw;
+    i64 P, Q;
+    int wgrad;
+} grad_problem;
+
+typedef struct {
+    const grad_problem *gp;
+    i64 first, last;
+} grad_slice;
+
+/* dx at (n, c, h, w) */
+static void dgrad_one(const grad_problem *g, i64 n, i64 c, i64 h, i64 wi, double *val, double *bnd)
+{
+    double acc = 0.0, b = 0.0;
+    for (i64 k = 0; k < g->K; ++k) {
+        for (i64 r = 0; r < g->R; ++r) {
+            i64 tp = h + g->pt - r * g->dh;          /* = p*u for a reading output */
+            if (tp < 0 || tp % g->u != 0)
+                continue;
+            i64 p = tp / g->u;
+            if (p >= g->P)
+                continue;
+            for (i64 s = 0; s < g->S; ++s) {
+                i64 tq = wi + g->pl - s * g->dw;     /* = q*v for a reading output */
+                if (tq < 0 || tq % g->v != 0)
+                    continue;
+                i64 q = tq / g->v;
+                if (q >= g->Q)
+                    continue;
+                double dv = g->dy[n * g->dys[0] + k * g->dys[1] + p * g->dys[2] + q * g->dys[3]];
+                double wv = g->w[k * g->ws[0] + c * g->ws[1] + r * g->ws[2] + s * g->ws[3]];
+                acc += dv * wv;
+                b += fabs(dv * wv);
+            }
+        }
+    }
+    *val = acc;
+    *bnd = b;
+}
+
+/* dw at (k, c, r, s) */
+static void wgrad_one(const grad_problem *g, i64 k, i64 c, i64 r, i64 s, double *val, double *bnd)
+{
+    double acc = 0.0, b = 0.0;
+    for (i64 n = 0; n < g->N; ++n) {
+        for (i64 p = 0; p < g->P; ++p) {
+            i64 h = p * g->u + r * g->dh - g->pt;
+            if (h < 0 || h >= g->H)
+                continue;                            /* zero padding row */
+            for (i64 q = 0; q < g->Q; ++q) {
+                i64 wi = q * g->v + s * g->dw - g->pl;
+                if (wi < 0 || wi >= g->W)
+                    continue;                        /* zero padding column */
+                double dv = g->dy[n * g->dys[0] + k * g->dys[1] + p * g->dys[2] + q * g->dys[3]];
+                double xv = g->x[n * g->xs[0] + c * g->xs[1] + h * g->xs[2] + wi * g->xs[3]];
+                acc += dv * xv;
+                b += fabs(dv * xv);
+            }
+        }
+    }
+    *val = acc;
+    *bnd = b;
+}
+
+static void *grad_worker(void *arg)
+{
+    const grad_slice *sl = (const grad_slice *)arg;
+    const grad_problem *g = sl->gp;
+    for (i64 pair = sl->first; pair < sl->last; ++pair) {
+        i64 a = pair / g->C, c = pair % g->C;      /* a = n (dgrad) or k (wgrad) */
+        i64 e2 = g->wgrad ? g->R : g->H, e3 = g->wgrad ? g->S : g->W;
+        for (i64 i2 = 0; i2 < e2; ++i2) {
+            for (i64 i3 = 0; i3 < e3; ++i3) {
+                double val, bnd;
+                if (g->wgrad)
+                    wgrad_one(g, a, c, i2, i3, &val, &bnd);
+                else
+                    dgrad_one(g, a, c, i2, i3, &val, &bnd);
+                i64 off = a * g->os[0] + c * g->os[1] + i2 * g->os[2] + i3 * g->os[3];
+                g->out[off] = val;
+                if (g->bound)
+                    g->bound[off] = bnd;
+            }
+        }
+    }
+    return NULL;
+}
+
+static int grad_run(grad_problem *g, int nthreads)
+{
+    i64 pairs = (i64)(g->wgrad ? g->K : g->N) * g->C;
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > 256)
+        nthreads = 256;
+    if ((i64)nthreads > pairs)
+        nthreads = (int)(pairs > 0 ? pairs : 1);
+    pthread_t tid[256];
+    grad_slice sl[256];
+    int started[256];
+    for (int t = 0; t < nthreads; ++t) {
+        sl[t].gp = g;
+        sl[t].first = pairs * t / nthreads;
+        sl[t].last = pairs * (t + 1) / nthreads;
+        started[t] = 0;
+    }
+    for (int t = 1; t < nthreads; ++t)
+        started[t] = pthread_create(&tid[t], NULL, grad_worker, &sl[t]) == 0;
+    grad_worker(&sl[0]);
+    for (int t = 1; t < nthreads; ++t) {
+        if (started[t])
+            pthread_join(tid[t], NULL);
+        else
+            grad_worker(&sl[t]);
+    }
+    return 0;
+}
+
+static int grad_fill(grad_problem *g, int N, int C, int H, int W, int K, int R, int S,
+                     int pad_top, int pad_bottom, int pad_left, int pad_right,
+                     int u, int v, int dil_h, int dil_w)
+{
+    if (N <= 0 || C <= 0 || H <= 0 || W <= 0 || K <= 0 || R <= 0 || S <= 0)
+        return 1;
+    g->N = N; g->C = C; g->H = H; g->W = W; g->K = K; g->R = R; g->S = S;
+    g->pt = pad_top; g->pl = pad_left; g->u = u; g->v = v; g->dh = dil_h; g->dw = dil_w;
+    g->P = oracle_out_extent(H, pad_top, pad_bottom, R, dil_h, u);
+    g->Q = oracle_out_extent(W, pad_left, pad_right, S, dil_w, v);
+    if (g->P < 0 || g->Q < 0)
+        return 1;
+    if (g->P == 0 || g->Q == 0)
+        return 2;
+    return 0;
+}
+
+/* dx (strides dxs = {n,c,h,w}) from dy (dys = {n,k,p,q}) and w (ws = {k,c,r,s}).
+ * Returns 0, 1 on a bad argument, 2 when the forward output is empty. */
+int oracle_conv2d_dgrad(const double *dy, const i64 *dys, const double *w, const i64 *ws,
+                        double *dx, const i64 *dxs, double *bound,
+                        int N, int C, int H, int W, int K, int R, int S,
+                        int pad_top, int pad_bottom, int pad_left, int pad_right,
+                        int u, int v, int dil_h, int dil_w, int nthreads)
+{
+    if (!dy || !dys || !w || !ws || !dx || !dxs)
+        return 1;
+    grad_problem g;
+    int rc = grad_fill(&g, N, C, H, W, K, R, S, pad_top, pad_bottom, pad_left, pad_right,
+                       u, v, dil_h, dil_w);
+    if (rc)
+        return rc;
+    g.dy = dy; g.w = w; g.x = NULL; g.out = dx; g.bound = bound; g.wgrad = 0;
+    for (int i = 0; i < 4; ++i) {
+        g.dys[i] = dys[i]; g.ws[i] = ws[i]; g.xs[i] = 0; g.os[i] = dxs[i];
+    }
+    return grad_run(&g, nthreads);
+}
+
+/* dw (strides dws = {k,c,r,s}) from x (xs = {n,c,h,w}) and dy (dys = {n,k,p,q}).
+ * Returns 0, 1 on a bad argument, 2 when the forward output is empty. */
+int oracle_conv2d_wgrad(const double *x, const i64 *xs, const double *dy, const i64 *dys,
+                        double *dw, const i64 *dws, double *bound,
+                        int N, int C, int H, int W, int K, int R, int S,
+                        int pad_top, int pad_bottom, int pad_left, int pad_right,
+                        int u, int v, int dil_h, int dil_w, int nthreads)
+{
+    if (!x || !xs || !dy || !dys || !dw || !dws)
+        return 1;
+    grad_problem g;
+    int rc = grad_fill(&g, N, C, H, W, K, R, S, pad_top, pad_bottom, pad_left, pad_right,
+                       u, v, dil_h, dil_w);
+    if (rc)
+        return rc;
+    g.dy = dy; g.w = NULL; g.x = x; g.out = dw; g.bound = bound; g.wgrad = 1;
+    for (int i = 0; i < 4; ++i) {
+        g.dys[i] = dys[i]; g.ws[i] = 0; g.xs[i] = xs[i]; g.os[i] = dws[i];
+    }
+    return grad_run(&g, nthreads);
+}

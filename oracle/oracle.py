@@ -7,7 +7,8 @@ It shares no code with the CUDA library.
 ``build()`` compiles ``conv_oracle.c`` with gcc into ``oracle/_build`` (no
 OpenMP runtime: plain pthreads).  ``conv2d_fprop`` takes numpy arrays in any
 layout (strides are read from the arrays) and returns FP64 y and
-bound = sum |x*w|.
+bound = sum |x*w|.  ``conv2d_dgrad`` and ``conv2d_wgrad`` are the gradients of
+that sum with respect to x and w (the backward routines, no kernel yet).
 """
 from __future__ import annotations
 
@@ -62,6 +63,11 @@ def load(path: Optional[str] = None):
                                                + [ctypes.c_double, ctypes.c_double, _dp, _dp,
                                                   ctypes.c_int, _i64p, ctypes.c_longlong,
                                                   _dp, _dp])
+    grad = [_dp, _i64p, _dp, _i64p, _dp, _i64p, _dp] + [ctypes.c_int] * 16
+    lib.oracle_conv2d_dgrad.restype = ctypes.c_int
+    lib.oracle_conv2d_dgrad.argtypes = grad
+    lib.oracle_conv2d_wgrad.restype = ctypes.c_int
+    lib.oracle_conv2d_wgrad.argtypes = grad
     if path is None:
         _lib = lib
     return lib
@@ -183,6 +189,67 @@ def conv2d_fprop_points(x: np.ndarray, w: np.ndarray, pts: np.ndarray, *, pads=(
     if rc != 0:
         raise ValueError(f"oracle_conv2d_fprop_points returned {rc}")
     return out, bnd
+
+
+def conv2d_dgrad(dy: np.ndarray, w: np.ndarray, in_hw: Tuple[int, int], *, pads=(0, 0, 0, 0),
+                 stride=(1, 1), dilation=(1, 1), nthreads: Optional[int] = None,
+                 lib=None) -> Tuple[np.ndarray, np.ndarray]:
+    """Gradient of the forward convolution with respect to x, for an input of
+    spatial size ``in_hw`` = (H, W): dy is NCHW-shaped [N, K, P, Q] FP64, w
+    KCRS FP64 (any strides).  Returns (dx, bound) as [N, C, H, W] FP64 arrays,
+    bound = sum |dy*w| over the products that make each dx."""
+    lib = lib or load()
+    dy = _as_f64_view(dy, "dy")
+    w = _as_f64_view(w, "w")
+    N, K, P, Q = dy.shape
+    K2, C, R, S = w.shape
+    if K2 != K:
+        raise ValueError("filter count mismatch between dy and w")
+    H, W = in_hw
+    pt, pb, pl, pr = pads
+    if (out_extent(H, pt, pb, R, dilation[0], stride[0], lib),
+            out_extent(W, pl, pr, S, dilation[1], stride[1], lib)) != (P, Q):
+        raise ValueError("dy does not have the forward output's extent")
+    dx = np.zeros((N, C, H, W), dtype=np.float64)
+    bound = np.zeros_like(dx)
+    rc = lib.oracle_conv2d_dgrad(
+        _ptr(dy), _strides(dy).ctypes.data_as(_i64p), _ptr(w), _strides(w).ctypes.data_as(_i64p),
+        _ptr(dx), _strides(dx).ctypes.data_as(_i64p), _ptr(bound),
+        N, C, H, W, K, R, S, pt, pb, pl, pr, stride[0], stride[1], dilation[0], dilation[1],
+        int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError(f"oracle_conv2d_dgrad returned {rc}")
+    return dx, bound
+
+
+def conv2d_wgrad(x: np.ndarray, dy: np.ndarray, filt_rs: Tuple[int, int], *, pads=(0, 0, 0, 0),
+                 stride=(1, 1), dilation=(1, 1), nthreads: Optional[int] = None,
+                 lib=None) -> Tuple[np.ndarray, np.ndarray]:
+    """Gradient of the forward convolution with respect to w, for filters of
+    size ``filt_rs`` = (R, S): x NCHW-shaped [N, C, H, W] FP64, dy [N, K, P, Q]
+    FP64 (any strides).  Returns (dw, bound) as [K, C, R, S] FP64 arrays."""
+    lib = lib or load()
+    x = _as_f64_view(x, "x")
+    dy = _as_f64_view(dy, "dy")
+    N, C, H, W = x.shape
+    N2, K, P, Q = dy.shape
+    if N2 != N:
+        raise ValueError("batch mismatch between x and dy")
+    R, S = filt_rs
+    pt, pb, pl, pr = pads
+    if (out_extent(H, pt, pb, R, dilation[0], stride[0], lib),
+            out_extent(W, pl, pr, S, dilation[1], stride[1], lib)) != (P, Q):
+        raise ValueError("dy does not have the forward output's extent")
+    dw = np.zeros((K, C, R, S), dtype=np.float64)
+    bound = np.zeros_like(dw)
+    rc = lib.oracle_conv2d_wgrad(
+        _ptr(x), _strides(x).ctypes.data_as(_i64p), _ptr(dy), _strides(dy).ctypes.data_as(_i64p),
+        _ptr(dw), _strides(dw).ctypes.data_as(_i64p), _ptr(bound),
+        N, C, H, W, K, R, S, pt, pb, pl, pr, stride[0], stride[1], dilation[0], dilation[1],
+        int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError(f"oracle_conv2d_wgrad returned {rc}")
+    return dw, bound
 
 
 if __name__ == "__main__":  # pragma: no cover

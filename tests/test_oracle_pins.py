@@ -316,7 +316,8 @@ def test_planted_mistake_is_caught(name):
     old, new = MUTANTS[name]
     src = open(oracle.SRC).read()
     assert old in src, f"mutation anchor missing for {name}"
-    tmp = tempfile.mkdtemp(prefix="oracle_mutant_")
+    os.makedirs(oracle.BUILD_DIR, exist_ok=True)
+    tmp = tempfile.mkdtemp(prefix="mutant_", dir=oracle.BUILD_DIR)  # inside the repo's build dir
     try:
         msrc = os.path.join(tmp, "conv_oracle_mutant.c")
         with open(msrc, "w") as f:
