@@ -180,7 +180,7 @@ def test_tc_window_parity_full(handle, layer):
                   expect_kernel="tc_window")
 
 
-@pytest.mark.parametrize("layer", [WINDOW_CASES[i] for i in (4, 5, 6, 10, 14)], ids=lambda l: l.name)
+@pytest.mark.parametrize("layer", [WINDOW_CASES[i] for i in (4, 5, 6, 10, 14, 18)], ids=lambda l: l.name)
 def test_tc_window_word_copies(handle, layer, monkeypatch):
     """Rows that could be bulk-staged, copied word by word instead."""
     monkeypatch.setenv("DLC_TC_WINSTAGE", "0")
@@ -188,7 +188,7 @@ def test_tc_window_word_copies(handle, layer, monkeypatch):
                   expect_kernel="tc_window")
 
 
-@pytest.mark.parametrize("layer", [WINDOW_CASES[i] for i in (0, 2, 5, 7, 12, 13, 15, 16, 17)],
+@pytest.mark.parametrize("layer", [WINDOW_CASES[i] for i in (0, 2, 5, 7, 12, 13, 15, 16, 17, 18)],
                          ids=lambda l: l.name)
 def test_tc_window_cta_pairs(handle, layer, monkeypatch):
     """CTA pairs sharing each MMA over 256 rows (opt-in)."""

@@ -48,4 +48,8 @@ WINDOW_CASES = [
     # slots) runs, where a tile that starts a new image waits for the MMAs of
     # the tile before it
     L("win_bf16_c24_k64_9x3_wide_short_ring", 19, 24, 12, 150, 64, 9, 3, **P(4, 4, 1, 1)),
+    # wide rows (one output row per tile) whose input rows are staged by bulk
+    # copies: 224 pixels x 3 channels = 1344-byte rows, 7x7 stride 2 (D = 16),
+    # left pad 2 so phase pixels start on 4-byte boundaries
+    L("win_bf16_c3_k64_7x7_s2_wide_staged", 2, 3, 20, 224, 64, 7, 7, **P(3, 3, 2, 4), u=2, v=2),
 ]
