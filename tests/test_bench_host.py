@@ -91,3 +91,22 @@ def test_reference_arm_prints_the_contract_line():
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
     assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+def test_bench_geometry_matches_the_oracle_extent():
+    """The benchmark's per-layer output size and FLOP count (which set the
+    reported TFLOP/s) agree with the pinned oracle's extent and with the
+    direct-convolution count 2*N*K*P*Q*C*R*S, for every workload layer."""
+    from oracle import oracle
+    from deep_learning_convolution_gb300 import synth
+    bench = _bench()
+    for wl, layers in synth.WORKLOADS.items():
+        for l in layers:
+            P, Q = bench.layer_output_dims(l)
+            assert P == oracle.out_extent(l.H, l.pad_top, l.pad_bottom, l.R, l.dil_h, l.u)
+            assert Q == oracle.out_extent(l.W, l.pad_left, l.pad_right, l.S, l.dil_w, l.v)
+            flops, _ = bench.layer_geometry(l, P, Q)
+            assert flops == 2 * l.N * l.K * P * Q * l.C * l.R * l.S
+        cfg = bench.workload_config(wl, 1)
+        assert cfg["flops_per_step"] == sum(
+            bench.layer_geometry(l, *bench.layer_output_dims(l))[0] for l in layers)
