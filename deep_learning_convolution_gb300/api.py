@@ -51,6 +51,9 @@ class Handle:
     def synchronize(self):
         B.dlcSynchronize(self.h)
 
+    def set_deterministic(self, on: bool = True):
+        B.dlcSetDeterministic(self.h, 1 if on else 0)
+
     def launches(self) -> int:
         return B.dlcGetLaunchCount(self.h)
 

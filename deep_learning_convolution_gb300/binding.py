@@ -67,6 +67,8 @@ SIGNATURES = {
     "dlcSynchronize": [_h],
     "dlcGetLastDeviceError": [_h, _pi, _pi],
     "dlcGetLaunchCount": [_h, POINTER(c_uint64)],
+    "dlcSetDeterministic": [_h, c_int],
+    "dlcGetDeterministic": [_h, _pi],
     "dlcCreateTensorDescriptor": [_ph],
     "dlcDestroyTensorDescriptor": [_h],
     "dlcSetTensor4dDescriptor": [_h, c_int, c_int, c_int, c_int, c_int, c_int],
@@ -192,6 +194,16 @@ def dlcGetLaunchCount(handle) -> int:
     n = c_uint64()
     _call("dlcGetLaunchCount", handle, byref(n))
     return n.value
+
+
+def dlcSetDeterministic(handle, deterministic: int):
+    _call("dlcSetDeterministic", handle, int(deterministic))
+
+
+def dlcGetDeterministic(handle) -> int:
+    v = c_int()
+    _call("dlcGetDeterministic", handle, byref(v))
+    return v.value
 
 
 def dlcCreateTensorDescriptor():

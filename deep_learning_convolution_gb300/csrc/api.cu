@@ -12,8 +12,9 @@
 #include "internal.h"
 
 // Scratch of dlcConvolutionForwardNoAlloc: DLC_NOALLOC_MAX_TILES split-tile
-// flags followed by two error words.  Device code never names it; host code
-// passes its device address, looked up once per device.
+// flags (used only by the opt-in stream-K schedule) followed by two error
+// words.  Device code never names it; host code passes its device address,
+// looked up once per device.
 static __device__ __align__(256) int dlc_noalloc_scratch[DLC_NOALLOC_MAX_TILES + 64];
 // Its repacked filter image for the window kernel.
 static __device__ __align__(256) unsigned char dlc_noalloc_wpack[DLC_WPACK_BYTES];
@@ -271,6 +272,20 @@ dlcStatus_t dlcGetStream(dlcHandle_t h, void **stream) {
     return DLC_STATUS_SUCCESS;
 }
 
+dlcStatus_t dlcSetDeterministic(dlcHandle_t h, int deterministic) {
+    if (!h) return DLC_STATUS_NOT_INITIALIZED;
+    if (deterministic != 0 && deterministic != 1) return DLC_STATUS_BAD_PARAM;
+    h->deterministic = deterministic;
+    return DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlcGetDeterministic(dlcHandle_t h, int *deterministic) {
+    if (!h) return DLC_STATUS_NOT_INITIALIZED;
+    if (!deterministic) return DLC_STATUS_BAD_PARAM;
+    *deterministic = h->deterministic;
+    return DLC_STATUS_SUCCESS;
+}
+
 dlcStatus_t dlcGetLastDeviceError(dlcHandle_t h, int *code, int *detail) {
     if (!h) return DLC_STATUS_NOT_INITIALIZED;
     if (!code || !detail) return DLC_STATUS_BAD_PARAM;
@@ -511,8 +526,9 @@ dlcStatus_t dlcConvolutionBiasActivationForward(dlcHandle_t h, const float *alph
 }
 
 // Per-device set-up of the allocation-free entry point: the scratch array's
-// device address (cudaGetSymbolAddress with the device current), the SM count
-// and the tensor-map encoders.  Done by the first call on each device.
+// device address (cudaGetSymbolAddress with the device current), every kernel
+// of the library loaded into the context, the SM count and the tensor-map
+// encoders.  Done by the first call on each device.
 namespace {
 struct NoAllocDevice {
     int ready = 0;
@@ -541,6 +557,11 @@ dlcStatus_t noalloc_setup(int dev, NoAllocDevice **out) {
         void *wptr = nullptr;
         if (cudaGetSymbolAddress((void **)&ptr, dlc_noalloc_scratch) != cudaSuccess || !ptr ||
             cudaGetSymbolAddress(&wptr, dlc_noalloc_wpack) != cudaSuccess || !wptr)
+            return DLC_STATUS_EXECUTION_FAILED;
+        // Load every kernel a later call may launch now: modules are loaded
+        // lazily, and a module load allocates device memory.
+        if (dlc_preload_tc() != DLC_STATUS_SUCCESS || dlc_preload_window() != DLC_STATUS_SUCCESS ||
+            dlc_preload_pair() != DLC_STATUS_SUCCESS)
             return DLC_STATUS_EXECUTION_FAILED;
         cudaDriverEntryPointQueryResult q1, q2;
         void *f1 = nullptr, *f2 = nullptr;
@@ -591,7 +612,6 @@ dlcStatus_t dlcConvolutionForwardNoAlloc(void *stream, const float *alpha,
     ctx.d_err = status ? status : nd->scratch + DLC_NOALLOC_MAX_TILES;
     ctx.sk_flags = nd->scratch;
     ctx.wpack = nd->wpack;
-    ctx.force_sk = 1;
     ctx.encode_tiled = nd->encode_tiled;
     ctx.encode_im2col = nd->encode_im2col;
     const dlcKernel_t k = dlc_tc_variant(&ctx, pb);

@@ -427,8 +427,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-// The pair kernel serves every im2col-eligible problem unless DLC_TC_PAIR=0
-// or the context asks for the stream-K schedule (the single-SM kernel's).
+// The pair kernel serves every im2col-eligible problem unless DLC_TC_PAIR=0.
 bool dlc_pdl_enabled() {
     static const bool on = [] {
         const char *ev = std::getenv("DLC_PDL");
@@ -437,10 +436,17 @@ bool dlc_pdl_enabled() {
     return on;
 }
 
-bool dlc_pair_enabled(const dlcContext *ctx) {
-    if (ctx && ctx->force_sk) return false;
+bool dlc_pair_enabled(const dlcContext *) {
     const char *ev = std::getenv("DLC_TC_PAIR");
     return !(ev && std::atoi(ev) == 0);
+}
+
+dlcStatus_t dlc_preload_pair() {
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, conv_pair_kernel<false>) != cudaSuccess ||
+        cudaFuncGetAttributes(&a, conv_pair_kernel<true>) != cudaSuccess)
+        return DLC_STATUS_EXECUTION_FAILED;
+    return DLC_STATUS_SUCCESS;
 }
 
 dlcStatus_t dlc_launch_pair(dlcContext *ctx, const ConvProblem &pb) {
@@ -585,7 +591,11 @@ dlcStatus_t dlc_launch_pair(dlcContext *ctx, const ConvProblem &pb) {
     p.num_units = p.num_tiles;
     {
         const char *ev = std::getenv("DLC_TC_PAIR_SPLIT");
-        const bool plain = p.y_tma && pb.beta == 0.f && pb.bias == nullptr && !pb.relu;
+        // The tail's partial sums meet in FP32 atomic adds in whatever order
+        // they arrive, so its outputs may differ in the last bits from run to
+        // run; a deterministic handle keeps whole tiles.
+        const bool plain = p.y_tma && pb.beta == 0.f && pb.bias == nullptr && !pb.relu &&
+                           !ctx->deterministic;
         const int C = max_clusters;
         const int rem = p.num_tiles % C;
         const int splits = rem > 0 ? std::min(std::min(C / rem, p.num_kb), 16) : 1;

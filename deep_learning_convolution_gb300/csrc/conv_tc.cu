@@ -1323,8 +1323,6 @@ dlcStatus_t dlc_launch_tc(dlcContext *ctx, const ConvProblem &pb, dlcKernel_t va
     const long long m_tiles =
         tp.img_tiles > 0 ? (long long)pb.N * tp.img_tiles : (tp.M + BM - 1) / BM;
     tp.num_tiles = m_tiles * tp.n_tiles;
-    // a context whose split-tile flags are a fixed array takes no more tiles
-    if (ctx->force_sk && tp.num_tiles > DLC_SK_FLAGS) return DLC_STATUS_NOT_SUPPORTED;
 
     // shared memory: A stages plus either B stages or the resident filter
     // tile, plus the epilogue's staging buffers when y is stored by TMA
@@ -1370,8 +1368,8 @@ dlcStatus_t dlc_launch_tc(dlcContext *ctx, const ConvProblem &pb, dlcKernel_t va
     if (sk_legal) {
         // Measured no faster than whole tiles on the small-image layers (the
         // parked partial costs an extra pass over the split tiles), so the
-        // stream-K schedule is opt-in: DLC_TC_STREAMK=1, or a caller's context.
-        tp.sk = ctx->force_sk ? 1 : 0;
+        // stream-K schedule is opt-in: DLC_TC_STREAMK=1.  Problems with more
+        // tiles than there are flags run whole tiles.
         if (const char *ev = std::getenv("DLC_TC_STREAMK")) tp.sk = std::atoi(ev) != 0;
     }
     if (tp.sk) {
@@ -1445,6 +1443,18 @@ dlcStatus_t dlc_launch_tc(dlcContext *ctx, const ConvProblem &pb, dlcKernel_t va
                            : launch_mode<false>(mode, tp, ta, tb, ty, (int)grid, smem, ctx->stream);
     if (err != cudaSuccess) return DLC_STATUS_EXECUTION_FAILED;
     ctx->launches += 1;
+    return DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlc_preload_tc() {
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, conv_fprop_tc_kernel<false, MODE_IM2COL>) != cudaSuccess ||
+        cudaFuncGetAttributes(&a, conv_fprop_tc_kernel<false, MODE_RUNS>) != cudaSuccess ||
+        cudaFuncGetAttributes(&a, conv_fprop_tc_kernel<false, MODE_GATHER>) != cudaSuccess ||
+        cudaFuncGetAttributes(&a, conv_fprop_tc_kernel<true, MODE_IM2COL>) != cudaSuccess ||
+        cudaFuncGetAttributes(&a, conv_fprop_tc_kernel<true, MODE_RUNS>) != cudaSuccess ||
+        cudaFuncGetAttributes(&a, conv_fprop_tc_kernel<true, MODE_GATHER>) != cudaSuccess)
+        return DLC_STATUS_EXECUTION_FAILED;
     return DLC_STATUS_SUCCESS;
 }
 

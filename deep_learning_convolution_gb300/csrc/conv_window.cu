@@ -1048,6 +1048,18 @@ cudaError_t win_launch(const WinParams &p, const CUtensorMap &ty, int sm_count, 
 
 bool dlc_window_ok(const ConvProblem &pb) { return window_plan(pb, nullptr, nullptr); }
 
+dlcStatus_t dlc_preload_window() {
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, window_pack_filters<uint16_t>) != cudaSuccess ||
+        cudaFuncGetAttributes(&a, window_pack_filters<uint32_t>) != cudaSuccess ||
+        cudaFuncGetAttributes(&a, conv_window_kernel<false, false>) != cudaSuccess ||
+        cudaFuncGetAttributes(&a, conv_window_kernel<false, true>) != cudaSuccess ||
+        cudaFuncGetAttributes(&a, conv_window_kernel<true, false>) != cudaSuccess ||
+        cudaFuncGetAttributes(&a, conv_window_kernel<true, true>) != cudaSuccess)
+        return DLC_STATUS_EXECUTION_FAILED;
+    return DLC_STATUS_SUCCESS;
+}
+
 dlcStatus_t dlc_launch_window(dlcContext *ctx, const ConvProblem &pb) {
     WinParams p;
     size_t smem = 0;

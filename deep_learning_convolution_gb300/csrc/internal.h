@@ -48,7 +48,7 @@ struct dlcContext {
     unsigned long long timeout_ns = 2000000000ull;  // pipeline wait limit
     int *sk_flags = nullptr;  // DLC_SK_FLAGS per-tile flags of split tiles (zero between launches)
     void *wpack = nullptr;    // DLC_WPACK_BYTES: filters repacked for the window kernel
-    int force_sk = 0;         // use the stream-K schedule whenever it is legal
+    int deterministic = 0;    // no split reductions whose partial sums meet in atomic adds
     EncodeTiledFn encode_tiled = nullptr;
     EncodeIm2colFn encode_im2col = nullptr;
 };
@@ -93,4 +93,10 @@ bool dlc_pair_enabled(const dlcContext *ctx);
 // them (programmatic dependent launch) unless DLC_PDL=0.
 bool dlc_pdl_enabled();
 dlcStatus_t dlc_launch_pair(dlcContext *ctx, const ConvProblem &pb);
+// Each loads every kernel of its translation unit into the current context
+// (CUDA loads modules lazily by default, and a module load allocates device
+// memory): the allocation-free entry point calls them at its per-device set-up.
+dlcStatus_t dlc_preload_tc();
+dlcStatus_t dlc_preload_window();
+dlcStatus_t dlc_preload_pair();
 

@@ -151,6 +151,17 @@ dlcStatus_t dlcDestroy(dlcHandle_t handle);
 dlcStatus_t dlcSetStream(dlcHandle_t handle, void *stream);
 dlcStatus_t dlcGetStream(dlcHandle_t handle, void **stream);
 
+/* Bitwise reproducibility.  By default (0) the SM-pair kernel splits the
+ * output tiles of a launch's last, mostly idle wave along the reduction and
+ * adds the partial sums into y with FP32 atomic adds, whose order varies from
+ * run to run: those outputs can differ in their last bits between runs (each
+ * run stays within the same error bound).  With deterministic = 1 every
+ * kernel sums each output in a fixed order, so repeated calls give identical
+ * bits, at the cost of the idle tail (a few microseconds per launch).
+ * BAD_PARAM unless deterministic is 0 or 1. */
+dlcStatus_t dlcSetDeterministic(dlcHandle_t handle, int deterministic);
+dlcStatus_t dlcGetDeterministic(dlcHandle_t handle, int *deterministic);
+
 /* Synchronizes the handle's stream.  Returns EXECUTION_FAILED if a kernel
  * recorded a device error since the last call (the error is then cleared). */
 dlcStatus_t dlcSynchronize(dlcHandle_t handle);
@@ -250,7 +261,17 @@ dlcStatus_t dlcGetConvolutionForwardKernel(dlcHandle_t handle,
  * addresses.  beta == 0 means y is not read (NaN in y is overwritten).
  * y must not overlap x or w (BAD_PARAM).  x and w must share a storage type
  * that matches the math mode: FP32 math takes FLOAT or BFLOAT16, TF32 math
- * takes FLOAT, BF16 math takes BFLOAT16 (else NOT_SUPPORTED). */
+ * takes FLOAT, BF16 math takes BFLOAT16 (else NOT_SUPPORTED).
+ * Non-finite inputs: x and w are expected finite.  An Inf or NaN in x reaches
+ * every output whose receptive field holds it, as the sum defines; the
+ * few-channel kernel (DLC_KERNEL_TC_WINDOW) also multiplies zero filter taps
+ * with the input pixels just outside a window that share its packed phase
+ * pixel, so there an output beside such a window can read NaN as well (same
+ * image, rows whose window holds the pixel, within one stride step plus one
+ * phase pixel of its column).  Every other kernel reads exactly each window.
+ * Sources: maxDNN page, method section (each output is its receptive field
+ * times the filter weights); cuDNN page, method section (C API, descriptors
+ * with arbitrary strides, caller-owned buffers). */
 dlcStatus_t dlcConvolutionForward(dlcHandle_t handle, const float *alpha,
                                   dlcTensorDescriptor_t xDesc, const void *x,
                                   dlcFilterDescriptor_t wDesc, const void *w,
@@ -294,18 +315,25 @@ dlcStatus_t dlcDebugWaitTimeoutSelfTest(dlcHandle_t handle, int timeout_us);
  * where the few-channel kernel repacks the filters); every GPU that loads the
  * library holds those arrays until the process exits.
  *
- * The tile schedule is stream-K whenever it is legal (beta == 0, FLOAT y, at
- * least one tile per SM): the CTAs of a launch meet through the scratch
- * flags.  Problems with more than DLC_NOALLOC_MAX_TILES output tiles (128
- * pixels x up to 256 filters each) are rejected with NOT_SUPPORTED, and so is
- * any problem the library cannot run on its tensor-core kernel.
+ * It launches the same kernels as dlcConvolutionForward would for the
+ * problem (each CTA pair or CTA works on whole output tiles or on an
+ * independent part of one; no CTA waits on another CTA of the launch, so
+ * other work running on the GPU at the same time cannot stall it), with the
+ * few-channel kernel's repacked filters in the fixed array.  The
+ * DLC_NOALLOC_MAX_TILES flags serve only the opt-in stream-K schedule
+ * (environment DLC_TC_STREAMK=1), whose CTAs do wait on one another and need
+ * them all resident; problems with more tiles than flags run whole tiles.
  *
- * The first call on a device sets that device up (it looks up the scratch
- * array's device address and the tensor-map encoders); make that first call
- * before any stream capture.  Every call reuses the same scratch arrays and
- * clears its flags on `stream` before launching, so calls whose work overlaps
- * on the GPU (other streams, other host threads) race with each other: issue
- * them one at a time.
+ * The first call on a device sets that device up: it looks up the scratch
+ * arrays' device addresses and the tensor-map encoders, and loads every
+ * kernel of the library into the context (CUDA loads modules lazily, and a
+ * module load allocates device memory), so later calls load nothing.  Make
+ * that first call before any stream capture.  A device reset
+ * (cudaDeviceReset) invalidates the set-up: calls after one are not
+ * supported.  Every call reuses the same scratch arrays and clears its flags
+ * on `stream` before launching, so calls whose work overlaps on the GPU (other
+ * streams, other host threads) race with each other: issue them one at a
+ * time.
  *
  * status: NULL, or a device-accessible array of two ints owned by the caller;
  *   the call zeroes it on `stream`, and a kernel that gives up on a pipeline

@@ -158,7 +158,9 @@ def conv2d_fprop_points(x: np.ndarray, w: np.ndarray, pts: np.ndarray, *, pads=(
                         relu: bool = False, x_axes: str = "NCHW", w_axes: str = "KCRS",
                         lib=None) -> Tuple[np.ndarray, np.ndarray]:
     """The oracle at sampled output coordinates ``pts`` (int64 [n,4]: n,k,p,q).
-    ``y_in`` (if used) is an NCHW-shaped [N,K,P,Q] array.  Returns (values, bound)."""
+    ``y_in`` (if used) is an [N,K,P,Q]-indexed FP64 array with any
+    non-negative strides (a transposed view is read in place).  Returns
+    (values, bound)."""
     lib = lib or load()
     x = _as_f64_view(x, "x")
     w = _as_f64_view(w, "w")
@@ -175,7 +177,10 @@ def conv2d_fprop_points(x: np.ndarray, w: np.ndarray, pts: np.ndarray, *, pads=(
     bnd = np.zeros(len(pts), dtype=np.float64)
     ys = None
     if y_in is not None:
-        y_in = np.ascontiguousarray(y_in, dtype=np.float64)
+        # any (non-negative) strides: the C side reads y_in through them
+        y_in = _as_f64_view(np.asarray(y_in), "y_in")
+        if y_in.shape[1] != K or y_in.ndim != 4 or min(y_in.strides) < 0:
+            raise ValueError("y_in must be an [N, K, P, Q] view with non-negative strides")
         ys = _strides(y_in)
     if bias is not None:
         bias = np.ascontiguousarray(bias, dtype=np.float64).reshape(K)

@@ -137,7 +137,28 @@ def check_epilogue(lib, seed=3):
     np.testing.assert_allclose(y2, plain + bias[None, :, None, None], rtol=1e-14, atol=1e-14)
 
 
-PIN_BATTERY = (check_golden, check_im2col, check_torch, check_epilogue)
+def check_points_epilogue(lib, seed=4):
+    """The point evaluator with beta != 0 reads y_in through its own strides:
+    compared with the closed form alpha*conv + beta*y_in + bias on a y_in held
+    as a transposed (NHWC-stored) view, so a dropped or misapplied stride
+    picks up the wrong y_in element."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    x, w = _rand(rng, 2, 3, 9, 8), _rand(rng, 4, 3, 3, 2)
+    kw = dict(pads=(1, 2, 0, 1), stride=(2, 1), dilation=(1, 1), lib=lib)
+    plain, _ = oracle.conv2d_fprop(x, w, **kw)
+    y_nhwc = _rand(rng, plain.shape[0], plain.shape[2], plain.shape[3], plain.shape[1])
+    y_in = y_nhwc.transpose(0, 3, 1, 2)   # [N,K,P,Q] view, channels innermost in memory
+    bias = _rand(rng, 4)
+    alpha, beta = -0.5, 1.75
+    pts = np.array([[n, k, p, q] for n in range(plain.shape[0]) for k in range(4)
+                    for p in range(plain.shape[2]) for q in range(plain.shape[3])])
+    v, _ = oracle.conv2d_fprop_points(x, w, pts, alpha=alpha, beta=beta, y_in=y_in, bias=bias,
+                                      **kw)
+    exp = alpha * plain + beta * y_in + bias[None, :, None, None]
+    np.testing.assert_allclose(v, exp.reshape(-1), rtol=1e-14, atol=1e-14)
+
+
+PIN_BATTERY = (check_golden, check_im2col, check_torch, check_epilogue, check_points_epilogue)
 
 
 # --------------------------------------------------------------------------
@@ -257,6 +278,10 @@ def test_bound_is_sum_of_abs_products(oracle_lib):
     assert (bound >= np.abs(y) - 1e-12).all()
 
 
+def test_points_beta_reads_strided_y_in(oracle_lib):
+    check_points_epilogue(oracle_lib)
+
+
 def test_points_match_full(oracle_lib):
     rng = np.random.Generator(np.random.PCG64(11))
     x, w = _rand(rng, 2, 3, 10, 9), _rand(rng, 4, 3, 3, 3)
@@ -308,6 +333,8 @@ MUTANTS = {
     "stride_axes_swapped": ("i64 wi = q * pr->v + s * pr->dw - pr->pl;",
                             "i64 wi = q * pr->u + s * pr->dw - pr->pl;"),
     "beta_ignored": ("val += pr->beta * pr->y_in[yoff];", "val += 0.0 * pr->y_in[yoff];"),
+    "points_y_in_strides_ignored": ("NULL, ys ? ys : zero_strides, NULL,",
+                                    "NULL, zero_strides, NULL,"),
 }
 
 
