@@ -1,13 +1,22 @@
 """Forward-convolution benchmark (conv fprop TFLOP/s, direct-convolution FLOPs).
 
-One step = the five convolution layers of the AlexNet-style stack (N=128,
-BF16, NHWC, FP32 output), each on its own seeded synthetic input, through the
-C ABI.  The metric counts only direct-convolution FLOPs 2*N*K*P*Q*C*R*S
-(maxDNN page, method and findings sections).  L2 is flushed (256 MiB write)
-between timed steps, outside the timed events.
+The headline line times the OverFeat-style stack (N=128, BF16, NHWC, FP32
+output; the largest configuration that fits one GPU); its ``configs`` key
+holds the same fields for the tiny FP32 layer, the AlexNet-style stack, the
+ResNet-50-style layer set and the TF32 NCHW speech stack.  Every workload's
+layers run on their own seeded synthetic inputs through the C ABI.  The
+metric counts only direct-convolution FLOPs 2*N*K*P*Q*C*R*S (maxDNN page,
+method and findings sections).
+
+One step runs the workload's whole stack ``reps_per_step`` times back to
+back (a fixed count per workload, so that the timed region of the default
+steps lasts about a second and clock samplers see the GPU busy); L2 is
+flushed (256 MiB write) between steps, outside the timed events, and one pass
+over a stack touches more than the 129 MB L2 (except the tiny layer, which is
+latency-bound and makes no roofline claim beyond that).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload alexnet|overfeat|resnet50|speech]
+                    [--workload overfeat|alexnet|resnet50|speech|tiny] [--no-configs]
 
 --impl reference times the CPU oracle (FP64 direct convolution) on the host
 cores on a bounded sample of the same workload.  Under torchrun with N > 1
@@ -30,6 +39,15 @@ sys.path.insert(0, ROOT)
 
 METRIC = "conv fprop TFLOP/s (direct-conv FLOPs) and % of GB300 dense tensor-core peak"
 L2_FLUSH_BYTES = 256 << 20
+L2_BYTES = 129e6
+HEADLINE = "overfeat"
+CONFIG_ORDER = ["tiny", "alexnet", "overfeat", "resnet50", "speech"]
+# Passes over the stack per step: about 40-60 ms of GPU work per step on
+# GB300, so 20 steps keep the GPU busy for about a second.
+REPS_PER_STEP = {"tiny": 2000, "alexnet": 200, "overfeat": 80, "resnet50": 40, "speech": 8}
+# FP32 FFMA peak of the strict-FP32 path (bound "alu"): 152 SMs x 128 FP32
+# lanes x 2 FLOP per fused multiply-add x 2.07 GHz.
+FFMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
 def env_rank():
@@ -89,16 +107,29 @@ def layer_output_dims(layer):
     return P, Q
 
 
-def workload_config(workload, world):
+def reps_for(workload, override=None):
+    return int(override) if override else REPS_PER_STEP[workload]
+
+
+def workload_config(workload, world, reps=None):
     """The `config` both arms print: the workload and how a step is timed."""
     from deep_learning_convolution_gb300 import synth
     layers = synth.WORKLOADS[workload]
-    step_flops = sum(layer_geometry(l, *layer_output_dims(l))[0] for l in layers)
+    reps = reps_for(workload, reps)
+    geo = [layer_geometry(l, *layer_output_dims(l)) for l in layers]
+    pass_flops = sum(g[0] for g in geo)
+    pass_bytes = sum(g[1] for g in geo)
+    l2 = (f"one pass touches {pass_bytes / 1e6:.0f} MB (> {L2_BYTES / 1e6:.0f} MB L2); "
+          if pass_bytes > L2_BYTES else
+          f"one pass touches {pass_bytes / 1e6:.2f} MB (resident in L2; latency-bound); ")
+    l2 += "L2 flushed between steps (256 MiB write, untimed)"
     return {"workload": f"{workload}_stack", "layers": [l.name for l in layers],
             "batch": layers[0].N, "layout": layers[0].layout,
-            "output": "fp32", "l2": "flushed between steps (256 MiB write, untimed)",
+            "math": {"bf16": "bf16", "tf32": "tf32", "f32": "fp32"}[layers[0].dtype],
+            "output": "fp32", "l2": l2,
             "parallelism": f"replicas{world}" if world > 1 else "single_gpu",
-            "flops_per_step": step_flops}
+            "reps_per_step": reps, "flops_per_pass": pass_flops,
+            "flops_per_step": pass_flops * reps}
 
 
 # ---------------------------------------------------------------------------
@@ -178,46 +209,56 @@ class ClockSampler:
 # our arm
 # ---------------------------------------------------------------------------
 
-def run_ours(args, rank, world, local_rank):
-    import numpy as np
+def _peak_for(workload, peaks):
+    """(peak, unit-of-peak description) of a workload's arithmetic: the BF16
+    tensor-core peak measured as a burst at the maximum SM clock (the
+    convolution kernels keep the clock at its maximum through the timed
+    region, where the seconds-long GEMM loop behind the sustained figure ran
+    power-capped at a lower clock, so the burst figure is the stricter
+    denominator), half of it for TF32 (only BF16 was measured; TF32 runs at
+    half the BF16 rate), the FFMA peak for the strict-FP32 layer."""
+    math = workload_config(workload, 1)["math"]
+    bf16 = peaks["bf16_tflops"]
+    src = f"{peaks['source']} bf16 burst"
+    if math == "tf32":
+        return bf16 / 2, src + " x 1/2 (tf32)"
+    if math == "fp32":
+        return FFMA_PEAK_TFLOPS, "FFMA: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz (derived)"
+    return bf16, src
+
+
+def run_workload(args, workload, handle, stream, dev, rank, world, local_rank, headline):
+    """Times `steps` steps of `workload` (each `reps_per_step` passes over its
+    stack); returns the JSON fields of one bench line."""
     import torch
     from deep_learning_convolution_gb300 import api, synth
-    from deep_learning_convolution_gb300 import build as dlc_build
-
-    dlc_build.build()
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-    stream = torch.cuda.current_stream()
-    handle = api.Handle(stream)
-    layers = synth.WORKLOADS[args.workload]
-
+    layers = synth.WORKLOADS[workload]
+    reps = reps_for(workload, args.reps_per_step if headline else None)
     probs = []
     for j, layer in enumerate(layers):
-        x, w, _ = synth.make_inputs(layer, synth.workload_seed(args.workload, j))
+        x, w, _ = synth.make_inputs(layer, synth.workload_seed(workload, j))
         xt, wt = api.layer_tensors(layer, x, w, dev)
         conv, y = api.layer_problem(handle, layer, xt, wt)
         n, k, p, q = conv.output_dim()
         flops, nbytes = layer_geometry(layer, p, q)
         probs.append(dict(layer=layer, x=xt, w=wt, y=y, conv=conv, flops=flops, bytes=nbytes,
-                          kernel=conv.kernel(xt, wt, y), host_x=x, host_w=w))
+                          kernel=conv.kernel(xt, wt, y)))
         del x, w
-    step_flops = sum(pr["flops"] for pr in probs)
+    pass_flops = sum(pr["flops"] for pr in probs)
+    step_flops = pass_flops * reps
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
-    def step():
-        for pr in probs:
-            pr["conv"](pr["x"], pr["w"], pr["y"])
-
     for _ in range(args.warmup):
-        step()
+        for _ in range(max(1, reps // 4)):
+            for pr in probs:
+                pr["conv"](pr["x"], pr["w"], pr["y"])
     torch.cuda.synchronize()
     handle.synchronize()
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(probs) + 1)] for _ in range(K)]
+    nl = len(probs)
+    # events around every layer launch of every pass, on the launch stream
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(reps * nl + 1)] for _ in range(K)]
     sampler = ClockSampler(local_rank)
     if world > 1:
         torch.distributed.barrier()
@@ -228,9 +269,12 @@ def run_ours(args, rank, world, local_rank):
     for i in range(K):
         flush.fill_(float(i))
         ev[i][0].record(stream)
-        for j, pr in enumerate(probs):
-            pr["conv"](pr["x"], pr["w"], pr["y"])
-            ev[i][j + 1].record(stream)
+        e = 1
+        for _ in range(reps):
+            for pr in probs:
+                pr["conv"](pr["x"], pr["w"], pr["y"])
+                ev[i][e].record(stream)
+                e += 1
     torch.cuda.synchronize()
     clocks = sampler.stop()
     if world > 1:
@@ -238,55 +282,58 @@ def run_ours(args, rank, world, local_rank):
     launches = handle.launches() - launches0
     handle.synchronize()  # raises if a kernel recorded a device error
 
-    per_layer_ms = [0.0] * len(probs)
+    per_layer_ms = [0.0] * nl
     total_ms = 0.0
     for i in range(K):
         total_ms += ev[i][0].elapsed_time(ev[i][-1])
-        for j in range(len(probs)):
-            per_layer_ms[j] += ev[i][j].elapsed_time(ev[i][j + 1])
+        for e in range(reps * nl):
+            per_layer_ms[e % nl] += ev[i][e].elapsed_time(ev[i][e + 1])
     total_ms, value = aggregate_over_ranks(total_ms, step_flops, K, world, dev)
     ms_per_step = total_ms / K
 
     peaks = load_peaks()
-    peak_tf = peaks["bf16_tflops"] if args.workload != "speech" else peaks["bf16_tflops"] / 2
+    peak_tf, peak_src = _peak_for(workload, peaks)
     layer_rows = []
     by_kernel = {}
+    n_launch = K * reps
     for j, pr in enumerate(probs):
-        t_s = per_layer_ms[j] / K * 1e-3
+        t_s = per_layer_ms[j] / n_launch * 1e-3
         tflops = pr["flops"] / t_s / 1e12
         gbs = pr["bytes"] / t_s / 1e9
         roof = min(peak_tf, pr["flops"] / pr["bytes"] * peaks["hbm_gbs"] / 1e3)
         layer_rows.append({"layer": pr["layer"].name, "kernel": pr["kernel"],
                            "us": round(t_s * 1e6, 2), "tflops": round(tflops, 1),
                            "hbm_gbs": round(gbs, 1),
-                           "bound": "tensor" if roof >= peak_tf else "hbm",
+                           "bound": ("alu" if workload == "tiny" else "tensor")
+                           if roof >= peak_tf else "hbm",
                            "roofline_tflops": round(roof, 1),
                            "frac_of_roofline": round(tflops / roof, 4)})
-        k = by_kernel.setdefault(pr["kernel"], {"flops": 0, "bytes": 0, "ms": 0.0, "launches": 0})
-        k["flops"] += pr["flops"]
-        k["bytes"] += pr["bytes"]
-        k["ms"] += per_layer_ms[j]
-        k["launches"] += K
+        kk = by_kernel.setdefault(pr["kernel"], {"flops": 0, "bytes": 0, "ms": 0.0, "launches": 0})
+        kk["flops"] += pr["flops"]
+        kk["bytes"] += pr["bytes"]
+        kk["ms"] += per_layer_ms[j]
+        kk["launches"] += n_launch
     dom_name, dom = max(by_kernel.items(), key=lambda kv: kv[1]["ms"])
     avg_launch_s = dom["ms"] / dom["launches"] * 1e-3
-    flops_per_launch = dom["flops"] / (dom["launches"] / K)
-    bytes_per_launch = dom["bytes"] / (dom["launches"] / K)
+    per_pass = dom["launches"] / n_launch          # launches of this kernel per pass
+    flops_per_launch = dom["flops"] / per_pass
+    bytes_per_launch = dom["bytes"] / per_pass
     ai = flops_per_launch / bytes_per_launch
-    tensor_bound = ai * peaks["hbm_gbs"] / 1e3 >= peak_tf
+    compute_bound = ai * peaks["hbm_gbs"] / 1e3 >= peak_tf
     traffic = None
     tfile = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tfile):
         with open(tfile) as f:
             td = json.load(f)
-        ent = td.get(args.workload, {}).get(dom_name)
+        ent = td.get(workload, {}).get(dom_name)
         if ent and ent.get("kernel_sha") == kernel_source_hash():
             traffic = ent.get("dram_bytes_per_launch")
-    if tensor_bound:
+    if compute_bound:
         achieved = flops_per_launch / avg_launch_s / 1e12
-        roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak_tf,
+        roofline = {"bound": "alu" if workload == "tiny" else "tensor",
+                    "achieved": round(achieved, 1), "peak": round(peak_tf, 1),
                     "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4), "traffic": traffic,
-                    "kernel": dom_name, "peak_source": f"{peaks['source']} bf16 burst" +
-                    (" x 1/2 (tf32)" if args.workload == "speech" else "")}
+                    "kernel": dom_name, "peak_source": peak_src}
     else:
         achieved = bytes_per_launch / avg_launch_s / 1e9
         roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
@@ -295,34 +342,65 @@ def run_ours(args, rank, world, local_rank):
                     "peak_source": f"{peaks['source']} copy bandwidth"}
 
     # end to end: pinned host buffers -> device -> conv -> host, every step
-    e2e = run_e2e(args, probs, handle, stream, dev, step_flops, world)
-
-    result = None
-    if rank == 0:
-        dtype = "bf16" if layers[0].dtype == "bf16" else layers[0].dtype
-        result = {
-            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
-            "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
-            "data": "synthetic",
-            "config": workload_config(args.workload, world),
-            "roofline": roofline,
-            "layers": layer_rows,
-            "e2e": e2e,
-            "gpu_launches": launches,
-            "clocks": clocks,
-        }
-        if not args.no_cpu_baseline:
-            result["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
+    e2e = run_e2e(args, probs, handle, stream, dev, pass_flops, world)
+    dtype = {"bf16": "bf16", "tf32": "tf32", "f32": "f32"}[layers[0].dtype]
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
+        "data": "synthetic",
+        "config": workload_config(workload, world, reps),
+        "roofline": roofline,
+        "layers": layer_rows,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(workload, budget_s=args.cpu_seconds if headline
+                                           else args.cpu_seconds_config)
     for pr in probs:
         pr["conv"].close()
+    del probs, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from deep_learning_convolution_gb300 import api
+    from deep_learning_convolution_gb300 import build as dlc_build
+
+    dlc_build.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    stream = torch.cuda.current_stream()
+    handle = api.Handle(stream)
+    result = run_workload(args, args.workload, handle, stream, dev, rank, world, local_rank,
+                          headline=True)
+    if not args.no_configs:
+        configs = {}
+        for wl in CONFIG_ORDER:
+            if wl == args.workload:
+                continue
+            r = run_workload(args, wl, handle, stream, dev, rank, world, local_rank,
+                             headline=False)
+            r.pop("metric")
+            r.pop("n_gpus")
+            configs[wl] = r
+        result["configs"] = configs
     handle.close()
     if world > 1:
         torch.distributed.destroy_process_group()
-    return result
+    return result if rank == 0 else None
 
 
-def run_e2e(args, probs, handle, stream, dev, step_flops, world):
+def run_e2e(args, probs, handle, stream, dev, pass_flops, world):
+    """End-to-end throughput: every e2e step copies one pass's inputs in from
+    pinned host memory, runs the pass and copies every y back."""
     import numpy as np
     import torch
     steps = max(3, min(args.steps, args.e2e_steps))
@@ -398,7 +476,7 @@ def run_e2e(args, probs, handle, stream, dev, step_flops, world):
     join()
     end.record(stream)
     torch.cuda.synchronize()
-    ms, value = aggregate_over_ranks(start.elapsed_time(end), step_flops, steps, world, dev)
+    ms, value = aggregate_over_ranks(start.elapsed_time(end), pass_flops, steps, world, dev)
     return {"value": round(value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(ms / steps, 3)}
 
@@ -467,7 +545,7 @@ def run_reference(args, rank, world):
             "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": workload_config(args.workload, world),
+            "config": workload_config(args.workload, world, args.reps_per_step),
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -507,11 +585,16 @@ def run_profile_layer(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="alexnet",
-                    choices=["alexnet", "overfeat", "resnet50", "speech"])
+    ap.add_argument("--workload", default=HEADLINE, choices=CONFIG_ORDER)
+    ap.add_argument("--reps-per-step", type=int, default=None,
+                    help="passes over the stack per step (default: the workload's fixed count)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="time only --workload (no `configs` key with the other workloads)")
+    ap.add_argument("--cpu-seconds-config", type=float, default=3.0,
+                    help="oracle time budget of each non-headline workload's cpu_baseline")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--e2e-out-streams", type=int, default=1,
                     help="streams the end-to-end run reads results back on")

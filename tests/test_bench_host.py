@@ -85,7 +85,10 @@ def test_reference_arm_prints_the_contract_line():
     bench = _bench()
     assert d["impl"] == "reference"
     assert d["metric"] == bench.METRIC and d["unit"] == "TFLOP/s" and d["higher_is_better"]
-    assert d["config"] == bench.workload_config("alexnet", 1)
+    assert d["config"] == bench.workload_config(bench.HEADLINE, 1)
+    assert d["config"]["workload"] == "overfeat_stack"
+    assert d["config"]["flops_per_step"] == (d["config"]["flops_per_pass"]
+                                             * d["config"]["reps_per_step"])
     assert d["value"] > 0 and d["steps"] == 1 and d["warmup"] == 3
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
@@ -108,5 +111,6 @@ def test_bench_geometry_matches_the_oracle_extent():
             flops, _ = bench.layer_geometry(l, P, Q)
             assert flops == 2 * l.N * l.K * P * Q * l.C * l.R * l.S
         cfg = bench.workload_config(wl, 1)
-        assert cfg["flops_per_step"] == sum(
+        assert cfg["flops_per_pass"] == sum(
             bench.layer_geometry(l, *bench.layer_output_dims(l))[0] for l in layers)
+        assert cfg["flops_per_step"] == cfg["flops_per_pass"] * cfg["reps_per_step"]
