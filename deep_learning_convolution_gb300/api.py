@@ -15,7 +15,9 @@ from typing import Optional, Sequence
 
 from . import binding as B
 
-MATH = {"fp32": B.DLC_MATH_FP32, "tf32": B.DLC_MATH_TF32, "bf16": B.DLC_MATH_BF16}
+MATH = {"fp32": B.DLC_MATH_FP32, "tf32": B.DLC_MATH_TF32, "bf16": B.DLC_MATH_BF16,
+        "fp64": B.DLC_MATH_FP64}
+MODE = {"cross_correlation": B.DLC_CROSS_CORRELATION, "convolution": B.DLC_CONVOLUTION}
 
 
 def _dtype_code(t) -> int:
@@ -24,6 +26,8 @@ def _dtype_code(t) -> int:
         return B.DLC_DATA_FLOAT
     if t.dtype == torch.bfloat16:
         return B.DLC_DATA_BFLOAT16
+    if t.dtype == torch.float64:
+        return B.DLC_DATA_DOUBLE
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
@@ -79,7 +83,7 @@ class Conv2dForward:
     def __init__(self, handle: Handle, x, w, y, *, x_axes: str = "NCHW", w_axes: str = "KCRS",
                  y_axes: str = "NCHW", pads: Sequence[int] = (0, 0, 0, 0),
                  stride: Sequence[int] = (1, 1), dilation: Sequence[int] = (1, 1),
-                 math: str = "bf16"):
+                 math: str = "bf16", mode: str = "cross_correlation"):
         self.handle = handle
         self.x_desc = B.dlcCreateTensorDescriptor()
         self.w_desc = B.dlcCreateFilterDescriptor()
@@ -102,6 +106,7 @@ class Conv2dForward:
         B.dlcSetConvolution2dDescriptor(self.conv, 0, 0, int(stride[0]), int(stride[1]),
                                         int(dilation[0]), int(dilation[1]), MATH[math])
         B.dlcSetConvolution2dPadding(self.conv, *[int(p) for p in pads])
+        B.dlcSetConvolutionMode(self.conv, MODE[mode])
 
     def output_dim(self):
         return B.dlcGetConvolution2dForwardOutputDim(self.conv, self.x_desc, self.w_desc)
@@ -144,6 +149,103 @@ class Conv2dForward:
             self.close()
         except Exception:
             pass
+
+
+class _Descriptors:
+    """Tensor, filter and convolution descriptors of one problem, in the
+    forward problem's terms: activations x [N,C,H,W], filters w [K,C,R,S],
+    outputs y [N,K,P,Q] (the backward routines read or write their gradients
+    with the same shapes)."""
+
+    def __init__(self, x, w, y, x_axes, w_axes, y_axes, pads, stride, dilation, math, mode):
+        self.x_desc = B.dlcCreateTensorDescriptor()
+        self.w_desc = B.dlcCreateFilterDescriptor()
+        self.y_desc = B.dlcCreateTensorDescriptor()
+        self.conv = B.dlcCreateConvolutionDescriptor()
+        xs, xst = _logical(x, x_axes, "NCHW")
+        B.dlcSetTensor4dDescriptorEx(self.x_desc, _dtype_code(x), *xs, *xst)
+        if w_axes not in ("KCRS", "KRSC"):
+            raise ValueError("filters must be KCRS or KRSC")
+        if not w.is_contiguous():
+            raise ValueError("filter tensors must be dense (contiguous)")
+        ws, _ = _logical(w, w_axes, "KCRS")
+        B.dlcSetFilter4dDescriptor(self.w_desc, _dtype_code(w),
+                                   B.DLC_TENSOR_NCHW if w_axes == "KCRS" else B.DLC_TENSOR_NHWC, *ws)
+        ys, yst = _logical(y, y_axes, "NCHW")
+        B.dlcSetTensor4dDescriptorEx(self.y_desc, _dtype_code(y), *ys, *yst)
+        B.dlcSetConvolution2dDescriptor(self.conv, 0, 0, int(stride[0]), int(stride[1]),
+                                        int(dilation[0]), int(dilation[1]), MATH[math])
+        B.dlcSetConvolution2dPadding(self.conv, *[int(p) for p in pads])
+        B.dlcSetConvolutionMode(self.conv, MODE[mode])
+
+    def close(self):
+        for d, f in ((self.x_desc, B.dlcDestroyTensorDescriptor),
+                     (self.y_desc, B.dlcDestroyTensorDescriptor),
+                     (self.w_desc, B.dlcDestroyFilterDescriptor),
+                     (self.conv, B.dlcDestroyConvolutionDescriptor)):
+            if d is not None:
+                f(d)
+        self.x_desc = self.y_desc = self.w_desc = self.conv = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Conv2dBackwardData(_Descriptors):
+    """dx = alpha * dgrad(w, dy) + beta * dx through dlcConvolutionBackwardData;
+    built from example tensors w [K,C,R,S], dy [N,K,P,Q] and dx [N,C,H,W]."""
+
+    def __init__(self, handle: Handle, w, dy, dx, *, w_axes="KCRS", dy_axes="NCHW",
+                 dx_axes="NCHW", pads=(0, 0, 0, 0), stride=(1, 1), dilation=(1, 1),
+                 math="bf16", mode="cross_correlation"):
+        self.handle = handle
+        super().__init__(dx, w, dy, dx_axes, w_axes, dy_axes, pads, stride, dilation, math, mode)
+
+    def kernel(self, w=None, dy=None, dx=None) -> str:
+        k = B.dlcGetConvolutionBackwardDataKernel(
+            self.handle.h, self.w_desc, w.data_ptr() if w is not None else 0, self.y_desc,
+            dy.data_ptr() if dy is not None else 0, self.conv, self.x_desc,
+            dx.data_ptr() if dx is not None else 0)
+        return B.KERNEL_NAMES[k]
+
+    def workspace_size(self) -> int:
+        return B.dlcGetConvolutionBackwardDataWorkspaceSize(self.handle.h, self.w_desc, self.y_desc,
+                                                            self.conv, self.x_desc)
+
+    def __call__(self, w, dy, dx, alpha: float = 1.0, beta: float = 0.0):
+        B.dlcConvolutionBackwardData(self.handle.h, alpha, self.w_desc, w.data_ptr(), self.y_desc,
+                                     dy.data_ptr(), self.conv, beta, self.x_desc, dx.data_ptr())
+        return dx
+
+
+class Conv2dBackwardFilter(_Descriptors):
+    """dw = alpha * wgrad(x, dy) + beta * dw through dlcConvolutionBackwardFilter;
+    built from example tensors x [N,C,H,W], dy [N,K,P,Q] and dw [K,C,R,S]."""
+
+    def __init__(self, handle: Handle, x, dy, dw, *, x_axes="NCHW", dy_axes="NCHW",
+                 dw_axes="KCRS", pads=(0, 0, 0, 0), stride=(1, 1), dilation=(1, 1),
+                 math="bf16", mode="cross_correlation"):
+        self.handle = handle
+        super().__init__(x, dw, dy, x_axes, dw_axes, dy_axes, pads, stride, dilation, math, mode)
+
+    def kernel(self, x=None, dy=None, dw=None) -> str:
+        k = B.dlcGetConvolutionBackwardFilterKernel(
+            self.handle.h, self.x_desc, x.data_ptr() if x is not None else 0, self.y_desc,
+            dy.data_ptr() if dy is not None else 0, self.conv, self.w_desc,
+            dw.data_ptr() if dw is not None else 0)
+        return B.KERNEL_NAMES[k]
+
+    def workspace_size(self) -> int:
+        return B.dlcGetConvolutionBackwardFilterWorkspaceSize(self.handle.h, self.x_desc,
+                                                              self.y_desc, self.conv, self.w_desc)
+
+    def __call__(self, x, dy, dw, alpha: float = 1.0, beta: float = 0.0):
+        B.dlcConvolutionBackwardFilter(self.handle.h, alpha, self.x_desc, x.data_ptr(), self.y_desc,
+                                       dy.data_ptr(), self.conv, beta, self.w_desc, dw.data_ptr())
+        return dw
 
 
 def output_dim(x, w, *, x_axes="NCHW", w_axes="KCRS", pads=(0, 0, 0, 0), stride=(1, 1),

@@ -28,11 +28,15 @@ DLC_STATUS_ALLOC_FAILED = 6
 
 DLC_DATA_FLOAT = 0
 DLC_DATA_BFLOAT16 = 1
+DLC_DATA_DOUBLE = 2
 DLC_TENSOR_NCHW = 0
 DLC_TENSOR_NHWC = 1
 DLC_MATH_FP32 = 0
 DLC_MATH_TF32 = 1
 DLC_MATH_BF16 = 2
+DLC_MATH_FP64 = 3
+DLC_CROSS_CORRELATION = 0
+DLC_CONVOLUTION = 1
 DLC_ACTIVATION_IDENTITY = 0
 DLC_ACTIVATION_RELU = 1
 DLC_KERNEL_NONE = 0
@@ -42,13 +46,16 @@ DLC_KERNEL_TC_GATHER = 3
 DLC_KERNEL_TC_GATHER_RUNS = 4
 DLC_KERNEL_TC_WINDOW = 5
 DLC_KERNEL_TC_IM2COL_PAIR = 6
+DLC_KERNEL_DIRECT = 7
+DLC_KERNEL_TC_WGRAD = 8
 DLC_DEVERR_NONE = 0
 DLC_DEVERR_WAIT_TIMEOUT = 1
 
 KERNEL_NAMES = {DLC_KERNEL_NONE: "none", DLC_KERNEL_FFMA: "ffma",
                 DLC_KERNEL_TC_IM2COL: "tc_im2col", DLC_KERNEL_TC_GATHER: "tc_gather",
                 DLC_KERNEL_TC_GATHER_RUNS: "tc_runs", DLC_KERNEL_TC_WINDOW: "tc_window",
-                DLC_KERNEL_TC_IM2COL_PAIR: "tc_im2col_pair"}
+                DLC_KERNEL_TC_IM2COL_PAIR: "tc_im2col_pair", DLC_KERNEL_DIRECT: "direct",
+                DLC_KERNEL_TC_WGRAD: "tc_wgrad"}
 
 _h = c_void_p          # opaque handle / descriptor
 _ph = POINTER(c_void_p)
@@ -90,6 +97,15 @@ SIGNATURES = {
     "dlcConvolutionForward": [_h, _pf, _h, c_void_p, _h, c_void_p, _h, _pf, _h, c_void_p],
     "dlcConvolutionBiasActivationForward": [_h, _pf, _h, c_void_p, _h, c_void_p, _h, _pf,
                                             c_void_p, c_int, _h, c_void_p],
+    "dlcSetConvolutionMode": [_h, c_int],
+    "dlcGetConvolutionMode": [_h, _pi],
+    "dlcConvolutionBackwardData": [_h, _pf, _h, c_void_p, _h, c_void_p, _h, _pf, _h, c_void_p],
+    "dlcConvolutionBackwardFilter": [_h, _pf, _h, c_void_p, _h, c_void_p, _h, _pf, _h, c_void_p],
+    "dlcGetConvolutionBackwardDataWorkspaceSize": [_h, _h, _h, _h, _h, POINTER(c_size_t)],
+    "dlcGetConvolutionBackwardFilterWorkspaceSize": [_h, _h, _h, _h, _h, POINTER(c_size_t)],
+    "dlcGetConvolutionBackwardDataKernel": [_h, _h, c_void_p, _h, c_void_p, _h, _h, c_void_p, _pi],
+    "dlcGetConvolutionBackwardFilterKernel": [_h, _h, c_void_p, _h, c_void_p, _h, _h, c_void_p,
+                                              _pi],
     "dlcDebugWaitTimeoutSelfTest": [_h, c_int],
     "dlcConvolutionForwardNoAlloc": [c_void_p, _pf, _h, c_void_p, _h, c_void_p, _h, _pf, _h,
                                      c_void_p, c_void_p],
@@ -317,3 +333,57 @@ def dlcConvolutionForwardNoAlloc(stream_ptr, alpha, x_desc, x_ptr, w_desc, w_ptr
     _call("dlcConvolutionForwardNoAlloc", c_void_p(stream_ptr or None), byref(a), x_desc,
           c_void_p(x_ptr), w_desc, c_void_p(w_ptr), conv, byref(b), y_desc, c_void_p(y_ptr),
           c_void_p(status_ptr or None))
+
+
+def dlcSetConvolutionMode(conv, mode: int):
+    _call("dlcSetConvolutionMode", conv, int(mode))
+
+
+def dlcGetConvolutionMode(conv) -> int:
+    m = c_int()
+    _call("dlcGetConvolutionMode", conv, byref(m))
+    return m.value
+
+
+def dlcConvolutionBackwardData(handle, alpha, w_desc, w_ptr, dy_desc, dy_ptr, conv, beta, dx_desc,
+                               dx_ptr):
+    a, b = c_float(alpha), c_float(beta)
+    _call("dlcConvolutionBackwardData", handle, byref(a), w_desc, c_void_p(w_ptr), dy_desc,
+          c_void_p(dy_ptr), conv, byref(b), dx_desc, c_void_p(dx_ptr))
+
+
+def dlcConvolutionBackwardFilter(handle, alpha, x_desc, x_ptr, dy_desc, dy_ptr, conv, beta, dw_desc,
+                                 dw_ptr):
+    a, b = c_float(alpha), c_float(beta)
+    _call("dlcConvolutionBackwardFilter", handle, byref(a), x_desc, c_void_p(x_ptr), dy_desc,
+          c_void_p(dy_ptr), conv, byref(b), dw_desc, c_void_p(dw_ptr))
+
+
+def dlcGetConvolutionBackwardDataWorkspaceSize(handle, w_desc, dy_desc, conv, dx_desc) -> int:
+    n = c_size_t()
+    _call("dlcGetConvolutionBackwardDataWorkspaceSize", handle, w_desc, dy_desc, conv, dx_desc,
+          byref(n))
+    return n.value
+
+
+def dlcGetConvolutionBackwardFilterWorkspaceSize(handle, x_desc, dy_desc, conv, dw_desc) -> int:
+    n = c_size_t()
+    _call("dlcGetConvolutionBackwardFilterWorkspaceSize", handle, x_desc, dy_desc, conv, dw_desc,
+          byref(n))
+    return n.value
+
+
+def dlcGetConvolutionBackwardDataKernel(handle, w_desc, w_ptr, dy_desc, dy_ptr, conv, dx_desc,
+                                        dx_ptr) -> int:
+    k = c_int()
+    _call("dlcGetConvolutionBackwardDataKernel", handle, w_desc, c_void_p(w_ptr or None), dy_desc,
+          c_void_p(dy_ptr or None), conv, dx_desc, c_void_p(dx_ptr or None), byref(k))
+    return k.value
+
+
+def dlcGetConvolutionBackwardFilterKernel(handle, x_desc, x_ptr, dy_desc, dy_ptr, conv, dw_desc,
+                                          dw_ptr) -> int:
+    k = c_int()
+    _call("dlcGetConvolutionBackwardFilterKernel", handle, x_desc, c_void_p(x_ptr or None),
+          dy_desc, c_void_p(dy_ptr or None), conv, dw_desc, c_void_p(dw_ptr or None), byref(k))
+    return k.value

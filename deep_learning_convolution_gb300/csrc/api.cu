@@ -29,9 +29,28 @@ int64_t out_extent(int64_t in, int64_t lo, int64_t hi, int64_t filt, int64_t dil
     return span / stride + 1;
 }
 
-size_t elt_size(dlcDataType_t t) { return t == DLC_DATA_BFLOAT16 ? 2 : 4; }
+size_t elt_size(dlcDataType_t t) { return (size_t)dlc_dtype_bytes(t); }
 
-bool valid_dtype(int t) { return t == DLC_DATA_FLOAT || t == DLC_DATA_BFLOAT16; }
+bool valid_dtype(int t) {
+    return t == DLC_DATA_FLOAT || t == DLC_DATA_BFLOAT16 || t == DLC_DATA_DOUBLE;
+}
+
+// Storage of the two inputs allowed by a math mode.
+bool math_takes(dlcMathType_t m, dlcDataType_t in) {
+    switch (m) {
+        case DLC_MATH_FP32: return in == DLC_DATA_FLOAT || in == DLC_DATA_BFLOAT16;
+        case DLC_MATH_TF32: return in == DLC_DATA_FLOAT;
+        case DLC_MATH_BF16: return in == DLC_DATA_BFLOAT16;
+        case DLC_MATH_FP64: return in == DLC_DATA_DOUBLE;
+    }
+    return false;
+}
+
+// Storage of the output allowed for given inputs: DOUBLE with DOUBLE, else
+// FLOAT or BFLOAT16.
+bool out_ok(dlcDataType_t in, dlcDataType_t out) {
+    return in == DLC_DATA_DOUBLE ? out == DLC_DATA_DOUBLE : out != DLC_DATA_DOUBLE;
+}
 bool valid_format(int f) { return f == DLC_TENSOR_NCHW || f == DLC_TENSOR_NHWC; }
 
 // Largest element offset reachable through (extent, stride) pairs.
@@ -87,16 +106,9 @@ dlcStatus_t resolve(dlcTensorDescriptor_t xd, const void *x, dlcFilterDescriptor
     if (P < 1 || Q < 1 || P > INT32_MAX || Q > INT32_MAX) return DLC_STATUS_BAD_PARAM;
     if (yd->n != xd->n || yd->c != wd->k || yd->h != P || yd->w != Q) return DLC_STATUS_BAD_PARAM;
 
-    switch (cd->math) {
-        case DLC_MATH_FP32: break;
-        case DLC_MATH_TF32:
-            if (xd->dtype != DLC_DATA_FLOAT) return DLC_STATUS_NOT_SUPPORTED;
-            break;
-        case DLC_MATH_BF16:
-            if (xd->dtype != DLC_DATA_BFLOAT16) return DLC_STATUS_NOT_SUPPORTED;
-            break;
-        default: return DLC_STATUS_BAD_PARAM;
-    }
+    if (cd->math < DLC_MATH_FP32 || cd->math > DLC_MATH_FP64) return DLC_STATUS_BAD_PARAM;
+    if (!math_takes(cd->math, xd->dtype) || !out_ok(xd->dtype, yd->dtype))
+        return DLC_STATUS_NOT_SUPPORTED;
 
     pb.N = xd->n; pb.C = xd->c; pb.H = xd->h; pb.W = xd->w;
     pb.K = wd->k; pb.R = wd->r; pb.S = wd->s; pb.P = (int)P; pb.Q = (int)Q;
@@ -113,6 +125,8 @@ dlcStatus_t resolve(dlcTensorDescriptor_t xd, const void *x, dlcFilterDescriptor
     filter_strides(wd, pb.ws);
     pb.x = x; pb.w = w; pb.y = y;
     pb.bias = nullptr; pb.alpha = 1.f; pb.beta = 0.f; pb.relu = 0;
+    pb.flip = cd->mode == DLC_CONVOLUTION ? 1 : 0;
+    pb.w_mn = 0;
 
     const int64_t yext[4] = {pb.N, pb.K, pb.P, pb.Q};
     if (!strides_injective(yext, pb.ys, 4)) return DLC_STATUS_BAD_PARAM;
@@ -138,8 +152,81 @@ dlcStatus_t resolve(dlcTensorDescriptor_t xd, const void *x, dlcFilterDescriptor
 }
 
 dlcKernel_t pick_kernel(const dlcContext *ctx, const ConvProblem &pb) {
-    if (pb.math == DLC_MATH_FP32) return DLC_KERNEL_FFMA;
+    if (pb.math == DLC_MATH_FP32 || pb.math == DLC_MATH_FP64) return DLC_KERNEL_FFMA;
     return dlc_tc_variant(ctx, pb);
+}
+
+// Convolution mode for the kernels that read filters through strides: the
+// mirrored taps as a view based at tap (R-1, S-1) with negated tap strides.
+// (The SM-pair kernel mirrors its filter-load coordinates instead.)
+void mirror_filter_view(ConvProblem &pb) {
+    const long long e = dlc_dtype_bytes(pb.xdt);
+    pb.w = static_cast<const char *>(pb.w) +
+           e * ((long long)(pb.R - 1) * pb.ws[2] + (long long)(pb.S - 1) * pb.ws[3]);
+    pb.ws[2] = -pb.ws[2];
+    pb.ws[3] = -pb.ws[3];
+    pb.flip = 0;
+}
+
+// Validates a backward problem.  `xd`/`x` describe the forward input (dx for
+// the data gradient), `wd`/`w` the filters (dw for the filter gradient),
+// `dyd`/`dy` the forward output's gradient; `out` says which of x (0) or w (1)
+// is written.
+dlcStatus_t resolve_bwd(dlcTensorDescriptor_t xd, const void *x, dlcFilterDescriptor_t wd,
+                        const void *w, dlcConvolutionDescriptor_t cd, dlcTensorDescriptor_t dyd,
+                        const void *dy, int out, bool check_ptrs, BwdProblem &bp) {
+    if (!xd || !wd || !cd || !dyd) return DLC_STATUS_BAD_PARAM;
+    if (!xd->set || !wd->set || !cd->set || !dyd->set) return DLC_STATUS_NOT_INITIALIZED;
+    if (xd->c != wd->c) return DLC_STATUS_BAD_PARAM;
+    const int64_t P = out_extent(xd->h, cd->pad_top, cd->pad_bottom, wd->r, cd->dil_h, cd->u);
+    const int64_t Q = out_extent(xd->w, cd->pad_left, cd->pad_right, wd->s, cd->dil_w, cd->v);
+    if (P < 1 || Q < 1 || P > INT32_MAX || Q > INT32_MAX) return DLC_STATUS_BAD_PARAM;
+    if (dyd->n != xd->n || dyd->c != wd->k || dyd->h != P || dyd->w != Q) return DLC_STATUS_BAD_PARAM;
+    // the two inputs share a storage type; the output's may differ
+    const dlcDataType_t in = out == 0 ? wd->dtype : xd->dtype;
+    const dlcDataType_t od = out == 0 ? xd->dtype : wd->dtype;
+    if (dyd->dtype != in) return DLC_STATUS_BAD_PARAM;
+    if (cd->math < DLC_MATH_FP32 || cd->math > DLC_MATH_FP64) return DLC_STATUS_BAD_PARAM;
+    if (!math_takes(cd->math, in) || !out_ok(in, od)) return DLC_STATUS_NOT_SUPPORTED;
+
+    bp.N = xd->n; bp.C = xd->c; bp.H = xd->h; bp.W = xd->w;
+    bp.K = wd->k; bp.R = wd->r; bp.S = wd->s; bp.P = (int)P; bp.Q = (int)Q;
+    bp.pt = cd->pad_top; bp.pb = cd->pad_bottom; bp.pl = cd->pad_left; bp.pr = cd->pad_right;
+    bp.u = cd->u; bp.v = cd->v; bp.dh = cd->dil_h; bp.dw = cd->dil_w;
+    bp.math = cd->math;
+    bp.in_dt = in;
+    bp.out_dt = od;
+    bp.wfmt = wd->format;
+    bp.flip = cd->mode == DLC_CONVOLUTION ? 1 : 0;
+    for (int i = 0; i < 4; ++i) {
+        bp.xs[i] = xd->stride[i];
+        bp.dys[i] = dyd->stride[i];
+    }
+    filter_strides(wd, bp.ws);
+    bp.x = x; bp.w = w; bp.dy = dy;
+    bp.alpha = 1.0; bp.beta = 0.0;
+
+    const int64_t xext[4] = {bp.N, bp.C, bp.H, bp.W};
+    const int64_t wext[4] = {bp.K, bp.C, bp.R, bp.S};
+    const int64_t yext[4] = {bp.N, bp.K, bp.P, bp.Q};
+    if (out == 0 && !strides_injective(xext, bp.xs, 4)) return DLC_STATUS_BAD_PARAM;
+    const int64_t xmax = max_offset(xext, bp.xs, 4);
+    const int64_t wmax = max_offset(wext, bp.ws, 4);
+    const int64_t ymax = max_offset(yext, bp.dys, 4);
+    const int64_t lim = (int64_t)1 << 60;
+    if (xmax >= lim || wmax >= lim || ymax >= lim) return DLC_STATUS_BAD_PARAM;
+    if (check_ptrs) {
+        if (!x || !w || !dy) return DLC_STATUS_BAD_PARAM;
+        const size_t ex = elt_size(xd->dtype), ew = elt_size(wd->dtype), ey = elt_size(in);
+        if ((uintptr_t)x % ex || (uintptr_t)w % ew || (uintptr_t)dy % ey) return DLC_STATUS_BAD_PARAM;
+        const uintptr_t x0 = (uintptr_t)x, x1 = x0 + (uintptr_t)(xmax + 1) * ex;
+        const uintptr_t w0 = (uintptr_t)w, w1 = w0 + (uintptr_t)(wmax + 1) * ew;
+        const uintptr_t y0 = (uintptr_t)dy, y1 = y0 + (uintptr_t)(ymax + 1) * ey;
+        const bool bad = out == 0 ? (ranges_overlap(x0, x1, w0, w1) || ranges_overlap(x0, x1, y0, y1))
+                                  : (ranges_overlap(w0, w1, x0, x1) || ranges_overlap(w0, w1, y0, y1));
+        if (bad) return DLC_STATUS_BAD_PARAM;
+    }
+    return DLC_STATUS_SUCCESS;
 }
 
 dlcStatus_t pending_device_error(dlcContext *h) {
@@ -166,8 +253,9 @@ dlcStatus_t forward(dlcHandle_t h, const float *alpha, dlcTensorDescriptor_t xd,
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return DLC_STATUS_BAD_PARAM;
     dlcKernel_t k = pick_kernel(h, pb);
-    if (k == DLC_KERNEL_FFMA) return dlc_launch_ffma(h, pb);
     if (k == DLC_KERNEL_NONE) return DLC_STATUS_NOT_SUPPORTED;
+    if (pb.flip && k != DLC_KERNEL_TC_IM2COL_PAIR) mirror_filter_view(pb);
+    if (k == DLC_KERNEL_FFMA) return dlc_launch_ffma(h, pb);
     return dlc_launch_tc(h, pb, k);
 }
 
@@ -424,7 +512,8 @@ dlcStatus_t dlcSetConvolution2dDescriptor(dlcConvolutionDescriptor_t d, int pad_
     if (!d) return DLC_STATUS_BAD_PARAM;
     if (pad_h < 0 || pad_w < 0 || u < 1 || v < 1 || dil_h < 1 || dil_w < 1)
         return DLC_STATUS_BAD_PARAM;
-    if (math != DLC_MATH_FP32 && math != DLC_MATH_TF32 && math != DLC_MATH_BF16)
+    if (math != DLC_MATH_FP32 && math != DLC_MATH_TF32 && math != DLC_MATH_BF16 &&
+        math != DLC_MATH_FP64)
         return DLC_STATUS_BAD_PARAM;
     const int big = 1 << 20;
     if (pad_h > big || pad_w > big || u > big || v > big || dil_h > big || dil_w > big)
@@ -614,14 +703,124 @@ dlcStatus_t dlcConvolutionForwardNoAlloc(void *stream, const float *alpha,
     ctx.wpack = nd->wpack;
     ctx.encode_tiled = nd->encode_tiled;
     ctx.encode_im2col = nd->encode_im2col;
+    if (pb.math == DLC_MATH_FP64) return DLC_STATUS_NOT_SUPPORTED;
     const dlcKernel_t k = dlc_tc_variant(&ctx, pb);
     if (k == DLC_KERNEL_NONE || k == DLC_KERNEL_FFMA) return DLC_STATUS_NOT_SUPPORTED;
+    if (pb.flip && k != DLC_KERNEL_TC_IM2COL_PAIR) mirror_filter_view(pb);
     // the flags and the error words start at zero on every call
     if (cudaMemsetAsync(nd->scratch, 0, (DLC_NOALLOC_MAX_TILES + 2) * sizeof(int), ctx.stream) !=
             cudaSuccess ||
         (status && cudaMemsetAsync(status, 0, 2 * sizeof(int), ctx.stream) != cudaSuccess))
         return DLC_STATUS_EXECUTION_FAILED;
     return dlc_launch_tc(&ctx, pb, k);
+}
+
+dlcStatus_t dlcSetConvolutionMode(dlcConvolutionDescriptor_t d, dlcConvolutionMode_t mode) {
+    if (!d) return DLC_STATUS_BAD_PARAM;
+    if (!d->set) return DLC_STATUS_NOT_INITIALIZED;
+    if (mode != DLC_CROSS_CORRELATION && mode != DLC_CONVOLUTION) return DLC_STATUS_BAD_PARAM;
+    d->mode = mode;
+    return DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlcGetConvolutionMode(dlcConvolutionDescriptor_t d, dlcConvolutionMode_t *mode) {
+    if (!d || !mode) return DLC_STATUS_BAD_PARAM;
+    if (!d->set) return DLC_STATUS_NOT_INITIALIZED;
+    *mode = d->mode;
+    return DLC_STATUS_SUCCESS;
+}
+
+// ---- backward routines -----------------------------------------------------------
+dlcStatus_t dlcConvolutionBackwardData(dlcHandle_t h, const float *alpha,
+                                       dlcFilterDescriptor_t wd, const void *w,
+                                       dlcTensorDescriptor_t dyd, const void *dy,
+                                       dlcConvolutionDescriptor_t cd, const float *beta,
+                                       dlcTensorDescriptor_t dxd, void *dx) {
+    if (!h) return DLC_STATUS_NOT_INITIALIZED;
+    if (!alpha || !beta) return DLC_STATUS_BAD_PARAM;
+    BwdProblem bp;
+    dlcStatus_t st = resolve_bwd(dxd, dx, wd, w, cd, dyd, dy, 0, true, bp);
+    if (st != DLC_STATUS_SUCCESS) return st;
+    bp.alpha = *alpha;
+    bp.beta = *beta;
+    st = pending_device_error(h);
+    if (st != DLC_STATUS_SUCCESS) return st;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return DLC_STATUS_BAD_PARAM;
+    return dlc_launch_dgrad(h, bp);
+}
+
+dlcStatus_t dlcConvolutionBackwardFilter(dlcHandle_t h, const float *alpha,
+                                         dlcTensorDescriptor_t xd, const void *x,
+                                         dlcTensorDescriptor_t dyd, const void *dy,
+                                         dlcConvolutionDescriptor_t cd, const float *beta,
+                                         dlcFilterDescriptor_t dwd, void *dw) {
+    if (!h) return DLC_STATUS_NOT_INITIALIZED;
+    if (!alpha || !beta) return DLC_STATUS_BAD_PARAM;
+    BwdProblem bp;
+    dlcStatus_t st = resolve_bwd(xd, x, dwd, dw, cd, dyd, dy, 1, true, bp);
+    if (st != DLC_STATUS_SUCCESS) return st;
+    bp.alpha = *alpha;
+    bp.beta = *beta;
+    st = pending_device_error(h);
+    if (st != DLC_STATUS_SUCCESS) return st;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return DLC_STATUS_BAD_PARAM;
+    return dlc_launch_wgrad(h, bp);
+}
+
+dlcStatus_t dlcGetConvolutionBackwardDataWorkspaceSize(dlcHandle_t h, dlcFilterDescriptor_t wd,
+                                                       dlcTensorDescriptor_t dyd,
+                                                       dlcConvolutionDescriptor_t cd,
+                                                       dlcTensorDescriptor_t dxd, size_t *bytes) {
+    if (!h) return DLC_STATUS_NOT_INITIALIZED;
+    if (!bytes) return DLC_STATUS_BAD_PARAM;
+    BwdProblem bp;
+    dlcStatus_t st = resolve_bwd(dxd, nullptr, wd, nullptr, cd, dyd, nullptr, 0, false, bp);
+    if (st != DLC_STATUS_SUCCESS) return st;
+    *bytes = 0;
+    return DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlcGetConvolutionBackwardFilterWorkspaceSize(dlcHandle_t h, dlcTensorDescriptor_t xd,
+                                                         dlcTensorDescriptor_t dyd,
+                                                         dlcConvolutionDescriptor_t cd,
+                                                         dlcFilterDescriptor_t dwd, size_t *bytes) {
+    if (!h) return DLC_STATUS_NOT_INITIALIZED;
+    if (!bytes) return DLC_STATUS_BAD_PARAM;
+    BwdProblem bp;
+    dlcStatus_t st = resolve_bwd(xd, nullptr, dwd, nullptr, cd, dyd, nullptr, 1, false, bp);
+    if (st != DLC_STATUS_SUCCESS) return st;
+    *bytes = 0;
+    return DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlcGetConvolutionBackwardDataKernel(dlcHandle_t h, dlcFilterDescriptor_t wd,
+                                                const void *w, dlcTensorDescriptor_t dyd,
+                                                const void *dy, dlcConvolutionDescriptor_t cd,
+                                                dlcTensorDescriptor_t dxd, const void *dx,
+                                                dlcKernel_t *kernel) {
+    if (!h) return DLC_STATUS_NOT_INITIALIZED;
+    if (!kernel) return DLC_STATUS_BAD_PARAM;
+    BwdProblem bp;
+    dlcStatus_t st = resolve_bwd(dxd, dx, wd, w, cd, dyd, dy, 0, false, bp);
+    if (st != DLC_STATUS_SUCCESS) return st;
+    *kernel = dlc_dgrad_variant(h, bp);
+    return DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlcGetConvolutionBackwardFilterKernel(dlcHandle_t h, dlcTensorDescriptor_t xd,
+                                                  const void *x, dlcTensorDescriptor_t dyd,
+                                                  const void *dy, dlcConvolutionDescriptor_t cd,
+                                                  dlcFilterDescriptor_t dwd, const void *dw,
+                                                  dlcKernel_t *kernel) {
+    if (!h) return DLC_STATUS_NOT_INITIALIZED;
+    if (!kernel) return DLC_STATUS_BAD_PARAM;
+    BwdProblem bp;
+    dlcStatus_t st = resolve_bwd(xd, x, dwd, dw, cd, dyd, dy, 1, false, bp);
+    if (st != DLC_STATUS_SUCCESS) return st;
+    *kernel = dlc_wgrad_variant(h, bp);
+    return DLC_STATUS_SUCCESS;
 }
 
 dlcStatus_t dlcDebugWaitTimeoutSelfTest(dlcHandle_t h, int timeout_us) {

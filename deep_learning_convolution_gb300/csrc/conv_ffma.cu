@@ -1,11 +1,13 @@
-// conv_ffma.cu -- strict FP32 direct convolution on CUDA cores.
+// conv_ffma.cu -- strict FP32 (and FP64) direct convolution on CUDA cores.
 //
 // Each thread owns output elements; the receptive-field dot product of the
 // maxDNN page's method section is accumulated with fused multiply-adds in
 // FP32, in the order c, r, s.  Taps that fall in the padding are skipped
 // (x reads as zero there).  No packing and no workspace (zero-memory-overhead
 // direct convolution page, method section).  Any strides, any layout, FP32 or
-// BF16 storage (BF16 is widened exactly to FP32 before the products).
+// BF16 storage (BF16 is widened exactly to FP32 before the products).  FP64
+// math (DOUBLE storage; the cuDNN page's method section offers double
+// precision) runs the same loop with double fused multiply-adds.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -36,6 +38,52 @@ __device__ __forceinline__ float load_f32<float>(const float *p, long long off) 
 template <>
 __device__ __forceinline__ float load_f32<unsigned short>(const unsigned short *p, long long off) {
     return __uint_as_float(static_cast<unsigned int>(__ldg(p + off)) << 16);
+}
+
+// FP64 problems: every value, product and sum in double.
+__global__ void __launch_bounds__(256) conv_fprop_dfma_kernel(const __grid_constant__ FfmaParams p) {
+    const double *x = static_cast<const double *>(p.x);
+    const double *w = static_cast<const double *>(p.w);
+    double *y = static_cast<double *>(p.y);
+    const long long total = (long long)p.N * p.K * p.P * p.Q;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        long long t = idx;
+        int n, k, op, oq;
+        if (p.k_fastest) {
+            k = (int)(t % p.K); t /= p.K;
+            oq = (int)(t % p.Q); t /= p.Q;
+            op = (int)(t % p.P); t /= p.P;
+            n = (int)t;
+        } else {
+            oq = (int)(t % p.Q); t /= p.Q;
+            op = (int)(t % p.P); t /= p.P;
+            k = (int)(t % p.K); t /= p.K;
+            n = (int)t;
+        }
+        const double *xn = x + (long long)n * p.xs[0];
+        const double *wk = w + (long long)k * p.ws[0];
+        double acc = 0.0;
+        for (int c = 0; c < p.C; ++c) {
+            for (int r = 0; r < p.R; ++r) {
+                const int h = op * p.u + r * p.dh - p.pt;
+                if (h < 0 || h >= p.H) continue;
+                for (int s = 0; s < p.S; ++s) {
+                    const int wi = oq * p.v + s * p.dw - p.pl;
+                    if (wi < 0 || wi >= p.W) continue;
+                    acc = __fma_rn(__ldg(xn + c * p.xs[1] + h * p.xs[2] + wi * p.xs[3]),
+                                   __ldg(wk + c * p.ws[1] + r * p.ws[2] + s * p.ws[3]), acc);
+                }
+            }
+        }
+        const long long yo = (long long)n * p.ys[0] + (long long)k * p.ys[1] +
+                             (long long)op * p.ys[2] + (long long)oq * p.ys[3];
+        double val = (double)p.alpha * acc;
+        if (p.beta != 0.f) val = __fma_rn((double)p.beta, y[yo], val);
+        if (p.bias) val += (double)__ldg(p.bias + k);
+        if (p.relu) val = fmax(val, 0.0);
+        y[yo] = val;
+    }
 }
 
 template <typename TI, typename TO>
@@ -123,7 +171,11 @@ dlcStatus_t dlc_launch_ffma(dlcContext *ctx, const ConvProblem &pb) {
     if (grid < 1) grid = 1;
     cudaError_t e;
     const bool xb = pb.xdt == DLC_DATA_BFLOAT16, yb = pb.ydt == DLC_DATA_BFLOAT16;
-    if (!xb && !yb) e = launch<float, float>(fp, grid, ctx->stream);
+    if (pb.xdt == DLC_DATA_DOUBLE) {
+        if (pb.ydt != DLC_DATA_DOUBLE) return DLC_STATUS_NOT_SUPPORTED;
+        conv_fprop_dfma_kernel<<<grid, 256, 0, ctx->stream>>>(fp);
+        e = cudaGetLastError();
+    } else if (!xb && !yb) e = launch<float, float>(fp, grid, ctx->stream);
     else if (!xb && yb) e = launch<float, unsigned short>(fp, grid, ctx->stream);
     else if (xb && !yb) e = launch<unsigned short, float>(fp, grid, ctx->stream);
     else e = launch<unsigned short, unsigned short>(fp, grid, ctx->stream);

@@ -56,6 +56,10 @@ struct PairParams {
     int y_tma;         // y through 2-D bulk tensor stores of 32 x 32 blocks
     int BN;            // filters per pair tile (BN/2 per CTA)
     int stages, num_kb, c_blocks, n_tiles;
+    // B operand: K-major rows of BN/2 filters (b_mn = 0), or MN-major (b_mn =
+    // 1): b_atoms boxes of 128 bytes of filters x BK reduction rows each.
+    int b_mn, b_atoms, flip;
+    uint32_t b_stage;  // bytes of one CTA's B stage
     int num_tiles;     // pair tiles: ceil(M / 256) * n_tiles
     // Split tail: tiles [full_tiles, num_tiles) -- the part of the last wave
     // that would leave most pairs idle -- are each split into tail_splits
@@ -100,8 +104,9 @@ __device__ void pair_produce(const PairParams &p, uint32_t rank, const CUtensorM
                              const CUtensorMap *tmB, uint32_t sA, uint32_t sB, uint64_t *full,
                              uint64_t *empty, const WaitCtl &ctl) {
     const int ST = p.stages;
-    const uint32_t b_half = (uint32_t)(p.BN / 2) * PROW;
+    const uint32_t b_half = p.b_stage;
     const uint32_t tx = 2u * (PA_BYTES + b_half);  // both CTAs' bytes land on the leader's barrier
+    const uint32_t atom_bytes = (uint32_t)BK * PROW;  // MN-major: BK rows of 128 bytes
     const uint32_t full0 = mapa_shared(smem_u32(full), 0);  // the leader's full barriers
     int stage = 0;
     uint32_t ph = 0;
@@ -123,7 +128,14 @@ __device__ void pair_produce(const PairParams &p, uint32_t rank, const CUtensorM
             if (rank == 0) mbar_arrive_expect_tx(&full[stage], tx);
             tma_load_im2col_4d_pair(sA + (uint32_t)stage * PA_BYTES, tmA, full0 + 8u * stage, cb * BK,
                                     wc, hc, n0, (uint16_t)(s * p.dw), (uint16_t)(r * p.dh));
-            tma_load_4d_pair(sB + (uint32_t)stage * b_half, tmB, full0 + 8u * stage, cb * BK, s, r, k0);
+            const int sc = p.flip ? p.S - 1 - s : s, rc = p.flip ? p.R - 1 - r : r;
+            if (p.b_mn) {
+                for (int a = 0; a < p.b_atoms; ++a)
+                    tma_load_4d_pair(sB + (uint32_t)stage * b_half + (uint32_t)a * atom_bytes, tmB,
+                                     full0 + 8u * stage, k0 + a * BK, sc, rc, cb * BK);
+            } else {
+                tma_load_4d_pair(sB + (uint32_t)stage * b_half, tmB, full0 + 8u * stage, cb * BK, sc, rc, k0);
+            }
             if (++stage == ST) stage = 0, ph ^= 1u;
             if (++cb == p.c_blocks) {
                 cb = 0;
@@ -138,8 +150,14 @@ __device__ void pair_mma(const PairParams &p, uint32_t tmem_base, uint32_t sA, u
                          uint64_t *full, uint64_t *empty, uint64_t *tfull, uint64_t *tempty,
                          uint64_t *mma_done, const WaitCtl &ctl) {
     const int ST = p.stages;
-    const uint32_t b_half = (uint32_t)(p.BN / 2) * PROW;
-    const uint64_t a0 = sw128_kmajor_desc(sA), b0 = sw128_kmajor_desc(sB);
+    const uint32_t b_half = p.b_stage;
+    constexpr int E = TF32 ? 4 : 2;
+    constexpr int BK = PROW / E;
+    const uint64_t a0 = sw128_kmajor_desc(sA);
+    // MN-major B: 8-row groups of K 1024 bytes apart, 128-byte column blocks
+    // of filters BK rows apart; one MMA's 32 bytes of K are 32/E rows.
+    const uint64_t b0 = p.b_mn ? sw128_mnmajor_desc(sB, (uint32_t)BK * PROW) : sw128_kmajor_desc(sB);
+    const uint32_t b_k = p.b_mn ? (32u / E) * PROW / 16u : 2u;
     const uint64_t a_step = PA_BYTES >> 4, b_step = b_half >> 4;
     int stage = 0, it = 0;
     uint32_t ph = 0;
@@ -165,9 +183,9 @@ __device__ void pair_mma(const PairParams &p, uint32_t tmem_base, uint32_t sA, u
 #pragma unroll
             for (int j = 0; j < 4; ++j) {  // 32 bytes of the 128-byte row each
                 if constexpr (TF32)
-                    umma_tf32_pair(d, ad + 2u * j, bd + 2u * j, p.idesc, acc);
+                    umma_tf32_pair(d, ad + 2u * j, bd + b_k * j, p.idesc, acc);
                 else
-                    umma_bf16_pair(d, ad + 2u * j, bd + 2u * j, p.idesc, acc);
+                    umma_bf16_pair(d, ad + 2u * j, bd + b_k * j, p.idesc, acc);
                 acc = 1;
             }
             umma_commit_pair(&empty[stage], 3);  // both CTAs' slots free once these are done
@@ -358,7 +376,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);  // same offset in both CTAs
     const int ST = p.stages;
-    const uint32_t b_half = (uint32_t)(p.BN / 2) * PROW;
+    const uint32_t b_half = p.b_stage;
     uint8_t *smA = smem;
     uint8_t *smB = smA + (size_t)ST * PA_BYTES;
     uint8_t *epi = smB + (size_t)ST * b_half;  // y staging (y_tma), 1024-aligned
@@ -482,6 +500,10 @@ dlcStatus_t dlc_launch_pair(dlcContext *ctx, const ConvProblem &pb) {
     p.c_blocks = (pb.C + BK - 1) / BK;
     p.num_kb = pb.R * pb.S * p.c_blocks;
     p.n_tiles = (pb.K + p.BN - 1) / p.BN;
+    p.flip = pb.flip;
+    p.b_mn = pb.w_mn;
+    p.b_atoms = (p.BN / 2 + BK - 1) / BK;
+    p.b_stage = p.b_mn ? (uint32_t)(p.b_atoms * BK * PROW) : (uint32_t)(p.BN / 2) * PROW;
     const long long m_pairs = (p.M + 2 * PBM - 1) / (2 * PBM);
     if (m_pairs * p.n_tiles > 0x7fffffffLL) return DLC_STATUS_NOT_SUPPORTED;
     p.num_tiles = (int)(m_pairs * p.n_tiles);
@@ -495,10 +517,10 @@ dlcStatus_t dlc_launch_pair(dlcContext *ctx, const ConvProblem &pb) {
         p.y_tma = (dense && !(ev && std::atoi(ev) == 0)) ? 1 : 0;
     }
     const int epi_bytes = p.y_tma ? PAIR_EPI_SMEM : 0;
-    const int stage_bytes = PA_BYTES + (p.BN / 2) * PROW;
+    const int stage_bytes = PA_BYTES + (int)p.b_stage;
     // slack after the barriers: one more half filter tile, so that no operand
     // read of the last stage can leave the CTA's shared memory
-    const int slack = (p.BN / 2) * PROW;
+    const int slack = (int)p.b_stage;
     int st = (PAIR_MAX_SMEM - 1024 - PAIR_BAR_AREA - slack - epi_bytes) / stage_bytes;
     p.stages = st > 8 ? 8 : st;
     if (const char *ev = std::getenv("DLC_TC_STAGES")) {
@@ -507,8 +529,8 @@ dlcStatus_t dlc_launch_pair(dlcContext *ctx, const ConvProblem &pb) {
     }
     if (p.stages < 2) return DLC_STATUS_INTERNAL_ERROR;
     const uint32_t fmt = tf32 ? 2u : 1u;
-    p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(p.BN >> 3) << 17) |
-              ((uint32_t)((2 * PBM) >> 4) << 24);
+    p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)p.b_mn << 16) |  // B MN-major
+              ((uint32_t)(p.BN >> 3) << 17) | ((uint32_t)((2 * PBM) >> 4) << 24);
     uint32_t cols = 32;
     while (cols < (uint32_t)(2 * p.BN)) cols <<= 1;
     p.tmem_cols = cols;
@@ -534,10 +556,13 @@ dlcStatus_t dlc_launch_pair(dlcContext *ctx, const ConvProblem &pb) {
                                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return DLC_STATUS_EXECUTION_FAILED;
-    const cuuint64_t wdim[4] = {(cuuint64_t)pb.C, (cuuint64_t)pb.S, (cuuint64_t)pb.R, (cuuint64_t)pb.K};
+    // K-major: {C, S, R, K} with a box of BK channels x BN/2 filters; MN-major
+    // (transposed filters): {K, S, R, C} with boxes of BK filters x BK channels
+    const cuuint64_t wdim[4] = {(cuuint64_t)(p.b_mn ? pb.K : pb.C), (cuuint64_t)pb.S, (cuuint64_t)pb.R,
+                                (cuuint64_t)(p.b_mn ? pb.C : pb.K)};
     const cuuint64_t wstr[3] = {(cuuint64_t)(pb.ws[3] * e), (cuuint64_t)(pb.ws[2] * e),
-                                (cuuint64_t)(pb.ws[0] * e)};
-    const cuuint32_t box[4] = {(cuuint32_t)BK, 1, 1, (cuuint32_t)(p.BN / 2)};
+                                (cuuint64_t)(pb.ws[p.b_mn ? 1 : 0] * e)};
+    const cuuint32_t box[4] = {(cuuint32_t)BK, 1, 1, (cuuint32_t)(p.b_mn ? BK : p.BN / 2)};
     const cuuint32_t ones[4] = {1, 1, 1, 1};
     r = ctx->encode_tiled(&tb, dt, 4, const_cast<void *>(pb.w), wdim, wstr, box, ones,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -1238,13 +1238,22 @@ bool y_tma_ok(const ConvProblem &pb) {
 
 }  // namespace
 
+bool dlc_im2col_ok(const ConvProblem &pb) { return tc_math_ok(pb) && im2col_ok(pb); }
+
 dlcKernel_t dlc_tc_variant(const dlcContext *ctx, const ConvProblem &pb) {
     if (!tc_math_ok(pb)) return DLC_KERNEL_NONE;
     if (!fits_i32((long long)pb.P * pb.Q)) return DLC_KERNEL_NONE;
-    if (im2col_ok(pb)) return dlc_pair_enabled(ctx) ? DLC_KERNEL_TC_IM2COL_PAIR : DLC_KERNEL_TC_IM2COL;
+    // Convolution mode (pb.flip): the SM-pair kernel mirrors its filter-load
+    // coordinates; the window and gather kernels read a mirrored strided view
+    // of the filters; the single-SM im2col and run-gather kernels, whose filter
+    // loads assume forward order, are not used.
+    if (im2col_ok(pb)) {
+        if (dlc_pair_enabled(ctx)) return DLC_KERNEL_TC_IM2COL_PAIR;
+        if (!pb.flip) return DLC_KERNEL_TC_IM2COL;
+    }
     if (dlc_window_ok(pb)) return DLC_KERNEL_TC_WINDOW;
     int a, b, c;
-    if (runs_ok(pb, &a, &b, &c)) return DLC_KERNEL_TC_GATHER_RUNS;
+    if (!pb.flip && runs_ok(pb, &a, &b, &c)) return DLC_KERNEL_TC_GATHER_RUNS;
     return DLC_KERNEL_TC_GATHER;
 }
 

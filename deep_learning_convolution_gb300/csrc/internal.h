@@ -26,6 +26,7 @@ struct dlcConvolutionStruct {
     int pad_top = 0, pad_bottom = 0, pad_left = 0, pad_right = 0;
     int u = 1, v = 1, dil_h = 1, dil_w = 1;
     dlcMathType_t math = DLC_MATH_FP32;
+    dlcConvolutionMode_t mode = DLC_CROSS_CORRELATION;
 };
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -59,6 +60,10 @@ struct dlcContext {
 // (at most the shared memory of one CTA).
 #define DLC_WPACK_BYTES (256 * 1024)
 
+inline int dlc_dtype_bytes(dlcDataType_t t) {
+    return t == DLC_DATA_BFLOAT16 ? 2 : (t == DLC_DATA_DOUBLE ? 8 : 4);
+}
+
 // A fully resolved forward problem (validated by the API layer).
 struct ConvProblem {
     int N, C, H, W, K, R, S, P, Q;
@@ -76,7 +81,40 @@ struct ConvProblem {
     const float *bias;
     float alpha, beta;
     int relu;
+    // Filter taps read mirrored, w[k, c, R-1-r, S-1-s] (convolution mode, and
+    // the data gradient's transposed filters).
+    int flip = 0;
+    // Filters given transposed: ws[0] is the stride of the output-channel
+    // index k and must be 1 (contiguous), ws[1] that of the reduction channel
+    // c.  The data gradient's problem reads the forward filters this way.
+    int w_mn = 0;
 };
+
+// A fully resolved backward problem (validated by the API layer), in the
+// forward problem's terms: x [N,C,H,W], w [K,C,R,S], dy [N,K,P,Q].  For the
+// data gradient x is the output dx; for the filter gradient w is the output dw.
+struct BwdProblem {
+    int N, C, H, W, K, R, S, P, Q;
+    int pt, pb, pl, pr, u, v, dh, dw;
+    dlcMathType_t math;
+    dlcDataType_t in_dt;   // storage of the two inputs
+    dlcDataType_t out_dt;  // storage of the output
+    dlcTensorFormat_t wfmt;
+    int flip;              // convolution mode: the forward read w[k,c,R-1-r,S-1-s]
+    const void *x;
+    int64_t xs[4];         // n, c, h, w
+    const void *w;
+    int64_t ws[4];         // k, c, r, s
+    const void *dy;
+    int64_t dys[4];        // n, k, p, q
+    double alpha, beta;
+};
+
+// conv_bwd.cu: data and filter gradients.
+dlcKernel_t dlc_dgrad_variant(const dlcContext *ctx, const BwdProblem &bp);
+dlcStatus_t dlc_launch_dgrad(dlcContext *ctx, const BwdProblem &bp);
+dlcKernel_t dlc_wgrad_variant(const dlcContext *ctx, const BwdProblem &bp);
+dlcStatus_t dlc_launch_wgrad(dlcContext *ctx, const BwdProblem &bp);
 
 // Kernel launchers (conv_ffma.cu, conv_tc.cu).  They return SUCCESS or an
 // error status and count launches in ctx->launches.
@@ -93,6 +131,8 @@ bool dlc_pair_enabled(const dlcContext *ctx);
 // them (programmatic dependent launch) unless DLC_PDL=0.
 bool dlc_pdl_enabled();
 dlcStatus_t dlc_launch_pair(dlcContext *ctx, const ConvProblem &pb);
+// conv_tc.cu: conditions of the TMA im2col lowering (single CTA and pairs).
+bool dlc_im2col_ok(const ConvProblem &pb);
 // Each loads every kernel of its translation unit into the current context
 // (CUDA loads modules lazily by default, and a module load allocates device
 // memory): the allocation-free entry point calls them at its per-device set-up.

@@ -472,4 +472,18 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
            | (static_cast<uint64_t>(2) << 61);                // 128-byte swizzle
 }
 
+// Shared-memory matrix descriptor for an MN-major operand tile stored with
+// the 128-byte swizzle: each 128-byte row holds consecutive M/N elements of
+// one K index, 8-row groups of K are 1024 bytes apart (stride offset), and
+// the next 128 bytes of M/N start `mn_block` bytes further (leading offset).
+// Tile base 1024-byte aligned; `saddr` may be advanced by whole 1024-byte row
+// groups to select a K slice.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr, uint32_t mn_block) {
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu)
+           | (static_cast<uint64_t>((mn_block >> 4) & 0x3FFFu) << 16)
+           | (static_cast<uint64_t>(1024 >> 4) << 32)
+           | (static_cast<uint64_t>(1) << 46)
+           | (static_cast<uint64_t>(2) << 61);
+}
+
 }  // namespace dlc

@@ -69,10 +69,11 @@ typedef enum {
 } dlcStatus_t;
 
 /* Storage type of x, w and y.  x and w must share it; y may be FLOAT or
- * BFLOAT16 independently.  Bias is always FLOAT. */
+ * BFLOAT16 independently (DOUBLE with DOUBLE inputs).  Bias is always FLOAT. */
 typedef enum {
     DLC_DATA_FLOAT = 0,
-    DLC_DATA_BFLOAT16 = 1
+    DLC_DATA_BFLOAT16 = 1,
+    DLC_DATA_DOUBLE = 2
 } dlcDataType_t;
 
 /* Layouts.  For activations NCHW / NHWC; for filters NCHW means KCRS and NHWC
@@ -82,14 +83,26 @@ typedef enum {
     DLC_TENSOR_NHWC = 1
 } dlcTensorFormat_t;
 
-/* Arithmetic.  FP32: FP32 products and sums on CUDA cores (FFMA), any storage
- * type.  TF32: tensor cores, FLOAT storage read as TF32, FP32 accumulation.
- * BF16: tensor cores, BFLOAT16 storage, FP32 accumulation. */
+/* Arithmetic.  FP32: FP32 products and sums on CUDA cores (FFMA), FLOAT or
+ * BFLOAT16 storage.  TF32: tensor cores, FLOAT storage read as TF32, FP32
+ * accumulation.  BF16: tensor cores, BFLOAT16 storage, FP32 accumulation.
+ * FP64: double-precision products and sums on CUDA cores (DFMA), DOUBLE
+ * storage throughout (the cuDNN page's method section: routines in single and
+ * double precision). */
 typedef enum {
     DLC_MATH_FP32 = 0,
     DLC_MATH_TF32 = 1,
-    DLC_MATH_BF16 = 2
+    DLC_MATH_BF16 = 2,
+    DLC_MATH_FP64 = 3
 } dlcMathType_t;
+
+/* Filter orientation (cuDNN page, method section).  CROSS_CORRELATION sums
+ * x[.., p*u + r*dh - pad_top, ..] * w[k,c,r,s] (the default, the formula at the
+ * top of this file); CONVOLUTION mirrors the filter taps, w[k,c,R-1-r,S-1-s]. */
+typedef enum {
+    DLC_CROSS_CORRELATION = 0,
+    DLC_CONVOLUTION = 1
+} dlcConvolutionMode_t;
 
 typedef enum {
     DLC_ACTIVATION_IDENTITY = 0,
@@ -109,9 +122,13 @@ typedef enum {
                                      (v*C*element size <= 64 bytes, no horizontal dilation,
                                      K <= 256): lowered rows read in place from packed input
                                      rows in shared memory */
-    DLC_KERNEL_TC_IM2COL_PAIR = 6 /* the TC_IM2COL lowering on pairs of SMs (a cluster of two
+    DLC_KERNEL_TC_IM2COL_PAIR = 6, /* the TC_IM2COL lowering on pairs of SMs (a cluster of two
                                      CTAs shares each MMA of 256 output pixels; each CTA
                                      loads half of the filter tile) */
+    DLC_KERNEL_DIRECT = 7,        /* backward routines and pooling: one output element per
+                                     thread, CUDA cores, any strides */
+    DLC_KERNEL_TC_WGRAD = 8       /* filter gradient on the tensor cores: pixels as the
+                                     reduction, both operands MN-major from TMA */
 } dlcKernel_t;
 
 /* Device error codes recorded by kernels (dlcGetLastDeviceError). */
@@ -229,6 +246,11 @@ dlcStatus_t dlcGetConvolution2dDescriptor(dlcConvolutionDescriptor_t desc, int *
                                           int *u, int *v, int *dilation_h, int *dilation_w,
                                           dlcMathType_t *math);
 
+/* Filter orientation (default CROSS_CORRELATION).  BAD_PARAM for another
+ * value; NOT_INITIALIZED before dlcSetConvolution2dDescriptor. */
+dlcStatus_t dlcSetConvolutionMode(dlcConvolutionDescriptor_t desc, dlcConvolutionMode_t mode);
+dlcStatus_t dlcGetConvolutionMode(dlcConvolutionDescriptor_t desc, dlcConvolutionMode_t *mode);
+
 /* ---- forward convolution ------------------------------------------------- */
 
 /* Output dimensions N, K, P, Q.  BAD_PARAM if C differs between x and w or
@@ -287,6 +309,74 @@ dlcStatus_t dlcConvolutionBiasActivationForward(dlcHandle_t handle, const float 
                                                 const float *beta, const float *bias,
                                                 dlcActivationMode_t activation,
                                                 dlcTensorDescriptor_t yDesc, void *y);
+
+/* ---- backward routines ---------------------------------------------------
+ *
+ * The cuDNN page's method section: beside the forward convolution the library
+ * offers routines for backward propagation.  They are the derivatives of the
+ * forward sum (with the descriptor's mode, pads, strides and dilations):
+ *
+ *   dx[n,c,h,w] = sum of dy[n,k,p,q] * w[k,c,r,s] over k, r, s and the outputs
+ *                 (p, q) with p*u + r*dh - pad_top = h, q*v + s*dw - pad_left = w
+ *   dw[k,c,r,s] = sum over n, p, q of dy[n,k,p,q] * x[n,c,p*u + r*dh - pad_top,
+ *                 q*v + s*dw - pad_left]   (x reads as zero outside the image)
+ *
+ * (in convolution mode w[k,c,r,s] reads w[k,c,R-1-r,S-1-s] and dw is written
+ * mirrored the same way).  The two inputs share a storage type matching the
+ * math mode as for the forward call (FP32 math: FLOAT or BFLOAT16; TF32:
+ * FLOAT; BF16: BFLOAT16; FP64: DOUBLE); the output is FLOAT or BFLOAT16 (DOUBLE
+ * for FP64).  dy's dimensions must be the forward output's (N, K, P, Q).  The
+ * output must not overlap an input (BAD_PARAM).  No workspace: the
+ * workspace-size queries return 0.  Asynchronous on the handle's stream.
+ */
+
+/* dx = alpha * dgrad(w, dy) + beta * dx (beta == 0: dx is not read).
+ * dxDesc gives N, C, H, W; wDesc K, C, R, S.  BF16 math with KRSC filters,
+ * channels-innermost dy and dx and no dilation runs on the tensor cores (one
+ * SM-pair launch per stride phase, filters read transposed); every other
+ * combination runs the direct kernel (DLC_KERNEL_DIRECT). */
+dlcStatus_t dlcConvolutionBackwardData(dlcHandle_t handle, const float *alpha,
+                                       dlcFilterDescriptor_t wDesc, const void *w,
+                                       dlcTensorDescriptor_t dyDesc, const void *dy,
+                                       dlcConvolutionDescriptor_t conv, const float *beta,
+                                       dlcTensorDescriptor_t dxDesc, void *dx);
+
+/* dw = alpha * wgrad(x, dy) + beta * dw.  dwDesc gives K, C, R, S and the
+ * layout of dw (KCRS or KRSC) and its storage type.  A FLOAT or DOUBLE dw may
+ * be written by reductions split over CTAs whose partial sums meet in atomic
+ * adds (their order varies; see dlcSetDeterministic, which turns the split
+ * off). */
+dlcStatus_t dlcConvolutionBackwardFilter(dlcHandle_t handle, const float *alpha,
+                                         dlcTensorDescriptor_t xDesc, const void *x,
+                                         dlcTensorDescriptor_t dyDesc, const void *dy,
+                                         dlcConvolutionDescriptor_t conv, const float *beta,
+                                         dlcFilterDescriptor_t dwDesc, void *dw);
+
+dlcStatus_t dlcGetConvolutionBackwardDataWorkspaceSize(dlcHandle_t handle,
+                                                       dlcFilterDescriptor_t wDesc,
+                                                       dlcTensorDescriptor_t dyDesc,
+                                                       dlcConvolutionDescriptor_t conv,
+                                                       dlcTensorDescriptor_t dxDesc,
+                                                       size_t *bytes);
+dlcStatus_t dlcGetConvolutionBackwardFilterWorkspaceSize(dlcHandle_t handle,
+                                                         dlcTensorDescriptor_t xDesc,
+                                                         dlcTensorDescriptor_t dyDesc,
+                                                         dlcConvolutionDescriptor_t conv,
+                                                         dlcFilterDescriptor_t dwDesc,
+                                                         size_t *bytes);
+
+/* Kernel the backward calls with these descriptors would launch (diagnostic;
+ * pointers may be NULL, alignment is then taken as satisfied). */
+dlcStatus_t dlcGetConvolutionBackwardDataKernel(dlcHandle_t handle, dlcFilterDescriptor_t wDesc,
+                                                const void *w, dlcTensorDescriptor_t dyDesc,
+                                                const void *dy, dlcConvolutionDescriptor_t conv,
+                                                dlcTensorDescriptor_t dxDesc, const void *dx,
+                                                dlcKernel_t *kernel);
+dlcStatus_t dlcGetConvolutionBackwardFilterKernel(dlcHandle_t handle, dlcTensorDescriptor_t xDesc,
+                                                  const void *x, dlcTensorDescriptor_t dyDesc,
+                                                  const void *dy, dlcConvolutionDescriptor_t conv,
+                                                  dlcFilterDescriptor_t dwDesc, const void *dw,
+                                                  dlcKernel_t *kernel);
 
 /* ---- self test of the device error path ---------------------------------- */
 

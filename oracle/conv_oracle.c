@@ -455,3 +455,68 @@ int oracle_conv2d_wgrad(const double *x, const i64 *xs, const double *dy, const 
     }
     return grad_run(&g, nthreads);
 }
+
+/* The same gradients at a list of coordinates pts[i] (n,c,h,w for dx;
+ * k,c,r,s for dw), i < npts: out[i] gets the sum, bound_out[i] (if not NULL)
+ * the sum of |products|.  Returns 0, 1 on a bad argument or coordinate, 2
+ * when the forward output is empty. */
+static int grad_points(grad_problem *g, const i64 *pts, i64 npts, double *out, double *bound_out)
+{
+    if (!pts || !out)
+        return 1;
+    for (i64 i = 0; i < npts; ++i) {
+        i64 a = pts[4 * i], c = pts[4 * i + 1], i2 = pts[4 * i + 2], i3 = pts[4 * i + 3];
+        i64 e0 = g->wgrad ? g->K : g->N, e2 = g->wgrad ? g->R : g->H, e3 = g->wgrad ? g->S : g->W;
+        if (a < 0 || a >= e0 || c < 0 || c >= g->C || i2 < 0 || i2 >= e2 || i3 < 0 || i3 >= e3)
+            return 1;
+        double val, bnd;
+        if (g->wgrad)
+            wgrad_one(g, a, c, i2, i3, &val, &bnd);
+        else
+            dgrad_one(g, a, c, i2, i3, &val, &bnd);
+        out[i] = val;
+        if (bound_out)
+            bound_out[i] = bnd;
+    }
+    return 0;
+}
+
+int oracle_conv2d_dgrad_points(const double *dy, const i64 *dys, const double *w, const i64 *ws,
+                               int N, int C, int H, int W, int K, int R, int S,
+                               int pad_top, int pad_bottom, int pad_left, int pad_right,
+                               int u, int v, int dil_h, int dil_w,
+                               const i64 *pts, i64 npts, double *out, double *bound_out)
+{
+    if (!dy || !dys || !w || !ws)
+        return 1;
+    grad_problem g;
+    int rc = grad_fill(&g, N, C, H, W, K, R, S, pad_top, pad_bottom, pad_left, pad_right,
+                       u, v, dil_h, dil_w);
+    if (rc)
+        return rc;
+    g.dy = dy; g.w = w; g.x = NULL; g.out = NULL; g.bound = NULL; g.wgrad = 0;
+    for (int i = 0; i < 4; ++i) {
+        g.dys[i] = dys[i]; g.ws[i] = ws[i]; g.xs[i] = 0; g.os[i] = 0;
+    }
+    return grad_points(&g, pts, npts, out, bound_out);
+}
+
+int oracle_conv2d_wgrad_points(const double *x, const i64 *xs, const double *dy, const i64 *dys,
+                               int N, int C, int H, int W, int K, int R, int S,
+                               int pad_top, int pad_bottom, int pad_left, int pad_right,
+                               int u, int v, int dil_h, int dil_w,
+                               const i64 *pts, i64 npts, double *out, double *bound_out)
+{
+    if (!x || !xs || !dy || !dys)
+        return 1;
+    grad_problem g;
+    int rc = grad_fill(&g, N, C, H, W, K, R, S, pad_top, pad_bottom, pad_left, pad_right,
+                       u, v, dil_h, dil_w);
+    if (rc)
+        return rc;
+    g.dy = dy; g.w = NULL; g.x = x; g.out = NULL; g.bound = NULL; g.wgrad = 1;
+    for (int i = 0; i < 4; ++i) {
+        g.dys[i] = dys[i]; g.ws[i] = 0; g.xs[i] = xs[i]; g.os[i] = 0;
+    }
+    return grad_points(&g, pts, npts, out, bound_out);
+}

@@ -68,6 +68,12 @@ def load(path: Optional[str] = None):
     lib.oracle_conv2d_dgrad.argtypes = grad
     lib.oracle_conv2d_wgrad.restype = ctypes.c_int
     lib.oracle_conv2d_wgrad.argtypes = grad
+    gpts = ([_dp, _i64p, _dp, _i64p] + [ctypes.c_int] * 15
+            + [_i64p, ctypes.c_longlong, _dp, _dp])
+    lib.oracle_conv2d_dgrad_points.restype = ctypes.c_int
+    lib.oracle_conv2d_dgrad_points.argtypes = gpts
+    lib.oracle_conv2d_wgrad_points.restype = ctypes.c_int
+    lib.oracle_conv2d_wgrad_points.argtypes = gpts
     if path is None:
         _lib = lib
     return lib
@@ -255,6 +261,54 @@ def conv2d_wgrad(x: np.ndarray, dy: np.ndarray, filt_rs: Tuple[int, int], *, pad
     if rc != 0:
         raise ValueError(f"oracle_conv2d_wgrad returned {rc}")
     return dw, bound
+
+
+def conv2d_dgrad_points(dy: np.ndarray, w: np.ndarray, in_hw: Tuple[int, int], pts: np.ndarray,
+                        *, pads=(0, 0, 0, 0), stride=(1, 1), dilation=(1, 1),
+                        lib=None) -> Tuple[np.ndarray, np.ndarray]:
+    """dx of :func:`conv2d_dgrad` at coordinates ``pts`` (int64 [n,4]:
+    n,c,h,w).  Returns (values, bound)."""
+    lib = lib or load()
+    dy = _as_f64_view(dy, "dy")
+    w = _as_f64_view(w, "w")
+    N, K, P, Q = dy.shape
+    _, C, R, S = w.shape
+    H, W = in_hw
+    pts = np.ascontiguousarray(pts, dtype=np.int64).reshape(-1, 4)
+    out = np.zeros(len(pts), dtype=np.float64)
+    bnd = np.zeros(len(pts), dtype=np.float64)
+    pt, pb, pl, pr = pads
+    rc = lib.oracle_conv2d_dgrad_points(
+        _ptr(dy), _strides(dy).ctypes.data_as(_i64p), _ptr(w), _strides(w).ctypes.data_as(_i64p),
+        N, C, H, W, K, R, S, pt, pb, pl, pr, stride[0], stride[1], dilation[0], dilation[1],
+        pts.ctypes.data_as(_i64p), len(pts), _ptr(out), _ptr(bnd))
+    if rc != 0:
+        raise ValueError(f"oracle_conv2d_dgrad_points returned {rc}")
+    return out, bnd
+
+
+def conv2d_wgrad_points(x: np.ndarray, dy: np.ndarray, filt_rs: Tuple[int, int], pts: np.ndarray,
+                        *, pads=(0, 0, 0, 0), stride=(1, 1), dilation=(1, 1),
+                        lib=None) -> Tuple[np.ndarray, np.ndarray]:
+    """dw of :func:`conv2d_wgrad` at coordinates ``pts`` (int64 [n,4]:
+    k,c,r,s).  Returns (values, bound)."""
+    lib = lib or load()
+    x = _as_f64_view(x, "x")
+    dy = _as_f64_view(dy, "dy")
+    N, C, H, W = x.shape
+    _, K, P, Q = dy.shape
+    R, S = filt_rs
+    pts = np.ascontiguousarray(pts, dtype=np.int64).reshape(-1, 4)
+    out = np.zeros(len(pts), dtype=np.float64)
+    bnd = np.zeros(len(pts), dtype=np.float64)
+    pt, pb, pl, pr = pads
+    rc = lib.oracle_conv2d_wgrad_points(
+        _ptr(x), _strides(x).ctypes.data_as(_i64p), _ptr(dy), _strides(dy).ctypes.data_as(_i64p),
+        N, C, H, W, K, R, S, pt, pb, pl, pr, stride[0], stride[1], dilation[0], dilation[1],
+        pts.ctypes.data_as(_i64p), len(pts), _ptr(out), _ptr(bnd))
+    if rc != 0:
+        raise ValueError(f"oracle_conv2d_wgrad_points returned {rc}")
+    return out, bnd
 
 
 if __name__ == "__main__":  # pragma: no cover

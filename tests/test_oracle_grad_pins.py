@@ -102,8 +102,26 @@ def _brute_force_element(lib):
         assert abs(dx[0, c, h, wi] - acc) <= 1e-13 and abs(bnd[0, c, h, wi] - b) <= 1e-13
 
 
+def _points(lib):
+    """The point evaluators give the full (pinned) gradients at every
+    coordinate, listed in a shuffled order."""
+    for cfg in (CONFIGS[0], CONFIGS[3]):
+        x, w, kw, rng = _case(cfg, 17)
+        y, _ = oracle.conv2d_fprop(x, w, lib=lib, **kw)
+        dy = rng.uniform(-1, 1, y.shape)
+        dx, bx = oracle.conv2d_dgrad(dy, w, x.shape[2:], lib=lib, **kw)
+        dw, bw = oracle.conv2d_wgrad(x, dy, w.shape[2:], lib=lib, **kw)
+        px = rng.permutation(np.argwhere(np.ones(dx.shape, bool)))
+        pw = rng.permutation(np.argwhere(np.ones(dw.shape, bool)))
+        v, b = oracle.conv2d_dgrad_points(dy, w, x.shape[2:], px, lib=lib, **kw)
+        assert np.array_equal(v, dx[tuple(px.T)]) and np.array_equal(b, bx[tuple(px.T)])
+        v, b = oracle.conv2d_wgrad_points(x, dy, w.shape[2:], pw, lib=lib, **kw)
+        assert np.array_equal(v, dw[tuple(pw.T)]) and np.array_equal(b, bw[tuple(pw.T)])
+
+
 PIN_BATTERY = [lambda lib, c=c: _adjoint(lib, c) for c in CONFIGS] + \
-              [lambda lib, c=c: _torch(lib, c) for c in CONFIGS] + [_one_by_one, _brute_force_element]
+              [lambda lib, c=c: _torch(lib, c) for c in CONFIGS] + [_one_by_one, _brute_force_element,
+                                                                   _points]
 
 
 @pytest.mark.parametrize("cfg", CONFIGS, ids=lambda c: "x".join(map(str, c[:7])))
@@ -124,7 +142,13 @@ def test_dgrad_element_matches_enumeration():
     _brute_force_element(oracle.load())
 
 
+def test_point_evaluators_match_full_gradients():
+    _points(oracle.load())
+
+
 MUTANTS = {
+    "points_coordinate_order": ("i64 a = pts[4 * i], c = pts[4 * i + 1],",
+                                "i64 c = pts[4 * i], a = pts[4 * i + 1],"),
     "dgrad_stride_divisibility_dropped": ("if (tp < 0 || tp % g->u != 0)", "if (tp < 0)"),
     "dgrad_dilation_ignored": ("i64 tp = h + g->pt - r * g->dh;", "i64 tp = h + g->pt - r;"),
     "dgrad_pad_side": ("i64 tq = wi + g->pl - s * g->dw;", "i64 tq = wi - g->pl - s * g->dw;"),
