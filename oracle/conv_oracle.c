@@ -250,7 +250,7 @@ int oracle_conv2d_fprop_points(const double *x, const i64 *xs, const double *w, 
 }
 
 /* ------------------------------------------------------------------------
- * Backward passes (the next rows of the path; no kernel yet).
+ * Backward passes (the data and filter gradients).
  *
  * "cuDNN: Efficient Primitives for Deep Learning", method section: the
  * library offers, beside the forward convolution, routines for the gradients
@@ -519,4 +519,107 @@ int oracle_conv2d_wgrad_points(const double *x, const i64 *xs, const double *dy,
         g.dys[i] = dys[i]; g.ws[i] = 0; g.xs[i] = xs[i]; g.os[i] = 0;
     }
     return grad_points(&g, pts, npts, out, bound_out);
+}
+
+/* ------------------------------------------------------------------------
+ * Pooling and activation forward (the cuDNN page's one-line summary and
+ * method section: pooling and activation functions are the library's other
+ * primitives, beside convolution).
+ *
+ *   pooling:    y[n,c,p,q] = alpha * POOL over the window rows
+ *               h = p*u - pad_top + i (i < R) and columns w = q*v - pad_left + j
+ *               (j < S) that lie inside the image of x[n,c,h,w]
+ *               + beta * y_in[n,c,p,q]
+ *     POOL = the largest value (mode 0), the sum divided by R*S (mode 1:
+ *     padding counted as zeros) or by the number of in-image elements (mode
+ *     2: padding excluded).  Output extent as the convolution's (floor), with
+ *     every pad smaller than the window so that no window is empty.
+ *   activation: y = alpha * f(x) + beta * y_in elementwise, f one of
+ *     identity (0), max(0, x) (1), 1 / (1 + e^-x) (2), tanh x (3),
+ *     min(max(0, x), coef) (4).
+ * FP64 throughout; strided addressing as above.
+ * ------------------------------------------------------------------------ */
+
+int oracle_pool2d_fprop(const double *x, const i64 *xs, double *y, const i64 *ys,
+                        int N, int C, int H, int W, int R, int S,
+                        int pad_top, int pad_bottom, int pad_left, int pad_right, int u, int v,
+                        int mode, double alpha, double beta, const double *y_in)
+{
+    if (!x || !xs || !y || !ys || N <= 0 || C <= 0 || H <= 0 || W <= 0 || R <= 0 || S <= 0)
+        return 1;
+    if (mode < 0 || mode > 2 || pad_top >= R || pad_bottom >= R || pad_left >= S || pad_right >= S)
+        return 1;
+    i64 P = oracle_out_extent(H, pad_top, pad_bottom, R, 1, u);
+    i64 Q = oracle_out_extent(W, pad_left, pad_right, S, 1, v);
+    if (P <= 0 || Q <= 0)
+        return 2;
+    for (i64 n = 0; n < N; ++n)
+        for (i64 c = 0; c < C; ++c)
+            for (i64 p = 0; p < P; ++p)
+                for (i64 q = 0; q < Q; ++q) {
+                    double acc = 0.0;
+                    i64 count = 0;
+                    int first = 1;
+                    for (i64 i = 0; i < R; ++i) {
+                        i64 h = p * u - pad_top + i;
+                        if (h < 0 || h >= H)
+                            continue;
+                        for (i64 j = 0; j < S; ++j) {
+                            i64 wi = q * v - pad_left + j;
+                            if (wi < 0 || wi >= W)
+                                continue;
+                            double xv = x[n * xs[0] + c * xs[1] + h * xs[2] + wi * xs[3]];
+                            if (mode == 0) {
+                                if (first || xv > acc)
+                                    acc = xv;
+                                first = 0;
+                            } else {
+                                acc += xv;
+                            }
+                            ++count;
+                        }
+                    }
+                    if (mode == 1)
+                        acc /= (double)(R * S);
+                    else if (mode == 2)
+                        acc /= (double)count;
+                    i64 yo = n * ys[0] + c * ys[1] + p * ys[2] + q * ys[3];
+                    double val = alpha * acc;
+                    if (beta != 0.0 && y_in)
+                        val += beta * y_in[yo];
+                    y[yo] = val;
+                }
+    return 0;
+}
+
+static double oracle_act(int mode, double xv, double coef)
+{
+    switch (mode) {
+        case 0: return xv;
+        case 1: return xv > 0.0 ? xv : 0.0;
+        case 2: return 1.0 / (1.0 + exp(-xv));
+        case 3: return tanh(xv);
+        case 4: return xv < 0.0 ? 0.0 : (xv > coef ? coef : xv);
+    }
+    return 0.0;
+}
+
+int oracle_activation_fprop(const double *x, const i64 *xs, double *y, const i64 *ys,
+                            int N, int C, int H, int W, int mode, double coef,
+                            double alpha, double beta, const double *y_in)
+{
+    if (!x || !xs || !y || !ys || N <= 0 || C <= 0 || H <= 0 || W <= 0 || mode < 0 || mode > 4)
+        return 1;
+    for (i64 n = 0; n < N; ++n)
+        for (i64 c = 0; c < C; ++c)
+            for (i64 h = 0; h < H; ++h)
+                for (i64 wi = 0; wi < W; ++wi) {
+                    double xv = x[n * xs[0] + c * xs[1] + h * xs[2] + wi * xs[3]];
+                    i64 yo = n * ys[0] + c * ys[1] + h * ys[2] + wi * ys[3];
+                    double val = alpha * oracle_act(mode, xv, coef);
+                    if (beta != 0.0 && y_in)
+                        val += beta * y_in[yo];
+                    y[yo] = val;
+                }
+    return 0;
 }

@@ -8,7 +8,9 @@ It shares no code with the CUDA library.
 OpenMP runtime: plain pthreads).  ``conv2d_fprop`` takes numpy arrays in any
 layout (strides are read from the arrays) and returns FP64 y and
 bound = sum |x*w|.  ``conv2d_dgrad`` and ``conv2d_wgrad`` are the gradients of
-that sum with respect to x and w (the backward routines, no kernel yet).
+that sum with respect to x and w (the backward routines), with point
+evaluators for sampled checks.  ``pool2d_fprop`` and ``activation_fprop``
+are the pooling and activation primitives.
 """
 from __future__ import annotations
 
@@ -68,6 +70,12 @@ def load(path: Optional[str] = None):
     lib.oracle_conv2d_dgrad.argtypes = grad
     lib.oracle_conv2d_wgrad.restype = ctypes.c_int
     lib.oracle_conv2d_wgrad.argtypes = grad
+    lib.oracle_pool2d_fprop.restype = ctypes.c_int
+    lib.oracle_pool2d_fprop.argtypes = ([_dp, _i64p, _dp, _i64p] + [ctypes.c_int] * 13
+                                        + [ctypes.c_double, ctypes.c_double, _dp])
+    lib.oracle_activation_fprop.restype = ctypes.c_int
+    lib.oracle_activation_fprop.argtypes = ([_dp, _i64p, _dp, _i64p] + [ctypes.c_int] * 5
+                                            + [ctypes.c_double] * 3 + [_dp])
     gpts = ([_dp, _i64p, _dp, _i64p] + [ctypes.c_int] * 15
             + [_i64p, ctypes.c_longlong, _dp, _dp])
     lib.oracle_conv2d_dgrad_points.restype = ctypes.c_int
@@ -309,6 +317,57 @@ def conv2d_wgrad_points(x: np.ndarray, dy: np.ndarray, filt_rs: Tuple[int, int],
     if rc != 0:
         raise ValueError(f"oracle_conv2d_wgrad_points returned {rc}")
     return out, bnd
+
+
+POOL_MODES = {"max": 0, "avg_include_pad": 1, "avg_exclude_pad": 2}
+ACT_MODES = {"identity": 0, "relu": 1, "sigmoid": 2, "tanh": 3, "clipped_relu": 4}
+
+
+def pool2d_fprop(x: np.ndarray, window: Tuple[int, int], *, mode: str = "max",
+                 pads=(0, 0, 0, 0), stride=(1, 1), alpha: float = 1.0, beta: float = 0.0,
+                 y_in: Optional[np.ndarray] = None, lib=None) -> np.ndarray:
+    """Pooling forward on an [N,C,H,W]-indexed FP64 array (any strides):
+    returns y [N,C,P,Q]; ``pads`` = (top, bottom, left, right), each smaller
+    than the window."""
+    lib = lib or load()
+    x = _as_f64_view(x, "x")
+    N, C, H, W = x.shape
+    R, S = window
+    pt, pb, pl, pr = pads
+    P = out_extent(H, pt, pb, R, 1, stride[0], lib)
+    Q = out_extent(W, pl, pr, S, 1, stride[1], lib)
+    if P <= 0 or Q <= 0:
+        raise ValueError("empty pooling output")
+    y = np.zeros((N, C, P, Q), dtype=np.float64)
+    if y_in is not None:
+        y_in = np.ascontiguousarray(y_in, dtype=np.float64).reshape(N, C, P, Q)
+    rc = lib.oracle_pool2d_fprop(_ptr(x), _strides(x).ctypes.data_as(_i64p), _ptr(y),
+                                 _strides(y).ctypes.data_as(_i64p), N, C, H, W, R, S,
+                                 pt, pb, pl, pr, stride[0], stride[1], POOL_MODES[mode],
+                                 float(alpha), float(beta), _ptr(y_in))
+    if rc != 0:
+        raise ValueError(f"oracle_pool2d_fprop returned {rc}")
+    return y
+
+
+def activation_fprop(x: np.ndarray, *, mode: str = "relu", coef: float = 0.0,
+                     alpha: float = 1.0, beta: float = 0.0, y_in: Optional[np.ndarray] = None,
+                     lib=None) -> np.ndarray:
+    """Activation forward y = alpha * f(x) + beta * y_in on an [N,C,H,W]-indexed
+    FP64 array (any strides); returns y [N,C,H,W]."""
+    lib = lib or load()
+    x = _as_f64_view(x, "x")
+    N, C, H, W = x.shape
+    y = np.zeros((N, C, H, W), dtype=np.float64)
+    if y_in is not None:
+        y_in = np.ascontiguousarray(y_in, dtype=np.float64).reshape(N, C, H, W)
+    rc = lib.oracle_activation_fprop(_ptr(x), _strides(x).ctypes.data_as(_i64p), _ptr(y),
+                                     _strides(y).ctypes.data_as(_i64p), N, C, H, W,
+                                     ACT_MODES[mode], float(coef), float(alpha), float(beta),
+                                     _ptr(y_in))
+    if rc != 0:
+        raise ValueError(f"oracle_activation_fprop returned {rc}")
+    return y
 
 
 if __name__ == "__main__":  # pragma: no cover

@@ -94,10 +94,12 @@ def strided_view(xt, axes: str, kind: str):
 
 def run_and_check(handle, layer, seed, *, batch=None, full=None, alpha=1.0, beta=0.0,
                   with_bias=False, relu=False, y_dtype=None, y_axes=None, expect_kernel=None,
-                  guard=True, points=65536, view=None, w_axes=None):
+                  guard=True, points=65536, view=None, w_axes=None, mode="cross_correlation"):
     """Runs one layer on the GPU and checks it against the oracle.
     `view` stores x as a strided view (see strided_view); `w_axes` overrides
-    the filter layout.  Returns the kernel name the library chose."""
+    the filter layout; `mode` "convolution" mirrors the filter taps (checked
+    against the oracle run on the mirrored filters).  Returns the kernel name
+    the library chose."""
     import torch
     x, w, bias = synth.make_inputs(layer, seed, batch=batch, with_bias=with_bias)
     xt, wt = api.layer_tensors(layer, x, w, "cuda")
@@ -130,7 +132,7 @@ def run_and_check(handle, layer, seed, *, batch=None, full=None, alpha=1.0, beta
         y.fill_(float("nan"))  # beta == 0 must overwrite NaN
     bias_t = torch.from_numpy(bias).cuda() if bias is not None else None
     conv = api.Conv2dForward(handle, xt, wt, y, x_axes=x_axes, w_axes=w_axes, y_axes=y_axes,
-                             math=api.math_of(layer), **kw)
+                             math=api.math_of(layer), mode=mode, **kw)
     kernel = conv.kernel(xt, wt, y)
     if expect_kernel is not None:
         assert kernel == expect_kernel, f"{layer.name}: kernel {kernel}, expected {expect_kernel}"
@@ -142,6 +144,8 @@ def run_and_check(handle, layer, seed, *, batch=None, full=None, alpha=1.0, beta
         assert (g == 12288.0).all(), f"{layer.name}: write outside y"
     yn = to_nchw(y, y_axes)
     x64, w64 = x.astype(np.float64), w.astype(np.float64)
+    if mode == "convolution":  # the definition with the filter taps mirrored
+        w64 = np.ascontiguousarray(w64[:, :, ::-1, ::-1])
     epi = dict(alpha=alpha, beta=beta, relu=relu,
                bias=None if bias is None else bias.astype(np.float64))
     y_bf16 = y_dtype == torch.bfloat16
