@@ -248,6 +248,68 @@ class Conv2dBackwardFilter(_Descriptors):
         return dw
 
 
+POOL_MODES = {"max": B.DLC_POOLING_MAX, "avg_include_pad": B.DLC_POOLING_AVERAGE_COUNT_INCLUDE_PADDING,
+              "avg_exclude_pad": B.DLC_POOLING_AVERAGE_COUNT_EXCLUDE_PADDING}
+ACT_MODES = {"identity": B.DLC_ACTIVATION_IDENTITY, "relu": B.DLC_ACTIVATION_RELU,
+             "sigmoid": B.DLC_ACTIVATION_SIGMOID, "tanh": B.DLC_ACTIVATION_TANH,
+             "clipped_relu": B.DLC_ACTIVATION_CLIPPED_RELU}
+
+
+class Pool2dForward:
+    """y = alpha * pool(x) + beta * y through dlcPoolingForward."""
+
+    def __init__(self, handle: Handle, x, y, *, window=(2, 2), mode="max", pads=(0, 0, 0, 0),
+                 stride=(2, 2), x_axes="NCHW", y_axes="NCHW"):
+        self.handle = handle
+        self.pool = B.dlcCreatePoolingDescriptor()
+        B.dlcSetPooling2dDescriptor(self.pool, POOL_MODES[mode], window[0], window[1], *pads,
+                                    stride[0], stride[1])
+        self.x_desc = B.dlcCreateTensorDescriptor()
+        self.y_desc = B.dlcCreateTensorDescriptor()
+        xs, xst = _logical(x, x_axes, "NCHW")
+        B.dlcSetTensor4dDescriptorEx(self.x_desc, _dtype_code(x), *xs, *xst)
+        ys, yst = _logical(y, y_axes, "NCHW")
+        B.dlcSetTensor4dDescriptorEx(self.y_desc, _dtype_code(y), *ys, *yst)
+
+    def output_dim(self):
+        return B.dlcGetPooling2dForwardOutputDim(self.pool, self.x_desc)
+
+    def kernel(self, x=None, y=None) -> str:
+        return B.KERNEL_NAMES[B.dlcGetPoolingForwardKernel(
+            self.handle.h, self.pool, self.x_desc, x.data_ptr() if x is not None else 0,
+            self.y_desc, y.data_ptr() if y is not None else 0)]
+
+    def __call__(self, x, y, alpha: float = 1.0, beta: float = 0.0):
+        B.dlcPoolingForward(self.handle.h, self.pool, alpha, self.x_desc, x.data_ptr(), beta,
+                            self.y_desc, y.data_ptr())
+        return y
+
+    def close(self):
+        if self.pool is not None:
+            B.dlcDestroyPoolingDescriptor(self.pool)
+            B.dlcDestroyTensorDescriptor(self.x_desc)
+            B.dlcDestroyTensorDescriptor(self.y_desc)
+            self.pool = None
+
+
+def activation_forward(handle: Handle, x, y, *, mode="relu", coef=0.0, alpha=1.0, beta=0.0,
+                       x_axes="NCHW", y_axes="NCHW"):
+    """y = alpha * f(x) + beta * y through dlcActivationForward (y may be x)."""
+    xd = B.dlcCreateTensorDescriptor()
+    yd = B.dlcCreateTensorDescriptor()
+    try:
+        xs, xst = _logical(x, x_axes, "NCHW")
+        B.dlcSetTensor4dDescriptorEx(xd, _dtype_code(x), *xs, *xst)
+        ys, yst = _logical(y, y_axes, "NCHW")
+        B.dlcSetTensor4dDescriptorEx(yd, _dtype_code(y), *ys, *yst)
+        B.dlcActivationForward(handle.h, ACT_MODES[mode], coef, alpha, xd, x.data_ptr(), beta, yd,
+                               y.data_ptr())
+    finally:
+        B.dlcDestroyTensorDescriptor(xd)
+        B.dlcDestroyTensorDescriptor(yd)
+    return y
+
+
 def output_dim(x, w, *, x_axes="NCHW", w_axes="KCRS", pads=(0, 0, 0, 0), stride=(1, 1),
                dilation=(1, 1)):
     """(N, K, P, Q) from the library's descriptor call (no GPU work)."""

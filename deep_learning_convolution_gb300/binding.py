@@ -13,7 +13,8 @@ from __future__ import annotations
 
 import ctypes
 import os
-from ctypes import POINTER, byref, c_char_p, c_float, c_int, c_int64, c_size_t, c_uint64, c_void_p
+from ctypes import (POINTER, byref, c_char_p, c_double, c_float, c_int, c_int64, c_size_t,
+                    c_uint64, c_void_p)
 
 from .build import LIB_PATH
 
@@ -39,6 +40,12 @@ DLC_CROSS_CORRELATION = 0
 DLC_CONVOLUTION = 1
 DLC_ACTIVATION_IDENTITY = 0
 DLC_ACTIVATION_RELU = 1
+DLC_ACTIVATION_SIGMOID = 2
+DLC_ACTIVATION_TANH = 3
+DLC_ACTIVATION_CLIPPED_RELU = 4
+DLC_POOLING_MAX = 0
+DLC_POOLING_AVERAGE_COUNT_INCLUDE_PADDING = 1
+DLC_POOLING_AVERAGE_COUNT_EXCLUDE_PADDING = 2
 DLC_KERNEL_NONE = 0
 DLC_KERNEL_FFMA = 1
 DLC_KERNEL_TC_IM2COL = 2
@@ -48,6 +55,7 @@ DLC_KERNEL_TC_WINDOW = 5
 DLC_KERNEL_TC_IM2COL_PAIR = 6
 DLC_KERNEL_DIRECT = 7
 DLC_KERNEL_TC_WGRAD = 8
+DLC_KERNEL_POOL_NHWC = 9
 DLC_DEVERR_NONE = 0
 DLC_DEVERR_WAIT_TIMEOUT = 1
 
@@ -55,7 +63,7 @@ KERNEL_NAMES = {DLC_KERNEL_NONE: "none", DLC_KERNEL_FFMA: "ffma",
                 DLC_KERNEL_TC_IM2COL: "tc_im2col", DLC_KERNEL_TC_GATHER: "tc_gather",
                 DLC_KERNEL_TC_GATHER_RUNS: "tc_runs", DLC_KERNEL_TC_WINDOW: "tc_window",
                 DLC_KERNEL_TC_IM2COL_PAIR: "tc_im2col_pair", DLC_KERNEL_DIRECT: "direct",
-                DLC_KERNEL_TC_WGRAD: "tc_wgrad"}
+                DLC_KERNEL_TC_WGRAD: "tc_wgrad", DLC_KERNEL_POOL_NHWC: "pool_nhwc"}
 
 _h = c_void_p          # opaque handle / descriptor
 _ph = POINTER(c_void_p)
@@ -106,6 +114,14 @@ SIGNATURES = {
     "dlcGetConvolutionBackwardDataKernel": [_h, _h, c_void_p, _h, c_void_p, _h, _h, c_void_p, _pi],
     "dlcGetConvolutionBackwardFilterKernel": [_h, _h, c_void_p, _h, c_void_p, _h, _h, c_void_p,
                                               _pi],
+    "dlcCreatePoolingDescriptor": [_ph],
+    "dlcDestroyPoolingDescriptor": [_h],
+    "dlcSetPooling2dDescriptor": [_h] + [c_int] * 9,
+    "dlcGetPooling2dDescriptor": [_h] + [_pi] * 9,
+    "dlcGetPooling2dForwardOutputDim": [_h, _h, _pi, _pi, _pi, _pi],
+    "dlcPoolingForward": [_h, _h, _pf, _h, c_void_p, _pf, _h, c_void_p],
+    "dlcGetPoolingForwardKernel": [_h, _h, _h, c_void_p, _h, c_void_p, _pi],
+    "dlcActivationForward": [_h, c_int, c_double, _pf, _h, c_void_p, _pf, _h, c_void_p],
     "dlcDebugWaitTimeoutSelfTest": [_h, c_int],
     "dlcConvolutionForwardNoAlloc": [c_void_p, _pf, _h, c_void_p, _h, c_void_p, _h, _pf, _h,
                                      c_void_p, c_void_p],
@@ -387,3 +403,49 @@ def dlcGetConvolutionBackwardFilterKernel(handle, x_desc, x_ptr, dy_desc, dy_ptr
     _call("dlcGetConvolutionBackwardFilterKernel", handle, x_desc, c_void_p(x_ptr or None),
           dy_desc, c_void_p(dy_ptr or None), conv, dw_desc, c_void_p(dw_ptr or None), byref(k))
     return k.value
+
+
+def dlcCreatePoolingDescriptor():
+    d = c_void_p()
+    _call("dlcCreatePoolingDescriptor", byref(d))
+    return d
+
+
+def dlcDestroyPoolingDescriptor(d):
+    _call("dlcDestroyPoolingDescriptor", d)
+
+
+def dlcSetPooling2dDescriptor(d, mode, r, s, pt, pb, pl, pr, u, v):
+    _call("dlcSetPooling2dDescriptor", d, int(mode), int(r), int(s), int(pt), int(pb), int(pl),
+          int(pr), int(u), int(v))
+
+
+def dlcGetPooling2dDescriptor(d):
+    vals = [c_int() for _ in range(9)]
+    _call("dlcGetPooling2dDescriptor", d, *[byref(v) for v in vals])
+    return tuple(v.value for v in vals)
+
+
+def dlcGetPooling2dForwardOutputDim(d, x_desc):
+    n, c, p, q = c_int(), c_int(), c_int(), c_int()
+    _call("dlcGetPooling2dForwardOutputDim", d, x_desc, byref(n), byref(c), byref(p), byref(q))
+    return n.value, c.value, p.value, q.value
+
+
+def dlcPoolingForward(handle, pool, alpha, x_desc, x_ptr, beta, y_desc, y_ptr):
+    a, b = c_float(alpha), c_float(beta)
+    _call("dlcPoolingForward", handle, pool, byref(a), x_desc, c_void_p(x_ptr), byref(b), y_desc,
+          c_void_p(y_ptr))
+
+
+def dlcGetPoolingForwardKernel(handle, pool, x_desc, x_ptr, y_desc, y_ptr) -> int:
+    k = c_int()
+    _call("dlcGetPoolingForwardKernel", handle, pool, x_desc, c_void_p(x_ptr or None), y_desc,
+          c_void_p(y_ptr or None), byref(k))
+    return k.value
+
+
+def dlcActivationForward(handle, mode, coef, alpha, x_desc, x_ptr, beta, y_desc, y_ptr):
+    a, b = c_float(alpha), c_float(beta)
+    _call("dlcActivationForward", handle, int(mode), c_double(coef), byref(a), x_desc,
+          c_void_p(x_ptr), byref(b), y_desc, c_void_p(y_ptr))

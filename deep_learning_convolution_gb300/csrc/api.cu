@@ -610,7 +610,8 @@ dlcStatus_t dlcConvolutionBiasActivationForward(dlcHandle_t h, const float *alph
                                                 dlcConvolutionDescriptor_t cd, const float *beta,
                                                 const float *bias, dlcActivationMode_t act,
                                                 dlcTensorDescriptor_t yd, void *y) {
-    if (act != DLC_ACTIVATION_IDENTITY && act != DLC_ACTIVATION_RELU) return DLC_STATUS_BAD_PARAM;
+    if (act < DLC_ACTIVATION_IDENTITY || act > DLC_ACTIVATION_CLIPPED_RELU) return DLC_STATUS_BAD_PARAM;
+    if (act != DLC_ACTIVATION_IDENTITY && act != DLC_ACTIVATION_RELU) return DLC_STATUS_NOT_SUPPORTED;
     return forward(h, alpha, xd, x, wd, w, cd, beta, bias, act == DLC_ACTIVATION_RELU, yd, y);
 }
 
@@ -821,6 +822,167 @@ dlcStatus_t dlcGetConvolutionBackwardFilterKernel(dlcHandle_t h, dlcTensorDescri
     if (st != DLC_STATUS_SUCCESS) return st;
     *kernel = dlc_wgrad_variant(h, bp);
     return DLC_STATUS_SUCCESS;
+}
+
+// ---- pooling and activation ---------------------------------------------------
+dlcStatus_t dlcCreatePoolingDescriptor(dlcPoolingDescriptor_t *d) {
+    if (!d) return DLC_STATUS_BAD_PARAM;
+    *d = new (std::nothrow) dlcPoolingStruct();
+    return *d ? DLC_STATUS_SUCCESS : DLC_STATUS_ALLOC_FAILED;
+}
+
+dlcStatus_t dlcDestroyPoolingDescriptor(dlcPoolingDescriptor_t d) {
+    delete d;
+    return DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlcSetPooling2dDescriptor(dlcPoolingDescriptor_t d, dlcPoolingMode_t mode, int r, int s,
+                                      int pt, int pb, int pl, int pr, int u, int v) {
+    if (!d) return DLC_STATUS_BAD_PARAM;
+    if (mode != DLC_POOLING_MAX && mode != DLC_POOLING_AVERAGE_COUNT_INCLUDE_PADDING &&
+        mode != DLC_POOLING_AVERAGE_COUNT_EXCLUDE_PADDING)
+        return DLC_STATUS_BAD_PARAM;
+    const int big = 1 << 20;
+    if (r < 1 || s < 1 || u < 1 || v < 1 || r > big || s > big || u > big || v > big)
+        return DLC_STATUS_BAD_PARAM;
+    if (pt < 0 || pb < 0 || pl < 0 || pr < 0 || pt >= r || pb >= r || pl >= s || pr >= s)
+        return DLC_STATUS_BAD_PARAM;
+    d->mode = mode;
+    d->r = r; d->s = s;
+    d->pad_top = pt; d->pad_bottom = pb; d->pad_left = pl; d->pad_right = pr;
+    d->u = u; d->v = v;
+    d->set = 1;
+    return DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlcGetPooling2dDescriptor(dlcPoolingDescriptor_t d, dlcPoolingMode_t *mode, int *r,
+                                      int *s, int *pt, int *pb, int *pl, int *pr, int *u, int *v) {
+    if (!d) return DLC_STATUS_BAD_PARAM;
+    if (!d->set) return DLC_STATUS_NOT_INITIALIZED;
+    if (mode) *mode = d->mode;
+    if (r) *r = d->r;
+    if (s) *s = d->s;
+    if (pt) *pt = d->pad_top;
+    if (pb) *pb = d->pad_bottom;
+    if (pl) *pl = d->pad_left;
+    if (pr) *pr = d->pad_right;
+    if (u) *u = d->u;
+    if (v) *v = d->v;
+    return DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlcGetPooling2dForwardOutputDim(dlcPoolingDescriptor_t d, dlcTensorDescriptor_t xd,
+                                            int *n, int *c, int *p, int *q) {
+    if (!d || !xd || !n || !c || !p || !q) return DLC_STATUS_BAD_PARAM;
+    if (!d->set || !xd->set) return DLC_STATUS_NOT_INITIALIZED;
+    const int64_t P = out_extent(xd->h, d->pad_top, d->pad_bottom, d->r, 1, d->u);
+    const int64_t Q = out_extent(xd->w, d->pad_left, d->pad_right, d->s, 1, d->v);
+    if (P < 1 || Q < 1 || P > INT32_MAX || Q > INT32_MAX) return DLC_STATUS_BAD_PARAM;
+    *n = xd->n; *c = xd->c; *p = (int)P; *q = (int)Q;
+    return DLC_STATUS_SUCCESS;
+}
+
+namespace {
+dlcStatus_t resolve_pool(dlcPoolingDescriptor_t d, dlcTensorDescriptor_t xd, const void *x,
+                         dlcTensorDescriptor_t yd, const void *y, bool check_ptrs, PoolProblem &pp) {
+    if (!d || !xd || !yd) return DLC_STATUS_BAD_PARAM;
+    if (!d->set || !xd->set || !yd->set) return DLC_STATUS_NOT_INITIALIZED;
+    int n, c, p, q;
+    dlcStatus_t st = dlcGetPooling2dForwardOutputDim(d, xd, &n, &c, &p, &q);
+    if (st != DLC_STATUS_SUCCESS) return st;
+    if (yd->n != n || yd->c != c || yd->h != p || yd->w != q) return DLC_STATUS_BAD_PARAM;
+    if (!out_ok(xd->dtype, yd->dtype)) return DLC_STATUS_NOT_SUPPORTED;
+    pp.N = n; pp.C = c; pp.H = xd->h; pp.W = xd->w; pp.R = d->r; pp.S = d->s; pp.P = p; pp.Q = q;
+    pp.pt = d->pad_top; pp.pl = d->pad_left; pp.u = d->u; pp.v = d->v; pp.mode = (int)d->mode;
+    pp.xdt = xd->dtype; pp.ydt = yd->dtype;
+    for (int i = 0; i < 4; ++i) {
+        pp.xs[i] = xd->stride[i];
+        pp.ys[i] = yd->stride[i];
+    }
+    pp.x = x; pp.y = const_cast<void *>(y);
+    pp.alpha = 1.0; pp.beta = 0.0;
+    const int64_t xext[4] = {pp.N, pp.C, pp.H, pp.W}, yext[4] = {pp.N, pp.C, pp.P, pp.Q};
+    if (!strides_injective(yext, pp.ys, 4)) return DLC_STATUS_BAD_PARAM;
+    const int64_t xmax = max_offset(xext, pp.xs, 4), ymax = max_offset(yext, pp.ys, 4);
+    if (xmax >= ((int64_t)1 << 60) || ymax >= ((int64_t)1 << 60)) return DLC_STATUS_BAD_PARAM;
+    if (check_ptrs) {
+        if (!x || !y) return DLC_STATUS_BAD_PARAM;
+        const size_t ex = elt_size(pp.xdt), ey = elt_size(pp.ydt);
+        if ((uintptr_t)x % ex || (uintptr_t)y % ey) return DLC_STATUS_BAD_PARAM;
+        const uintptr_t x0 = (uintptr_t)x, y0 = (uintptr_t)y;
+        if (ranges_overlap(x0, x0 + (uintptr_t)(xmax + 1) * ex, y0, y0 + (uintptr_t)(ymax + 1) * ey))
+            return DLC_STATUS_BAD_PARAM;
+    }
+    return DLC_STATUS_SUCCESS;
+}
+}  // namespace
+
+dlcStatus_t dlcPoolingForward(dlcHandle_t h, dlcPoolingDescriptor_t d, const float *alpha,
+                              dlcTensorDescriptor_t xd, const void *x, const float *beta,
+                              dlcTensorDescriptor_t yd, void *y) {
+    if (!h) return DLC_STATUS_NOT_INITIALIZED;
+    if (!alpha || !beta) return DLC_STATUS_BAD_PARAM;
+    PoolProblem pp;
+    dlcStatus_t st = resolve_pool(d, xd, x, yd, y, true, pp);
+    if (st != DLC_STATUS_SUCCESS) return st;
+    pp.alpha = *alpha;
+    pp.beta = *beta;
+    st = pending_device_error(h);
+    if (st != DLC_STATUS_SUCCESS) return st;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return DLC_STATUS_BAD_PARAM;
+    return dlc_launch_pool(h, pp);
+}
+
+dlcStatus_t dlcGetPoolingForwardKernel(dlcHandle_t h, dlcPoolingDescriptor_t d,
+                                       dlcTensorDescriptor_t xd, const void *x,
+                                       dlcTensorDescriptor_t yd, const void *y, dlcKernel_t *kernel) {
+    if (!h) return DLC_STATUS_NOT_INITIALIZED;
+    if (!kernel) return DLC_STATUS_BAD_PARAM;
+    PoolProblem pp;
+    dlcStatus_t st = resolve_pool(d, xd, x, yd, y, false, pp);
+    if (st != DLC_STATUS_SUCCESS) return st;
+    *kernel = dlc_pool_variant(pp);
+    return DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlcActivationForward(dlcHandle_t h, dlcActivationMode_t mode, double coef,
+                                 const float *alpha, dlcTensorDescriptor_t xd, const void *x,
+                                 const float *beta, dlcTensorDescriptor_t yd, void *y) {
+    if (!h) return DLC_STATUS_NOT_INITIALIZED;
+    if (!alpha || !beta || !xd || !yd) return DLC_STATUS_BAD_PARAM;
+    if (!xd->set || !yd->set) return DLC_STATUS_NOT_INITIALIZED;
+    if (mode < DLC_ACTIVATION_IDENTITY || mode > DLC_ACTIVATION_CLIPPED_RELU) return DLC_STATUS_BAD_PARAM;
+    if (xd->n != yd->n || xd->c != yd->c || xd->h != yd->h || xd->w != yd->w) return DLC_STATUS_BAD_PARAM;
+    if (!out_ok(xd->dtype, yd->dtype)) return DLC_STATUS_NOT_SUPPORTED;
+    if (!x || !y) return DLC_STATUS_BAD_PARAM;
+    ActProblem ap;
+    ap.N = xd->n; ap.C = xd->c; ap.H = xd->h; ap.W = xd->w; ap.mode = (int)mode;
+    ap.xdt = xd->dtype; ap.ydt = yd->dtype;
+    bool same = xd->dtype == yd->dtype;
+    for (int i = 0; i < 4; ++i) {
+        ap.xs[i] = xd->stride[i];
+        ap.ys[i] = yd->stride[i];
+        same = same && ap.xs[i] == ap.ys[i];
+    }
+    const int64_t ext[4] = {ap.N, ap.C, ap.H, ap.W};
+    if (!strides_injective(ext, ap.ys, 4)) return DLC_STATUS_BAD_PARAM;
+    const int64_t xmax = max_offset(ext, ap.xs, 4), ymax = max_offset(ext, ap.ys, 4);
+    if (xmax >= ((int64_t)1 << 60) || ymax >= ((int64_t)1 << 60)) return DLC_STATUS_BAD_PARAM;
+    const size_t ex = elt_size(ap.xdt), ey = elt_size(ap.ydt);
+    if ((uintptr_t)x % ex || (uintptr_t)y % ey) return DLC_STATUS_BAD_PARAM;
+    const bool in_place = x == y && same;
+    const uintptr_t x0 = (uintptr_t)x, y0 = (uintptr_t)y;
+    if (!in_place &&
+        ranges_overlap(x0, x0 + (uintptr_t)(xmax + 1) * ex, y0, y0 + (uintptr_t)(ymax + 1) * ey))
+        return DLC_STATUS_BAD_PARAM;
+    ap.x = x; ap.y = y;
+    ap.alpha = *alpha; ap.beta = *beta; ap.coef = coef;
+    dlcStatus_t st = pending_device_error(h);
+    if (st != DLC_STATUS_SUCCESS) return st;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return DLC_STATUS_BAD_PARAM;
+    return dlc_launch_activation(h, ap);
 }
 
 dlcStatus_t dlcDebugWaitTimeoutSelfTest(dlcHandle_t h, int timeout_us) {

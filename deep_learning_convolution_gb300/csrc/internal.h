@@ -21,6 +21,14 @@ struct dlcFilterStruct {
     int k = 0, c = 0, r = 0, s = 0;
 };
 
+struct dlcPoolingStruct {
+    int set = 0;
+    dlcPoolingMode_t mode = DLC_POOLING_MAX;
+    int r = 1, s = 1;
+    int pad_top = 0, pad_bottom = 0, pad_left = 0, pad_right = 0;
+    int u = 1, v = 1;
+};
+
 struct dlcConvolutionStruct {
     int set = 0;
     int pad_top = 0, pad_bottom = 0, pad_left = 0, pad_right = 0;
@@ -109,6 +117,34 @@ struct BwdProblem {
     int64_t dys[4];        // n, k, p, q
     double alpha, beta;
 };
+
+// Pooling forward (validated): x [N,C,H,W] -> y [N,C,P,Q].
+struct PoolProblem {
+    int N, C, H, W, R, S, P, Q;
+    int pt, pl, u, v, mode;
+    dlcDataType_t xdt, ydt;
+    const void *x;
+    int64_t xs[4];
+    void *y;
+    int64_t ys[4];
+    double alpha, beta;
+};
+
+// Activation forward (validated): y = alpha * f(x) + beta * y, both [N,C,H,W].
+struct ActProblem {
+    int N, C, H, W, mode;
+    dlcDataType_t xdt, ydt;
+    const void *x;
+    int64_t xs[4];
+    void *y;
+    int64_t ys[4];
+    double alpha, beta, coef;
+};
+
+// pool_act.cu
+dlcKernel_t dlc_pool_variant(const PoolProblem &pp);
+dlcStatus_t dlc_launch_pool(dlcContext *ctx, const PoolProblem &pp);
+dlcStatus_t dlc_launch_activation(dlcContext *ctx, const ActProblem &ap);
 
 // conv_bwd.cu: data and filter gradients.
 dlcKernel_t dlc_dgrad_variant(const dlcContext *ctx, const BwdProblem &bp);

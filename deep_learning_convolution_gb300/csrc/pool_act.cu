@@ -1,0 +1,369 @@
+// pool_act.cu -- pooling and activation forward.
+//
+// The cuDNN page's one-line summary and method section name pooling and
+// activation functions as the library's other primitives beside convolution,
+// with the same descriptors, arbitrary strides and caller-owned buffers.
+//
+//   pooling:    y[n,c,p,q] = alpha * POOL_{i<R, j<S, in image} x[n, c, p*u - pad_top + i,
+//                                                            q*v - pad_left + j]
+//                            + beta * y[n,c,p,q]
+//               POOL = maximum, or sum / (R*S) (padding counted), or sum / (number
+//               of in-image elements) (padding excluded); every pad is smaller than
+//               the window, so no window is empty.
+//   activation: y = alpha * f(x) + beta * y, f = identity, max(0,x), 1/(1+e^-x),
+//               tanh x or min(max(0,x), coef).
+//
+// Both are memory-bound: they read x once from DRAM and write y once, so the
+// kernels are sized for bandwidth.  With channels innermost (NHWC) each thread
+// owns 16 bytes of channels of one output pixel and reads the window's pixels
+// as 16-byte vectors (consecutive threads read consecutive bytes); dense
+// tensors of one layout run the activation as a flat array of 16-byte
+// vectors; anything else takes one element per thread through the strides.
+// Grids are a multiple of the SM count (grid-stride loops).  Sums and
+// comparisons are in FP32 (FP64 for DOUBLE storage); BF16 is widened exactly.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "internal.h"
+
+namespace {
+
+template <typename T> struct Io;
+template <> struct Io<float> {
+    using acc = float;
+    __device__ static float ld(const float *p, long long o) { return __ldg(p + o); }
+    __device__ static void st(float *p, long long o, float v) { p[o] = v; }
+};
+template <> struct Io<unsigned short> {
+    using acc = float;
+    __device__ static float ld(const unsigned short *p, long long o) {
+        return __uint_as_float(static_cast<unsigned int>(__ldg(p + o)) << 16);
+    }
+    __device__ static void st(unsigned short *p, long long o, float v) {
+        __nv_bfloat16 b = __float2bfloat16_rn(v);
+        p[o] = *reinterpret_cast<unsigned short *>(&b);
+    }
+};
+template <> struct Io<double> {
+    using acc = double;
+    __device__ static double ld(const double *p, long long o) { return __ldg(p + o); }
+    __device__ static void st(double *p, long long o, double v) { p[o] = v; }
+};
+
+struct PoolParams {
+    int N, C, H, W, R, S, P, Q;
+    int pt, pl, u, v, mode;
+    long long xs[4], ys[4];
+    const void *x;
+    void *y;
+    double alpha, beta;
+};
+
+// Widen 16 bytes of x into V accumulators.
+template <typename T, typename A, int V>
+__device__ __forceinline__ void unpack16(const uint4 &q, A (&out)[V]) {
+    if constexpr (sizeof(T) == 2) {
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            out[2 * i] = __uint_as_float(w[i] << 16);
+            out[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    } else if constexpr (sizeof(T) == 4) {
+        out[0] = __uint_as_float(q.x);
+        out[1] = __uint_as_float(q.y);
+        out[2] = __uint_as_float(q.z);
+        out[3] = __uint_as_float(q.w);
+    } else {
+        out[0] = __hiloint2double((int)q.y, (int)q.x);
+        out[1] = __hiloint2double((int)q.w, (int)q.z);
+    }
+}
+
+// Channels-innermost pooling: one thread per (output pixel, 16-byte chunk of
+// channels); C * sizeof(TI) is a multiple of 16 and both bases 16-byte aligned.
+template <typename TI, typename TO>
+__global__ void __launch_bounds__(256) pool_nhwc_kernel(const __grid_constant__ PoolParams p) {
+    using A = typename Io<TI>::acc;
+    constexpr int V = 16 / (int)sizeof(TI);
+    const TI *x = static_cast<const TI *>(p.x);
+    TO *y = static_cast<TO *>(p.y);
+    const int chunks = p.C / V;
+    const long long total = (long long)p.N * p.P * p.Q * chunks;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        long long t = idx;
+        const int ch = (int)(t % chunks); t /= chunks;
+        const int oq = (int)(t % p.Q); t /= p.Q;
+        const int op = (int)(t % p.P);
+        const int n = (int)(t / p.P);
+        A acc[V];
+        const bool is_max = p.mode == 0;
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] = is_max ? (A)-INFINITY : (A)0;
+        int count = 0;
+        const TI *xn = x + (long long)n * p.xs[0] + (long long)ch * V;
+        const int h0 = op * p.u - p.pt, w0 = oq * p.v - p.pl;
+        for (int i = 0; i < p.R; ++i) {
+            const int h = h0 + i;
+            if (h < 0 || h >= p.H) continue;
+            for (int j = 0; j < p.S; ++j) {
+                const int wi = w0 + j;
+                if (wi < 0 || wi >= p.W) continue;
+                const uint4 q4 = __ldg(reinterpret_cast<const uint4 *>(
+                    xn + (long long)h * p.xs[2] + (long long)wi * p.xs[3]));
+                A v[V];
+                unpack16<TI, A, V>(q4, v);
+#pragma unroll
+                for (int e = 0; e < V; ++e) acc[e] = is_max ? (v[e] > acc[e] ? v[e] : acc[e]) : acc[e] + v[e];
+                ++count;
+            }
+        }
+        const A div = p.mode == 1 ? (A)(p.R * p.S) : (A)count;
+        const long long yo = (long long)n * p.ys[0] + (long long)op * p.ys[2] + (long long)oq * p.ys[3] +
+                             (long long)ch * V;
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+            A val = (A)p.alpha * (is_max ? acc[e] : acc[e] / div);
+            if (p.beta != 0.0) val += (A)p.beta * (A)Io<TO>::ld(y, yo + e);
+            Io<TO>::st(y, yo + e, val);
+        }
+    }
+}
+
+// Any layout: one output element per thread, outputs enumerated with the
+// unit-stride axis of y innermost.
+template <typename TI, typename TO>
+__global__ void __launch_bounds__(256) pool_any_kernel(const __grid_constant__ PoolParams p,
+                                                       int c_fastest) {
+    using A = typename Io<TI>::acc;
+    const TI *x = static_cast<const TI *>(p.x);
+    TO *y = static_cast<TO *>(p.y);
+    const long long total = (long long)p.N * p.C * p.P * p.Q;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        long long t = idx;
+        int n, c, op, oq;
+        if (c_fastest) {
+            c = (int)(t % p.C); t /= p.C;
+            oq = (int)(t % p.Q); t /= p.Q;
+            op = (int)(t % p.P);
+            n = (int)(t / p.P);
+        } else {
+            oq = (int)(t % p.Q); t /= p.Q;
+            op = (int)(t % p.P); t /= p.P;
+            c = (int)(t % p.C);
+            n = (int)(t / p.C);
+        }
+        const bool is_max = p.mode == 0;
+        A acc = is_max ? (A)-INFINITY : (A)0;
+        int count = 0;
+        const TI *xc = x + (long long)n * p.xs[0] + (long long)c * p.xs[1];
+        for (int i = 0; i < p.R; ++i) {
+            const int h = op * p.u - p.pt + i;
+            if (h < 0 || h >= p.H) continue;
+            for (int j = 0; j < p.S; ++j) {
+                const int wi = oq * p.v - p.pl + j;
+                if (wi < 0 || wi >= p.W) continue;
+                const A v = Io<TI>::ld(xc, (long long)h * p.xs[2] + (long long)wi * p.xs[3]);
+                acc = is_max ? (v > acc ? v : acc) : acc + v;
+                ++count;
+            }
+        }
+        if (!is_max) acc /= p.mode == 1 ? (A)(p.R * p.S) : (A)count;
+        const long long yo = (long long)n * p.ys[0] + (long long)c * p.ys[1] + (long long)op * p.ys[2] +
+                             (long long)oq * p.ys[3];
+        A val = (A)p.alpha * acc;
+        if (p.beta != 0.0) val += (A)p.beta * (A)Io<TO>::ld(y, yo);
+        Io<TO>::st(y, yo, val);
+    }
+}
+
+struct ActParams {
+    int N, C, H, W, mode;
+    long long xs[4], ys[4];
+    const void *x;
+    void *y;
+    double alpha, beta, coef;
+};
+
+__device__ __forceinline__ float exp_of(float v) { return expf(v); }
+__device__ __forceinline__ double exp_of(double v) { return exp(v); }
+__device__ __forceinline__ float tanh_of(float v) { return tanhf(v); }
+__device__ __forceinline__ double tanh_of(double v) { return tanh(v); }
+
+template <typename A>
+__device__ __forceinline__ A act_fn(int mode, A v, A coef) {
+    switch (mode) {
+        case 1: return v > (A)0 ? v : (A)0;
+        case 2: return (A)1 / ((A)1 + exp_of(-v));
+        case 3: return tanh_of(v);
+        case 4: return v < (A)0 ? (A)0 : (v > coef ? coef : v);
+        default: return v;
+    }
+}
+
+// Flat path: x and y dense with the same strides (elements 0 .. n-1 of both).
+template <typename TI, typename TO>
+__global__ void __launch_bounds__(256) act_flat_kernel(const __grid_constant__ ActParams p, long long n) {
+    using A = typename Io<TI>::acc;
+    constexpr int V = 16 / (int)sizeof(TI);
+    const TI *x = static_cast<const TI *>(p.x);
+    TO *y = static_cast<TO *>(p.y);
+    const long long nv = n / V;
+    const A alpha = (A)p.alpha, beta = (A)p.beta, coef = (A)p.coef;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nv;
+         i += (long long)gridDim.x * blockDim.x) {
+        const uint4 q4 = __ldg(reinterpret_cast<const uint4 *>(x) + i);
+        A v[V];
+        unpack16<TI, A, V>(q4, v);
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+            A val = alpha * act_fn<A>(p.mode, v[e], coef);
+            if (beta != (A)0) val += beta * (A)Io<TO>::ld(y, i * V + e);
+            Io<TO>::st(y, i * V + e, val);
+        }
+    }
+    // the tail of fewer than V elements
+    for (long long i = nv * V + (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        A val = alpha * act_fn<A>(p.mode, (A)Io<TI>::ld(x, i), coef);
+        if (beta != (A)0) val += beta * (A)Io<TO>::ld(y, i);
+        Io<TO>::st(y, i, val);
+    }
+}
+
+template <typename TI, typename TO>
+__global__ void __launch_bounds__(256) act_any_kernel(const __grid_constant__ ActParams p) {
+    using A = typename Io<TI>::acc;
+    const TI *x = static_cast<const TI *>(p.x);
+    TO *y = static_cast<TO *>(p.y);
+    const long long total = (long long)p.N * p.C * p.H * p.W;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        long long t = idx;
+        const int wi = (int)(t % p.W); t /= p.W;
+        const int h = (int)(t % p.H); t /= p.H;
+        const int c = (int)(t % p.C);
+        const int n = (int)(t / p.C);
+        const long long xo = (long long)n * p.xs[0] + (long long)c * p.xs[1] + (long long)h * p.xs[2] +
+                             (long long)wi * p.xs[3];
+        const long long yo = (long long)n * p.ys[0] + (long long)c * p.ys[1] + (long long)h * p.ys[2] +
+                             (long long)wi * p.ys[3];
+        A val = (A)p.alpha * act_fn<A>(p.mode, (A)Io<TI>::ld(x, xo), (A)p.coef);
+        if (p.beta != 0.0) val += (A)p.beta * (A)Io<TO>::ld(y, yo);
+        Io<TO>::st(y, yo, val);
+    }
+}
+
+int grid_of(const dlcContext *ctx, long long work) {
+    const long long blocks = (work + 255) / 256;
+    const long long cap = (long long)ctx->sm_count * 8;
+    return (int)std::max(1LL, std::min(blocks, cap));
+}
+
+template <typename TI, typename TO>
+cudaError_t launch_pool(const dlcContext *ctx, const PoolParams &p, bool nhwc) {
+    if (nhwc) {
+        const long long work = (long long)p.N * p.P * p.Q * (p.C / (16 / (int)sizeof(TI)));
+        pool_nhwc_kernel<TI, TO><<<grid_of(ctx, work), 256, 0, ctx->stream>>>(p);
+    } else {
+        const long long work = (long long)p.N * p.C * p.P * p.Q;
+        pool_any_kernel<TI, TO><<<grid_of(ctx, work), 256, 0, ctx->stream>>>(p, p.ys[1] == 1 ? 1 : 0);
+    }
+    return cudaGetLastError();
+}
+
+template <typename TI, typename TO>
+cudaError_t launch_act(const dlcContext *ctx, const ActParams &p, long long flat_n) {
+    if (flat_n > 0) {
+        act_flat_kernel<TI, TO><<<grid_of(ctx, flat_n / (16 / (long long)sizeof(TI)) + 1), 256, 0,
+                                  ctx->stream>>>(p, flat_n);
+    } else {
+        act_any_kernel<TI, TO><<<grid_of(ctx, (long long)p.N * p.C * p.H * p.W), 256, 0, ctx->stream>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+template <template <typename, typename> class F, typename... Args>
+cudaError_t by_types(dlcDataType_t ti, dlcDataType_t to, Args &&...args) {
+    if (ti == DLC_DATA_DOUBLE && to == DLC_DATA_DOUBLE) return F<double, double>::run(args...);
+    if (ti == DLC_DATA_FLOAT && to == DLC_DATA_FLOAT) return F<float, float>::run(args...);
+    if (ti == DLC_DATA_FLOAT && to == DLC_DATA_BFLOAT16) return F<float, unsigned short>::run(args...);
+    if (ti == DLC_DATA_BFLOAT16 && to == DLC_DATA_FLOAT) return F<unsigned short, float>::run(args...);
+    if (ti == DLC_DATA_BFLOAT16 && to == DLC_DATA_BFLOAT16)
+        return F<unsigned short, unsigned short>::run(args...);
+    return cudaErrorInvalidValue;
+}
+
+template <typename TI, typename TO> struct PoolRun {
+    static cudaError_t run(const dlcContext *ctx, const PoolParams &p, bool nhwc) {
+        return launch_pool<TI, TO>(ctx, p, nhwc);
+    }
+};
+template <typename TI, typename TO> struct ActRun {
+    static cudaError_t run(const dlcContext *ctx, const ActParams &p, long long flat_n) {
+        return launch_act<TI, TO>(ctx, p, flat_n);
+    }
+};
+
+// True if the 4-D (extent, stride) pairs cover exactly the offsets 0 .. n-1.
+bool dense(const int *ext, const int64_t *str) {
+    int idx[4] = {0, 1, 2, 3};
+    std::sort(idx, idx + 4, [&](int a, int b) { return str[a] < str[b]; });
+    long long expect = 1;
+    for (int i = 0; i < 4; ++i) {
+        const int d = idx[i];
+        if (ext[d] == 1) continue;
+        if (str[d] != expect) return false;
+        expect *= ext[d];
+    }
+    return true;
+}
+
+}  // namespace
+
+dlcKernel_t dlc_pool_variant(const PoolProblem &pp) {
+    const int e = dlc_dtype_bytes(pp.xdt);
+    const bool nhwc = pp.xs[1] == 1 && pp.ys[1] == 1 && (pp.C * e) % 16 == 0 &&
+                      (pp.xs[3] * e) % 16 == 0 && (pp.xs[2] * e) % 16 == 0 && (pp.xs[0] * e) % 16 == 0 &&
+                      ((uintptr_t)pp.x % 16) == 0;
+    return nhwc ? DLC_KERNEL_POOL_NHWC : DLC_KERNEL_DIRECT;
+}
+
+dlcStatus_t dlc_launch_pool(dlcContext *ctx, const PoolProblem &pp) {
+    PoolParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.N = pp.N; p.C = pp.C; p.H = pp.H; p.W = pp.W; p.R = pp.R; p.S = pp.S; p.P = pp.P; p.Q = pp.Q;
+    p.pt = pp.pt; p.pl = pp.pl; p.u = pp.u; p.v = pp.v; p.mode = pp.mode;
+    for (int i = 0; i < 4; ++i) {
+        p.xs[i] = pp.xs[i];
+        p.ys[i] = pp.ys[i];
+    }
+    p.x = pp.x; p.y = pp.y; p.alpha = pp.alpha; p.beta = pp.beta;
+    const bool nhwc = dlc_pool_variant(pp) == DLC_KERNEL_POOL_NHWC;
+    if (by_types<PoolRun>(pp.xdt, pp.ydt, ctx, p, nhwc) != cudaSuccess) return DLC_STATUS_EXECUTION_FAILED;
+    ctx->launches += 1;
+    return DLC_STATUS_SUCCESS;
+}
+
+dlcStatus_t dlc_launch_activation(dlcContext *ctx, const ActProblem &ap) {
+    ActParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.N = ap.N; p.C = ap.C; p.H = ap.H; p.W = ap.W; p.mode = ap.mode;
+    for (int i = 0; i < 4; ++i) {
+        p.xs[i] = ap.xs[i];
+        p.ys[i] = ap.ys[i];
+    }
+    p.x = ap.x; p.y = ap.y; p.alpha = ap.alpha; p.beta = ap.beta; p.coef = ap.coef;
+    const int ext[4] = {ap.N, ap.C, ap.H, ap.W};
+    bool same = true;
+    for (int i = 0; i < 4; ++i) same = same && ap.xs[i] == ap.ys[i];
+    const long long n = (long long)ap.N * ap.C * ap.H * ap.W;
+    const long long flat = (same && dense(ext, ap.xs) && ((uintptr_t)ap.x % 16) == 0) ? n : 0;
+    if (by_types<ActRun>(ap.xdt, ap.ydt, ctx, p, flat) != cudaSuccess) return DLC_STATUS_EXECUTION_FAILED;
+    ctx->launches += 1;
+    return DLC_STATUS_SUCCESS;
+}

@@ -104,10 +104,25 @@ typedef enum {
     DLC_CONVOLUTION = 1
 } dlcConvolutionMode_t;
 
+/* Activation functions (cuDNN page, summary and method section).  The fused
+ * convolution epilogue takes IDENTITY and RELU; dlcActivationForward takes
+ * every mode: f(x) = x, max(0, x), 1 / (1 + e^-x), tanh x, min(max(0, x), coef). */
 typedef enum {
     DLC_ACTIVATION_IDENTITY = 0,
-    DLC_ACTIVATION_RELU = 1
+    DLC_ACTIVATION_RELU = 1,
+    DLC_ACTIVATION_SIGMOID = 2,
+    DLC_ACTIVATION_TANH = 3,
+    DLC_ACTIVATION_CLIPPED_RELU = 4
 } dlcActivationMode_t;
+
+/* Pooling (cuDNN page, summary and method section): the largest value of the
+ * window's in-image elements, or their sum divided by the window size (the
+ * padding counts as zeros) or by their number (the padding is excluded). */
+typedef enum {
+    DLC_POOLING_MAX = 0,
+    DLC_POOLING_AVERAGE_COUNT_INCLUDE_PADDING = 1,
+    DLC_POOLING_AVERAGE_COUNT_EXCLUDE_PADDING = 2
+} dlcPoolingMode_t;
 
 /* Which kernel a forward call launches (diagnostic). */
 typedef enum {
@@ -127,8 +142,10 @@ typedef enum {
                                      loads half of the filter tile) */
     DLC_KERNEL_DIRECT = 7,        /* backward routines and pooling: one output element per
                                      thread, CUDA cores, any strides */
-    DLC_KERNEL_TC_WGRAD = 8       /* filter gradient on the tensor cores: pixels as the
+    DLC_KERNEL_TC_WGRAD = 8,      /* filter gradient on the tensor cores: pixels as the
                                      reduction, both operands MN-major from TMA */
+    DLC_KERNEL_POOL_NHWC = 9      /* pooling with channels innermost: 16-byte vectors of
+                                     channels per thread */
 } dlcKernel_t;
 
 /* Device error codes recorded by kernels (dlcGetLastDeviceError). */
@@ -141,6 +158,7 @@ typedef struct dlcContext *dlcHandle_t;
 typedef struct dlcTensorStruct *dlcTensorDescriptor_t;
 typedef struct dlcFilterStruct *dlcFilterDescriptor_t;
 typedef struct dlcConvolutionStruct *dlcConvolutionDescriptor_t;
+typedef struct dlcPoolingStruct *dlcPoolingDescriptor_t;
 
 /* ---- library ------------------------------------------------------------ */
 
@@ -377,6 +395,54 @@ dlcStatus_t dlcGetConvolutionBackwardFilterKernel(dlcHandle_t handle, dlcTensorD
                                                   const void *dy, dlcConvolutionDescriptor_t conv,
                                                   dlcFilterDescriptor_t dwDesc, const void *dw,
                                                   dlcKernel_t *kernel);
+
+/* ---- pooling and activation forward ----------------------------------------
+ *
+ * The cuDNN page's summary and method section: pooling and activation
+ * functions beside convolution, with the same tensor descriptors (any
+ * strides) and caller-owned device buffers.  x and y may have different
+ * layouts; storage FLOAT or BFLOAT16 (independently) or DOUBLE for both.
+ * Sums and comparisons run in FP32 (FP64 for DOUBLE).  alpha and beta as for
+ * the convolution (beta == 0: y is not read).  Asynchronous on the handle's
+ * stream.  x and y must not overlap, except that dlcActivationForward may
+ * run in place (x == y with identical descriptors).
+ */
+
+dlcStatus_t dlcCreatePoolingDescriptor(dlcPoolingDescriptor_t *desc);
+dlcStatus_t dlcDestroyPoolingDescriptor(dlcPoolingDescriptor_t desc);
+
+/* Window R x S, pads (each smaller than the window along its axis, so that
+ * no window is empty), strides u, v >= 1.  BAD_PARAM otherwise. */
+dlcStatus_t dlcSetPooling2dDescriptor(dlcPoolingDescriptor_t desc, dlcPoolingMode_t mode,
+                                      int window_h, int window_w, int pad_top, int pad_bottom,
+                                      int pad_left, int pad_right, int u, int v);
+dlcStatus_t dlcGetPooling2dDescriptor(dlcPoolingDescriptor_t desc, dlcPoolingMode_t *mode,
+                                      int *window_h, int *window_w, int *pad_top,
+                                      int *pad_bottom, int *pad_left, int *pad_right, int *u,
+                                      int *v);
+
+/* Output dimensions N, C, P, Q (P = floor((H + pad_top + pad_bottom - R) / u) + 1,
+ * Q likewise). */
+dlcStatus_t dlcGetPooling2dForwardOutputDim(dlcPoolingDescriptor_t desc,
+                                            dlcTensorDescriptor_t xDesc, int *n, int *c, int *p,
+                                            int *q);
+
+/* y[n,c,p,q] = alpha * POOL(window of x[n,c]) + beta * y[n,c,p,q]. */
+dlcStatus_t dlcPoolingForward(dlcHandle_t handle, dlcPoolingDescriptor_t desc, const float *alpha,
+                              dlcTensorDescriptor_t xDesc, const void *x, const float *beta,
+                              dlcTensorDescriptor_t yDesc, void *y);
+
+/* Kernel dlcPoolingForward would launch (diagnostic; pointers may be NULL). */
+dlcStatus_t dlcGetPoolingForwardKernel(dlcHandle_t handle, dlcPoolingDescriptor_t desc,
+                                       dlcTensorDescriptor_t xDesc, const void *x,
+                                       dlcTensorDescriptor_t yDesc, const void *y,
+                                       dlcKernel_t *kernel);
+
+/* y = alpha * f(x) + beta * y elementwise; x and y of the same dimensions.
+ * coef is the ceiling of CLIPPED_RELU (ignored otherwise). */
+dlcStatus_t dlcActivationForward(dlcHandle_t handle, dlcActivationMode_t mode, double coef,
+                                 const float *alpha, dlcTensorDescriptor_t xDesc, const void *x,
+                                 const float *beta, dlcTensorDescriptor_t yDesc, void *y);
 
 /* ---- self test of the device error path ---------------------------------- */
 
