@@ -385,9 +385,20 @@ dlcStatus_t dlc_launch_dgrad(dlcContext *ctx, const BwdProblem &bp) {
     return DLC_STATUS_SUCCESS;
 }
 
-dlcKernel_t dlc_wgrad_variant(const dlcContext *, const BwdProblem &) { return DLC_KERNEL_DIRECT; }
+dlcKernel_t dlc_wgrad_variant(const dlcContext *, const BwdProblem &bp) {
+    // the tensor-core kernel writes dw in forward tap order; convolution mode
+    // (mirrored taps) takes the direct kernel
+    return (!bp.flip && dlc_wgrad_tc_ok(bp)) ? DLC_KERNEL_TC_WGRAD : DLC_KERNEL_DIRECT;
+}
 
 dlcStatus_t dlc_launch_wgrad(dlcContext *ctx, const BwdProblem &bp) {
+    if (dlc_wgrad_variant(ctx, bp) == DLC_KERNEL_TC_WGRAD) {
+        // dw = beta * dw first; the kernel adds alpha times its partial sums
+        const long long dims[4] = {bp.K, bp.C, bp.R, bp.S};
+        dlcStatus_t st = scale_any(ctx, bp.out_dt, const_cast<void *>(bp.w), dims, bp.ws, bp.beta);
+        if (st != DLC_STATUS_SUCCESS) return st;
+        return dlc_launch_wgrad_tc(ctx, bp);
+    }
     BwdParams p = params_of(bp);
     const long long elems = (long long)bp.K * bp.C * bp.R * bp.S;
     const long long red = (long long)bp.N * bp.P * bp.Q;

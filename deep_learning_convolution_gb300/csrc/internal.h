@@ -150,6 +150,9 @@ dlcStatus_t dlc_launch_activation(dlcContext *ctx, const ActProblem &ap);
 dlcKernel_t dlc_dgrad_variant(const dlcContext *ctx, const BwdProblem &bp);
 dlcStatus_t dlc_launch_dgrad(dlcContext *ctx, const BwdProblem &bp);
 dlcKernel_t dlc_wgrad_variant(const dlcContext *ctx, const BwdProblem &bp);
+// conv_wgrad.cu: the filter gradient on the tensor cores (adds into dw).
+bool dlc_wgrad_tc_ok(const BwdProblem &bp);
+dlcStatus_t dlc_launch_wgrad_tc(dlcContext *ctx, const BwdProblem &bp);
 dlcStatus_t dlc_launch_wgrad(dlcContext *ctx, const BwdProblem &bp);
 
 // Kernel launchers (conv_ffma.cu, conv_tc.cu).  They return SUCCESS or an

@@ -226,6 +226,39 @@ __device__ __forceinline__ void tma_store_2d_s(const CUtensorMap *m, uint32_t sr
         : "memory");
 }
 
+// 2-D tiled load into shared memory at a shared::cta address.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, uint64_t *bar, int c0,
+                                            int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+// im2col load (as tma_load_im2col_4d) into a shared::cta address.
+__device__ __forceinline__ void tma_load_im2col_4d(uint32_t dst, const CUtensorMap *m, uint64_t *bar,
+                                                   int c, int w, int h, int n, uint16_t w_off,
+                                                   uint16_t h_off) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.im2col.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], {%7, %8};" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c), "r"(w), "r"(h), "r"(n),
+        "h"(w_off), "h"(h_off)
+        : "memory");
+}
+
+// Bulk tensor reduce-add of a 3-D FP32 box from shared memory into global
+// memory (element-wise atomic add at the L2; out-of-tensor parts are skipped).
+__device__ __forceinline__ void tma_reduce_add_3d_s(const CUtensorMap *m, uint32_t src, int c0, int c1,
+                                                    int c2) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(m)),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
 // Bulk tensor reduce-add of a 2-D FP32 box from shared memory into global
 // memory (element-wise atomic add at the L2; out-of-tensor parts are skipped).
 __device__ __forceinline__ void tma_reduce_add_2d_s(const CUtensorMap *m, uint32_t src, int c0, int c1) {

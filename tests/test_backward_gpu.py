@@ -318,10 +318,31 @@ WGRAD = [
 ]
 
 
+WGRAD_TC = {"wg_3x3_s1_c64_k64", "wg_3x3_s2_c72_k96"}
+
+
 @pytest.mark.parametrize("layer", WGRAD, ids=lambda l: l.name)
 def test_wgrad(layer):
-    run_wgrad(layer, 730)
-    run_wgrad(layer, 731, mode="convolution", alpha=0.75, beta=0.5)
+    tc = layer.name in WGRAD_TC
+    run_wgrad(layer, 730, expect="tc_wgrad" if tc else "direct")
+    run_wgrad(layer, 731, alpha=0.75, beta=0.5, expect="tc_wgrad" if tc else "direct")
+    run_wgrad(layer, 732, mode="convolution", alpha=0.75, beta=0.5, expect="direct")
+
+
+WGRAD_TC_MORE = [
+    L("wg_tc_c136_k200_5x5", 2, 136, 12, 14, 200, 5, 5, pad_top=2, pad_bottom=1, pad_left=0,
+      pad_right=3),
+    L("wg_tc_c384_k256_3x3", 4, 384, 13, 13, 256, 3, 3, **P1),
+    L("wg_tc_c64_k64_1x1_s2", 3, 64, 14, 14, 64, 1, 1, u=2, v=2),
+    L("wg_tc_c96_k64_11x11_s4", 2, 96, 35, 35, 64, 11, 11, pad_top=2, pad_bottom=2, pad_left=2,
+      pad_right=2, u=4, v=4),
+]
+
+
+@pytest.mark.parametrize("layer", WGRAD_TC_MORE, ids=lambda l: l.name)
+def test_wgrad_tensor_cores(layer):
+    run_wgrad(layer, 734, expect="tc_wgrad")
+    run_wgrad(layer, 735, alpha=-0.5, beta=2.0, expect="tc_wgrad", deterministic=True)
 
 
 def test_wgrad_bf16_output_and_determinism():
@@ -333,6 +354,6 @@ def test_wgrad_bf16_output_and_determinism():
     assert torch.equal(a, b), "deterministic filter gradients differ between runs"
 
 
-@pytest.mark.parametrize("layer", FULL_SIZE[1:3], ids=lambda l: l.name)
+@pytest.mark.parametrize("layer", FULL_SIZE, ids=lambda l: l.name)
 def test_wgrad_full_size_sampled(layer):
-    run_wgrad(layer, 740, full=False)
+    run_wgrad(layer, 740, full=False, expect="tc_wgrad")
