@@ -366,6 +366,161 @@ def run_workload(args, workload, handle, stream, dev, rank, world, local_rank, h
     return res
 
 
+# Backward routines and the pooling/activation primitives, timed like the
+# forward workloads (steps of reps_per_step passes, per-launch CUDA events).
+EXTRA_REPS = {"overfeat_bwd_data": 40, "overfeat_bwd_filter": 24, "alexnet_pool_act": 300}
+
+
+def _bwd_layers():
+    from deep_learning_convolution_gb300 import synth
+    # the tensor-core layers of the headline stack (layer 1 reads the 3-channel image)
+    return [l for l in synth.WORKLOADS["overfeat"] if l.C % 8 == 0]
+
+
+def _extra_ops(name, handle, dev):
+    """[(label, launch(), flops, bytes, kernel, bound)] for one extra workload."""
+    import numpy as np
+    import torch
+    from deep_learning_convolution_gb300 import api, synth
+    ops = []
+    if name in ("overfeat_bwd_data", "overfeat_bwd_filter"):
+        for j, layer in enumerate(synth.WORKLOADS["overfeat"]):
+            if layer not in _bwd_layers():
+                continue
+            x, w, _ = synth.make_inputs(layer, synth.workload_seed("overfeat", j))
+            P, Q = layer_output_dims(layer)
+            rng = np.random.default_rng(j)
+            dy = synth.round_values(rng.standard_normal((layer.N, layer.K, P, Q), dtype=np.float32), "bf16")
+            xt, wt = api.layer_tensors(layer, x, w, dev)
+            dyt = api.layer_tensors(layer, dy, w[:1], dev)[0]
+            kw = dict(pads=(layer.pad_top, layer.pad_bottom, layer.pad_left, layer.pad_right),
+                      stride=(layer.u, layer.v), dilation=(layer.dil_h, layer.dil_w))
+            flops = 2 * layer.N * layer.K * P * Q * layer.C * layer.R * layer.S
+            if name == "overfeat_bwd_data":
+                dx = torch.empty_like(xt, dtype=torch.float32)
+                op = api.Conv2dBackwardData(handle, wt, dyt, dx, w_axes="KRSC", dy_axes="NHWC",
+                                            dx_axes="NHWC", math="bf16", **kw)
+                nbytes = dyt.numel() * 2 + wt.numel() * 2 + dx.numel() * 4
+                ops.append((layer.name + "_dgrad", (lambda op=op, a=wt, b=dyt, c=dx: op(a, b, c)),
+                            flops, nbytes, op.kernel(wt, dyt, dx), "tensor", op))
+            else:
+                dw = torch.empty(wt.shape, dtype=torch.float32, device=dev)
+                op = api.Conv2dBackwardFilter(handle, xt, dyt, dw, x_axes="NHWC", dy_axes="NHWC",
+                                              dw_axes="KRSC", math="bf16", **kw)
+                nbytes = xt.numel() * 2 + dyt.numel() * 2 + dw.numel() * 4
+                ops.append((layer.name + "_wgrad", (lambda op=op, a=xt, b=dyt, c=dw: op(a, b, c)),
+                            flops, nbytes, op.kernel(xt, dyt, dw), "tensor", op))
+    elif name == "alexnet_pool_act":
+        rng = np.random.default_rng(5)
+        x = synth.round_values(rng.standard_normal((128, 64, 55, 55), dtype=np.float32), "bf16")
+        xt = api.layer_tensors(synth.Layer("a", 128, 64, 55, 55, 1, 1, 1), x, x[:1, :1], dev)[0]
+        y = torch.empty((128, 27, 27, 64), dtype=torch.bfloat16, device=dev)
+        pool = api.Pool2dForward(handle, xt, y, window=(3, 3), mode="max", stride=(2, 2),
+                                 x_axes="NHWC", y_axes="NHWC")
+        ops.append(("alex1_out_maxpool_3x3s2", (lambda: pool(xt, y)), 0,
+                    xt.numel() * 2 + y.numel() * 2, pool.kernel(xt, y), "hbm", pool))
+        ya = torch.empty_like(xt)
+        ops.append(("alex1_out_relu", (lambda: api.activation_forward(handle, xt, ya, mode="relu",
+                                                                      x_axes="NHWC", y_axes="NHWC")),
+                    0, xt.numel() * 4, "flat", "hbm", None))
+    return ops
+
+
+def run_extra(args, name, handle, stream, dev, local_rank, world):
+    """The bench fields of one extra workload (backward routines or the
+    pooling and activation primitives)."""
+    import torch
+    ops = _extra_ops(name, handle, dev)
+    reps = EXTRA_REPS[name]
+    for _ in range(args.warmup):
+        for _ in range(max(1, reps // 4)):
+            for o in ops:
+                o[1]()
+    torch.cuda.synchronize()
+    handle.synchronize()
+    K = args.steps
+    nl = len(ops)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(reps * nl + 1)] for _ in range(K)]
+    sampler = ClockSampler(local_rank)
+    torch.cuda.synchronize()
+    launches0 = handle.launches()
+    sampler.start()
+    time.sleep(0.05)
+    for i in range(K):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        e = 1
+        for _ in range(reps):
+            for o in ops:
+                o[1]()
+                ev[i][e].record(stream)
+                e += 1
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    launches = handle.launches() - launches0
+    handle.synchronize()
+    per_ms = [0.0] * nl
+    total_ms = 0.0
+    for i in range(K):
+        total_ms += ev[i][0].elapsed_time(ev[i][-1])
+        for e in range(reps * nl):
+            per_ms[e % nl] += ev[i][e].elapsed_time(ev[i][e + 1])
+    pass_flops = sum(o[2] for o in ops)
+    pass_bytes = sum(o[3] for o in ops)
+    hbm_bound = pass_flops == 0
+    # TFLOP/s from FLOPs, or GB/s from bytes (1e12 FLOP = 1e3 GB per unit)
+    total_ms, value = aggregate_over_ranks(total_ms, pass_flops * reps if not hbm_bound
+                                           else pass_bytes * reps * 1e3, K, world, dev)
+    peaks = load_peaks()
+    rows = []
+    n_launch = K * reps
+    for j, o in enumerate(ops):
+        t_s = per_ms[j] / n_launch * 1e-3
+        gbs = o[3] / t_s / 1e9
+        if o[5] == "hbm":
+            rows.append({"layer": o[0], "kernel": o[4], "us": round(t_s * 1e6, 2),
+                         "hbm_gbs": round(gbs, 1), "bound": "hbm",
+                         "frac_of_roofline": round(gbs / peaks["hbm_gbs"], 4)})
+        else:
+            tf = o[2] / t_s / 1e12
+            roof = min(peaks["bf16_tflops"], o[2] / o[3] * peaks["hbm_gbs"] / 1e3)
+            rows.append({"layer": o[0], "kernel": o[4], "us": round(t_s * 1e6, 2),
+                         "tflops": round(tf, 1), "hbm_gbs": round(gbs, 1),
+                         "bound": "tensor" if roof >= peaks["bf16_tflops"] else "hbm",
+                         "roofline_tflops": round(roof, 1), "frac_of_roofline": round(tf / roof, 4)})
+    dom = max(range(nl), key=lambda j: per_ms[j])
+    t_dom = per_ms[dom] / n_launch * 1e-3
+    if hbm_bound:
+        ach = ops[dom][3] / t_dom / 1e9
+        roofline = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None,
+                    "kernel": ops[dom][4], "peak_source": f"{peaks['source']} copy bandwidth"}
+        unit, metric = "GB/s", "pooling/activation GB/s (x read + y written once)"
+    else:
+        kern = ops[dom][4]
+        fl = sum(o[2] for o in ops if o[4] == kern)
+        t = sum(per_ms[j] for j in range(nl) if ops[j][4] == kern) / n_launch * 1e-3
+        ach = fl / t / 1e12
+        roofline = {"bound": "tensor", "achieved": round(ach, 1), "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4),
+                    "traffic": None, "kernel": kern,
+                    "peak_source": f"{peaks['source']} bf16 burst"}
+        unit, metric = "TFLOP/s", "TFLOP/s (direct-conv FLOPs of the gradient)"
+    res = {"what": metric, "value": round(value, 2), "unit": unit, "steps": K,
+           "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4), "dtype": "bf16",
+           "config": {"workload": name, "layers": [o[0] for o in ops], "reps_per_step": reps,
+                      "l2": "flushed between steps (256 MiB write, untimed)"},
+           "roofline": roofline, "layers": rows, "gpu_launches": launches, "clocks": clocks,
+           "e2e": None}
+    for o in ops:
+        if o[6] is not None:
+            o[6].close()
+    del ops, flush
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     from deep_learning_convolution_gb300 import api
@@ -391,6 +546,8 @@ def run_ours(args, rank, world, local_rank):
             r.pop("metric")
             r.pop("n_gpus")
             configs[wl] = r
+        for name in EXTRA_REPS:
+            configs[name] = run_extra(args, name, handle, stream, dev, local_rank, world)
         result["configs"] = configs
     handle.close()
     if world > 1:

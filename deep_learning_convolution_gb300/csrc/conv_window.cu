@@ -97,7 +97,9 @@ struct WinParams {
     int ring_bytes;
     int row_bytes;    // bytes of one input row (x_word)
     int x_stage;      // new input rows arrive by one bulk copy per tile into a stage buffer
-    int stage_bytes;  // bytes of one of the two stage buffers: rows * row_bytes
+    int x_shift;      // rows start on any element boundary: the copy takes the 16-byte
+                      // aligned superset of the rows and the repack reads them shifted
+    int stage_bytes;  // bytes of one of the two stage buffers: rows * row_bytes (+ 32)
     const void *wpack;  // the filter slabs, packed by window_pack_filters
     int b_img_bytes;    // bytes of one CTA's part: R*steps*(BN/ctas) rows of 32
     int pair;           // launched as CTA pairs (cta_group::2, M = 256 per MMA)
@@ -311,25 +313,60 @@ __device__ __forceinline__ void sts128v(uint32_t addr, uint32_t a, uint32_t b, u
                  : "memory");
 }
 
+// The in-image part of a tile's new rows i in [i0, rows): stage rows lo ..
+// lo + n - 1 (relative to i0), starting at byte src of x.
+__device__ __forceinline__ void stage_span(const WinParams &p, const WinTile &wt, int i0, int esz,
+                                           int &lo, int &n, long long &src) {
+    const int h0 = wt.p0 * p.u - p.pt + i0;
+    lo = max(0, -h0);
+    n = max(0, min(p.rows - i0, p.H - h0) - lo);
+    src = ((long long)wt.n * p.xs[0] + (long long)(h0 + lo) * p.xs[2]) * esz;
+}
+
 // Bulk-copies the new rows of a tile -- tile rows i in [i0, rows), input rows
 // p0*u - pt + i -- that lie inside the image into stage buffer `sbuf` (stage
 // row i - i0; dense rows are consecutive in x, so one copy), completing on
-// `bar`.  A tile past the last one (a pair's missing second tile) copies
+// `bar`.  With x_shift the rows need not start on 16-byte boundaries: the copy
+// takes the 16-byte-aligned superset of their bytes to the buffer's start,
+// and stage row i - i0 begins (start mod 16) + (i - i0 - lo) * row_bytes bytes
+// in.  A tile past the last one (a pair's missing second tile) copies
 // nothing but still completes the barrier's phase.
 __device__ void stage_rows(const WinParams &p, uint32_t sbuf, const WinTile &wt, bool valid, int i0,
                            uint64_t *bar, int esz) {
     int lo = 0, n = 0;
     long long src = 0;
-    if (valid) {
-        const int h0 = wt.p0 * p.u - p.pt + i0;
-        lo = max(0, -h0);
-        n = max(0, min(p.rows - i0, p.H - h0) - lo);
-        src = ((long long)wt.n * p.xs[0] + (long long)(h0 + lo) * p.xs[2]) * esz;
+    if (valid) stage_span(p, wt, i0, esz, lo, n, src);
+    const char *g = static_cast<const char *>(p.x) + src;
+    uint32_t bytes = (uint32_t)n * (uint32_t)p.row_bytes;
+    uint32_t dst = sbuf + (uint32_t)lo * (uint32_t)p.row_bytes;
+    if (p.x_shift && n > 0) {
+        const uint32_t shift = (uint32_t)(reinterpret_cast<uintptr_t>(g) & 15u);
+        g -= shift;
+        bytes = (shift + bytes + 15u) & ~15u;
+        dst = sbuf;
     }
-    const uint32_t bytes = (uint32_t)n * (uint32_t)p.row_bytes;
-    mbar_arrive_expect_tx(bar, bytes);
-    if (n > 0)
-        bulk_load_1d(sbuf + (uint32_t)lo * (uint32_t)p.row_bytes, static_cast<const char *>(p.x) + src, bytes, bar);
+    mbar_arrive_expect_tx(bar, n > 0 ? bytes : 0u);
+    if (n > 0) bulk_load_1d(dst, g, bytes, bar);
+}
+
+__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr);
+
+// Bytes [b, b+4) of a staged row at shared address rb (even; rows of 2-byte
+// elements may start 2 bytes past a word), zero outside [0, rowb).
+__device__ __forceinline__ uint32_t row_word(uint32_t rb, int b, uint32_t rowb) {
+    const uint32_t a = rb + (uint32_t)b;
+    if (b >= 0 && (uint32_t)b + 4u <= rowb) {
+        if ((a & 3u) == 0) return lds32(a);
+        return __funnelshift_r(lds32(a - 2u), lds32(a + 2u), 16);
+    }
+    const uint32_t lo = (b >= 0 && (uint32_t)b < rowb) ? lds16(a) : 0u;
+    const uint32_t hi = (b + 2 >= 0 && (uint32_t)(b + 2) < rowb) ? lds16(a + 2u) : 0u;
+    return lo | (hi << 16);
 }
 
 // Packs a tile's new rows from the stage buffer into their ring slots (and
@@ -339,6 +376,7 @@ __device__ void stage_rows(const WinParams &p, uint32_t sbuf, const WinTile &wt,
 // for rows outside the image) and one 16-byte store, its chunk XORed with
 // address bits 7.. (a step spans whole swizzle periods, so the XOR depends on
 // the lane only).  Two steps' loads are in flight before their stores.
+template <bool SHIFT>
 __device__ void repack_rows(const WinParams &p, uint32_t ring, uint32_t sbuf, const uint32_t *rtab,
                             const WinTile &wt, int base, int i0, int warp, int lane) {
     constexpr int NW = PROD_THREADS / 32;
@@ -361,6 +399,15 @@ __device__ void repack_rows(const WinParams &p, uint32_t ring, uint32_t sbuf, co
     const uint32_t rowb = (uint32_t)p.row_bytes;
     const uint32_t mdelta = (uint32_t)p.RS * (uint32_t)p.slot_bytes;
     const int gnb = G * p.nb;
+    // x_shift: stage row ri begins at sbuf + adj + ri*rowb (see stage_rows)
+    int adj = 0;
+    if (SHIFT) {
+        int slo, sn;
+        long long src;
+        stage_span(p, wt, i0, esz, slo, sn, src);
+        const int shift = (int)(reinterpret_cast<uintptr_t>(static_cast<const char *>(p.x) + src) & 15u);
+        adj = shift - slo * p.row_bytes;
+    }
     int ri = lo / spr, st0 = lo - (lo / spr) * spr;  // the warp's first (row, step)
 #pragma unroll 1
     for (int item = lo; item < hi; ++ri, st0 = 0) {
@@ -372,7 +419,7 @@ __device__ void repack_rows(const WinParams &p, uint32_t ring, uint32_t sbuf, co
         int pos;
         const int slot = ring_slot(p, rtab[i], base, pos);
         const bool mirror = pos < p.J - 1;
-        const uint32_t rb = sbuf + (uint32_t)ri * rowb;
+        const uint32_t rb = sbuf + (uint32_t)(adj + ri * (int)rowb);
         int bt = (P0 + st0 * G + dp) * p.nb - lb + b0;
         uint32_t paddr = ring + (uint32_t)slot * (uint32_t)p.slot_bytes + (uint32_t)(st0 * G + dp) * p.D + cho;
         for (int st = st0; st < st1; st += 2) {
@@ -381,8 +428,33 @@ __device__ void repack_rows(const WinParams &p, uint32_t ring, uint32_t sbuf, co
             for (int k = 0; k < 2; ++k) {
                 const int b = bt + k * gnb;
 #pragma unroll
-                for (int w = 0; w < 4; ++w)
-                    v[k][w] = (st + k < st1 && w < nw && (unsigned)(b + 4 * w) < rowb) ? lds32(rb + b + 4 * w) : 0u;
+                for (int w = 0; w < 4; ++w) v[k][w] = 0u;
+                if (st + k >= st1) continue;
+                if constexpr (SHIFT) {
+                    if (nw == 4 && b >= 0 && (uint32_t)b + 16u <= rowb) {
+                        // the whole chunk inside the row: 4 aligned words, or 5
+                        // and a 16-bit shift when the row starts 2 bytes past a word
+                        const uint32_t a = rb + (uint32_t)b;
+                        if ((a & 3u) == 0) {
+#pragma unroll
+                            for (int w = 0; w < 4; ++w) v[k][w] = lds32(a + 4u * w);
+                        } else {
+                            uint32_t t[5];
+#pragma unroll
+                            for (int w = 0; w < 5; ++w) t[w] = lds32(a - 2u + 4u * w);
+#pragma unroll
+                            for (int w = 0; w < 4; ++w) v[k][w] = __funnelshift_r(t[w], t[w + 1], 16);
+                        }
+                    } else {
+#pragma unroll
+                        for (int w = 0; w < 4; ++w)
+                            if (w < nw) v[k][w] = row_word(rb, b + 4 * w, rowb);
+                    }
+                } else {
+#pragma unroll
+                    for (int w = 0; w < 4; ++w)
+                        v[k][w] = (w < nw && (unsigned)(b + 4 * w) < rowb) ? lds32(rb + b + 4 * w) : 0u;
+                }
             }
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
@@ -517,9 +589,14 @@ __device__ void win_produce(const WinParams &p, uint32_t rank, uint32_t sB, uint
                            nx.valid, c1 ? max(0, p.rows - p.J * p.u) : 0, &sfull[(it + 1) & 1], ESZ);
                 ++staged;
             }
-            if (walk.valid)
-                repack_rows(p, sRing, sStage + (uint32_t)buf * (uint32_t)p.stage_bytes, rtab,
-                            walk.tile(p), walk.base, i0, warp, lane);
+            if (walk.valid) {
+                if (p.x_shift)
+                    repack_rows<true>(p, sRing, sStage + (uint32_t)buf * (uint32_t)p.stage_bytes, rtab,
+                                      walk.tile(p), walk.base, i0, warp, lane);
+                else
+                    repack_rows<false>(p, sRing, sStage + (uint32_t)buf * (uint32_t)p.stage_bytes, rtab,
+                                       walk.tile(p), walk.base, i0, warp, lane);
+            }
         } else {
             if (!ok) break;
             if (walk.valid) pack_rows<T>(p, sRing, rtab, walk.tile(p), walk.base, i0, warp, lane);
@@ -1096,10 +1173,35 @@ dlcStatus_t dlc_launch_window(dlcContext *ctx, const ConvProblem &pb) {
         bool on = p.x_word && dense && p.row_bytes % 16 == 0 && ((uintptr_t)pb.x % 16) == 0 &&
                   (pb.xs[0] * e) % 16 == 0 && (pb.xs[2] * e) % 16 == 0 && stage < (1LL << 20) &&
                   smem + 2 * (size_t)stage + epi1 <= (size_t)WIN_MAX_SMEM;
+        // rows on any element boundary: stage the 16-byte-aligned superset of a
+        // tile's rows (its round-up never passes the end of x, whose size is a
+        // multiple of 16 bytes) and read it shifted
+        const long long xbytes = ((long long)(pb.N - 1) * pb.xs[0] + (long long)pb.H * pb.xs[2]) * e;
+        const long long stage2 = (stage + 32 + 15) / 16 * 16;
+        bool shift = !on && contiguous && dense && p.nb % 4 == 0 && ((uintptr_t)pb.x % 16) == 0 &&
+                     pb.xs[0] >= (long long)pb.H * pb.xs[2] && xbytes % 16 == 0 && stage2 < (1LL << 20);
+        if (shift && smem + 2 * (size_t)stage2 + epi1 > (size_t)WIN_MAX_SMEM && !p.disc_wait) {
+            // make room with the short ring (kspan + J slots per phase; a tile
+            // that starts a new run of rows waits for its predecessor's MMAs)
+            const long long tail = ((long long)p.px_read * p.D + 1023) & ~1023LL;
+            const int rs2 = p.kspan + p.J;
+            const long long ring2 = (long long)pb.u * (rs2 + p.J - 1) * p.slot_bytes + tail;
+            const size_t smem2 = smem - (size_t)p.ring_bytes + (size_t)ring2;
+            if (rs2 < p.RS && smem2 + 2 * (size_t)stage2 + epi1 <= (size_t)WIN_MAX_SMEM) {
+                p.RS = rs2;
+                p.RSJ = rs2 + p.J - 1;
+                p.disc_wait = 1;
+                p.ring_bytes = (int)ring2;
+                smem = smem2;
+            }
+        }
+        shift = shift && smem + 2 * (size_t)stage2 + epi1 <= (size_t)WIN_MAX_SMEM;
         if (const char *ev = std::getenv("DLC_TC_WINSTAGE")) on = on && std::atoi(ev) != 0;
-        p.x_stage = on ? 1 : 0;
-        p.stage_bytes = on ? (int)stage : 0;
-        if (on) smem += 2 * (size_t)stage;
+        const bool sh = shift && !(std::getenv("DLC_TC_WINSTAGE") && std::atoi(std::getenv("DLC_TC_WINSTAGE")) == 0);
+        p.x_stage = (on || sh) ? 1 : 0;
+        p.x_shift = sh ? 1 : 0;
+        p.stage_bytes = on ? (int)stage : (sh ? (int)stage2 : 0);
+        if (p.x_stage) smem += 2 * (size_t)p.stage_bytes;
     }
     p.epi_bufs = (p.y_tma && smem + 2 * WIN_EPI_SMEM <= (size_t)WIN_MAX_SMEM) ? 2 : 1;
     if (p.y_tma) smem += (size_t)p.epi_bufs * WIN_EPI_SMEM;

@@ -55,6 +55,7 @@ template <> struct Io<double> {
 struct PoolParams {
     int N, C, H, W, R, S, P, Q;
     int pt, pl, u, v, mode;
+    int y_vec;  // channels-innermost y whose 16-byte channel chunks are aligned
     long long xs[4], ys[4];
     const void *x;
     void *y;
@@ -79,6 +80,45 @@ __device__ __forceinline__ void unpack16(const uint4 &q, A (&out)[V]) {
     } else {
         out[0] = __hiloint2double((int)q.y, (int)q.x);
         out[1] = __hiloint2double((int)q.w, (int)q.z);
+    }
+}
+
+// V consecutive results as 32-bit words of TO storage.
+template <typename TO, typename A, int V>
+__device__ __forceinline__ void pack_words(const A (&v)[V], uint32_t *w) {
+    if constexpr (sizeof(TO) == 2) {
+#pragma unroll
+        for (int i = 0; i < V / 2; ++i) {
+            const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn((float)v[2 * i]));
+            const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn((float)v[2 * i + 1]));
+            w[i] = lo | (hi << 16);
+        }
+    } else if constexpr (sizeof(TO) == 4) {
+#pragma unroll
+        for (int i = 0; i < V; ++i) w[i] = __float_as_uint((float)v[i]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            const double d = (double)v[i];
+            w[2 * i] = (uint32_t)__double2loint(d);
+            w[2 * i + 1] = (uint32_t)__double2hiint(d);
+        }
+    }
+}
+
+// Stores V results (V * sizeof(TO) = 8, 16 or 32 bytes, address aligned to
+// that size or 16) with vector stores.
+template <typename TO, typename A, int V>
+__device__ __forceinline__ void store_vec(TO *dst, const A (&v)[V]) {
+    constexpr int WORDS = V * (int)sizeof(TO) / 4;
+    uint32_t w[WORDS];
+    pack_words<TO, A, V>(v, w);
+    if constexpr (WORDS == 2) {
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < WORDS / 4; ++i)
+            reinterpret_cast<uint4 *>(dst)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
     }
 }
 
@@ -126,9 +166,14 @@ __global__ void __launch_bounds__(256) pool_nhwc_kernel(const __grid_constant__ 
                              (long long)ch * V;
 #pragma unroll
         for (int e = 0; e < V; ++e) {
-            A val = (A)p.alpha * (is_max ? acc[e] : acc[e] / div);
-            if (p.beta != 0.0) val += (A)p.beta * (A)Io<TO>::ld(y, yo + e);
-            Io<TO>::st(y, yo + e, val);
+            acc[e] = (A)p.alpha * (is_max ? acc[e] : acc[e] / div);
+            if (p.beta != 0.0) acc[e] += (A)p.beta * (A)Io<TO>::ld(y, yo + e);
+        }
+        if (p.y_vec) {
+            store_vec<TO, A, V>(y + yo, acc);
+        } else {
+#pragma unroll
+            for (int e = 0; e < V; ++e) Io<TO>::st(y, yo + e, acc[e]);
         }
     }
 }
@@ -214,16 +259,24 @@ __global__ void __launch_bounds__(256) act_flat_kernel(const __grid_constant__ A
     TO *y = static_cast<TO *>(p.y);
     const long long nv = n / V;
     const A alpha = (A)p.alpha, beta = (A)p.beta, coef = (A)p.coef;
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nv;
-         i += (long long)gridDim.x * blockDim.x) {
-        const uint4 q4 = __ldg(reinterpret_cast<const uint4 *>(x) + i);
-        A v[V];
-        unpack16<TI, A, V>(q4, v);
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    // two vectors per thread and iteration, both loads issued before any use
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += 2 * stride) {
+        const long long i2 = i + stride;
+        const uint4 qa = __ldg(reinterpret_cast<const uint4 *>(x) + i);
+        const uint4 qb = i2 < nv ? __ldg(reinterpret_cast<const uint4 *>(x) + i2) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int e = 0; e < V; ++e) {
-            A val = alpha * act_fn<A>(p.mode, v[e], coef);
-            if (beta != (A)0) val += beta * (A)Io<TO>::ld(y, i * V + e);
-            Io<TO>::st(y, i * V + e, val);
+        for (int h = 0; h < 2; ++h) {
+            const long long j = h ? i2 : i;
+            if (j >= nv) break;
+            A v[V];
+            unpack16<TI, A, V>(h ? qb : qa, v);
+#pragma unroll
+            for (int e = 0; e < V; ++e) {
+                v[e] = alpha * act_fn<A>(p.mode, v[e], coef);
+                if (beta != (A)0) v[e] += beta * (A)Io<TO>::ld(y, j * V + e);
+            }
+            store_vec<TO, A, V>(y + j * V, v);
         }
     }
     // the tail of fewer than V elements
@@ -344,6 +397,13 @@ dlcStatus_t dlc_launch_pool(dlcContext *ctx, const PoolProblem &pp) {
     }
     p.x = pp.x; p.y = pp.y; p.alpha = pp.alpha; p.beta = pp.beta;
     const bool nhwc = dlc_pool_variant(pp) == DLC_KERNEL_POOL_NHWC;
+    {
+        // a chunk of 16 bytes of x channels is 16 / sizeof(x) * sizeof(y) bytes of y
+        const int ex = dlc_dtype_bytes(pp.xdt), ey = dlc_dtype_bytes(pp.ydt);
+        const long long vb = 16LL / ex * ey, al = std::min(vb, 16LL);
+        p.y_vec = nhwc && ((uintptr_t)pp.y % al) == 0 && (pp.ys[0] * ey) % al == 0 &&
+                  (pp.ys[2] * ey) % al == 0 && (pp.ys[3] * ey) % al == 0;
+    }
     if (by_types<PoolRun>(pp.xdt, pp.ydt, ctx, p, nhwc) != cudaSuccess) return DLC_STATUS_EXECUTION_FAILED;
     ctx->launches += 1;
     return DLC_STATUS_SUCCESS;
@@ -362,7 +422,9 @@ dlcStatus_t dlc_launch_activation(dlcContext *ctx, const ActProblem &ap) {
     bool same = true;
     for (int i = 0; i < 4; ++i) same = same && ap.xs[i] == ap.ys[i];
     const long long n = (long long)ap.N * ap.C * ap.H * ap.W;
-    const long long flat = (same && dense(ext, ap.xs) && ((uintptr_t)ap.x % 16) == 0) ? n : 0;
+    const long long vb = 16LL / dlc_dtype_bytes(ap.xdt) * dlc_dtype_bytes(ap.ydt);
+    const long long flat = (same && dense(ext, ap.xs) && ((uintptr_t)ap.x % 16) == 0 &&
+                            ((uintptr_t)ap.y % std::min(vb, 16LL)) == 0) ? n : 0;
     if (by_types<ActRun>(ap.xdt, ap.ydt, ctx, p, flat) != cudaSuccess) return DLC_STATUS_EXECUTION_FAILED;
     ctx->launches += 1;
     return DLC_STATUS_SUCCESS;

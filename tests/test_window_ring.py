@@ -135,15 +135,28 @@ def walk_cta(p, pair, ub, ue, rank, new_run_step=None):
         reads_prev = reads
 
 
+def short_ring(p):
+    """The plan with the short ring (kspan + J slots per phase), which the
+    kernel also takes to make room for staged rows."""
+    q = dict(p)
+    q["RS"] = min(p["RS"], p["kspan"] + p["J"])
+    q["RSJ"] = q["RS"] + p["J"] - 1
+    q["short"] = q["RS"] < 2 * p["kspan"] or p["short"]
+    return q
+
+
+@pytest.mark.parametrize("ring", ["planned", "short"])
 @pytest.mark.parametrize("pair", [False, True], ids=["single", "pairs"])
 @pytest.mark.parametrize("layer", WINDOW_CASES + [synth.WORKLOADS["alexnet"][0],
                                                   synth.WORKLOADS["overfeat"][0],
                                                   synth.WORKLOADS["speech"][0]],
                          ids=lambda l: l.name)
-def test_ring_rows_reach_their_mmas(layer, pair):
+def test_ring_rows_reach_their_mmas(layer, pair, ring):
     esz = 4 if layer.dtype == "tf32" else 2
     p = plan(layer, esz, pair)
     assert p is not None, "the window kernel takes this layer"
+    if ring == "short":
+        p = short_ring(p)
     for grid in (152, 7, 1):
         G = min(grid, p["units"])
         for c in range(G):

@@ -52,4 +52,11 @@ WINDOW_CASES = [
     # copies: 224 pixels x 3 channels = 1344-byte rows, 7x7 stride 2 (D = 16),
     # left pad 2 so phase pixels start on 4-byte boundaries
     L("win_bf16_c3_k64_7x7_s2_wide_staged", 2, 3, 20, 224, 64, 7, 7, **P(3, 3, 2, 4), u=2, v=2),
+    # OverFeat's first layer at N = 8: 1386-byte rows (2 bytes past a word on
+    # every other row), staged as the 16-byte-aligned superset and repacked
+    # shifted
+    L("win_bf16_c3_k96_11x11_s4_ovf_shifted", 8, 3, 231, 231, 96, 11, 11, u=4, v=4),
+    # left pad 3 and odd rows on the shifted staging: 3*2*3 = 18 bytes of
+    # padding before a phase pixel
+    L("win_bf16_c3_k64_7x7_s2_shifted_pad3", 4, 3, 21, 41, 64, 7, 7, **P(3, 3, 3, 3), u=2, v=2),
 ]
