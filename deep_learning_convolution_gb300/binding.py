@@ -56,6 +56,7 @@ DLC_KERNEL_TC_IM2COL_PAIR = 6
 DLC_KERNEL_DIRECT = 7
 DLC_KERNEL_TC_WGRAD = 8
 DLC_KERNEL_POOL_NHWC = 9
+DLC_KERNEL_TC_ROWSTACK = 10
 DLC_DEVERR_NONE = 0
 DLC_DEVERR_WAIT_TIMEOUT = 1
 
@@ -63,7 +64,8 @@ KERNEL_NAMES = {DLC_KERNEL_NONE: "none", DLC_KERNEL_FFMA: "ffma",
                 DLC_KERNEL_TC_IM2COL: "tc_im2col", DLC_KERNEL_TC_GATHER: "tc_gather",
                 DLC_KERNEL_TC_GATHER_RUNS: "tc_runs", DLC_KERNEL_TC_WINDOW: "tc_window",
                 DLC_KERNEL_TC_IM2COL_PAIR: "tc_im2col_pair", DLC_KERNEL_DIRECT: "direct",
-                DLC_KERNEL_TC_WGRAD: "tc_wgrad", DLC_KERNEL_POOL_NHWC: "pool_nhwc"}
+                DLC_KERNEL_TC_WGRAD: "tc_wgrad", DLC_KERNEL_POOL_NHWC: "pool_nhwc",
+                DLC_KERNEL_TC_ROWSTACK: "tc_rowstack"}
 
 _h = c_void_p          # opaque handle / descriptor
 _ph = POINTER(c_void_p)

@@ -21,7 +21,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libdlc.so")
 
 SOURCES = ["api.cu", "conv_ffma.cu", "conv_tc.cu", "conv_window.cu", "conv_pair.cu", "conv_bwd.cu",
-           "conv_wgrad.cu", "pool_act.cu"]
+           "conv_wgrad.cu", "pool_act.cu", "conv_rowstack.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

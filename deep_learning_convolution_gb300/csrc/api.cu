@@ -294,6 +294,7 @@ dlcStatus_t dlcCreate(dlcHandle_t *handle) {
     if (!h) return DLC_STATUS_ALLOC_FAILED;
     h->device = dev;
     h->sm_count = prop.multiProcessorCount;
+    h->wpack_bytes = DLC_HANDLE_WPACK_BYTES;
     if (cudaHostAlloc((void **)&h->h_err, 4 * sizeof(int), cudaHostAllocMapped) != cudaSuccess) {
         delete h;
         return DLC_STATUS_EXECUTION_FAILED;
@@ -306,7 +307,7 @@ dlcStatus_t dlcCreate(dlcHandle_t *handle) {
     }
     if (cudaMalloc((void **)&h->sk_flags, DLC_SK_FLAGS * sizeof(int)) != cudaSuccess ||
         cudaMemset(h->sk_flags, 0, DLC_SK_FLAGS * sizeof(int)) != cudaSuccess ||
-        cudaMalloc(&h->wpack, DLC_WPACK_BYTES) != cudaSuccess) {
+        cudaMalloc(&h->wpack, DLC_HANDLE_WPACK_BYTES) != cudaSuccess) {
         if (h->sk_flags) cudaFree(h->sk_flags);
         if (h->wpack) cudaFree(h->wpack);
         cudaFreeHost(h->h_err);
@@ -651,7 +652,7 @@ dlcStatus_t noalloc_setup(int dev, NoAllocDevice **out) {
         // Load every kernel a later call may launch now: modules are loaded
         // lazily, and a module load allocates device memory.
         if (dlc_preload_tc() != DLC_STATUS_SUCCESS || dlc_preload_window() != DLC_STATUS_SUCCESS ||
-            dlc_preload_pair() != DLC_STATUS_SUCCESS)
+            dlc_preload_pair() != DLC_STATUS_SUCCESS || dlc_preload_rowstack() != DLC_STATUS_SUCCESS)
             return DLC_STATUS_EXECUTION_FAILED;
         cudaDriverEntryPointQueryResult q1, q2;
         void *f1 = nullptr, *f2 = nullptr;
@@ -702,6 +703,7 @@ dlcStatus_t dlcConvolutionForwardNoAlloc(void *stream, const float *alpha,
     ctx.d_err = status ? status : nd->scratch + DLC_NOALLOC_MAX_TILES;
     ctx.sk_flags = nd->scratch;
     ctx.wpack = nd->wpack;
+    ctx.wpack_bytes = DLC_WPACK_BYTES;
     ctx.encode_tiled = nd->encode_tiled;
     ctx.encode_im2col = nd->encode_im2col;
     if (pb.math == DLC_MATH_FP64) return DLC_STATUS_NOT_SUPPORTED;

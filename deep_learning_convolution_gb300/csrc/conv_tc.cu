@@ -1252,6 +1252,7 @@ dlcKernel_t dlc_tc_variant(const dlcContext *ctx, const ConvProblem &pb) {
         if (!pb.flip) return DLC_KERNEL_TC_IM2COL;
     }
     if (dlc_window_ok(pb)) return DLC_KERNEL_TC_WINDOW;
+    if (dlc_rowstack_ok(ctx, pb)) return DLC_KERNEL_TC_ROWSTACK;
     int a, b, c;
     if (!pb.flip && runs_ok(pb, &a, &b, &c)) return DLC_KERNEL_TC_GATHER_RUNS;
     return DLC_KERNEL_TC_GATHER;
@@ -1260,6 +1261,7 @@ dlcKernel_t dlc_tc_variant(const dlcContext *ctx, const ConvProblem &pb) {
 dlcStatus_t dlc_launch_tc(dlcContext *ctx, const ConvProblem &pb, dlcKernel_t variant) {
     if (variant == DLC_KERNEL_TC_WINDOW) return dlc_launch_window(ctx, pb);
     if (variant == DLC_KERNEL_TC_IM2COL_PAIR) return dlc_launch_pair(ctx, pb);
+    if (variant == DLC_KERNEL_TC_ROWSTACK) return dlc_launch_rowstack(ctx, pb);
     int mode;
     if (variant == DLC_KERNEL_TC_IM2COL) mode = MODE_IM2COL;
     else if (variant == DLC_KERNEL_TC_GATHER_RUNS) mode = MODE_RUNS;

@@ -56,7 +56,8 @@ struct dlcContext {
     uint64_t launches = 0;
     unsigned long long timeout_ns = 2000000000ull;  // pipeline wait limit
     int *sk_flags = nullptr;  // DLC_SK_FLAGS per-tile flags of split tiles (zero between launches)
-    void *wpack = nullptr;    // DLC_WPACK_BYTES: filters repacked for the window kernel
+    void *wpack = nullptr;    // filters repacked for the window and row-stack kernels
+    size_t wpack_bytes = 0;   // its size
     int deterministic = 0;    // no split reductions whose partial sums meet in atomic adds
     EncodeTiledFn encode_tiled = nullptr;
     EncodeIm2colFn encode_im2col = nullptr;
@@ -64,9 +65,12 @@ struct dlcContext {
 
 // Split-tile flags owned by a handle: at most this many tiles per launch use them.
 #define DLC_SK_FLAGS 4096
-// Device bytes a handle keeps for the window kernel's repacked filter image
-// (at most the shared memory of one CTA).
+// Device bytes of the window kernel's repacked filter image (at most the
+// shared memory of one CTA): the allocation-free entry point's fixed array.
 #define DLC_WPACK_BYTES (256 * 1024)
+// Device bytes a handle keeps for repacked filters: the window kernel's image
+// or the row-stack kernel's filter slices (up to about one filter bank).
+#define DLC_HANDLE_WPACK_BYTES (2 * 1024 * 1024)
 
 inline int dlc_dtype_bytes(dlcDataType_t t) {
     return t == DLC_DATA_BFLOAT16 ? 2 : (t == DLC_DATA_DOUBLE ? 8 : 4);
@@ -178,4 +182,9 @@ bool dlc_im2col_ok(const ConvProblem &pb);
 dlcStatus_t dlc_preload_tc();
 dlcStatus_t dlc_preload_window();
 dlcStatus_t dlc_preload_pair();
+dlcStatus_t dlc_preload_rowstack();
+// conv_rowstack.cu: TF32 channel-planar layers with few filters and unit
+// horizontal stride (filters stacked over output rows as the MMA's M side).
+bool dlc_rowstack_ok(const dlcContext *ctx, const ConvProblem &pb);
+dlcStatus_t dlc_launch_rowstack(dlcContext *ctx, const ConvProblem &pb);
 

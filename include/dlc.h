@@ -144,8 +144,12 @@ typedef enum {
                                      thread, CUDA cores, any strides */
     DLC_KERNEL_TC_WGRAD = 8,      /* filter gradient on the tensor cores: pixels as the
                                      reduction, both operands MN-major from TMA */
-    DLC_KERNEL_POOL_NHWC = 9      /* pooling with channels innermost: 16-byte vectors of
+    DLC_KERNEL_POOL_NHWC = 9,     /* pooling with channels innermost: 16-byte vectors of
                                      channels per thread */
+    DLC_KERNEL_TC_ROWSTACK = 10   /* TF32, channel-planar (NCHW) x, unit horizontal stride,
+                                     up to 64 filters: filters stacked over output rows as the
+                                     MMA's M side, output pixels (per phase q mod 4) as N,
+                                     read in place from shifted copies of input rows */
 } dlcKernel_t;
 
 /* Device error codes recorded by kernels (dlcGetLastDeviceError). */
@@ -308,7 +312,12 @@ dlcStatus_t dlcGetConvolutionForwardKernel(dlcHandle_t handle,
  * with the input pixels just outside a window that share its packed phase
  * pixel, so there an output beside such a window can read NaN as well (same
  * image, rows whose window holds the pixel, within one stride step plus one
- * phase pixel of its column).  Every other kernel reads exactly each window.
+ * phase pixel of its column).  The row-stack kernel (DLC_KERNEL_TC_ROWSTACK)
+ * likewise multiplies zero filter taps with input pixels up to 3 columns past
+ * a window and with input rows of its block of output rows that a given
+ * output row does not read: there an output of the same image, within that
+ * block of rows and within 4 columns of such a pixel, can read NaN.  Every
+ * other kernel reads exactly each window.
  * Sources: maxDNN page, method section (each output is its receptive field
  * times the filter weights); cuDNN page, method section (C API, descriptors
  * with arbitrary strides, caller-owned buffers). */

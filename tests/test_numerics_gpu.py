@@ -16,7 +16,10 @@ the window kernel (few-channel layers) also multiplies zero filter taps with
 the real input pixels that share a packed phase pixel with a window's edge,
 so there an output next to such a window may be NaN: only NaN, only in image
 n0, only in rows whose window holds h0 and only within one phase pixel of the
-Inf's column.
+Inf's column.  The row-stack kernel multiplies zero taps with the input rows
+of its block of 4 output rows and up to 3 columns past a window: only NaN,
+only in image n0, only in the blocks of rows that hold a hit row, and only
+within 4 columns of the Inf's.
 """
 import numpy as np
 import pytest
@@ -89,6 +92,8 @@ NONFINITE_CASES = [
        pad_right=2), "tc_im2col_pair"),
     (L("nf_runs_tf32_nchw_c32", 2, 32, 20, 23, 32, 3, 3, pad_top=1, pad_bottom=1, pad_left=1,
        pad_right=1, dtype="tf32", layout="NCHW"), "tc_runs"),
+    (L("nf_rowstack_tf32_nchw_c32", 2, 32, 20, 23, 32, 3, 3, pad_top=1, pad_bottom=1, pad_left=1,
+       pad_right=1, dtype="tf32", layout="NCHW"), "tc_rowstack"),
     (L("nf_ffma_nchw_c8", 2, 8, 16, 16, 16, 3, 3, pad_top=1, pad_bottom=1, pad_left=1,
        pad_right=1, dtype="f32", layout="NCHW"), "ffma"),
     (L("nf_window_c3_11x11_s4", 2, 3, 67, 67, 64, 11, 11, pad_top=2, pad_bottom=2, pad_left=2,
@@ -97,10 +102,12 @@ NONFINITE_CASES = [
 
 
 @pytest.mark.parametrize("layer,kernel", NONFINITE_CASES, ids=lambda v: getattr(v, "name", v))
-def test_one_inf_in_x(layer, kernel):
+def test_one_inf_in_x(layer, kernel, monkeypatch):
     import torch
     from deep_learning_convolution_gb300 import api
     _need_cuda()
+    if kernel == "tc_runs":
+        monkeypatch.setenv("DLC_TC_ROWSTACK", "0")
     x, w, _ = synth.make_inputs(layer, 5150)
     n0, c0, h0, w0 = 1, layer.C // 2, layer.H // 2, layer.W // 2 + 1
     x[n0, c0, h0, w0] = np.inf
@@ -126,7 +133,17 @@ def test_one_inf_in_x(layer, kernel):
     tol = 1e-5 * bound + 1e-6
     assert (np.abs(got[ok] - ref[ok]) <= tol[ok]).all()
     spurious = ~hit & ~np.isfinite(got)
-    if kernel != "tc_window":
+    if kernel == "tc_rowstack":
+        # zero filter taps meet the Inf in the other output rows of its block of
+        # 4 and up to 3 columns past a window
+        assert np.isnan(got[spurious]).all()
+        nn, kk, pp, qq = np.nonzero(spurious)
+        assert (nn == n0).all()
+        hit_rows = np.unique(np.nonzero(hit[n0])[1])
+        assert all(np.abs(hit_rows - p_).min() < 4 and p_ // 4 in hit_rows // 4 for p_ in pp)
+        off = w0 - (qq - layer.pad_left)
+        assert ((off >= -4) & (off < layer.S + 4)).all()
+    elif kernel != "tc_window":
         assert not spurious.any(), f"{int(spurious.sum())} outputs non-finite off the window"
     else:
         assert np.isnan(got[spurious]).all()

@@ -161,10 +161,52 @@ RUN_CASES = [
 
 @pytest.mark.parametrize("layer", RUN_CASES, ids=lambda l: l.name)
 def test_tc_runs_parity_full(handle, layer, monkeypatch):
-    # most of these layers take the window kernel by default
+    # most of these layers take the window or row-stack kernel by default
     monkeypatch.setenv("DLC_TC_WINDOW", "0")
+    monkeypatch.setenv("DLC_TC_ROWSTACK", "0")
     run_and_check(handle, layer, 2000 + RUN_CASES.index(layer), full=True,
                   expect_kernel="tc_runs")
+
+
+# ---------------------------------------------------------------------------
+# tensor cores, row-stack kernel: TF32 channel-planar layers with few filters
+# and unit horizontal stride; filters stacked over output rows as M
+# ---------------------------------------------------------------------------
+
+ROWSTACK_CASES = [
+    # speech layer 2 at N = 2 on a narrower input: 21 x 11 filters, stride 2 x 1
+    L("rs_speech2_like", 2, 32, 41, 90, 32, 21, 11, **P(10, 10, 5, 5), u=2, dtype="tf32",
+      layout="NCHW"),
+    # ragged: 17 channels (a partial group), 3x3 filters (one chunk per channel),
+    # Q = 29 (not a multiple of 4), P = 9 (a partial block of 4 rows)
+    L("rs_c17_k32_3x3", 3, 17, 9, 29, 32, 3, 3, **P(1, 1, 1, 1), dtype="tf32", layout="NCHW"),
+    # 48 filters (two rows of 64 per block), 5x13 filters (4 chunks), stride 3
+    L("rs_c19_k48_5x13_s3", 2, 19, 20, 41, 48, 5, 13, **P(2, 0, 6, 3), u=3, dtype="tf32",
+      layout="NCHW"),
+    # 16 filters, 1x1 (a single tap), several images per tile
+    L("rs_c21_k16_1x1", 5, 21, 6, 21, 16, 1, 1, dtype="tf32", layout="NCHW"),
+    # 64 filters, 7x12 filters, asymmetric pads, Q = 50
+    L("rs_c36_k64_7x12", 2, 36, 15, 55, 64, 7, 12, **P(3, 1, 4, 2), dtype="tf32", layout="NCHW"),
+    # a single output row and column per image
+    L("rs_c24_k32_3x3_tiny", 3, 24, 3, 3, 32, 3, 3, dtype="tf32", layout="NCHW"),
+]
+
+
+@pytest.mark.parametrize("layer", ROWSTACK_CASES, ids=lambda l: l.name)
+def test_tc_rowstack_parity_full(handle, layer):
+    run_and_check(handle, layer, 2700 + ROWSTACK_CASES.index(layer), full=True,
+                  expect_kernel="tc_rowstack")
+
+
+@pytest.mark.parametrize("layer", ROWSTACK_CASES[:2], ids=lambda l: l.name)
+def test_tc_rowstack_epilogue_and_modes(handle, layer):
+    import torch
+    run_and_check(handle, layer, 2750, full=True, alpha=-0.5, beta=1.25, with_bias=True,
+                  relu=True, expect_kernel="tc_rowstack")
+    run_and_check(handle, layer, 2751, full=True, y_dtype=torch.bfloat16,
+                  expect_kernel="tc_rowstack")
+    run_and_check(handle, layer, 2752, full=True, y_axes="NHWC", mode="convolution",
+                  expect_kernel="tc_rowstack")
 
 
 # ---------------------------------------------------------------------------
@@ -244,10 +286,16 @@ def test_kcrs_filters_with_nhwc_activations_use_gather(handle):
      "tc_window"),
     (L("tf32_nchw_wview_w", 2, 4, 12, 13, 32, 3, 5, **P(1, 1, 2, 2), dtype="tf32",
        layout="NCHW"), "width_pad", "tc_window"),
+    (L("tf32_nchw_c20_wview_rs", 2, 20, 12, 13, 32, 3, 5, **P(1, 1, 2, 2), dtype="tf32",
+       layout="NCHW"), "width_pad", "tc_rowstack"),
+    (L("tf32_nchw_c20_imgpad_rs", 2, 20, 12, 13, 32, 3, 5, **P(1, 1, 2, 2), dtype="tf32",
+       layout="NCHW"), "image_pad", "tc_rowstack"),
 ], ids=lambda v: v.name if hasattr(v, "name") else str(v))
 def test_strided_views(handle, layer, view, kernel, monkeypatch):
     if kernel != "tc_window":
         monkeypatch.setenv("DLC_TC_WINDOW", "0")
+    if kernel != "tc_rowstack":
+        monkeypatch.setenv("DLC_TC_ROWSTACK", "0")
     if kernel == "tc_im2col":
         monkeypatch.setenv("DLC_TC_PAIR", "0")
     run_and_check(handle, layer, 2600, full=True, view=view, expect_kernel=kernel)
@@ -368,7 +416,7 @@ def test_workspace_is_zero_and_kernel_choice(handle):
     expect = {"alexnet": ["tc_window"] + ["tc_im2col_pair"] * 4,
               "overfeat": ["tc_window"] + ["tc_im2col_pair"] * 4,
               "resnet50": ["tc_im2col_pair"] * len(synth.WORKLOADS["resnet50"]),
-              "speech": ["tc_window", "tc_runs"], "tiny": ["ffma"]}
+              "speech": ["tc_window", "tc_rowstack"], "tiny": ["ffma"]}
     for wl, kinds in expect.items():
         for layer, kind in zip(synth.WORKLOADS[wl], kinds):
             x, w, _ = synth.make_inputs(layer, 1, batch=1)

@@ -35,7 +35,8 @@ CASES = [
     # 154 output tiles on the SM-pair im2col kernel
     L("noalloc_bf16_c64_k64_70", 4, 64, 70, 70, 64, 3, 3, pad_top=1, pad_bottom=1, pad_left=1,
       pad_right=1),
-    # 32 channels, TF32, NCHW: the run-gather kernel
+    # 32 channels, TF32, NCHW: the row-stack kernel (its filter slices in the
+    # fixed array)
     L("noalloc_tf32_nchw_c32_k32_99", 2, 32, 99, 99, 32, 3, 3, pad_top=1, pad_bottom=1,
       pad_left=1, pad_right=1, dtype="tf32", layout="NCHW"),
     # a first layer (3 channels, 11x11, stride 4): the window kernel, whose
