@@ -29,14 +29,16 @@
 // A work unit is (NI images, J output rows, two phases): two TMEM
 // accumulators of N columns.  For every input row t and group of 4 channels a
 // stage holds the filter slices (A: one TMA load of the packed filter image,
-// 32-byte swizzled K-major, rows j read at filter row R-1-r = R-1-t+j*u by a
-// strided box, out-of-range rows zero-filled) and the shifted copies of the
-// 4 channels' input rows for both phases and all NI images (B).  One issuer
+// 128-byte swizzled K-major with four MMAs' slices per 128-byte row, rows j
+// read at filter row R-1-r = R-1-t+j*u by a strided box, out-of-range rows
+// zero-filled) and the shifted copies of the
+// 4 channels' input rows for both phases and all NI images (B).  One copier
 // warp stages each input row once, as a 16-byte-aligned superset, with bulk
-// copies into a ring of three raw buffers two stages ahead, and loads the
-// filter slices; eight builder warps repack the raw rows into the two phase
-// copies.  A stage's full barrier counts the builders' arrivals and the
-// issuer's, which carries the filter bytes.  Input rows outside the image
+// copies into a ring of three raw buffers as far ahead as they are free;
+// eight builder warps repack the raw rows into the two phase copies; one
+// thread of a fifteenth warp loads the filter slices.  A stage's full
+// barrier counts the builders' arrivals and the loader's, which carries the
+// filter bytes.  Input rows outside the image
 // contribute nothing and their stages are skipped.  Four epilogue warps read
 // the accumulators and store y (alpha, beta*y, bias, ReLU) through its
 // strides.  Every wait is bounded.
@@ -57,13 +59,15 @@ constexpr int RS_M = 128;            // MMA rows
 constexpr int RS_CG = 4;             // channels per stage
 constexpr int RS_PH = 4;             // phases: 16 bytes / 4-byte elements
 constexpr int RS_BUILD_WARPS = 8;
-constexpr int RS_PROD_WARPS = RS_BUILD_WARPS + 1;           // the copy issuer and the builders
-constexpr int RS_THREADS = (RS_PROD_WARPS + 1 + 4) * 32;  // producers, MMA, epilogue
+constexpr int RS_PROD_WARPS = RS_BUILD_WARPS + 1;           // the raw-row copier and the builders
+constexpr int RS_MMA_WARP = RS_PROD_WARPS;
+constexpr int RS_A_WARP = RS_MMA_WARP + 5;                  // after the four epilogue warps
+constexpr int RS_THREADS = (RS_A_WARP + 1) * 32;
 constexpr int RS_RAW = 3;            // raw-row buffers
-constexpr int RS_RAW_LAG = 2;        // stages the raw copies run ahead
 constexpr int RS_MAX_SMEM = 232448;
-constexpr int RS_BAR_AREA = 1024;  // barriers, then the MMA descriptor table
+constexpr int RS_BAR_AREA = 256;     // barriers
 constexpr int RS_MAX_MPG = 16;       // MMAs per stage and phase
+constexpr int RS_MAX_RB = 256;       // row blocks the unit order sorts
 
 struct RsParams {
     int N, C, H, W, K, R, S, P, Q;
@@ -77,11 +81,14 @@ struct RsParams {
     int seg_a, NI, Nmma;   // rows per image segment, images per tile, MMA N (multiple of 16)
     int copy_bytes;        // bytes of one shifted row copy (all NI images)
     int b_stage;           // bytes of one stage's B copies: 2 phases x 4 channels
-    int a_stage;           // bytes of one stage's A slices: mpg x 4 KiB
+    int acols;             // 128-byte A columns per stage: ceil(mpg/4), four MMAs' slices each
+    int a_stage;           // bytes of one stage's A: acols x 16 KiB
     int raw_bytes;         // bytes of one staged input row (16-byte-aligned superset)
     int raw_stage;         // bytes of one of the RS_RAW raw-row buffers: 4 channels x NI rows
     int stages;
     int row_blocks, img_groups, tiles, units;
+    int sorted;                   // row_order holds the row blocks, most input rows first
+    unsigned short row_order[RS_MAX_RB];
     uint32_t b_off[RS_MAX_MPG];   // start of MMA i's first chunk within a phase's copies
     uint32_t b_lbo[RS_MAX_MPG];   // bytes from its first to its second chunk
     long long xs[4], ys[4];
@@ -101,12 +108,22 @@ struct RsUnit {
     int g, pb, pass;
 };
 
+// Unit u of the CTA walk (CTA b takes u = b, b + G, b + 2G, ..., G CTAs).
+// Units are ranked row block by row block, the blocks with the most input
+// rows inside the image first, and within a block by image group and pass;
+// a CTA's second, fourth, ... whole round takes the ranks in reverse, so the
+// light blocks of the last rounds even out the heavy ones of the first.
 __device__ __forceinline__ RsUnit rs_unit(const RsParams &p, int u) {
+    const int G = gridDim.x;
+    const int round = u / G;
+    int rank = u;
+    if ((round & 1) && (round + 1) * G <= p.units) rank = round * G + (G - 1 - (u - round * G));
     RsUnit w;
-    w.pass = u & 1;
-    const int t = u >> 1;
-    w.pb = t % p.row_blocks;
-    w.g = t / p.row_blocks;
+    w.pass = rank & 1;
+    const int t = rank >> 1;
+    const int s = t / p.img_groups;
+    w.g = t - s * p.img_groups;
+    w.pb = p.sorted ? (int)p.row_order[s] : s;
     return w;
 }
 
@@ -121,19 +138,24 @@ __device__ __forceinline__ bool rs_row_in(const RsParams &p, int pb, int t) {
 struct RsWalk {
     int u, t, cg;
     bool valid;
+    RsUnit w;  // unit u's coordinates
+    __device__ void enter(const RsParams &p) {
+        valid = u < p.units;
+        if (valid) w = rs_unit(p, u);
+    }
     __device__ void first(const RsParams &p) {
         u = blockIdx.x;
         t = 0;
         cg = 0;
-        valid = u < p.units;
+        enter(p);
         settle(p);
     }
     __device__ void settle(const RsParams &p) {  // skip rows outside the image
-        while (valid && !rs_row_in(p, rs_unit(p, u).pb, t)) {
+        while (valid && !rs_row_in(p, w.pb, t)) {
             if (++t == p.T) {
                 t = 0;
                 u += gridDim.x;
-                valid = u < p.units;
+                enter(p);
             }
         }
     }
@@ -143,7 +165,7 @@ struct RsWalk {
         if (++t == p.T) {
             t = 0;
             u += gridDim.x;
-            valid = u < p.units;
+            enter(p);
         }
         settle(p);
     }
@@ -158,152 +180,225 @@ __device__ __forceinline__ const float *rs_row_ptr(const RsParams &p, const RsUn
     return p.x + (long long)(in ? n : 0) * p.xs[0] + (long long)(in ? c : 0) * p.xs[1] + (long long)h * p.xs[2];
 }
 
-// Thread 0: bulk-copies the stage's input rows (RS_CG channels x NI images)
-// into raw buffer `rb`, each as the 16-byte-aligned superset of its bytes at
-// slot (cl*NI + ii)*raw_bytes, completing on `bar`.
-__device__ void rs_copy_raw(const RsParams &p, uint32_t rb, const RsWalk &st, uint64_t *bar) {
-    uint32_t total = 0;
-    const RsUnit w = rs_unit(p, st.u);
-    for (int pass = 0; pass < 2; ++pass) {
-        if (pass == 1) mbar_arrive_expect_tx(bar, total);
-        for (int cl = 0; cl < RS_CG; ++cl)
-            for (int ii = 0; ii < p.NI; ++ii) {
-                bool in;
-                const float *src = rs_row_ptr(p, w, st.t, st.cg, cl, ii, in);
-                if (!in) continue;
-                const uintptr_t a = reinterpret_cast<uintptr_t>(src);
-                const unsigned long long a16 = a & ~15ull;
-                const unsigned long long beg = std::max<unsigned long long>(a16, p.x_beg16);
-                const unsigned long long end = std::min<unsigned long long>(
-                    (a + 4ull * (unsigned long long)p.W + 15ull) & ~15ull, p.x_end16);
-                if (end <= beg) continue;  // the row lies in the first or last 16 bytes of x
-                const uint32_t bytes = (uint32_t)(end - beg);
-                if (pass == 0)
-                    total += bytes;
-                else
-                    bulk_load_1d(rb + (uint32_t)((cl * p.NI + ii) * p.raw_bytes) + (uint32_t)(beg - a16),
-                                 reinterpret_cast<const void *>(beg), bytes, bar);
-            }
+// Bytes of input row (cl, ii) of a stage that its bulk copy moves: the
+// 16-byte-aligned superset of the row, clipped to the 16-byte-aligned part
+// of x (0 when the row lies in the first or last 16 bytes of x or past C, N).
+__device__ __forceinline__ uint32_t rs_raw_span(const RsParams &p, const RsUnit &w, const RsWalk &st, int cl,
+                                                int ii, unsigned long long &beg, unsigned long long &a16) {
+    bool in;
+    const float *src = rs_row_ptr(p, w, st.t, st.cg, cl, ii, in);
+    const uintptr_t a = reinterpret_cast<uintptr_t>(src);
+    a16 = a & ~15ull;
+    beg = a16 > p.x_beg16 ? a16 : p.x_beg16;
+    unsigned long long end = (a + 4ull * (unsigned long long)p.W + 15ull) & ~15ull;
+    end = end < p.x_end16 ? end : p.x_end16;
+    return (in && end > beg) ? (uint32_t)(end - beg) : 0u;
+}
+
+// Warp 0: bulk-copies the stage's input rows (RS_CG channels x NI images)
+// into raw buffer `rb`, row (cl, ii) at slot (cl*NI + ii)*raw_bytes, one row
+// per lane; lane 0 first announces the total bytes on `bar`.
+__device__ void rs_copy_raw(const RsParams &p, uint32_t rb, const RsWalk &st, uint64_t *bar, int lane) {
+    const int combos = RS_CG * p.NI;
+    unsigned long long beg = 0, a16 = 0;
+    uint32_t bytes = 0;
+    if (lane < combos) bytes = rs_raw_span(p, st.w, st, lane / p.NI, lane % p.NI, beg, a16);
+    uint32_t total = bytes;
+    for (int cmb = lane + 32; cmb < combos; cmb += 32) total += rs_raw_span(p, st.w, st, cmb / p.NI, cmb % p.NI, beg, a16);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+    if (lane == 0) mbar_arrive_expect_tx(bar, total);
+    __syncwarp();
+    if (bytes)
+        bulk_load_1d(rb + (uint32_t)(lane * p.raw_bytes) + (uint32_t)(beg - a16), reinterpret_cast<const void *>(beg),
+                     bytes, bar);
+    for (int cmb = lane + 32; cmb < combos; cmb += 32) {
+        const uint32_t b = rs_raw_span(p, st.w, st, cmb / p.NI, cmb % p.NI, beg, a16);
+        if (b)
+            bulk_load_1d(rb + (uint32_t)(cmb * p.raw_bytes) + (uint32_t)(beg - a16), reinterpret_cast<const void *>(beg),
+                         b, bar);
     }
 }
+
+// Rows [0, rows) of the shifted copies of one (channel, image) row, lane
+// strided: row a of the copy for phase b0 holds elements e0 .. e0+3 of the
+// input row, e0 = 4a + b0 - pl, and the copy for b0 + 1 elements e0+1 ..
+// e0+4.  Rows in [fa, fb) find all five in the raw row, at words
+// 4*(g0 + a) + O .. + 4 (O = the offset within a 16-byte word, the same for
+// every row), and take them with 16-byte loads, several rows' loads at a
+// time; the others (a few at each end) take each element from the raw
+// row, from x (the first and last 16 bytes of x are not staged) or zero
+// (padding, past C or N, or past the image segment).
+__device__ __forceinline__ void rs_copy_rows(const uint4 *raw4, const uint32_t *raw1, uint4 *dst0, uint4 *dst1,
+                                             int rows, int fa, int fb, int g0, int O, int e0_0, int sh, int e_lo,
+                                             int avail, int lim, const float *src, int W, int lane) {
+    constexpr int U = 4;  // rows a lane loads before it stores
+    for (int a0 = fa + lane; a0 < fb; a0 += 32 * U) {
+        uint4 v[U][2];
+#pragma unroll
+        for (int j = 0; j < U; ++j)
+            if (a0 + 32 * j < fb) {
+                v[j][0] = raw4[g0 + a0 + 32 * j];
+                v[j][1] = raw4[g0 + a0 + 32 * j + 1];
+            }
+#pragma unroll
+        for (int j = 0; j < U; ++j)
+            if (a0 + 32 * j < fb) {
+                uint32_t q[8] = {v[j][0].x, v[j][0].y, v[j][0].z, v[j][0].w,
+                                 v[j][1].x, v[j][1].y, v[j][1].z, v[j][1].w};
+                // words O .. O+4 of the two: shift down by 2, then by 1 (O is
+                // the same for every lane)
+                if (O & 2) {
+#pragma unroll
+                    for (int l = 0; l < 6; ++l) q[l] = q[l + 2];
+                }
+                if (O & 1) {
+#pragma unroll
+                    for (int l = 0; l < 5; ++l) q[l] = q[l + 1];
+                }
+                dst0[a0 + 32 * j] = make_uint4(q[0], q[1], q[2], q[3]);
+                dst1[a0 + 32 * j] = make_uint4(q[1], q[2], q[3], q[4]);
+            }
+    }
+    const int edge = fa + (rows - fb);
+    for (int i = lane; i < edge; i += 32) {
+        const int a = i < fa ? i : fb + (i - fa);
+        const int e0 = e0_0 + 4 * a;
+        uint32_t el[5];
+#pragma unroll
+        for (int l = 0; l < 5; ++l) {
+            const int e = e0 + l;
+            el[l] = 0u;
+            if (a < lim && e >= 0 && e < W)
+                el[l] = (e >= e_lo && e < avail) ? raw1[sh + e] : __float_as_uint(__ldg(src + e));
+        }
+        dst0[a] = make_uint4(el[0], el[1], el[2], el[3]);
+        dst1[a] = make_uint4(el[1], el[2], el[3], el[4]);
+    }
+}
+
+// A builder warp's (channel slot, image slot) pair and where its copies go.
+struct RsCombo {
+    int cl, ii, rows;
+    size_t raw_off, dst0_off, dst1_off;  // bytes within a raw buffer / a stage's B
+    __device__ void set(const RsParams &p, int cmb) {
+        ii = cmb % p.NI;
+        cl = cmb / p.NI;
+        const int r0 = ii * p.seg_a;
+        rows = (ii == p.NI - 1 ? p.Nmma + p.cpc - 1 : r0 + p.seg_a) - r0;  // the last copy also feeds the tail
+        raw_off = (size_t)cmb * p.raw_bytes;
+        dst0_off = (size_t)cl * p.copy_bytes + 16 * (size_t)r0;
+        dst1_off = (size_t)(RS_CG + cl) * p.copy_bytes + 16 * (size_t)r0;
+    }
+};
 
 // The shifted row copies of one stage from its raw rows: for phase slot ph
 // (phase b = 2*pass + ph), channel slot cl and image slot ii, row a of the
 // copy holds x[n, c, h, 4a + b - pl + l], l < 4 (zero outside the row, past C
-// or N).  Warp w builds the copies of (cl, ii) = w, w + 8, ..., both phases,
-// one row per lane and step: the 5 elements both phases' chunks take lie in
-// two aligned 16-byte words of the raw row; rows past the last image segment
-// (read only for unstored outputs) are zeros.
-__device__ void rs_build_b(const RsParams &p, uint32_t sb, uint32_t rb, const RsUnit &w, int t, int cg,
-                           int warp, int lane) {
-    const int combos = RS_CG * p.NI;
-    const int tail = p.Nmma + p.cpc - 1;  // rows the MMAs read per copy
-    const int b0 = 2 * w.pass;
-    for (int cmb = warp; cmb < combos; cmb += RS_BUILD_WARPS) {
-        const int ii = cmb % p.NI;
-        const int cl = cmb / p.NI;
-        bool in;
-        const float *src = rs_row_ptr(p, w, t, cg, cl, ii, in);
-        const uintptr_t ra = reinterpret_cast<uintptr_t>(src);
-        const uint32_t slot = rb + (uint32_t)((cl * p.NI + ii) * p.raw_bytes);
-        const int sh = (int)((ra & 15u) >> 2);  // element e of the row is word sh + e of the slot
-        // elements [e_lo, avail) are in the copy (the first and last rows of x
-        // may start before or end after it; those elements come from x)
-        const unsigned long long cbeg = std::max<unsigned long long>(ra & ~15ull, p.x_beg16);
-        const unsigned long long cend = std::min<unsigned long long>((ra + 4ull * p.W + 15ull) & ~15ull, p.x_end16);
-        const int e_lo = cbeg > ra ? (int)((cbeg - ra + 3) / 4) : 0;
-        const int avail = cend > ra ? (int)std::min<unsigned long long>((unsigned long long)p.W, (cend - ra) / 4) : 0;
-        const uint32_t dst0 = sb + (uint32_t)(cl * p.copy_bytes);
-        const uint32_t dst1 = sb + (uint32_t)((RS_CG + cl) * p.copy_bytes);
-        const int r0 = ii * p.seg_a;
-        const int r1 = ii == p.NI - 1 ? tail : r0 + p.seg_a;
-        for (int row = r0 + lane; row < r1; row += 32) {
-            const int a = row - r0;
-            const int e0 = 4 * a + b0 - p.pl;  // phase b0 takes e0 .. e0+3, b0+1 takes e0+1 .. e0+4
-            uint32_t el[5] = {0u, 0u, 0u, 0u, 0u};
-            if (in && a < p.seg_a) {
-                if (e0 >= e_lo && e0 + 4 < avail) {
-                    const int wd = sh + e0;
-                    const uint32_t base = slot + 16u * (uint32_t)(wd >> 2);
-                    uint32_t q[8];
-                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                                 : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]) : "r"(base));
-                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                                 : "=r"(q[4]), "=r"(q[5]), "=r"(q[6]), "=r"(q[7]) : "r"(base + 16u));
-                    const int o = wd & 3;
-#pragma unroll
-                    for (int l = 0; l < 5; ++l)
-                        el[l] = o == 0 ? q[l] : (o == 1 ? q[l + 1] : (o == 2 ? q[l + 2] : q[l + 3]));
-                } else {
-#pragma unroll
-                    for (int l = 0; l < 5; ++l) {
-                        const int e = e0 + l;
-                        if (e >= e_lo && e < avail)
-                            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(el[l]) : "r"(slot + 4u * (uint32_t)(sh + e)));
-                        else if (e >= 0 && e < p.W)
-                            el[l] = __float_as_uint(__ldg(src + e));
-                    }
-                }
-            }
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst0 + 16u * (uint32_t)row), "r"(el[0]),
-                         "r"(el[1]), "r"(el[2]), "r"(el[3])
-                         : "memory");
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst1 + 16u * (uint32_t)row), "r"(el[1]),
-                         "r"(el[2]), "r"(el[3]), "r"(el[4])
-                         : "memory");
-        }
+// or N); rows past the last image segment (read only for unstored outputs)
+// are zeros.  fa_c / fb_c: the fast rows of a row that lies wholly in the
+// staged part of x, for this pass.
+__device__ __forceinline__ void rs_build_one(const RsParams &p, uint8_t *sb, const uint8_t *rb, const RsWalk &st,
+                                             const RsCombo &cb, int fa_c, int fb_c, int lane) {
+    bool in;
+    const float *src = rs_row_ptr(p, st.w, st.t, st.cg, cb.cl, cb.ii, in);
+    const uintptr_t ra = reinterpret_cast<uintptr_t>(src);
+    const int sh = (int)((ra & 15u) >> 2);  // element e of the row is word sh + e of the slot
+    const int e0_0 = 2 * st.w.pass - p.pl;  // element of row 0 of the first phase's copy
+    int e_lo = 0, avail = p.W, fa = fa_c, fb = fb_c;
+    const unsigned long long c_lo = ra & ~15ull, c_hi = (ra + 4ull * p.W + 15ull) & ~15ull;
+    if (!in) {
+        fa = fb = 0;
+    } else if (c_lo < p.x_beg16 || c_hi > p.x_end16) {
+        // the first or last row of x: elements [e_lo, avail) are staged, the
+        // others come from x
+        const unsigned long long cbeg = c_lo > p.x_beg16 ? c_lo : p.x_beg16;
+        const unsigned long long cend = c_hi < p.x_end16 ? c_hi : p.x_end16;
+        e_lo = cbeg > ra ? (int)((cbeg - ra + 3) / 4) : 0;
+        avail = cend > ra ? (int)std::min<unsigned long long>((unsigned long long)p.W, (cend - ra) / 4) : 0;
+        const int lo = e_lo - e0_0;  // fast rows: 4a >= lo and 4a <= hi
+        const int hi = avail - 5 - e0_0;
+        fa = lo > 0 ? (lo + 3) / 4 : 0;
+        fb = hi >= 0 ? std::min(hi / 4 + 1, p.seg_a) : 0;
+        fb = std::max(fb, fa);
     }
+    const int wb = sh + e0_0;           // word of element e0_0 in the slot (may be negative)
+    const int O = wb & 3, g0 = wb >> 2;  // arithmetic shift: floor
+    const int lim = in ? p.seg_a : 0;
+    uint4 *dst0 = reinterpret_cast<uint4 *>(sb + cb.dst0_off);
+    uint4 *dst1 = reinterpret_cast<uint4 *>(sb + cb.dst1_off);
+    const uint4 *raw4 = reinterpret_cast<const uint4 *>(rb + cb.raw_off);
+    const uint32_t *raw1 = reinterpret_cast<const uint32_t *>(rb + cb.raw_off);
+    rs_copy_rows(raw4, raw1, dst0, dst1, cb.rows, fa, fb, g0, O, e0_0, sh, e_lo, avail, lim, src, p.W, lane);
 }
 
-// Warp 0 lane 0 issues the copies: the raw rows of up to stage k + 2 (a ring
-// of three raw buffers, each freed by the builders), then the filter slices
-// of stage k (one TMA box: J rows u apart from packed row R-1-t on, the
-// slices of the stage's channel group).  Warps 1..8 build the stage's shifted
-// row copies from its raw rows and arrive on its full barrier (which also
-// takes the filter bytes).
-__device__ void rs_issue(const RsParams &p, const CUtensorMap *tmA, uint32_t sA, uint32_t sRaw,
-                         uint64_t *empty, uint64_t *full, uint64_t *rawfull, uint64_t *rawempty,
-                         const WaitCtl &ctl) {
-    const int ST = p.stages;
+// One lane's bounded wait, its outcome shared with the warp.
+__device__ __forceinline__ bool rs_warp_wait(uint64_t *bar, uint32_t parity, const WaitCtl &ctl, int where,
+                                             int lane) {
+    int ok = 0;
+    if (lane == 0) ok = mbar_wait(bar, parity, ctl, where) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Warp 0 bulk-copies the raw rows of the stages in order, each into one of
+// RS_RAW buffers once the builders have freed it.  The builders (warps 1..8)
+// build a stage's shifted row copies from its raw rows and arrive on its full
+// barrier.
+__device__ void rs_copy_stages(const RsParams &p, uint32_t sRaw, uint64_t *rawfull, uint64_t *rawempty,
+                               const WaitCtl &ctl, int lane) {
     volatile int no_abort = 0;
     const WaitCtl drain{&no_abort, p.err, p.timeout_ns};
-    RsWalk a, r;  // the stage whose filters come next, and whose raw rows come next
-    a.first(p);
-    r = a;
-    int kr = 0, stage = 0;
-    uint32_t ph = 0;
+    RsWalk r;
+    r.first(p);
+    int kr = 0;
     bool ok = true;
-    for (int k = 0; ok && a.valid; ++k) {
-        // raw rows up to stage k + RS_RAW_LAG, each into a buffer the builders freed
-        while (ok && r.valid && kr <= k + RS_RAW_LAG) {
-            if (kr >= RS_RAW)
-                ok = mbar_wait(&rawempty[kr % RS_RAW], (uint32_t)((kr / RS_RAW) - 1) & 1u, ctl, 36);
-            if (!ok) break;
-            fence_proxy_async_smem();
-            rs_copy_raw(p, sRaw + (uint32_t)(kr % RS_RAW) * (uint32_t)p.raw_stage, r, &rawfull[kr % RS_RAW]);
-            ++kr;
-            r.next(p);
-        }
+    for (; ok && r.valid; ++kr, r.next(p)) {
+        if (kr >= RS_RAW) ok = rs_warp_wait(&rawempty[kr % RS_RAW], (uint32_t)((kr / RS_RAW) - 1) & 1u, ctl, 36, lane);
         if (!ok) break;
-        ok = mbar_wait(&empty[stage], ph ^ 1u, ctl, 31);
-        if (!ok) break;
-        // the issuer's arrival carries the filter bytes, so the stage cannot
-        // complete on the builders' arrivals alone
-        mbar_arrive_expect_tx(&full[stage], (uint32_t)p.a_stage);
-        tma_load_4d_u32(sA + (uint32_t)stage * p.a_stage, tmA, &full[stage], 0, 0, p.R - 1 - a.t,
-                        a.cg * p.mpg);
-        if (++stage == ST) stage = 0, ph ^= 1u;
-        a.next(p);
+        fence_proxy_async_smem();
+        rs_copy_raw(p, sRaw + (uint32_t)(kr % RS_RAW) * (uint32_t)p.raw_stage, r, &rawfull[kr % RS_RAW], lane);
     }
     // no copy may land after the CTA exits: wait for each raw buffer's last copy
-    for (int j = kr > RS_RAW ? kr - RS_RAW : 0; j < kr; ++j)
-        mbar_wait(&rawfull[j % RS_RAW], (uint32_t)(j / RS_RAW) & 1u, drain, 93);
+    if (lane == 0)
+        for (int j = kr > RS_RAW ? kr - RS_RAW : 0; j < kr; ++j)
+            mbar_wait(&rawfull[j % RS_RAW], (uint32_t)(j / RS_RAW) & 1u, drain, 93);
+    __syncwarp();
 }
 
-__device__ void rs_build(const RsParams &p, uint32_t sB, uint32_t sRaw, uint64_t *full, uint64_t *empty,
+// One thread loads each stage's filter slices once its buffers are free
+// (one TMA box: J rows u apart from packed row R-1-t on, the stage's channel
+// group's columns); its arrival on the full barrier carries their bytes, so
+// the stage cannot complete on the builders' arrivals alone.
+__device__ void rs_load_filters(const RsParams &p, const CUtensorMap *tmA, uint32_t sA, uint64_t *empty,
+                                uint64_t *full, const WaitCtl &ctl) {
+    const int ST = p.stages;
+    RsWalk a;
+    a.first(p);
+    int stage = 0;
+    uint32_t ph = 0;
+    for (; a.valid; a.next(p)) {
+        if (!mbar_wait(&empty[stage], ph ^ 1u, ctl, 31)) break;
+        mbar_arrive_expect_tx(&full[stage], (uint32_t)p.a_stage);
+        tma_load_4d_u32(sA + (uint32_t)stage * p.a_stage, tmA, &full[stage], 0, 0, p.R - 1 - a.t, a.cg * p.acols);
+        if (++stage == ST) stage = 0, ph ^= 1u;
+    }
+}
+
+__device__ void rs_build(const RsParams &p, uint8_t *sB, const uint8_t *sRaw, uint64_t *full, uint64_t *empty,
                          uint64_t *rawfull, uint64_t *rawempty, const WaitCtl &ctl) {
     const int warp = (threadIdx.x >> 5) - 1, lane = threadIdx.x & 31;
     const int ST = p.stages;
+    const int combos = RS_CG * p.NI;
+    // the fast rows of a wholly staged row, per pass (phases 0-1, 2-3)
+    int fa_c[2], fb_c[2];
+    for (int ps = 0; ps < 2; ++ps) {
+        const int e0_0 = 2 * ps - p.pl;
+        fa_c[ps] = e0_0 < 0 ? (3 - e0_0) / 4 : 0;
+        const int hi = p.W - 5 - e0_0;
+        fb_c[ps] = std::max(hi >= 0 ? std::min(hi / 4 + 1, p.seg_a) : 0, fa_c[ps]);
+    }
+    RsCombo mine;  // the warp's pair when there is at most one per warp
+    if (warp < combos) mine.set(p, warp);
     int stage = 0;
     uint32_t ph = 0;
     RsWalk cur;
@@ -317,8 +412,15 @@ __device__ void rs_build(const RsParams &p, uint32_t sB, uint32_t sRaw, uint64_t
                      "bar.red.or.pred r, 1, %2, q;\n\tselp.b32 %0, 1, 0, r;\n\t}\n"
                      : "=r"(stop) : "r"(stop), "n"(RS_BUILD_WARPS * 32) : "memory");
         if (stop) break;
-        rs_build_b(p, sB + (uint32_t)stage * p.b_stage, sRaw + (uint32_t)(k % RS_RAW) * (uint32_t)p.raw_stage,
-                   rs_unit(p, cur.u), cur.t, cur.cg, warp, lane);
+        uint8_t *sb = sB + (size_t)stage * p.b_stage;
+        const uint8_t *rb = sRaw + (size_t)(k % RS_RAW) * p.raw_stage;
+        const int ps = cur.w.pass;
+        if (warp < combos) rs_build_one(p, sb, rb, cur, mine, fa_c[ps], fb_c[ps], lane);
+        for (int cmb = warp + RS_BUILD_WARPS; cmb < combos; cmb += RS_BUILD_WARPS) {
+            RsCombo cb;
+            cb.set(p, cmb);
+            rs_build_one(p, sb, rb, cur, cb, fa_c[ps], fb_c[ps], lane);
+        }
         fence_proxy_async_smem();  // the copies, for the tensor core
         mbar_arrive(&full[stage]);
         mbar_arrive(&rawempty[k % RS_RAW]);
@@ -329,21 +431,26 @@ __device__ void rs_build(const RsParams &p, uint32_t sB, uint32_t sRaw, uint64_t
 
 __device__ void rs_mma(const RsParams &p, uint32_t tmem_base, uint32_t sA, uint32_t sB, uint64_t *full,
                        uint64_t *empty, uint64_t *tfull, uint64_t *tempty, uint64_t *mma_done,
-                       volatile uint64_t *dtab, const WaitCtl &ctl) {
+                       const WaitCtl &ctl) {
     const int ST = p.stages;
-    // A: 32-byte swizzled K-major slices of 128 rows x 32 bytes (8-row groups 256 bytes apart)
-    const uint64_t a_hi = (1ull << 16) | ((uint64_t)(256 >> 4) << 32) | (1ull << 46) | (6ull << 61);
+    // A: 128-byte swizzled K-major, 128 rows of 128 bytes per column (8-row
+    // groups 1024 bytes apart); MMA i reads the 32 bytes at (i % 4) * 32 of
+    // column i / 4
+    const uint64_t a0 = (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61) |
+                        (uint64_t)((sA >> 4) & 0x3FFFu);
     // B: no swizzle, 16-byte rows, 8-row core matrices 128 bytes apart; the
-    // leading offset (second chunk) per MMA
+    // leading offset (second chunk) per MMA.  The stage-0 descriptors of a
+    // stage's MMAs stay in registers.
     const uint64_t b_hi = ((uint64_t)(128 >> 4) << 32) | (1ull << 46);
-    // the stage-0 descriptors of every MMA of a stage, in shared memory
-    for (int i = 0; i < p.mpg; ++i) {
-        dtab[i] = a_hi | (uint64_t)(((sA + 4096u * (uint32_t)i) >> 4) & 0x3FFFu);
+    uint64_t bd[2][RS_MAX_MPG];
+#pragma unroll
+    for (int i = 0; i < RS_MAX_MPG; ++i)
+#pragma unroll
         for (int q = 0; q < 2; ++q)
-            dtab[RS_MAX_MPG * (1 + q) + i] =
-                b_hi | (uint64_t)(((sB + (uint32_t)(q * RS_CG * p.copy_bytes) + p.b_off[i]) >> 4) & 0x3FFFu) |
-                ((uint64_t)((p.b_lbo[i] >> 4) & 0x3FFFu) << 16);
-    }
+            bd[q][i] = i < p.mpg ? (b_hi |
+                                    (uint64_t)(((sB + (uint32_t)(q * RS_CG * p.copy_bytes) + p.b_off[i]) >> 4) & 0x3FFFu) |
+                                    ((uint64_t)((p.b_lbo[i] >> 4) & 0x3FFFu) << 16))
+                                 : 0ull;
     int stage = 0, it = 0;
     uint32_t ph = 0;
     bool ok = true;
@@ -366,14 +473,15 @@ __device__ void rs_mma(const RsParams &p, uint32_t tmem_base, uint32_t sA, uint3
                 // start fields move by whole stages (addresses below 256 KiB: no carry)
                 const uint64_t ao = (uint64_t)(((uint32_t)stage * (uint32_t)p.a_stage) >> 4);
                 const uint64_t bo = (uint64_t)(((uint32_t)stage * (uint32_t)p.b_stage) >> 4);
-#pragma unroll 1
+#pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     const uint32_t d = tmem_base + (uint32_t)(q * p.Nmma);
-                    const volatile uint64_t *bt = dtab + RS_MAX_MPG * (1 + q);
-#pragma unroll 1
-                    for (int i = 0; i < p.mpg; ++i) {
+#pragma unroll
+                    for (int i = 0; i < RS_MAX_MPG; ++i) {
                         // the unit's first MMA into each accumulator starts it
-                        umma_tf32_nc(d, dtab[i] + ao, bt[i] + bo, p.idesc, (acc | (uint32_t)i) ? 1u : 0u);
+                        if (i < p.mpg)
+                            umma_tf32_nc(d, a0 + ao + (uint64_t)(1024 * (i >> 2) + 2 * (i & 3)), bd[q][i] + bo, p.idesc,
+                                         (acc | (uint32_t)i) ? 1u : 0u);
                     }
                 }
                 acc = 1;
@@ -490,7 +598,7 @@ __global__ void __launch_bounds__(RS_THREADS, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == RS_PROD_WARPS) {
+    if (warp == RS_MMA_WARP) {
         tmem_alloc(tmem_slot, p.tmem_cols);
         tmem_relinquish();
     }
@@ -500,16 +608,17 @@ __global__ void __launch_bounds__(RS_THREADS, 1)
     const uint32_t tmem_base = *tmem_slot;
     const WaitCtl ctl{abort_flag, p.err, p.timeout_ns};
     if (warp == 0) {
+        rs_copy_stages(p, smem_u32(smRaw), rawfull, rawempty, ctl, lane);
+    } else if (warp == RS_A_WARP) {
         if (lane == 0) {
             prefetch_tmap(&tmA);
-            rs_issue(p, &tmA, smem_u32(smA), smem_u32(smRaw), empty, full, rawfull, rawempty, ctl);
+            rs_load_filters(p, &tmA, smem_u32(smA), empty, full, ctl);
         }
     } else if (warp < RS_PROD_WARPS) {
-        rs_build(p, smem_u32(smB), smem_u32(smRaw), full, empty, rawfull, rawempty, ctl);
-    } else if (warp == RS_PROD_WARPS) {
+        rs_build(p, smB, smRaw, full, empty, rawfull, rawempty, ctl);
+    } else if (warp == RS_MMA_WARP) {
         if (lane == 0)
-            rs_mma(p, tmem_base, smem_u32(smA), smem_u32(smB), full, empty, tfull, tempty, mma_done,
-                   reinterpret_cast<volatile uint64_t *>(reinterpret_cast<uint8_t *>(bars) + 256), ctl);
+            rs_mma(p, tmem_base, smem_u32(smA), smem_u32(smB), full, empty, tfull, tempty, mma_done, ctl);
     } else {
         rs_epilogue(p, tmem_base, tfull, tempty, ctl);
     }
@@ -517,33 +626,35 @@ __global__ void __launch_bounds__(RS_THREADS, 1)
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    if (warp == RS_PROD_WARPS) tmem_dealloc(tmem_base, p.tmem_cols);
+    if (warp == RS_MMA_WARP) tmem_dealloc(tmem_base, p.tmem_cols);
 }
 
-// The filters as MMA A slices, in the order the convolution's TMA box reads
-// them: image [m][rr][k][8] (m = MMA slice over (channel group, MMA), rr =
-// R-1-r, k < K_pad filters, 8 reduction elements), each element the filter
-// tap of its (channel, s) chunk or zero.  One thread per element.
+// The filters as MMA A operands, in the order the convolution's TMA box reads
+// them: image [m][rr][k][32] (m = (channel group, 128-byte column), rr =
+// R-1-r, k < K_pad filters, 32 reduction elements: four MMAs' 8 each), each
+// element the filter tap of its (channel, s) chunk or zero.  One thread per
+// element.
 __global__ void rowstack_pack_filters(const __grid_constant__ RsParams p, const float *w, long long ws0,
                                       long long ws1, long long ws2, long long ws3, float *img) {
     griddep_wait();  // the previous convolution may still read the image
     griddep_launch_dependents();
-    const long long total = (long long)p.groups * p.mpg * p.R * p.K_pad * 8;
+    const long long total = (long long)p.groups * p.acols * p.R * p.K_pad * 32;
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= total) return;
-    const int e = (int)(i & 7);
-    long long t = i >> 3;
+    const int f = (int)(i & 31);
+    long long t = i >> 5;
     const int k = (int)(t % p.K_pad);
     t /= p.K_pad;
     const int rr = (int)(t % p.R);
     const int m = (int)(t / p.R);
-    const int cg = m / p.mpg, mi = m - cg * p.mpg;
+    const int cg = m / p.acols, col = m - cg * p.acols;
+    const int mi = 4 * col + (f >> 3), e = f & 7;  // MMA of the stage, its element
     const int chunk = 2 * mi + (e >> 2);
     const int c = cg * RS_CG + chunk / p.cpc;
     const int s = 4 * (chunk % p.cpc) + (e & 3);
     const int r = p.R - 1 - rr;
     float v = 0.f;
-    if (k < p.K && c < p.C && s < p.S)
+    if (mi < p.mpg && k < p.K && c < p.C && s < p.S)
         v = __ldg(w + (long long)k * ws0 + (long long)c * ws1 + (long long)r * ws2 + (long long)s * ws3);
     img[i] = v;
 }
@@ -581,7 +692,8 @@ bool rowstack_plan(const ConvProblem &pb, size_t wpack_bytes, RsParams *out, siz
     p.copy_bytes = (p.Nmma + p.cpc - 1) * 16;
     p.copy_bytes = ((p.copy_bytes + 127) / 128) * 128;
     p.b_stage = 2 * RS_CG * p.copy_bytes;
-    p.a_stage = p.mpg * 4096;
+    p.acols = (p.mpg + 3) / 4;
+    p.a_stage = p.acols * 16384;
     p.raw_bytes = ((pb.W * 4 + 15 + 15) / 16) * 16;
     p.raw_stage = RS_CG * p.NI * p.raw_bytes;
     const int stage = p.a_stage + p.b_stage;
@@ -596,11 +708,23 @@ bool rowstack_plan(const ConvProblem &pb, size_t wpack_bytes, RsParams *out, siz
     }
     p.row_blocks = (pb.P + p.J - 1) / p.J;
     p.img_groups = (pb.N + p.NI - 1) / p.NI;
+    if (p.row_blocks <= RS_MAX_RB) {
+        // input rows of each row block inside the image: its stages
+        int rows_in[RS_MAX_RB];
+        for (int b = 0; b < p.row_blocks; ++b) {
+            const int h0 = b * p.J * pb.u - pb.pt;
+            rows_in[b] = std::max(0, std::min(h0 + p.T, pb.H) - std::max(h0, 0));
+            p.row_order[b] = (unsigned short)b;
+        }
+        std::stable_sort(p.row_order, p.row_order + p.row_blocks,
+                         [&](unsigned short a, unsigned short b) { return rows_in[a] > rows_in[b]; });
+        p.sorted = 1;
+    }
     const long long tiles = (long long)p.row_blocks * p.img_groups;
     if (tiles * 2 > 0x7fffffffLL) return false;
     p.tiles = (int)tiles;
     p.units = 2 * p.tiles;
-    const long long img = (long long)p.groups * p.mpg * pb.R * p.K_pad * 32;
+    const long long img = (long long)p.groups * p.acols * pb.R * p.K_pad * 128;
     if (img > (long long)wpack_bytes) return false;
     if (p.J * pb.u > 256 || pb.u > 8) return false;  // the filter box's strided rows
     uint32_t cols = 32;
@@ -656,22 +780,22 @@ dlcStatus_t dlc_launch_rowstack(dlcContext *ctx, const ConvProblem &pb) {
     p.timeout_ns = ctx->timeout_ns;
 
     float *img = static_cast<float *>(ctx->wpack);
-    // the packed image as {8 elements, K_pad filters, R rows, slices}; the
+    // the packed image as {32 elements, K_pad filters, R rows, columns}; the
     // box takes J rows u apart (element stride u along the rows) and a
-    // stage's mpg slices, 32-byte swizzled
+    // stage's columns, 128-byte swizzled
     CUtensorMap ta;
     std::memset(&ta, 0, sizeof(ta));
-    const int slices = p.groups * p.mpg;
-    const cuuint64_t dim[4] = {8, (cuuint64_t)p.K_pad, (cuuint64_t)pb.R, (cuuint64_t)slices};
-    const cuuint64_t str[3] = {32, (cuuint64_t)p.K_pad * 32, (cuuint64_t)pb.R * p.K_pad * 32};
-    const cuuint32_t box[4] = {8, (cuuint32_t)p.K_pad, (cuuint32_t)(p.J * pb.u), (cuuint32_t)p.mpg};
+    const int slices = p.groups * p.acols;
+    const cuuint64_t dim[4] = {32, (cuuint64_t)p.K_pad, (cuuint64_t)pb.R, (cuuint64_t)slices};
+    const cuuint64_t str[3] = {128, (cuuint64_t)p.K_pad * 128, (cuuint64_t)pb.R * p.K_pad * 128};
+    const cuuint32_t box[4] = {32, (cuuint32_t)p.K_pad, (cuuint32_t)(p.J * pb.u), (cuuint32_t)p.acols};
     const cuuint32_t estr[4] = {1, 1, (cuuint32_t)pb.u, 1};
     if (ctx->encode_tiled(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, img, dim, str, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return DLC_STATUS_EXECUTION_FAILED;
     {
-        const long long total = (long long)slices * pb.R * p.K_pad * 8;
+        const long long total = (long long)slices * pb.R * p.K_pad * 32;
         cudaLaunchConfig_t cfg;
         std::memset(&cfg, 0, sizeof(cfg));
         cudaLaunchAttribute attr[1];

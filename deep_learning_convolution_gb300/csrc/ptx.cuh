@@ -78,6 +78,27 @@ struct WaitCtl {
     unsigned long long timeout_ns;   // limit of one wait
 };
 
+// The same test, but a thread whose phase is not yet complete is suspended
+// until it completes or `hint_ns` nanoseconds pass.  A waiting warp then takes
+// no issue slots from the warps that share its scheduler (a plain try_wait
+// returns after a short, system-chosen time, and a loop around it keeps the
+// warp eligible for issue the whole time it waits).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Longest suspension of one try_wait inside a bounded wait: the abort flag
+// and the time limit are looked at this often.
+constexpr uint32_t kWaitSleepNs = 20000;
+
 // Waits for the phase of `bar` with the given parity to complete.  Gives up
 // (returns false) when another role has aborted or after ctl.timeout_ns, in
 // which case it records DLC_DEVERR_WAIT_TIMEOUT with `where` and raises the
@@ -86,16 +107,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
                                           int where) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    uint32_t n = 0;
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((++n & 31u) == 0) {
-            if (*ctl.abort_flag) return false;
-            if (globaltimer_ns() - t0 > ctl.timeout_ns) {
-                *ctl.abort_flag = 1;
-                record_error(ctl.err, 1 /* DLC_DEVERR_WAIT_TIMEOUT */, where);
-                return false;
-            }
+        if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
+        if (*ctl.abort_flag) return false;
+        if (globaltimer_ns() - t0 > ctl.timeout_ns) {
+            *ctl.abort_flag = 1;
+            record_error(ctl.err, 1 /* DLC_DEVERR_WAIT_TIMEOUT */, where);
+            return false;
         }
     }
 }
@@ -115,20 +133,29 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t pa
     return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_try_wait_cluster_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, const WaitCtl &ctl,
                                                   int where) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    uint32_t n = 0;
     while (true) {
-        if (mbar_try_wait_cluster(bar, parity)) return true;
-        if ((++n & 31u) == 0) {
-            if (*ctl.abort_flag) return false;
-            if (globaltimer_ns() - t0 > ctl.timeout_ns) {
-                *ctl.abort_flag = 1;
-                record_error(ctl.err, 1 /* DLC_DEVERR_WAIT_TIMEOUT */, where);
-                return false;
-            }
+        if (mbar_try_wait_cluster_sleep(bar, parity, kWaitSleepNs)) return true;
+        if (*ctl.abort_flag) return false;
+        if (globaltimer_ns() - t0 > ctl.timeout_ns) {
+            *ctl.abort_flag = 1;
+            record_error(ctl.err, 1 /* DLC_DEVERR_WAIT_TIMEOUT */, where);
+            return false;
         }
     }
 }

@@ -26,8 +26,11 @@ MODE_CASES = [
        pad_right=0), "tc_im2col_pair"),
     (L("cm_window_c3_11x11_s4", 2, 3, 47, 47, 64, 11, 11, pad_top=2, pad_bottom=2, pad_left=2,
        pad_right=2, u=4, v=4), "tc_window"),
-    (L("cm_gather_tf32_nchw_c32", 2, 32, 13, 11, 40, 3, 5, **P1, dtype="tf32", layout="NCHW"),
+    # more than 64 filters: past the row-stack kernel's limit
+    (L("cm_gather_tf32_nchw_c32", 2, 32, 13, 11, 72, 3, 5, **P1, dtype="tf32", layout="NCHW"),
      "tc_gather"),
+    (L("cm_rowstack_tf32_nchw_c32", 2, 32, 13, 11, 40, 3, 5, **P1, dtype="tf32", layout="NCHW"),
+     "tc_rowstack"),
     (L("cm_ffma_nchw", 2, 8, 16, 16, 16, 3, 3, **P1, dtype="f32", layout="NCHW"), "ffma"),
 ]
 
