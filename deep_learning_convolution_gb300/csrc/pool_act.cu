@@ -124,17 +124,18 @@ __device__ __forceinline__ void store_vec(TO *dst, const A (&v)[V]) {
 
 // Channels-innermost pooling: one thread per (output pixel, 16-byte chunk of
 // channels); C * sizeof(TI) is a multiple of 16 and both bases 16-byte aligned.
-template <typename TI, typename TO>
+// I: the index type of the output enumeration (32-bit when the count fits,
+// whose divisions are far cheaper than 64-bit ones).
+template <typename TI, typename TO, typename I>
 __global__ void __launch_bounds__(256) pool_nhwc_kernel(const __grid_constant__ PoolParams p) {
     using A = typename Io<TI>::acc;
     constexpr int V = 16 / (int)sizeof(TI);
     const TI *x = static_cast<const TI *>(p.x);
     TO *y = static_cast<TO *>(p.y);
     const int chunks = p.C / V;
-    const long long total = (long long)p.N * p.P * p.Q * chunks;
-    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-         idx += (long long)gridDim.x * blockDim.x) {
-        long long t = idx;
+    const I total = (I)((long long)p.N * p.P * p.Q * chunks);
+    for (I idx = (I)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (I)gridDim.x * blockDim.x) {
+        I t = idx;
         const int ch = (int)(t % chunks); t /= chunks;
         const int oq = (int)(t % p.Q); t /= p.Q;
         const int op = (int)(t % p.P);
@@ -180,16 +181,15 @@ __global__ void __launch_bounds__(256) pool_nhwc_kernel(const __grid_constant__ 
 
 // Any layout: one output element per thread, outputs enumerated with the
 // unit-stride axis of y innermost.
-template <typename TI, typename TO>
+template <typename TI, typename TO, typename I>
 __global__ void __launch_bounds__(256) pool_any_kernel(const __grid_constant__ PoolParams p,
                                                        int c_fastest) {
     using A = typename Io<TI>::acc;
     const TI *x = static_cast<const TI *>(p.x);
     TO *y = static_cast<TO *>(p.y);
-    const long long total = (long long)p.N * p.C * p.P * p.Q;
-    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-         idx += (long long)gridDim.x * blockDim.x) {
-        long long t = idx;
+    const I total = (I)((long long)p.N * p.C * p.P * p.Q);
+    for (I idx = (I)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (I)gridDim.x * blockDim.x) {
+        I t = idx;
         int n, c, op, oq;
         if (c_fastest) {
             c = (int)(t % p.C); t /= p.C;
@@ -288,15 +288,14 @@ __global__ void __launch_bounds__(256) act_flat_kernel(const __grid_constant__ A
     }
 }
 
-template <typename TI, typename TO>
+template <typename TI, typename TO, typename I>
 __global__ void __launch_bounds__(256) act_any_kernel(const __grid_constant__ ActParams p) {
     using A = typename Io<TI>::acc;
     const TI *x = static_cast<const TI *>(p.x);
     TO *y = static_cast<TO *>(p.y);
-    const long long total = (long long)p.N * p.C * p.H * p.W;
-    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-         idx += (long long)gridDim.x * blockDim.x) {
-        long long t = idx;
+    const I total = (I)((long long)p.N * p.C * p.H * p.W);
+    for (I idx = (I)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (I)gridDim.x * blockDim.x) {
+        I t = idx;
         const int wi = (int)(t % p.W); t /= p.W;
         const int h = (int)(t % p.H); t /= p.H;
         const int c = (int)(t % p.C);
@@ -319,12 +318,20 @@ int grid_of(const dlcContext *ctx, long long work) {
 
 template <typename TI, typename TO>
 cudaError_t launch_pool(const dlcContext *ctx, const PoolParams &p, bool nhwc) {
+    // 32-bit enumeration while the count and the grid-stride step stay below 2^31
+    constexpr long long kSmall = 1LL << 30;
     if (nhwc) {
         const long long work = (long long)p.N * p.P * p.Q * (p.C / (16 / (int)sizeof(TI)));
-        pool_nhwc_kernel<TI, TO><<<grid_of(ctx, work), 256, 0, ctx->stream>>>(p);
+        if (work < kSmall)
+            pool_nhwc_kernel<TI, TO, int><<<grid_of(ctx, work), 256, 0, ctx->stream>>>(p);
+        else
+            pool_nhwc_kernel<TI, TO, long long><<<grid_of(ctx, work), 256, 0, ctx->stream>>>(p);
     } else {
         const long long work = (long long)p.N * p.C * p.P * p.Q;
-        pool_any_kernel<TI, TO><<<grid_of(ctx, work), 256, 0, ctx->stream>>>(p, p.ys[1] == 1 ? 1 : 0);
+        if (work < kSmall)
+            pool_any_kernel<TI, TO, int><<<grid_of(ctx, work), 256, 0, ctx->stream>>>(p, p.ys[1] == 1 ? 1 : 0);
+        else
+            pool_any_kernel<TI, TO, long long><<<grid_of(ctx, work), 256, 0, ctx->stream>>>(p, p.ys[1] == 1 ? 1 : 0);
     }
     return cudaGetLastError();
 }
@@ -335,7 +342,11 @@ cudaError_t launch_act(const dlcContext *ctx, const ActParams &p, long long flat
         act_flat_kernel<TI, TO><<<grid_of(ctx, flat_n / (16 / (long long)sizeof(TI)) + 1), 256, 0,
                                   ctx->stream>>>(p, flat_n);
     } else {
-        act_any_kernel<TI, TO><<<grid_of(ctx, (long long)p.N * p.C * p.H * p.W), 256, 0, ctx->stream>>>(p);
+        const long long work = (long long)p.N * p.C * p.H * p.W;
+        if (work < (1LL << 30))
+            act_any_kernel<TI, TO, int><<<grid_of(ctx, work), 256, 0, ctx->stream>>>(p);
+        else
+            act_any_kernel<TI, TO, long long><<<grid_of(ctx, work), 256, 0, ctx->stream>>>(p);
     }
     return cudaGetLastError();
 }
