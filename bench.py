@@ -78,10 +78,30 @@ def load_peaks():
             "source": "fallback"}
 
 
-def kernel_source_hash():
+# The sources each kernel's device code is built from (beside the shared
+# headers): a DRAM-traffic figure in profiles/traffic.json stays valid while
+# these files are unchanged.
+KERNEL_SOURCES = {
+    "tc_im2col_pair": ["conv_pair.cu"],
+    "tc_im2col": ["conv_tc.cu"], "tc_gather_runs": ["conv_tc.cu"], "tc_gather": ["conv_tc.cu"],
+    "tc_window": ["conv_window.cu"],
+    "tc_rowstack": ["conv_rowstack.cu"],
+    "ffma": ["conv_ffma.cu"],
+    "tc_wgrad": ["conv_wgrad.cu"], "direct": ["conv_bwd.cu"],
+    "pool_nhwc": ["pool_act.cu"], "flat": ["pool_act.cu"],
+}
+SHARED_SOURCES = ["ptx.cuh", "internal.h"]
+
+
+def kernel_source_hash(kernel=None):
+    """Hash of the sources of `kernel` and the shared headers (all sources when
+    the kernel is not listed)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "deep_learning_convolution_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    files = sorted(os.listdir(csrc))
+    if kernel in KERNEL_SOURCES:
+        files = sorted(set(KERNEL_SOURCES[kernel] + SHARED_SOURCES))
+    for f in files:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -326,7 +346,7 @@ def run_workload(args, workload, handle, stream, dev, rank, world, local_rank, h
         with open(tfile) as f:
             td = json.load(f)
         ent = td.get(workload, {}).get(dom_name)
-        if ent and ent.get("kernel_sha") == kernel_source_hash():
+        if ent and ent.get("kernel_sha") == kernel_source_hash(dom_name):
             traffic = ent.get("dram_bytes_per_launch")
     if compute_bound:
         achieved = flops_per_launch / avg_launch_s / 1e12
