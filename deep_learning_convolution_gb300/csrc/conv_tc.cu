@@ -1251,8 +1251,10 @@ dlcKernel_t dlc_tc_variant(const dlcContext *ctx, const ConvProblem &pb) {
         if (dlc_pair_enabled(ctx)) return DLC_KERNEL_TC_IM2COL_PAIR;
         if (!pb.flip) return DLC_KERNEL_TC_IM2COL;
     }
-    if (dlc_window_ok(pb)) return DLC_KERNEL_TC_WINDOW;
+    // channel-planar TF32 layers with few filters: the row-stack kernel's
+    // MMAs are 192-256 pixels wide where the window kernel's are 64
     if (dlc_rowstack_ok(ctx, pb)) return DLC_KERNEL_TC_ROWSTACK;
+    if (dlc_window_ok(pb)) return DLC_KERNEL_TC_WINDOW;
     int a, b, c;
     if (!pb.flip && runs_ok(pb, &a, &b, &c)) return DLC_KERNEL_TC_GATHER_RUNS;
     return DLC_KERNEL_TC_GATHER;

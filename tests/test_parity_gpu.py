@@ -189,6 +189,18 @@ ROWSTACK_CASES = [
     L("rs_c36_k64_7x12", 2, 36, 15, 55, 64, 7, 12, **P(3, 1, 4, 2), dtype="tf32", layout="NCHW"),
     # a single output row and column per image
     L("rs_c24_k32_3x3_tiny", 3, 24, 3, 3, 32, 3, 3, dtype="tf32", layout="NCHW"),
+    # horizontal stride 2 (two phases per unit), one channel (four input rows
+    # per stage), a speech-layer-1-like 41x11 filter, Q = 35
+    L("rs_c1_k32_41x11_s2", 2, 1, 47, 70, 32, 41, 11, **P(20, 20, 5, 5), u=2, v=2, dtype="tf32",
+      layout="NCHW"),
+    # two channels (two input rows per stage), stride 1x2, odd width
+    L("rs_c2_k16_5x7_s1x2", 3, 2, 13, 37, 16, 5, 7, **P(2, 2, 3, 3), v=2, dtype="tf32",
+      layout="NCHW"),
+    # three channels and one empty slot, 64 filters, stride 2, 3x5
+    L("rs_c3_k64_3x5_s2", 2, 3, 17, 30, 64, 3, 5, **P(1, 1, 2, 2), u=2, v=2, dtype="tf32",
+      layout="NCHW"),
+    # one channel, stride 1, 48 filters, 7x9
+    L("rs_c1_k48_7x9", 2, 1, 20, 33, 48, 7, 9, **P(3, 3, 4, 4), dtype="tf32", layout="NCHW"),
 ]
 
 
@@ -216,14 +228,21 @@ def test_tc_rowstack_epilogue_and_modes(handle, layer):
 
 
 
+@pytest.fixture
+def no_rowstack(monkeypatch):
+    """The window kernel's channel-planar TF32 cases would go to the row-stack
+    kernel; these tests keep them on the window kernel."""
+    monkeypatch.setenv("DLC_TC_ROWSTACK", "0")
+
+
 @pytest.mark.parametrize("layer", WINDOW_CASES, ids=lambda l: l.name)
-def test_tc_window_parity_full(handle, layer):
+def test_tc_window_parity_full(handle, layer, no_rowstack):
     run_and_check(handle, layer, 2300 + WINDOW_CASES.index(layer), full=True,
                   expect_kernel="tc_window")
 
 
 @pytest.mark.parametrize("layer", [WINDOW_CASES[i] for i in (4, 5, 6, 10, 14, 18)], ids=lambda l: l.name)
-def test_tc_window_word_copies(handle, layer, monkeypatch):
+def test_tc_window_word_copies(handle, layer, monkeypatch, no_rowstack):
     """Rows that could be bulk-staged, copied word by word instead."""
     monkeypatch.setenv("DLC_TC_WINSTAGE", "0")
     run_and_check(handle, layer, 2360 + WINDOW_CASES.index(layer), full=True,
@@ -232,7 +251,7 @@ def test_tc_window_word_copies(handle, layer, monkeypatch):
 
 @pytest.mark.parametrize("layer", [WINDOW_CASES[i] for i in (0, 2, 5, 7, 12, 13, 15, 16, 17, 18)],
                          ids=lambda l: l.name)
-def test_tc_window_cta_pairs(handle, layer, monkeypatch):
+def test_tc_window_cta_pairs(handle, layer, monkeypatch, no_rowstack):
     """CTA pairs sharing each MMA over 256 rows (opt-in)."""
     monkeypatch.setenv("DLC_TC_WINPAIR", "1")
     run_and_check(handle, layer, 2370 + WINDOW_CASES.index(layer), full=True,
@@ -240,7 +259,7 @@ def test_tc_window_cta_pairs(handle, layer, monkeypatch):
 
 
 @pytest.mark.parametrize("y_axes", ["NCHW", "NHWC"])
-def test_tc_window_epilogue(handle, y_axes):
+def test_tc_window_epilogue(handle, y_axes, no_rowstack):
     import torch
     run_and_check(handle, WINDOW_CASES[0], 2390, full=True, y_axes=y_axes, alpha=-0.5,
                   beta=0.75, with_bias=True, relu=True, expect_kernel="tc_window")
@@ -416,7 +435,7 @@ def test_workspace_is_zero_and_kernel_choice(handle):
     expect = {"alexnet": ["tc_window"] + ["tc_im2col_pair"] * 4,
               "overfeat": ["tc_window"] + ["tc_im2col_pair"] * 4,
               "resnet50": ["tc_im2col_pair"] * len(synth.WORKLOADS["resnet50"]),
-              "speech": ["tc_window", "tc_rowstack"], "tiny": ["ffma"]}
+              "speech": ["tc_rowstack", "tc_rowstack"], "tiny": ["ffma"]}
     for wl, kinds in expect.items():
         for layer, kind in zip(synth.WORKLOADS[wl], kinds):
             x, w, _ = synth.make_inputs(layer, 1, batch=1)
