@@ -16,9 +16,11 @@
 // Both are memory-bound: they read x once from DRAM and write y once, so the
 // kernels are sized for bandwidth.  With channels innermost (NHWC) each thread
 // owns 16 bytes of channels of one output pixel and reads the window's pixels
-// as 16-byte vectors (consecutive threads read consecutive bytes); dense
-// tensors of one layout run the activation as a flat array of 16-byte
-// vectors; anything else takes one element per thread through the strides.
+// as 16-byte vectors (consecutive threads read consecutive bytes; a 3 x 3
+// window's nine loads are issued together); dense tensors of one layout run
+// the activation as a flat array of 16-byte vectors, four per thread in
+// flight, one kernel per function; anything else takes one element per
+// thread through the strides.
 // Grids are a multiple of the SM count (grid-stride loops).  Sums and
 // comparisons are in FP32 (FP64 for DOUBLE storage); BF16 is widened exactly.
 #include <cuda_bf16.h>
@@ -125,8 +127,10 @@ __device__ __forceinline__ void store_vec(TO *dst, const A (&v)[V]) {
 // Channels-innermost pooling: one thread per (output pixel, 16-byte chunk of
 // channels); C * sizeof(TI) is a multiple of 16 and both bases 16-byte aligned.
 // I: the index type of the output enumeration (32-bit when the count fits,
-// whose divisions are far cheaper than 64-bit ones).
-template <typename TI, typename TO, typename I>
+// whose divisions are far cheaper than 64-bit ones).  FIX: 0, or the window
+// size when it is FIX x FIX, whose loads are then all issued before the first
+// is used.
+template <typename TI, typename TO, typename I, int FIX>
 __global__ void __launch_bounds__(256) pool_nhwc_kernel(const __grid_constant__ PoolParams p) {
     using A = typename Io<TI>::acc;
     constexpr int V = 16 / (int)sizeof(TI);
@@ -147,19 +151,43 @@ __global__ void __launch_bounds__(256) pool_nhwc_kernel(const __grid_constant__ 
         int count = 0;
         const TI *xn = x + (long long)n * p.xs[0] + (long long)ch * V;
         const int h0 = op * p.u - p.pt, w0 = oq * p.v - p.pl;
-        for (int i = 0; i < p.R; ++i) {
-            const int h = h0 + i;
-            if (h < 0 || h >= p.H) continue;
-            for (int j = 0; j < p.S; ++j) {
-                const int wi = w0 + j;
-                if (wi < 0 || wi >= p.W) continue;
-                const uint4 q4 = __ldg(reinterpret_cast<const uint4 *>(
-                    xn + (long long)h * p.xs[2] + (long long)wi * p.xs[3]));
+        if constexpr (FIX > 0) {
+            uint4 q4[FIX * FIX];
+            bool in[FIX * FIX];
+#pragma unroll
+            for (int i = 0; i < FIX; ++i)
+#pragma unroll
+                for (int j = 0; j < FIX; ++j) {
+                    const int h = h0 + i, wi = w0 + j;
+                    in[i * FIX + j] = h >= 0 && h < p.H && wi >= 0 && wi < p.W;
+                    q4[i * FIX + j] = in[i * FIX + j] ? __ldg(reinterpret_cast<const uint4 *>(
+                                                           xn + (long long)h * p.xs[2] + (long long)wi * p.xs[3]))
+                                                     : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+            for (int t = 0; t < FIX * FIX; ++t) {
+                if (!in[t]) continue;
                 A v[V];
-                unpack16<TI, A, V>(q4, v);
+                unpack16<TI, A, V>(q4[t], v);
 #pragma unroll
                 for (int e = 0; e < V; ++e) acc[e] = is_max ? (v[e] > acc[e] ? v[e] : acc[e]) : acc[e] + v[e];
                 ++count;
+            }
+        } else {
+            for (int i = 0; i < p.R; ++i) {
+                const int h = h0 + i;
+                if (h < 0 || h >= p.H) continue;
+                for (int j = 0; j < p.S; ++j) {
+                    const int wi = w0 + j;
+                    if (wi < 0 || wi >= p.W) continue;
+                    const uint4 q4 = __ldg(reinterpret_cast<const uint4 *>(
+                        xn + (long long)h * p.xs[2] + (long long)wi * p.xs[3]));
+                    A v[V];
+                    unpack16<TI, A, V>(q4, v);
+#pragma unroll
+                    for (int e = 0; e < V; ++e) acc[e] = is_max ? (v[e] > acc[e] ? v[e] : acc[e]) : acc[e] + v[e];
+                    ++count;
+                }
             }
         }
         const A div = p.mode == 1 ? (A)(p.R * p.S) : (A)count;
@@ -250,39 +278,44 @@ __device__ __forceinline__ A act_fn(int mode, A v, A coef) {
     }
 }
 
-// Flat path: x and y dense with the same strides (elements 0 .. n-1 of both).
-template <typename TI, typename TO>
+// Flat path: x and y dense with the same strides (elements 0 .. n-1 of both),
+// one kernel per activation MODE.  Each thread loads four 16-byte vectors
+// before it uses any.
+template <typename TI, typename TO, int MODE>
 __global__ void __launch_bounds__(256) act_flat_kernel(const __grid_constant__ ActParams p, long long n) {
     using A = typename Io<TI>::acc;
     constexpr int V = 16 / (int)sizeof(TI);
+    constexpr int U = 4;
     const TI *x = static_cast<const TI *>(p.x);
     TO *y = static_cast<TO *>(p.y);
     const long long nv = n / V;
     const A alpha = (A)p.alpha, beta = (A)p.beta, coef = (A)p.coef;
     const long long stride = (long long)gridDim.x * blockDim.x;
-    // two vectors per thread and iteration, both loads issued before any use
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += 2 * stride) {
-        const long long i2 = i + stride;
-        const uint4 qa = __ldg(reinterpret_cast<const uint4 *>(x) + i);
-        const uint4 qb = i2 < nv ? __ldg(reinterpret_cast<const uint4 *>(x) + i2) : make_uint4(0, 0, 0, 0);
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += U * stride) {
+        uint4 q[U];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const long long j = h ? i2 : i;
-            if (j >= nv) break;
+        for (int h = 0; h < U; ++h) {
+            const long long jv = i + h * stride;
+            q[h] = jv < nv ? __ldg(reinterpret_cast<const uint4 *>(x) + jv) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int h = 0; h < U; ++h) {
+            const long long jv = i + h * stride;
+            if (jv >= nv) break;
             A v[V];
-            unpack16<TI, A, V>(h ? qb : qa, v);
+            unpack16<TI, A, V>(q[h], v);
 #pragma unroll
             for (int e = 0; e < V; ++e) {
-                v[e] = alpha * act_fn<A>(p.mode, v[e], coef);
-                if (beta != (A)0) v[e] += beta * (A)Io<TO>::ld(y, j * V + e);
+                v[e] = alpha * act_fn<A>(MODE, v[e], coef);
+                if (beta != (A)0) v[e] += beta * (A)Io<TO>::ld(y, jv * V + e);
             }
-            store_vec<TO, A, V>(y + j * V, v);
+            store_vec<TO, A, V>(y + jv * V, v);
         }
     }
     // the tail of fewer than V elements
     for (long long i = nv * V + (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (long long)gridDim.x * blockDim.x) {
-        A val = alpha * act_fn<A>(p.mode, (A)Io<TI>::ld(x, i), coef);
+        A val = alpha * act_fn<A>(MODE, (A)Io<TI>::ld(x, i), coef);
         if (beta != (A)0) val += beta * (A)Io<TO>::ld(y, i);
         Io<TO>::st(y, i, val);
     }
@@ -322,10 +355,12 @@ cudaError_t launch_pool(const dlcContext *ctx, const PoolParams &p, bool nhwc) {
     constexpr long long kSmall = 1LL << 30;
     if (nhwc) {
         const long long work = (long long)p.N * p.P * p.Q * (p.C / (16 / (int)sizeof(TI)));
-        if (work < kSmall)
-            pool_nhwc_kernel<TI, TO, int><<<grid_of(ctx, work), 256, 0, ctx->stream>>>(p);
+        if (work < kSmall && p.R == 3 && p.S == 3)
+            pool_nhwc_kernel<TI, TO, int, 3><<<grid_of(ctx, work), 256, 0, ctx->stream>>>(p);
+        else if (work < kSmall)
+            pool_nhwc_kernel<TI, TO, int, 0><<<grid_of(ctx, work), 256, 0, ctx->stream>>>(p);
         else
-            pool_nhwc_kernel<TI, TO, long long><<<grid_of(ctx, work), 256, 0, ctx->stream>>>(p);
+            pool_nhwc_kernel<TI, TO, long long, 0><<<grid_of(ctx, work), 256, 0, ctx->stream>>>(p);
     } else {
         const long long work = (long long)p.N * p.C * p.P * p.Q;
         if (work < kSmall)
@@ -339,8 +374,14 @@ cudaError_t launch_pool(const dlcContext *ctx, const PoolParams &p, bool nhwc) {
 template <typename TI, typename TO>
 cudaError_t launch_act(const dlcContext *ctx, const ActParams &p, long long flat_n) {
     if (flat_n > 0) {
-        act_flat_kernel<TI, TO><<<grid_of(ctx, flat_n / (16 / (long long)sizeof(TI)) + 1), 256, 0,
-                                  ctx->stream>>>(p, flat_n);
+        const int grid = grid_of(ctx, flat_n / (16 / (long long)sizeof(TI)) + 1);
+        switch (p.mode) {
+            case 1: act_flat_kernel<TI, TO, 1><<<grid, 256, 0, ctx->stream>>>(p, flat_n); break;
+            case 2: act_flat_kernel<TI, TO, 2><<<grid, 256, 0, ctx->stream>>>(p, flat_n); break;
+            case 3: act_flat_kernel<TI, TO, 3><<<grid, 256, 0, ctx->stream>>>(p, flat_n); break;
+            case 4: act_flat_kernel<TI, TO, 4><<<grid, 256, 0, ctx->stream>>>(p, flat_n); break;
+            default: act_flat_kernel<TI, TO, 0><<<grid, 256, 0, ctx->stream>>>(p, flat_n); break;
+        }
     } else {
         const long long work = (long long)p.N * p.C * p.H * p.W;
         if (work < (1LL << 30))
