@@ -14,8 +14,9 @@
 // core matrices, or the 32-/64-byte swizzle, which the tensor core applies on
 // absolute shared-memory address bits -- therefore reads the lowered rows of
 // up to 128 consecutive output pixels straight out of the packed input row.
-// Filter taps are reordered to the same (a, phi, c) order once per call and
-// stay resident in every CTA's shared memory.
+// Filter taps are reordered to the same (a, phi, c) order once per call by a
+// small kernel (into a device buffer the handle owns) and loaded into every
+// CTA's shared memory with one bulk copy, where they stay resident.
 //
 // Tiles: the 128 MMA rows are J output rows of one image (Qs rows each, Qs a
 // power of two covering every pixel a stored output reads, J = 128/Qs) or, for
@@ -38,13 +39,19 @@
 // filters.
 //
 // Roles (one persistent CTA per SM): eight producer warps write the new rows of
-// the next tile into the ring (4-byte asynchronous copies, or element loads;
-// padding words, pixels outside the image and rows outside it are zeros); one
-// thread issues R*steps MMAs (32 bytes of reduction each) per tile into one of
-// two TMEM accumulators; four epilogue warps read the accumulator, apply
-// alpha, beta*y, bias and ReLU and store y (bulk tensor stores of 32x32 blocks
-// when y is dense FP32).  Every wait is bounded and records an error word when
-// it runs out.
+// the next tile into the ring.  Where rows are dense, thread 0 first stages
+// them in one of two buffers with bulk copies of their 16-byte-aligned
+// supersets (a row may start on any element boundary: the repack shifts it by
+// its offset), and the warps repack the staged rows into phase pixels with
+// shared-memory loads and 16-byte stores; other layouts take 4-byte
+// asynchronous copies or element loads.  Padding words, pixels outside the
+// image and rows outside it are zeros.  Warp 0 also writes the tile's MMA
+// descriptors (one per MMA) into one of two small tables.  One thread issues
+// R*steps MMAs (32 bytes of reduction each) per tile into one of four TMEM
+// accumulators (two when four would pass 512 columns); four epilogue warps
+// read the accumulator, apply alpha, beta*y, bias and ReLU and store y (bulk
+// tensor stores of 32x32 blocks when y is dense FP32).  Every wait is bounded
+// and records an error word when it runs out.
 #include <cuda_bf16.h>
 
 #include <algorithm>

@@ -1,7 +1,8 @@
 /*
- * dlc.h -- C ABI of the GB300 (sm_103a) 2-D convolution forward library.
+ * dlc.h -- C ABI of the GB300 (sm_103a) 2-D convolution library: the forward
+ * convolution, its two backward routines, pooling and activation forward.
  *
- * The library computes the forward (FPROP) convolution layer
+ * The forward (FPROP) convolution layer is
  *
  *   y[n,k,p,q] = act( alpha * sum_{c,r,s} x[n, c, p*u + r*dh - pad_top, q*v + s*dw - pad_left]
  *                                         * w[k,c,r,s]
@@ -38,12 +39,13 @@
  *    the device (a pipeline wait that ran out of time) are recorded in the
  *    handle and reported as DLC_STATUS_EXECUTION_FAILED by the next launching
  *    call on that handle and by dlcSynchronize(), which clears them.
- *  - The library allocates no device memory on the forward path.  dlcCreate
- *    allocates one small mapped host word for device error reports, the
- *    split-tile flags and a 256 KiB device buffer where forward calls of the
- *    few-channel kernel repack the filters before the convolution reads
+ *  - The library allocates no device memory on any forward or backward call.
+ *    dlcCreate allocates one small mapped host word for device error
+ *    reports, the split-tile flags and a 2 MiB device buffer where calls of
+ *    the few-channel kernels repack the filters before the convolution reads
  *    them (so two calls on one handle must not overlap on the GPU: use one
- *    handle per stream).
+ *    handle per stream).  This buffer departs from the cuDNN page's "no
+ *    auxiliary buffers"; the caller-visible workspace is zero.
  *  - A handle is not thread-safe; use one handle per host thread.
  */
 #ifndef DLC_H_
@@ -176,9 +178,11 @@ dlcStatus_t dlcGetVersion(int *version);
 
 /* Creates a handle bound to the current CUDA device and the legacy default
  * stream.  Allocates the host-side context, one mapped host word for
- * device error reports, the split-tile flags and the 256 KiB filter-repacking
+ * device error reports, the split-tile flags and the 2 MiB filter-repacking
  * buffer.  BAD_PARAM if handle is NULL, NOT_SUPPORTED if the
- * device is not compute capability 10.3, EXECUTION_FAILED on a CUDA error. */
+ * device is not compute capability 10.3, EXECUTION_FAILED on a CUDA error.
+ * Source: cuDNN page, method section (a C library whose calls take a context
+ * created once and bound to a stream). */
 dlcStatus_t dlcCreate(dlcHandle_t *handle);
 
 /* Frees the handle (does not synchronize; the caller must ensure no launched
@@ -186,7 +190,8 @@ dlcStatus_t dlcCreate(dlcHandle_t *handle);
 dlcStatus_t dlcDestroy(dlcHandle_t handle);
 
 /* Sets the stream (a cudaStream_t passed as void*; NULL = legacy default
- * stream) on which later calls launch. */
+ * stream) on which later calls launch.  Source: cuDNN page, method section
+ * (the library runs on the caller's stream). */
 dlcStatus_t dlcSetStream(dlcHandle_t handle, void *stream);
 dlcStatus_t dlcGetStream(dlcHandle_t handle, void **stream);
 
@@ -197,12 +202,14 @@ dlcStatus_t dlcGetStream(dlcHandle_t handle, void **stream);
  * run stays within the same error bound).  With deterministic = 1 every
  * kernel sums each output in a fixed order, so repeated calls give identical
  * bits, at the cost of the idle tail (a few microseconds per launch).
- * BAD_PARAM unless deterministic is 0 or 1. */
+ * BAD_PARAM unless deterministic is 0 or 1.  No counterpart on the pages
+ * (they are silent on reproducibility). */
 dlcStatus_t dlcSetDeterministic(dlcHandle_t handle, int deterministic);
 dlcStatus_t dlcGetDeterministic(dlcHandle_t handle, int *deterministic);
 
 /* Synchronizes the handle's stream.  Returns EXECUTION_FAILED if a kernel
- * recorded a device error since the last call (the error is then cleared). */
+ * recorded a device error since the last call (the error is then cleared).
+ * No counterpart on the pages: the bounded-wait failure report. */
 dlcStatus_t dlcSynchronize(dlcHandle_t handle);
 
 /* Synchronizes, then writes the last recorded device error code
@@ -219,12 +226,15 @@ dlcStatus_t dlcCreateTensorDescriptor(dlcTensorDescriptor_t *desc);
 dlcStatus_t dlcDestroyTensorDescriptor(dlcTensorDescriptor_t desc);
 
 /* Dense 4-D tensor in NCHW or NHWC order.  All sizes must be >= 1 and the
- * element count must fit in 63 bits. */
+ * element count must fit in 63 bits.  Source: cuDNN page, method section
+ * (opaque tensor descriptors; NCHW and NHWC both supported) and findings
+ * section (non-square images). */
 dlcStatus_t dlcSetTensor4dDescriptor(dlcTensorDescriptor_t desc, dlcTensorFormat_t format,
                                      dlcDataType_t dtype, int n, int c, int h, int w);
 
 /* 4-D tensor with arbitrary non-negative strides (elements) for the logical
- * axes n, c, h, w: any layout, including sub-tensor views. */
+ * axes n, c, h, w: any layout, including sub-tensor views.  Source: cuDNN
+ * page, method section (arbitrary strides along each dimension). */
 dlcStatus_t dlcSetTensor4dDescriptorEx(dlcTensorDescriptor_t desc, dlcDataType_t dtype,
                                        int n, int c, int h, int w,
                                        int64_t nStride, int64_t cStride,
@@ -240,7 +250,9 @@ dlcStatus_t dlcGetTensor4dDescriptor(dlcTensorDescriptor_t desc, dlcDataType_t *
 dlcStatus_t dlcCreateFilterDescriptor(dlcFilterDescriptor_t *desc);
 dlcStatus_t dlcDestroyFilterDescriptor(dlcFilterDescriptor_t desc);
 
-/* Dense K x C x R x S filter bank; format NCHW = KCRS, NHWC = KRSC. */
+/* Dense K x C x R x S filter bank; format NCHW = KCRS, NHWC = KRSC.
+ * Source: cuDNN page, method section (filter descriptors beside the tensor
+ * descriptors; the filter layout follows the data layout). */
 dlcStatus_t dlcSetFilter4dDescriptor(dlcFilterDescriptor_t desc, dlcDataType_t dtype,
                                      dlcTensorFormat_t format, int k, int c, int r, int s);
 
@@ -254,12 +266,16 @@ dlcStatus_t dlcDestroyConvolutionDescriptor(dlcConvolutionDescriptor_t desc);
 
 /* Symmetric padding pad_h (top and bottom) and pad_w (left and right),
  * strides u (vertical) and v (horizontal), dilations, arithmetic.  Pads >= 0,
- * strides and dilations >= 1. */
+ * strides and dilations >= 1.  Source: cuDNN page, method section (padding
+ * and strides of the convolution descriptor); maxDNN page, method section
+ * (the arithmetic counted as direct-convolution FLOPs); dilation enters as
+ * r*dh, s*dw (the pages are silent: the common convention). */
 dlcStatus_t dlcSetConvolution2dDescriptor(dlcConvolutionDescriptor_t desc, int pad_h, int pad_w,
                                           int u, int v, int dilation_h, int dilation_w,
                                           dlcMathType_t math);
 
-/* Asymmetric padding (replaces the symmetric pads). */
+/* Asymmetric padding (replaces the symmetric pads).  Source: cuDNN page,
+ * findings section (asymmetric padding). */
 dlcStatus_t dlcSetConvolution2dPadding(dlcConvolutionDescriptor_t desc, int pad_top,
                                        int pad_bottom, int pad_left, int pad_right);
 
@@ -269,21 +285,27 @@ dlcStatus_t dlcGetConvolution2dDescriptor(dlcConvolutionDescriptor_t desc, int *
                                           dlcMathType_t *math);
 
 /* Filter orientation (default CROSS_CORRELATION).  BAD_PARAM for another
- * value; NOT_INITIALIZED before dlcSetConvolution2dDescriptor. */
+ * value; NOT_INITIALIZED before dlcSetConvolution2dDescriptor.  Source: cuDNN
+ * page, method section (both convolution and cross-correlation; CONVOLUTION
+ * mirrors the filter taps in both axes). */
 dlcStatus_t dlcSetConvolutionMode(dlcConvolutionDescriptor_t desc, dlcConvolutionMode_t mode);
 dlcStatus_t dlcGetConvolutionMode(dlcConvolutionDescriptor_t desc, dlcConvolutionMode_t *mode);
 
 /* ---- forward convolution ------------------------------------------------- */
 
 /* Output dimensions N, K, P, Q.  BAD_PARAM if C differs between x and w or
- * if the dilated filter does not fit the padded input (P or Q < 1). */
+ * if the dilated filter does not fit the padded input (P or Q < 1).  Source:
+ * maxDNN page, method section (one output per receptive-field position; a
+ * partial last window is dropped: the floor above). */
 dlcStatus_t dlcGetConvolution2dForwardOutputDim(dlcConvolutionDescriptor_t conv,
                                                 dlcTensorDescriptor_t xDesc,
                                                 dlcFilterDescriptor_t wDesc,
                                                 int *n, int *k, int *p, int *q);
 
 /* Workspace needed by dlcConvolutionForward: always 0 bytes (zero memory
- * overhead).  Validates the problem like the forward call. */
+ * overhead).  Validates the problem like the forward call.  Source:
+ * zero-memory-overhead page, abstract; cuDNN page, method section (no
+ * auxiliary buffers). */
 dlcStatus_t dlcGetConvolutionForwardWorkspaceSize(dlcHandle_t handle,
                                                   dlcTensorDescriptor_t xDesc,
                                                   dlcFilterDescriptor_t wDesc,
@@ -291,7 +313,8 @@ dlcStatus_t dlcGetConvolutionForwardWorkspaceSize(dlcHandle_t handle,
                                                   dlcTensorDescriptor_t yDesc, size_t *bytes);
 
 /* Kernel a forward call with these descriptors and pointers would launch;
- * x, w and y may be NULL (alignment is then taken as satisfied). */
+ * x, w and y may be NULL (alignment is then taken as satisfied).  No
+ * counterpart on the pages (a diagnostic). */
 dlcStatus_t dlcGetConvolutionForwardKernel(dlcHandle_t handle,
                                            dlcTensorDescriptor_t xDesc, const void *x,
                                            dlcFilterDescriptor_t wDesc, const void *w,
@@ -315,9 +338,10 @@ dlcStatus_t dlcGetConvolutionForwardKernel(dlcHandle_t handle,
  * phase pixel of its column).  The row-stack kernel (DLC_KERNEL_TC_ROWSTACK)
  * likewise multiplies zero filter taps with input pixels up to 3 columns past
  * a window and with input rows of its block of output rows that a given
- * output row does not read: there an output of the same image, within that
- * block of rows and within 4 columns of such a pixel, can read NaN.  Every
- * other kernel reads exactly each window.
+ * output row does not read (for one-channel layers also up to 3 input rows
+ * past the block's span): there an output of the same image, within that
+ * block of rows and within 4 horizontal strides of such a pixel, can read
+ * NaN.  Every other kernel reads exactly each window.
  * Sources: maxDNN page, method section (each output is its receptive field
  * times the filter weights); cuDNN page, method section (C API, descriptors
  * with arbitrary strides, caller-owned buffers). */
@@ -328,7 +352,9 @@ dlcStatus_t dlcConvolutionForward(dlcHandle_t handle, const float *alpha,
                                   dlcTensorDescriptor_t yDesc, void *y);
 
 /* y = act(alpha * conv(x, w) + beta * y + bias[k]); bias is a device array of
- * K floats or NULL (no bias).  Otherwise as dlcConvolutionForward. */
+ * K floats or NULL (no bias).  Otherwise as dlcConvolutionForward.  Source:
+ * the layer's epilogue (bias and activation after the sum); cuDNN page,
+ * method section (activation functions beside the convolution). */
 dlcStatus_t dlcConvolutionBiasActivationForward(dlcHandle_t handle, const float *alpha,
                                                 dlcTensorDescriptor_t xDesc, const void *x,
                                                 dlcFilterDescriptor_t wDesc, const void *w,
@@ -361,7 +387,9 @@ dlcStatus_t dlcConvolutionBiasActivationForward(dlcHandle_t handle, const float 
  * dxDesc gives N, C, H, W; wDesc K, C, R, S.  BF16 math with KRSC filters,
  * channels-innermost dy and dx and no dilation runs on the tensor cores (one
  * SM-pair launch per stride phase, filters read transposed); every other
- * combination runs the direct kernel (DLC_KERNEL_DIRECT). */
+ * combination runs the direct kernel (DLC_KERNEL_DIRECT).  Source: cuDNN
+ * page, method section (backward routines); maxDNN page, research questions
+ * (the forward techniques carry over to the backward pass). */
 dlcStatus_t dlcConvolutionBackwardData(dlcHandle_t handle, const float *alpha,
                                        dlcFilterDescriptor_t wDesc, const void *w,
                                        dlcTensorDescriptor_t dyDesc, const void *dy,
@@ -372,7 +400,9 @@ dlcStatus_t dlcConvolutionBackwardData(dlcHandle_t handle, const float *alpha,
  * layout of dw (KCRS or KRSC) and its storage type.  A FLOAT or DOUBLE dw may
  * be written by reductions split over CTAs whose partial sums meet in atomic
  * adds (their order varies; see dlcSetDeterministic, which turns the split
- * off). */
+ * off).  Source: cuDNN page, method section (backward routines); batch-reduce
+ * GEMM page, method section (the same building block, reducing over the
+ * output pixels). */
 dlcStatus_t dlcConvolutionBackwardFilter(dlcHandle_t handle, const float *alpha,
                                          dlcTensorDescriptor_t xDesc, const void *x,
                                          dlcTensorDescriptor_t dyDesc, const void *dy,
@@ -393,7 +423,8 @@ dlcStatus_t dlcGetConvolutionBackwardFilterWorkspaceSize(dlcHandle_t handle,
                                                          size_t *bytes);
 
 /* Kernel the backward calls with these descriptors would launch (diagnostic;
- * pointers may be NULL, alignment is then taken as satisfied). */
+ * pointers may be NULL, alignment is then taken as satisfied).  No
+ * counterpart on the pages. */
 dlcStatus_t dlcGetConvolutionBackwardDataKernel(dlcHandle_t handle, dlcFilterDescriptor_t wDesc,
                                                 const void *w, dlcTensorDescriptor_t dyDesc,
                                                 const void *dy, dlcConvolutionDescriptor_t conv,
@@ -421,7 +452,9 @@ dlcStatus_t dlcCreatePoolingDescriptor(dlcPoolingDescriptor_t *desc);
 dlcStatus_t dlcDestroyPoolingDescriptor(dlcPoolingDescriptor_t desc);
 
 /* Window R x S, pads (each smaller than the window along its axis, so that
- * no window is empty), strides u, v >= 1.  BAD_PARAM otherwise. */
+ * no window is empty), strides u, v >= 1.  BAD_PARAM otherwise.  Source:
+ * cuDNN page, method section (pooling); the pad rule is this library's
+ * reading (the page is silent). */
 dlcStatus_t dlcSetPooling2dDescriptor(dlcPoolingDescriptor_t desc, dlcPoolingMode_t mode,
                                       int window_h, int window_w, int pad_top, int pad_bottom,
                                       int pad_left, int pad_right, int u, int v);
@@ -436,7 +469,10 @@ dlcStatus_t dlcGetPooling2dForwardOutputDim(dlcPoolingDescriptor_t desc,
                                             dlcTensorDescriptor_t xDesc, int *n, int *c, int *p,
                                             int *q);
 
-/* y[n,c,p,q] = alpha * POOL(window of x[n,c]) + beta * y[n,c,p,q]. */
+/* y[n,c,p,q] = alpha * POOL(window of x[n,c]) + beta * y[n,c,p,q].
+ * POOL: the maximum, or the window sum over R*S (padding counted) or over the
+ * in-image elements (padding excluded).  Source: cuDNN page, summary and
+ * method section (pooling beside convolution). */
 dlcStatus_t dlcPoolingForward(dlcHandle_t handle, dlcPoolingDescriptor_t desc, const float *alpha,
                               dlcTensorDescriptor_t xDesc, const void *x, const float *beta,
                               dlcTensorDescriptor_t yDesc, void *y);
@@ -448,7 +484,10 @@ dlcStatus_t dlcGetPoolingForwardKernel(dlcHandle_t handle, dlcPoolingDescriptor_
                                        dlcKernel_t *kernel);
 
 /* y = alpha * f(x) + beta * y elementwise; x and y of the same dimensions.
- * coef is the ceiling of CLIPPED_RELU (ignored otherwise). */
+ * coef is the ceiling of CLIPPED_RELU (ignored otherwise).  Source: cuDNN
+ * page, summary and method section (activation functions; the page names no
+ * list: identity, ReLU, sigmoid, tanh and clipped ReLU are this library's
+ * reading). */
 dlcStatus_t dlcActivationForward(dlcHandle_t handle, dlcActivationMode_t mode, double coef,
                                  const float *alpha, dlcTensorDescriptor_t xDesc, const void *x,
                                  const float *beta, dlcTensorDescriptor_t yDesc, void *y);
@@ -458,7 +497,7 @@ dlcStatus_t dlcActivationForward(dlcHandle_t handle, dlcActivationMode_t mode, d
 /* Launches one block whose pipeline wait is on a barrier nothing completes,
  * with a limit of timeout_us microseconds (1..1000000).  The kernel records
  * DLC_DEVERR_WAIT_TIMEOUT and returns; no GPU fault is involved.  Used by the
- * tests of the error path. */
+ * tests of the error path.  No counterpart on the pages. */
 dlcStatus_t dlcDebugWaitTimeoutSelfTest(dlcHandle_t handle, int timeout_us);
 
 /* ---- forward convolution that allocates nothing ---------------------------
