@@ -58,6 +58,7 @@ struct WgParams {
     int m_tiles, c_tiles, tiles;   // tiles = m_tiles * c_tiles * R * S
     int kblocks;                   // ceil(M / 64)
     int splits, units;             // pixel-block ranges per tile; units = tiles * splits
+    int dn, dp, dq;                // one pixel block (64 pixels) as images, rows, columns
     float alpha;
     uint32_t idesc, tmem_cols, acc_stride;
     int *err;
@@ -92,21 +93,32 @@ __device__ void wg_produce(const WgParams &p, const CUtensorMap *tmA, const CUte
         const WgUnit w = wg_unit(p, u);
         const int r = w.rs / p.S, s = w.rs - (w.rs / p.S) * p.S;
         const int k0 = w.kt * WG_BM, c0 = w.ct * p.BN;
-        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+        // the first pixel of the unit's first block; later blocks step by 64
+        // pixels without a division
+        long long m0 = (long long)w.kb0 * WG_BP;
+        int n0 = (int)(m0 / p.PQ);
+        int p0, q0;
+        {
+            const int rem = (int)(m0 - (long long)n0 * p.PQ);
+            p0 = rem / p.Q;
+            q0 = rem - p0 * p.Q;
+        }
+        for (int kb = w.kb0; kb < w.kb1; ++kb, m0 += WG_BP) {
             if (!mbar_wait(&empty[stage], ph ^ 1u, ctl, 11)) return;
             mbar_arrive_expect_tx(&full[stage], tx);
-            const long long m0 = (long long)kb * WG_BP;
             const uint32_t a = sA + (uint32_t)stage * WG_A_BYTES;
             tma_load_2d(a, tmA, &full[stage], k0, (int)m0);
             tma_load_2d(a + WG_ATOM, tmA, &full[stage], k0 + 64, (int)m0);
-            const int n0 = (int)(m0 / p.PQ);
-            const int rem = (int)(m0 - (long long)n0 * p.PQ);
-            const int p0 = rem / p.Q, q0 = rem - (rem / p.Q) * p.Q;
             const uint32_t b = sB + (uint32_t)stage * b_bytes;
             for (int at = 0; at < p.b_atoms; ++at)
                 tma_load_im2col_4d(b + (uint32_t)at * WG_ATOM, tmB, &full[stage], c0 + at * 64,
                                    q0 * p.v - p.pl, p0 * p.u - p.pt, n0, (uint16_t)(s * p.dw),
                                    (uint16_t)(r * p.dh));
+            q0 += p.dq;
+            p0 += p.dp;
+            n0 += p.dn;
+            if (q0 >= p.Q) q0 -= p.Q, ++p0;
+            if (p0 >= p.P) p0 -= p.P, ++n0;
             if (++stage == ST) stage = 0, ph ^= 1u;
         }
     }
@@ -362,6 +374,9 @@ dlcStatus_t dlc_launch_wgrad_tc(dlcContext *ctx, const BwdProblem &bp) {
         splits = std::max(1, std::min((want + p.tiles - 1) / p.tiles, p.kblocks / 32));
     }
     p.splits = splits;
+    p.dn = (int)(WG_BP / p.PQ);
+    p.dp = (int)((WG_BP % p.PQ) / p.Q);
+    p.dq = (int)((WG_BP % p.PQ) % p.Q);
     if ((long long)p.tiles * splits > 0x7fffffffLL) return DLC_STATUS_NOT_SUPPORTED;
     p.units = p.tiles * splits;
     p.alpha = (float)bp.alpha;
