@@ -438,19 +438,21 @@ __device__ void repack_rows(const WinParams &p, uint32_t ring, uint32_t sbuf, co
                 for (int w = 0; w < 4; ++w) v[k][w] = 0u;
                 if (st + k >= st1) continue;
                 if constexpr (SHIFT) {
-                    if (nw == 4 && b >= 0 && (uint32_t)b + 16u <= rowb) {
-                        // the whole chunk inside the row: 4 aligned words, or 5
-                        // and a 16-bit shift when the row starts 2 bytes past a word
+                    if (nw > 0 && b >= 0 && (uint32_t)b + 4u * (uint32_t)nw <= rowb) {
+                        // the chunk's nw data words inside the row: aligned words,
+                        // or one more and a 16-bit shift when the row starts 2
+                        // bytes past a word (nw is the same for every step of
+                        // this lane)
                         const uint32_t a = rb + (uint32_t)b;
                         if ((a & 3u) == 0) {
 #pragma unroll
-                            for (int w = 0; w < 4; ++w) v[k][w] = lds32(a + 4u * w);
+                            for (int w = 0; w < 4; ++w) v[k][w] = w < nw ? lds32(a + 4u * w) : 0u;
                         } else {
                             uint32_t t[5];
 #pragma unroll
-                            for (int w = 0; w < 5; ++w) t[w] = lds32(a - 2u + 4u * w);
+                            for (int w = 0; w < 5; ++w) t[w] = w <= nw ? lds32(a - 2u + 4u * w) : 0u;
 #pragma unroll
-                            for (int w = 0; w < 4; ++w) v[k][w] = __funnelshift_r(t[w], t[w + 1], 16);
+                            for (int w = 0; w < 4; ++w) v[k][w] = w < nw ? __funnelshift_r(t[w], t[w + 1], 16) : 0u;
                         }
                     } else {
 #pragma unroll
