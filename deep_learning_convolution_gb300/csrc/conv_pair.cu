@@ -362,7 +362,7 @@ __device__ void pair_epilogue(const PairParams &p, uint32_t rank, uint32_t tmem_
         if (lane == 0) mbar_arrive_cluster(tempty0 + 8u * buf);  // release on the leader
     }
     // staged stores must finish reading shared memory before the CTA exits
-    if (p.y_tma && lane == 0) bulk_wait_group_all();
+    if (p.y_tma && lane == 0) bulk_wait_group_read<0>();
     __syncwarp();
 }
 

@@ -1020,8 +1020,9 @@ __device__ void epilogue(const TcParams &p, uint32_t tmem_base, uint64_t *tfull,
         if (lane == 0) mbar_arrive(&tempty[buf]);
         ++t;
     }
-    // staged stores must finish reading shared memory (and land) before exit
-    if (p.y_tma && lane == 0) bulk_wait_group_all();
+    // staged stores must finish reading shared memory before the CTA exits (the
+    // grid's completion makes their writes visible)
+    if (p.y_tma && lane == 0) bulk_wait_group_read<0>();
     __syncwarp();
 }
 

@@ -238,7 +238,7 @@ __device__ void wg_epilogue(const WgParams &p, uint32_t tmem_base, uint64_t *tfu
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);
     }
-    if (lane == 0) bulk_wait_group_all();
+    if (lane == 0) bulk_wait_group_read<0>();  // shared memory read before exit
     __syncwarp();
 }
 

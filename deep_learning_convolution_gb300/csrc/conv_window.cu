@@ -886,7 +886,7 @@ __device__ void win_epilogue(const WinParams &p, uint32_t rank, uint32_t tmem_ba
         }
     }
     // staged stores must finish reading shared memory before the CTA exits
-    if (p.y_tma && lane == 0) bulk_wait_group_all();
+    if (p.y_tma && lane == 0) bulk_wait_group_read<0>();
     __syncwarp();
 }
 

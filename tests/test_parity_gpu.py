@@ -99,7 +99,7 @@ PAIR_CASES = IM2COL_CASES + [
     # ragged: the last pair tile's second CTA has no rows at all
     L("pair_bf16_c64_k64_3x3_ragged", 1, 64, 11, 11, 64, 3, 3, **P(1, 1, 1, 1)),
     # a last channel block with one MMA's worth of channels (BF16 72 = 64 + 8,
-    # TF32 40 = 32 + 8): the MMAs over its zero fill are skipped
+    # TF32 40 = 32 + 8): the rest of the block is zero fill
     L("pair_bf16_c72_k64_3x3", 2, 72, 13, 13, 64, 3, 3, **P(1, 1, 1, 1)),
     L("pair_tf32_c40_k32_3x3", 2, 40, 12, 12, 32, 3, 3, **P(1, 1, 1, 1), dtype="tf32"),
 ]
