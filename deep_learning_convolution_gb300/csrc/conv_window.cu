@@ -672,37 +672,58 @@ __device__ void win_mma(const WinParams &p, uint32_t tmem_base, uint32_t sB, con
     if (PAIR) ok = ok && warp_wait<true>(bpeer, 0u, ctl, 13);
     int ub, ue;
     unit_range<PAIR>(p, ub, ue);
-    int it = 0;
-    for (int u = ub; ok && u < ue; ++u, ++it) {
-        const int buf = it & 1;
-        const uint32_t ph = (uint32_t)(it >> 1) & 1u;
-        const int abuf = it & ((1 << p.nacc_log2) - 1);  // accumulator
-        const uint32_t aph = (uint32_t)(it >> p.nacc_log2) & 1u;
-        // (pairs: the other CTA's epilogue and producers arrive remotely)
-        if (!warp_wait<PAIR>(&tempty[abuf], aph ^ 1u, ctl, 3)) break;
-        if (!warp_wait<PAIR>(&full[buf], ph, ctl, 4)) break;
-        tc_fence_after_sync();
-        if (lane == 0) {
+    // MMAs m0 .. m1-1 of a unit: 32 bytes of window each
+    auto issue = [&](uint32_t d, const uint32_t *tab, uint64_t &bd, int m0, int m1) {
+#pragma unroll 4
+        for (int m = m0; m < m1; ++m) {
+            const uint64_t ad = a_hi | tab[m];
+            const uint32_t acc = m > 0 ? 1u : 0u;
+            if constexpr (PAIR) {
+                if constexpr (TF32)
+                    umma_tf32_pair(d, ad, bd, idesc, acc);
+                else
+                    umma_bf16_pair(d, ad, bd, idesc, acc);
+            } else {
+                if constexpr (TF32)
+                    umma_tf32_nc(d, ad, bd, idesc, acc);
+                else
+                    umma_bf16_nc(d, ad, bd, idesc, acc);
+            }
+            bd += slab16;
+        }
+    };
+    // (pairs: the other CTA's epilogue and producers arrive remotely)
+    auto wait = [&](uint64_t *bar, uint32_t parity, int where) {
+        return PAIR ? mbar_wait_cluster(bar, parity, ctl, where) : mbar_wait(bar, parity, ctl, where);
+    };
+    auto done = [&](uint64_t *bar, uint32_t parity) {
+        return PAIR ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity);
+    };
+    // One lane runs the loop.  While a unit's last MMAs are still queued on
+    // the tensor pipe it looks, without waiting, whether the next unit's
+    // accumulator and ring rows are ready: if so the next unit's MMAs follow
+    // the commits with no wait in between.
+    if (lane == 0 && ok) {
+        const int head = nm > 4 ? nm - 4 : 0;  // MMAs issued before the look-ahead
+        const int amask = (1 << p.nacc_log2) - 1;
+        bool ready = false;
+        int it = 0;
+        for (int u = ub; u < ue; ++u, ++it) {
+            const int buf = it & 1;
+            const int abuf = it & amask;  // accumulator
+            if (!ready) {
+                if (!wait(&tempty[abuf], ((uint32_t)(it >> p.nacc_log2) & 1u) ^ 1u, 3)) break;
+                if (!wait(&full[buf], (uint32_t)(it >> 1) & 1u, 4)) break;
+            }
+            tc_fence_after_sync();
             const uint32_t d = tmem_base + (uint32_t)abuf * p.acc_stride;
             const uint32_t *tab = atab + buf * nm;  // written by the producers
             uint64_t bd = b0;
-#pragma unroll 4
-            for (int m = 0; m < nm; ++m) {  // 32 bytes of window per MMA
-                const uint64_t ad = a_hi | tab[m];
-                const uint32_t acc = m > 0 ? 1u : 0u;
-                if constexpr (PAIR) {
-                    if constexpr (TF32)
-                        umma_tf32_pair(d, ad, bd, idesc, acc);
-                    else
-                        umma_bf16_pair(d, ad, bd, idesc, acc);
-                } else {
-                    if constexpr (TF32)
-                        umma_tf32_nc(d, ad, bd, idesc, acc);
-                    else
-                        umma_bf16_nc(d, ad, bd, idesc, acc);
-                }
-                bd += slab16;
-            }
+            issue(d, tab, bd, 0, head);
+            const int in = it + 1;
+            ready = u + 1 < ue && done(&tempty[in & amask], ((uint32_t)(in >> p.nacc_log2) & 1u) ^ 1u) &&
+                    done(&full[in & 1], (uint32_t)(in >> 1) & 1u);
+            issue(d, tab, bd, head, nm);
             if (PAIR) {
                 umma_commit_pair(&empty[buf], 3);  // both CTAs' rings may take new rows
                 umma_commit_pair(&tfull[abuf], 3);  // both CTAs' accumulator rows ready
@@ -711,8 +732,8 @@ __device__ void win_mma(const WinParams &p, uint32_t tmem_base, uint32_t sB, con
                 umma_commit(&tfull[abuf]);
             }
         }
-        __syncwarp();
     }
+    __syncwarp();
     // Every MMA issued must complete before tensor memory is released.
     if (lane == 0) {
         if (PAIR)
