@@ -13,7 +13,10 @@ back (a fixed count per workload, so that the timed region of the default
 steps lasts about a second and clock samplers see the GPU busy); L2 is
 flushed (256 MiB write) between steps, outside the timed events, and one pass
 over a stack touches more than the 129 MB L2 (except the tiny layer, which is
-latency-bound and makes no roofline claim beyond that).
+latency-bound and makes no roofline claim beyond that).  A step is timed by
+CUDA events at its start and end; per-layer times (and the dominant kernel's
+roofline fraction) come from events after every launch of one pass in eight,
+so that the other passes run without events between their launches.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload overfeat|alexnet|resnet50|speech|tiny] [--no-configs]
@@ -131,6 +134,54 @@ def reps_for(workload, override=None):
     return int(override) if override else REPS_PER_STEP[workload]
 
 
+# Passes of a step that carry per-launch events: one in INST_EVERY.  An event
+# recorded between two launches keeps the second kernel from starting while
+# the first drains (programmatic dependent launch); with one after every
+# launch the stacks ran 1-6 % slower.  The other passes run as a user's would.
+INST_EVERY = 8
+TIMING = (f"step: start and end CUDA events; layers: per-launch CUDA events in one pass "
+          f"of every {INST_EVERY}")
+
+
+def instrumented_passes(reps):
+    return [r for r in range(reps) if r % INST_EVERY == INST_EVERY // 2] or [reps // 2]
+
+
+def time_steps(K, reps, launchers, flush, stream):
+    """Runs K steps of `reps` passes over `launchers` (one call per layer),
+    L2 flushed before each step outside its timed events.  Returns the summed
+    step time in ms (each step's start and end events), the per-launcher time
+    summed over the instrumented passes, and how many passes that was."""
+    import torch
+    inst = instrumented_passes(reps)
+    slot = {r: i for i, r in enumerate(inst)}
+    nl = len(launchers)
+    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+    ev_pass = [[[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1)] for _ in inst]
+               for _ in range(K)]
+    for i in range(K):
+        flush.fill_(float(i))
+        ev_step[i][0].record(stream)
+        for r in range(reps):
+            ev = ev_pass[i][slot[r]] if r in slot else None
+            if ev is not None:
+                ev[0].record(stream)
+            for j, launch in enumerate(launchers):
+                launch()
+                if ev is not None:
+                    ev[j + 1].record(stream)
+        ev_step[i][1].record(stream)
+    torch.cuda.synchronize()
+    total_ms = sum(a.elapsed_time(b) for a, b in ev_step)
+    per = [0.0] * nl
+    for i in range(K):
+        for ev in ev_pass[i]:
+            for j in range(nl):
+                per[j] += ev[j].elapsed_time(ev[j + 1])
+    return total_ms, per, K * len(inst)
+
+
 def workload_config(workload, world, reps=None):
     """The `config` both arms print: the workload and how a step is timed."""
     from deep_learning_convolution_gb300 import synth
@@ -149,7 +200,7 @@ def workload_config(workload, world, reps=None):
             "output": "fp32", "l2": l2,
             "parallelism": f"replicas{world}" if world > 1 else "single_gpu",
             "reps_per_step": reps, "flops_per_pass": pass_flops,
-            "flops_per_step": pass_flops * reps}
+            "flops_per_step": pass_flops * reps, "timing": TIMING}
 
 
 # ---------------------------------------------------------------------------
@@ -276,9 +327,9 @@ def run_workload(args, workload, handle, stream, dev, rank, world, local_rank, h
     handle.synchronize()
 
     K = args.steps
-    nl = len(probs)
-    # events around every layer launch of every pass, on the launch stream
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(reps * nl + 1)] for _ in range(K)]
+    # step time from each step's start and end events on the launch stream;
+    # per-layer times from per-launch events in one pass of every INST_EVERY
+    launchers = [(lambda pr=pr: pr["conv"](pr["x"], pr["w"], pr["y"])) for pr in probs]
     sampler = ClockSampler(local_rank)
     if world > 1:
         torch.distributed.barrier()
@@ -286,28 +337,13 @@ def run_workload(args, workload, handle, stream, dev, rank, world, local_rank, h
     launches0 = handle.launches()
     sampler.start()
     time.sleep(0.05)
-    for i in range(K):
-        flush.fill_(float(i))
-        ev[i][0].record(stream)
-        e = 1
-        for _ in range(reps):
-            for pr in probs:
-                pr["conv"](pr["x"], pr["w"], pr["y"])
-                ev[i][e].record(stream)
-                e += 1
-    torch.cuda.synchronize()
+    total_ms, per_layer_ms, n_launch = time_steps(K, reps, launchers, flush, stream)
     clocks = sampler.stop()
     if world > 1:
         torch.distributed.barrier()
     launches = handle.launches() - launches0
     handle.synchronize()  # raises if a kernel recorded a device error
 
-    per_layer_ms = [0.0] * nl
-    total_ms = 0.0
-    for i in range(K):
-        total_ms += ev[i][0].elapsed_time(ev[i][-1])
-        for e in range(reps * nl):
-            per_layer_ms[e % nl] += ev[i][e].elapsed_time(ev[i][e + 1])
     total_ms, value = aggregate_over_ranks(total_ms, step_flops, K, world, dev)
     ms_per_step = total_ms / K
 
@@ -315,7 +351,6 @@ def run_workload(args, workload, handle, stream, dev, rank, world, local_rank, h
     peak_tf, peak_src = _peak_for(workload, peaks)
     layer_rows = []
     by_kernel = {}
-    n_launch = K * reps
     for j, pr in enumerate(probs):
         t_s = per_layer_ms[j] / n_launch * 1e-3
         tflops = pr["flops"] / t_s / 1e12
@@ -387,7 +422,8 @@ def run_workload(args, workload, handle, stream, dev, rank, world, local_rank, h
 
 
 # Backward routines and the pooling/activation primitives, timed like the
-# forward workloads (steps of reps_per_step passes, per-launch CUDA events).
+# forward workloads (steps of reps_per_step passes; per-launch CUDA events in
+# one pass of every INST_EVERY).
 EXTRA_REPS = {"overfeat_bwd_data": 40, "overfeat_bwd_filter": 24, "alexnet_pool_act": 300}
 
 
@@ -461,31 +497,15 @@ def run_extra(args, name, handle, stream, dev, local_rank, world):
     K = args.steps
     nl = len(ops)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(reps * nl + 1)] for _ in range(K)]
     sampler = ClockSampler(local_rank)
     torch.cuda.synchronize()
     launches0 = handle.launches()
     sampler.start()
     time.sleep(0.05)
-    for i in range(K):
-        flush.fill_(float(i))
-        ev[i][0].record(stream)
-        e = 1
-        for _ in range(reps):
-            for o in ops:
-                o[1]()
-                ev[i][e].record(stream)
-                e += 1
-    torch.cuda.synchronize()
+    total_ms, per_ms, n_launch = time_steps(K, reps, [o[1] for o in ops], flush, stream)
     clocks = sampler.stop()
     launches = handle.launches() - launches0
     handle.synchronize()
-    per_ms = [0.0] * nl
-    total_ms = 0.0
-    for i in range(K):
-        total_ms += ev[i][0].elapsed_time(ev[i][-1])
-        for e in range(reps * nl):
-            per_ms[e % nl] += ev[i][e].elapsed_time(ev[i][e + 1])
     pass_flops = sum(o[2] for o in ops)
     pass_bytes = sum(o[3] for o in ops)
     hbm_bound = pass_flops == 0
@@ -494,7 +514,6 @@ def run_extra(args, name, handle, stream, dev, local_rank, world):
                                            else pass_bytes * reps * 1e3, K, world, dev)
     peaks = load_peaks()
     rows = []
-    n_launch = K * reps
     for j, o in enumerate(ops):
         t_s = per_ms[j] / n_launch * 1e-3
         gbs = o[3] / t_s / 1e9
@@ -530,7 +549,7 @@ def run_extra(args, name, handle, stream, dev, local_rank, world):
     res = {"what": metric, "value": round(value, 2), "unit": unit, "steps": K,
            "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4), "dtype": "bf16",
            "config": {"workload": name, "layers": [o[0] for o in ops], "reps_per_step": reps,
-                      "l2": "flushed between steps (256 MiB write, untimed)"},
+                      "l2": "flushed between steps (256 MiB write, untimed)", "timing": TIMING},
            "roofline": roofline, "layers": rows, "gpu_launches": launches, "clocks": clocks,
            "e2e": None}
     for o in ops:
