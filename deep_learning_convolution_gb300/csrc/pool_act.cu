@@ -17,7 +17,8 @@
 // kernels are sized for bandwidth.  With channels innermost (NHWC) each thread
 // owns 16 bytes of channels of one output pixel and reads the window's pixels
 // as 16-byte vectors (consecutive threads read consecutive bytes; a 3 x 3
-// window's nine loads are issued together); dense tensors of one layout run
+// window's nine loads are issued together; a maximum of BF16 compares the
+// stored pairs without widening them); dense tensors of one layout run
 // the activation as a flat array of 16-byte vectors, four per thread in
 // flight, one kernel per function; anything else takes one element per
 // thread through the strides.
@@ -124,6 +125,78 @@ __device__ __forceinline__ void store_vec(TO *dst, const A (&v)[V]) {
     }
 }
 
+// Maximum or sum over a window of 16-byte vectors of channels.  fetch(i, j, q)
+// loads tap (i, j) into q and says whether it lies in the image; FIX > 0 (a
+// FIX x FIX window) issues every load before the first is used.  The maximum
+// of BF16 storage compares the stored pairs in place (max.bf16x2, which like
+// fmaxf passes over a NaN operand) and widens only the result: it is one of
+// the stored values either way.  Sums are taken in A.  Returns the number of
+// in-image taps.
+template <typename TI, typename A, int V, bool MAX, int FIX, typename F>
+__device__ __forceinline__ int pool_window(const F &fetch, int R, int S, A (&acc)[V]) {
+    int count = 0;
+    if constexpr (MAX && sizeof(TI) == 2) {
+        __nv_bfloat162 m[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m[k] = __bfloat162bfloat162(__ushort_as_bfloat16((unsigned short)0xff80u));
+        auto take = [&](const uint4 &q) {
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) m[k] = __hmax2(m[k], *reinterpret_cast<const __nv_bfloat162 *>(&w[k]));
+        };
+        if constexpr (FIX > 0) {
+            uint4 q[FIX * FIX];
+            bool in[FIX * FIX];
+#pragma unroll
+            for (int t = 0; t < FIX * FIX; ++t) in[t] = fetch(t / FIX, t % FIX, q[t]);
+#pragma unroll
+            for (int t = 0; t < FIX * FIX; ++t)
+                if (in[t]) take(q[t]), ++count;
+        } else {
+            for (int i = 0; i < R; ++i)
+                for (int j = 0; j < S; ++j) {
+                    uint4 q;
+                    if (fetch(i, j, q)) take(q), ++count;
+                }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            acc[2 * k] = __bfloat162float(m[k].x);
+            acc[2 * k + 1] = __bfloat162float(m[k].y);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc[e] = MAX ? (A)-INFINITY : (A)0;
+        auto take = [&](const uint4 &q) {
+            A v[V];
+            unpack16<TI, A, V>(q, v);
+#pragma unroll
+            for (int e = 0; e < V; ++e) {
+                if constexpr (MAX)
+                    acc[e] = sizeof(A) == 8 ? (A)fmax((double)acc[e], (double)v[e]) : (A)fmaxf((float)acc[e], (float)v[e]);
+                else
+                    acc[e] += v[e];
+            }
+        };
+        if constexpr (FIX > 0) {
+            uint4 q[FIX * FIX];
+            bool in[FIX * FIX];
+#pragma unroll
+            for (int t = 0; t < FIX * FIX; ++t) in[t] = fetch(t / FIX, t % FIX, q[t]);
+#pragma unroll
+            for (int t = 0; t < FIX * FIX; ++t)
+                if (in[t]) take(q[t]), ++count;
+        } else {
+            for (int i = 0; i < R; ++i)
+                for (int j = 0; j < S; ++j) {
+                    uint4 q;
+                    if (fetch(i, j, q)) take(q), ++count;
+                }
+        }
+    }
+    return count;
+}
+
 // Channels-innermost pooling: one thread per (output pixel, 16-byte chunk of
 // channels); C * sizeof(TI) is a multiple of 16 and both bases 16-byte aligned.
 // I: the index type of the output enumeration (32-bit when the count fits,
@@ -146,50 +219,17 @@ __global__ void __launch_bounds__(256) pool_nhwc_kernel(const __grid_constant__ 
         const int n = (int)(t / p.P);
         A acc[V];
         const bool is_max = p.mode == 0;
-#pragma unroll
-        for (int i = 0; i < V; ++i) acc[i] = is_max ? (A)-INFINITY : (A)0;
-        int count = 0;
         const TI *xn = x + (long long)n * p.xs[0] + (long long)ch * V;
         const int h0 = op * p.u - p.pt, w0 = oq * p.v - p.pl;
-        if constexpr (FIX > 0) {
-            uint4 q4[FIX * FIX];
-            bool in[FIX * FIX];
-#pragma unroll
-            for (int i = 0; i < FIX; ++i)
-#pragma unroll
-                for (int j = 0; j < FIX; ++j) {
-                    const int h = h0 + i, wi = w0 + j;
-                    in[i * FIX + j] = h >= 0 && h < p.H && wi >= 0 && wi < p.W;
-                    q4[i * FIX + j] = in[i * FIX + j] ? __ldg(reinterpret_cast<const uint4 *>(
-                                                           xn + (long long)h * p.xs[2] + (long long)wi * p.xs[3]))
-                                                     : make_uint4(0, 0, 0, 0);
-                }
-#pragma unroll
-            for (int t = 0; t < FIX * FIX; ++t) {
-                if (!in[t]) continue;
-                A v[V];
-                unpack16<TI, A, V>(q4[t], v);
-#pragma unroll
-                for (int e = 0; e < V; ++e) acc[e] = is_max ? (v[e] > acc[e] ? v[e] : acc[e]) : acc[e] + v[e];
-                ++count;
-            }
-        } else {
-            for (int i = 0; i < p.R; ++i) {
-                const int h = h0 + i;
-                if (h < 0 || h >= p.H) continue;
-                for (int j = 0; j < p.S; ++j) {
-                    const int wi = w0 + j;
-                    if (wi < 0 || wi >= p.W) continue;
-                    const uint4 q4 = __ldg(reinterpret_cast<const uint4 *>(
-                        xn + (long long)h * p.xs[2] + (long long)wi * p.xs[3]));
-                    A v[V];
-                    unpack16<TI, A, V>(q4, v);
-#pragma unroll
-                    for (int e = 0; e < V; ++e) acc[e] = is_max ? (v[e] > acc[e] ? v[e] : acc[e]) : acc[e] + v[e];
-                    ++count;
-                }
-            }
-        }
+        auto fetch = [&](int i, int j, uint4 &q) {
+            const int h = h0 + i, wi = w0 + j;
+            const bool in = h >= 0 && h < p.H && wi >= 0 && wi < p.W;
+            q = in ? __ldg(reinterpret_cast<const uint4 *>(xn + (long long)h * p.xs[2] + (long long)wi * p.xs[3]))
+                   : make_uint4(0, 0, 0, 0);
+            return in;
+        };
+        const int count = is_max ? pool_window<TI, A, V, true, FIX>(fetch, p.R, p.S, acc)
+                                 : pool_window<TI, A, V, false, FIX>(fetch, p.R, p.S, acc);
         const A div = p.mode == 1 ? (A)(p.R * p.S) : (A)count;
         const long long yo = (long long)n * p.ys[0] + (long long)op * p.ys[2] + (long long)oq * p.ys[3] +
                              (long long)ch * V;

@@ -2,8 +2,9 @@
 through the C ABI.
 
 Pooling: every mode (max, average counting the padding and not), NHWC
-inputs on the vectorised channel kernel (BF16, FP32) and NCHW / strided
-inputs on the per-element kernel, FP64 storage, alpha/beta, ragged extents,
+inputs on the vectorised channel kernel (BF16, FP32; a BF16 maximum
+compared in stored pairs) and NCHW /
+strided inputs on the per-element kernel, FP64 storage, alpha/beta, ragged extents,
 asymmetric pads, an AlexNet-sized max pooling (3 x 3, stride 2 over
 128 x 55 x 55 x 64 BF16) checked in full.  The maximum is exact (it selects a
 stored value); an average of m terms carries FP32 rounding, bounded by
@@ -68,6 +69,14 @@ POOL_CASES = [
     ("avginc_nhwc_c3", 2, 3, 10, 10, (2, 2), (1, 1, 1, 1), (2, 2), "bf16", "NHWC", "f32", "direct"),
     ("max_nchw_f64", 2, 4, 9, 9, (3, 2), (1, 1, 1, 0), (2, 2), "f64", "NCHW", "f64", "direct"),
     ("avgexc_nhwc_f64", 1, 6, 8, 9, (3, 3), (1, 1, 1, 1), (1, 1), "f64", "NHWC", "f64", "pool_nhwc"),
+    # wide rows, pads above the first output row and below the last
+    ("max_nhwc_bf16_wide", 2, 64, 40, 100, (3, 3), (1, 1, 1, 1), (1, 1), "bf16", "NHWC", "bf16",
+     "pool_nhwc"),
+    ("avginc_nhwc_bf16_wide", 2, 64, 23, 100, (3, 3), (2, 2, 1, 0), (2, 2), "bf16", "NHWC", "f32",
+     "pool_nhwc"),
+    # 512 FP32 channels: 128 chunks a pixel
+    ("max_nhwc_f32_wide", 1, 512, 6, 40, (3, 3), (1, 1, 1, 1), (1, 1), "f32", "NHWC", "f32",
+     "pool_nhwc"),
 ]
 MODES = {"max": "max", "avginc": "avg_include_pad", "avgexc": "avg_exclude_pad"}
 
