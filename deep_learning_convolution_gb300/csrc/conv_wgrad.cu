@@ -28,6 +28,16 @@
 // operands MN-major) into one of two TMEM accumulators; warps 2-5 read the
 // accumulator, scale it by alpha, stage 32 x 32 blocks in shared memory and
 // reduce-add them into dw.  Every wait is bounded.
+//
+// With more than 128 filters the CTAs work in pairs (a cluster of two, as the
+// forward pair kernel): one MMA of M = 256 filters (128 per CTA, each from its
+// own dy block) and N = BN channels, of which each CTA loads half of the x
+// block.  Per SM a k-block then moves 16 KiB of dy and BN/2 x 128 bytes of x
+// instead of BN x 128: a single CTA at BN = 256 moves 48 KiB per 680 cycles of
+// MMAs, more than the SM takes in.  Both CTAs' loads complete on the leader's
+// barrier; the leader issues the MMAs and commits to both CTAs' barriers; each
+// CTA's epilogue adds its 128 filter rows and releases the accumulator on the
+// leader's barrier.
 #include <algorithm>
 #include <cstdlib>
 #include <cstring>
@@ -81,18 +91,28 @@ __device__ __forceinline__ WgUnit wg_unit(const WgParams &p, int u) {
     return w;
 }
 
-__device__ void wg_produce(const WgParams &p, const CUtensorMap *tmA, const CUtensorMap *tmB,
+// The first work unit of this CTA (or pair) and the step to its next.
+template <bool PAIR>
+__device__ __forceinline__ int wg_first() { return PAIR ? (int)cluster_id_x() : (int)blockIdx.x; }
+template <bool PAIR>
+__device__ __forceinline__ int wg_step() { return PAIR ? (int)num_clusters_x() : (int)gridDim.x; }
+
+template <bool PAIR>
+__device__ void wg_produce(const WgParams &p, uint32_t rank, const CUtensorMap *tmA, const CUtensorMap *tmB,
                            uint32_t sA, uint32_t sB, uint64_t *full, uint64_t *empty,
                            const WaitCtl &ctl) {
     const int ST = p.stages;
     const uint32_t b_bytes = (uint32_t)p.b_atoms * WG_ATOM;
-    const uint32_t tx = WG_A_BYTES + b_bytes;
+    // a pair's stage completes on the leader's barrier with both CTAs' bytes
+    const uint32_t tx = (PAIR ? 2u : 1u) * (WG_A_BYTES + b_bytes);
+    const uint32_t full0 = PAIR ? mapa_shared(smem_u32(full), 0) : 0u;
     int stage = 0;
     uint32_t ph = 0;
-    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+    for (int u = wg_first<PAIR>(); u < p.units; u += wg_step<PAIR>()) {
         const WgUnit w = wg_unit(p, u);
         const int r = w.rs / p.S, s = w.rs - (w.rs / p.S) * p.S;
-        const int k0 = w.kt * WG_BM, c0 = w.ct * p.BN;
+        const int k0 = w.kt * (PAIR ? 2 * WG_BM : WG_BM) + (int)rank * WG_BM;
+        const int c0 = w.ct * p.BN + (int)rank * (p.b_atoms * 64);
         // the first pixel of the unit's first block; later blocks step by 64
         // pixels without a division
         long long m0 = (long long)w.kb0 * WG_BP;
@@ -105,15 +125,25 @@ __device__ void wg_produce(const WgParams &p, const CUtensorMap *tmA, const CUte
         }
         for (int kb = w.kb0; kb < w.kb1; ++kb, m0 += WG_BP) {
             if (!mbar_wait(&empty[stage], ph ^ 1u, ctl, 11)) return;
-            mbar_arrive_expect_tx(&full[stage], tx);
+            if (!PAIR || rank == 0) mbar_arrive_expect_tx(&full[stage], tx);
             const uint32_t a = sA + (uint32_t)stage * WG_A_BYTES;
-            tma_load_2d(a, tmA, &full[stage], k0, (int)m0);
-            tma_load_2d(a + WG_ATOM, tmA, &full[stage], k0 + 64, (int)m0);
             const uint32_t b = sB + (uint32_t)stage * b_bytes;
-            for (int at = 0; at < p.b_atoms; ++at)
-                tma_load_im2col_4d(b + (uint32_t)at * WG_ATOM, tmB, &full[stage], c0 + at * 64,
-                                   q0 * p.v - p.pl, p0 * p.u - p.pt, n0, (uint16_t)(s * p.dw),
-                                   (uint16_t)(r * p.dh));
+            if constexpr (PAIR) {
+                const uint32_t fb = full0 + 8u * (uint32_t)stage;
+                tma_load_2d_pair(a, tmA, fb, k0, (int)m0);
+                tma_load_2d_pair(a + WG_ATOM, tmA, fb, k0 + 64, (int)m0);
+                for (int at = 0; at < p.b_atoms; ++at)
+                    tma_load_im2col_4d_pair(b + (uint32_t)at * WG_ATOM, tmB, fb, c0 + at * 64,
+                                            q0 * p.v - p.pl, p0 * p.u - p.pt, n0, (uint16_t)(s * p.dw),
+                                            (uint16_t)(r * p.dh));
+            } else {
+                tma_load_2d(a, tmA, &full[stage], k0, (int)m0);
+                tma_load_2d(a + WG_ATOM, tmA, &full[stage], k0 + 64, (int)m0);
+                for (int at = 0; at < p.b_atoms; ++at)
+                    tma_load_im2col_4d(b + (uint32_t)at * WG_ATOM, tmB, &full[stage], c0 + at * 64,
+                                       q0 * p.v - p.pl, p0 * p.u - p.pt, n0, (uint16_t)(s * p.dw),
+                                       (uint16_t)(r * p.dh));
+            }
             q0 += p.dq;
             p0 += p.dp;
             n0 += p.dn;
@@ -124,6 +154,7 @@ __device__ void wg_produce(const WgParams &p, const CUtensorMap *tmA, const CUte
     }
 }
 
+template <bool PAIR>
 __device__ void wg_mma(const WgParams &p, uint32_t tmem_base, uint32_t sA, uint32_t sB,
                        uint64_t *full, uint64_t *empty, uint64_t *tfull, uint64_t *tempty,
                        uint64_t *mma_done, const WaitCtl &ctl) {
@@ -137,11 +168,13 @@ __device__ void wg_mma(const WgParams &p, uint32_t tmem_base, uint32_t sA, uint3
     int stage = 0, it = 0;
     uint32_t ph = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x, ++it) {
+    for (int u = wg_first<PAIR>(); ok && u < p.units; u += wg_step<PAIR>(), ++it) {
         const WgUnit w = wg_unit(p, u);
         const int buf = it & 1;
         const uint32_t aph = (uint32_t)(it >> 1) & 1u;
-        if (!mbar_wait(&tempty[buf], aph ^ 1u, ctl, 13)) {
+        // (pairs: both CTAs' epilogues arrive, the other one remotely)
+        if (!(PAIR ? mbar_wait_cluster(&tempty[buf], aph ^ 1u, ctl, 13)
+                   : mbar_wait(&tempty[buf], aph ^ 1u, ctl, 13))) {
             ok = false;
             break;
         }
@@ -157,10 +190,16 @@ __device__ void wg_mma(const WgParams &p, uint32_t tmem_base, uint32_t sA, uint3
             tc_fence_after_sync();
 #pragma unroll
             for (int j = 0; j < WG_BP / 16; ++j) {
-                umma_bf16_nc(d, ad + 128u * j, bd + 128u * j, p.idesc, acc);
+                if constexpr (PAIR)
+                    umma_bf16_pair(d, ad + 128u * j, bd + 128u * j, p.idesc, acc);
+                else
+                    umma_bf16_nc(d, ad + 128u * j, bd + 128u * j, p.idesc, acc);
                 acc = 1;
             }
-            umma_commit(&empty[stage]);
+            if (PAIR)
+                umma_commit_pair(&empty[stage], 3);  // both CTAs' slots free once these are done
+            else
+                umma_commit(&empty[stage]);
             if (++stage == ST) {
                 stage = 0;
                 ph ^= 1u;
@@ -172,7 +211,10 @@ __device__ void wg_mma(const WgParams &p, uint32_t tmem_base, uint32_t sA, uint3
             }
         }
         if (!ok) break;
-        umma_commit(&tfull[buf]);
+        if (PAIR)
+            umma_commit_pair(&tfull[buf], 3);  // both CTAs' accumulator rows are ready
+        else
+            umma_commit(&tfull[buf]);
     }
     if (!ok) {
         // loads issued for stages not consumed land on these barriers; wait
@@ -184,19 +226,23 @@ __device__ void wg_mma(const WgParams &p, uint32_t tmem_base, uint32_t sA, uint3
             if (++stage == ST) stage = 0, ph ^= 1u;
         }
     }
-    umma_commit(mma_done);
-    volatile int dummy = 0;
-    const WaitCtl fin{&dummy, p.err, p.timeout_ns};
-    mbar_wait(mma_done, 0u, fin, 98);
+    // every MMA issued must complete before tensor memory is released (the
+    // kernel waits for this commit in both CTAs)
+    if (PAIR)
+        umma_commit_pair(mma_done, 3);
+    else
+        umma_commit(mma_done);
 }
 
-__device__ void wg_epilogue(const WgParams &p, uint32_t tmem_base, uint64_t *tfull, uint64_t *tempty,
-                            uint32_t epi_smem, const CUtensorMap *tmD, const WaitCtl &ctl) {
+template <bool PAIR>
+__device__ void wg_epilogue(const WgParams &p, uint32_t rank, uint32_t tmem_base, uint64_t *tfull,
+                            uint64_t *tempty, uint32_t epi_smem, const CUtensorMap *tmD, const WaitCtl &ctl) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31: filters
     const uint32_t my_bufs = epi_smem + (uint32_t)(quad * 2 * WG_EPI_BUF);
+    const uint32_t tempty0 = PAIR ? mapa_shared(smem_u32(tempty), 0) : 0u;  // the leader's barriers
     int nbuf = 0, it = 0;
-    for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++it) {
+    for (int u = wg_first<PAIR>(); u < p.units; u += wg_step<PAIR>(), ++it) {
         const WgUnit w = wg_unit(p, u);
         const int buf = it & 1;
         const uint32_t ph = (uint32_t)(it >> 1) & 1u;
@@ -206,7 +252,7 @@ __device__ void wg_epilogue(const WgParams &p, uint32_t tmem_base, uint64_t *tfu
         if (!okw) break;
         __syncwarp();
         tc_fence_after_sync();
-        const int krow = w.kt * WG_BM + quad * 32;
+        const int krow = w.kt * (PAIR ? 2 * WG_BM : WG_BM) + (int)rank * WG_BM + quad * 32;
         const int c0 = w.ct * p.BN;
         const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)buf * p.acc_stride;
         for (int cc = 0; cc < p.BN && c0 + cc < p.C; cc += 32) {
@@ -236,18 +282,24 @@ __device__ void wg_epilogue(const WgParams &p, uint32_t tmem_base, uint64_t *tfu
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[buf]);
+        if (lane == 0) {
+            if (PAIR)
+                mbar_arrive_cluster(tempty0 + 8u * (uint32_t)buf);  // release on the leader
+            else
+                mbar_arrive(&tempty[buf]);
+        }
     }
     if (lane == 0) bulk_wait_group_read<0>();  // shared memory read before exit
     __syncwarp();
 }
 
+template <bool PAIR>
 __global__ void __launch_bounds__(WG_THREADS, 1)
     conv_wgrad_kernel(const __grid_constant__ WgParams p, const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmD) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
-    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);  // same offset in both CTAs
     const int ST = p.stages;
     const uint32_t b_bytes = (uint32_t)p.b_atoms * WG_ATOM;
     uint8_t *smA = smem;
@@ -263,14 +315,15 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
     if (threadIdx.x == 0) {
         for (int i = 0; i < ST; ++i) {
-            mbar_init(&full[i], 1u);
-            mbar_init(&empty[i], 1u);
+            mbar_init(&full[i], 1u);   // the (leader's) expect-tx arrival
+            mbar_init(&empty[i], 1u);  // the (leader's) commit
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1u);
-            mbar_init(&tempty[i], 4u);  // one arrival per epilogue warp
+            mbar_init(&tempty[i], PAIR ? 8u : 4u);  // one arrival per epilogue warp (of both CTAs)
         }
         mbar_init(mma_done, 1u);
         *abort_flag = 0;
@@ -282,27 +335,45 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
         prefetch_tmap(&tmD);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, p.tmem_cols);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(tmem_slot, p.tmem_cols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, p.tmem_cols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before_sync();
     __syncthreads();
+    if (PAIR) cluster_sync();  // both CTAs' barriers exist before any remote arrival
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
     const WaitCtl ctl{abort_flag, p.err, p.timeout_ns};
     if (warp == 0) {
-        if (lane == 0) wg_produce(p, &tmA, &tmB, smem_u32(smA), smem_u32(smB), full, empty, ctl);
+        if (lane == 0) wg_produce<PAIR>(p, rank, &tmA, &tmB, smem_u32(smA), smem_u32(smB), full, empty, ctl);
     } else if (warp == 1) {
-        if (lane == 0) wg_mma(p, tmem_base, smem_u32(smA), smem_u32(smB), full, empty, tfull, tempty,
-                              mma_done, ctl);
+        if (lane == 0 && rank == 0)
+            wg_mma<PAIR>(p, tmem_base, smem_u32(smA), smem_u32(smB), full, empty, tfull, tempty, mma_done,
+                         ctl);
+        if (lane == 0) {  // the (leader's) final commit reaches this CTA
+            volatile int dummy = 0;
+            const WaitCtl fin{&dummy, p.err, p.timeout_ns};
+            mbar_wait(mma_done, 0u, fin, 98);
+        }
     } else {
-        wg_epilogue(p, tmem_base, tfull, tempty, smem_u32(epi), &tmD, ctl);
+        wg_epilogue<PAIR>(p, rank, tmem_base, tfull, tempty, smem_u32(epi), &tmD, ctl);
     }
     __syncwarp();
     tc_fence_before_sync();
     __syncthreads();
+    if (PAIR) cluster_sync();  // neither CTA leaves while the pair's MMAs or loads may touch it
     tc_fence_after_sync();
-    if (warp == 1) tmem_dealloc(tmem_base, p.tmem_cols);
+    if (warp == 1) {
+        if (PAIR)
+            tmem_dealloc_pair(tmem_base, p.tmem_cols);
+        else
+            tmem_dealloc(tmem_base, p.tmem_cols);
+    }
 }
 
 // x channels-innermost with 16-byte strides, dy dense channels-innermost
@@ -349,20 +420,26 @@ dlcStatus_t dlc_launch_wgrad_tc(dlcContext *ctx, const BwdProblem &bp) {
     p.pt = bp.pt; p.pl = bp.pl; p.u = bp.u; p.v = bp.v; p.dh = bp.dh; p.dw = bp.dw;
     p.M = (long long)bp.N * bp.P * bp.Q;
     p.PQ = bp.P * bp.Q;
-    // channels per tile: the 64-channel multiple up to 256 that pads C least
-    // (ties to the wider tile)
-    p.BN = 64;
+    // SM pairs once there are more filters than one CTA's 128 (DLC_TC_WGRAD_PAIR=0: single CTAs)
+    const bool pair = bp.K > WG_BM && [] {
+        const char *ev = std::getenv("DLC_TC_WGRAD_PAIR");
+        return !(ev && std::atoi(ev) == 0);
+    }();
+    // channels per tile: the multiple of 64 (128 for a pair: each CTA loads
+    // whole 64-channel blocks) up to 256 that pads C least (ties to the wider)
+    p.BN = pair ? 128 : 64;
     long long best = -1;
     for (int bn : {256, 192, 128, 64}) {
+        if (pair && bn % 128) continue;
         const long long pad = (long long)((bp.C + bn - 1) / bn) * bn - bp.C;
         if (best < 0 || pad < best) best = pad, p.BN = bn;
     }
     if (const char *ev = std::getenv("DLC_TC_WGRAD_BN")) {
         const int bn = std::atoi(ev);
-        if (bn == 64 || bn == 128 || bn == 192 || bn == 256) p.BN = bn;
+        if (bn == 128 || bn == 256 || (!pair && (bn == 64 || bn == 192))) p.BN = bn;
     }
-    p.b_atoms = p.BN / 64;
-    p.m_tiles = (bp.K + WG_BM - 1) / WG_BM;
+    p.b_atoms = (pair ? p.BN / 2 : p.BN) / 64;  // 64-channel blocks of x a CTA loads
+    p.m_tiles = (bp.K + (pair ? 2 : 1) * WG_BM - 1) / ((pair ? 2 : 1) * WG_BM);
     p.c_tiles = (bp.C + p.BN - 1) / p.BN;
     p.tiles = p.m_tiles * p.c_tiles * bp.R * bp.S;
     p.kblocks = (int)((p.M + WG_BP - 1) / WG_BP);
@@ -370,7 +447,7 @@ dlcStatus_t dlc_launch_wgrad_tc(dlcContext *ctx, const BwdProblem &bp) {
     // GPU, each unit at least 32 pixel blocks
     int splits = 1;
     if (!ctx->deterministic) {
-        const int want = 2 * ctx->sm_count;
+        const int want = 2 * (pair ? ctx->sm_count / 2 : ctx->sm_count);
         splits = std::max(1, std::min((want + p.tiles - 1) / p.tiles, p.kblocks / 32));
     }
     p.splits = splits;
@@ -384,9 +461,10 @@ dlcStatus_t dlc_launch_wgrad_tc(dlcContext *ctx, const BwdProblem &bp) {
     int st = (WG_MAX_SMEM - 1024 - WG_BAR_AREA - WG_EPI_SMEM - stage_bytes) / stage_bytes;
     p.stages = std::min(st, 8);
     if (p.stages < 2) return DLC_STATUS_INTERNAL_ERROR;
-    // BF16 A and B, FP32 D, both operands MN-major (transpose bits 15, 16)
+    // BF16 A and B, FP32 D, both operands MN-major (transpose bits 15, 16);
+    // M = 256 for a pair (128 rows in each CTA)
     p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) |
-              ((uint32_t)(p.BN >> 3) << 17) | ((uint32_t)(WG_BM >> 4) << 24);
+              ((uint32_t)(p.BN >> 3) << 17) | ((uint32_t)(((pair ? 2 : 1) * WG_BM) >> 4) << 24);
     uint32_t cols = 32;
     while (cols < (uint32_t)(2 * p.BN)) cols <<= 1;
     p.tmem_cols = cols;
@@ -435,11 +513,34 @@ dlcStatus_t dlc_launch_wgrad_tc(dlcContext *ctx, const BwdProblem &bp) {
             return DLC_STATUS_EXECUTION_FAILED;
     }
     const size_t smem = 1024 + (size_t)p.stages * stage_bytes + WG_EPI_SMEM + WG_BAR_AREA;
-    if (cudaFuncSetAttribute(conv_wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
+    auto kern = pair ? conv_wgrad_kernel<true> : conv_wgrad_kernel<false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return DLC_STATUS_EXECUTION_FAILED;
-    const int grid = std::max(1, std::min(p.units, ctx->sm_count));
-    conv_wgrad_kernel<<<grid, WG_THREADS, smem, ctx->stream>>>(p, ta, tb, td);
+    if (!pair) {
+        const int grid = std::max(1, std::min(p.units, ctx->sm_count));
+        kern<<<grid, WG_THREADS, smem, ctx->stream>>>(p, ta, tb, td);
+    } else {
+        // persistent pairs: as many clusters of two as can be resident at once
+        cudaLaunchConfig_t cfg;
+        std::memset(&cfg, 0, sizeof(cfg));
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.blockDim = dim3(WG_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = ctx->stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.gridDim = dim3(2 * (ctx->sm_count / 2), 1, 1);
+        int max_clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&max_clusters, (const void *)kern, &cfg) != cudaSuccess ||
+            max_clusters < 1)
+            return DLC_STATUS_EXECUTION_FAILED;
+        cfg.gridDim = dim3(2 * std::max(1, std::min(p.units, max_clusters)), 1, 1);
+        if (cudaLaunchKernelEx(&cfg, kern, p, ta, tb, td) != cudaSuccess) return DLC_STATUS_EXECUTION_FAILED;
+    }
     if (cudaGetLastError() != cudaSuccess) return DLC_STATUS_EXECUTION_FAILED;
     ctx->launches += 1;
     return DLC_STATUS_SUCCESS;

@@ -510,6 +510,15 @@ __device__ __forceinline__ void tma_load_im2col_4d_pair(uint32_t dst, const CUte
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *m, uint32_t cbar,
+                                                 int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(cbar), "r"(c0), "r"(c1)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap *m, uint32_t cbar,
                                                  int c0, int c1, int c2, int c3) {
     asm volatile(

@@ -339,8 +339,14 @@ WGRAD_TC_MORE = [
 ]
 
 
+@pytest.mark.parametrize("pair", ["1", "0"], ids=["sm_pairs", "single_sm"])
 @pytest.mark.parametrize("layer", WGRAD_TC_MORE, ids=lambda l: l.name)
-def test_wgrad_tensor_cores(layer):
+def test_wgrad_tensor_cores(layer, pair, monkeypatch):
+    """More than 128 filters run on SM pairs (M = 256 per MMA) unless
+    DLC_TC_WGRAD_PAIR=0; both agree with the oracle."""
+    if pair == "0" and layer.K <= 128:
+        pytest.skip("up to 128 filters always run on single SMs")
+    monkeypatch.setenv("DLC_TC_WGRAD_PAIR", pair)
     run_wgrad(layer, 734, expect="tc_wgrad")
     run_wgrad(layer, 735, alpha=-0.5, beta=2.0, expect="tc_wgrad", deterministic=True)
 
