@@ -37,7 +37,7 @@ using namespace dlc;
 constexpr int PBM = 128;                    // output pixels per CTA
 constexpr int PROW = 128;                   // bytes of one swizzled reduction row
 constexpr int PA_BYTES = PBM * PROW;        // A stage: 16 KiB
-constexpr int PAIR_THREADS = 192;
+constexpr int PAIR_THREADS = 224;
 constexpr int PAIR_MAX_SMEM = 232448;
 constexpr int PAIR_BAR_AREA = 256;
 constexpr int PAIR_EPI_BUF = 32 * 128;             // one warp's 32 rows x 32 FP32 columns
@@ -59,6 +59,7 @@ struct PairParams {
     // B operand: K-major rows of BN/2 filters (b_mn = 0), or MN-major (b_mn =
     // 1): b_atoms boxes of 128 bytes of filters x BK reduction rows each.
     int b_mn, b_atoms, flip;
+    int split_load;    // a second warp issues the B loads
     uint32_t b_stage;  // bytes of one CTA's B stage
     int num_tiles;     // pair tiles: ceil(M / 256) * n_tiles
     // Split tail: tiles [full_tiles, num_tiles) -- the part of the last wave
@@ -99,7 +100,9 @@ __device__ __forceinline__ bool pair_drain(uint64_t *bar, uint32_t parity, const
     return mbar_wait(bar, parity, c, 95);
 }
 
-template <int BK>
+// PART 0: this thread issues both operands' loads; 1: A (and arms the
+// barrier), 2: B only -- two threads of different warps share a stage's loads.
+template <int BK, int PART>
 __device__ void pair_produce(const PairParams &p, uint32_t rank, const CUtensorMap *tmA,
                              const CUtensorMap *tmB, uint32_t sA, uint32_t sB, uint64_t *full,
                              uint64_t *empty, const WaitCtl &ctl) {
@@ -125,11 +128,14 @@ __device__ void pair_produce(const PairParams &p, uint32_t rank, const CUtensorM
         int s = rs0 % p.S, r = rs0 / p.S;
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
             if (!mbar_wait(&empty[stage], ph ^ 1u, ctl, 1)) return;
-            if (rank == 0) mbar_arrive_expect_tx(&full[stage], tx);
-            tma_load_im2col_4d_pair(sA + (uint32_t)stage * PA_BYTES, tmA, full0 + 8u * stage, cb * BK,
-                                    wc, hc, n0, (uint16_t)(s * p.dw), (uint16_t)(r * p.dh));
+            if (PART != 2) {
+                if (rank == 0) mbar_arrive_expect_tx(&full[stage], tx);
+                tma_load_im2col_4d_pair(sA + (uint32_t)stage * PA_BYTES, tmA, full0 + 8u * stage, cb * BK,
+                                        wc, hc, n0, (uint16_t)(s * p.dw), (uint16_t)(r * p.dh));
+            }
             const int sc = p.flip ? p.S - 1 - s : s, rc = p.flip ? p.R - 1 - r : r;
-            if (p.b_mn) {
+            if (PART == 1) {
+            } else if (p.b_mn) {
                 for (int a = 0; a < p.b_atoms; ++a)
                     tma_load_4d_pair(sB + (uint32_t)stage * b_half + (uint32_t)a * atom_bytes, tmB,
                                      full0 + 8u * stage, k0 + a * BK, sc, rc, cb * BK);
@@ -422,7 +428,14 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
     griddep_wait();  // no global memory before the grid ahead of this one is done
 
     if (warp == 0) {
-        if (lane == 0) pair_produce<BK>(p, rank, &tmA, &tmB, sA, sB, full, empty, ctl);
+        if (lane == 0) {
+            if (p.split_load)
+                pair_produce<BK, 1>(p, rank, &tmA, &tmB, sA, sB, full, empty, ctl);
+            else
+                pair_produce<BK, 0>(p, rank, &tmA, &tmB, sA, sB, full, empty, ctl);
+        }
+    } else if (warp == 6) {
+        if (lane == 0 && p.split_load) pair_produce<BK, 2>(p, rank, &tmA, &tmB, sA, sB, full, empty, ctl);
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) pair_mma<TF32>(p, tmem_base, sA, sB, full, empty, tfull, tempty, mma_done, ctl);
         // the leader's final commit reaches both CTAs; it also covers every
@@ -502,6 +515,10 @@ dlcStatus_t dlc_launch_pair(dlcContext *ctx, const ConvProblem &pb) {
     p.n_tiles = (pb.K + p.BN - 1) / p.BN;
     p.flip = pb.flip;
     p.b_mn = pb.w_mn;
+    {
+        const char *ev = std::getenv("DLC_TC_PAIR_SPLITLOAD");
+        p.split_load = (ev && std::atoi(ev) == 0) ? 0 : 1;
+    }
     p.b_atoms = (p.BN / 2 + BK - 1) / BK;
     p.b_stage = p.b_mn ? (uint32_t)(p.b_atoms * BK * PROW) : (uint32_t)(p.BN / 2) * PROW;
     const long long m_pairs = (p.M + 2 * PBM - 1) / (2 * PBM);
