@@ -37,7 +37,8 @@ using namespace dlc;
 constexpr int PBM = 128;                    // output pixels per CTA
 constexpr int PROW = 128;                   // bytes of one swizzled reduction row
 constexpr int PA_BYTES = PBM * PROW;        // A stage: 16 KiB
-constexpr int PAIR_THREADS = 224;
+constexpr int PAIR_EPI_WARP0 = 3;          // warps 0-2 load and issue; the epilogue follows
+constexpr int PAIR_MAX_THREADS = (PAIR_EPI_WARP0 + 8) * 32;
 constexpr int PAIR_MAX_SMEM = 232448;
 constexpr int PAIR_BAR_AREA = 256;
 constexpr int PAIR_EPI_BUF = 32 * 128;             // one warp's 32 rows x 32 FP32 columns
@@ -60,6 +61,7 @@ struct PairParams {
     // 1): b_atoms boxes of 128 bytes of filters x BK reduction rows each.
     int b_mn, b_atoms, flip;
     int split_load;    // a second warp issues the B loads
+    int epi_parts;     // 1: four epilogue warps; 2: eight, two per TMEM lane quarter
     uint32_t b_stage;  // bytes of one CTA's B stage
     int num_tiles;     // pair tiles: ceil(M / 256) * n_tiles
     // Split tail: tiles [full_tiles, num_tiles) -- the part of the last wave
@@ -284,12 +286,15 @@ __device__ void pair_epilogue(const PairParams &p, uint32_t rank, uint32_t tmem_
                               uint64_t *tfull, uint64_t *tempty, uint32_t epi_smem,
                               const CUtensorMap *tmY, const WaitCtl &ctl) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // a warp reads the TMEM lanes of its warp index mod 4; with eight warps
+    // each quarter has two, taking alternate 32-column chunks (part 0, 1)
     const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
+    const int part = (warp - PAIR_EPI_WARP0) >> 2;
     const int row = quad * 32 + lane;
     const bool plain = p.beta == 0.f && p.bias == nullptr && !p.relu && !p.y_bf16 && p.ys[1] == 1;
     const uint32_t tempty0 = mapa_shared(smem_u32(tempty), 0);  // the leader's barriers
     float *yf = static_cast<float *>(p.y);
-    const uint32_t my_bufs = epi_smem + (uint32_t)(quad * 2 * PAIR_EPI_BUF);
+    const uint32_t my_bufs = epi_smem + (uint32_t)((warp - PAIR_EPI_WARP0) * 2 * PAIR_EPI_BUF);
     int nbuf = 0;
     int it = 0;
     for (int u = (int)cluster_id_x(); u < p.num_units; u += (int)num_clusters_x(), ++it) {
@@ -314,7 +319,7 @@ __device__ void pair_epilogue(const PairParams &p, uint32_t rank, uint32_t tmem_
             ybase = (long long)n * p.ys[0] + (long long)op * p.ys[2] + (long long)oq * p.ys[3];
         }
         const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)buf * p.acc_stride;
-        for (int c0 = 0; c0 < p.BN && kt + c0 < p.K; c0 += 32) {
+        for (int c0 = 32 * part; c0 < p.BN && kt + c0 < p.K; c0 += 32 * p.epi_parts) {
             uint32_t v[32];
             tmem_ld_32x32b_x32(taddr + (uint32_t)c0, v);
             tmem_ld_wait();
@@ -373,7 +378,7 @@ __device__ void pair_epilogue(const PairParams &p, uint32_t rank, uint32_t tmem_
 }
 
 template <bool TF32>
-__global__ void __launch_bounds__(PAIR_THREADS, 1)
+__global__ void __launch_bounds__(PAIR_MAX_THREADS, 1)
     conv_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmY) {
     constexpr int BK = PROW / (TF32 ? 4 : 2);
@@ -386,7 +391,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
     uint8_t *smA = smem;
     uint8_t *smB = smA + (size_t)ST * PA_BYTES;
     uint8_t *epi = smB + (size_t)ST * b_half;  // y staging (y_tma), 1024-aligned
-    uint64_t *bars = reinterpret_cast<uint64_t *>(epi + (p.y_tma ? PAIR_EPI_SMEM : 0));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(epi + (p.y_tma ? p.epi_parts * PAIR_EPI_SMEM : 0));
     uint64_t *full = bars;
     uint64_t *empty = bars + ST;
     uint64_t *tfull = bars + 2 * ST;
@@ -404,7 +409,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1u);
-            mbar_init(&tempty[i], 8u);  // four epilogue warps of each CTA (leader's copy)
+            mbar_init(&tempty[i], 8u * (uint32_t)p.epi_parts);  // every epilogue warp of both CTAs
         }
         mbar_init(mma_done, 1u);
         *abort_flag = 0;
@@ -434,7 +439,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
             else
                 pair_produce<BK, 0>(p, rank, &tmA, &tmB, sA, sB, full, empty, ctl);
         }
-    } else if (warp == 6) {
+    } else if (warp == 2) {
         if (lane == 0 && p.split_load) pair_produce<BK, 2>(p, rank, &tmA, &tmB, sA, sB, full, empty, ctl);
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) pair_mma<TF32>(p, tmem_base, sA, sB, full, empty, tfull, tempty, mma_done, ctl);
@@ -533,7 +538,14 @@ dlcStatus_t dlc_launch_pair(dlcContext *ctx, const ConvProblem &pb) {
         const char *ev = std::getenv("DLC_TC_PAIR_YTMA");  // =0 for direct stores
         p.y_tma = (dense && !(ev && std::atoi(ev) == 0)) ? 1 : 0;
     }
-    const int epi_bytes = p.y_tma ? PAIR_EPI_SMEM : 0;
+    // eight epilogue warps when a tile's few k-blocks take less time than its
+    // epilogue (DLC_TC_PAIR_EPI=4 or 8 sets the count)
+    p.epi_parts = p.num_kb <= 4 ? 2 : 1;
+    if (const char *ev = std::getenv("DLC_TC_PAIR_EPI")) {
+        const int e = std::atoi(ev);
+        if (e == 4 || e == 8) p.epi_parts = e / 4;
+    }
+    const int epi_bytes = p.y_tma ? p.epi_parts * PAIR_EPI_SMEM : 0;
     const int stage_bytes = PA_BYTES + (int)p.b_stage;
     // slack after the barriers: one more half filter tile, so that no operand
     // read of the last stage can leave the CTA's shared memory
@@ -612,7 +624,7 @@ dlcStatus_t dlc_launch_pair(dlcContext *ctx, const ConvProblem &pb) {
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = dlc_pdl_enabled() ? 1 : 0;
-    cfg.blockDim = dim3(PAIR_THREADS, 1, 1);
+    cfg.blockDim = dim3((PAIR_EPI_WARP0 + 4 * p.epi_parts) * 32, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = ctx->stream;
     cfg.attrs = attr;

@@ -116,10 +116,14 @@ def test_tc_im2col_pair_parity_full(handle, layer, bn, monkeypatch):
                   expect_kernel="tc_im2col_pair")
 
 
+@pytest.mark.parametrize("epi", ["4", "8"], ids=["epi4", "epi8"])
 @pytest.mark.parametrize("layer", [PAIR_CASES[i] for i in (0, 1, 2, 5, 8, 9, 10)],
                          ids=lambda l: l.name)
-def test_tc_im2col_pair_bulk_stores(handle, layer):
-    """y written through 2-D bulk tensor stores of 32 x 32 blocks (the default)."""
+def test_tc_im2col_pair_bulk_stores(handle, layer, epi, monkeypatch):
+    """y written through 2-D bulk tensor stores of 32 x 32 blocks (the default),
+    by four epilogue warps or eight (two per TMEM lane quarter, alternate
+    32-column chunks)."""
+    monkeypatch.setenv("DLC_TC_PAIR_EPI", epi)
     run_and_check(handle, layer, 1150 + PAIR_CASES.index(layer), full=True, with_bias=True,
                   relu=True, expect_kernel="tc_im2col_pair")
 
