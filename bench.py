@@ -756,6 +756,28 @@ def run_profile_layer(args):
     from deep_learning_convolution_gb300 import build as dlc_build
     dlc_build.build()
     j = args.profile_layer
+    if args.workload in EXTRA_REPS:  # one op of a backward or pooling workload
+        handle = api.Handle()
+        ops = _extra_ops(args.workload, handle, "cuda")
+        op = ops[j]
+        for _ in range(args.reps):
+            op[1]()
+        torch.cuda.synchronize()
+        handle.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record()
+        for _ in range(args.reps):
+            op[1]()
+        end.record()
+        torch.cuda.synchronize()
+        handle.synchronize()
+        print(json.dumps({"layer": op[0], "kernel": op[4],
+                          "us_per_launch": round(start.elapsed_time(end) * 1e3 / args.reps, 2)}))
+        for o in ops:
+            if o[6] is not None:
+                o[6].close()
+        handle.close()
+        return
     layer = synth.WORKLOADS[args.workload][j]
     x, w, _ = synth.make_inputs(layer, synth.workload_seed(args.workload, j), batch=args.batch)
     handle = api.Handle()
@@ -784,7 +806,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default=HEADLINE, choices=CONFIG_ORDER)
+    ap.add_argument("--workload", default=HEADLINE, choices=CONFIG_ORDER + list(EXTRA_REPS),
+                    help="the backward and pooling workloads only with --profile-layer")
     ap.add_argument("--reps-per-step", type=int, default=None,
                     help="passes over the stack per step (default: the workload's fixed count)")
     ap.add_argument("--no-configs", action="store_true",
@@ -804,6 +827,8 @@ def main():
     if args.profile_layer is not None:
         run_profile_layer(args)
         return
+    if args.workload in EXTRA_REPS:
+        ap.error(f"--workload {args.workload} goes with --profile-layer (the bench times it in `configs`)")
     if args.warmup < 3:
         args.warmup = 3
     rank, world, local_rank = env_rank()
