@@ -12,13 +12,15 @@
 // MMA falls from A + B to A + B/2 -- the single-SM kernel's stages are bound by
 // that traffic at BN = 192..256.
 //
-// Roles (per CTA, 6 warps): warp 0 lane 0 issues the TMA loads of both CTAs'
-// halves of a stage, which complete on the LEADER's (rank 0) full barrier;
-// warp 1 lane 0 of the leader alone issues the MMAs and commits each stage
-// back to the empty barriers of both CTAs (multicast); warps 2-5 of each CTA
-// read their CTA's 128 accumulator rows from tensor memory, apply the epilogue
-// and store y, then release the accumulator on the leader's barrier.  Every
-// wait is bounded; both CTAs meet at a cluster barrier before tensor memory is
+// Roles (per CTA, 7 or 11 warps): warp 0 lane 0 issues the A (im2col) loads
+// and arms the stage's barrier, warp 2 lane 0 the B (filter) loads -- both
+// CTAs' loads complete on the LEADER's (rank 0) full barrier; warp 1 lane 0 of
+// the leader alone issues the MMAs and commits each stage back to the empty
+// barriers of both CTAs (multicast); warps 3-6 (or 3-10 for tiles of at most
+// four k-blocks, two warps per TMEM lane quarter) of each CTA read their CTA's
+// 128 accumulator rows from tensor memory, apply the epilogue and store y,
+// then release the accumulator on the leader's barrier.  Every wait is
+// bounded; both CTAs meet at a cluster barrier before tensor memory is
 // released.
 #include <cuda_bf16.h>
 
