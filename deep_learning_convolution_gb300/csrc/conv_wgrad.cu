@@ -443,12 +443,21 @@ dlcStatus_t dlc_launch_wgrad_tc(dlcContext *ctx, const BwdProblem &bp) {
     p.c_tiles = (bp.C + p.BN - 1) / p.BN;
     p.tiles = p.m_tiles * p.c_tiles * bp.R * bp.S;
     p.kblocks = (int)((p.M + WG_BP - 1) / WG_BP);
-    // split the pixel reduction so that about two waves of units fill the
-    // GPU, each unit at least 32 pixel blocks
+    // split the pixel reduction where it shortens the busiest CTA (or pair):
+    // s ranges of each tile make rounds(s) = ceil(tiles * s / workers) rounds of
+    // units of kblocks / s k-blocks each, and a unit costs about ten k-blocks
+    // more (its reduce-add epilogue and pipeline fill); the cheapest s, the
+    // fewest ranges among equals, each range at least 16 k-blocks
     int splits = 1;
     if (!ctx->deterministic) {
-        const int want = 2 * (pair ? ctx->sm_count / 2 : ctx->sm_count);
-        splits = std::max(1, std::min((want + p.tiles - 1) / p.tiles, p.kblocks / 32));
+        const long long workers = pair ? ctx->sm_count / 2 : ctx->sm_count;
+        const int smax = std::max(1, std::min(32, p.kblocks / 16));
+        double best = -1.0;
+        for (int sp = 1; sp <= smax; ++sp) {
+            const long long rounds = ((long long)p.tiles * sp + workers - 1) / workers;
+            const double cost = (double)rounds * ((double)p.kblocks / sp + 10.0);
+            if (best < 0 || cost < best - 1e-9) best = cost, splits = sp;
+        }
     }
     p.splits = splits;
     p.dn = (int)(WG_BP / p.PQ);
