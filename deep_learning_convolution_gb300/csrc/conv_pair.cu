@@ -106,13 +106,17 @@ __device__ __forceinline__ bool pair_drain(uint64_t *bar, uint32_t parity, const
 
 // PART 0: this thread issues both operands' loads; 1: A (and arms the
 // barrier), 2: B only -- two threads of different warps share a stage's loads.
-template <int BK, int PART>
+// MIXED: the last channel block of a tap holds at most 32 channels and comes
+// in 64-byte rows (tmA2 / tmB2: 32-channel boxes, 64-byte swizzle) -- half the
+// bytes of a full block, for half its MMAs.
+template <int BK, int PART, bool MIXED>
 __device__ void pair_produce(const PairParams &p, uint32_t rank, const CUtensorMap *tmA,
-                             const CUtensorMap *tmB, uint32_t sA, uint32_t sB, uint64_t *full,
-                             uint64_t *empty, const WaitCtl &ctl) {
+                             const CUtensorMap *tmB, const CUtensorMap *tmA2, const CUtensorMap *tmB2,
+                             uint32_t sA, uint32_t sB, uint64_t *full, uint64_t *empty, const WaitCtl &ctl) {
     const int ST = p.stages;
     const uint32_t b_half = p.b_stage;
     const uint32_t tx = 2u * (PA_BYTES + b_half);  // both CTAs' bytes land on the leader's barrier
+    const uint32_t tx_h = tx / 2u;                 // a block of 64-byte rows
     const uint32_t atom_bytes = (uint32_t)BK * PROW;  // MN-major: BK rows of 128 bytes
     const uint32_t full0 = mapa_shared(smem_u32(full), 0);  // the leader's full barriers
     int stage = 0;
@@ -132,13 +136,17 @@ __device__ void pair_produce(const PairParams &p, uint32_t rank, const CUtensorM
         int s = rs0 % p.S, r = rs0 / p.S;
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
             if (!mbar_wait(&empty[stage], ph ^ 1u, ctl, 1)) return;
+            const bool half = MIXED && cb == p.c_blocks - 1;
             if (PART != 2) {
-                if (rank == 0) mbar_arrive_expect_tx(&full[stage], tx);
-                tma_load_im2col_4d_pair(sA + (uint32_t)stage * PA_BYTES, tmA, full0 + 8u * stage, cb * BK,
-                                        wc, hc, n0, (uint16_t)(s * p.dw), (uint16_t)(r * p.dh));
+                if (rank == 0) mbar_arrive_expect_tx(&full[stage], half ? tx_h : tx);
+                tma_load_im2col_4d_pair(sA + (uint32_t)stage * PA_BYTES, half ? tmA2 : tmA, full0 + 8u * stage,
+                                        cb * BK, wc, hc, n0, (uint16_t)(s * p.dw), (uint16_t)(r * p.dh));
             }
             const int sc = p.flip ? p.S - 1 - s : s, rc = p.flip ? p.R - 1 - r : r;
             if (PART == 1) {
+            } else if (MIXED) {
+                tma_load_4d_pair(sB + (uint32_t)stage * b_half, half ? tmB2 : tmB, full0 + 8u * stage, cb * BK,
+                                 sc, rc, k0);
             } else if (p.b_mn) {
                 for (int a = 0; a < p.b_atoms; ++a)
                     tma_load_4d_pair(sB + (uint32_t)stage * b_half + (uint32_t)a * atom_bytes, tmB,
@@ -155,7 +163,7 @@ __device__ void pair_produce(const PairParams &p, uint32_t rank, const CUtensorM
     }
 }
 
-template <bool TF32>
+template <bool TF32, bool MIXED>
 __device__ void pair_mma(const PairParams &p, uint32_t tmem_base, uint32_t sA, uint32_t sB,
                          uint64_t *full, uint64_t *empty, uint64_t *tfull, uint64_t *tempty,
                          uint64_t *mma_done, const WaitCtl &ctl) {
@@ -169,6 +177,9 @@ __device__ void pair_mma(const PairParams &p, uint32_t tmem_base, uint32_t sA, u
     const uint64_t b0 = p.b_mn ? sw128_mnmajor_desc(sB, (uint32_t)BK * PROW) : sw128_kmajor_desc(sB);
     const uint32_t b_k = p.b_mn ? (32u / E) * PROW / 16u : 2u;
     const uint64_t a_step = PA_BYTES >> 4, b_step = b_half >> 4;
+    // a block of 64-byte rows: the same start address, the 64-byte swizzle's
+    // stride and layout bits (the XOR of the two descriptors of one address)
+    const uint64_t to64 = sw64_kmajor_desc(sA) ^ sw128_kmajor_desc(sA);
     int stage = 0, it = 0;
     uint32_t ph = 0;
     bool ok = true;
@@ -184,19 +195,37 @@ __device__ void pair_mma(const PairParams &p, uint32_t tmem_base, uint32_t sA, u
         const uint32_t d = tmem_base + (uint32_t)buf * p.acc_stride;
         uint64_t ad = a0 + a_step * stage, bd = b0 + b_step * stage;
         uint32_t acc = 0;
+        int cb = MIXED ? w.kb0 % p.c_blocks : 0;
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
             if (!mbar_wait(&full[stage], ph, ctl, 4)) {
                 ok = false;
                 break;
             }
             tc_fence_after_sync();
+            if constexpr (MIXED && !TF32) {
+                if (cb == p.c_blocks - 1) {  // 32 channels in 64-byte rows: two MMAs
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {  // 32 bytes of the 128-byte row each
-                if constexpr (TF32)
-                    umma_tf32_pair(d, ad + 2u * j, bd + b_k * j, p.idesc, acc);
-                else
-                    umma_bf16_pair(d, ad + 2u * j, bd + b_k * j, p.idesc, acc);
-                acc = 1;
+                    for (int j = 0; j < 2; ++j) {
+                        umma_bf16_pair(d, (ad ^ to64) + 2u * j, (bd ^ to64) + 2u * j, p.idesc, acc);
+                        acc = 1;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        umma_bf16_pair(d, ad + 2u * j, bd + 2u * j, p.idesc, acc);
+                        acc = 1;
+                    }
+                }
+                if (++cb == p.c_blocks) cb = 0;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {  // 32 bytes of the 128-byte row each
+                    if constexpr (TF32)
+                        umma_tf32_pair(d, ad + 2u * j, bd + b_k * j, p.idesc, acc);
+                    else
+                        umma_bf16_pair(d, ad + 2u * j, bd + b_k * j, p.idesc, acc);
+                    acc = 1;
+                }
             }
             umma_commit_pair(&empty[stage], 3);  // both CTAs' slots free once these are done
             if (++stage == ST) {
@@ -379,10 +408,11 @@ __device__ void pair_epilogue(const PairParams &p, uint32_t rank, uint32_t tmem_
     __syncwarp();
 }
 
-template <bool TF32>
+template <bool TF32, bool MIXED>
 __global__ void __launch_bounds__(PAIR_MAX_THREADS, 1)
     conv_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmY) {
+                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmY,
+                     const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2) {
     constexpr int BK = PROW / (TF32 ? 4 : 2);
     griddep_launch_dependents();  // the next grid may claim SMs this one leaves
     extern __shared__ uint8_t smem_raw[];
@@ -420,6 +450,10 @@ __global__ void __launch_bounds__(PAIR_MAX_THREADS, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
+        if (MIXED) {
+            prefetch_tmap(&tmA2);
+            prefetch_tmap(&tmB2);
+        }
     }
     if (warp == 1) {
         tmem_alloc_pair(tmem_slot, p.tmem_cols);
@@ -437,14 +471,15 @@ __global__ void __launch_bounds__(PAIR_MAX_THREADS, 1)
     if (warp == 0) {
         if (lane == 0) {
             if (p.split_load)
-                pair_produce<BK, 1>(p, rank, &tmA, &tmB, sA, sB, full, empty, ctl);
+                pair_produce<BK, 1, MIXED>(p, rank, &tmA, &tmB, &tmA2, &tmB2, sA, sB, full, empty, ctl);
             else
-                pair_produce<BK, 0>(p, rank, &tmA, &tmB, sA, sB, full, empty, ctl);
+                pair_produce<BK, 0, MIXED>(p, rank, &tmA, &tmB, &tmA2, &tmB2, sA, sB, full, empty, ctl);
         }
     } else if (warp == 2) {
-        if (lane == 0 && p.split_load) pair_produce<BK, 2>(p, rank, &tmA, &tmB, sA, sB, full, empty, ctl);
+        if (lane == 0 && p.split_load)
+            pair_produce<BK, 2, MIXED>(p, rank, &tmA, &tmB, &tmA2, &tmB2, sA, sB, full, empty, ctl);
     } else if (warp == 1) {
-        if (lane == 0 && rank == 0) pair_mma<TF32>(p, tmem_base, sA, sB, full, empty, tfull, tempty, mma_done, ctl);
+        if (lane == 0 && rank == 0) pair_mma<TF32, MIXED>(p, tmem_base, sA, sB, full, empty, tfull, tempty, mma_done, ctl);
         // the leader's final commit reaches both CTAs; it also covers every
         // stage the MMAs consumed, i.e. every load of either CTA
         if (lane == 0) pair_drain(mma_done, 0u, p);
@@ -481,8 +516,9 @@ bool dlc_pair_enabled(const dlcContext *) {
 
 dlcStatus_t dlc_preload_pair() {
     cudaFuncAttributes a;
-    if (cudaFuncGetAttributes(&a, conv_pair_kernel<false>) != cudaSuccess ||
-        cudaFuncGetAttributes(&a, conv_pair_kernel<true>) != cudaSuccess)
+    if (cudaFuncGetAttributes(&a, conv_pair_kernel<false, false>) != cudaSuccess ||
+        cudaFuncGetAttributes(&a, conv_pair_kernel<false, true>) != cudaSuccess ||
+        cudaFuncGetAttributes(&a, conv_pair_kernel<true, false>) != cudaSuccess)
         return DLC_STATUS_EXECUTION_FAILED;
     return DLC_STATUS_SUCCESS;
 }
@@ -518,6 +554,12 @@ dlcStatus_t dlc_launch_pair(dlcContext *ctx, const ConvProblem &pb) {
         if (bn >= 32 && bn <= 256 && bn % 32 == 0) p.BN = bn;
     }
     p.c_blocks = (pb.C + BK - 1) / BK;
+    // the last channel block in 64-byte rows when it holds at most 32
+    // channels (BF16, K-major filters; DLC_TC_PAIR_MIXED=0 keeps it whole)
+    const bool mixed = !tf32 && !pb.w_mn && pb.C % BK != 0 && pb.C % BK <= BK / 2 && [] {
+        const char *ev = std::getenv("DLC_TC_PAIR_MIXED");
+        return !(ev && std::atoi(ev) == 0);
+    }();
     p.num_kb = pb.R * pb.S * p.c_blocks;
     p.n_tiles = (pb.K + p.BN - 1) / p.BN;
     p.flip = pb.flip;
@@ -600,6 +642,22 @@ dlcStatus_t dlc_launch_pair(dlcContext *ctx, const ConvProblem &pb) {
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return DLC_STATUS_EXECUTION_FAILED;
 
+    // the 32-channel boxes of a mixed last block: 64-byte swizzled rows
+    CUtensorMap ta2, tb2;
+    std::memset(&ta2, 0, sizeof(ta2));
+    std::memset(&tb2, 0, sizeof(tb2));
+    if (mixed) {
+        if (ctx->encode_im2col(&ta2, dt, 4, const_cast<void *>(pb.x), gdim, gstr, lower, upper,
+                               (cuuint32_t)(BK / 2), (cuuint32_t)PBM, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                               CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return DLC_STATUS_EXECUTION_FAILED;
+        const cuuint32_t box2[4] = {(cuuint32_t)(BK / 2), 1, 1, (cuuint32_t)(p.BN / 2)};
+        if (ctx->encode_tiled(&tb2, dt, 4, const_cast<void *>(pb.w), wdim, wstr, box2, ones,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return DLC_STATUS_EXECUTION_FAILED;
+    }
     const size_t smem = 1024 + (size_t)p.stages * stage_bytes + epi_bytes + PAIR_BAR_AREA + slack;
     CUtensorMap ty;
     std::memset(&ty, 0, sizeof(ty));
@@ -614,7 +672,8 @@ dlcStatus_t dlc_launch_pair(dlcContext *ctx, const ConvProblem &pb) {
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return DLC_STATUS_EXECUTION_FAILED;
     }
-    auto kern = tf32 ? conv_pair_kernel<true> : conv_pair_kernel<false>;
+    auto kern = tf32 ? conv_pair_kernel<true, false>
+                     : (mixed ? conv_pair_kernel<false, true> : conv_pair_kernel<false, false>);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return DLC_STATUS_EXECUTION_FAILED;
     cudaLaunchConfig_t cfg;
@@ -669,7 +728,7 @@ dlcStatus_t dlc_launch_pair(dlcContext *ctx, const ConvProblem &pb) {
     }
     cfg.gridDim = dim3(2 * clusters, 1, 1);
     cfg.numAttrs = 2;
-    if (cudaLaunchKernelEx(&cfg, kern, p, ta, tb, ty) != cudaSuccess) return DLC_STATUS_EXECUTION_FAILED;
+    if (cudaLaunchKernelEx(&cfg, kern, p, ta, tb, ty, ta2, tb2) != cudaSuccess) return DLC_STATUS_EXECUTION_FAILED;
     ctx->launches += 1;
     return DLC_STATUS_SUCCESS;
 }

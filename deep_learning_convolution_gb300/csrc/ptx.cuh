@@ -584,6 +584,17 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
            | (static_cast<uint64_t>(2) << 61);                // 128-byte swizzle
 }
 
+// The same for the 64-byte swizzle: rows of 64 bytes, 8-row groups 512 bytes
+// apart, tile base 512-byte aligned; `saddr` may be advanced by 32 bytes
+// inside the row.
+__device__ __forceinline__ uint64_t sw64_kmajor_desc(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu)
+           | (static_cast<uint64_t>(1) << 16)
+           | (static_cast<uint64_t>(512 >> 4) << 32)
+           | (static_cast<uint64_t>(1) << 46)
+           | (static_cast<uint64_t>(4) << 61);                // 64-byte swizzle
+}
+
 // Shared-memory matrix descriptor for an MN-major operand tile stored with
 // the 128-byte swizzle: each 128-byte row holds consecutive M/N elements of
 // one K index, 8-row groups of K are 1024 bytes apart (stride offset), and

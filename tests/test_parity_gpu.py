@@ -139,6 +139,29 @@ def test_tc_im2col_pair_split_tail(handle, layer, split, monkeypatch):
                   expect_kernel="tc_im2col_pair")
 
 
+# channel counts whose last 64-channel block holds at most 32 channels: that
+# block comes in 64-byte rows (32-channel boxes, two MMAs) unless
+# DLC_TC_PAIR_MIXED=0
+MIXED_CASES = [
+    IM2COL_CASES[1],  # 96 = 64 + 32
+    L("pair_bf16_c72_k64_3x3_mixed", 2, 72, 13, 13, 64, 3, 3, **P(1, 1, 1, 1)),
+    L("pair_bf16_c160_k96_3x3_s2_mixed", 2, 160, 15, 17, 96, 3, 3, **P(1, 1, 1, 1), u=2, v=2),
+    L("pair_bf16_c136_k200_5x5_mixed", 2, 136, 12, 14, 200, 5, 5, **P(2, 1, 0, 3)),
+]
+
+
+@pytest.mark.parametrize("mixed", ["1", "0"], ids=["mixed_last_block", "whole_blocks"])
+@pytest.mark.parametrize("layer", MIXED_CASES, ids=lambda l: l.name)
+def test_tc_im2col_pair_mixed_last_block(handle, layer, mixed, monkeypatch):
+    monkeypatch.setenv("DLC_TC_PAIR_MIXED", mixed)
+    seed = 1196 + MIXED_CASES.index(layer)
+    run_and_check(handle, layer, seed, full=True, expect_kernel="tc_im2col_pair")
+    run_and_check(handle, layer, seed + 10, full=True, alpha=0.5, beta=0.25, with_bias=True,
+                  relu=True, expect_kernel="tc_im2col_pair")
+    run_and_check(handle, layer, seed + 20, full=True, mode="convolution",
+                  expect_kernel="tc_im2col_pair")
+
+
 def test_tc_im2col_pair_epilogue(handle):
     import torch
     layer = IM2COL_CASES[1]
