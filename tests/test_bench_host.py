@@ -114,3 +114,21 @@ def test_bench_geometry_matches_the_oracle_extent():
         assert cfg["flops_per_pass"] == sum(
             bench.layer_geometry(l, *bench.layer_output_dims(l))[0] for l in layers)
         assert cfg["flops_per_step"] == cfg["flops_per_pass"] * cfg["reps_per_step"]
+
+
+def test_per_launch_events_ride_on_one_pass_in_eight():
+    """Every step carries per-launch events on at least one pass, on one pass in
+    INST_EVERY when the step has that many, and never past the step's end; the
+    timing description names the same rate."""
+    b = _bench()
+    E, h = b.INST_EVERY, b.INST_EVERY // 2
+    for reps in (1, 2, 7, 8, 9, 12, 13, 40, 80, 200, 2000):
+        inst = b.instrumented_passes(reps)
+        assert inst, reps
+        assert all(0 <= r < reps for r in inst), (reps, inst)
+        assert len(set(inst)) == len(inst)
+        # passes r < reps with r = h mod E: ceil((reps - h) / E) of them, or one
+        assert len(inst) == max(1, (reps - h + E - 1) // E), (reps, inst)
+    assert f"one pass of every {b.INST_EVERY}" in b.TIMING
+    for w in b.REPS_PER_STEP:
+        assert b.workload_config(w, 1)["timing"] == b.TIMING
