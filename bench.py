@@ -476,9 +476,8 @@ def _extra_ops(name, handle, dev):
         ops.append(("alex1_out_maxpool_3x3s2", (lambda: pool(xt, y)), 0,
                     xt.numel() * 2 + y.numel() * 2, pool.kernel(xt, y), "hbm", pool))
         ya = torch.empty_like(xt)
-        ops.append(("alex1_out_relu", (lambda: api.activation_forward(handle, xt, ya, mode="relu",
-                                                                      x_axes="NHWC", y_axes="NHWC")),
-                    0, xt.numel() * 4, "flat", "hbm", None))
+        relu = api.ActivationForward(handle, xt, ya, mode="relu", x_axes="NHWC", y_axes="NHWC")
+        ops.append(("alex1_out_relu", (lambda: relu(xt, ya)), 0, xt.numel() * 4, "flat", "hbm", relu))
     return ops
 
 

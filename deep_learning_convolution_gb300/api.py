@@ -292,22 +292,44 @@ class Pool2dForward:
             self.pool = None
 
 
+class ActivationForward:
+    """y = alpha * f(x) + beta * y through dlcActivationForward (y may be x),
+    with the tensor descriptors built once for repeated calls on the same
+    shapes and layouts."""
+
+    def __init__(self, handle: Handle, x, y, *, mode="relu", coef=0.0, x_axes="NCHW",
+                 y_axes="NCHW"):
+        self.handle = handle
+        self.mode = ACT_MODES[mode]
+        self.coef = float(coef)
+        self.x_desc = B.dlcCreateTensorDescriptor()
+        self.y_desc = B.dlcCreateTensorDescriptor()
+        xs, xst = _logical(x, x_axes, "NCHW")
+        B.dlcSetTensor4dDescriptorEx(self.x_desc, _dtype_code(x), *xs, *xst)
+        ys, yst = _logical(y, y_axes, "NCHW")
+        B.dlcSetTensor4dDescriptorEx(self.y_desc, _dtype_code(y), *ys, *yst)
+
+    def __call__(self, x, y, alpha: float = 1.0, beta: float = 0.0):
+        B.dlcActivationForward(self.handle.h, self.mode, self.coef, alpha, self.x_desc, x.data_ptr(),
+                               beta, self.y_desc, y.data_ptr())
+        return y
+
+    def close(self):
+        if self.x_desc is not None:
+            B.dlcDestroyTensorDescriptor(self.x_desc)
+            B.dlcDestroyTensorDescriptor(self.y_desc)
+            self.x_desc = None
+
+
 def activation_forward(handle: Handle, x, y, *, mode="relu", coef=0.0, alpha=1.0, beta=0.0,
                        x_axes="NCHW", y_axes="NCHW"):
-    """y = alpha * f(x) + beta * y through dlcActivationForward (y may be x)."""
-    xd = B.dlcCreateTensorDescriptor()
-    yd = B.dlcCreateTensorDescriptor()
+    """y = alpha * f(x) + beta * y through dlcActivationForward (y may be x):
+    one call of ActivationForward, its descriptors built and destroyed here."""
+    op = ActivationForward(handle, x, y, mode=mode, coef=coef, x_axes=x_axes, y_axes=y_axes)
     try:
-        xs, xst = _logical(x, x_axes, "NCHW")
-        B.dlcSetTensor4dDescriptorEx(xd, _dtype_code(x), *xs, *xst)
-        ys, yst = _logical(y, y_axes, "NCHW")
-        B.dlcSetTensor4dDescriptorEx(yd, _dtype_code(y), *ys, *yst)
-        B.dlcActivationForward(handle.h, ACT_MODES[mode], coef, alpha, xd, x.data_ptr(), beta, yd,
-                               y.data_ptr())
+        return op(x, y, alpha=alpha, beta=beta)
     finally:
-        B.dlcDestroyTensorDescriptor(xd)
-        B.dlcDestroyTensorDescriptor(yd)
-    return y
+        op.close()
 
 
 def output_dim(x, w, *, x_axes="NCHW", w_axes="KCRS", pads=(0, 0, 0, 0), stride=(1, 1),

@@ -198,3 +198,34 @@ def test_activation(mode, dt, shape, axes, ydt):
         got = z.permute(*[axes.index(a) for a in "NCHW"]).double().cpu().numpy()
         assert_within(got, ref, tol, f"activation {mode} in place")
     handle.close()
+
+
+def test_activation_op_reused():
+    """One ActivationForward object (descriptors built once) called repeatedly,
+    with different alpha / beta and different tensors of the same shape."""
+    import torch
+    from deep_learning_convolution_gb300 import api
+    _need_cuda()
+    rng = np.random.default_rng(960)
+    shape, axes = (2, 24, 9, 11), "NHWC"
+    handle = api.Handle()
+    x0 = _vals(rng.uniform(-3, 3, shape), "bf16")
+    op = api.ActivationForward(handle, _dev(x0, "bf16", axes), torch.empty((2, 9, 11, 24), device="cuda"),
+                               mode="clipped_relu", coef=1.5, x_axes=axes, y_axes=axes)
+    try:
+        for i, (alpha, beta) in enumerate(((1.0, 0.0), (-0.5, 2.0), (2.0, -1.0))):
+            x = _vals(rng.uniform(-3, 3, shape), "bf16")
+            xt = _dev(x, "bf16", axes)
+            old = _vals(rng.uniform(-1, 1, shape), "f32")
+            y = _dev(old, "f32", axes)
+            op(xt, y, alpha=alpha, beta=beta)
+            torch.cuda.synchronize()
+            handle.synchronize()
+            got = y.permute(*[axes.index(a) for a in "NCHW"]).double().cpu().numpy()
+            ref = oracle.activation_fprop(x, mode="clipped_relu", coef=1.5, alpha=alpha, beta=beta,
+                                          y_in=old if beta else None)
+            tol = 4e-7 * np.abs(ref) + 4e-7 + (4e-7 * np.abs(beta * old) if beta else 0.0)
+            assert_within(got, ref, tol, f"activation op call {i}")
+    finally:
+        op.close()
+        handle.close()
