@@ -14,9 +14,11 @@ steps lasts about a second and clock samplers see the GPU busy); L2 is
 flushed (256 MiB write) between steps, outside the timed events, and one pass
 over a stack touches more than the 129 MB L2 (except the tiny layer, which is
 latency-bound and makes no roofline claim beyond that).  A step is timed by
-CUDA events at its start and end; per-layer times (and the dominant kernel's
-roofline fraction) come from events after every launch of one pass in eight,
-so that the other passes run without events between their launches.
+CUDA events at its start and end.  Its passes go in blocks of eight: one pass
+launched directly with an event after every launch (the per-layer times and
+the dominant kernel's roofline fraction come from these), then a CUDA graph of
+the other seven passes, captured once before the timed region from the same
+library calls, replayed.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload overfeat|alexnet|resnet50|speech|tiny] [--no-configs]
@@ -139,20 +141,76 @@ def reps_for(workload, override=None):
 # the first drains (programmatic dependent launch); with one after every
 # launch the stacks ran 1-6 % slower.  The other passes run as a user's would.
 INST_EVERY = 8
-TIMING = (f"step: start and end CUDA events; layers: per-launch CUDA events in one pass "
-          f"of every {INST_EVERY}")
+TIMING_DIRECT = (f"step: start and end CUDA events; every pass launched directly, one in "
+                 f"{INST_EVERY} with a CUDA event after every launch (the per-layer times)")
+TIMING = (f"step: start and end CUDA events; of every {INST_EVERY} passes one is launched "
+          f"directly with a CUDA event after every launch (the per-layer times) and "
+          f"{INST_EVERY - 1} are replayed as one captured CUDA graph")
 
 
 def instrumented_passes(reps):
     return [r for r in range(reps) if r % INST_EVERY == INST_EVERY // 2] or [reps // 2]
 
 
-def time_steps(K, reps, launchers, flush, stream):
-    """Runs K steps of `reps` passes over `launchers` (one call per layer),
-    L2 flushed before each step outside its timed events.  Returns the summed
-    step time in ms (each step's start and end events), the per-launcher time
-    summed over the instrumented passes, and how many passes that was."""
+def capture_passes(launchers, stream, handle, n):
+    """A CUDA graph of `n` passes over `launchers` captured on `stream`, and
+    the library launches it holds (the handle's count over the capture); or
+    (None, 0) when the capture fails, and the steps launch every pass."""
     import torch
+    try:
+        g = torch.cuda.CUDAGraph()
+        l0 = handle.launches()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(n):
+                for launch in launchers:
+                    launch()
+        per = handle.launches() - l0
+        with torch.cuda.stream(stream):
+            g.replay()  # the first replay uploads the graph
+        torch.cuda.synchronize()
+        return g, per
+    except Exception:
+        torch.cuda.synchronize()
+        return None, 0
+
+
+def time_steps(K, reps, launchers, flush, stream, graph=None):
+    """Runs K steps of `reps` passes over `launchers` (one call per layer),
+    L2 flushed before each step outside its timed events.  With `graph` (a
+    capture of INST_EVERY - 1 passes; reps a multiple of INST_EVERY) each block
+    of INST_EVERY passes is one pass launched with an event after every launch,
+    then the graph; otherwise every pass is launched, one in INST_EVERY with
+    those events.  Returns the summed step time in ms (each step's start and
+    end events), the per-launcher time summed over the instrumented passes,
+    how many passes that was, and how many graph replays ran."""
+    import torch
+    if graph is not None and reps % INST_EVERY == 0:
+        blocks = reps // INST_EVERY
+        nl = len(launchers)
+        ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(K)]
+        ev_pass = [[[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1)]
+                    for _ in range(blocks)] for _ in range(K)]
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                flush.fill_(float(i))
+                ev_step[i][0].record(stream)
+                for b in range(blocks):
+                    ev = ev_pass[i][b]
+                    ev[0].record(stream)
+                    for j, launch in enumerate(launchers):
+                        launch()
+                        ev[j + 1].record(stream)
+                    graph.replay()
+                ev_step[i][1].record(stream)
+        torch.cuda.synchronize()
+        total_ms = sum(a.elapsed_time(b) for a, b in ev_step)
+        per = [0.0] * nl
+        for i in range(K):
+            for ev in ev_pass[i]:
+                for j in range(nl):
+                    per[j] += ev[j].elapsed_time(ev[j + 1])
+        return total_ms, per, K * blocks, K * blocks
     inst = instrumented_passes(reps)
     slot = {r: i for i, r in enumerate(inst)}
     nl = len(launchers)
@@ -179,7 +237,7 @@ def time_steps(K, reps, launchers, flush, stream):
         for ev in ev_pass[i]:
             for j in range(nl):
                 per[j] += ev[j].elapsed_time(ev[j + 1])
-    return total_ms, per, K * len(inst)
+    return total_ms, per, K * len(inst), 0
 
 
 def workload_config(workload, world, reps=None):
@@ -200,7 +258,7 @@ def workload_config(workload, world, reps=None):
             "output": "fp32", "l2": l2,
             "parallelism": f"replicas{world}" if world > 1 else "single_gpu",
             "reps_per_step": reps, "flops_per_pass": pass_flops,
-            "flops_per_step": pass_flops * reps, "timing": TIMING}
+            "flops_per_step": pass_flops * reps}
 
 
 # ---------------------------------------------------------------------------
@@ -330,6 +388,8 @@ def run_workload(args, workload, handle, stream, dev, rank, world, local_rank, h
     # step time from each step's start and end events on the launch stream;
     # per-layer times from per-launch events in one pass of every INST_EVERY
     launchers = [(lambda pr=pr: pr["conv"](pr["x"], pr["w"], pr["y"])) for pr in probs]
+    graph, per_graph = (capture_passes(launchers, stream, handle, INST_EVERY - 1)
+                        if reps % INST_EVERY == 0 else (None, 0))
     sampler = ClockSampler(local_rank)
     if world > 1:
         torch.distributed.barrier()
@@ -337,11 +397,12 @@ def run_workload(args, workload, handle, stream, dev, rank, world, local_rank, h
     launches0 = handle.launches()
     sampler.start()
     time.sleep(0.05)
-    total_ms, per_layer_ms, n_launch = time_steps(K, reps, launchers, flush, stream)
+    total_ms, per_layer_ms, n_launch, replays = time_steps(K, reps, launchers, flush, stream, graph)
     clocks = sampler.stop()
     if world > 1:
         torch.distributed.barrier()
-    launches = handle.launches() - launches0
+    # direct launches counted by the handle, plus the kernels of every replay
+    launches = handle.launches() - launches0 + replays * per_graph
     handle.synchronize()  # raises if a kernel recorded a device error
 
     total_ms, value = aggregate_over_ranks(total_ms, step_flops, K, world, dev)
@@ -405,6 +466,7 @@ def run_workload(args, workload, handle, stream, dev, rank, world, local_rank, h
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
         "data": "synthetic",
         "config": workload_config(workload, world, reps),
+        "timing": TIMING if graph is not None else TIMING_DIRECT,
         "roofline": roofline,
         "layers": layer_rows,
         "e2e": e2e,
@@ -424,7 +486,7 @@ def run_workload(args, workload, handle, stream, dev, rank, world, local_rank, h
 # Backward routines and the pooling/activation primitives, timed like the
 # forward workloads (steps of reps_per_step passes; per-launch CUDA events in
 # one pass of every INST_EVERY).
-EXTRA_REPS = {"overfeat_bwd_data": 40, "overfeat_bwd_filter": 24, "alexnet_pool_act": 300}
+EXTRA_REPS = {"overfeat_bwd_data": 40, "overfeat_bwd_filter": 24, "alexnet_pool_act": 304}
 
 
 def _bwd_layers():
@@ -496,14 +558,16 @@ def run_extra(args, name, handle, stream, dev, local_rank, world):
     K = args.steps
     nl = len(ops)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    graph, per_graph = (capture_passes([o[1] for o in ops], stream, handle, INST_EVERY - 1)
+                        if reps % INST_EVERY == 0 else (None, 0))
     sampler = ClockSampler(local_rank)
     torch.cuda.synchronize()
     launches0 = handle.launches()
     sampler.start()
     time.sleep(0.05)
-    total_ms, per_ms, n_launch = time_steps(K, reps, [o[1] for o in ops], flush, stream)
+    total_ms, per_ms, n_launch, replays = time_steps(K, reps, [o[1] for o in ops], flush, stream, graph)
     clocks = sampler.stop()
-    launches = handle.launches() - launches0
+    launches = handle.launches() - launches0 + replays * per_graph
     handle.synchronize()
     pass_flops = sum(o[2] for o in ops)
     pass_bytes = sum(o[3] for o in ops)
@@ -548,7 +612,8 @@ def run_extra(args, name, handle, stream, dev, local_rank, world):
     res = {"what": metric, "value": round(value, 2), "unit": unit, "steps": K,
            "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4), "dtype": "bf16",
            "config": {"workload": name, "layers": [o[0] for o in ops], "reps_per_step": reps,
-                      "l2": "flushed between steps (256 MiB write, untimed)", "timing": TIMING},
+                      "l2": "flushed between steps (256 MiB write, untimed)"},
+           "timing": TIMING if graph is not None else TIMING_DIRECT,
            "roofline": roofline, "layers": rows, "gpu_launches": launches, "clocks": clocks,
            "e2e": None}
     for o in ops:
@@ -570,7 +635,10 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    stream = torch.cuda.current_stream()
+    # a stream of its own (the legacy default stream cannot be captured in a
+    # CUDA graph), current for every torch operation of the run
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
     handle = api.Handle(stream)
     result = run_workload(args, args.workload, handle, stream, dev, rank, world, local_rank,
                           headline=True)
@@ -741,6 +809,7 @@ def run_reference(args, rank, world):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
             "config": workload_config(args.workload, world, args.reps_per_step),
+            "timing": "host wall clock (perf_counter) around each sampled layer",
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,

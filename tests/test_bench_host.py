@@ -119,7 +119,8 @@ def test_bench_geometry_matches_the_oracle_extent():
 def test_per_launch_events_ride_on_one_pass_in_eight():
     """Every step carries per-launch events on at least one pass, on one pass in
     INST_EVERY when the step has that many, and never past the step's end; the
-    timing description names the same rate."""
+    timing descriptions name the same rate; every workload's step is whole
+    blocks of INST_EVERY passes (one direct pass and one graph replay each)."""
     b = _bench()
     E, h = b.INST_EVERY, b.INST_EVERY // 2
     for reps in (1, 2, 7, 8, 9, 12, 13, 40, 80, 200, 2000):
@@ -129,6 +130,8 @@ def test_per_launch_events_ride_on_one_pass_in_eight():
         assert len(set(inst)) == len(inst)
         # passes r < reps with r = h mod E: ceil((reps - h) / E) of them, or one
         assert len(inst) == max(1, (reps - h + E - 1) // E), (reps, inst)
-    assert f"one pass of every {b.INST_EVERY}" in b.TIMING
-    for w in b.REPS_PER_STEP:
-        assert b.workload_config(w, 1)["timing"] == b.TIMING
+    assert f"of every {b.INST_EVERY} passes one" in b.TIMING
+    assert f"{b.INST_EVERY - 1} are replayed" in b.TIMING
+    assert f"one in {b.INST_EVERY}" in b.TIMING_DIRECT
+    for reps in list(b.REPS_PER_STEP.values()) + list(b.EXTRA_REPS.values()):
+        assert reps % b.INST_EVERY == 0, reps
