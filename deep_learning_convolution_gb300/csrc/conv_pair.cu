@@ -344,8 +344,15 @@ __device__ void pair_epilogue(const PairParams &p, uint32_t rank, uint32_t tmem_
         const bool valid = m < p.M;
         long long ybase = 0;
         if (valid) {
-            const int n = (int)(m / p.PQ);
-            const int rem = (int)(m - (long long)n * p.PQ);
+            int n, rem;
+            if (p.M <= 0x7fffffffLL) {  // a 32-bit division (the 64-bit one is a long call)
+                const uint32_t m32 = (uint32_t)m, pq = (uint32_t)p.PQ;
+                n = (int)(m32 / pq);
+                rem = (int)(m32 - (uint32_t)n * pq);
+            } else {
+                n = (int)(m / p.PQ);
+                rem = (int)(m - (long long)n * p.PQ);
+            }
             const int op = rem / p.Q, oq = rem - op * p.Q;
             ybase = (long long)n * p.ys[0] + (long long)op * p.ys[2] + (long long)oq * p.ys[3];
         }
@@ -401,7 +408,7 @@ __device__ void pair_epilogue(const PairParams &p, uint32_t rank, uint32_t tmem_
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(tempty0 + 8u * buf);  // release on the leader
+        if (lane == 0) mbar_arrive_tmem_free(tempty0 + 8u * buf);  // release on the leader
     }
     // staged stores must finish reading shared memory before the CTA exits
     if (p.y_tma && lane == 0) bulk_wait_group_read<0>();

@@ -284,7 +284,7 @@ __device__ void wg_epilogue(const WgParams &p, uint32_t rank, uint32_t tmem_base
         __syncwarp();
         if (lane == 0) {
             if (PAIR)
-                mbar_arrive_cluster(tempty0 + 8u * (uint32_t)buf);  // release on the leader
+                mbar_arrive_tmem_free(tempty0 + 8u * (uint32_t)buf);  // release on the leader
             else
                 mbar_arrive(&tempty[buf]);
         }

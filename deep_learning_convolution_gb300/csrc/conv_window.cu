@@ -901,7 +901,7 @@ __device__ void win_epilogue(const WinParams &p, uint32_t rank, uint32_t tmem_ba
         __syncwarp();
         if (lane == 0) {
             if (PAIR)
-                mbar_arrive_cluster(tempty_l + 8u * buf);  // released on the leader
+                mbar_arrive_tmem_free(tempty_l + 8u * buf);  // released on the leader
             else
                 mbar_arrive(&tempty[buf]);
         }

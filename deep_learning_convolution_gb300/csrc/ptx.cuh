@@ -492,6 +492,17 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
                  : "memory");
 }
 
+// Hands a TMEM accumulator back to the MMA thread of the leader CTA, after the
+// arriving thread's tcgen05.wait::ld and tcgen05.fence::before_thread_sync.
+// Nothing in generic memory passes from the epilogue to the MMA thread, so the
+// release is at CTA scope: a cluster-scope release waits until this thread's
+// earlier global writes are visible (about 1 us under an epilogue's stores),
+// and the MMAs of the next tile waited on that.
+__device__ __forceinline__ void mbar_arrive_tmem_free(uint32_t caddr) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(caddr)
+                 : "memory");
+}
+
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                      : "memory");
