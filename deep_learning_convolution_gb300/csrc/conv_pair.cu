@@ -333,12 +333,7 @@ __device__ void pair_epilogue(const PairParams &p, uint32_t rank, uint32_t tmem_
         const int t = w.tile;
         const int buf = it & 1;
         const uint32_t ph = (uint32_t)(it >> 1) & 1u;
-        int okw = 0;
-        if (lane == 0) okw = mbar_wait(&tfull[buf], ph, ctl, 5) ? 1 : 0;
-        okw = __shfl_sync(0xffffffffu, okw, 0);
-        if (!okw) break;
-        __syncwarp();
-        tc_fence_after_sync();
+        // the unit's output rows, worked out before its accumulator is ready
         const long long m = (long long)(t / p.n_tiles) * (2 * PBM) + (long long)rank * PBM + row;
         const int kt = (t % p.n_tiles) * p.BN;
         const bool valid = m < p.M;
@@ -356,6 +351,12 @@ __device__ void pair_epilogue(const PairParams &p, uint32_t rank, uint32_t tmem_
             const int op = rem / p.Q, oq = rem - op * p.Q;
             ybase = (long long)n * p.ys[0] + (long long)op * p.ys[2] + (long long)oq * p.ys[3];
         }
+        int okw = 0;
+        if (lane == 0) okw = mbar_wait(&tfull[buf], ph, ctl, 5) ? 1 : 0;
+        okw = __shfl_sync(0xffffffffu, okw, 0);
+        if (!okw) break;
+        __syncwarp();
+        tc_fence_after_sync();
         const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)buf * p.acc_stride;
         for (int c0 = 32 * part; c0 < p.BN && kt + c0 < p.K; c0 += 32 * p.epi_parts) {
             uint32_t v[32];
