@@ -17,6 +17,10 @@
 // output pixel.
 //
 // A work unit is (128 filters, BN channels, one tap, a range of pixel blocks).
+// A pair with at most 128 channels stacks two taps instead: each CTA loads all
+// channels of its own tap (2r and 2r + 1 of the unit's tap pair r), so one MMA
+// of N = 2 x 64 x ceil(C/64) serves both taps from one dy block, where one tap
+// per unit would pad N to 128 channels per tap and load dy once per tap.
 // The pixel reduction is split into ranges when the tiles alone cannot fill
 // the GPU; every unit adds alpha times its partial sum into dw with bulk
 // tensor reduce-adds (dw scaled by beta beforehand), so the split's partial
@@ -68,6 +72,7 @@ struct WgParams {
     int m_tiles, c_tiles, tiles;   // tiles = m_tiles * c_tiles * R * S
     int kblocks;                   // ceil(M / 64)
     int splits, units;             // pixel-block ranges per tile; units = tiles * splits
+    int stack;                     // pairs: each CTA's x block is a different tap (below)
     int dn, dp, dq;                // one pixel block (64 pixels) as images, rows, columns
     float alpha;
     uint32_t idesc, tmem_cols, acc_stride;
@@ -110,9 +115,12 @@ __device__ void wg_produce(const WgParams &p, uint32_t rank, const CUtensorMap *
     uint32_t ph = 0;
     for (int u = wg_first<PAIR>(); u < p.units; u += wg_step<PAIR>()) {
         const WgUnit w = wg_unit(p, u);
-        const int r = w.rs / p.S, s = w.rs - (w.rs / p.S) * p.S;
+        // stacked taps: this CTA's tap of the pair (the last tap again when
+        // R*S is odd; the epilogue drops its columns)
+        const int tap = p.stack ? min(2 * w.rs + (int)rank, p.R * p.S - 1) : w.rs;
+        const int r = tap / p.S, s = tap - (tap / p.S) * p.S;
         const int k0 = w.kt * (PAIR ? 2 * WG_BM : WG_BM) + (int)rank * WG_BM;
-        const int c0 = w.ct * p.BN + (int)rank * (p.b_atoms * 64);
+        const int c0 = p.stack ? 0 : w.ct * p.BN + (int)rank * (p.b_atoms * 64);
         // the first pixel of the unit's first block; later blocks step by 64
         // pixels without a division
         long long m0 = (long long)w.kb0 * WG_BP;
@@ -254,8 +262,16 @@ __device__ void wg_epilogue(const WgParams &p, uint32_t rank, uint32_t tmem_base
         tc_fence_after_sync();
         const int krow = w.kt * (PAIR ? 2 * WG_BM : WG_BM) + (int)rank * WG_BM + quad * 32;
         const int c0 = w.ct * p.BN;
+        const int half = p.b_atoms * 64;  // accumulator columns from each CTA's x block
         const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)buf * p.acc_stride;
-        for (int cc = 0; cc < p.BN && c0 + cc < p.C; cc += 32) {
+        for (int cc = 0; cc < p.BN && (p.stack || c0 + cc < p.C); cc += 32) {
+            int ch = c0 + cc, tap = w.rs;
+            if (p.stack) {  // columns [0, half) are tap 2*rs, [half, BN) tap 2*rs + 1
+                const int h = cc >= half ? 1 : 0;
+                ch = cc - h * half;
+                tap = 2 * w.rs + h;
+                if (ch >= p.C || tap >= p.R * p.S) continue;  // warp-uniform
+            }
             uint32_t v[32];
             tmem_ld_32x32b_x32(taddr + (uint32_t)cc, v);
             tmem_ld_wait();
@@ -275,7 +291,7 @@ __device__ void wg_epilogue(const WgParams &p, uint32_t rank, uint32_t tmem_base
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {  // channels past C and filters past K are not written
-                tma_reduce_add_3d_s(tmD, sb, c0 + cc, w.rs, krow);
+                tma_reduce_add_3d_s(tmD, sb, ch, tap, krow);
                 bulk_commit_group();
             }
             ++nbuf;
@@ -442,6 +458,17 @@ dlcStatus_t dlc_launch_wgrad_tc(dlcContext *ctx, const BwdProblem &bp) {
     p.m_tiles = (bp.K + (pair ? 2 : 1) * WG_BM - 1) / ((pair ? 2 : 1) * WG_BM);
     p.c_tiles = (bp.C + p.BN - 1) / p.BN;
     p.tiles = p.m_tiles * p.c_tiles * bp.R * bp.S;
+    // a pair with at most 128 channels stacks two taps (DLC_TC_WGRAD_STACK=0: one tap a unit)
+    p.stack = pair && bp.C <= 128 && bp.R * bp.S >= 2 && [] {
+        const char *ev = std::getenv("DLC_TC_WGRAD_STACK");
+        return !(ev && std::atoi(ev) == 0);
+    }();
+    if (p.stack) {
+        p.b_atoms = (bp.C + 63) / 64;
+        p.BN = 2 * 64 * p.b_atoms;
+        p.c_tiles = 1;
+        p.tiles = p.m_tiles * ((bp.R * bp.S + 1) / 2);
+    }
     p.kblocks = (int)((p.M + WG_BP - 1) / WG_BP);
     // split the pixel reduction where it shortens the busiest CTA (or pair):
     // s ranges of each tile make rounds(s) = ceil(tiles * s / workers) rounds of

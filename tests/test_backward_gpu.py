@@ -351,6 +351,32 @@ def test_wgrad_tensor_cores(layer, pair, monkeypatch):
     run_wgrad(layer, 735, alpha=-0.5, beta=2.0, expect="tc_wgrad", deterministic=True)
 
 
+# Pairs with at most 128 channels stack two filter taps per unit (one per CTA
+# of the pair): odd and even tap counts (the odd one's last unit has a single
+# tap), one or two 64-channel blocks, channels short of a block, stride and
+# dilation.
+WGRAD_STACK = [
+    L("wg_stack_c96_k256_5x5", 2, 96, 12, 12, 256, 5, 5, pad_top=2, pad_bottom=2, pad_left=2,
+      pad_right=2),
+    L("wg_stack_c64_k192_3x3", 3, 64, 11, 9, 192, 3, 3, **P1),
+    L("wg_stack_c128_k160_2x3_s2", 2, 128, 13, 15, 160, 2, 3, pad_top=1, pad_bottom=0,
+      pad_left=1, pad_right=1, u=2, v=2),
+    L("wg_stack_c72_k136_3x3_d2", 2, 72, 14, 13, 136, 3, 3, pad_top=2, pad_bottom=2, pad_left=1,
+      pad_right=2, dil_h=2, dil_w=2),
+]
+
+
+@pytest.mark.parametrize("stack", ["1", "0"], ids=["stacked_taps", "one_tap"])
+@pytest.mark.parametrize("layer", WGRAD_STACK, ids=lambda l: l.name)
+def test_wgrad_stacked_taps(layer, stack, monkeypatch):
+    """SM pairs with two taps a unit (the default at <= 128 channels) and with
+    one tap a unit (DLC_TC_WGRAD_STACK=0) both agree with the oracle, split
+    and deterministic, with alpha and beta."""
+    monkeypatch.setenv("DLC_TC_WGRAD_STACK", stack)
+    run_wgrad(layer, 736, expect="tc_wgrad")
+    run_wgrad(layer, 737, alpha=-0.5, beta=2.0, expect="tc_wgrad", deterministic=True)
+
+
 def test_wgrad_bf16_output_and_determinism():
     import torch
     layer = WGRAD[0]
