@@ -259,6 +259,16 @@ def test_dgrad_tensor_cores(layer):
     run_dgrad(layer, 700, expect="tc_im2col_pair")
 
 
+@pytest.mark.parametrize("loaders", ["0", "1", "2"], ids=["one_thread", "a_b_split", "alternate"])
+@pytest.mark.parametrize("layer", [DGRAD_TC[i] for i in (1, 3, 6)], ids=lambda l: l.name)
+def test_dgrad_load_issue(layer, loaders, monkeypatch):
+    """The data gradient with the SM-pair kernel's loads issued by one thread,
+    by two (A and B) and by two taking alternate k-blocks (the default for its
+    MN-major filters)."""
+    monkeypatch.setenv("DLC_TC_PAIR_SPLITLOAD", loaders)
+    run_dgrad(layer, 705, expect="tc_im2col_pair")
+
+
 def test_dgrad_alpha_beta_and_bf16_output():
     import torch
     layer = DGRAD_TC[1]

@@ -139,6 +139,16 @@ def test_tc_im2col_pair_split_tail(handle, layer, split, monkeypatch):
                   expect_kernel="tc_im2col_pair")
 
 
+@pytest.mark.parametrize("loaders", ["0", "1", "2"], ids=["one_thread", "a_b_split", "alternate"])
+@pytest.mark.parametrize("layer", [PAIR_CASES[i] for i in (0, 3, 9)], ids=lambda l: l.name)
+def test_tc_im2col_pair_load_issue(handle, layer, loaders, monkeypatch):
+    """The SM-pair kernel's loads issued by one thread, by two (A and B), or by
+    two taking alternate k-blocks (DLC_TC_PAIR_SPLITLOAD=0/1/2): the same y."""
+    monkeypatch.setenv("DLC_TC_PAIR_SPLITLOAD", loaders)
+    run_and_check(handle, layer, 1190 + PAIR_CASES.index(layer), full=True, beta=0.5,
+                  expect_kernel="tc_im2col_pair")
+
+
 # channel counts whose last 64-channel block holds at most 32 channels: that
 # block comes in 64-byte rows (32-channel boxes, two MMAs) unless
 # DLC_TC_PAIR_MIXED=0
