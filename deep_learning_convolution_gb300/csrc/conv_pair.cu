@@ -59,6 +59,7 @@ struct PairParams {
     int y_tma;         // y through 2-D bulk tensor stores of 32 x 32 blocks
     int BN;            // filters per pair tile (BN/2 per CTA)
     int stages, num_kb, c_blocks, n_tiles;
+    int kps;           // k-blocks per stage (1 or 2): one full wait and one commit per stage
     // B operand: K-major rows of BN/2 filters (b_mn = 0), or MN-major (b_mn =
     // 1): b_atoms boxes of 128 bytes of filters x BK reduction rows each.
     int b_mn, b_atoms, flip;
@@ -113,7 +114,7 @@ __device__ __forceinline__ bool pair_drain(uint64_t *bar, uint32_t parity, const
 // MIXED: the last channel block of a tap holds at most 32 channels and comes
 // in 64-byte rows (tmA2 / tmB2: 32-channel boxes, 64-byte swizzle) -- half the
 // bytes of a full block, for half its MMAs.
-template <int BK, int PART, bool MIXED>
+template <int BK, int PART, bool MIXED, int KPS>
 __device__ void pair_produce(const PairParams &p, uint32_t rank, const CUtensorMap *tmA,
                              const CUtensorMap *tmB, const CUtensorMap *tmA2, const CUtensorMap *tmB2,
                              uint32_t sA, uint32_t sB, uint64_t *full, uint64_t *empty, const WaitCtl &ctl) {
@@ -123,9 +124,10 @@ __device__ void pair_produce(const PairParams &p, uint32_t rank, const CUtensorM
     const uint32_t tx_h = tx / 2u;                 // a block of 64-byte rows
     const uint32_t atom_bytes = (uint32_t)BK * PROW;  // MN-major: BK rows of 128 bytes
     const uint32_t full0 = mapa_shared(smem_u32(full), 0);  // the leader's full barriers
+    const uint32_t a_stage = (uint32_t)KPS * PA_BYTES, b_stage = (uint32_t)KPS * b_half;
     int stage = 0;
     uint32_t ph = 0;
-    int kc = 0;  // k-blocks so far (PART 3 / 4 issue the even / odd ones)
+    int gc = 0;  // stages so far (PART 3 / 4 fill the even / odd ones)
     for (int u = (int)cluster_id_x(); u < p.num_units; u += (int)num_clusters_x()) {
         const PairUnit w = pair_unit(p, u);
         const int t = w.tile;
@@ -139,35 +141,46 @@ __device__ void pair_produce(const PairParams &p, uint32_t rank, const CUtensorM
         int cb = w.kb0 % p.c_blocks;
         const int rs0 = w.kb0 / p.c_blocks;
         int s = rs0 % p.S, r = rs0 / p.S;
-        for (int kb = w.kb0; kb < w.kb1; ++kb, ++kc) {
-            if (PART >= 3 && (kc & 1) != PART - 3) {  // the other thread's k-block
-                if (++stage == ST) stage = 0, ph ^= 1u;
-                if (++cb == p.c_blocks) {
-                    cb = 0;
-                    if (++s == p.S) s = 0, ++r;
+        int sub = 0;  // k-block `sub` of its stage (KPS = 2: a unit's last stage may hold one)
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+            const bool last = KPS == 1 || sub == 1 || kb + 1 == w.kb1;  // the stage's last k-block
+            if (PART < 3 || (gc & 1) == PART - 3) {  // (PART 3 / 4: this thread's stage)
+                if (sub == 0) {
+                    if (!mbar_wait(&empty[stage], ph ^ 1u, ctl, 1)) return;
+                    if (PART != 2 && rank == 0) {  // the stage's bytes, both CTAs
+                        uint32_t gtx = (MIXED && cb == p.c_blocks - 1) ? tx_h : tx;
+                        if (!last) {
+                            const int c2 = cb + 1 == p.c_blocks ? 0 : cb + 1;
+                            gtx += (MIXED && c2 == p.c_blocks - 1) ? tx_h : tx;
+                        }
+                        mbar_arrive_expect_tx(&full[stage], gtx);
+                    }
                 }
-                continue;
+                const bool half = MIXED && cb == p.c_blocks - 1;
+                const uint32_t a_dst = sA + (uint32_t)stage * a_stage + (uint32_t)sub * PA_BYTES;
+                const uint32_t b_dst = sB + (uint32_t)stage * b_stage + (uint32_t)sub * b_half;
+                if (PART != 2)
+                    tma_load_im2col_4d_pair(a_dst, half ? tmA2 : tmA, full0 + 8u * stage, cb * BK, wc, hc, n0,
+                                            (uint16_t)(s * p.dw), (uint16_t)(r * p.dh));
+                const int sc = p.flip ? p.S - 1 - s : s, rc = p.flip ? p.R - 1 - r : r;
+                if (PART == 1) {
+                } else if (MIXED) {
+                    tma_load_4d_pair(b_dst, half ? tmB2 : tmB, full0 + 8u * stage, cb * BK, sc, rc, k0);
+                } else if (p.b_mn) {
+                    for (int a = 0; a < p.b_atoms; ++a)
+                        tma_load_4d_pair(b_dst + (uint32_t)a * atom_bytes, tmB, full0 + 8u * stage, k0 + a * BK,
+                                         sc, rc, cb * BK);
+                } else {
+                    tma_load_4d_pair(b_dst, tmB, full0 + 8u * stage, cb * BK, sc, rc, k0);
+                }
             }
-            if (!mbar_wait(&empty[stage], ph ^ 1u, ctl, 1)) return;
-            const bool half = MIXED && cb == p.c_blocks - 1;
-            if (PART != 2) {
-                if (rank == 0) mbar_arrive_expect_tx(&full[stage], half ? tx_h : tx);
-                tma_load_im2col_4d_pair(sA + (uint32_t)stage * PA_BYTES, half ? tmA2 : tmA, full0 + 8u * stage,
-                                        cb * BK, wc, hc, n0, (uint16_t)(s * p.dw), (uint16_t)(r * p.dh));
-            }
-            const int sc = p.flip ? p.S - 1 - s : s, rc = p.flip ? p.R - 1 - r : r;
-            if (PART == 1) {
-            } else if (MIXED) {
-                tma_load_4d_pair(sB + (uint32_t)stage * b_half, half ? tmB2 : tmB, full0 + 8u * stage, cb * BK,
-                                 sc, rc, k0);
-            } else if (p.b_mn) {
-                for (int a = 0; a < p.b_atoms; ++a)
-                    tma_load_4d_pair(sB + (uint32_t)stage * b_half + (uint32_t)a * atom_bytes, tmB,
-                                     full0 + 8u * stage, k0 + a * BK, sc, rc, cb * BK);
+            if (last) {
+                if (++stage == ST) stage = 0, ph ^= 1u;
+                ++gc;
+                sub = 0;
             } else {
-                tma_load_4d_pair(sB + (uint32_t)stage * b_half, tmB, full0 + 8u * stage, cb * BK, sc, rc, k0);
+                sub = 1;
             }
-            if (++stage == ST) stage = 0, ph ^= 1u;
             if (++cb == p.c_blocks) {
                 cb = 0;
                 if (++s == p.S) s = 0, ++r;
@@ -176,7 +189,7 @@ __device__ void pair_produce(const PairParams &p, uint32_t rank, const CUtensorM
     }
 }
 
-template <bool TF32, bool MIXED>
+template <bool TF32, bool MIXED, int KPS>
 __device__ void pair_mma(const PairParams &p, uint32_t tmem_base, uint32_t sA, uint32_t sB,
                          uint64_t *full, uint64_t *empty, uint64_t *tfull, uint64_t *tempty,
                          uint64_t *mma_done, const WaitCtl &ctl) {
@@ -189,7 +202,8 @@ __device__ void pair_mma(const PairParams &p, uint32_t tmem_base, uint32_t sA, u
     // of filters BK rows apart; one MMA's 32 bytes of K are 32/E rows.
     const uint64_t b0 = p.b_mn ? sw128_mnmajor_desc(sB, (uint32_t)BK * PROW) : sw128_kmajor_desc(sB);
     const uint32_t b_k = p.b_mn ? (32u / E) * PROW / 16u : 2u;
-    const uint64_t a_step = PA_BYTES >> 4, b_step = b_half >> 4;
+    const uint64_t a_sub = PA_BYTES >> 4, b_sub = b_half >> 4;        // next k-block of a stage
+    const uint64_t a_step = a_sub * KPS, b_step = b_sub * KPS;        // next stage
     // a block of 64-byte rows: the same start address, the 64-byte swizzle's
     // stride and layout bits (the XOR of the two descriptors of one address)
     const uint64_t to64 = sw64_kmajor_desc(sA) ^ sw128_kmajor_desc(sA);
@@ -209,23 +223,28 @@ __device__ void pair_mma(const PairParams &p, uint32_t tmem_base, uint32_t sA, u
         uint64_t ad = a0 + a_step * stage, bd = b0 + b_step * stage;
         uint32_t acc = 0;
         int cb = MIXED ? w.kb0 % p.c_blocks : 0;
+        int sub = 0;  // k-block `sub` of its stage
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
-            if (!mbar_wait(&full[stage], ph, ctl, 4)) {
-                ok = false;
-                break;
+            if (sub == 0) {
+                if (!mbar_wait(&full[stage], ph, ctl, 4)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
             }
-            tc_fence_after_sync();
+            const uint64_t as = KPS == 1 ? ad : ad + a_sub * (uint32_t)sub;
+            const uint64_t bs = KPS == 1 ? bd : bd + b_sub * (uint32_t)sub;
             if constexpr (MIXED && !TF32) {
                 if (cb == p.c_blocks - 1) {  // 32 channels in 64-byte rows: two MMAs
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
-                        umma_bf16_pair(d, (ad ^ to64) + 2u * j, (bd ^ to64) + 2u * j, p.idesc, acc);
+                        umma_bf16_pair(d, (as ^ to64) + 2u * j, (bs ^ to64) + 2u * j, p.idesc, acc);
                         acc = 1;
                     }
                 } else {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        umma_bf16_pair(d, ad + 2u * j, bd + 2u * j, p.idesc, acc);
+                        umma_bf16_pair(d, as + 2u * j, bs + 2u * j, p.idesc, acc);
                         acc = 1;
                     }
                 }
@@ -234,12 +253,17 @@ __device__ void pair_mma(const PairParams &p, uint32_t tmem_base, uint32_t sA, u
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {  // 32 bytes of the 128-byte row each
                     if constexpr (TF32)
-                        umma_tf32_pair(d, ad + 2u * j, bd + b_k * j, p.idesc, acc);
+                        umma_tf32_pair(d, as + 2u * j, bs + b_k * j, p.idesc, acc);
                     else
-                        umma_bf16_pair(d, ad + 2u * j, bd + b_k * j, p.idesc, acc);
+                        umma_bf16_pair(d, as + 2u * j, bs + b_k * j, p.idesc, acc);
                     acc = 1;
                 }
             }
+            if (KPS == 2 && sub == 0 && kb + 1 < w.kb1) {  // the stage's other k-block follows
+                sub = 1;
+                continue;
+            }
+            sub = 0;
             umma_commit_pair(&empty[stage], 3);  // both CTAs' slots free once these are done
             if (++stage == ST) {
                 stage = 0;
@@ -429,7 +453,7 @@ __device__ void pair_epilogue(const PairParams &p, uint32_t rank, uint32_t tmem_
     __syncwarp();
 }
 
-template <bool TF32, bool MIXED>
+template <bool TF32, bool MIXED, int KPS>
 __global__ void __launch_bounds__(PAIR_MAX_THREADS, 1)
     conv_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmY,
@@ -442,8 +466,8 @@ __global__ void __launch_bounds__(PAIR_MAX_THREADS, 1)
     const int ST = p.stages;
     const uint32_t b_half = p.b_stage;
     uint8_t *smA = smem;
-    uint8_t *smB = smA + (size_t)ST * PA_BYTES;
-    uint8_t *epi = smB + (size_t)ST * b_half;  // y staging (y_tma), 1024-aligned
+    uint8_t *smB = smA + (size_t)ST * KPS * PA_BYTES;
+    uint8_t *epi = smB + (size_t)ST * KPS * b_half;  // y staging (y_tma), 1024-aligned
     uint64_t *bars = reinterpret_cast<uint64_t *>(epi + (p.y_tma ? p.epi_parts * PAIR_EPI_SMEM : 0));
     uint64_t *full = bars;
     uint64_t *empty = bars + ST;
@@ -492,19 +516,19 @@ __global__ void __launch_bounds__(PAIR_MAX_THREADS, 1)
     if (warp == 0) {
         if (lane == 0) {
             if (p.split_load == 2)
-                pair_produce<BK, 3, MIXED>(p, rank, &tmA, &tmB, &tmA2, &tmB2, sA, sB, full, empty, ctl);
+                pair_produce<BK, 3, MIXED, KPS>(p, rank, &tmA, &tmB, &tmA2, &tmB2, sA, sB, full, empty, ctl);
             else if (p.split_load)
-                pair_produce<BK, 1, MIXED>(p, rank, &tmA, &tmB, &tmA2, &tmB2, sA, sB, full, empty, ctl);
+                pair_produce<BK, 1, MIXED, KPS>(p, rank, &tmA, &tmB, &tmA2, &tmB2, sA, sB, full, empty, ctl);
             else
-                pair_produce<BK, 0, MIXED>(p, rank, &tmA, &tmB, &tmA2, &tmB2, sA, sB, full, empty, ctl);
+                pair_produce<BK, 0, MIXED, KPS>(p, rank, &tmA, &tmB, &tmA2, &tmB2, sA, sB, full, empty, ctl);
         }
     } else if (warp == 2) {
         if (lane == 0 && p.split_load == 2)
-            pair_produce<BK, 4, MIXED>(p, rank, &tmA, &tmB, &tmA2, &tmB2, sA, sB, full, empty, ctl);
+            pair_produce<BK, 4, MIXED, KPS>(p, rank, &tmA, &tmB, &tmA2, &tmB2, sA, sB, full, empty, ctl);
         else if (lane == 0 && p.split_load)
-            pair_produce<BK, 2, MIXED>(p, rank, &tmA, &tmB, &tmA2, &tmB2, sA, sB, full, empty, ctl);
+            pair_produce<BK, 2, MIXED, KPS>(p, rank, &tmA, &tmB, &tmA2, &tmB2, sA, sB, full, empty, ctl);
     } else if (warp == 1) {
-        if (lane == 0 && rank == 0) pair_mma<TF32, MIXED>(p, tmem_base, sA, sB, full, empty, tfull, tempty, mma_done, ctl);
+        if (lane == 0 && rank == 0) pair_mma<TF32, MIXED, KPS>(p, tmem_base, sA, sB, full, empty, tfull, tempty, mma_done, ctl);
         // the leader's final commit reaches both CTAs; it also covers every
         // stage the MMAs consumed, i.e. every load of either CTA
         if (lane == 0) pair_drain(mma_done, 0u, p);
@@ -541,9 +565,12 @@ bool dlc_pair_enabled(const dlcContext *) {
 
 dlcStatus_t dlc_preload_pair() {
     cudaFuncAttributes a;
-    if (cudaFuncGetAttributes(&a, conv_pair_kernel<false, false>) != cudaSuccess ||
-        cudaFuncGetAttributes(&a, conv_pair_kernel<false, true>) != cudaSuccess ||
-        cudaFuncGetAttributes(&a, conv_pair_kernel<true, false>) != cudaSuccess)
+    if (cudaFuncGetAttributes(&a, conv_pair_kernel<false, false, 1>) != cudaSuccess ||
+        cudaFuncGetAttributes(&a, conv_pair_kernel<false, true, 1>) != cudaSuccess ||
+        cudaFuncGetAttributes(&a, conv_pair_kernel<true, false, 1>) != cudaSuccess ||
+        cudaFuncGetAttributes(&a, conv_pair_kernel<false, false, 2>) != cudaSuccess ||
+        cudaFuncGetAttributes(&a, conv_pair_kernel<false, true, 2>) != cudaSuccess ||
+        cudaFuncGetAttributes(&a, conv_pair_kernel<true, false, 2>) != cudaSuccess)
         return DLC_STATUS_EXECUTION_FAILED;
     return DLC_STATUS_SUCCESS;
 }
@@ -619,11 +646,21 @@ dlcStatus_t dlc_launch_pair(dlcContext *ctx, const ConvProblem &pb) {
         if (e == 4 || e == 8) p.epi_parts = e / 4;
     }
     const int epi_bytes = p.y_tma ? p.epi_parts * PAIR_EPI_SMEM : 0;
-    const int stage_bytes = PA_BYTES + (int)p.b_stage;
     // slack after the barriers: one more half filter tile, so that no operand
     // read of the last stage can leave the CTA's shared memory
     const int slack = (int)p.b_stage;
-    int st = (PAIR_MAX_SMEM - 1024 - PAIR_BAR_AREA - slack - epi_bytes) / stage_bytes;
+    const int room = PAIR_MAX_SMEM - 1024 - PAIR_BAR_AREA - slack - epi_bytes;
+    // one k-block a stage; DLC_TC_PAIR_KPS=2 puts two in each (one full wait
+    // and one commit for eight MMAs, half the stages): measured within noise of
+    // one on the bench's layers (4-5 % faster on the 64- and 96-channel-output
+    // ones, 1-3 % slower on others), so not the default
+    p.kps = 1;
+    if (const char *ev = std::getenv("DLC_TC_PAIR_KPS")) {
+        const int k = std::atoi(ev);
+        if (k == 1 || (k == 2 && room / (2 * (PA_BYTES + (int)p.b_stage)) >= 2)) p.kps = k;
+    }
+    const int stage_bytes = p.kps * (PA_BYTES + (int)p.b_stage);
+    int st = room / stage_bytes;
     p.stages = st > 8 ? 8 : st;
     if (const char *ev = std::getenv("DLC_TC_STAGES")) {
         const int s2 = std::atoi(ev);
@@ -701,8 +738,10 @@ dlcStatus_t dlc_launch_pair(dlcContext *ctx, const ConvProblem &pb) {
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return DLC_STATUS_EXECUTION_FAILED;
     }
-    auto kern = tf32 ? conv_pair_kernel<true, false>
-                     : (mixed ? conv_pair_kernel<false, true> : conv_pair_kernel<false, false>);
+    auto kern = p.kps == 2 ? (tf32 ? conv_pair_kernel<true, false, 2>
+                                   : (mixed ? conv_pair_kernel<false, true, 2> : conv_pair_kernel<false, false, 2>))
+                           : (tf32 ? conv_pair_kernel<true, false, 1>
+                                   : (mixed ? conv_pair_kernel<false, true, 1> : conv_pair_kernel<false, false, 1>));
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return DLC_STATUS_EXECUTION_FAILED;
     cudaLaunchConfig_t cfg;

@@ -269,6 +269,13 @@ def test_dgrad_load_issue(layer, loaders, monkeypatch):
     run_dgrad(layer, 705, expect="tc_im2col_pair")
 
 
+@pytest.mark.parametrize("layer", [DGRAD_TC[i] for i in (1, 2, 6)], ids=lambda l: l.name)
+def test_dgrad_two_kblocks_a_stage(layer, monkeypatch):
+    """The data gradient with two k-blocks per pipeline stage (DLC_TC_PAIR_KPS=2)."""
+    monkeypatch.setenv("DLC_TC_PAIR_KPS", "2")
+    run_dgrad(layer, 707, expect="tc_im2col_pair")
+
+
 def test_dgrad_alpha_beta_and_bf16_output():
     import torch
     layer = DGRAD_TC[1]

@@ -149,6 +149,18 @@ def test_tc_im2col_pair_load_issue(handle, layer, loaders, monkeypatch):
                   expect_kernel="tc_im2col_pair")
 
 
+@pytest.mark.parametrize("kps", ["2"], ids=["two_kblocks_a_stage"])
+@pytest.mark.parametrize("layer", [PAIR_CASES[i] for i in (0, 1, 3, 7, 9, 10)],
+                         ids=lambda l: l.name)
+def test_tc_im2col_pair_two_kblocks_a_stage(handle, layer, kps, monkeypatch):
+    """Two k-blocks per pipeline stage (DLC_TC_PAIR_KPS=2), split tail and whole
+    tiles alike, with a unit's odd last k-block alone in its stage (the 96-channel
+    case: a full and a 64-byte-row block per tap)."""
+    monkeypatch.setenv("DLC_TC_PAIR_KPS", kps)
+    run_and_check(handle, layer, 1210 + PAIR_CASES.index(layer), full=True, beta=0.5,
+                  with_bias=True, expect_kernel="tc_im2col_pair")
+
+
 # channel counts whose last 64-channel block holds at most 32 channels: that
 # block comes in 64-byte rows (32-channel boxes, two MMAs) unless
 # DLC_TC_PAIR_MIXED=0
