@@ -107,10 +107,11 @@ __device__ __forceinline__ bool pair_drain(uint64_t *bar, uint32_t parity, const
 
 // PART 0: this thread issues both operands' loads; 1: A (and arms the
 // barrier), 2: B only -- two threads of different warps share a stage's loads;
-// 3 and 4: both operands of the even / odd k-blocks (counted over all of the
+// 3 and 4: both operands of the even / odd stages (counted over all of the
 // CTA's units) -- two threads take turns, each stepping through every k-block
-// to keep the ring's stage and phase.  One thread's wait, arm and issue take
-// about as long as a small-BN k-block's MMAs.
+// to keep the ring's stage and phase (used with MN-major filters, whose B
+// takes one load per 64-filter block).  KPS k-blocks share a stage: its one
+// full barrier, armed once for all their bytes, and its one commit.
 // MIXED: the last channel block of a tap holds at most 32 channels and comes
 // in 64-byte rows (tmA2 / tmB2: 32-channel boxes, 64-byte swizzle) -- half the
 // bytes of a full block, for half its MMAs.
