@@ -13,13 +13,15 @@
 // that traffic at BN = 192..256.
 //
 // Roles (per CTA, 7 or 11 warps): warp 0 lane 0 issues the A (im2col) loads
-// and arms the stage's barrier, warp 2 lane 0 the B (filter) loads -- both
-// CTAs' loads complete on the LEADER's (rank 0) full barrier; warp 1 lane 0 of
+// and arms the stage's barrier, warp 2 lane 0 the B (filter) loads (with
+// MN-major filters the two take alternate stages, each issuing both operands)
+// -- both CTAs' loads complete on the LEADER's (rank 0) full barrier; warp 1 lane 0 of
 // the leader alone issues the MMAs and commits each stage back to the empty
 // barriers of both CTAs (multicast); warps 3-6 (or 3-10 for tiles of at most
 // four k-blocks, two warps per TMEM lane quarter) of each CTA read their CTA's
 // 128 accumulator rows from tensor memory, apply the epilogue and store y,
-// then release the accumulator on the leader's barrier.  Every wait is
+// then release the accumulator on the leader's barrier (a CTA-scope release:
+// no generic memory passes to the MMA thread).  Every wait is
 // bounded; both CTAs meet at a cluster barrier before tensor memory is
 // released.
 #include <cuda_bf16.h>
