@@ -28,6 +28,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <type_traits>
 
 #include "internal.h"
 
@@ -59,6 +60,7 @@ struct PoolParams {
     int N, C, H, W, R, S, P, Q;
     int pt, pl, u, v, mode;
     int y_vec;  // channels-innermost y whose 16-byte channel chunks are aligned
+    int raw_max;  // BF16 max pooling into BF16 y, alpha 1, beta 0: maxima stored as they are
     long long xs[4], ys[4];
     const void *x;
     void *y;
@@ -132,33 +134,42 @@ __device__ __forceinline__ void store_vec(TO *dst, const A (&v)[V]) {
 // fmaxf passes over a NaN operand) and widens only the result: it is one of
 // the stored values either way.  Sums are taken in A.  Returns the number of
 // in-image taps.
+// The BF16 maximum of a window: four pairs of stored values (from -inf when
+// no tap is in the image); returns the number of in-image taps.
+template <int FIX, typename F>
+__device__ __forceinline__ int bf16_max_window(const F &fetch, int R, int S, __nv_bfloat162 (&m)[4]) {
+    int count = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) m[k] = __bfloat162bfloat162(__ushort_as_bfloat16((unsigned short)0xff80u));
+    auto take = [&](const uint4 &q) {
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m[k] = __hmax2(m[k], *reinterpret_cast<const __nv_bfloat162 *>(&w[k]));
+    };
+    if constexpr (FIX > 0) {
+        uint4 q[FIX * FIX];
+        bool in[FIX * FIX];
+#pragma unroll
+        for (int t = 0; t < FIX * FIX; ++t) in[t] = fetch(t / FIX, t % FIX, q[t]);
+#pragma unroll
+        for (int t = 0; t < FIX * FIX; ++t)
+            if (in[t]) take(q[t]), ++count;
+    } else {
+        for (int i = 0; i < R; ++i)
+            for (int j = 0; j < S; ++j) {
+                uint4 q;
+                if (fetch(i, j, q)) take(q), ++count;
+            }
+    }
+    return count;
+}
+
 template <typename TI, typename A, int V, bool MAX, int FIX, typename F>
 __device__ __forceinline__ int pool_window(const F &fetch, int R, int S, A (&acc)[V]) {
     int count = 0;
     if constexpr (MAX && sizeof(TI) == 2) {
         __nv_bfloat162 m[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) m[k] = __bfloat162bfloat162(__ushort_as_bfloat16((unsigned short)0xff80u));
-        auto take = [&](const uint4 &q) {
-            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) m[k] = __hmax2(m[k], *reinterpret_cast<const __nv_bfloat162 *>(&w[k]));
-        };
-        if constexpr (FIX > 0) {
-            uint4 q[FIX * FIX];
-            bool in[FIX * FIX];
-#pragma unroll
-            for (int t = 0; t < FIX * FIX; ++t) in[t] = fetch(t / FIX, t % FIX, q[t]);
-#pragma unroll
-            for (int t = 0; t < FIX * FIX; ++t)
-                if (in[t]) take(q[t]), ++count;
-        } else {
-            for (int i = 0; i < R; ++i)
-                for (int j = 0; j < S; ++j) {
-                    uint4 q;
-                    if (fetch(i, j, q)) take(q), ++count;
-                }
-        }
+        count = bf16_max_window<FIX>(fetch, R, S, m);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             acc[2 * k] = __bfloat162float(m[k].x);
@@ -228,6 +239,16 @@ __global__ void __launch_bounds__(256) pool_nhwc_kernel(const __grid_constant__ 
                    : make_uint4(0, 0, 0, 0);
             return in;
         };
+        if constexpr (sizeof(TI) == 2 && std::is_same<TI, TO>::value) {
+            if (p.raw_max) {  // the maxima are stored values: written back without widening
+                __nv_bfloat162 m[4];
+                bf16_max_window<FIX>(fetch, p.R, p.S, m);
+                const long long yr = (long long)n * p.ys[0] + (long long)op * p.ys[2] + (long long)oq * p.ys[3] +
+                                     (long long)ch * V;
+                *reinterpret_cast<uint4 *>(y + yr) = *reinterpret_cast<const uint4 *>(m);
+                continue;
+            }
+        }
         const int count = is_max ? pool_window<TI, A, V, true, FIX>(fetch, p.R, p.S, acc)
                                  : pool_window<TI, A, V, false, FIX>(fetch, p.R, p.S, acc);
         const A div = p.mode == 1 ? (A)(p.R * p.S) : (A)count;
@@ -495,6 +516,8 @@ dlcStatus_t dlc_launch_pool(dlcContext *ctx, const PoolProblem &pp) {
         const long long vb = 16LL / ex * ey, al = std::min(vb, 16LL);
         p.y_vec = nhwc && ((uintptr_t)pp.y % al) == 0 && (pp.ys[0] * ey) % al == 0 &&
                   (pp.ys[2] * ey) % al == 0 && (pp.ys[3] * ey) % al == 0;
+        p.raw_max = p.y_vec && pp.mode == 0 && pp.xdt == DLC_DATA_BFLOAT16 && pp.ydt == DLC_DATA_BFLOAT16 &&
+                    pp.alpha == 1.0 && pp.beta == 0.0;
     }
     if (by_types<PoolRun>(pp.xdt, pp.ydt, ctx, p, nhwc) != cudaSuccess) return DLC_STATUS_EXECUTION_FAILED;
     ctx->launches += 1;

@@ -81,7 +81,7 @@ POOL_CASES = [
 MODES = {"max": "max", "avginc": "avg_include_pad", "avgexc": "avg_exclude_pad"}
 
 
-def run_pool(case, seed, alpha=1.0, beta=0.0):
+def run_pool(case, seed, alpha=1.0, beta=0.0, exact=False):
     import torch
     from deep_learning_convolution_gb300 import api
     name, N, C, H, W, win, pads, stride, dt, axes, ydt, kernel = case
@@ -118,6 +118,8 @@ def run_pool(case, seed, alpha=1.0, beta=0.0):
         tol = tol + rel * np.abs(beta * old)
     if ydt == "bf16":
         tol = tol + 2.0 ** -8 * np.abs(ref)
+    if exact:  # a maximum is one of the stored values: equal to the bit
+        assert np.array_equal(got, ref), f"pool {name}: max differs from the oracle's"
     assert_within(got, ref, tol, f"pool {name}")
     op.close()
     handle.close()
@@ -133,7 +135,17 @@ def test_pooling(case):
 def test_pooling_alexnet_size_full():
     _need_cuda()
     run_pool(("max_nhwc_bf16_alex", 128, 64, 55, 55, (3, 3), (0, 0, 0, 0), (2, 2), "bf16", "NHWC",
-              "bf16", "pool_nhwc"), 902)
+              "bf16", "pool_nhwc"), 902, exact=True)
+
+
+@pytest.mark.parametrize("case", [c for c in POOL_CASES if c[0].startswith("max") and c[8] == "bf16"],
+                         ids=lambda c: c[0])
+def test_max_pooling_bf16_exact(case):
+    """BF16 max pooling with alpha = 1 and beta = 0 (into BF16 y the maxima
+    are written back as stored, into FP32 y widened): equal to the oracle's
+    maximum to the bit, padding included."""
+    _need_cuda()
+    run_pool(case, 903, exact=True)
 
 
 def test_pooling_rejects_pad_not_smaller_than_window():
