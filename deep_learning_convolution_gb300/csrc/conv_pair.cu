@@ -785,7 +785,15 @@ dlcStatus_t dlc_launch_pair(dlcContext *ctx, const ConvProblem &pb) {
         const int C = max_clusters;
         const int rem = p.num_tiles % C;
         const int splits = rem > 0 ? std::min(std::min(C / rem, p.num_kb), 16) : 1;
-        if (plain && splits >= 2 && !(ev && std::atoi(ev) == 0)) {
+        // worth it when the pieces are shorter than a whole tile by more than
+        // about ten k-blocks: a piece's reduce-add epilogue and the zeroing
+        // memset between launches cost that much (measured: a 1x1 layer of
+        // eight k-blocks a tile ran 17.5 us split, 13.3 us whole; 3x3 layers
+        // of 36-72 k-blocks gain 3-8 us).  DLC_TC_PAIR_SPLIT=0: never; =2:
+        // whenever the tail leaves clusters idle.
+        const int mode = ev ? std::atoi(ev) : 1;
+        const bool worth = p.num_kb - (p.num_kb + splits - 1) / splits > 10;
+        if (plain && splits >= 2 && mode != 0 && (worth || mode == 2)) {
             p.full_tiles = p.num_tiles - rem;
             p.tail_splits = splits;
             p.num_units = p.full_tiles + rem * splits;

@@ -24,6 +24,7 @@ L = synth.Layer
 
 CASES = [
     # 1600 output pixels: 7 SM-pair tiles, every one split along the reduction
+    # (DLC_TC_PAIR_SPLIT=2: split even where whole tiles would be as fast)
     L("graph_bf16_c64_k128_20", 4, 64, 20, 20, 128, 3, 3, pad_top=1, pad_bottom=1, pad_left=1,
       pad_right=1),
     L("graph_bf16_c3_11x11_s4", 2, 3, 63, 63, 64, 11, 11, pad_top=2, pad_bottom=2, pad_left=2,
@@ -41,7 +42,7 @@ def _check(y, x_axes, ref, tol, what):
 
 
 @pytest.mark.parametrize("layer", CASES, ids=lambda l: l.name)
-def test_replayed_passes_match_oracle(layer):
+def test_replayed_passes_match_oracle(layer, monkeypatch):
     import torch
     import bench
     from deep_learning_convolution_gb300 import api
@@ -50,6 +51,7 @@ def test_replayed_passes_match_oracle(layer):
 
     if not torch.cuda.is_available():
         pytest.fail("GPU tests need CUDA")
+    monkeypatch.setenv("DLC_TC_PAIR_SPLIT", "2")
     dlc_build.build()
     x, w, _ = synth.make_inputs(layer, 4242)
     ref, bound = oracle.conv2d_fprop(

@@ -128,7 +128,7 @@ def test_tc_im2col_pair_bulk_stores(handle, layer, epi, monkeypatch):
                   relu=True, expect_kernel="tc_im2col_pair")
 
 
-@pytest.mark.parametrize("split", ["1", "0"], ids=["split_tail", "whole_tiles"])
+@pytest.mark.parametrize("split", ["2", "0"], ids=["split_tail", "whole_tiles"])
 @pytest.mark.parametrize("layer", [PAIR_CASES[i] for i in (0, 1, 3, 7, 9, 10)],
                          ids=lambda l: l.name)
 def test_tc_im2col_pair_split_tail(handle, layer, split, monkeypatch):
